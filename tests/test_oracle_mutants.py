@@ -1,0 +1,172 @@
+"""Plant plausible mistakes in copies of the oracle and check that a pin catches each.
+
+Each mutant below is the oracle with one slip a reader could make when
+restating the pages: a dropped max subtraction, the wrong axis, a missing
+exp, a flipped sign, masked lanes loaded as 0 instead of -inf, a dropped
+tail tile, a merge that forgets to rescale.  A pin suite that lets one of
+these through would not be trusted to judge the CUDA path.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import oracle
+from test_oracle_pins import MERGE_CHECKS, ROW_SUM_CHECKS, SOFTMAX_CHECKS
+
+
+def _rows(x):
+    a = np.asarray(x, dtype=np.float64)
+    return a[None, :] if a.ndim == 1 else a
+
+
+def sm_no_max_shift(x):
+    a = _rows(x)
+    with np.errstate(all="ignore"):
+        e = np.exp(a)
+        return e / e.sum(axis=1, keepdims=True)
+
+
+def sm_wrong_axis(x):
+    a = _rows(x)
+    with np.errstate(all="ignore"):
+        e = np.exp(a - a.max(axis=0, keepdims=True))
+        return e / e.sum(axis=0, keepdims=True)
+
+
+def sm_min_shift(x):
+    a = _rows(x)
+    with np.errstate(all="ignore"):
+        e = np.exp(a - a.min(axis=1, keepdims=True))
+        return e / e.sum(axis=1, keepdims=True)
+
+
+def sm_no_exp(x):
+    a = _rows(x)
+    with np.errstate(all="ignore"):
+        e = a - a.max(axis=1, keepdims=True)
+        return e / e.sum(axis=1, keepdims=True)
+
+
+def sm_flipped_sign(x):
+    a = _rows(x)
+    with np.errstate(all="ignore"):
+        e = np.exp(a.max(axis=1, keepdims=True) - a)
+        return e / e.sum(axis=1, keepdims=True)
+
+
+def sm_divide_by_max(x):
+    a = _rows(x)
+    with np.errstate(all="ignore"):
+        e = np.exp(a - a.max(axis=1, keepdims=True))
+        return e / e.max(axis=1, keepdims=True)
+
+
+def sm_global_sum(x):
+    a = _rows(x)
+    with np.errstate(all="ignore"):
+        e = np.exp(a - a.max(axis=1, keepdims=True))
+        return e / e.sum()
+
+
+def sm_mask_as_zero(x):
+    a = np.where(np.isneginf(_rows(x)), 0.0, _rows(x))
+    return oracle.softmax_rows(a)
+
+
+def sm_drop_last_column(x):
+    a = _rows(x)
+    y = oracle.softmax_rows(a[:, :-1]) if a.shape[1] > 1 else oracle.softmax_rows(a)
+    out = np.zeros_like(a)
+    out[:, :y.shape[1]] = y
+    return out
+
+
+SOFTMAX_MUTANTS = [sm_no_max_shift, sm_wrong_axis, sm_min_shift, sm_no_exp, sm_flipped_sign,
+                   sm_divide_by_max, sm_global_sum, sm_mask_as_zero, sm_drop_last_column]
+
+
+def rst_drop_tail(row, block):
+    r = np.asarray(row, dtype=np.float64).ravel()
+    acc = np.zeros(block)
+    trace = []
+    for start in range(0, r.size - block + 1, block):   # forgets the ragged tile
+        acc = acc + r[start:start + block]
+        trace.append(acc.copy())
+    return trace, float(acc.sum())
+
+
+def rst_wraparound(row, block):
+    r = np.asarray(row, dtype=np.float64).ravel()
+    acc = np.zeros(block)
+    trace = []
+    for start in range(0, r.size, block):
+        tile = np.resize(r[start:], block)                  # masked lanes not zero
+        acc = acc + tile
+        trace.append(acc.copy())
+    return trace, float(acc.sum())
+
+
+def rs_mean(x):
+    return np.mean(_rows(x), axis=1) if _rows(x).shape[1] else np.zeros(_rows(x).shape[0])
+
+
+def rs_float32(x):
+    return np.sum(_rows(x).astype(np.float32), axis=1, dtype=np.float32).astype(np.float64)
+
+
+ROW_SUM_MUTANTS = [(oracle.row_sum, rst_drop_tail), (oracle.row_sum, rst_wraparound),
+                   (rs_mean, oracle.row_sum_tiles), (rs_float32, oracle.row_sum_tiles)]
+
+
+def mg_no_rescale(a, b):
+    return (max(a[0], b[0]), a[1] + b[1])
+
+
+def mg_min(a, b):
+    m = min(a[0], b[0]) if min(a[0], b[0]) != -np.inf else max(a[0], b[0])
+    with np.errstate(all="ignore"):
+        ta = 0.0 if a[0] == -np.inf else a[1] * float(np.exp(a[0] - m))
+        tb = 0.0 if b[0] == -np.inf else b[1] * float(np.exp(b[0] - m))
+    return (m, ta + tb)
+
+
+def mg_flipped(a, b):
+    m = max(a[0], b[0])
+    if m == -np.inf:
+        return (-np.inf, 0.0)
+    ta = 0.0 if a[0] == -np.inf else a[1] * float(np.exp(m - a[0]))
+    tb = 0.0 if b[0] == -np.inf else b[1] * float(np.exp(m - b[0]))
+    return (m, ta + tb)
+
+
+def mg_unguarded(a, b):
+    m = max(a[0], b[0])
+    with np.errstate(all="ignore"):
+        return (m, a[1] * float(np.exp(a[0] - m)) + b[1] * float(np.exp(b[0] - m)))
+
+
+MERGE_MUTANTS = [mg_no_rescale, mg_min, mg_flipped, mg_unguarded]
+
+
+def _caught(fn, *args) -> bool:
+    try:
+        fn(*args)
+    except (AssertionError, ValueError, FloatingPointError, IndexError):
+        return True
+    return False
+
+
+@pytest.mark.parametrize("mutant", SOFTMAX_MUTANTS, ids=lambda m: m.__name__)
+def test_softmax_mutant_is_caught(mutant):
+    assert any(_caught(check, mutant) for check in SOFTMAX_CHECKS)
+
+
+@pytest.mark.parametrize("pair", ROW_SUM_MUTANTS, ids=lambda p: p[0].__name__ + "+" + p[1].__name__)
+def test_row_sum_mutant_is_caught(pair):
+    assert any(_caught(check, *pair) for check in ROW_SUM_CHECKS)
+
+
+@pytest.mark.parametrize("mutant", MERGE_MUTANTS, ids=lambda m: m.__name__)
+def test_merge_mutant_is_caught(mutant):
+    assert any(_caught(check, oracle.partial, mutant) for check in MERGE_CHECKS)

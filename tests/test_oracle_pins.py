@@ -1,0 +1,260 @@
+"""Pins for the float64 oracle: values the pages print and facts the mathematics fixes.
+
+None of these retypes the oracle's own formula.  The softmax is pinned by
+closed forms (uniform row, two-element sigmoid, one-hot limit), invariants
+(rows sum to one, shift invariance), brute force along a different route
+(un-shifted exp over an exactly rounded sum, in pure Python) and library
+routines (torch / scipy softmax in float64).  The row sum is pinned by the
+lecture's worked example (3,1,4,1 | 5,9,2,6 | 5,3 -> 39), Gauss's closed form
+and an exactly rounded sum.  ``test_oracle_mutants.py`` plants plausible
+mistakes in copies of these functions and checks that a pin here fails.
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------- fixtures ----
+
+def load_worked_example():
+    rec = {}
+    with open(os.path.join(GOLDEN, "row_sum_worked_example.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, val = line.split(":", 1)
+            rec[key.strip()] = [float(v) for v in val.split()]
+    return rec
+
+
+def small_cases():
+    """Small matrices in each workload's value recipe (ragged shapes included)."""
+    out = []
+    for name, (M, N) in {"c1": (7, 256), "c2": (5, 1000), "c3": (3, 4097),
+                         "c4": (6, 333), "c5": (2, 5003)}.items():
+        w = workloads.WORKLOADS[name].with_shape(M, N)
+        out.append((name, workloads.matrix(w).astype(np.float64)))
+    return out
+
+
+# ------------------------------------------------------- softmax pin checks ----
+
+def check_rows_sum_to_one(sm):
+    for name, x in small_cases():
+        y = sm(x)
+        assert y.shape == x.shape, name
+        assert np.all(np.isfinite(y)), name
+        assert np.max(np.abs(np.sum(y, axis=1) - 1.0)) <= 1e-12, name
+
+
+def check_shift_invariance(sm):
+    rng = np.random.default_rng(11)
+    x = rng.normal(0.0, 3.0, size=(4, 37))
+    base = sm(x)
+    for c in (-100.0, 1000.0):
+        shifted = sm(x + c)
+        assert np.all(np.isfinite(shifted)), c
+        assert np.max(np.abs(shifted - base)) <= 1e-12, c
+
+
+def check_constant_row(sm):
+    for N in (1, 2, 3, 7, 256, 1000):
+        for v in (-5.0, 0.0, 42.0):
+            y = sm(np.full((2, N), v))
+            assert np.all(y == 1.0 / N), (N, v)
+
+
+def check_two_element_sigmoid(sm):
+    rng = np.random.default_rng(12)
+    for _ in range(200):
+        x0, x1 = rng.uniform(-30, 30, size=2)
+        y = sm(np.array([[x0, x1]]))[0]
+        s0 = 1.0 / (1.0 + math.exp(x1 - x0))
+        s1 = 1.0 / (1.0 + math.exp(x0 - x1))
+        assert abs(y[0] - s0) <= 1e-14 * max(s0, 1e-300) + 1e-300
+        assert abs(y[1] - s1) <= 1e-14 * max(s1, 1e-300) + 1e-300
+
+
+def check_brute_force(sm):
+    """Un-shifted exp over an exactly rounded sum, element by element, in pure Python."""
+    rng = np.random.default_rng(13)
+    for M, N in ((3, 5), (5, 3), (1, 8), (4, 1), (2, 7)):
+        x = rng.uniform(-20, 20, size=(M, N))
+        y = sm(x)
+        for i in range(M):
+            den = math.fsum(math.exp(v) for v in x[i])
+            for j in range(N):
+                want = math.exp(x[i, j]) / den
+                assert abs(y[i, j] - want) <= 1e-14 * want, (M, N, i, j)
+
+
+def check_library(sm):
+    torch = pytest.importorskip("torch")
+    scipy_special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(14)
+    x = rng.normal(0, 4, size=(9, 50))
+    y = sm(x)
+    t = torch.softmax(torch.from_numpy(x), dim=1).numpy()
+    s = scipy_special.softmax(x, axis=1)
+    assert np.max(np.abs(y - t)) <= 1e-15
+    assert np.max(np.abs(y - s)) <= 1e-15
+
+
+def check_one_hot_limit(sm):
+    x = np.zeros((3, 10))
+    for i, j in enumerate((0, 4, 9)):
+        x[i, j] = 1e4
+    y = sm(x)
+    for i, j in enumerate((0, 4, 9)):
+        want = np.zeros(10)
+        want[j] = 1.0
+        assert np.array_equal(y[i], want)
+
+
+def check_masked_entries(sm):
+    w = workloads.WORKLOADS["c4"].with_shape(4, 4096)
+    x = workloads.matrix(w).astype(np.float64)
+    y = sm(x)
+    neg = np.isneginf(x)
+    assert neg.sum() == 4 * 41
+    assert np.all(y[neg] == 0.0)
+    for i in range(4):
+        spikes = x[i] == 50.0
+        assert spikes.sum() == 205
+        vals = y[i][spikes]
+        assert np.all(vals == vals[0])      # ties share the mass exactly
+        # the spikes dominate: all other entries are below e^(max normal - 50)
+        assert vals.sum() > 1.0 - 1e-9
+
+
+def check_all_masked_row_is_nan(sm):
+    x = np.array([[-np.inf, -np.inf, -np.inf], [0.0, -np.inf, 0.0]])
+    y = sm(x)
+    assert np.all(np.isnan(y[0]))
+    assert y[1, 0] == 0.5 and y[1, 1] == 0.0 and y[1, 2] == 0.5
+
+
+SOFTMAX_CHECKS = [
+    check_rows_sum_to_one, check_shift_invariance, check_constant_row,
+    check_two_element_sigmoid, check_brute_force, check_library,
+    check_one_hot_limit, check_masked_entries, check_all_masked_row_is_nan,
+]
+
+
+# ------------------------------------------------------- row-sum pin checks ----
+
+def check_worked_example(rs, rst):
+    g = load_worked_example()
+    row = np.array(g["row"])
+    block = int(g["block"][0])
+    trace, total = rst(row, block)
+    assert len(trace) == 3
+    for k in range(3):
+        assert list(trace[k]) == g[f"acc_after_tile_{k}"]
+    assert total == g["total"][0] == 39.0
+    assert rs(row[None, :])[0] == 39.0
+
+
+def check_gauss(rs, rst):
+    for N in (1, 2, 10, 999, 4096, 32768):
+        x = np.arange(1, N + 1, dtype=np.float64)[None, :]
+        assert rs(x)[0] == N * (N + 1) // 2
+        assert rst(x[0], 1024)[1] == N * (N + 1) // 2
+
+
+def check_exact_sum(rs, rst):
+    for name, x in small_cases():
+        x = np.where(np.isfinite(x), x, 0.0)
+        got = rs(x)
+        for i in range(x.shape[0]):
+            want = math.fsum(x[i])
+            scale = math.fsum(abs(v) for v in x[i])
+            assert abs(got[i] - want) <= 1e-13 * scale, name
+            assert abs(rst(x[i], 128)[1] - want) <= 1e-13 * scale, name
+
+
+def check_empty_rows(rs, rst):
+    assert np.array_equal(rs(np.zeros((3, 0))), np.zeros(3))
+    assert rst(np.zeros(0), 4) == ([], 0.0)
+
+
+ROW_SUM_CHECKS = [check_worked_example, check_gauss, check_exact_sum, check_empty_rows]
+
+
+# --------------------------------------------------------- merge pin checks ----
+
+def check_merge_equals_unsplit(part, mg):
+    rng = np.random.default_rng(15)
+    for trial in range(50):
+        N = int(rng.integers(2, 400))
+        x = rng.normal(0, 5, size=N)
+        if trial % 5 == 0:
+            x[rng.choice(N, size=N // 3, replace=False)] = -np.inf
+        whole_m = float(np.max(x))
+        whole_s = math.fsum(math.exp(v - whole_m) for v in x)
+        k = int(rng.integers(1, min(N, 9)))
+        cuts = sorted(rng.choice(np.arange(1, N), size=k, replace=False).tolist())
+        bounds = [0] + cuts + [N]
+        parts = [part(x[a:b]) for a, b in zip(bounds[:-1], bounds[1:])]
+        order = rng.permutation(len(parts))
+        acc = (-np.inf, 0.0)
+        for idx in order:
+            acc = mg(acc, parts[idx])
+        assert acc[0] == whole_m
+        assert abs(acc[1] - whole_s) <= 1e-13 * whole_s
+
+
+def check_merge_identity_and_masked(part, mg):
+    p = (1.5, 3.25)
+    assert mg((-np.inf, 0.0), p) == p
+    assert mg(p, (-np.inf, 0.0)) == p
+    masked = part(np.array([-np.inf, -np.inf]))
+    assert masked == (-np.inf, 0.0)
+    got = mg(masked, part(np.array([0.0, 0.0])))
+    assert got == (0.0, 2.0)
+    assert mg(masked, masked) == (-np.inf, 0.0)
+
+
+MERGE_CHECKS = [check_merge_equals_unsplit, check_merge_identity_and_masked]
+
+
+# ------------------------------------------------------------------- tests ----
+
+@pytest.mark.parametrize("check", SOFTMAX_CHECKS, ids=lambda c: c.__name__)
+def test_softmax_pins(check):
+    check(oracle.softmax_rows)
+
+
+@pytest.mark.parametrize("check", ROW_SUM_CHECKS, ids=lambda c: c.__name__)
+def test_row_sum_pins(check):
+    check(oracle.row_sum, oracle.row_sum_tiles)
+
+
+@pytest.mark.parametrize("check", MERGE_CHECKS, ids=lambda c: c.__name__)
+def test_merge_pins(check):
+    check(oracle.partial, oracle.merge)
+
+
+def test_split_softmax_matches_definition():
+    rng = np.random.default_rng(16)
+    x = rng.normal(0, 3, size=(6, 1000))
+    x[2, ::7] = -np.inf
+    for cuts in ([500], [1, 999], [10, 250, 251, 700]):
+        assert np.max(np.abs(oracle.softmax_rows_split(x, cuts) - oracle.softmax_rows(x))) <= 1e-15
+    for check in (check_rows_sum_to_one, check_brute_force, check_masked_entries,
+                  check_one_hot_limit, check_shift_invariance):
+        check(lambda a: oracle.softmax_rows_split(a, [1] if np.asarray(a).shape[1] > 1 else []))
+
+
+def test_empty_columns():
+    assert oracle.softmax_rows(np.zeros((4, 0))).shape == (4, 0)
