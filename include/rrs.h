@@ -1,0 +1,163 @@
+/*
+ * rrs.h -- C ABI of the GB300 row-wise softmax and row-sum library (librrs.so).
+ *
+ * The two operations are the ones the CS336 lecture 06 pages build their
+ * reduction kernels around:
+ *
+ *   softmax_rows  "Kernels, Triton, XLA", section "Reductions and tiling:
+ *                 softmax, row sum, matmul" (and "GPU High-Performance
+ *                 Programming", section 7.5.1): for every row i,
+ *                   m_i = max_j x[i,j],  s_i = sum_j exp(x[i,j] - m_i),
+ *                   y[i,j] = exp(x[i,j] - m_i) / s_i.
+ *   row_sum       same section, paragraph "Row sum, when the row doesn't
+ *                 fit": out[i] = sum_j x[i,j].
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ * - Data are fp32.  x, y and out are DEVICE pointers (cudaMalloc, a caching
+ *   allocator or managed memory) owned by the caller; the library neither
+ *   frees nor keeps them.  Host pointers are rejected (RRS_ERR_INVALID_ARG).
+ * - Row i of x occupies x[i*ld .. i*ld + N).  y uses the same ld.  The gap
+ *   [N, ld) of every row of y is never written; the gap of x is never read.
+ * - stream is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream).  All work is enqueued on it and the call returns without
+ *   synchronising; results are ordered before later work on that stream.
+ * - Any ld >= N and any 4-byte-aligned pointer is accepted.  The 128-bit
+ *   vector paths run when x and y are 16-byte aligned and ld % 4 == 0;
+ *   otherwise a scalar path gives the same results.
+ * - Arguments are checked before anything is enqueued.  A failed launch
+ *   returns RRS_ERR_CUDA and rrs_last_error() holds the runtime's message.
+ * - Rows that contain +inf or NaN, or are entirely -inf, come out as NaN
+ *   (the naive five steps give (-inf) - (-inf) or inf - inf there).  -inf
+ *   entries of other rows come out as exactly 0.
+ * - Calls are thread-safe.  The split-row paths use a small per-(device,
+ *   stream) workspace the library allocates on first use and keeps.
+ */
+#ifndef RRS_H
+#define RRS_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define RRS_API __attribute__((visibility("default")))
+#else
+#define RRS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum rrs_status {
+  RRS_OK = 0,
+  RRS_ERR_INVALID_ARG = 1, /* negative size, ld < N, null or host pointer, misaligned float */
+  RRS_ERR_ALIAS = 2,       /* the byte ranges of x and y (or out) overlap */
+  RRS_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed; see rrs_last_error() */
+  RRS_ERR_TIMEOUT = 4,     /* a split-row kernel gave up waiting for its peers (rrs_device_error) */
+  RRS_ERR_NOMEM = 5,       /* the workspace could not be allocated */
+  RRS_ERR_UNSUPPORTED = 6  /* a forced path cannot run this shape on this device */
+} rrs_status;
+
+/* Execution paths of softmax_rows (the planner picks one; tests may force one). */
+typedef enum rrs_path {
+  RRS_PATH_AUTO = -1,
+  RRS_PATH_TWO_PHASE = 0,   /* any shape/alignment: partial (max,sum) per chunk, then merge + re-read + write */
+  RRS_PATH_ROW_REGS = 1,    /* a group of 1..32 warps keeps the whole row in registers; 1 read + 1 write */
+  RRS_PATH_ROW_STAGED = 2,  /* persistent CTAs stage rows in shared memory with bulk async copies (TMA) */
+  RRS_PATH_CLUSTER = 3,     /* row split over a thread-block cluster; (max,sum) merged through DSMEM */
+  RRS_PATH_GRID = 4,        /* row split over co-resident CTAs; (max,sum) merged through global memory */
+  RRS_PATH_COUNT = 5
+} rrs_path;
+
+/* Execution paths of row_sum. */
+typedef enum rrs_sum_path {
+  RRS_SUM_AUTO = -1,
+  RRS_SUM_ROW = 0,          /* one CTA (or warp) per row, per-thread accumulators, fixed-order tree */
+  RRS_SUM_SPLIT = 1,        /* rows split into chunks; partial sums merged in fixed order by a 2nd kernel */
+  RRS_SUM_COUNT = 2
+} rrs_sum_path;
+
+/* A launch plan: what the host side decided for one call (pure host logic). */
+typedef struct rrs_plan {
+  int32_t path;          /* rrs_path or rrs_sum_path */
+  int32_t threads;       /* threads per CTA */
+  int64_t grid;          /* CTAs launched (first kernel for two-kernel paths) */
+  int32_t cluster;       /* CTAs per cluster (1 = no cluster) */
+  int32_t vec;           /* float4 registers per thread per row segment (0 for streaming paths) */
+  int32_t warps_per_row; /* warps that share one row (ROW_REGS) */
+  int32_t rows_per_cta;  /* rows one CTA holds at a time */
+  int64_t ctas_per_row;  /* CTAs one row is split over (split paths) */
+  int64_t chunk;         /* columns per CTA segment in split paths (last one shorter) */
+  int64_t rounds;        /* persistent rounds (GRID / STAGED) */
+  int32_t smem_bytes;    /* dynamic shared memory per CTA */
+  int32_t vector_io;     /* 1 if 128-bit loads/stores are used */
+  int64_t workspace_bytes;
+} rrs_plan;
+
+/* y = softmax over each row of x (see the top of this file).
+ * x, y: device fp32, M rows of N valid entries, row stride ld (elements).
+ * M == 0 or N == 0: no work, RRS_OK.  Errors: RRS_ERR_INVALID_ARG (M < 0,
+ * N < 0, ld < N, ld < 1, null/host pointer, pointer not 4-byte aligned,
+ * extent overflow), RRS_ERR_ALIAS (x and y overlap), RRS_ERR_CUDA,
+ * RRS_ERR_NOMEM. */
+RRS_API int softmax_rows(const float* x, float* y, int64_t M, int64_t N, int64_t ld, void* stream);
+
+/* out[i] = sum_j x[i*ld + j] for i < M (fp32 accumulation, fixed order:
+ * bitwise reproducible run to run).  N == 0 writes zeros (the sum's
+ * identity).  out: device, M floats, must not overlap x.  Errors as for
+ * softmax_rows. */
+RRS_API int row_sum(const float* x, float* out, int64_t M, int64_t N, int64_t ld, void* stream);
+
+/* Synchronises `stream`, then returns and clears the device-side error word
+ * of the current device: RRS_ERR_TIMEOUT if a split-row kernel stopped
+ * waiting for its peers since the last call (its output is then incomplete),
+ * RRS_OK otherwise, RRS_ERR_CUDA if the synchronisation failed. */
+RRS_API int rrs_device_error(void* stream);
+
+/* Static string naming a status code. */
+RRS_API const char* rrs_status_string(int status);
+
+/* The calling thread's last error message ("" if none). */
+RRS_API const char* rrs_last_error(void);
+
+/* Frees every cached workspace (after a device synchronisation).  Later
+ * calls allocate again on demand.  Returns RRS_OK or RRS_ERR_CUDA. */
+RRS_API int rrs_release_workspace(void);
+
+/* Force a path for later calls from any thread (testing / measurement):
+ * softmax_path is an rrs_path, sum_path an rrs_sum_path; AUTO restores the
+ * planner.  A forced path that cannot run a shape makes the call return
+ * RRS_ERR_UNSUPPORTED.  Returns RRS_OK or RRS_ERR_INVALID_ARG. */
+RRS_API int rrs_force_path(int softmax_path, int sum_path);
+
+/* The planner, as pure host logic: the plan softmax_rows / row_sum would use
+ * for this shape on a device with `sm_count` SMs and `smem_optin` bytes of
+ * opt-in shared memory per CTA.  `vector_ok` says whether x and y are
+ * 16-byte aligned with ld % 4 == 0.  Honors rrs_force_path.  Returns RRS_OK,
+ * RRS_ERR_INVALID_ARG or RRS_ERR_UNSUPPORTED; touches no GPU. */
+RRS_API int rrs_plan_softmax(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_count,
+                             int smem_optin, rrs_plan* plan);
+RRS_API int rrs_plan_row_sum(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_count,
+                             int smem_optin, rrs_plan* plan);
+
+/* Occupancy arithmetic used by the planner ("Kernels, Triton, XLA", section
+ * "Where the abstraction leaks", worked example on register pressure):
+ * blocks of `threads` threads using `regs` registers each on an SM with
+ * `sm_regs` registers and `max_warps` resident warps.  Writes the resident
+ * blocks and warps; returns occupancy in basis points (1/100 %). */
+RRS_API int rrs_occupancy(int threads, int regs, int sm_regs, int max_warps,
+                          int* blocks, int* warps);
+
+/* Wave arithmetic (same page, problem 6.2): `blocks` CTAs on `slots`
+ * concurrent CTA slots.  Writes the size of the last wave and the idle slots
+ * in it; returns the number of waves. */
+RRS_API int64_t rrs_waves(int64_t blocks, int64_t slots, int64_t* last_wave, int64_t* idle);
+
+/* Library version, major*10000 + minor*100 + patch. */
+RRS_API int rrs_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RRS_H */

@@ -1,0 +1,159 @@
+// Single-pass row softmax with the whole row held in registers.
+//
+// The pages' fused kernel gives one block a whole row, loads it once with
+// masked lanes set to -inf, and does max, subtract, exp, sum and divide on
+// chip, so each element crosses HBM once each way ("Kernels, Triton, XLA",
+// section "Reductions and tiling"; "GPU High-Performance Programming",
+// section 7.5.1).  Here the unit that owns a row is a GROUP of GW warps
+// (GW = 1 for rows up to 2048 floats, so short rows need no shared memory
+// or barrier at all), each thread keeps VEC float4 of the row in registers
+// (thread coarsening), and consecutive threads take consecutive float4 so
+// every warp access is a full, coalesced 512-byte run.
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace rrs {
+namespace {
+
+// Group-wide max / sum: warp shuffles, then one shared-memory step across the
+// GW warps of the group, guarded by the group's own named barrier.
+template <int GW>
+__device__ __forceinline__ float group_max(float v, float* red, int gw, int lane, int bar_id) {
+  v = warp_max(v);
+  if constexpr (GW == 1) {
+    return v;
+  } else {
+    if (lane == 0) red[gw] = v;
+    named_barrier(bar_id, 32 * GW);
+    float r = (lane < GW) ? red[lane] : neg_inf();
+    return warp_max(r);
+  }
+}
+
+template <int GW>
+__device__ __forceinline__ float group_sum(float v, float* red, int gw, int lane, int bar_id) {
+  v = warp_sum(v);
+  if constexpr (GW == 1) {
+    return v;
+  } else {
+    if (lane == 0) red[gw] = v;
+    named_barrier(bar_id, 32 * GW);
+    float r = (lane < GW) ? red[lane] : 0.f;
+    return warp_sum(r);
+  }
+}
+
+template <int GW>
+__host__ __device__ constexpr int threads_for() { return (32 * GW < 128) ? 128 : 32 * GW; }
+
+// x, y: 16-byte aligned, ld % 4 == 0.  Row r is owned by group
+// (blockIdx.x * groups + group), striding by gridDim.x * groups.
+template <int VEC, int GW>
+__global__ void __launch_bounds__(threads_for<GW>())
+softmax_row_regs_kernel(const float* __restrict__ x, float* __restrict__ y, int64_t M, int32_t N,
+                        int64_t ld) {
+  constexpr int kThreads = threads_for<GW>();
+  constexpr int kGroups = kThreads / (32 * GW);
+  constexpr int kGT = 32 * GW;  // threads per group
+  __shared__ float red_m[32];
+  __shared__ float red_s[32];
+
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int group = warp / GW;
+  const int gw = warp % GW;
+  const int gt = gw * 32 + lane;
+  const int bar_id = 1 + group;
+  float* gm = red_m + group * GW;
+  float* gs = red_s + group * GW;
+
+  const int n4 = N >> 2;
+  const int rem = N & 3;
+  const float kNeg = neg_inf();
+
+  for (int64_t row = (int64_t)blockIdx.x * kGroups + group; row < M;
+       row += (int64_t)gridDim.x * kGroups) {
+    const float* xr = x + row * ld;
+    float* yr = y + row * ld;
+    const float4* xr4 = reinterpret_cast<const float4*>(xr);
+    float4* yr4 = reinterpret_cast<float4*>(yr);
+
+    float4 v[VEC];
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+      const int c = i * kGT + gt;
+      v[i] = (c < n4) ? load_stream(xr4 + c) : make_float4(kNeg, kNeg, kNeg, kNeg);
+    }
+    float t = (gt < rem) ? load_stream(xr + 4 * n4 + gt) : kNeg;  // ragged tail, N % 4 != 0
+
+    // (1) row max
+    float m = t;
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) m = max_nan(m, max4(v[i]));
+    m = group_max<GW>(m, gm, gw, lane, bar_id);
+
+    // (2)+(3) subtract and exponentiate in place, (4) row sum
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+      v[i].x = exp_shifted(v[i].x, m);
+      v[i].y = exp_shifted(v[i].y, m);
+      v[i].z = exp_shifted(v[i].z, m);
+      v[i].w = exp_shifted(v[i].w, m);
+      s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+    }
+    t = exp_shifted(t, m);
+    s += t;
+    s = group_sum<GW>(s, gs, gw, lane, bar_id);
+
+    // (5) divide: one reciprocal per row, then a multiply per element
+    const float inv = 1.0f / s;
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+      const int c = i * kGT + gt;
+      if (c < n4) {
+        store_stream(yr4 + c, make_float4(v[i].x * inv, v[i].y * inv, v[i].z * inv, v[i].w * inv));
+      }
+    }
+    if (gt < rem) store_stream(yr + 4 * n4 + gt, t * inv);
+  }
+}
+
+template <int VEC, int GW>
+cudaError_t launch_rr(const rrs_plan& p, const float* x, float* y, int64_t M, int64_t N,
+                      int64_t ld, cudaStream_t s) {
+  constexpr int kThreads = threads_for<GW>();
+  if (p.threads != kThreads) return cudaErrorInvalidConfiguration;
+  softmax_row_regs_kernel<VEC, GW>
+      <<<(unsigned)p.grid, kThreads, 0, s>>>(x, y, M, (int32_t)N, ld);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_softmax_row_regs(const rrs_plan& p, const float* x, float* y, int64_t M,
+                                    int64_t N, int64_t ld, cudaStream_t s) {
+  const int gw = p.warps_per_row;
+  const int vec = p.vec;
+#define RRS_RR(V, G) \
+  if (vec == V && gw == G) return launch_rr<V, G>(p, x, y, M, N, ld, s);
+  RRS_RR(1, 1)
+  RRS_RR(2, 1)
+  RRS_RR(4, 1)
+  RRS_RR(8, 1)
+  RRS_RR(16, 1)
+  RRS_RR(4, 2)
+  RRS_RR(8, 2)
+  RRS_RR(4, 4)
+  RRS_RR(8, 4)
+  RRS_RR(4, 8)
+  RRS_RR(8, 8)
+  RRS_RR(4, 16)
+  RRS_RR(8, 16)
+  RRS_RR(4, 32)
+  RRS_RR(8, 32)
+#undef RRS_RR
+  return cudaErrorInvalidConfiguration;
+}
+
+}  // namespace rrs

@@ -1,0 +1,347 @@
+// Split-row softmax: a row too long for one CTA's registers is cut into
+// segments owned by different CTAs, each segment's partial (max, sum) is
+// formed on chip, and the partials are merged with the rule
+//     m = max(m_a, m_b),   s = s_a exp(m_a - m) + s_b exp(m_b - m),
+// which follows from s = sum_j exp(x_j - m) (the pages stop at the row sum
+// for rows that overflow a block -- "Kernels, Triton, XLA", section
+// "Reductions and tiling", "Row sum, when the row doesn't fit" -- and the
+// softmax needs a max as well as a sum, hence the pair).
+//
+// Two variants live here:
+//  * CLUSTER  -- the CTAs of one row form a thread-block cluster; each keeps
+//    its segment in registers, publishes (m_c, s_c) in its shared memory, and
+//    every CTA reads all peers' pairs over DSMEM after one cluster barrier.
+//    One HBM read and one write per element.
+//  * TWO_PHASE -- any length and alignment: kernel 1 writes each chunk's
+//    online (m, s) to a workspace, kernel 2 merges a row's partials, re-reads
+//    its chunk and writes y.  12 bytes of traffic per element unless the
+//    re-read hits L2; the fallback for shapes the other paths do not take.
+#include <cooperative_groups.h>
+
+#include "device_common.cuh"
+#include "internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace rrs {
+
+// Set by kernels that wait on peers with a bounded spin, read by
+// rrs_device_error().
+__device__ unsigned int g_device_error = 0;
+
+namespace {
+
+constexpr int kT = kSplitThreads;
+constexpr int kW = kT / 32;
+
+__device__ __forceinline__ float cta_max(float v, float* red) {
+  v = warp_max(v);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float r = (lane < kW) ? red[lane] : neg_inf();
+  return warp_max(r);
+}
+
+__device__ __forceinline__ float cta_sum(float v, float* red) {
+  v = warp_sum(v);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float r = (lane < kW) ? red[lane] : 0.f;
+  return warp_sum(r);
+}
+
+// CTA-wide merge of per-thread partials; every thread gets the result.
+// `red` must not be in use by another reduction until the caller's next
+// __syncthreads().
+__device__ __forceinline__ MaxSum cta_merge(MaxSum p, MaxSum* red) {
+  p = warp_merge(p);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) red[warp] = p;
+  __syncthreads();
+  MaxSum q = (lane < kW) ? red[lane] : MaxSum{neg_inf(), 0.f};
+  return warp_merge(q);
+}
+
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// ----------------------------------------------------------------- CLUSTER ---
+// Grid: clusters of `cs` CTAs along x; cluster k owns rows k, k + nclusters, ...
+// Rank r of a cluster owns float4 columns [r*seg4, min((r+1)*seg4, n4)) of the
+// row, seg4 = ceil(n4 / cs) <= VEC * kT; the last rank also owns the N % 4
+// scalar tail.  x, y 16-byte aligned, ld % 4 == 0.
+template <int VEC>
+__global__ void __launch_bounds__(kT)
+softmax_cluster_kernel(const float* __restrict__ x, float* __restrict__ y, int64_t M, int32_t N,
+                       int64_t ld) {
+  __shared__ float red_m[kW];
+  __shared__ float red_s[kW];
+  __shared__ MaxSum part;   // this CTA's (m_c, s_c), read by its peers
+  __shared__ MaxSum whole;  // the merged pair of the row
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int cs = (int)cluster.num_blocks();
+  const int rank = (int)cluster.block_rank();
+  const int64_t nclusters = gridDim.x / cs;
+  const int64_t cluster_id = blockIdx.x / cs;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+
+  const int n4 = N >> 2;
+  const int rem = N & 3;
+  const int seg4 = (n4 + cs - 1) / cs;
+  const int b4 = rank * seg4;
+  const int e4 = min(b4 + seg4, n4);
+  const bool has_tail = (rank == cs - 1) && (tid < rem);
+  const float kNeg = neg_inf();
+
+  for (int64_t row = cluster_id; row < M; row += nclusters) {
+    const float* xr = x + row * ld;
+    float* yr = y + row * ld;
+    const float4* xr4 = reinterpret_cast<const float4*>(xr);
+    float4* yr4 = reinterpret_cast<float4*>(yr);
+
+    float4 v[VEC];
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+      const int c = b4 + i * kT + tid;
+      v[i] = (c < e4) ? load_stream(xr4 + c) : make_float4(kNeg, kNeg, kNeg, kNeg);
+    }
+    float t = has_tail ? load_stream(xr + 4 * n4 + tid) : kNeg;
+
+    float mc = t;
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) mc = max_nan(mc, max4(v[i]));
+    mc = cta_max(mc, red_m);
+    const bool empty = (mc == kNeg);  // segment holds only -inf (or nothing)
+
+    float sc = 0.f;
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+      v[i].x = empty ? 0.f : exp_shifted(v[i].x, mc);
+      v[i].y = empty ? 0.f : exp_shifted(v[i].y, mc);
+      v[i].z = empty ? 0.f : exp_shifted(v[i].z, mc);
+      v[i].w = empty ? 0.f : exp_shifted(v[i].w, mc);
+      sc += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+    }
+    t = empty ? 0.f : exp_shifted(t, mc);
+    sc += t;
+    sc = cta_sum(sc, red_s);
+
+    if (tid == 0) part = MaxSum{mc, sc};
+    cluster_arrive_release();  // publish `part` to the cluster
+    cluster_wait_acquire();    // every peer's `part` is visible
+
+    if (warp == 0) {
+      MaxSum q{kNeg, 0.f};
+      if (lane < cs) q = *cluster.map_shared_rank(&part, lane);
+      q = warp_merge(q);  // same lanes, same order in every CTA: identical result
+      if (lane == 0) whole = q;
+    }
+    cluster_arrive_release();  // done reading the peers' `part`
+    __syncthreads();
+    const MaxSum w = whole;
+    const bool bad = !(w.s == w.s) || w.m == kNeg;  // NaN / inf / all -inf row
+    const float scale = bad ? __int_as_float(0x7fc00000)
+                            : (empty ? 0.f : exp_shifted(mc, w.m) / w.s);
+
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+      const int c = b4 + i * kT + tid;
+      if (c < e4) {
+        store_stream(yr4 + c,
+                     make_float4(v[i].x * scale, v[i].y * scale, v[i].z * scale, v[i].w * scale));
+      }
+    }
+    if (has_tail) store_stream(yr + 4 * n4 + tid, t * scale);
+    cluster_wait_acquire();  // peers finished reading `part` before it is reused / freed
+  }
+}
+
+// --------------------------------------------------------------- TWO_PHASE ---
+constexpr int kUnroll = 4;
+
+// Per-thread online partial over columns [b, e) of row xr.
+template <bool V4>
+__device__ __forceinline__ MaxSum chunk_partial(const float* __restrict__ xr, int64_t b, int64_t e,
+                                                int64_t N) {
+  MaxSum p{neg_inf(), 0.f};
+  const int tid = threadIdx.x;
+  int64_t scalar_from = b;
+  if constexpr (V4) {
+    // b is a multiple of 4; the vector part stops at e, or at N & ~3 in the last chunk.
+    const int64_t e4 = ((e == N) ? (N & ~int64_t(3)) : e) >> 2;
+    const float4* x4 = reinterpret_cast<const float4*>(xr);
+    for (int64_t k = (b >> 2) + tid; k < e4; k += (int64_t)kT * kUnroll) {
+      float4 a[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t idx = k + (int64_t)u * kT;
+        // plain (L2-allocating) load: the finalize kernel re-reads this chunk
+        a[u] = (idx < e4) ? x4[idx] : make_float4(neg_inf(), neg_inf(), neg_inf(), neg_inf());
+      }
+      float bm = max4(a[0]);
+#pragma unroll
+      for (int u = 1; u < kUnroll; ++u) bm = max_nan(bm, max4(a[u]));
+      rescale_to(p, bm);
+      if (p.m != neg_inf()) {
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          p.s += (exp_shifted(a[u].x, p.m) + exp_shifted(a[u].y, p.m)) +
+                 (exp_shifted(a[u].z, p.m) + exp_shifted(a[u].w, p.m));
+        }
+      }
+    }
+    scalar_from = e4 << 2;
+  }
+  for (int64_t j = scalar_from + tid; j < e; j += kT) {
+    const float v = xr[j];
+    rescale_to(p, v);
+    if (p.m != neg_inf()) p.s += exp_shifted(v, p.m);
+  }
+  return p;
+}
+
+template <bool V4>
+__global__ void __launch_bounds__(kT)
+softmax_partials_kernel(const float* __restrict__ x, MaxSum* __restrict__ part, int64_t M,
+                        int64_t N, int64_t ld, int64_t chunk, int64_t C) {
+  __shared__ MaxSum red[kW];
+  const int64_t work = M * C;
+  for (int64_t w = blockIdx.x; w < work; w += gridDim.x) {
+    const int64_t row = w / C;
+    const int64_t c = w - row * C;
+    const int64_t b = c * chunk;
+    const int64_t e = min(b + chunk, N);
+    MaxSum p = chunk_partial<V4>(x + row * ld, b, e, N);
+    p = cta_merge(p, red);
+    if (threadIdx.x == 0) part[w] = p;
+    __syncthreads();
+  }
+}
+
+template <bool V4>
+__global__ void __launch_bounds__(kT)
+softmax_finalize_kernel(const float* __restrict__ x, float* __restrict__ y,
+                        const MaxSum* __restrict__ part, int64_t M, int64_t N, int64_t ld,
+                        int64_t chunk, int64_t C) {
+  __shared__ MaxSum red[kW];
+  const int64_t work = M * C;
+  const int tid = threadIdx.x;
+  for (int64_t w = blockIdx.x; w < work; w += gridDim.x) {
+    const int64_t row = w / C;
+    const int64_t c = w - row * C;
+    // Every CTA of the row merges the same partials in the same order.
+    MaxSum q{neg_inf(), 0.f};
+    for (int64_t k = tid; k < C; k += kT) q = merge(q, part[row * C + k]);
+    q = cta_merge(q, red);
+    const float m = q.m;
+    const float inv = 1.0f / q.s;
+
+    const int64_t b = c * chunk;
+    const int64_t e = min(b + chunk, N);
+    const float* xr = x + row * ld;
+    float* yr = y + row * ld;
+    int64_t scalar_from = b;
+    if constexpr (V4) {
+      const int64_t e4 = ((e == N) ? (N & ~int64_t(3)) : e) >> 2;
+      const float4* x4 = reinterpret_cast<const float4*>(xr);
+      float4* y4 = reinterpret_cast<float4*>(yr);
+      for (int64_t k = (b >> 2) + tid; k < e4; k += (int64_t)kT * kUnroll) {
+        float4 a[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int64_t idx = k + (int64_t)u * kT;
+          if (idx < e4) a[u] = load_stream(x4 + idx);
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int64_t idx = k + (int64_t)u * kT;
+          if (idx < e4) {
+            store_stream(y4 + idx, make_float4(exp_shifted(a[u].x, m) * inv,
+                                               exp_shifted(a[u].y, m) * inv,
+                                               exp_shifted(a[u].z, m) * inv,
+                                               exp_shifted(a[u].w, m) * inv));
+          }
+        }
+      }
+      scalar_from = e4 << 2;
+    }
+    for (int64_t j = scalar_from + tid; j < e; j += kT) yr[j] = exp_shifted(xr[j], m) * inv;
+    __syncthreads();
+  }
+}
+
+template <int VEC>
+cudaError_t launch_cluster_vec(const rrs_plan& p, const float* x, float* y, int64_t M, int64_t N,
+                               int64_t ld, cudaStream_t s) {
+  auto kern = softmax_cluster_kernel<VEC>;
+  if (p.cluster > 8) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.grid, 1, 1);
+  cfg.blockDim = dim3(kT, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)p.cluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, x, y, M, (int32_t)N, ld);
+}
+
+}  // namespace
+
+cudaError_t launch_softmax_cluster(const rrs_plan& p, const float* x, float* y, int64_t M,
+                                   int64_t N, int64_t ld, cudaStream_t s) {
+  if (p.threads != kT) return cudaErrorInvalidConfiguration;
+  switch (p.vec) {
+    case 4: return launch_cluster_vec<4>(p, x, y, M, N, ld, s);
+    case 8: return launch_cluster_vec<8>(p, x, y, M, N, ld, s);
+    default: return cudaErrorInvalidConfiguration;
+  }
+}
+
+cudaError_t launch_softmax_two_phase(const rrs_plan& p, const float* x, float* y, int64_t M,
+                                     int64_t N, int64_t ld, void* workspace, cudaStream_t s) {
+  if (p.threads != kT) return cudaErrorInvalidConfiguration;
+  MaxSum* part = static_cast<MaxSum*>(workspace);
+  const unsigned grid = (unsigned)p.grid;
+  if (p.vector_io) {
+    softmax_partials_kernel<true><<<grid, kT, 0, s>>>(x, part, M, N, ld, p.chunk, p.ctas_per_row);
+    softmax_finalize_kernel<true>
+        <<<grid, kT, 0, s>>>(x, y, part, M, N, ld, p.chunk, p.ctas_per_row);
+  } else {
+    softmax_partials_kernel<false><<<grid, kT, 0, s>>>(x, part, M, N, ld, p.chunk, p.ctas_per_row);
+    softmax_finalize_kernel<false>
+        <<<grid, kT, 0, s>>>(x, y, part, M, N, ld, p.chunk, p.ctas_per_row);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_device_error(cudaStream_t s, unsigned* value) {
+  unsigned host = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&host, g_device_error, sizeof(host), 0,
+                                            cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && host != 0) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbolAsync(g_device_error, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  }
+  *value = host;
+  return e;
+}
+
+}  // namespace rrs

@@ -1,0 +1,99 @@
+"""Helpers for the GPU parity tests: guarded device buffers and the tolerance checks.
+
+Tolerances (floating point, fp32 kernel against the float64 oracle):
+  * max |y - y_oracle| <= 2e-6 over every finite row;
+  * max_i |sum_j y_ij - 1| <= 1e-5 (sum taken in float64 on the host);
+  * |y - y_oracle| <= 1e-5 * y_oracle wherever y_oracle >= 1e-30;
+  * y == 0 exactly where x == -inf (rows with a finite entry);
+  * rows the oracle makes NaN (all -inf, +inf, NaN inside) are all NaN;
+  * row sums: |r - r_oracle| <= 1e-5 * sum_j |x_ij| (an absolute 1e-5 is
+    below one fp32 ulp of sums of magnitude 100+).
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+SENTINEL_BITS = 0x7FC0DEAD        # a quiet NaN nobody computes
+GUARD = 64                        # floats of canary before and after each buffer
+
+ABS_TOL = 2e-6
+ROW_SUM_TOL = 1e-5
+REL_TOL = 1e-5
+REL_FLOOR = 1e-30
+SUM_TOL = 1e-5
+
+
+def sentinel_fill(t: torch.Tensor) -> None:
+    t.view(torch.int32).fill_(SENTINEL_BITS - (1 << 32) if SENTINEL_BITS >= 1 << 31 else SENTINEL_BITS)
+
+
+class Guarded:
+    """A device buffer of ``M`` rows of stride ``ld`` with canaries around it.
+
+    ``offset`` shifts the matrix start by that many floats (misaligned bases).
+    """
+
+    def __init__(self, M: int, ld: int, offset: int = 0, device="cuda"):
+        self.M, self.ld, self.offset = M, ld, offset
+        self.n = M * ld
+        self.raw = torch.empty(self.n + 2 * GUARD + offset, dtype=torch.float32, device=device)
+        sentinel_fill(self.raw)
+        self.start = GUARD + offset
+        self.mat = self.raw[self.start:self.start + self.n].view(M, ld) if M * ld else \
+            self.raw[self.start:self.start].view(M, ld)
+
+    @property
+    def ptr(self) -> int:
+        return self.raw.data_ptr() + 4 * self.start
+
+    def load(self, host: np.ndarray) -> None:
+        self.mat.copy_(torch.from_numpy(np.ascontiguousarray(host, dtype=np.float32)))
+
+    def untouched_outside(self, N: int) -> bool:
+        """True if every float outside the M x N window still holds the sentinel."""
+        bits = self.raw.view(torch.int32).cpu().numpy().astype(np.int64) & 0xFFFFFFFF
+        mask = np.ones(bits.shape, dtype=bool)
+        for i in range(self.M):
+            a = self.start + i * self.ld
+            mask[a:a + N] = False
+        return bool(np.all(bits[mask] == SENTINEL_BITS))
+
+
+def check_softmax(got: np.ndarray, x: np.ndarray, where: str = "") -> dict:
+    """Assert the tolerances above; returns the measured errors."""
+    got = np.asarray(got, dtype=np.float64)
+    want = oracle.softmax_rows(x)
+    M, N = want.shape
+    assert got.shape == (M, N), where
+    nan_rows = np.isnan(want).any(axis=1)
+    for i in np.nonzero(nan_rows)[0]:
+        assert np.all(np.isnan(got[i])), f"{where}: row {i} should be NaN"
+    ok = ~nan_rows
+    res = {"max_abs": 0.0, "row_sum": 0.0, "max_rel": 0.0}
+    if not ok.any() or N == 0:
+        return res
+    g, w, xv = got[ok], want[ok], np.asarray(x, dtype=np.float64)[ok]
+    assert np.all(np.isfinite(g)), f"{where}: non-finite output"
+    abs_err = float(np.max(np.abs(g - w)))
+    row_err = float(np.max(np.abs(g.sum(axis=1) - 1.0)))
+    big = w >= REL_FLOOR
+    rel_err = float(np.max(np.abs(g[big] - w[big]) / w[big])) if big.any() else 0.0
+    assert abs_err <= ABS_TOL, f"{where}: max abs err {abs_err:.3e}"
+    assert row_err <= ROW_SUM_TOL, f"{where}: row-sum err {row_err:.3e}"
+    assert rel_err <= REL_TOL, f"{where}: max rel err {rel_err:.3e}"
+    neg = np.isneginf(xv)
+    assert np.all(g[neg] == 0.0), f"{where}: -inf entries must give exactly 0"
+    res.update(max_abs=abs_err, row_sum=row_err, max_rel=rel_err)
+    return res
+
+
+def check_row_sum(got: np.ndarray, x: np.ndarray, where: str = "") -> float:
+    xv = np.asarray(x, dtype=np.float64)
+    want = oracle.row_sum(xv)
+    scale = np.sum(np.abs(xv), axis=1)
+    err = np.abs(np.asarray(got, dtype=np.float64) - want)
+    assert np.all(err <= SUM_TOL * scale + 0.0), f"{where}: row-sum err {float(np.max(err)):.3e}"
+    return float(np.max(err / np.maximum(scale, 1e-300))) if err.size else 0.0

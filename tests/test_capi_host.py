@@ -1,0 +1,176 @@
+"""Host-side tests of the C ABI (no GPU): exports, argument checks, the planner.
+
+Only calls that return before anything touches CUDA are made here: argument
+errors, the pure planner and the occupancy / wave arithmetic.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rrs.h")
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+OK, INVALID, ALIAS, CUDA, TIMEOUT, NOMEM, UNSUPPORTED = range(7)
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return re.findall(r"RRS_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_header_declares_the_two_entry_points(lib):
+    names = declared_symbols()
+    assert "softmax_rows" in names and "row_sum" in names
+    assert len(names) == len(set(names))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in enumerate(["RRS_OK", "RRS_ERR_INVALID_ARG", "RRS_ERR_ALIAS", "RRS_ERR_CUDA",
+                                 "RRS_ERR_TIMEOUT", "RRS_ERR_NOMEM", "RRS_ERR_UNSUPPORTED"]):
+        assert lib.rrs_status_string(code).decode() == name
+    assert lib.rrs_status_string(99).decode() == "RRS_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("fn", ["softmax_rows", "row_sum"])
+def test_argument_errors_before_any_launch(lib, fn):
+    f = getattr(lib, fn)
+    a, b = 0x10000, 0x900000
+    assert f(a, b, -1, 4, 4, None) == INVALID            # M < 0
+    assert f(a, b, 4, -1, 4, None) == INVALID            # N < 0
+    assert f(a, b, 4, 8, 7, None) == INVALID             # ld < N
+    assert f(a, b, 4, 0, 0, None) == INVALID             # ld < 1
+    assert f(a, b, 0, 8, 8, None) == OK                  # no rows: no work
+    assert f(None, None, 0, 8, 8, None) == OK
+    assert f(None, b, 4, 8, 8, None) == INVALID          # null x
+    assert f(a, None, 4, 8, 8, None) == INVALID          # null y / out
+    assert f(a + 2, b, 4, 8, 8, None) == INVALID         # not 4-byte aligned
+    assert f(a, a + 16, 4, 8, 8, None) == ALIAS          # overlapping ranges
+    assert f(a, b, 1 << 62, 1 << 20, 1 << 20, None) == INVALID  # extent overflow
+
+
+def test_softmax_no_columns_is_a_no_op(lib):
+    assert lib.softmax_rows(0x10000, 0x900000, 4, 0, 1, None) == OK
+
+
+def test_force_path_rejects_unknown(lib):
+    assert lib.rrs_force_path(99, -1) == INVALID
+    assert lib.rrs_force_path(-1, 99) == INVALID
+    assert lib.rrs_force_path(-1, -1) == OK
+
+
+# ----------------------------------------------------------------- planner ----
+
+def plan(M, N, ld=None, vector_ok=True, sms=152):
+    import row_reduction_softmax_gb300 as rrs
+    return rrs.plan_softmax(M, N, ld, vector_ok, sms)
+
+
+def test_planner_on_the_five_workloads(lib):
+    assert plan(128, 256)["path_name"] == "row_regs"
+    p2 = plan(8192, 1024)
+    assert p2["path_name"] == "row_regs" and p2["warps_per_row"] == 1 and p2["vec"] == 8
+    p3 = plan(4096, 32768)
+    assert p3["path_name"] == "cluster" and p3["cluster"] == 4 and p3["grid"] == 4096 * 4
+    p4 = plan(16384, 4096)
+    assert p4["path_name"] == "row_regs" and p4["warps_per_row"] == 4
+    p5 = plan(32, 1 << 20)
+    assert p5["path_name"] in ("two_phase", "grid")
+
+
+def test_planner_unaligned_takes_scalar_path(lib):
+    p = plan(100, 1000, ld=1001, vector_ok=False)
+    assert p["path_name"] == "two_phase" and p["vector_io"] == 0
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 31, 127, 128, 129, 255, 256, 257, 1000, 1024, 2047,
+                               2048, 2049, 4095, 4096, 4097, 8191, 16384, 16385, 32767, 32768,
+                               65536, 131072, 131073, 1 << 20, (1 << 20) + 3])
+@pytest.mark.parametrize("M", [1, 7, 152, 4096])
+def test_planner_covers_every_column(lib, M, N):
+    p = plan(M, N)
+    assert 32 <= p["threads"] <= 1024 and p["threads"] % 32 == 0
+    assert p["grid"] >= 1
+    n4 = N // 4
+    if p["path_name"] == "row_regs":
+        gt = 32 * p["warps_per_row"]
+        assert p["vec"] * gt >= n4 and (N % 4) <= gt
+        assert p["rows_per_cta"] * gt == p["threads"]
+    elif p["path_name"] == "cluster":
+        cs = p["cluster"]
+        assert 1 <= cs <= 16 and p["grid"] % cs == 0
+        seg4 = -(-n4 // cs)
+        assert seg4 <= p["vec"] * p["threads"]
+    elif p["path_name"] == "two_phase":
+        C, chunk = p["ctas_per_row"], p["chunk"]
+        assert chunk % 1024 == 0 and C * chunk >= N > (C - 1) * chunk
+        assert p["workspace_bytes"] == M * C * 8
+
+
+def test_forced_paths(lib):
+    import row_reduction_softmax_gb300 as rrs
+    try:
+        rrs.force_path("cluster")
+        assert plan(64, 1024)["path_name"] == "cluster"
+        rrs.force_path("two_phase")
+        assert plan(64, 1024)["path_name"] == "two_phase"
+        rrs.force_path("row_regs")
+        with pytest.raises(rrs.RRSError) as e:
+            plan(4, 65536)
+        assert e.value.status == UNSUPPORTED
+        with pytest.raises(rrs.RRSError):
+            plan(4, 1024, vector_ok=False)
+    finally:
+        rrs.force_path("auto", "auto")
+
+
+def test_row_sum_planner(lib):
+    import row_reduction_softmax_gb300 as rrs
+    p = rrs.plan_row_sum(4096, 32768)
+    assert p["path_name"] == "row" and p["threads"] == 512
+    p = rrs.plan_row_sum(32, 1 << 20)
+    assert p["path_name"] == "split" and p["ctas_per_row"] * p["chunk"] >= 1 << 20
+    p = rrs.plan_row_sum(10, 10)
+    assert p["path_name"] == "row" and p["warps_per_row"] == 1
+
+
+# ------------------------------------------- occupancy and wave arithmetic ----
+
+def load_hardware_problems():
+    rows = []
+    with open(os.path.join(GOLDEN, "hardware_problems.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            kind, rest = line.split(":", 1)
+            lhs, rhs = rest.split("->")
+            args = dict(kv.split("=") for kv in lhs.split())
+            want = dict(kv.split("=") for kv in rhs.split())
+            rows.append((kind.strip(), args, want))
+    return rows
+
+
+def test_occupancy_and_waves_match_the_lecture_problems(lib):
+    import row_reduction_softmax_gb300 as rrs
+    seen = set()
+    for kind, a, want in load_hardware_problems():
+        seen.add(kind)
+        if kind == "occupancy":
+            blocks, warps, pct = rrs.occupancy(int(a["threads"]), int(a["regs"]), int(a["sm_regs"]),
+                                               int(a["max_warps"]))
+            assert (blocks, warps) == (int(want["blocks"]), int(want["warps"]))
+            assert pct == float(want["percent"])
+        elif kind == "waves":
+            n, last, idle = rrs.waves(int(a["blocks"]), int(a["sms"]))
+            assert (n, last, idle) == (int(want["waves"]), int(want["last"]), int(want["idle"]))
+    assert seen == {"occupancy", "waves"}

@@ -1,0 +1,213 @@
+"""GPU parity of softmax_rows against the float64 oracle, through the C ABI.
+
+Small shapes run on every execution path (forced), with canary regions
+around x and y, leading-dimension gaps, misaligned bases and ragged tails;
+full-size workloads run on the path the planner picks (the launch the bench
+times) and are compared on sampled rows, plus properties on every row.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import row_reduction_softmax_gb300 as rrs
+import workloads
+from gpu_helpers import Guarded, check_softmax
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+PATHS = ["row_regs", "cluster", "two_phase"]
+
+SHAPES = [(1, 1), (3, 2), (5, 3), (7, 5), (4, 31), (9, 33), (16, 128), (17, 129), (128, 256),
+          (33, 1000), (8, 1024), (5, 2047), (3, 2049), (6, 4097), (4, 8191), (2, 16385),
+          (3, 32768), (2, 40000), (2, 131072), (2, 300001)]
+
+
+def supports(path: str, N: int, vector_ok: bool) -> bool:
+    if path == "row_regs":
+        return vector_ok and N <= 32768
+    if path == "cluster":
+        return vector_ok and N <= 131072
+    return True
+
+
+@pytest.fixture(autouse=True)
+def _auto_path(lib):
+    rrs.force_path("auto", "auto")
+    yield
+    rrs.force_path("auto", "auto")
+
+
+def run(x_host: np.ndarray, N: int, ld: int, path: str = "auto", x_off: int = 0, y_off: int = 0):
+    """softmax_rows through the C ABI on guarded buffers; returns (y[:, :N], guards_ok)."""
+    M = x_host.shape[0]
+    xb = Guarded(M, ld, x_off)
+    yb = Guarded(M, ld, y_off)
+    # only the M x N window is written: the ld gap keeps the NaN sentinel, so
+    # a kernel that reads past N poisons its row
+    xb.mat[:, :N].copy_(torch.from_numpy(np.ascontiguousarray(x_host[:, :N], dtype=np.float32)))
+    rrs.force_path(path)
+    rrs.softmax_rows_ptr(xb.ptr, yb.ptr, M, N, ld, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    y = yb.mat[:, :N].cpu().numpy()
+    return y, yb.untouched_outside(N) and xb.untouched_outside(N)
+
+
+def recipe(name: str, M: int, N: int) -> np.ndarray:
+    return workloads.matrix(workloads.WORKLOADS[name].with_shape(M, N))
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("M,N", SHAPES)
+def test_parity_small(path, M, N):
+    if not supports(path, N, True):
+        pytest.skip("shape outside this path")
+    name = ["c1", "c2", "c3", "c4", "c5"][(M + N) % 5]
+    x = recipe(name, M, N)
+    y, guards = run(x, N, N, path)
+    check_softmax(y, x, f"{path} {M}x{N} {name}")
+    assert guards, "wrote outside the M x N window"
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("M,N,gap", [(5, 1000, 4), (3, 4096, 8), (4, 32768, 4), (6, 257, 12)])
+def test_leading_dimension_gap(path, M, N, gap):
+    if not supports(path, N, True):
+        pytest.skip("shape outside this path")
+    x = recipe("c4", M, N)
+    y, guards = run(x, N, N + gap, path)
+    check_softmax(y, x, f"{path} ld={N + gap}")
+    assert guards
+
+
+@pytest.mark.parametrize("M,N,ld,x_off,y_off", [(4, 1000, 1001, 0, 0), (3, 4096, 4096, 1, 0),
+                                                (3, 4096, 4096, 0, 3), (5, 33, 35, 2, 1),
+                                                (2, 40000, 40003, 1, 1)])
+def test_unaligned_takes_scalar_path(M, N, ld, x_off, y_off):
+    x = recipe("c2", M, N)
+    y, guards = run(x, N, ld, "auto", x_off, y_off)
+    check_softmax(y, x, f"unaligned {M}x{N} ld={ld}")
+    assert guards
+    with pytest.raises(rrs.RRSError) as e:
+        run(x, N, ld, "row_regs", x_off, y_off)
+    assert e.value.status == 6
+
+
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("N", [2, 7, 1024, 5000, 40000])
+def test_special_values(path, N):
+    if not supports(path, N, True):
+        pytest.skip("shape outside this path")
+    rng = np.random.default_rng(N)
+    x = rng.normal(0, 3, size=(8, N)).astype(np.float32)
+    x[0] = -np.inf                              # all masked: NaN row
+    x[1, :] = 7.25                              # constant row: uniform
+    x[2, 1:] = -np.inf                          # one finite entry: one-hot
+    x[3, N // 2] = np.inf                       # +inf: NaN row
+    x[4, N - 1] = np.nan                        # NaN: NaN row
+    x[5, ::2] = -np.inf                         # half masked
+    x[6] += 1000.0                              # large offset (shift invariance)
+    x[7, 0] = 88.0                              # a spike near exp's fp32 range
+    y, guards = run(x, N, N, path)
+    check_softmax(y, x, f"{path} specials N={N}")
+    assert guards
+    assert np.all(y[1] == y[1][0])
+    assert y[2, 0] == 1.0 and np.all(y[2, 1:] == 0.0)
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_shift_invariance_on_gpu(path):
+    N = 4096 if path != "cluster" else 40000
+    x = recipe("c2", 16, N)
+    y0, _ = run(x, N, N, path)
+    y1, _ = run(x + np.float32(1000.0), N, N, path)
+    check_softmax(y1, x + np.float32(1000.0), "shifted")
+    assert np.max(np.abs(y0.astype(np.float64) - y1)) <= 2e-6
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_bitwise_deterministic(path):
+    N = 2049 if path != "cluster" else 50000
+    x = recipe("c3", 32, N)
+    a, _ = run(x, N, N, path)
+    b, _ = run(x, N, N, path)
+    assert np.array_equal(a.view(np.int32), b.view(np.int32))
+
+
+def test_empty_and_tensor_api():
+    x = torch.randn(0, 7, device="cuda")
+    assert rrs.softmax_rows(x).shape == (0, 7)
+    x = torch.randn(5, 0, device="cuda")
+    assert rrs.softmax_rows(x).shape == (5, 0)
+    x = torch.randn(6, 100, device="cuda")
+    y = rrs.softmax_rows(x)
+    torch.cuda.synchronize()
+    check_softmax(y.cpu().numpy(), x.cpu().numpy(), "tensor api")
+    with pytest.raises(ValueError):
+        rrs.softmax_rows(x.cpu())
+    with pytest.raises(ValueError):
+        rrs.softmax_rows(x.double())
+
+
+def test_rejects_host_memory():
+    host = np.zeros((4, 64), dtype=np.float32)
+    dev = torch.zeros(4, 64, device="cuda")
+    with pytest.raises(rrs.RRSError) as e:
+        rrs.softmax_rows_ptr(host.ctypes.data, dev.data_ptr(), 4, 64, 64, 0)
+    assert e.value.status == 1
+    with pytest.raises(rrs.RRSError) as e:
+        rrs.softmax_rows_ptr(dev.data_ptr(), dev.data_ptr() + 64, 4, 64, 64, 0)
+    assert e.value.status == 2
+
+
+def test_two_streams_use_separate_workspaces():
+    rrs.force_path("two_phase")
+    xs = [recipe("c5", 4, 300000 + 17 * i) for i in range(2)]
+    outs = []
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    dev_x = [torch.from_numpy(x).cuda() for x in xs]
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for s, dx in zip(streams, dev_x):
+            with torch.cuda.stream(s):
+                outs.append(rrs.softmax_rows(dx))
+    torch.cuda.synchronize()
+    for k, y in enumerate(outs):
+        check_softmax(y.cpu().numpy(), xs[k % 2], f"stream {k % 2}")
+
+
+# ------------------------------------------------------- full-size workloads --
+
+SAMPLE_ROWS = 12
+
+
+def sampled_rows(M: int, seed: int) -> list[int]:
+    rng = np.random.default_rng(seed + 1000)
+    rows = {0, M - 1, M // 2}
+    rows.update(rng.choice(M, size=min(M, SAMPLE_ROWS), replace=False).tolist())
+    return sorted(rows)
+
+
+@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c4", "c5"])
+def test_full_size_workload(name):
+    w = workloads.WORKLOADS[name]
+    x_host = workloads.matrix(w)
+    x = torch.from_numpy(x_host).cuda()
+    y = torch.empty_like(x)
+    rrs.softmax_rows(x, y)                     # the planner's path, as the bench launches it
+    torch.cuda.synchronize()
+    assert rrs.device_error() == 0
+    rows = sampled_rows(w.M, w.seed)
+    got = y[rows].cpu().numpy()
+    check_softmax(got, x_host[rows], f"{name} sampled rows")
+    # properties on every row, computed on the device in float64
+    sums = y.double().sum(dim=1)
+    assert float((sums - 1.0).abs().max()) <= 1e-5
+    assert bool(torch.isfinite(y).all())
+    if name == "c4":
+        assert bool((y[torch.isneginf(x)] == 0).all())
+        spikes = x == 50.0
+        assert int(spikes.sum()) == w.M * 205
+    del x, y
+    torch.cuda.empty_cache()
