@@ -108,6 +108,30 @@ RRS_API int softmax_rows(const float* x, float* y, int64_t M, int64_t N, int64_t
  * softmax_rows. */
 RRS_API int row_sum(const float* x, float* out, int64_t M, int64_t N, int64_t ld, void* stream);
 
+/* softmax_rows for callers that cannot allocate device memory.  The paper
+ * has no counterpart: this is a deployment variant of the same operation.
+ *
+ * Some callers may not call cudaMalloc or anything that allocates: a
+ * plugin's execute hook inside an inference engine that owns all device
+ * memory, or a latency-critical loop where an allocation could synchronise
+ * the device or fail mid-step.  softmax_rows may allocate a small workspace
+ * the first time it meets a stream; this call never allocates.  It runs the
+ * two-phase kernels with their (max, sum) partials in a fixed 1 MiB array of
+ * device memory inside the library (131072 pairs), which every GPU that
+ * loads the library holds until the process exits.
+ *
+ * Same arguments, layout, results and error codes as softmax_rows, plus
+ * RRS_ERR_INVALID_ARG when M > 131072 (each row needs a slot).  Rows are cut
+ * into at most 131072 / M chunks, so few-row calls keep their parallelism.
+ * The first call on a device looks up the array's device address with that
+ * device current; make that first call before any stream capture.  All calls
+ * on a device share the array and it keeps the last call's contents (nothing
+ * needs clearing: each call writes every slot it reads).  Calls whose kernels
+ * overlap on the GPU -- on different streams or host threads -- race on it,
+ * so order them on one stream. */
+RRS_API int softmax_rows_noalloc(const float* x, float* y, int64_t M, int64_t N, int64_t ld,
+                                 void* stream);
+
 /* Synchronises `stream`, then returns and clears the device-side error word
  * of the current device: RRS_ERR_TIMEOUT if a split-row kernel stopped
  * waiting for its peers since the last call (its output is then incomplete),

@@ -64,6 +64,7 @@ _P = ctypes.c_void_p
 
 _SIGNATURES = {
     "softmax_rows": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P]),
+    "softmax_rows_noalloc": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P]),
     "row_sum": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P]),
     "rrs_device_error": (ctypes.c_int, [_P]),
     "rrs_status_string": (ctypes.c_char_p, [ctypes.c_int]),

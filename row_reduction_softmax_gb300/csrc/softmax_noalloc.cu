@@ -1,0 +1,134 @@
+// softmax_rows_noalloc: the row softmax for callers that may not allocate
+// device memory.
+//
+// Some callers cannot call cudaMalloc (or any allocating routine) on the
+// path that calls this library: a plugin's execute/enqueue hook inside an
+// inference engine, where the host framework owns every byte of device
+// memory and allocation there is forbidden; or a latency-critical loop where
+// an allocation could synchronise the device or fail under memory pressure
+// halfway through a step.  softmax_rows may allocate a small workspace on
+// first use of a stream; this entry point never does.  It runs the same
+// two-phase kernels (per-chunk (max, sum) partials, then merge, re-read and
+// write) with the partials in a fixed array of device memory that is part of
+// the library image itself.
+//
+// The array is a file-scope __device__ variable, so every GPU that loads the
+// library holds it until the process exits.  In host code its name is only a
+// host-side stand-in, never a device address: the device address is taken
+// once per device with cudaGetSymbolAddress, with that device current, and
+// passed to the kernels.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <climits>
+#include <cstring>
+#include <map>
+#include <mutex>
+
+#include "device_common.cuh"
+#include "internal.h"
+#include "rrs.h"
+
+namespace rrs {
+namespace {
+
+// Capacity: (max, sum) pairs, one per (row, chunk) of a call.  8 bytes each,
+// so 1 MiB of device memory per GPU.
+constexpr int64_t kNoAllocPairs = 131072;
+
+static __device__ __align__(256) MaxSum g_noalloc_partials[kNoAllocPairs];
+
+struct NoAllocDevice {
+  void* scratch = nullptr;  // device address of g_noalloc_partials on this device
+  int sm_count = 0;
+};
+
+std::mutex g_noalloc_mu;
+std::map<int, NoAllocDevice> g_noalloc_devices;
+
+// Set-up, once per device, with that device current (the caller's current
+// device at its first call): look up the scratch array's device address.
+int noalloc_device(int dev, NoAllocDevice* out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  auto it = g_noalloc_devices.find(dev);
+  if (it != g_noalloc_devices.end()) {
+    *out = it->second;
+    return RRS_OK;
+  }
+  NoAllocDevice d;
+  cudaError_t e = cudaGetSymbolAddress(&d.scratch, g_noalloc_partials);
+  if (e != cudaSuccess || d.scratch == nullptr) return RRS_ERR_CUDA;
+  e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return RRS_ERR_CUDA;
+  g_noalloc_devices[dev] = d;
+  *out = d;
+  return RRS_OK;
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace
+}  // namespace rrs
+
+using namespace rrs;
+
+extern "C" RRS_API int softmax_rows_noalloc(const float* x, float* y, int64_t M, int64_t N,
+                                            int64_t ld, void* stream) {
+  if (M < 0 || N < 0) return RRS_ERR_INVALID_ARG;
+  if (ld < 1 || ld < N) return RRS_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return RRS_OK;
+  if (!x || !y) return RRS_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(x) % 4 || reinterpret_cast<uintptr_t>(y) % 4)
+    return RRS_ERR_INVALID_ARG;
+  if (M - 1 > (INT64_MAX / 8 - N) / ld) return RRS_ERR_INVALID_ARG;
+  // Every row needs at least one (max, sum) slot of the fixed scratch.
+  if (M > kNoAllocPairs) return RRS_ERR_INVALID_ARG;
+  const int64_t bytes = ((M - 1) * ld + N) * 4;
+  const uintptr_t xa = reinterpret_cast<uintptr_t>(x), ya = reinterpret_cast<uintptr_t>(y);
+  if (xa < ya + (uintptr_t)bytes && ya < xa + (uintptr_t)bytes)
+    return RRS_ERR_ALIAS;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return RRS_ERR_CUDA;
+  for (const void* p : {static_cast<const void*>(x), static_cast<const void*>(y)}) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return RRS_ERR_INVALID_ARG;
+    }
+    const bool ok = a.type == cudaMemoryTypeManaged || (a.type == cudaMemoryTypeDevice && a.device == dev);
+    if (!ok) return RRS_ERR_INVALID_ARG;
+  }
+  NoAllocDevice d;
+  int st = noalloc_device(dev, &d);
+  if (st != RRS_OK) return st;
+
+  // Chunks per row: enough CTAs to fill the GPU, chunks of at least 1024
+  // columns, and never more (row, chunk) pairs than the scratch holds.
+  int64_t C = std::max<int64_t>(1, std::min(cdiv(4 * (int64_t)d.sm_count, M), cdiv(N, 4096)));
+  C = std::min<int64_t>(C, kNoAllocPairs / M);
+  const int64_t chunk = cdiv(cdiv(N, C), kChunkAlign) * kChunkAlign;
+  C = cdiv(N, chunk);
+
+  rrs_plan plan;
+  std::memset(&plan, 0, sizeof(plan));
+  plan.path = RRS_PATH_TWO_PHASE;
+  plan.threads = kSplitThreads;
+  plan.cluster = 1;
+  plan.ctas_per_row = C;
+  plan.chunk = chunk;
+  plan.rows_per_cta = 1;
+  plan.rounds = 1;
+  plan.grid = std::min<int64_t>(M * C, 32 * (int64_t)d.sm_count);
+  plan.vector_io = (xa % 16 == 0 && ya % 16 == 0 && ld % 4 == 0) ? 1 : 0;
+  plan.workspace_bytes = 0;
+
+  // All calls on this device share the one scratch array and it keeps the
+  // last call's partials.  Nothing in it needs to start at zero: the first
+  // kernel writes every slot the second kernel reads.  Two calls whose
+  // kernels overlap on the GPU (other streams, other host threads) race on it.
+  e = launch_softmax_two_phase(plan, x, y, M, N, ld, d.scratch, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return RRS_ERR_CUDA;
+  return RRS_OK;
+}
