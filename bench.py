@@ -218,6 +218,17 @@ def oracle_parity_row_sum(out_dev, w, rows):
             "max_normwise": float(np.max(np.abs(got - want) / scale))}
 
 
+def kernel_of(plan: dict) -> str:
+    """Name of the kernel a plan launches (the two-phase path launches two)."""
+    name = plan["path_name"]
+    if name == "row_staged":
+        return "softmax_staged_rows_kernel" if plan["vec"] > 0 else "softmax_staged_long_kernel"
+    return {"row_regs": "softmax_row_regs_kernel", "cluster": "softmax_cluster_kernel",
+            "two_phase": "softmax_partials_kernel+softmax_finalize_kernel",
+            "grid": "softmax_grid_kernel", "row": "row_sum_rows_kernel",
+            "split": "row_sum_partials_kernel+row_sum_finalize_kernel"}.get(name, name)
+
+
 def l2_pairs(torch, pair_bytes: int) -> int:
     l2 = getattr(torch.cuda.get_device_properties(torch.cuda.current_device()), "L2_cache_size", 0) \
         or 129 * 10**6
@@ -291,10 +302,7 @@ def run_ours(args):
     alg_bytes = 8 * M * N
     achieved = alg_bytes / (ms_per_step / 1e3) / 1e9
     peak, peak_kind = measured_hbm_peak()
-    kernel_name = {"row_regs": "softmax_row_regs_kernel", "cluster": "softmax_cluster_kernel",
-                   "two_phase": "softmax_partials_kernel+softmax_finalize_kernel",
-                   "row_staged": "softmax_row_staged_kernel", "grid": "softmax_grid_kernel"
-                   }.get(plan["path_name"], plan["path_name"])
+    kernel_name = kernel_of(plan)
     parity = oracle_parity_softmax(ys[(args.steps - 1) % npairs], w, sampled_rows(M, 16, w.seed)) \
         if rank == 0 else None
 
@@ -458,6 +466,7 @@ def run_suite(args, torch, rrs, dev, rank):
         ms = ev0.elapsed_time(ev1) / args.suite_steps
         gbs = alg / (ms / 1e3) / 1e9
         entry = {"workload": name, "op": op, "M": M, "N": N, "path": plan["path_name"],
+                 "kernel": kernel_of(plan),
                  "grid": plan["grid"], "threads": plan["threads"], "cluster": plan["cluster"],
                  "ms_per_call": ms, "rows_per_s": M / (ms / 1e3), "hbm_gbs": gbs,
                  "frac_of_8tbs": gbs / ROOFLINE_GBS, "frac_of_peak": gbs / peak,

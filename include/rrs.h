@@ -92,6 +92,8 @@ typedef struct rrs_plan {
   int32_t smem_bytes;    /* dynamic shared memory per CTA */
   int32_t vector_io;     /* 1 if 128-bit loads/stores are used */
   int64_t workspace_bytes;
+  int32_t stages;        /* shared-memory ring depth (staged paths) */
+  int32_t tile;          /* floats per shared-memory stage (staged paths) */
 } rrs_plan;
 
 /* y = softmax over each row of x (see the top of this file).

@@ -50,6 +50,7 @@ class Plan(ctypes.Structure):
         ("rows_per_cta", ctypes.c_int32), ("ctas_per_row", ctypes.c_int64),
         ("chunk", ctypes.c_int64), ("rounds", ctypes.c_int64), ("smem_bytes", ctypes.c_int32),
         ("vector_io", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
+        ("stages", ctypes.c_int32), ("tile", ctypes.c_int32),
     ]
 
     def as_dict(self) -> dict:

@@ -10,10 +10,12 @@
 #include <algorithm>
 #include <atomic>
 #include <climits>
+#include <cmath>
 #include <cstring>
 #include <map>
 #include <mutex>
 #include <string>
+#include <tuple>
 #include <utility>
 
 #include "internal.h"
@@ -63,25 +65,32 @@ int device_info(int dev, DeviceInfo* out) {
   if (e == cudaSuccess)
     e = cudaDeviceGetAttribute(&d.coop_launch, cudaDevAttrCooperativeLaunch, dev);
   if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
+  d.grid_per_sm = grid_blocks_per_sm();
   g_devices[dev] = d;
   *out = d;
   return RRS_OK;
 }
 
 // --------------------------------------------------------------- workspace ---
-// One buffer per (device, stream): calls on one stream are ordered, so they
-// can share it; calls on different streams never do.  Grown with the
-// stream-ordered allocator, so growth is ordered after earlier work on the
-// stream that still reads the old buffer.
+// One buffer per (device, stream, kind): calls on one stream are ordered, so
+// they can share it; calls on different streams never do.  Grown with the
+// stream-ordered allocator (ordered after earlier work on the stream that
+// still reads the old buffer) and zero-filled when (re)allocated.  The GRID
+// kind also carries the ticket its partials are published under: one per
+// launch, never 0, so slots left by earlier launches never look current.
+enum WorkspaceKind { kWsTwoPhase = 0, kWsGrid = 1, kWsRowSum = 2 };
+
 struct Workspace {
   void* ptr = nullptr;
   size_t bytes = 0;
+  uint32_t ticket = 0;
 };
-std::map<std::pair<int, uintptr_t>, Workspace> g_workspaces;
+std::map<std::tuple<int, uintptr_t, int>, Workspace> g_workspaces;
 
-int get_workspace(int dev, cudaStream_t s, size_t bytes, void** ptr) {
+int get_workspace(int dev, cudaStream_t s, int kind, size_t bytes, void** ptr,
+                  uint32_t* ticket = nullptr) {
   std::lock_guard<std::mutex> lock(g_mu);
-  Workspace& w = g_workspaces[{dev, reinterpret_cast<uintptr_t>(s)}];
+  Workspace& w = g_workspaces[{dev, reinterpret_cast<uintptr_t>(s), kind}];
   if (w.bytes < bytes) {
     if (w.ptr) {
       cudaError_t e = cudaFreeAsync(w.ptr, s);
@@ -96,7 +105,13 @@ int get_workspace(int dev, cudaStream_t s, size_t bytes, void** ptr) {
       (void)cudaGetLastError();
       return fail(RRS_ERR_NOMEM, std::string("cudaMallocAsync(workspace): ") + cudaGetErrorString(e));
     }
+    e = cudaMemsetAsync(w.ptr, 0, want, s);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(workspace)");
     w.bytes = want;
+  }
+  if (ticket) {
+    if (++w.ticket == 0) w.ticket = 1;
+    *ticket = w.ticket;
   }
   *ptr = w.ptr;
   return RRS_OK;
@@ -195,31 +210,165 @@ void plan_two_phase(int64_t M, int64_t N, int sm_count, rrs_plan* p) {
   p->rounds = 1;
 }
 
+// Staged paths: one CTA per SM, shared-memory ring of `stages` stages.
+int64_t staged_budget(int smem_optin) { return (int64_t)smem_optin - staged_header_bytes(); }
+
+// Long rows keep a segment resident as 4 sub-tiles with at least 3 more
+// stages to prefetch into: a sub-tile is at most budget / 7.
+int64_t staged_tile_max(int smem_optin) { return (staged_budget(smem_optin) / 7) / 16 * 4; }
+
+constexpr int64_t kStagedRowsMaxN = 8192;
+constexpr int64_t kRowRegsAutoMaxN = 16384;
+constexpr double kPerSmBytesPerSec = 6.7e12 / 152.0;  // planning model only
+constexpr double kRoundSec = 0.3e-6;                   // per-round fixed cost (planning model)
+
+bool plan_staged_rows(int64_t M, int64_t N, int sm_count, int smem_optin, rrs_plan* p) {
+  if (N % 4 != 0 || N > kStagedRowsMaxN) return false;
+  const int64_t n4 = N / 4;
+  int gw, vec;
+  if (n4 <= 32 * 16) {
+    gw = 1;
+    vec = std::max(1, pow2_ceil(ceil_div(n4, 32)));
+  } else {
+    vec = 8;
+    gw = pow2_ceil(ceil_div(n4, 32 * 8));
+  }
+  const int64_t G = std::min<int64_t>(M, sm_count);
+  const int64_t rows_per_cta = ceil_div(M, G);
+  const int64_t tile = round_up(N, 32);  // stage stride: a multiple of 128 bytes
+  // Stage s is filled by producer lane s % groups and drained by consumer
+  // group s % groups, so the ring depth is a multiple of the group count.
+  const int64_t groups = staged_consumer_warps() / gw;
+  int64_t ns = std::min<int64_t>(std::min<int64_t>(staged_max_stages(),
+                                                   staged_budget(smem_optin) / (tile * 4)),
+                                 round_up(rows_per_cta, groups));
+  ns = ns / groups * groups;
+  if (ns < groups) return false;
+  p->path = RRS_PATH_ROW_STAGED;
+  p->vec = vec;
+  p->warps_per_row = gw;
+  p->threads = staged_threads();
+  p->grid = G;
+  p->rows_per_cta = 1;
+  p->ctas_per_row = 1;
+  p->chunk = N;
+  p->rounds = rows_per_cta;
+  p->stages = (int32_t)ns;
+  p->tile = (int32_t)tile;
+  p->smem_bytes = (int32_t)(staged_header_bytes() + ns * tile * 4);
+  return true;
+}
+
+bool plan_staged_long(int64_t M, int64_t N, int sm_count, int smem_optin, rrs_plan* p) {
+  if (N % 4 != 0) return false;
+  const int64_t tile = round_up(ceil_div(N, 4), 4);
+  if (tile > staged_tile_max(smem_optin)) return false;
+  const int64_t ns = std::min<int64_t>(staged_max_stages(), staged_budget(smem_optin) / (tile * 4));
+  const int64_t G = std::min<int64_t>(M, sm_count);
+  p->path = RRS_PATH_ROW_STAGED;
+  p->vec = 0;
+  p->warps_per_row = 8;
+  p->threads = staged_threads();
+  p->grid = G;
+  p->rows_per_cta = 1;
+  p->ctas_per_row = 1;
+  p->chunk = N;
+  p->rounds = ceil_div(M, G);
+  p->stages = (int32_t)ns;
+  p->tile = (int32_t)tile;
+  p->smem_bytes = (int32_t)(staged_header_bytes() + ns * tile * 4);
+  return true;
+}
+
+// GRID: C segments per row of at most kGridThreads * kGridMaxVec float4
+// each, R rows per round, R * C <= G = SMs x resident CTAs.  C is chosen to
+// minimise rounds x (per-CTA segment time + a fixed per-round cost).
+bool plan_grid(int64_t M, int64_t N, int sm_count, int per_sm, int coop_ok, rrs_plan* p) {
+  if (N % 4 != 0 || !coop_ok || per_sm < 1) return false;
+  const int64_t G = (int64_t)sm_count * per_sm;
+  const int64_t cap = (int64_t)kGridThreads * kGridMaxVec * 4;  // floats per CTA
+  const int64_t c_min = ceil_div(N, cap);
+  if (c_min > G) return false;
+  const double per_cta_bw = kPerSmBytesPerSec / (double)per_sm;
+  double best = 1e300;
+  int64_t best_seg = 0, best_c = 0, best_r = 0;
+  for (int64_t c = c_min; c <= G; ++c) {
+    const int64_t seg = round_up(ceil_div(N, c), 4);
+    const int64_t C = ceil_div(N, seg);
+    int64_t R = std::min<int64_t>(G / C, M);
+    if (R < 1) continue;
+    const double rounds = (double)ceil_div(M, R);
+    const double t = rounds * (8.0 * (double)seg / per_cta_bw + kRoundSec);
+    if (t < best * (1.0 - 1e-9)) {
+      best = t;
+      best_seg = seg;
+      best_c = C;
+      best_r = R;
+    }
+  }
+  if (best_seg == 0) return false;
+  p->path = RRS_PATH_GRID;
+  p->vec = (ceil_div(best_seg, 4) <= (int64_t)kGridThreads * 2) ? 2 : 4;
+  p->warps_per_row = kGridThreads / 32;
+  p->threads = kGridThreads;
+  p->grid = best_r * best_c;
+  p->rows_per_cta = (int32_t)best_r;
+  p->ctas_per_row = best_c;
+  p->chunk = best_seg;
+  p->rounds = ceil_div(M, best_r);
+  p->workspace_bytes = M * best_c * 16;
+  return true;
+}
+
 int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_count,
-                      int smem_optin, int cluster_ok, int forced, rrs_plan* p) {
+                      int smem_optin, int cluster_ok, int coop_ok, int grid_per_sm, int forced,
+                      rrs_plan* p) {
   std::memset(p, 0, sizeof(*p));
   if (M < 0 || N < 0 || ld < 1 || ld < N || sm_count < 1)
     return fail(RRS_ERR_INVALID_ARG, "bad shape or device description");
-  (void)smem_optin;
   p->cluster = 1;
   p->vector_io = vector_ok ? 1 : 0;
   if (M == 0 || N == 0) {
     p->path = (forced == RRS_PATH_AUTO) ? RRS_PATH_ROW_REGS : forced;
     return RRS_OK;
   }
-  int path = forced;
-  if (path == RRS_PATH_AUTO) {
+  if (forced == RRS_PATH_AUTO) {
+    // Measured on GB300: registers win for rows that fit one CTA, the cluster
+    // split for rows up to 16 CTAs' registers, the two-phase split beyond.
+    rrs_plan c;
     if (!vector_ok) {
-      path = RRS_PATH_TWO_PHASE;
-    } else if (N <= 16384) {
-      path = RRS_PATH_ROW_REGS;
-    } else if (cluster_ok && N <= (int64_t)kClusterMax * kSplitThreads * kClusterVec * 4) {
-      path = RRS_PATH_CLUSTER;
+      plan_two_phase(M, N, sm_count, p);
+    } else if (N % 4 != 0) {
+      if (row_regs_fits(N)) plan_row_regs(M, N, sm_count, p);
+      else plan_two_phase(M, N, sm_count, p);
+    } else if (N <= kRowRegsAutoMaxN) {
+      plan_row_regs(M, N, sm_count, p);
+    } else if (cluster_ok && plan_cluster(M, N, &c)) {
+      *p = c;
     } else {
-      path = RRS_PATH_TWO_PHASE;
+      plan_two_phase(M, N, sm_count, p);
     }
+    p->cluster = std::max(p->cluster, 1);
+    p->vector_io = vector_ok ? 1 : 0;
+    return RRS_OK;
   }
+  const int path = forced;
   switch (path) {
+    case RRS_PATH_ROW_STAGED:
+      if (vector_ok && (plan_staged_rows(M, N, sm_count, smem_optin, p) ||
+                        plan_staged_long(M, N, sm_count, smem_optin, p))) {
+        p->cluster = 1;
+        p->vector_io = 1;
+        return RRS_OK;
+      }
+      return fail(RRS_ERR_UNSUPPORTED, "ROW_STAGED needs 16-byte alignment, N % 4 == 0, N <= 32912");
+    case RRS_PATH_GRID:
+      if (vector_ok && plan_grid(M, N, sm_count, grid_per_sm, coop_ok, p)) {
+        p->cluster = 1;
+        p->vector_io = 1;
+        return RRS_OK;
+      }
+      return fail(RRS_ERR_UNSUPPORTED, "GRID needs 16-byte alignment, N % 4 == 0, cooperative launch");
     case RRS_PATH_ROW_REGS:
       if (!vector_ok || !row_regs_fits(N))
         return fail(RRS_ERR_UNSUPPORTED, "ROW_REGS needs 16-byte alignment and N <= 32768");
@@ -319,7 +468,7 @@ RRS_API int rrs_force_path(int softmax_path, int sum_path) {
 RRS_API int rrs_plan_softmax(int64_t M, int64_t N, int64_t ld, int vector_ok_flag, int sm_count,
                              int smem_optin, rrs_plan* plan) {
   if (!plan) return RRS_ERR_INVALID_ARG;
-  return plan_softmax_impl(M, N, ld, vector_ok_flag, sm_count, smem_optin, 1,
+  return plan_softmax_impl(M, N, ld, vector_ok_flag, sm_count, smem_optin, 1, 1, kDefaultGridPerSm,
                            g_force_softmax.load(), plan);
 }
 
@@ -376,7 +525,8 @@ RRS_API int softmax_rows(const float* x, float* y, int64_t M, int64_t N, int64_t
 
   rrs_plan plan;
   st = plan_softmax_impl(M, N, ld, vector_ok(x, y, ld) ? 1 : 0, info.sm_count, info.smem_optin,
-                         info.cluster_launch, g_force_softmax.load(), &plan);
+                         info.cluster_launch, info.coop_launch, info.grid_per_sm,
+                         g_force_softmax.load(), &plan);
   if (st != RRS_OK) return st;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -387,9 +537,22 @@ RRS_API int softmax_rows(const float* x, float* y, int64_t M, int64_t N, int64_t
     case RRS_PATH_CLUSTER:
       e = launch_softmax_cluster(plan, x, y, M, N, ld, s);
       break;
+    case RRS_PATH_ROW_STAGED:
+      e = (plan.vec > 0) ? launch_softmax_staged_rows(plan, x, y, M, N, ld, s)
+                         : launch_softmax_staged_long(plan, x, y, M, N, ld, s);
+      break;
+    case RRS_PATH_GRID: {
+      void* ws = nullptr;
+      uint32_t ticket = 0;
+      if ((st = get_workspace(dev, s, kWsGrid, (size_t)plan.workspace_bytes, &ws, &ticket)) != RRS_OK)
+        return st;
+      e = launch_softmax_grid(plan, x, y, M, N, ld, ws, ticket, s);
+      break;
+    }
     case RRS_PATH_TWO_PHASE: {
       void* ws = nullptr;
-      if ((st = get_workspace(dev, s, (size_t)plan.workspace_bytes, &ws)) != RRS_OK) return st;
+      if ((st = get_workspace(dev, s, kWsTwoPhase, (size_t)plan.workspace_bytes, &ws)) != RRS_OK)
+        return st;
       e = launch_softmax_two_phase(plan, x, y, M, N, ld, ws, s);
       break;
     }
@@ -435,7 +598,8 @@ RRS_API int row_sum(const float* x, float* out, int64_t M, int64_t N, int64_t ld
       break;
     case RRS_SUM_SPLIT: {
       void* ws = nullptr;
-      if ((st = get_workspace(dev, s, (size_t)plan.workspace_bytes, &ws)) != RRS_OK) return st;
+      if ((st = get_workspace(dev, s, kWsRowSum, (size_t)plan.workspace_bytes, &ws)) != RRS_OK)
+        return st;
       e = launch_row_sum_split(plan, x, out, M, N, ld, ws, s);
       break;
     }
@@ -447,9 +611,11 @@ RRS_API int row_sum(const float* x, float* out, int64_t M, int64_t N, int64_t ld
 }
 
 RRS_API int rrs_device_error(void* stream) {
-  unsigned v = 0;
-  cudaError_t e = read_and_clear_device_error(static_cast<cudaStream_t>(stream), &v);
+  unsigned a = 0, b = 0;
+  cudaError_t e = read_and_clear_staged_error(static_cast<cudaStream_t>(stream), &a);
+  if (e == cudaSuccess) e = read_and_clear_grid_error(static_cast<cudaStream_t>(stream), &b);
   if (e != cudaSuccess) return fail_cuda(e, "rrs_device_error");
+  const unsigned v = a | b;
   return v ? fail(RRS_ERR_TIMEOUT, "a split-row kernel stopped waiting for its peers") : RRS_OK;
 }
 
@@ -460,7 +626,7 @@ RRS_API int rrs_release_workspace(void) {
   int status = RRS_OK;
   for (auto& kv : g_workspaces) {
     if (!kv.second.ptr) continue;
-    if (cudaSetDevice(kv.first.first) == cudaSuccess) {
+    if (cudaSetDevice(std::get<0>(kv.first)) == cudaSuccess) {
       cudaError_t e = cudaDeviceSynchronize();
       if (e == cudaSuccess) e = cudaFree(kv.second.ptr);
       if (e != cudaSuccess) status = fail_cuda(e, "rrs_release_workspace");

@@ -38,11 +38,19 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// 2^t on the SFU (PTX ex2.approx.ftz.f32: relative error about 2^-22 over
+// the whole range; results below the smallest normal float flush to +0).
+__device__ __forceinline__ float exp2_sfu(float t) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(t));
+  return r;
+}
+
 // exp(v - m) as 2^((v - m) log2 e).  v - m is exact where v == m, so the
 // row maximum always maps to exactly 1 and tied maxima stay tied; v = -inf
 // gives exactly 0; m = -inf (a row with no finite entry) gives NaN.
 __device__ __forceinline__ float exp_shifted(float v, float m) {
-  return exp2f((v - m) * kLog2e);
+  return exp2_sfu((v - m) * kLog2e);
 }
 
 __device__ __forceinline__ float max4(const float4& v) {
@@ -55,6 +63,13 @@ __device__ __forceinline__ float4 load_stream(const float4* p) { return __ldcs(p
 __device__ __forceinline__ void store_stream(float4* p, const float4& v) { __stcs(p, v); }
 __device__ __forceinline__ float load_stream(const float* p) { return __ldcs(p); }
 __device__ __forceinline__ void store_stream(float* p, float v) { __stcs(p, v); }
+
+// Start of every kernel launched with launch_pdl(): allow the next kernel on
+// the stream to be scheduled, then wait for the previous one to complete.
+__device__ __forceinline__ void pdl_entry() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
 // Named barrier over `threads` threads (a multiple of 32) of this CTA.
 __device__ __forceinline__ void named_barrier(int id, int threads) {

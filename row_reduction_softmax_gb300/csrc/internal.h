@@ -15,7 +15,11 @@ struct DeviceInfo {
   int smem_optin = 0;       // max dynamic shared memory per CTA (opt-in), bytes
   int cluster_launch = 0;   // thread-block clusters supported
   int coop_launch = 0;      // cooperative launch supported
+  int grid_per_sm = 0;      // resident CTAs per SM of the GRID kernel
 };
+
+// Planner default for a GB300 when no device is queried (rrs_plan_softmax).
+constexpr int kDefaultGridPerSm = 2;
 
 // Tuning limits shared by the planner and the launchers.
 constexpr int kRowRegsMaxVec = 16;       // float4 registers per thread (warp-per-row)
@@ -23,6 +27,8 @@ constexpr int kSplitThreads = 256;       // CTA size of the cluster / two-phase 
 constexpr int kClusterVec = 8;           // float4 per thread in a cluster CTA segment
 constexpr int kClusterMax = 16;          // largest cluster (non-portable beyond 8)
 constexpr int64_t kChunkAlign = 1024;    // two-phase chunk granularity (elements)
+constexpr int kGridThreads = 512;        // CTA size of the GRID kernel
+constexpr int kGridMaxVec = 4;           // float4 registers per thread per segment (GRID)
 
 // ---- softmax launchers (return the launch's cudaError_t) ----
 cudaError_t launch_softmax_row_regs(const rrs_plan& p, const float* x, float* y, int64_t M,
@@ -32,13 +38,33 @@ cudaError_t launch_softmax_cluster(const rrs_plan& p, const float* x, float* y, 
 cudaError_t launch_softmax_two_phase(const rrs_plan& p, const float* x, float* y, int64_t M,
                                      int64_t N, int64_t ld, void* workspace, cudaStream_t s);
 
+// Persistent TMA-staged kernels (softmax_staged.cu): ROW_STAGED plans with
+// vec > 0 run staged_rows (rows in registers), vec == 0 run staged_long
+// (a row staged as <= 4 shared-memory sub-tiles).
+int staged_header_bytes();
+int staged_max_stages();
+int staged_threads();
+int staged_consumer_warps();
+cudaError_t launch_softmax_staged_rows(const rrs_plan& p, const float* x, float* y, int64_t M,
+                                       int64_t N, int64_t ld, cudaStream_t s);
+cudaError_t launch_softmax_staged_long(const rrs_plan& p, const float* x, float* y, int64_t M,
+                                       int64_t N, int64_t ld, cudaStream_t s);
+
+// GRID plans (softmax_grid.cu): rows split over a cooperative persistent
+// grid of R * C CTAs; `workspace` holds 16 bytes per (row, segment) slot,
+// zero-filled when allocated, and `ticket` is unique per launch on it.
+cudaError_t launch_softmax_grid(const rrs_plan& p, const float* x, float* y, int64_t M, int64_t N,
+                                int64_t ld, void* workspace, uint32_t ticket, cudaStream_t s);
+int grid_blocks_per_sm();
+
 // ---- row-sum launchers ----
 cudaError_t launch_row_sum_rows(const rrs_plan& p, const float* x, float* out, int64_t M,
                                 int64_t N, int64_t ld, cudaStream_t s);
 cudaError_t launch_row_sum_split(const rrs_plan& p, const float* x, float* out, int64_t M,
                                  int64_t N, int64_t ld, void* workspace, cudaStream_t s);
 
-// ---- device error word (set by kernels that wait on peers with a bound) ----
-cudaError_t read_and_clear_device_error(cudaStream_t s, unsigned* value);
+// ---- device error words (set by kernels whose bounded waits ran out) ----
+cudaError_t read_and_clear_staged_error(cudaStream_t s, unsigned* value);
+cudaError_t read_and_clear_grid_error(cudaStream_t s, unsigned* value);
 
 }  // namespace rrs

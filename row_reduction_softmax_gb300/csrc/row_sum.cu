@@ -13,6 +13,7 @@
 //    second kernel adds a row's chunk sums in index order.
 #include "device_common.cuh"
 #include "internal.h"
+#include "launch_util.h"
 
 namespace rrs {
 namespace {
@@ -77,6 +78,7 @@ row_sum_rows_kernel(const float* __restrict__ x, float* __restrict__ out, int64_
   const int gw = warp % GW;
   const int gt = gw * 32 + lane;
   float* gred = red + group * GW;
+  pdl_entry();
 
   for (int64_t row = (int64_t)blockIdx.x * kGroups + group; row < M;
        row += (int64_t)gridDim.x * kGroups) {
@@ -100,6 +102,7 @@ row_sum_partials_kernel(const float* __restrict__ x, float* __restrict__ part, i
                         int64_t N, int64_t ld, int64_t chunk, int64_t C) {
   __shared__ float red[kSplitT / 32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  pdl_entry();
   for (int64_t w = blockIdx.x; w < M * C; w += gridDim.x) {
     const int64_t row = w / C;
     const int64_t c = w - row * C;
@@ -121,6 +124,7 @@ row_sum_finalize_kernel(const float* __restrict__ part, float* __restrict__ out,
                         int64_t C) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * 4;
+  pdl_entry();
   for (int64_t row = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5); row < M; row += warps) {
     float s = 0.f;
     for (int64_t k = lane; k < C; k += 32) s += part[row * C + k];
@@ -134,12 +138,11 @@ cudaError_t launch_rows_gw(const rrs_plan& p, const float* x, float* out, int64_
                            int64_t ld, cudaStream_t s) {
   constexpr int kThreads = sum_threads<GW>();
   if (p.threads != kThreads) return cudaErrorInvalidConfiguration;
-  if (p.vector_io) {
-    row_sum_rows_kernel<GW, true><<<(unsigned)p.grid, kThreads, 0, s>>>(x, out, M, N, ld);
-  } else {
-    row_sum_rows_kernel<GW, false><<<(unsigned)p.grid, kThreads, 0, s>>>(x, out, M, N, ld);
-  }
-  return cudaGetLastError();
+  if (p.vector_io)
+    return launch_pdl(row_sum_rows_kernel<GW, true>, dim3((unsigned)p.grid), dim3(kThreads), 0, s, 0,
+                      x, out, M, N, ld);
+  return launch_pdl(row_sum_rows_kernel<GW, false>, dim3((unsigned)p.grid), dim3(kThreads), 0, s, 0,
+                    x, out, M, N, ld);
 }
 
 }  // namespace
@@ -161,17 +164,16 @@ cudaError_t launch_row_sum_split(const rrs_plan& p, const float* x, float* out, 
                                  int64_t N, int64_t ld, void* workspace, cudaStream_t s) {
   if (p.threads != kSplitT) return cudaErrorInvalidConfiguration;
   float* part = static_cast<float*>(workspace);
-  if (p.vector_io) {
-    row_sum_partials_kernel<true>
-        <<<(unsigned)p.grid, kSplitT, 0, s>>>(x, part, M, N, ld, p.chunk, p.ctas_per_row);
-  } else {
-    row_sum_partials_kernel<false>
-        <<<(unsigned)p.grid, kSplitT, 0, s>>>(x, part, M, N, ld, p.chunk, p.ctas_per_row);
-  }
+  const dim3 grid((unsigned)p.grid), block(kSplitT);
+  cudaError_t e = p.vector_io
+                      ? launch_pdl(row_sum_partials_kernel<true>, grid, block, 0, s, 0, x, part, M,
+                                   N, ld, p.chunk, p.ctas_per_row)
+                      : launch_pdl(row_sum_partials_kernel<false>, grid, block, 0, s, 0, x, part, M,
+                                   N, ld, p.chunk, p.ctas_per_row);
+  if (e != cudaSuccess) return e;
   const int64_t fin_grid = (M + 3) / 4;
-  row_sum_finalize_kernel<<<(unsigned)(fin_grid < 65535 ? fin_grid : 65535), 128, 0, s>>>(
-      part, out, M, p.ctas_per_row);
-  return cudaGetLastError();
+  return launch_pdl(row_sum_finalize_kernel, dim3((unsigned)(fin_grid < 65535 ? fin_grid : 65535)),
+                    dim3(128), 0, s, 0, static_cast<const float*>(part), out, M, p.ctas_per_row);
 }
 
 }  // namespace rrs

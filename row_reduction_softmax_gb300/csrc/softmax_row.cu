@@ -11,6 +11,7 @@
 // every warp access is a full, coalesced 512-byte run.
 #include "device_common.cuh"
 #include "internal.h"
+#include "launch_util.h"
 
 namespace rrs {
 namespace {
@@ -70,6 +71,7 @@ softmax_row_regs_kernel(const float* __restrict__ x, float* __restrict__ y, int6
   const int n4 = N >> 2;
   const int rem = N & 3;
   const float kNeg = neg_inf();
+  pdl_entry();
 
   for (int64_t row = (int64_t)blockIdx.x * kGroups + group; row < M;
        row += (int64_t)gridDim.x * kGroups) {
@@ -124,9 +126,8 @@ cudaError_t launch_rr(const rrs_plan& p, const float* x, float* y, int64_t M, in
                       int64_t ld, cudaStream_t s) {
   constexpr int kThreads = threads_for<GW>();
   if (p.threads != kThreads) return cudaErrorInvalidConfiguration;
-  softmax_row_regs_kernel<VEC, GW>
-      <<<(unsigned)p.grid, kThreads, 0, s>>>(x, y, M, (int32_t)N, ld);
-  return cudaGetLastError();
+  return launch_pdl(softmax_row_regs_kernel<VEC, GW>, dim3((unsigned)p.grid), dim3(kThreads), 0, s,
+                    0, x, y, M, (int32_t)N, ld);
 }
 
 }  // namespace

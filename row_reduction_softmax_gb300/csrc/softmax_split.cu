@@ -20,14 +20,11 @@
 
 #include "device_common.cuh"
 #include "internal.h"
+#include "launch_util.h"
 
 namespace cg = cooperative_groups;
 
 namespace rrs {
-
-// Set by kernels that wait on peers with a bounded spin, read by
-// rrs_device_error().
-__device__ unsigned int g_device_error = 0;
 
 namespace {
 
@@ -67,6 +64,11 @@ __device__ __forceinline__ MaxSum cta_merge(MaxSum p, MaxSum* red) {
 __device__ __forceinline__ void cluster_arrive_release() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
+// Arrival that orders nothing: used once this CTA's reads of its peers'
+// shared memory have been consumed (their values are already in registers).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_wait_acquire() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -100,6 +102,7 @@ softmax_cluster_kernel(const float* __restrict__ x, float* __restrict__ y, int64
   const int e4 = min(b4 + seg4, n4);
   const bool has_tail = (rank == cs - 1) && (tid < rem);
   const float kNeg = neg_inf();
+  pdl_entry();
 
   for (int64_t row = cluster_id; row < M; row += nclusters) {
     const float* xr = x + row * ld;
@@ -144,7 +147,7 @@ softmax_cluster_kernel(const float* __restrict__ x, float* __restrict__ y, int64
       q = warp_merge(q);  // same lanes, same order in every CTA: identical result
       if (lane == 0) whole = q;
     }
-    cluster_arrive_release();  // done reading the peers' `part`
+    cluster_arrive_relaxed();  // done reading the peers' `part`
     __syncthreads();
     const MaxSum w = whole;
     const bool bad = !(w.s == w.s) || w.m == kNeg;  // NaN / inf / all -inf row
@@ -214,6 +217,7 @@ softmax_partials_kernel(const float* __restrict__ x, MaxSum* __restrict__ part, 
                         int64_t N, int64_t ld, int64_t chunk, int64_t C) {
   __shared__ MaxSum red[kW];
   const int64_t work = M * C;
+  pdl_entry();
   for (int64_t w = blockIdx.x; w < work; w += gridDim.x) {
     const int64_t row = w / C;
     const int64_t c = w - row * C;
@@ -234,6 +238,7 @@ softmax_finalize_kernel(const float* __restrict__ x, float* __restrict__ y,
   __shared__ MaxSum red[kW];
   const int64_t work = M * C;
   const int tid = threadIdx.x;
+  pdl_entry();
   for (int64_t w = blockIdx.x; w < work; w += gridDim.x) {
     const int64_t row = w / C;
     const int64_t c = w - row * C;
@@ -286,19 +291,8 @@ cudaError_t launch_cluster_vec(const rrs_plan& p, const float* x, float* y, int6
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)p.grid, 1, 1);
-  cfg.blockDim = dim3(kT, 1, 1);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)p.cluster;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, x, y, M, (int32_t)N, ld);
+  return launch_pdl(kern, dim3((unsigned)p.grid), dim3(kT), 0, s, p.cluster, x, y, M, (int32_t)N,
+                    ld);
 }
 
 }  // namespace
@@ -317,30 +311,21 @@ cudaError_t launch_softmax_two_phase(const rrs_plan& p, const float* x, float* y
                                      int64_t N, int64_t ld, void* workspace, cudaStream_t s) {
   if (p.threads != kT) return cudaErrorInvalidConfiguration;
   MaxSum* part = static_cast<MaxSum*>(workspace);
-  const unsigned grid = (unsigned)p.grid;
+  const dim3 grid((unsigned)p.grid), block(kT);
+  cudaError_t e;
   if (p.vector_io) {
-    softmax_partials_kernel<true><<<grid, kT, 0, s>>>(x, part, M, N, ld, p.chunk, p.ctas_per_row);
-    softmax_finalize_kernel<true>
-        <<<grid, kT, 0, s>>>(x, y, part, M, N, ld, p.chunk, p.ctas_per_row);
+    e = launch_pdl(softmax_partials_kernel<true>, grid, block, 0, s, 0, x, part, M, N, ld, p.chunk,
+                   p.ctas_per_row);
+    if (e == cudaSuccess)
+      e = launch_pdl(softmax_finalize_kernel<true>, grid, block, 0, s, 0, x, y, part, M, N, ld,
+                     p.chunk, p.ctas_per_row);
   } else {
-    softmax_partials_kernel<false><<<grid, kT, 0, s>>>(x, part, M, N, ld, p.chunk, p.ctas_per_row);
-    softmax_finalize_kernel<false>
-        <<<grid, kT, 0, s>>>(x, y, part, M, N, ld, p.chunk, p.ctas_per_row);
+    e = launch_pdl(softmax_partials_kernel<false>, grid, block, 0, s, 0, x, part, M, N, ld, p.chunk,
+                   p.ctas_per_row);
+    if (e == cudaSuccess)
+      e = launch_pdl(softmax_finalize_kernel<false>, grid, block, 0, s, 0, x, y, part, M, N, ld,
+                     p.chunk, p.ctas_per_row);
   }
-  return cudaGetLastError();
-}
-
-cudaError_t read_and_clear_device_error(cudaStream_t s, unsigned* value) {
-  unsigned host = 0;
-  cudaError_t e = cudaMemcpyFromSymbolAsync(&host, g_device_error, sizeof(host), 0,
-                                            cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  if (e == cudaSuccess && host != 0) {
-    const unsigned zero = 0;
-    e = cudaMemcpyToSymbolAsync(g_device_error, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
-  }
-  *value = host;
   return e;
 }
 

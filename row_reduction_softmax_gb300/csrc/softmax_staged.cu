@@ -1,0 +1,470 @@
+// Persistent, TMA-staged softmax kernels.
+//
+// The pages' fused softmax reads each row into on-chip memory once, reduces
+// it there and writes it once ("Kernels, Triton, XLA", section "Reductions
+// and tiling"); their row sum shows the tile loop for rows that overflow one
+// block (same section, "Row sum, when the row doesn't fit").  On GB300 the
+// HBM stream is kept busy by decoupling the loads from the arithmetic:
+//
+//  * one CTA per SM (the grid never has a tail wave: every CTA gets the same
+//    number of rows, +-1) runs a PRODUCER warp whose lanes issue 1-D bulk
+//    async copies (the TMA engine) of row data into a ring of NS
+//    shared-memory stages, each guarded by a "full" and an "empty" mbarrier
+//    (small copies are issued from several lanes: one lane issues them at
+//    only about one per 0.3 us);
+//  * sixteen CONSUMER warps wait on "full", pull the stage into registers or
+//    read it in place, reduce, and write y with 128-bit streaming stores,
+//    then arrive on "empty" so the producer can refill the stage.
+//
+// Two kernels:
+//  * staged_rows -- rows of at most 8192 floats.  A group of GW warps owns a
+//    row; the stage is released as soon as the row sits in registers.
+//    Stage s is always filled by producer lane s % G and drained by consumer
+//    group s % G (G groups, NS a multiple of G), so each stage's uses are
+//    ordered by one lane and one group -- which the parity waits need: a
+//    wait for use u of a stage must never start before use u - 1 completed.
+//  * staged_long -- rows up to about 32K floats: a whole row is staged as up
+//    to four sub-tiles that stay resident while the next row's sub-tiles
+//    stream in; pass 1 takes the row max, pass 2 the sum of exp(x - max),
+//    pass 3 normalises from shared memory and releases the stages.
+//
+// Every wait is bounded (1 s, %globaltimer).  On timeout a kernel sets the
+// device error word, makes the rest of its CTA stop, waits (bounded) for the
+// copies it has in flight and returns; rrs_device_error() reports it.
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "device_common.cuh"
+#include "internal.h"
+#include "launch_util.h"
+#include "sm100_async.cuh"
+
+namespace rrs {
+
+// Set by kernels that gave up a bounded wait; read by rrs_device_error().
+__device__ unsigned int g_device_error = 0;
+
+namespace {
+
+constexpr int kConsumerWarps = 16;
+constexpr int kConsumers = 32 * kConsumerWarps;
+constexpr int kThreads = kConsumers + 32;  // + the producer warp
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kConsumerBar = 1;            // named barrier of the consumer threads
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+constexpr unsigned kErrTimeout = 1u;
+constexpr unsigned kErrConfig = 2u;        // a launch whose stage count breaks the ring's rules
+
+// Dynamic shared memory layout: a fixed header, then the NS stages.
+constexpr int kMaxStages = 64;
+constexpr int kFullOff = 0;                        // uint64_t[kMaxStages]
+constexpr int kEmptyOff = kFullOff + 8 * kMaxStages;
+constexpr int kAbortOff = kEmptyOff + 8 * kMaxStages;  // int
+constexpr int kFailOff = kAbortOff + 16;               // int
+constexpr int kRedMOff = kFailOff + 16;                // float[32]
+constexpr int kRedSOff = kRedMOff + 128;               // float[32]
+constexpr int kWholeOff = kRedSOff + 128;              // MaxSum
+constexpr int kHeaderBytes = 2048;
+static_assert(kWholeOff + 16 <= kHeaderBytes, "header overflow");
+
+// Bounded wait on an mbarrier phase.  False on timeout (error word and the
+// CTA's abort flag set) or if another thread of the CTA already aborted.
+__device__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  uint32_t n = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++n & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        atomicOr(&g_device_error, kErrTimeout);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
+// After an abort: wait (bounded, one deadline) for the last copies the
+// producer issued, so none lands in shared memory after the CTA exits.
+__device__ void drain_copies(uint64_t* full, int64_t issued, int NS) {
+  const uint64_t t0 = global_timer_ns();
+  const int64_t first = issued > NS ? issued - NS : 0;
+  for (int64_t q = first; q < issued; ++q) {
+    const int s = (int)(q % NS);
+    const uint32_t parity = (uint32_t)((q / NS) & 1);
+    while (!mbar_try_wait(&full[s], parity)) {
+      if (global_timer_ns() - t0 > kWaitLimitNs) return;
+    }
+  }
+}
+
+__device__ __forceinline__ void init_barriers(unsigned char* smem, int NS, uint32_t empty_count) {
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kFullOff);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + kEmptyOff);
+  for (int s = 0; s < NS; ++s) {
+    mbar_init(&full[s], 1);
+    mbar_init(&empty[s], empty_count);
+  }
+  *reinterpret_cast<volatile int*>(smem + kAbortOff) = 0;
+  *reinterpret_cast<volatile int*>(smem + kFailOff) = 0;
+  fence_mbar_init();
+}
+
+template <int GW>
+__device__ __forceinline__ float group_max(float v, float* red, int g, int gw, int lane) {
+  v = warp_max(v);
+  if constexpr (GW == 1) {
+    return v;
+  } else {
+    if (lane == 0) red[g * GW + gw] = v;
+    named_barrier(1 + g, 32 * GW);
+    return warp_max((lane < GW) ? red[g * GW + lane] : neg_inf());
+  }
+}
+
+template <int GW>
+__device__ __forceinline__ float group_sum(float v, float* red, int g, int gw, int lane) {
+  v = warp_sum(v);
+  if constexpr (GW == 1) {
+    return v;
+  } else {
+    if (lane == 0) red[g * GW + gw] = v;
+    named_barrier(1 + g, 32 * GW);
+    return warp_sum((lane < GW) ? red[g * GW + lane] : 0.f);
+  }
+}
+
+// ------------------------------------------------------------ staged_rows ---
+// Rows b, b + G, b + 2G, ... of CTA b (G = gridDim.x); local row j sits in
+// stage j % NS, is issued by producer lane j % kGroups and consumed by warp
+// group j % kGroups (NS % kGroups == 0).  Needs N % 4 == 0, 16-byte aligned
+// x and y, ld % 4 == 0, N <= 32 * GW * VEC * 4.
+template <int VEC, int GW>
+__global__ void __launch_bounds__(kThreads, 1)
+softmax_staged_rows_kernel(const float* __restrict__ x, float* __restrict__ y, int64_t M,
+                           int32_t N, int64_t ld, int32_t NS, int32_t stage_stride) {
+  constexpr int kGroups = kConsumerWarps / GW;
+  constexpr int kGT = 32 * GW;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kFullOff);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + kEmptyOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortOff);
+  float* red_m = reinterpret_cast<float*>(smem + kRedMOff);
+  float* red_s = reinterpret_cast<float*>(smem + kRedSOff);
+  unsigned char* stages = smem + kHeaderBytes;
+
+  if (NS < kGroups || NS > kMaxStages || NS % kGroups != 0) {  // uniform: every thread returns
+    if (threadIdx.x == 0) atomicOr(&g_device_error, kErrConfig);
+    return;
+  }
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) init_barriers(smem, NS, GW);
+  __syncthreads();
+  pdl_entry();
+
+  const int64_t G = gridDim.x;
+  const int64_t b = blockIdx.x;
+  const int64_t my_rows = (M > b) ? (M - b + G - 1) / G : 0;
+  const uint32_t row_bytes = (uint32_t)N * 4u;
+
+  if (warp == kProducerWarp) {
+    if (lane < kGroups) {
+      const uint64_t pol = l2_evict_first_policy();
+      int64_t j = lane;
+      bool ok = true;
+      for (; j < my_rows; j += kGroups) {
+        const int s = (int)(j % NS);
+        if (j >= NS && !wait_bounded(&empty[s], (uint32_t)(((j / NS) - 1) & 1), abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], row_bytes);
+        bulk_load(stages + (size_t)s * stage_stride, x + (b + j * G) * ld, row_bytes, &full[s], pol);
+      }
+      if (!ok) drain_copies(full, j, NS);
+    }
+    return;
+  }
+
+  const int g = warp / GW;
+  const int gw = warp % GW;
+  const int gt = gw * 32 + lane;
+  const int n4 = N >> 2;
+  const float kNeg = neg_inf();
+
+  for (int64_t j = g; j < my_rows; j += kGroups) {
+    const int s = (int)(j % NS);
+    bool ok = wait_bounded(&full[s], (uint32_t)((j / NS) & 1), abort_flag);
+    if constexpr (GW > 1) ok = !barrier_or(1 + g, kGT, !ok);  // one decision per group
+    if (!ok) break;
+
+    const float4* sm = reinterpret_cast<const float4*>(stages + (size_t)s * stage_stride);
+    float4 v[VEC];
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+      const int c = i * kGT + gt;
+      v[i] = (c < n4) ? sm[c] : make_float4(kNeg, kNeg, kNeg, kNeg);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);  // the row is in registers: stage free
+
+    float m = kNeg;
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) m = max_nan(m, max4(v[i]));
+    m = group_max<GW>(m, red_m, g, gw, lane);
+
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+      v[i].x = exp_shifted(v[i].x, m);
+      v[i].y = exp_shifted(v[i].y, m);
+      v[i].z = exp_shifted(v[i].z, m);
+      v[i].w = exp_shifted(v[i].w, m);
+      sum += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+    }
+    sum = group_sum<GW>(sum, red_s, g, gw, lane);
+    const float inv = 1.0f / sum;
+
+    float4* yr4 = reinterpret_cast<float4*>(y + (b + j * G) * ld);
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+      const int c = i * kGT + gt;
+      if (c < n4) {
+        store_stream(yr4 + c, make_float4(v[i].x * inv, v[i].y * inv, v[i].z * inv, v[i].w * inv));
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------ staged_long ---
+__device__ __forceinline__ float consumer_max(float v, float* red, int warp, int lane) {
+  v = warp_max(v);
+  if (lane == 0) red[warp] = v;
+  named_barrier(kConsumerBar, kConsumers);
+  const float r = warp_max((lane < kConsumerWarps) ? red[lane] : neg_inf());
+  named_barrier(kConsumerBar, kConsumers);  // `red` is rewritten by the next reduction
+  return r;
+}
+
+__device__ __forceinline__ float consumer_sum(float v, float* red, int warp, int lane) {
+  v = warp_sum(v);
+  if (lane == 0) red[warp] = v;
+  named_barrier(kConsumerBar, kConsumers);
+  const float r = warp_sum((lane < kConsumerWarps) ? red[lane] : 0.f);
+  named_barrier(kConsumerBar, kConsumers);
+  return r;
+}
+
+constexpr int kLongUnroll = 4;
+
+// CTA b takes rows b, b + G, b + 2G, ... (G = gridDim.x); each row is staged
+// as n_sub <= 4 sub-tiles of tile_floats (the last may be shorter).  Every
+// consumer thread goes through every row in order, so each stage's uses are
+// ordered by the same threads.
+__global__ void __launch_bounds__(kThreads, 1)
+softmax_staged_long_kernel(const float* __restrict__ x, float* __restrict__ y, int64_t M,
+                           int64_t N, int64_t ld, int32_t tile_floats, int32_t NS) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kFullOff);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + kEmptyOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortOff);
+  float* red = reinterpret_cast<float*>(smem + kRedMOff);
+  unsigned char* stages = smem + kHeaderBytes;
+  const size_t stage_bytes = (size_t)tile_floats * 4;
+
+  const int64_t G = gridDim.x;
+  const int64_t b = blockIdx.x;
+  const int n_sub = (int)((N + tile_floats - 1) / tile_floats);
+  const int64_t items = (M > b) ? (M - b + G - 1) / G : 0;
+  if (NS > kMaxStages || n_sub > NS || N <= 0) {  // uniform: every thread returns
+    if (threadIdx.x == 0) atomicOr(&g_device_error, kErrConfig);
+    return;
+  }
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) init_barriers(smem, NS, kConsumerWarps);
+  __syncthreads();
+  pdl_entry();
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      int64_t q = 0;
+      bool ok = true;
+      for (int64_t k = 0; k < items && ok; ++k) {
+        const float* src = x + (b + k * G) * ld;
+        for (int t = 0; t < n_sub; ++t, ++q) {
+          const int s = (int)(q % NS);
+          if (q >= NS && !wait_bounded(&empty[s], (uint32_t)(((q / NS) - 1) & 1), abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int64_t t0 = (int64_t)t * tile_floats;
+          const uint32_t bytes = (uint32_t)(min((int64_t)tile_floats, N - t0) * 4);
+          mbar_arrive_expect_tx(&full[s], bytes);
+          bulk_load(stages + (size_t)s * stage_bytes, src + t0, bytes, &full[s], pol);
+        }
+      }
+      if (!ok) drain_copies(full, q, NS);
+    }
+    return;
+  }
+
+  const int tid = threadIdx.x;  // 0 .. kConsumers-1
+  const float kNeg = neg_inf();
+  int64_t q = 0;
+  for (int64_t k = 0; k < items; ++k, q += n_sub) {
+    const int64_t row = b + k * G;
+
+    // pass 1: row max (each sub-tile as it lands)
+    float m = kNeg;
+    bool ok = true;
+    for (int t = 0; t < n_sub; ++t) {
+      const int s = (int)((q + t) % NS);
+      ok = wait_bounded(&full[s], (uint32_t)(((q + t) / NS) & 1), abort_flag);
+      ok = !barrier_or(kConsumerBar, kConsumers, !ok);
+      if (!ok) break;
+      const float4* sm = reinterpret_cast<const float4*>(stages + (size_t)s * stage_bytes);
+      const int nf4 = (int)(min((int64_t)tile_floats, N - (int64_t)t * tile_floats) >> 2);
+      for (int i = tid; i < nf4; i += kConsumers * kLongUnroll) {
+#pragma unroll
+        for (int u = 0; u < kLongUnroll; ++u) {
+          const int idx = i + u * kConsumers;
+          if (idx < nf4) m = max_nan(m, max4(sm[idx]));
+        }
+      }
+    }
+    if (!ok) break;
+    m = consumer_max(m, red, warp, lane);
+
+    // pass 2: sum of exp(x - m) (an all -inf row gives m = -inf, sum 0, y NaN)
+    float sum = 0.f;
+    if (m != kNeg) {
+      for (int t = 0; t < n_sub; ++t) {
+        const int s = (int)((q + t) % NS);
+        const float4* sm = reinterpret_cast<const float4*>(stages + (size_t)s * stage_bytes);
+        const int nf4 = (int)(min((int64_t)tile_floats, N - (int64_t)t * tile_floats) >> 2);
+        for (int i = tid; i < nf4; i += kConsumers * kLongUnroll) {
+#pragma unroll
+          for (int u = 0; u < kLongUnroll; ++u) {
+            const int idx = i + u * kConsumers;
+            if (idx < nf4) {
+              const float4 a = sm[idx];
+              sum += (exp_shifted(a.x, m) + exp_shifted(a.y, m)) +
+                     (exp_shifted(a.z, m) + exp_shifted(a.w, m));
+            }
+          }
+        }
+      }
+    }
+    sum = consumer_sum(sum, red, warp, lane);
+
+    // pass 3: normalise from shared memory, store, release each sub-tile
+    const float inv = 1.0f / sum;
+    float* yr = y + row * ld;
+    for (int t = 0; t < n_sub; ++t) {
+      const int s = (int)((q + t) % NS);
+      const float4* sm = reinterpret_cast<const float4*>(stages + (size_t)s * stage_bytes);
+      float4* y4 = reinterpret_cast<float4*>(yr + (int64_t)t * tile_floats);
+      const int nf4 = (int)(min((int64_t)tile_floats, N - (int64_t)t * tile_floats) >> 2);
+      for (int i = tid; i < nf4; i += kConsumers * kLongUnroll) {
+#pragma unroll
+        for (int u = 0; u < kLongUnroll; ++u) {
+          const int idx = i + u * kConsumers;
+          if (idx < nf4) {
+            const float4 a = sm[idx];
+            store_stream(y4 + idx, make_float4(exp_shifted(a.x, m) * inv,
+                                               exp_shifted(a.y, m) * inv,
+                                               exp_shifted(a.z, m) * inv,
+                                               exp_shifted(a.w, m) * inv));
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------- launch ---
+std::mutex g_attr_mu;
+std::set<std::pair<const void*, int>> g_attr_done;
+
+cudaError_t allow_dynamic_smem(const void* kernel) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  if (g_attr_done.count({kernel, dev})) return cudaSuccess;
+  int optin = 0;
+  e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  if (e == cudaSuccess) g_attr_done.insert({kernel, dev});
+  return e;
+}
+
+template <int VEC, int GW>
+cudaError_t launch_rows_vg(const rrs_plan& p, const float* x, float* y, int64_t M, int64_t N,
+                           int64_t ld, cudaStream_t s) {
+  auto kern = softmax_staged_rows_kernel<VEC, GW>;
+  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern));
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kern, dim3((unsigned)p.grid), dim3(kThreads), (size_t)p.smem_bytes, s, 0, x, y,
+                    M, (int32_t)N, ld, p.stages, p.tile * 4);
+}
+
+}  // namespace
+
+int staged_header_bytes() { return kHeaderBytes; }
+int staged_max_stages() { return kMaxStages; }
+int staged_threads() { return kThreads; }
+int staged_consumer_warps() { return kConsumerWarps; }
+
+cudaError_t launch_softmax_staged_rows(const rrs_plan& p, const float* x, float* y, int64_t M,
+                                       int64_t N, int64_t ld, cudaStream_t s) {
+  if (p.threads != kThreads) return cudaErrorInvalidConfiguration;
+  const int gw = p.warps_per_row, vec = p.vec;
+#define RRS_SR(V, G) \
+  if (vec == V && gw == G) return launch_rows_vg<V, G>(p, x, y, M, N, ld, s);
+  RRS_SR(1, 1)
+  RRS_SR(2, 1)
+  RRS_SR(4, 1)
+  RRS_SR(8, 1)
+  RRS_SR(16, 1)
+  RRS_SR(8, 2)
+  RRS_SR(8, 4)
+  RRS_SR(8, 8)
+#undef RRS_SR
+  return cudaErrorInvalidConfiguration;
+}
+
+cudaError_t launch_softmax_staged_long(const rrs_plan& p, const float* x, float* y, int64_t M,
+                                       int64_t N, int64_t ld, cudaStream_t s) {
+  if (p.threads != kThreads) return cudaErrorInvalidConfiguration;
+  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(softmax_staged_long_kernel));
+  if (e != cudaSuccess) return e;
+  return launch_pdl(softmax_staged_long_kernel, dim3((unsigned)p.grid), dim3(kThreads),
+                    (size_t)p.smem_bytes, s, 0, x, y, M, N, ld, p.tile, p.stages);
+}
+
+cudaError_t read_and_clear_staged_error(cudaStream_t s, unsigned* value) {
+  unsigned host = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&host, g_device_error, sizeof(host), 0,
+                                            cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && host != 0) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbolAsync(g_device_error, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  }
+  *value = host;
+  return e;
+}
+
+}  // namespace rrs

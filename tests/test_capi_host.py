@@ -76,7 +76,8 @@ def plan(M, N, ld=None, vector_ok=True, sms=152):
 
 
 def test_planner_on_the_five_workloads(lib):
-    assert plan(128, 256)["path_name"] == "row_regs"
+    p1 = plan(128, 256)
+    assert p1["path_name"] == "row_regs" and p1["warps_per_row"] == 1 and p1["vec"] == 2
     p2 = plan(8192, 1024)
     assert p2["path_name"] == "row_regs" and p2["warps_per_row"] == 1 and p2["vec"] == 8
     p3 = plan(4096, 32768)
@@ -84,7 +85,19 @@ def test_planner_on_the_five_workloads(lib):
     p4 = plan(16384, 4096)
     assert p4["path_name"] == "row_regs" and p4["warps_per_row"] == 4
     p5 = plan(32, 1 << 20)
-    assert p5["path_name"] in ("two_phase", "grid")
+    assert p5["path_name"] == "two_phase"
+
+
+def test_grid_plan_for_the_longest_rows(lib):
+    import row_reduction_softmax_gb300 as rrs
+    try:
+        rrs.force_path("grid")
+        p5 = plan(32, 1 << 20)
+        assert p5["path_name"] == "grid" and p5["threads"] == 512
+        # 152 segments of 6900 floats per row, 2 rows per round over all 304 CTAs
+        assert (p5["ctas_per_row"], p5["rows_per_cta"], p5["grid"], p5["rounds"]) == (152, 2, 304, 16)
+    finally:
+        rrs.force_path("auto", "auto")
 
 
 def test_planner_unaligned_takes_scalar_path(lib):
@@ -114,6 +127,22 @@ def test_planner_covers_every_column(lib, M, N):
         C, chunk = p["ctas_per_row"], p["chunk"]
         assert chunk % 1024 == 0 and C * chunk >= N > (C - 1) * chunk
         assert p["workspace_bytes"] == M * C * 8
+    elif p["path_name"] == "row_staged":
+        assert N % 4 == 0 and p["threads"] == 544 and p["grid"] == min(M, 152)
+        assert p["smem_bytes"] == 2048 + p["stages"] * p["tile"] * 4 <= 232448
+        if p["vec"] > 0:                                    # whole rows in registers
+            assert p["vec"] * 32 * p["warps_per_row"] * 4 >= N and p["tile"] >= N
+            groups = 16 // p["warps_per_row"]
+            assert p["stages"] % groups == 0 and groups <= p["stages"] <= 64
+        else:                                               # a row staged as <= 4 sub-tiles
+            assert p["tile"] % 4 == 0 and -(-N // p["tile"]) <= 4 < p["stages"]
+    elif p["path_name"] == "grid":
+        C, seg = p["ctas_per_row"], p["chunk"]
+        assert N % 4 == 0 and seg % 4 == 0 and C * seg >= N > (C - 1) * seg
+        R = p["rows_per_cta"]
+        assert p["threads"] == 512 and p["grid"] == R * C <= 2 * 152 and R <= M
+        assert -(-seg // 4) <= 512 * p["vec"] and p["vec"] in (2, 4)
+        assert p["rounds"] == -(-M // R) and p["workspace_bytes"] == M * C * 16
 
 
 def test_forced_paths(lib):
@@ -123,6 +152,13 @@ def test_forced_paths(lib):
         assert plan(64, 1024)["path_name"] == "cluster"
         rrs.force_path("two_phase")
         assert plan(64, 1024)["path_name"] == "two_phase"
+        rrs.force_path("grid")
+        assert plan(64, 1024)["path_name"] == "grid"
+        rrs.force_path("row_staged")
+        assert plan(64, 30000)["path_name"] == "row_staged"
+        assert plan(64, 1024)["path_name"] == "row_staged"
+        with pytest.raises(rrs.RRSError):
+            plan(64, 1022)                                  # N % 4 != 0
         rrs.force_path("row_regs")
         with pytest.raises(rrs.RRSError) as e:
             plan(4, 65536)

@@ -17,7 +17,7 @@ from gpu_helpers import Guarded, check_softmax
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-PATHS = ["row_regs", "cluster", "two_phase"]
+PATHS = ["row_regs", "cluster", "two_phase", "row_staged", "grid"]
 
 SHAPES = [(1, 1), (3, 2), (5, 3), (7, 5), (4, 31), (9, 33), (16, 128), (17, 129), (128, 256),
           (33, 1000), (8, 1024), (5, 2047), (3, 2049), (6, 4097), (4, 8191), (2, 16385),
@@ -31,6 +31,10 @@ def supports(path: str, N: int, ld: int) -> bool:
         return vector_ok and N <= 32768
     if path == "cluster":
         return vector_ok and N <= 131072
+    if path == "row_staged":
+        return vector_ok and N % 4 == 0 and N <= 32912
+    if path == "grid":
+        return vector_ok and N % 4 == 0
     return True
 
 
@@ -120,7 +124,7 @@ def test_special_values(path, N):
 
 @pytest.mark.parametrize("path", PATHS)
 def test_shift_invariance_on_gpu(path):
-    N = 4096 if path != "cluster" else 40000
+    N = 40000 if path in ("cluster", "grid") else 4096
     # values on a 2^-8 grid, so x + 1000 is exact in fp32 and the shift is a true shift
     x = np.round(recipe("c2", 16, N) * 256.0).astype(np.float32) / np.float32(256.0)
     xs = x + np.float32(1000.0)
@@ -133,7 +137,7 @@ def test_shift_invariance_on_gpu(path):
 
 @pytest.mark.parametrize("path", PATHS)
 def test_bitwise_deterministic(path):
-    N = 2052 if path != "cluster" else 50000
+    N = 50000 if path in ("cluster", "grid") else 2052
     x = recipe("c3", 32, N)
     a, _ = run(x, N, N, path)
     b, _ = run(x, N, N, path)
@@ -216,3 +220,4 @@ def test_full_size_workload(name):
         assert int(spikes.sum()) == w.M * 205
     del x, y
     torch.cuda.empty_cache()
+
