@@ -156,6 +156,15 @@ RRS_API int rrs_release_workspace(void);
  * RRS_ERR_UNSUPPORTED.  Returns RRS_OK or RRS_ERR_INVALID_ARG. */
 RRS_API int rrs_force_path(int softmax_path, int sum_path);
 
+/* Fault injection for failure-detection tests (no counterpart in the
+ * paper).  kind 1: in later GRID launches, CTA 0 never publishes the
+ * partial of its first row segment, so that row's bounded waits run out
+ * (about 1 s); the kernel returns early, rrs_device_error() then reports
+ * RRS_ERR_TIMEOUT, the output of that call is incomplete, and the CUDA
+ * context stays usable.  kind 0 turns injection off.  Nothing here faults
+ * or hangs the GPU.  Returns RRS_OK or RRS_ERR_INVALID_ARG. */
+RRS_API int rrs_inject_fault(int kind);
+
 /* The planner, as pure host logic: the plan softmax_rows / row_sum would use
  * for this shape on a device with `sm_count` SMs and `smem_optin` bytes of
  * opt-in shared memory per CTA.  `vector_ok` says whether x and y are

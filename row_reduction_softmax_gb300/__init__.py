@@ -72,6 +72,7 @@ _SIGNATURES = {
     "rrs_last_error": (ctypes.c_char_p, []),
     "rrs_release_workspace": (ctypes.c_int, []),
     "rrs_force_path": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
+    "rrs_inject_fault": (ctypes.c_int, [ctypes.c_int]),
     "rrs_plan_softmax": (ctypes.c_int, [_I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                         ctypes.POINTER(Plan)]),
     "rrs_plan_row_sum": (ctypes.c_int, [_I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int,

@@ -27,6 +27,7 @@ namespace {
 thread_local std::string g_last_error;
 std::atomic<int> g_force_softmax{RRS_PATH_AUTO};
 std::atomic<int> g_force_sum{RRS_SUM_AUTO};
+std::atomic<int> g_fault{0};
 
 int fail(int status, const std::string& msg) {
   g_last_error = msg;
@@ -65,7 +66,6 @@ int device_info(int dev, DeviceInfo* out) {
   if (e == cudaSuccess)
     e = cudaDeviceGetAttribute(&d.coop_launch, cudaDevAttrCooperativeLaunch, dev);
   if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
-  d.grid_per_sm = grid_blocks_per_sm();
   g_devices[dev] = d;
   *out = d;
   return RRS_OK;
@@ -220,7 +220,8 @@ int64_t staged_tile_max(int smem_optin) { return (staged_budget(smem_optin) / 7)
 constexpr int64_t kStagedRowsMaxN = 8192;
 constexpr int64_t kRowRegsAutoMaxN = 16384;
 constexpr double kPerSmBytesPerSec = 6.7e12 / 152.0;  // planning model only
-constexpr double kRoundSec = 0.3e-6;                   // per-round fixed cost (planning model)
+constexpr double kItemSec = 1.5e-6;                    // per-segment fixed cost (planning model)
+constexpr int64_t kGridMaxSegments = 160;              // slots one exchange warp polls
 
 bool plan_staged_rows(int64_t M, int64_t N, int sm_count, int smem_optin, rrs_plan* p) {
   if (N % 4 != 0 || N > kStagedRowsMaxN) return false;
@@ -280,49 +281,54 @@ bool plan_staged_long(int64_t M, int64_t N, int sm_count, int smem_optin, rrs_pl
   return true;
 }
 
-// GRID: C segments per row of at most kGridThreads * kGridMaxVec float4
-// each, R rows per round, R * C <= G = SMs x resident CTAs.  C is chosen to
-// minimise rounds x (per-CTA segment time + a fixed per-round cost).
-bool plan_grid(int64_t M, int64_t N, int sm_count, int per_sm, int coop_ok, rrs_plan* p) {
-  if (N % 4 != 0 || !coop_ok || per_sm < 1) return false;
-  const int64_t G = (int64_t)sm_count * per_sm;
-  const int64_t cap = (int64_t)kGridThreads * kGridMaxVec * 4;  // floats per CTA
-  const int64_t c_min = ceil_div(N, cap);
-  if (c_min > G) return false;
-  const double per_cta_bw = kPerSmBytesPerSec / (double)per_sm;
+// GRID: C segments of a row on C CTAs (one per SM), R rows per round,
+// R * C <= SMs; each segment is one shared-memory stage and the ring holds
+// at least 3 (the segment being finalised, the next one, one in flight).
+// C minimises rounds x (per-SM segment time + a fixed per-segment cost).
+bool plan_grid(int64_t M, int64_t N, int sm_count, int smem_optin, int coop_ok, rrs_plan* p) {
+  if (N % 4 != 0 || !coop_ok) return false;
+  const int64_t budget = staged_budget(smem_optin);
   double best = 1e300;
-  int64_t best_seg = 0, best_c = 0, best_r = 0;
-  for (int64_t c = c_min; c <= G; ++c) {
+  int64_t b_seg = 0, b_c = 0, b_r = 0, b_ns = 0, b_stride = 0;
+  for (int64_t c = 1; c <= sm_count; ++c) {
     const int64_t seg = round_up(ceil_div(N, c), 4);
     const int64_t C = ceil_div(N, seg);
-    int64_t R = std::min<int64_t>(G / C, M);
+    const int64_t stride = round_up(seg * 4, 128);
+    const int64_t ns = std::min<int64_t>(staged_max_stages(), budget / stride);
+    if (ns < 3) continue;
+    const int64_t R = std::min<int64_t>(sm_count / C, M);
     if (R < 1) continue;
     const double rounds = (double)ceil_div(M, R);
-    const double t = rounds * (8.0 * (double)seg / per_cta_bw + kRoundSec);
+    if (C > kGridMaxSegments) continue;
+    const double t = rounds * (8.0 * (double)seg / kPerSmBytesPerSec + kItemSec);
     if (t < best * (1.0 - 1e-9)) {
       best = t;
-      best_seg = seg;
-      best_c = C;
-      best_r = R;
+      b_seg = seg;
+      b_c = C;
+      b_r = R;
+      b_ns = ns;
+      b_stride = stride;
     }
   }
-  if (best_seg == 0) return false;
+  if (b_seg == 0) return false;
   p->path = RRS_PATH_GRID;
-  p->vec = (ceil_div(best_seg, 4) <= (int64_t)kGridThreads * 2) ? 2 : 4;
-  p->warps_per_row = kGridThreads / 32;
-  p->threads = kGridThreads;
-  p->grid = best_r * best_c;
-  p->rows_per_cta = (int32_t)best_r;
-  p->ctas_per_row = best_c;
-  p->chunk = best_seg;
-  p->rounds = ceil_div(M, best_r);
-  p->workspace_bytes = M * best_c * 16;
+  p->vec = 0;
+  p->warps_per_row = staged_consumer_warps();
+  p->threads = staged_threads();
+  p->grid = b_r * b_c;
+  p->rows_per_cta = (int32_t)b_r;
+  p->ctas_per_row = b_c;
+  p->chunk = b_seg;
+  p->rounds = ceil_div(M, b_r);
+  p->stages = (int32_t)b_ns;
+  p->tile = (int32_t)(b_stride / 4);
+  p->smem_bytes = (int32_t)(staged_header_bytes() + b_ns * b_stride);
+  p->workspace_bytes = M * b_c * 16;
   return true;
 }
 
 int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_count,
-                      int smem_optin, int cluster_ok, int coop_ok, int grid_per_sm, int forced,
-                      rrs_plan* p) {
+                      int smem_optin, int cluster_ok, int coop_ok, int forced, rrs_plan* p) {
   std::memset(p, 0, sizeof(*p));
   if (M < 0 || N < 0 || ld < 1 || ld < N || sm_count < 1)
     return fail(RRS_ERR_INVALID_ARG, "bad shape or device description");
@@ -334,7 +340,8 @@ int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_co
   }
   if (forced == RRS_PATH_AUTO) {
     // Measured on GB300: registers win for rows that fit one CTA, the cluster
-    // split for rows up to 16 CTAs' registers, the two-phase split beyond.
+    // split for rows up to 16 CTAs' registers, the staged grid split beyond,
+    // the two-phase split for what the grid cannot hold or align.
     rrs_plan c;
     if (!vector_ok) {
       plan_two_phase(M, N, sm_count, p);
@@ -345,6 +352,7 @@ int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_co
       plan_row_regs(M, N, sm_count, p);
     } else if (cluster_ok && plan_cluster(M, N, &c)) {
       *p = c;
+    } else if (plan_grid(M, N, sm_count, smem_optin, coop_ok, p)) {
     } else {
       plan_two_phase(M, N, sm_count, p);
     }
@@ -363,7 +371,7 @@ int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_co
       }
       return fail(RRS_ERR_UNSUPPORTED, "ROW_STAGED needs 16-byte alignment, N % 4 == 0, N <= 32912");
     case RRS_PATH_GRID:
-      if (vector_ok && plan_grid(M, N, sm_count, grid_per_sm, coop_ok, p)) {
+      if (vector_ok && plan_grid(M, N, sm_count, smem_optin, coop_ok, p)) {
         p->cluster = 1;
         p->vector_io = 1;
         return RRS_OK;
@@ -465,10 +473,16 @@ RRS_API int rrs_force_path(int softmax_path, int sum_path) {
   return RRS_OK;
 }
 
+RRS_API int rrs_inject_fault(int kind) {
+  if (kind < 0 || kind > 1) return RRS_ERR_INVALID_ARG;
+  g_fault.store(kind);
+  return RRS_OK;
+}
+
 RRS_API int rrs_plan_softmax(int64_t M, int64_t N, int64_t ld, int vector_ok_flag, int sm_count,
                              int smem_optin, rrs_plan* plan) {
   if (!plan) return RRS_ERR_INVALID_ARG;
-  return plan_softmax_impl(M, N, ld, vector_ok_flag, sm_count, smem_optin, 1, 1, kDefaultGridPerSm,
+  return plan_softmax_impl(M, N, ld, vector_ok_flag, sm_count, smem_optin, 1, 1,
                            g_force_softmax.load(), plan);
 }
 
@@ -525,8 +539,7 @@ RRS_API int softmax_rows(const float* x, float* y, int64_t M, int64_t N, int64_t
 
   rrs_plan plan;
   st = plan_softmax_impl(M, N, ld, vector_ok(x, y, ld) ? 1 : 0, info.sm_count, info.smem_optin,
-                         info.cluster_launch, info.coop_launch, info.grid_per_sm,
-                         g_force_softmax.load(), &plan);
+                         info.cluster_launch, info.coop_launch, g_force_softmax.load(), &plan);
   if (st != RRS_OK) return st;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -546,7 +559,7 @@ RRS_API int softmax_rows(const float* x, float* y, int64_t M, int64_t N, int64_t
       uint32_t ticket = 0;
       if ((st = get_workspace(dev, s, kWsGrid, (size_t)plan.workspace_bytes, &ws, &ticket)) != RRS_OK)
         return st;
-      e = launch_softmax_grid(plan, x, y, M, N, ld, ws, ticket, s);
+      e = launch_softmax_staged_grid(plan, x, y, M, N, ld, ws, ticket, g_fault.load(), s);
       break;
     }
     case RRS_PATH_TWO_PHASE: {
@@ -611,11 +624,9 @@ RRS_API int row_sum(const float* x, float* out, int64_t M, int64_t N, int64_t ld
 }
 
 RRS_API int rrs_device_error(void* stream) {
-  unsigned a = 0, b = 0;
-  cudaError_t e = read_and_clear_staged_error(static_cast<cudaStream_t>(stream), &a);
-  if (e == cudaSuccess) e = read_and_clear_grid_error(static_cast<cudaStream_t>(stream), &b);
+  unsigned v = 0;
+  cudaError_t e = read_and_clear_staged_error(static_cast<cudaStream_t>(stream), &v);
   if (e != cudaSuccess) return fail_cuda(e, "rrs_device_error");
-  const unsigned v = a | b;
   return v ? fail(RRS_ERR_TIMEOUT, "a split-row kernel stopped waiting for its peers") : RRS_OK;
 }
 

@@ -15,11 +15,7 @@ struct DeviceInfo {
   int smem_optin = 0;       // max dynamic shared memory per CTA (opt-in), bytes
   int cluster_launch = 0;   // thread-block clusters supported
   int coop_launch = 0;      // cooperative launch supported
-  int grid_per_sm = 0;      // resident CTAs per SM of the GRID kernel
 };
-
-// Planner default for a GB300 when no device is queried (rrs_plan_softmax).
-constexpr int kDefaultGridPerSm = 2;
 
 // Tuning limits shared by the planner and the launchers.
 constexpr int kRowRegsMaxVec = 16;       // float4 registers per thread (warp-per-row)
@@ -27,8 +23,7 @@ constexpr int kSplitThreads = 256;       // CTA size of the cluster / two-phase 
 constexpr int kClusterVec = 8;           // float4 per thread in a cluster CTA segment
 constexpr int kClusterMax = 16;          // largest cluster (non-portable beyond 8)
 constexpr int64_t kChunkAlign = 1024;    // two-phase chunk granularity (elements)
-constexpr int kGridThreads = 512;        // CTA size of the GRID kernel
-constexpr int kGridMaxVec = 4;           // float4 registers per thread per segment (GRID)
+
 
 // ---- softmax launchers (return the launch's cudaError_t) ----
 cudaError_t launch_softmax_row_regs(const rrs_plan& p, const float* x, float* y, int64_t M,
@@ -49,13 +44,14 @@ cudaError_t launch_softmax_staged_rows(const rrs_plan& p, const float* x, float*
                                        int64_t N, int64_t ld, cudaStream_t s);
 cudaError_t launch_softmax_staged_long(const rrs_plan& p, const float* x, float* y, int64_t M,
                                        int64_t N, int64_t ld, cudaStream_t s);
-
-// GRID plans (softmax_grid.cu): rows split over a cooperative persistent
-// grid of R * C CTAs; `workspace` holds 16 bytes per (row, segment) slot,
-// zero-filled when allocated, and `ticket` is unique per launch on it.
-cudaError_t launch_softmax_grid(const rrs_plan& p, const float* x, float* y, int64_t M, int64_t N,
-                                int64_t ld, void* workspace, uint32_t ticket, cudaStream_t s);
-int grid_blocks_per_sm();
+// GRID plans: rows split over a cooperative grid of R * C CTAs (one per SM);
+// `workspace` holds 16 bytes per (row, segment) slot, zero-filled when
+// allocated, and `ticket` is unique per launch on that workspace.
+// `fault` != 0 (testing only, rrs_inject_fault): CTA 0 never publishes the
+// partial of its first segment, so its row's waits run out.
+cudaError_t launch_softmax_staged_grid(const rrs_plan& p, const float* x, float* y, int64_t M,
+                                       int64_t N, int64_t ld, void* workspace, uint32_t ticket,
+                                       int fault, cudaStream_t s);
 
 // ---- row-sum launchers ----
 cudaError_t launch_row_sum_rows(const rrs_plan& p, const float* x, float* out, int64_t M,
@@ -65,6 +61,5 @@ cudaError_t launch_row_sum_split(const rrs_plan& p, const float* x, float* out, 
 
 // ---- device error words (set by kernels whose bounded waits ran out) ----
 cudaError_t read_and_clear_staged_error(cudaStream_t s, unsigned* value);
-cudaError_t read_and_clear_grid_error(cudaStream_t s, unsigned* value);
 
 }  // namespace rrs

@@ -82,6 +82,18 @@ __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
   return v;
 }
 
+// 64-bit relaxed accesses: naturally aligned, single-copy atomic, so a value
+// packed with a tag in one word is seen whole or not at all.
+__device__ __forceinline__ uint64_t ld_relaxed_gpu_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed_gpu_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 // Acquire side of a release store observed through relaxed loads.
 __device__ __forceinline__ void fence_acquire_gpu() {
   asm volatile("fence.acq_rel.gpu;" ::: "memory");

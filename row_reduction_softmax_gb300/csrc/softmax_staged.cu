@@ -27,6 +27,11 @@
 //    to four sub-tiles that stay resident while the next row's sub-tiles
 //    stream in; pass 1 takes the row max, pass 2 the sum of exp(x - max),
 //    pass 3 normalises from shared memory and releases the stages.
+//  * staged_grid -- rows longer than a cluster's registers: each row is cut
+//    into C segments held by C co-resident CTAs; a segment's (max, sum)
+//    partial goes to a ticketed global slot, and each CTA publishes the next
+//    row's partial before it waits for the current row's C partials, so the
+//    exchange overlaps useful work while the ring keeps prefetching.
 //
 // Every wait is bounded (1 s, %globaltimer).  On timeout a kernel sets the
 // device error word, makes the rest of its CTA stop, waits (bounded) for the
@@ -260,6 +265,7 @@ __device__ __forceinline__ float consumer_sum(float v, float* red, int warp, int
 }
 
 constexpr int kLongUnroll = 4;
+constexpr int kGridBatch = 8;  // float4 per thread folded at once in a grid partial
 
 // CTA b takes rows b, b + G, b + 2G, ... (G = gridDim.x); each row is staged
 // as n_sub <= 4 sub-tiles of tile_floats (the last may be shorter).  Every
@@ -391,6 +397,207 @@ softmax_staged_long_kernel(const float* __restrict__ x, float* __restrict__ y, i
   }
 }
 
+// ------------------------------------------------------------ staged_grid ---
+// Rows too long for a cluster: CTA g of a cooperative grid of R * C CTAs (one
+// per SM) always holds segment c = g % C of rows g / C + k * R, k = 0, 1, ...
+// Item k (one row segment of seg floats) is one ring stage, prefetched by the
+// producer as far ahead as the ring allows.
+//
+// A segment's partial (m_c, s_c) goes to global slot [row, c] as two 64-bit
+// words, (ticket << 32 | bits(m_c)) and (ticket << 32 | bits(s_c)), written
+// and read with relaxed 64-bit accesses: each word is single-copy atomic, so
+// a reader that sees this launch's ticket in a word has that word's value,
+// and no fence is needed on either side.
+//
+// Warps 1..15 compute partials: P(k) = wait for the stage, fold it into an
+// exact per-thread (max, sum), merge over the 15 warps, publish.  Warp 0 is
+// the exchange warp: E(k) = poll the row's C slots, merge them in slot order
+// (identically in every CTA of the row).  Partials run `lead` items ahead:
+// iteration k runs P(k + lead) on warps 1..15 while warp 0 runs E(k); then
+// all 16 warps meet, and warps 1..15 normalise the staged segment k, store y
+// and release the stage.  E(k) needs P(k) of its row's CTAs, each published
+// before that CTA's own E(k - lead); all of a row's CTAs are resident
+// (cooperative launch), so the waits end.
+__device__ __forceinline__ uint64_t pack_tagged(uint32_t ticket, float v) {
+  return ((uint64_t)ticket << 32) | (uint64_t)__float_as_uint(v);
+}
+
+constexpr int kPartialBar = 2;                     // warps 1..15
+constexpr int kMaxSlotsPerLane = 5;                // C <= 160: a row's slots over 32 lanes
+constexpr int kPartialThreads = kConsumers - 32;
+
+__global__ void __launch_bounds__(kThreads, 1)
+softmax_staged_grid_kernel(const float* __restrict__ x, float* __restrict__ y, int64_t M,
+                           int64_t N, int64_t ld, int64_t seg, int32_t C, int32_t R, int32_t NS,
+                           int32_t stage_stride, uint64_t* __restrict__ slots, uint32_t ticket,
+                           int32_t fault) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kFullOff);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + kEmptyOff);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortOff);
+  volatile int* fail_flag = reinterpret_cast<volatile int*>(smem + kFailOff);
+  MaxSum* redp = reinterpret_cast<MaxSum*>(smem + kRedMOff);  // 16 pairs
+  MaxSum* whole = reinterpret_cast<MaxSum*>(smem + kWholeOff);
+  unsigned char* stages = smem + kHeaderBytes;
+
+  const int c = (int)(blockIdx.x % C);
+  const int64_t row0 = blockIdx.x / C;
+  const int64_t seg_begin = (int64_t)c * seg;
+  const int64_t seg_n = min(seg, N - seg_begin);
+  const int64_t items = (M > row0) ? (M - row0 + R - 1) / R : 0;
+  if (NS < 3 || NS > kMaxStages || seg_n <= 0 || seg_n * 4 > stage_stride ||
+      C > 32 * kMaxSlotsPerLane) {  // uniform
+    if (threadIdx.x == 0) atomicOr(&g_device_error, kErrConfig);
+    return;
+  }
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) init_barriers(smem, NS, kConsumerWarps);
+  __syncthreads();
+  pdl_entry();
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();
+      const uint32_t bytes = (uint32_t)(seg_n * 4);
+      int64_t k = 0;
+      bool ok = true;
+      for (; k < items; ++k) {
+        const int st = (int)(k % NS);
+        if (k >= NS && !wait_bounded(&empty[st], (uint32_t)(((k / NS) - 1) & 1), abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[st], bytes);
+        bulk_load(stages + (size_t)st * stage_stride, x + (row0 + k * R) * ld + seg_begin, bytes,
+                  &full[st], pol);
+      }
+      if (!ok) drain_copies(full, k, NS);
+    }
+    return;
+  }
+
+  const int nf4 = (int)(seg_n >> 2);
+  const float kNeg = neg_inf();
+  const int ptid = threadIdx.x - 32;  // index among warps 1..15
+
+  // P(k) on warps 1..15: false if a wait ran out (the same answer in all of them).
+  auto partial = [&](int64_t k) -> bool {
+    const int st = (int)(k % NS);
+    const bool got = wait_bounded(&full[st], (uint32_t)((k / NS) & 1), abort_flag);
+    const float4* sm = reinterpret_cast<const float4*>(stages + (size_t)st * stage_stride);
+    MaxSum p{kNeg, 0.f};
+    if (got) {
+      for (int i0 = ptid; i0 < nf4; i0 += kPartialThreads * kGridBatch) {
+        float4 a[kGridBatch];
+        float bm = kNeg;
+#pragma unroll
+        for (int u = 0; u < kGridBatch; ++u) {
+          const int idx = i0 + u * kPartialThreads;
+          a[u] = (idx < nf4) ? sm[idx] : make_float4(kNeg, kNeg, kNeg, kNeg);
+          bm = max_nan(bm, max4(a[u]));
+        }
+        rescale_to(p, bm);
+        if (p.m != kNeg) {
+#pragma unroll
+          for (int u = 0; u < kGridBatch; ++u) {
+            p.s += (exp_shifted(a[u].x, p.m) + exp_shifted(a[u].y, p.m)) +
+                   (exp_shifted(a[u].z, p.m) + exp_shifted(a[u].w, p.m));
+          }
+        }
+      }
+    }
+    p = warp_merge(p);
+    if (lane == 0) redp[warp] = p;
+    if (barrier_or(kPartialBar, kPartialThreads, !got)) return false;
+    MaxSum q = (lane >= 1 && lane < kConsumerWarps) ? redp[lane] : MaxSum{kNeg, 0.f};
+    q = warp_merge(q);  // every warp merges the same pairs in the same order
+    named_barrier(kPartialBar, kPartialThreads);  // `redp` is rewritten by the next merge
+    if (ptid == 0 && !(fault != 0 && blockIdx.x == 0 && k == 0)) {
+      uint64_t* sl = slots + 2 * ((row0 + k * R) * C + c);
+      st_relaxed_gpu_u64(sl, pack_tagged(ticket, q.m));
+      st_relaxed_gpu_u64(sl + 1, pack_tagged(ticket, q.s));
+    }
+    return true;
+  };
+
+  // Partials run `lead` items ahead of the exchange: the consumers hold
+  // stages k .. k + lead, the rest of the ring is in flight.
+  const int lead = min(3, NS - 2);
+  if (warp > 0) {
+    for (int64_t k = 0; k < lead && k < items; ++k) {
+      if (!partial(k)) {  // seen by every consumer warp after the first meeting
+        if (ptid == 0) *fail_flag = 1;
+      }
+    }
+  }
+  for (int64_t k = 0; k < items; ++k) {
+    const int64_t row = row0 + k * R;
+    if (warp == 0) {
+      // E(k): poll the row's C slots (both words of each) with relaxed loads
+      const uint64_t* rs = slots + 2 * row * C;
+      const uint64_t t0 = global_timer_ns();
+      bool seen = false;
+      uint32_t n = 0;
+      MaxSum acc{kNeg, 0.f};
+      while (!*fail_flag) {
+        // all of this lane's slot words are loaded before any is used, so the
+        // poll costs one round trip to L2, not one per slot
+        uint64_t wm[kMaxSlotsPerLane], ws[kMaxSlotsPerLane];
+#pragma unroll
+        for (int j = 0; j < kMaxSlotsPerLane; ++j) {
+          const int l = lane + 32 * j;
+          wm[j] = (l < C) ? ld_relaxed_gpu_u64(rs + 2 * l) : pack_tagged(ticket, kNeg);
+          ws[j] = (l < C) ? ld_relaxed_gpu_u64(rs + 2 * l + 1) : pack_tagged(ticket, 0.f);
+        }
+        bool mine = true;
+        MaxSum a{kNeg, 0.f};
+#pragma unroll
+        for (int j = 0; j < kMaxSlotsPerLane; ++j) {
+          mine &= ((uint32_t)(wm[j] >> 32) == ticket) && ((uint32_t)(ws[j] >> 32) == ticket);
+          a = merge(a, MaxSum{__uint_as_float((uint32_t)wm[j]), __uint_as_float((uint32_t)ws[j])});
+        }
+        if (__all_sync(kFullMask, mine)) {
+          seen = true;
+          acc = a;
+          break;
+        }
+        if ((++n & 15u) == 0 && (*abort_flag || global_timer_ns() - t0 > kWaitLimitNs)) break;
+      }
+      acc = warp_merge(acc);
+      if (lane == 0) {
+        *whole = acc;
+        if (!seen) {
+          atomicOr(&g_device_error, kErrTimeout);
+          *abort_flag = 1;
+          *fail_flag = 1;
+        }
+      }
+    } else if (k + lead < items && !partial(k + lead)) {
+      if (ptid == 0) *fail_flag = 1;
+    }
+    named_barrier(kConsumerBar, kConsumers);
+    const bool failed = *fail_flag != 0;
+    const MaxSum w = *whole;
+    named_barrier(kConsumerBar, kConsumers);  // `whole` and the flag are rewritten next round
+    if (failed) return;
+
+    const int st = (int)(k % NS);
+    if (warp > 0) {
+      const float4* sm = reinterpret_cast<const float4*>(stages + (size_t)st * stage_stride);
+      float4* y4 = reinterpret_cast<float4*>(y + row * ld + seg_begin);
+      const float inv = 1.0f / w.s;
+      for (int i = ptid; i < nf4; i += kPartialThreads) {
+        const float4 a = sm[i];
+        store_stream(y4 + i, make_float4(exp_shifted(a.x, w.m) * inv, exp_shifted(a.y, w.m) * inv,
+                                         exp_shifted(a.z, w.m) * inv, exp_shifted(a.w, w.m) * inv));
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+  }
+}
+
 // ---------------------------------------------------------------- launch ---
 std::mutex g_attr_mu;
 std::set<std::pair<const void*, int>> g_attr_done;
@@ -451,6 +658,27 @@ cudaError_t launch_softmax_staged_long(const rrs_plan& p, const float* x, float*
   if (e != cudaSuccess) return e;
   return launch_pdl(softmax_staged_long_kernel, dim3((unsigned)p.grid), dim3(kThreads),
                     (size_t)p.smem_bytes, s, 0, x, y, M, N, ld, p.tile, p.stages);
+}
+
+cudaError_t launch_softmax_staged_grid(const rrs_plan& p, const float* x, float* y, int64_t M,
+                                       int64_t N, int64_t ld, void* workspace, uint32_t ticket,
+                                       int fault, cudaStream_t s) {
+  if (p.threads != kThreads) return cudaErrorInvalidConfiguration;
+  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(softmax_staged_grid_kernel));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)p.smem_bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, softmax_staged_grid_kernel, x, y, M, N, ld, p.chunk,
+                            (int32_t)p.ctas_per_row, p.rows_per_cta, p.stages, p.tile * 4,
+                            static_cast<uint64_t*>(workspace), ticket, (int32_t)fault);
 }
 
 cudaError_t read_and_clear_staged_error(cudaStream_t s, unsigned* value) {

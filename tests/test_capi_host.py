@@ -62,6 +62,11 @@ def test_softmax_no_columns_is_a_no_op(lib):
     assert lib.softmax_rows(0x10000, 0x900000, 4, 0, 1, None) == OK
 
 
+def test_inject_fault_rejects_unknown(lib):
+    assert lib.rrs_inject_fault(7) == INVALID
+    assert lib.rrs_inject_fault(0) == OK
+
+
 def test_force_path_rejects_unknown(lib):
     assert lib.rrs_force_path(99, -1) == INVALID
     assert lib.rrs_force_path(-1, 99) == INVALID
@@ -85,7 +90,7 @@ def test_planner_on_the_five_workloads(lib):
     p4 = plan(16384, 4096)
     assert p4["path_name"] == "row_regs" and p4["warps_per_row"] == 4
     p5 = plan(32, 1 << 20)
-    assert p5["path_name"] == "two_phase"
+    assert p5["path_name"] == "grid"
 
 
 def test_grid_plan_for_the_longest_rows(lib):
@@ -93,9 +98,10 @@ def test_grid_plan_for_the_longest_rows(lib):
     try:
         rrs.force_path("grid")
         p5 = plan(32, 1 << 20)
-        assert p5["path_name"] == "grid" and p5["threads"] == 512
-        # 152 segments of 6900 floats per row, 2 rows per round over all 304 CTAs
-        assert (p5["ctas_per_row"], p5["rows_per_cta"], p5["grid"], p5["rounds"]) == (152, 2, 304, 16)
+        assert p5["path_name"] == "grid" and p5["threads"] == 544
+        # 76 segments of 13800 floats (one 55 KB stage each) per row, 2 rows per round
+        assert (p5["ctas_per_row"], p5["rows_per_cta"], p5["grid"], p5["rounds"]) == (76, 2, 152, 16)
+        assert p5["stages"] == 4 and p5["tile"] >= p5["chunk"]
     finally:
         rrs.force_path("auto", "auto")
 
@@ -140,8 +146,9 @@ def test_planner_covers_every_column(lib, M, N):
         C, seg = p["ctas_per_row"], p["chunk"]
         assert N % 4 == 0 and seg % 4 == 0 and C * seg >= N > (C - 1) * seg
         R = p["rows_per_cta"]
-        assert p["threads"] == 512 and p["grid"] == R * C <= 2 * 152 and R <= M
-        assert -(-seg // 4) <= 512 * p["vec"] and p["vec"] in (2, 4)
+        assert p["threads"] == 544 and p["grid"] == R * C <= 152 and R <= M and C <= 160
+        assert p["tile"] >= seg and p["tile"] % 32 == 0 and 3 <= p["stages"] <= 64
+        assert p["smem_bytes"] == 2048 + p["stages"] * p["tile"] * 4 <= 232448
         assert p["rounds"] == -(-M // R) and p["workspace_bytes"] == M * C * 16
 
 
