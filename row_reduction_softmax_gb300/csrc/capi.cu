@@ -220,7 +220,7 @@ int64_t staged_tile_max(int smem_optin) { return (staged_budget(smem_optin) / 7)
 constexpr int64_t kStagedRowsMaxN = 8192;
 constexpr int64_t kRowRegsAutoMaxN = 16384;
 constexpr double kPerSmBytesPerSec = 6.7e12 / 152.0;  // planning model only
-constexpr double kItemSec = 1.5e-6;                    // per-segment fixed cost (planning model)
+constexpr double kItemSec = 0.4e-6;                    // per-segment fixed cost (planning model)
 constexpr int64_t kGridMaxSegments = 160;              // slots one exchange warp polls
 
 bool plan_staged_rows(int64_t M, int64_t N, int sm_count, int smem_optin, rrs_plan* p) {
@@ -282,24 +282,27 @@ bool plan_staged_long(int64_t M, int64_t N, int sm_count, int smem_optin, rrs_pl
 }
 
 // GRID: C segments of a row on C CTAs (one per SM), R rows per round,
-// R * C <= SMs; each segment is one shared-memory stage and the ring holds
-// at least 3 (the segment being finalised, the next one, one in flight).
-// C minimises rounds x (per-SM segment time + a fixed per-segment cost).
+// R * C <= SMs; a segment is one shared-memory stage and, in registers, at
+// most 8 float4 per thread of the grid kernel's partial warps.  The ring
+// holds at least 2 stages.  C minimises rounds x (per-SM segment time + a
+// fixed per-segment cost).
+
 bool plan_grid(int64_t M, int64_t N, int sm_count, int smem_optin, int coop_ok, rrs_plan* p) {
   if (N % 4 != 0 || !coop_ok) return false;
   const int64_t budget = staged_budget(smem_optin);
+  const int64_t kGridMaxSegFloats = 8 * 4 * (int64_t)grid_partial_threads();
   double best = 1e300;
   int64_t b_seg = 0, b_c = 0, b_r = 0, b_ns = 0, b_stride = 0;
-  for (int64_t c = 1; c <= sm_count; ++c) {
+  for (int64_t c = std::max<int64_t>(1, ceil_div(N, kGridMaxSegFloats)); c <= sm_count; ++c) {
     const int64_t seg = round_up(ceil_div(N, c), 4);
     const int64_t C = ceil_div(N, seg);
+    if (C > kGridMaxSegments || seg > kGridMaxSegFloats) continue;
     const int64_t stride = round_up(seg * 4, 128);
     const int64_t ns = std::min<int64_t>(staged_max_stages(), budget / stride);
-    if (ns < 3) continue;
+    if (ns < 2) continue;
     const int64_t R = std::min<int64_t>(sm_count / C, M);
     if (R < 1) continue;
     const double rounds = (double)ceil_div(M, R);
-    if (C > kGridMaxSegments) continue;
     const double t = rounds * (8.0 * (double)seg / kPerSmBytesPerSec + kItemSec);
     if (t < best * (1.0 - 1e-9)) {
       best = t;
@@ -311,10 +314,11 @@ bool plan_grid(int64_t M, int64_t N, int sm_count, int smem_optin, int coop_ok, 
     }
   }
   if (b_seg == 0) return false;
+  const int64_t per_thread = ceil_div(ceil_div(b_seg, 4), grid_partial_threads());
   p->path = RRS_PATH_GRID;
-  p->vec = 0;
-  p->warps_per_row = staged_consumer_warps();
-  p->threads = staged_threads();
+  p->vec = per_thread <= 2 ? 2 : (per_thread <= 4 ? 4 : 8);
+  p->warps_per_row = grid_threads() / 32 - 1;
+  p->threads = grid_threads();
   p->grid = b_r * b_c;
   p->rows_per_cta = (int32_t)b_r;
   p->ctas_per_row = b_c;

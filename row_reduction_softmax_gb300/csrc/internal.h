@@ -40,6 +40,8 @@ int staged_header_bytes();
 int staged_max_stages();
 int staged_threads();
 int staged_consumer_warps();
+int grid_threads();
+int grid_partial_threads();
 cudaError_t launch_softmax_staged_rows(const rrs_plan& p, const float* x, float* y, int64_t M,
                                        int64_t N, int64_t ld, cudaStream_t s);
 cudaError_t launch_softmax_staged_long(const rrs_plan& p, const float* x, float* y, int64_t M,

@@ -94,6 +94,14 @@ __device__ __forceinline__ void st_relaxed_gpu_u64(uint64_t* p, uint64_t v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+// Publish a 64-bit word at GPU scope with an atomic exchange: atomics are
+// performed at L2, so other SMs' relaxed loads see the value promptly.
+__device__ __forceinline__ void publish_gpu_u64(uint64_t* p, uint64_t v) {
+  uint64_t old;
+  asm volatile("atom.relaxed.gpu.global.exch.b64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+  (void)old;
+}
+
 // Acquire side of a release store observed through relaxed loads.
 __device__ __forceinline__ void fence_acquire_gpu() {
   asm volatile("fence.acq_rel.gpu;" ::: "memory");

@@ -265,7 +265,6 @@ __device__ __forceinline__ float consumer_sum(float v, float* red, int warp, int
 }
 
 constexpr int kLongUnroll = 4;
-constexpr int kGridBatch = 8;  // float4 per thread folded at once in a grid partial
 
 // CTA b takes rows b, b + G, b + 2G, ... (G = gridDim.x); each row is staged
 // as n_sub <= 4 sub-tiles of tile_floats (the last may be shorter).  Every
@@ -409,24 +408,35 @@ softmax_staged_long_kernel(const float* __restrict__ x, float* __restrict__ y, i
 // a reader that sees this launch's ticket in a word has that word's value,
 // and no fence is needed on either side.
 //
-// Warps 1..15 compute partials: P(k) = wait for the stage, fold it into an
-// exact per-thread (max, sum), merge over the 15 warps, publish.  Warp 0 is
-// the exchange warp: E(k) = poll the row's C slots, merge them in slot order
-// (identically in every CTA of the row).  Partials run `lead` items ahead:
-// iteration k runs P(k + lead) on warps 1..15 while warp 0 runs E(k); then
-// all 16 warps meet, and warps 1..15 normalise the staged segment k, store y
-// and release the stage.  E(k) needs P(k) of its row's CTAs, each published
-// before that CTA's own E(k - lead); all of a row's CTAs are resident
-// (cooperative launch), so the waits end.
+// Warps 1..14 compute partials: P(k) = wait for stage k, copy this thread's
+// float4 of it into registers and release the stage at once, reduce the
+// segment max m_c over the 14 warps, form e = exp(x - m_c), reduce the sum
+// s_c and publish (by atomic exchange, performed at L2, so peers see it
+// promptly).  Warp 0 is the exchange warp:
+// E(k) = poll the row's C slots (every load issued before any is used) and
+// merge them in slot order, identically in every CTA of the row.  Partials
+// run LEAD items ahead: iteration k runs P(k + LEAD) on warps 1..14 (into a
+// spare register set) while warp 0 runs E(k); then the 15 consumer warps
+// meet and warps 1..14 write y = e * exp(m_c - m) / s of item k.  E(k) needs
+// P(k) of its row's CTAs, each published before that CTA's own E(k - LEAD);
+// all of a row's CTAs are resident (cooperative launch), so the waits end.
 __device__ __forceinline__ uint64_t pack_tagged(uint32_t ticket, float v) {
   return ((uint64_t)ticket << 32) | (uint64_t)__float_as_uint(v);
 }
 
-constexpr int kPartialBar = 2;                     // warps 1..15
-constexpr int kMaxSlotsPerLane = 5;                // C <= 160: a row's slots over 32 lanes
-constexpr int kPartialThreads = kConsumers - 32;
+// The grid kernel runs 16 warps (512 threads, so up to 128 registers):
+// warp 0 exchanges, warps 1..14 compute partials, warp 15 produces.
+constexpr int kGThreads = 512;
+constexpr int kGProducerWarp = 15;
+constexpr int kGConsumerWarps = 15;
+constexpr int kGConsumers = 32 * kGConsumerWarps;
+constexpr int kPartialBar = 2;                      // warps 1..14
+constexpr int kPartialWarps = kGConsumerWarps - 1;
+constexpr int kPartialThreads = 32 * kPartialWarps;
+constexpr int kMaxSlotsPerLane = 5;                 // C <= 160: a row's slots over 32 lanes
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <int VEC, int LEAD>
+__global__ void __launch_bounds__(kGThreads, 1)
 softmax_staged_grid_kernel(const float* __restrict__ x, float* __restrict__ y, int64_t M,
                            int64_t N, int64_t ld, int64_t seg, int32_t C, int32_t R, int32_t NS,
                            int32_t stage_stride, uint64_t* __restrict__ slots, uint32_t ticket,
@@ -436,7 +446,6 @@ softmax_staged_grid_kernel(const float* __restrict__ x, float* __restrict__ y, i
   uint64_t* empty = reinterpret_cast<uint64_t*>(smem + kEmptyOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortOff);
   volatile int* fail_flag = reinterpret_cast<volatile int*>(smem + kFailOff);
-  MaxSum* redp = reinterpret_cast<MaxSum*>(smem + kRedMOff);  // 16 pairs
   MaxSum* whole = reinterpret_cast<MaxSum*>(smem + kWholeOff);
   unsigned char* stages = smem + kHeaderBytes;
 
@@ -445,18 +454,19 @@ softmax_staged_grid_kernel(const float* __restrict__ x, float* __restrict__ y, i
   const int64_t seg_begin = (int64_t)c * seg;
   const int64_t seg_n = min(seg, N - seg_begin);
   const int64_t items = (M > row0) ? (M - row0 + R - 1) / R : 0;
-  if (NS < 3 || NS > kMaxStages || seg_n <= 0 || seg_n * 4 > stage_stride ||
-      C > 32 * kMaxSlotsPerLane) {  // uniform
+  const int nf4 = (int)(seg_n >> 2);
+  if (NS < 2 || NS > kMaxStages || seg_n <= 0 || seg_n * 4 > stage_stride ||
+      C > 32 * kMaxSlotsPerLane || nf4 > VEC * kPartialThreads) {  // uniform
     if (threadIdx.x == 0) atomicOr(&g_device_error, kErrConfig);
     return;
   }
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) init_barriers(smem, NS, kConsumerWarps);
+  if (threadIdx.x == 0) init_barriers(smem, NS, kPartialWarps);
   __syncthreads();
   pdl_entry();
 
-  if (warp == kProducerWarp) {
+  if (warp == kGProducerWarp) {
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
       const uint32_t bytes = (uint32_t)(seg_n * 4);
@@ -465,6 +475,12 @@ softmax_staged_grid_kernel(const float* __restrict__ x, float* __restrict__ y, i
       for (; k < items; ++k) {
         const int st = (int)(k % NS);
         if (k >= NS && !wait_bounded(&empty[st], (uint32_t)(((k / NS) - 1) & 1), abort_flag)) {
+          ok = false;
+          break;
+        }
+        // every CTA's first segment gates the first exchange of its row: let
+        // it land before the rest of the ring is queued behind it in HBM
+        if (k == 2 && NS > 2 && !wait_bounded(&full[0], 0, abort_flag)) {
           ok = false;
           break;
         }
@@ -477,124 +493,163 @@ softmax_staged_grid_kernel(const float* __restrict__ x, float* __restrict__ y, i
     return;
   }
 
-  const int nf4 = (int)(seg_n >> 2);
   const float kNeg = neg_inf();
-  const int ptid = threadIdx.x - 32;  // index among warps 1..15
+  const int ptid = threadIdx.x - 32;  // index among warps 1..14
+  float* red_m = reinterpret_cast<float*>(smem + kRedMOff);
+  float* red_s = reinterpret_cast<float*>(smem + kRedSOff);
 
-  // P(k) on warps 1..15: false if a wait ran out (the same answer in all of them).
-  auto partial = [&](int64_t k) -> bool {
+  // P(k) on warps 1..14 into register set v: e = exp(x - m_c) against the
+  // segment max m_c (a max reduction, then a sum reduction -- no exps in the
+  // reduction trees).  False if a wait ran out (the same answer in all of them).
+  auto partial = [&](int64_t k, float4 (&v)[VEC], float& mc_out) -> bool {
     const int st = (int)(k % NS);
     const bool got = wait_bounded(&full[st], (uint32_t)((k / NS) & 1), abort_flag);
     const float4* sm = reinterpret_cast<const float4*>(stages + (size_t)st * stage_stride);
-    MaxSum p{kNeg, 0.f};
-    if (got) {
-      for (int i0 = ptid; i0 < nf4; i0 += kPartialThreads * kGridBatch) {
-        float4 a[kGridBatch];
-        float bm = kNeg;
 #pragma unroll
-        for (int u = 0; u < kGridBatch; ++u) {
-          const int idx = i0 + u * kPartialThreads;
-          a[u] = (idx < nf4) ? sm[idx] : make_float4(kNeg, kNeg, kNeg, kNeg);
-          bm = max_nan(bm, max4(a[u]));
-        }
-        rescale_to(p, bm);
-        if (p.m != kNeg) {
-#pragma unroll
-          for (int u = 0; u < kGridBatch; ++u) {
-            p.s += (exp_shifted(a[u].x, p.m) + exp_shifted(a[u].y, p.m)) +
-                   (exp_shifted(a[u].z, p.m) + exp_shifted(a[u].w, p.m));
-          }
-        }
-      }
+    for (int i = 0; i < VEC; ++i) {
+      const int idx = ptid + i * kPartialThreads;
+      v[i] = (got && idx < nf4) ? sm[idx] : make_float4(kNeg, kNeg, kNeg, kNeg);
     }
-    p = warp_merge(p);
-    if (lane == 0) redp[warp] = p;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);  // the segment is in registers: stage free
+    float m = kNeg;
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) m = max_nan(m, max4(v[i]));
+    m = warp_max(m);
+    if (lane == 0) red_m[warp] = m;
     if (barrier_or(kPartialBar, kPartialThreads, !got)) return false;
-    MaxSum q = (lane >= 1 && lane < kConsumerWarps) ? redp[lane] : MaxSum{kNeg, 0.f};
-    q = warp_merge(q);  // every warp merges the same pairs in the same order
-    named_barrier(kPartialBar, kPartialThreads);  // `redp` is rewritten by the next merge
+    m = warp_max((lane >= 1 && lane < kGConsumerWarps) ? red_m[lane] : kNeg);
+    const bool none = (m == kNeg);  // only -inf (or nothing) in this segment
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+      v[i].x = none ? 0.f : exp_shifted(v[i].x, m);
+      v[i].y = none ? 0.f : exp_shifted(v[i].y, m);
+      v[i].z = none ? 0.f : exp_shifted(v[i].z, m);
+      v[i].w = none ? 0.f : exp_shifted(v[i].w, m);
+      sum += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+    }
+    sum = warp_sum(sum);
+    if (lane == 0) red_s[warp] = sum;
+    named_barrier(kPartialBar, kPartialThreads);
+    sum = warp_sum((lane >= 1 && lane < kGConsumerWarps) ? red_s[lane] : 0.f);
+    mc_out = m;
     if (ptid == 0 && !(fault != 0 && blockIdx.x == 0 && k == 0)) {
       uint64_t* sl = slots + 2 * ((row0 + k * R) * C + c);
-      st_relaxed_gpu_u64(sl, pack_tagged(ticket, q.m));
-      st_relaxed_gpu_u64(sl + 1, pack_tagged(ticket, q.s));
+      publish_gpu_u64(sl, pack_tagged(ticket, m));
+      publish_gpu_u64(sl + 1, pack_tagged(ticket, sum));
     }
     return true;
   };
 
-  // Partials run `lead` items ahead of the exchange: the consumers hold
-  // stages k .. k + lead, the rest of the ring is in flight.
-  const int lead = min(3, NS - 2);
-  if (warp > 0) {
-    for (int64_t k = 0; k < lead && k < items; ++k) {
-      if (!partial(k)) {  // seen by every consumer warp after the first meeting
-        if (ptid == 0) *fail_flag = 1;
+  // E(k) on warp 0: merged (m, s) of the row into *whole; sets the fail flag
+  // if the wait ran out.
+  auto exchange = [&](int64_t k) {
+    const uint64_t* rs = slots + 2 * (row0 + k * R) * C;
+    const uint64_t t0 = global_timer_ns();
+    bool seen = false;
+    uint32_t n = 0;
+    MaxSum acc{kNeg, 0.f};
+    while (!*fail_flag) {
+      uint64_t wm[kMaxSlotsPerLane], ws[kMaxSlotsPerLane];
+#pragma unroll
+      for (int j = 0; j < kMaxSlotsPerLane; ++j) {
+        const int l = lane + 32 * j;
+        wm[j] = (l < C) ? ld_relaxed_gpu_u64(rs + 2 * l) : pack_tagged(ticket, kNeg);
+        ws[j] = (l < C) ? ld_relaxed_gpu_u64(rs + 2 * l + 1) : pack_tagged(ticket, 0.f);
+      }
+      bool mine = true;
+#pragma unroll
+      for (int j = 0; j < kMaxSlotsPerLane; ++j) {
+        mine &= ((uint32_t)(wm[j] >> 32) == ticket) && ((uint32_t)(ws[j] >> 32) == ticket);
+      }
+      if (__all_sync(kFullMask, mine)) {
+#pragma unroll
+        for (int j = 0; j < kMaxSlotsPerLane; ++j) {
+          acc = merge(acc, MaxSum{__uint_as_float((uint32_t)wm[j]), __uint_as_float((uint32_t)ws[j])});
+        }
+        seen = true;
+        break;
+      }
+      if ((++n & 15u) == 0 && (*abort_flag || global_timer_ns() - t0 > kWaitLimitNs)) break;
+    }
+    acc = warp_merge(acc);
+    if (lane == 0) {
+      *whole = acc;
+      if (!seen) {
+        atomicOr(&g_device_error, kErrTimeout);
+        *abort_flag = 1;
+        *fail_flag = 1;
       }
     }
+  };
+
+  // The exchange warp and the partial warps run separate loops that meet at
+  // the same two consumer barriers per item, so the partial warps' register
+  // sets are never live in the exchange warp's code.
+  if (warp == 0) {
+    for (int64_t k = 0; k < items; ++k) {
+      exchange(k);
+      named_barrier(kConsumerBar, kGConsumers);
+      const bool failed = *fail_flag != 0;
+      named_barrier(kConsumerBar, kGConsumers);  // `whole` and the flag are rewritten next round
+      if (failed) return;
+    }
+    return;
   }
-  for (int64_t k = 0; k < items; ++k) {
-    const int64_t row = row0 + k * R;
-    if (warp == 0) {
-      // E(k): poll the row's C slots (both words of each) with relaxed loads
-      const uint64_t* rs = slots + 2 * row * C;
-      const uint64_t t0 = global_timer_ns();
-      bool seen = false;
-      uint32_t n = 0;
-      MaxSum acc{kNeg, 0.f};
-      while (!*fail_flag) {
-        // all of this lane's slot words are loaded before any is used, so the
-        // poll costs one round trip to L2, not one per slot
-        uint64_t wm[kMaxSlotsPerLane], ws[kMaxSlotsPerLane];
-#pragma unroll
-        for (int j = 0; j < kMaxSlotsPerLane; ++j) {
-          const int l = lane + 32 * j;
-          wm[j] = (l < C) ? ld_relaxed_gpu_u64(rs + 2 * l) : pack_tagged(ticket, kNeg);
-          ws[j] = (l < C) ? ld_relaxed_gpu_u64(rs + 2 * l + 1) : pack_tagged(ticket, 0.f);
-        }
-        bool mine = true;
-        MaxSum a{kNeg, 0.f};
-#pragma unroll
-        for (int j = 0; j < kMaxSlotsPerLane; ++j) {
-          mine &= ((uint32_t)(wm[j] >> 32) == ticket) && ((uint32_t)(ws[j] >> 32) == ticket);
-          a = merge(a, MaxSum{__uint_as_float((uint32_t)wm[j]), __uint_as_float((uint32_t)ws[j])});
-        }
-        if (__all_sync(kFullMask, mine)) {
-          seen = true;
-          acc = a;
-          break;
-        }
-        if ((++n & 15u) == 0 && (*abort_flag || global_timer_ns() - t0 > kWaitLimitNs)) break;
-      }
-      acc = warp_merge(acc);
-      if (lane == 0) {
-        *whole = acc;
-        if (!seen) {
-          atomicOr(&g_device_error, kErrTimeout);
-          *abort_flag = 1;
-          *fail_flag = 1;
-        }
-      }
-    } else if (k + lead < items && !partial(k + lead)) {
+
+  // Partial warps, one item: P(k + LEAD) into `ahead` (while warp 0 runs
+  // E(k)), then y of item k from `cur`.  LEAD + 1 register sets rotate: the
+  // item being written, those whose exchange is pending, the one being
+  // formed.  False once the CTA must stop.
+  auto step = [&](int64_t k, float4 (&cur)[VEC], float mtc, float4 (&ahead)[VEC], float& mta) {
+    if (k + LEAD < items && !partial(k + LEAD, ahead, mta)) {
       if (ptid == 0) *fail_flag = 1;
     }
-    named_barrier(kConsumerBar, kConsumers);
+    named_barrier(kConsumerBar, kGConsumers);
     const bool failed = *fail_flag != 0;
     const MaxSum w = *whole;
-    named_barrier(kConsumerBar, kConsumers);  // `whole` and the flag are rewritten next round
-    if (failed) return;
-
-    const int st = (int)(k % NS);
-    if (warp > 0) {
-      const float4* sm = reinterpret_cast<const float4*>(stages + (size_t)st * stage_stride);
-      float4* y4 = reinterpret_cast<float4*>(y + row * ld + seg_begin);
-      const float inv = 1.0f / w.s;
-      for (int i = ptid; i < nf4; i += kPartialThreads) {
-        const float4 a = sm[i];
-        store_stream(y4 + i, make_float4(exp_shifted(a.x, w.m) * inv, exp_shifted(a.y, w.m) * inv,
-                                         exp_shifted(a.z, w.m) * inv, exp_shifted(a.w, w.m) * inv));
+    named_barrier(kConsumerBar, kGConsumers);
+    if (failed) return false;
+    const bool bad = !(w.s == w.s) || w.m == kNeg;  // NaN / inf / all -inf row
+    const float scale =
+        bad ? __int_as_float(0x7fc00000) : (mtc == kNeg ? 0.f : exp_shifted(mtc, w.m) / w.s);
+    float4* y4 = reinterpret_cast<float4*>(y + (row0 + k * R) * ld + seg_begin);
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) {
+      const int idx = ptid + i * kPartialThreads;
+      if (idx < nf4) {
+        store_stream(y4 + idx, make_float4(cur[i].x * scale, cur[i].y * scale, cur[i].z * scale,
+                                           cur[i].w * scale));
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
+    return true;
+  };
+
+  float4 a[VEC], b[VEC];
+  float ma = kNeg, mb = kNeg;
+  bool ok = true;
+  if constexpr (LEAD == 1) {
+    if (items > 0) ok = partial(0, a, ma);
+    if (!ok && ptid == 0) *fail_flag = 1;  // seen by every consumer warp at the first meeting
+    for (int64_t k = 0; k < items; k += 2) {
+      if (!step(k, a, ma, b, mb)) return;
+      if (k + 1 >= items) break;
+      if (!step(k + 1, b, mb, a, ma)) return;
+    }
+  } else {
+    float4 cc[VEC];
+    float mc = kNeg;
+    if (items > 0) ok = partial(0, a, ma);
+    if (ok && items > 1) ok = partial(1, b, mb);
+    if (!ok && ptid == 0) *fail_flag = 1;
+    for (int64_t k = 0; k < items; k += 3) {
+      if (!step(k, a, ma, cc, mc)) return;
+      if (k + 1 >= items) break;
+      if (!step(k + 1, b, mb, a, ma)) return;
+      if (k + 2 >= items) break;
+      if (!step(k + 2, cc, mc, b, mb)) return;
+    }
   }
 }
 
@@ -632,6 +687,8 @@ int staged_header_bytes() { return kHeaderBytes; }
 int staged_max_stages() { return kMaxStages; }
 int staged_threads() { return kThreads; }
 int staged_consumer_warps() { return kConsumerWarps; }
+int grid_threads() { return kGThreads; }
+int grid_partial_threads() { return kPartialThreads; }
 
 cudaError_t launch_softmax_staged_rows(const rrs_plan& p, const float* x, float* y, int64_t M,
                                        int64_t N, int64_t ld, cudaStream_t s) {
@@ -663,12 +720,21 @@ cudaError_t launch_softmax_staged_long(const rrs_plan& p, const float* x, float*
 cudaError_t launch_softmax_staged_grid(const rrs_plan& p, const float* x, float* y, int64_t M,
                                        int64_t N, int64_t ld, void* workspace, uint32_t ticket,
                                        int fault, cudaStream_t s) {
-  if (p.threads != kThreads) return cudaErrorInvalidConfiguration;
-  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(softmax_staged_grid_kernel));
+  if (p.threads != kGThreads) return cudaErrorInvalidConfiguration;
+  // segments of up to 4 float4 per thread run partials two items ahead (three
+  // register sets); longer ones, up to 8 float4, one item ahead
+  auto k2 = softmax_staged_grid_kernel<2, 2>;
+  auto k4 = softmax_staged_grid_kernel<4, 2>;
+  auto k8 = softmax_staged_grid_kernel<8, 1>;
+  const void* kern = p.vec == 2 ? reinterpret_cast<const void*>(k2)
+                   : p.vec == 4 ? reinterpret_cast<const void*>(k4)
+                   : p.vec == 8 ? reinterpret_cast<const void*>(k8) : nullptr;
+  if (!kern) return cudaErrorInvalidConfiguration;
+  cudaError_t e = allow_dynamic_smem(kern);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.grid, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(kGThreads, 1, 1);
   cfg.dynamicSmemBytes = (size_t)p.smem_bytes;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -676,9 +742,16 @@ cudaError_t launch_softmax_staged_grid(const rrs_plan& p, const float* x, float*
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, softmax_staged_grid_kernel, x, y, M, N, ld, p.chunk,
-                            (int32_t)p.ctas_per_row, p.rows_per_cta, p.stages, p.tile * 4,
-                            static_cast<uint64_t*>(workspace), ticket, (int32_t)fault);
+  uint64_t* slots = static_cast<uint64_t*>(workspace);
+  const int32_t C = (int32_t)p.ctas_per_row;
+  if (p.vec == 2)
+    return cudaLaunchKernelEx(&cfg, k2, x, y, M, N, ld, p.chunk, C, p.rows_per_cta, p.stages,
+                              p.tile * 4, slots, ticket, (int32_t)fault);
+  if (p.vec == 4)
+    return cudaLaunchKernelEx(&cfg, k4, x, y, M, N, ld, p.chunk, C, p.rows_per_cta, p.stages,
+                              p.tile * 4, slots, ticket, (int32_t)fault);
+  return cudaLaunchKernelEx(&cfg, k8, x, y, M, N, ld, p.chunk, C, p.rows_per_cta, p.stages,
+                            p.tile * 4, slots, ticket, (int32_t)fault);
 }
 
 cudaError_t read_and_clear_staged_error(cudaStream_t s, unsigned* value) {

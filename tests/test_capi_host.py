@@ -98,10 +98,10 @@ def test_grid_plan_for_the_longest_rows(lib):
     try:
         rrs.force_path("grid")
         p5 = plan(32, 1 << 20)
-        assert p5["path_name"] == "grid" and p5["threads"] == 544
+        assert p5["path_name"] == "grid" and p5["threads"] == 512
         # 76 segments of 13800 floats (one 55 KB stage each) per row, 2 rows per round
         assert (p5["ctas_per_row"], p5["rows_per_cta"], p5["grid"], p5["rounds"]) == (76, 2, 152, 16)
-        assert p5["stages"] == 4 and p5["tile"] >= p5["chunk"]
+        assert p5["stages"] == 4 and p5["tile"] >= p5["chunk"] and p5["vec"] == 8
     finally:
         rrs.force_path("auto", "auto")
 
@@ -146,8 +146,9 @@ def test_planner_covers_every_column(lib, M, N):
         C, seg = p["ctas_per_row"], p["chunk"]
         assert N % 4 == 0 and seg % 4 == 0 and C * seg >= N > (C - 1) * seg
         R = p["rows_per_cta"]
-        assert p["threads"] == 544 and p["grid"] == R * C <= 152 and R <= M and C <= 160
-        assert p["tile"] >= seg and p["tile"] % 32 == 0 and 3 <= p["stages"] <= 64
+        assert p["threads"] == 512 and p["grid"] == R * C <= 152 and R <= M and C <= 160
+        assert p["tile"] >= seg and p["tile"] % 32 == 0 and 2 <= p["stages"] <= 64
+        assert -(-seg // 4) <= p["vec"] * 448 and p["vec"] in (2, 4, 8)
         assert p["smem_bytes"] == 2048 + p["stages"] * p["tile"] * 4 <= 232448
         assert p["rounds"] == -(-M // R) and p["workspace_bytes"] == M * C * 16
 
