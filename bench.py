@@ -78,6 +78,22 @@ def dist_env():
             int(os.environ.get("WORLD_SIZE", "1")))
 
 
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """The slowest rank's time: every rank gets the max over all ranks."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rows_per_s(M: int, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: rows of all replicas over the slowest rank's time."""
+    return world * M * steps / (max_ms / 1e3)
+
+
 def measured_hbm_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -225,7 +241,7 @@ def kernel_of(plan: dict) -> str:
         return "softmax_staged_rows_kernel" if plan["vec"] > 0 else "softmax_staged_long_kernel"
     return {"row_regs": "softmax_row_regs_kernel", "cluster": "softmax_cluster_kernel",
             "two_phase": "softmax_partials_kernel+softmax_finalize_kernel",
-            "grid": "softmax_grid_kernel", "row": "row_sum_rows_kernel",
+            "grid": "softmax_staged_grid_kernel", "row": "row_sum_rows_kernel",
             "split": "row_sum_partials_kernel+row_sum_finalize_kernel"}.get(name, name)
 
 
@@ -288,17 +304,12 @@ def run_ours(args):
     torch.cuda.synchronize()
     sampler.stop()
     barrier()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
     if rrs.device_error() != 0:
         raise SystemExit("device error word set during the timed region")
 
     ms_per_step = ms / args.steps
-    rows_per_s = world * M * args.steps / (ms / 1e3)
+    rows_per_s = job_rows_per_s(M, args.steps, world, ms)
     alg_bytes = 8 * M * N
     achieved = alg_bytes / (ms_per_step / 1e3) / 1e9
     peak, peak_kind = measured_hbm_peak()
