@@ -1,4 +1,4 @@
-"""Float64 CPU oracle for the row-wise softmax and the row sum.
+"""Float64 CPU oracle for the row-wise softmax, the row sum and their variants.
 
 TEST INFRASTRUCTURE ONLY.  Nothing in the product path imports, calls or
 executes this package: only ``tests/``, ``__graft_entry__.smoke()`` and the
@@ -30,6 +30,17 @@ Where the pages are silent the oracle takes these readings:
   b with partials (m_a, s_a), (m_b, s_b), m = max(m_a, m_b) and
   s = s_a exp(m_a - m) + s_b exp(m_b - m), identity (-inf, 0), and a segment
   whose max is -inf contributes 0 (never exp(-inf - -inf)).
+* The log-softmax is not on the pages.  It is read as the logarithm of their
+  softmax: log(exp(x - m) / s) = (x - m) - log(s).  -inf entries give -inf;
+  the rows that give NaN in the softmax give NaN.
+* The row max is the first of the naive softmax's five steps; the row mean is
+  the row sum divided by N.  An empty row has max -inf (the max's identity)
+  and mean NaN (0 / 0).
+* The column softmax (a softmax down each column, over the rows) is the
+  pages' softmax with rows and columns exchanged; the lecture transcript's
+  question after the softmax kernel asks for it, and the answer is the same
+  computation with the strides swapped (transcript, the softmax kernel's
+  Q&A).
 
 Pins (see ``tests/test_oracle_pins.py``): every function here is checked
 against values the pages print or the mathematics fixes, never against itself.
@@ -45,6 +56,10 @@ __all__ = [
     "partial",
     "merge",
     "softmax_rows_split",
+    "log_softmax_rows",
+    "row_max",
+    "row_mean",
+    "softmax_cols",
 ]
 
 
@@ -158,3 +173,62 @@ def softmax_rows_split(x, cuts) -> np.ndarray:
         with np.errstate(invalid="ignore", divide="ignore"):
             out[i] = np.exp(a[i] - m) / s if m != -np.inf else np.nan
     return out
+
+
+def log_softmax_rows(x) -> np.ndarray:
+    """Row-wise log-softmax of an M x N matrix, in float64.
+
+    The logarithm of the pages' softmax ("Kernels, Triton, XLA", section
+    "Reductions and tiling"), which the pages do not show: (1) max of each
+    row, (2) subtract it, (3) exponentiate, (4) sum each row, (5) take the log
+    of the sum, (6) subtract it from the shifted row: (x - m) - log(s).
+    """
+    a = _as_rows(x)
+    if a.shape[1] == 0:
+        return a.copy()
+    with np.errstate(invalid="ignore", over="ignore", divide="ignore"):
+        m = np.max(a, axis=1, keepdims=True)          # (1) row max
+        z = a - m                                       # (2) subtract
+        e = np.exp(z)                                   # (3) exponentiate
+        s = np.sum(e, axis=1, keepdims=True)            # (4) row sum
+        return z - np.log(s)                            # (5), (6)
+
+
+def row_max(x) -> np.ndarray:
+    """Max of each row, in float64: step (1) of the naive softmax on "Kernels,
+    Triton, XLA", section "Reductions and tiling".  A row holding a NaN gives
+    NaN; an empty row gives -inf."""
+    a = _as_rows(x)
+    if a.shape[1] == 0:
+        return np.full(a.shape[0], -np.inf)
+    return np.max(a, axis=1)
+
+
+def row_mean(x) -> np.ndarray:
+    """Mean of each row, in float64: the row sum ("Kernels, Triton, XLA",
+    paragraph "Row sum, when the row doesn't fit") divided by N.  An empty row
+    gives NaN."""
+    a = _as_rows(x)
+    if a.shape[1] == 0:
+        return np.full(a.shape[0], np.nan)
+    return np.sum(a, axis=1) / a.shape[1]
+
+
+def softmax_cols(x) -> np.ndarray:
+    """Softmax down each column of an M x N matrix (over the rows), in float64.
+
+    The five naive steps with the reduction taken over i for every column j:
+    (1) m_j = max_i x[i, j], (2) subtract, (3) exponentiate, (4) s_j = sum_i,
+    (5) divide.  A column that is all -inf, or holds +inf or NaN, is NaN.
+    """
+    a = np.asarray(x, dtype=np.float64)
+    if a.ndim != 2:
+        raise ValueError("expected an M x N matrix")
+    if a.shape[0] == 0:
+        return a.copy()
+    with np.errstate(invalid="ignore", over="ignore"):
+        m = np.max(a, axis=0, keepdims=True)          # (1) column max
+        z = a - m                                       # (2) subtract
+        numerator = np.exp(z)                           # (3) exponentiate
+        denominator = np.sum(numerator, axis=0, keepdims=True)  # (4) column sum
+        return numerator / denominator                  # (5) divide

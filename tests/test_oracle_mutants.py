@@ -12,7 +12,8 @@ import numpy as np
 import pytest
 
 import oracle
-from test_oracle_pins import MERGE_CHECKS, ROW_SUM_CHECKS, SOFTMAX_CHECKS
+from test_oracle_pins import (LOG_SOFTMAX_CHECKS, MERGE_CHECKS, ROW_MAX_CHECKS, ROW_MEAN_CHECKS,
+                              ROW_SUM_CHECKS, SOFTMAX_CHECKS, SOFTMAX_COLS_CHECKS)
 
 
 def _rows(x):
@@ -170,3 +171,112 @@ def test_row_sum_mutant_is_caught(pair):
 @pytest.mark.parametrize("mutant", MERGE_MUTANTS, ids=lambda m: m.__name__)
 def test_merge_mutant_is_caught(mutant):
     assert any(_caught(check, oracle.partial, mutant) for check in MERGE_CHECKS)
+
+
+
+def lsm_no_log(x):
+    a = _rows(x)
+    with np.errstate(all="ignore"):
+        z = a - a.max(axis=1, keepdims=True)
+        return z - np.exp(z).sum(axis=1, keepdims=True)      # forgot the log
+
+
+def lsm_flipped(x):
+    a = _rows(x)
+    with np.errstate(all="ignore"):
+        z = a.max(axis=1, keepdims=True) - a
+        return z - np.log(np.exp(-z).sum(axis=1, keepdims=True))
+
+
+def lsm_unshifted_log(x):
+    a = _rows(x)
+    with np.errstate(all="ignore"):
+        z = a - a.max(axis=1, keepdims=True)
+        return a - np.log(np.exp(z).sum(axis=1, keepdims=True))   # m dropped from the output
+
+
+def lsm_log_of_softmax_max(x):
+    a = _rows(x)
+    with np.errstate(all="ignore"):
+        z = a - a.max(axis=1, keepdims=True)
+        return z - np.log(np.exp(z).max(axis=1, keepdims=True))
+
+
+LOG_SOFTMAX_MUTANTS = [lsm_no_log, lsm_flipped, lsm_unshifted_log, lsm_log_of_softmax_max]
+
+
+def rmax_min(x):
+    a = _rows(x)
+    return np.min(a, axis=1) if a.shape[1] else np.full(a.shape[0], -np.inf)
+
+
+def rmax_nan_ignoring(x):
+    a = _rows(x)
+    return np.nanmax(a, axis=1) if a.shape[1] else np.full(a.shape[0], -np.inf)
+
+
+def rmax_empty_zero(x):
+    a = _rows(x)
+    return np.max(a, axis=1) if a.shape[1] else np.zeros(a.shape[0])
+
+
+ROW_MAX_MUTANTS = [rmax_min, rmax_nan_ignoring, rmax_empty_zero]
+
+
+def rmean_n_minus_one(x):
+    a = _rows(x)
+    return a.sum(axis=1) / max(a.shape[1] - 1, 1) if a.shape[1] else np.full(a.shape[0], np.nan)
+
+
+def rmean_sum(x):
+    a = _rows(x)
+    return a.sum(axis=1) if a.shape[1] else np.full(a.shape[0], np.nan)
+
+
+def rmean_empty_zero(x):
+    a = _rows(x)
+    return a.sum(axis=1) / a.shape[1] if a.shape[1] else np.zeros(a.shape[0])
+
+
+ROW_MEAN_MUTANTS = [rmean_n_minus_one, rmean_sum, rmean_empty_zero]
+
+
+def scols_wrong_axis(x):
+    return oracle.softmax_rows(np.asarray(x, dtype=np.float64))
+
+
+def scols_no_shift(x):
+    a = np.asarray(x, dtype=np.float64)
+    with np.errstate(all="ignore"):
+        e = np.exp(a)
+        return e / e.sum(axis=0, keepdims=True)
+
+
+def scols_row_max_shift(x):
+    a = np.asarray(x, dtype=np.float64)
+    with np.errstate(all="ignore"):
+        e = np.exp(a - a.max(axis=1, keepdims=True))
+        return e / e.sum(axis=0, keepdims=True)
+
+
+SOFTMAX_COLS_MUTANTS = [scols_wrong_axis, scols_no_shift, scols_row_max_shift]
+
+
+@pytest.mark.parametrize("mutant", LOG_SOFTMAX_MUTANTS, ids=lambda m: m.__name__)
+def test_log_softmax_mutant_is_caught(mutant):
+    assert any(_caught(check, mutant) for check in LOG_SOFTMAX_CHECKS)
+
+
+@pytest.mark.parametrize("mutant", ROW_MAX_MUTANTS, ids=lambda m: m.__name__)
+def test_row_max_mutant_is_caught(mutant):
+    assert any(_caught(check, mutant) for check in ROW_MAX_CHECKS)
+
+
+@pytest.mark.parametrize("mutant", ROW_MEAN_MUTANTS, ids=lambda m: m.__name__)
+def test_row_mean_mutant_is_caught(mutant):
+    assert any(_caught(check, mutant) for check in ROW_MEAN_CHECKS)
+
+
+@pytest.mark.parametrize("mutant", SOFTMAX_COLS_MUTANTS, ids=lambda m: m.__name__)
+def test_softmax_cols_mutant_is_caught(mutant):
+    assert any(_caught(check, mutant) for check in SOFTMAX_COLS_CHECKS)

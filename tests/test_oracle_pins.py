@@ -258,3 +258,170 @@ def test_split_softmax_matches_definition():
 
 def test_empty_columns():
     assert oracle.softmax_rows(np.zeros((4, 0))).shape == (4, 0)
+
+
+# ------------------------------------------------- log-softmax pin checks ----
+
+def check_log_exp_is_softmax(lsm):
+    """exp of the log-softmax is the (independently pinned) softmax."""
+    for name, x in small_cases():
+        got = np.exp(lsm(x))
+        want = oracle.softmax_rows(x)
+        assert np.max(np.abs(got - want)) <= 1e-13, name
+
+
+def check_log_two_element(lsm):
+    rng = np.random.default_rng(21)
+    for _ in range(200):
+        x0, x1 = rng.uniform(-30, 30, size=2)
+        y = lsm(np.array([[x0, x1]]))[0]
+        want0 = -math.log1p(math.exp(x1 - x0))     # log sigma(x0 - x1)
+        want1 = -math.log1p(math.exp(x0 - x1))
+        assert abs(y[0] - want0) <= 1e-13 * max(1.0, abs(want0))
+        assert abs(y[1] - want1) <= 1e-13 * max(1.0, abs(want1))
+
+
+def check_log_brute_force(lsm):
+    """x_j - log(sum_k exp(x_k)) with an exactly rounded sum (no max shift)."""
+    rng = np.random.default_rng(22)
+    for M, N in ((3, 5), (5, 3), (1, 8), (2, 7)):
+        x = rng.uniform(-20, 20, size=(M, N))
+        y = lsm(x)
+        for i in range(M):
+            lse = math.log(math.fsum(math.exp(v) for v in x[i]))
+            for j in range(N):
+                assert abs(y[i, j] - (x[i, j] - lse)) <= 1e-13 * max(1.0, abs(y[i, j]))
+
+
+def check_log_library(lsm):
+    torch = pytest.importorskip("torch")
+    scipy_special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(23)
+    x = rng.normal(0, 4, size=(9, 50))
+    y = lsm(x)
+    assert np.max(np.abs(y - torch.log_softmax(torch.from_numpy(x), dim=1).numpy())) <= 1e-13
+    assert np.max(np.abs(y - scipy_special.log_softmax(x, axis=1))) <= 1e-13
+
+
+def check_log_special_rows(lsm):
+    for N in (1, 2, 7, 1000):
+        y = lsm(np.full((1, N), 3.5))[0]
+        assert np.max(np.abs(y + math.log(N))) <= 1e-15 * max(1.0, math.log(N))
+    y = lsm(np.array([[0.0, -np.inf, 0.0], [-np.inf, -np.inf, -np.inf]]))
+    assert y[0, 1] == -np.inf and abs(y[0, 0] + math.log(2)) <= 1e-16
+    assert np.all(np.isnan(y[1]))
+    rng = np.random.default_rng(24)
+    x = rng.normal(0, 3, size=(3, 40))
+    for c in (-100.0, 1000.0):                        # shift invariance
+        assert np.max(np.abs(lsm(x + c) - lsm(x))) <= 1e-11
+
+
+LOG_SOFTMAX_CHECKS = [check_log_exp_is_softmax, check_log_two_element, check_log_brute_force,
+                      check_log_library, check_log_special_rows]
+
+
+# ------------------------------------------------- row max / mean pin checks ----
+
+def check_max_worked_example(rmax):
+    g = load_worked_example()
+    assert rmax(np.array(g["row"])[None, :])[0] == 9.0      # 3 1 4 1 5 9 2 6 5 3
+
+
+def check_max_brute_force(rmax):
+    for name, x in small_cases():
+        got = rmax(x)
+        for i in range(x.shape[0]):
+            assert got[i] == max(x[i].tolist()), name   # Python's max, element by element
+
+
+def check_max_special(rmax):
+    x = np.array([[1.0, np.nan, 3.0], [-np.inf, -np.inf, -np.inf], [-np.inf, -7.0, -np.inf]])
+    got = rmax(x)
+    assert math.isnan(got[0]) and got[1] == -np.inf and got[2] == -7.0
+    assert np.all(rmax(np.zeros((2, 0))) == -np.inf)
+
+
+def check_mean_worked_example(rmean):
+    g = load_worked_example()
+    assert rmean(np.array(g["row"])[None, :])[0] == 39.0 / 10.0
+
+
+def check_mean_gauss(rmean):
+    for N in (1, 2, 10, 999, 4096):
+        x = np.arange(1, N + 1, dtype=np.float64)[None, :]
+        assert rmean(x)[0] == (N + 1) / 2
+
+
+def check_mean_exact(rmean):
+    for name, x in small_cases():
+        x = np.where(np.isfinite(x), x, 0.0)
+        got = rmean(x)
+        for i in range(x.shape[0]):
+            want = math.fsum(x[i]) / x.shape[1]
+            scale = math.fsum(abs(v) for v in x[i]) / x.shape[1]
+            assert abs(got[i] - want) <= 1e-13 * scale, name
+    assert np.all(np.isnan(rmean(np.zeros((2, 0)))))
+
+
+ROW_MAX_CHECKS = [check_max_worked_example, check_max_brute_force, check_max_special]
+ROW_MEAN_CHECKS = [check_mean_worked_example, check_mean_gauss, check_mean_exact]
+
+
+# ------------------------------------------------- column softmax pin checks ----
+
+def check_cols_transposed_rows(scols):
+    """A column softmax is the (independently pinned) row softmax of the transpose."""
+    for name, x in small_cases():
+        xt = np.ascontiguousarray(x.T)                # N x M: columns of length M
+        assert np.max(np.abs(scols(xt) - oracle.softmax_rows(x).T)) <= 1e-15, name
+
+
+def check_cols_sum_to_one(scols):
+    rng = np.random.default_rng(25)
+    x = rng.normal(0, 3, size=(300, 17))
+    assert np.max(np.abs(scols(x).sum(axis=0) - 1.0)) <= 1e-12
+
+
+def check_cols_two_rows(scols):
+    rng = np.random.default_rng(26)
+    x = rng.uniform(-30, 30, size=(2, 50))
+    y = scols(x)
+    for j in range(50):
+        want = 1.0 / (1.0 + math.exp(x[1, j] - x[0, j]))
+        assert abs(y[0, j] - want) <= 1e-14 * max(want, 1e-300) + 1e-300
+
+
+def check_cols_library_and_shift(scols):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(27)
+    x = rng.normal(0, 4, size=(60, 9))
+    y = scols(x)
+    assert np.max(np.abs(y - torch.softmax(torch.from_numpy(x), dim=0).numpy())) <= 1e-15
+    assert np.max(np.abs(scols(x + 1000.0) - y)) <= 1e-12
+    z = np.array([[-np.inf, 0.0], [-np.inf, -np.inf]])
+    got = scols(z)
+    assert np.all(np.isnan(got[:, 0])) and got[0, 1] == 1.0 and got[1, 1] == 0.0
+
+
+SOFTMAX_COLS_CHECKS = [check_cols_transposed_rows, check_cols_sum_to_one, check_cols_two_rows,
+                       check_cols_library_and_shift]
+
+
+@pytest.mark.parametrize("check", LOG_SOFTMAX_CHECKS, ids=lambda c: c.__name__)
+def test_log_softmax_pins(check):
+    check(oracle.log_softmax_rows)
+
+
+@pytest.mark.parametrize("check", ROW_MAX_CHECKS, ids=lambda c: c.__name__)
+def test_row_max_pins(check):
+    check(oracle.row_max)
+
+
+@pytest.mark.parametrize("check", ROW_MEAN_CHECKS, ids=lambda c: c.__name__)
+def test_row_mean_pins(check):
+    check(oracle.row_mean)
+
+
+@pytest.mark.parametrize("check", SOFTMAX_COLS_CHECKS, ids=lambda c: c.__name__)
+def test_softmax_cols_pins(check):
+    check(oracle.softmax_cols)
