@@ -42,6 +42,11 @@ Where the pages are silent the oracle takes these readings:
   computation with the strides swapped (transcript, the softmax kernel's
   Q&A).
 
+* GeLU is the tanh approximation the pages implement three ways ("Kernels,
+  Triton, XLA", section "GeLU three ways: the case for fusion"; "GPU
+  High-Performance Programming", section 7.4.1), with the constants as
+  printed there: 0.5 x (1 + tanh(0.79788456 (x + 0.044715 x^3))).
+
 Pins (see ``tests/test_oracle_pins.py``): every function here is checked
 against values the pages print or the mathematics fixes, never against itself.
 """
@@ -60,6 +65,7 @@ __all__ = [
     "row_max",
     "row_mean",
     "softmax_cols",
+    "gelu",
 ]
 
 
@@ -232,3 +238,16 @@ def softmax_cols(x) -> np.ndarray:
         numerator = np.exp(z)                           # (3) exponentiate
         denominator = np.sum(numerator, axis=0, keepdims=True)  # (4) column sum
         return numerator / denominator                  # (5) divide
+
+
+GELU_C = 0.79788456      # the pages' constant (sqrt(2 / pi) to 8 digits)
+GELU_K = 0.044715
+
+
+def gelu(x) -> np.ndarray:
+    """GeLU, tanh approximation, elementwise in float64, as the pages write it
+    ("Kernels, Triton, XLA", section "GeLU three ways"): the inner polynomial
+    a = 0.79788456 (x + 0.044715 x^3), then 0.5 x (1 + tanh(a))."""
+    a = np.asarray(x, dtype=np.float64)
+    inner = GELU_C * (a + GELU_K * a * a * a)
+    return 0.5 * a * (1.0 + np.tanh(inner))

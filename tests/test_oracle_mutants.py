@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 import oracle
-from test_oracle_pins import (LOG_SOFTMAX_CHECKS, MERGE_CHECKS, ROW_MAX_CHECKS, ROW_MEAN_CHECKS,
+from test_oracle_pins import (GELU_CHECKS, LOG_SOFTMAX_CHECKS, MERGE_CHECKS, ROW_MAX_CHECKS, ROW_MEAN_CHECKS,
                               ROW_SUM_CHECKS, SOFTMAX_CHECKS, SOFTMAX_COLS_CHECKS)
 
 
@@ -280,3 +280,32 @@ def test_row_mean_mutant_is_caught(mutant):
 @pytest.mark.parametrize("mutant", SOFTMAX_COLS_MUTANTS, ids=lambda m: m.__name__)
 def test_softmax_cols_mutant_is_caught(mutant):
     assert any(_caught(check, mutant) for check in SOFTMAX_COLS_CHECKS)
+
+
+
+def gelu_no_half(x):
+    a = np.asarray(x, dtype=np.float64)
+    return a * (1.0 + np.tanh(0.79788456 * (a + 0.044715 * a ** 3)))
+
+
+def gelu_square_term(x):
+    a = np.asarray(x, dtype=np.float64)
+    return 0.5 * a * (1.0 + np.tanh(0.79788456 * (a + 0.044715 * a ** 2)))
+
+
+def gelu_minus_tanh(x):
+    a = np.asarray(x, dtype=np.float64)
+    return 0.5 * a * (1.0 - np.tanh(0.79788456 * (a + 0.044715 * a ** 3)))
+
+
+def gelu_sigmoid_form(x):                     # x * sigmoid(1.702 x): a different approximation
+    a = np.asarray(x, dtype=np.float64)
+    return a / (1.0 + np.exp(-1.702 * a))
+
+
+GELU_MUTANTS = [gelu_no_half, gelu_square_term, gelu_minus_tanh, gelu_sigmoid_form]
+
+
+@pytest.mark.parametrize("mutant", GELU_MUTANTS, ids=lambda m: m.__name__)
+def test_gelu_mutant_is_caught(mutant):
+    assert any(_caught(check, mutant) for check in GELU_CHECKS)

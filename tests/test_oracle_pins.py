@@ -425,3 +425,46 @@ def test_row_mean_pins(check):
 @pytest.mark.parametrize("check", SOFTMAX_COLS_CHECKS, ids=lambda c: c.__name__)
 def test_softmax_cols_pins(check):
     check(oracle.softmax_cols)
+
+
+
+# ------------------------------------------------------------- GeLU pin checks ----
+
+def check_gelu_closed_values(g):
+    assert g(np.array([0.0]))[0] == 0.0
+    want1 = 0.5 * (1.0 + math.tanh(0.79788456 * (1.0 + 0.044715)))   # x = 1, the pages' check value
+    assert abs(g(np.array([1.0]))[0] - want1) <= 1e-16
+    assert abs(want1 - 0.8411919906) <= 1e-9                          # the number itself
+    big = np.array([10.0, 30.0, 1e3])
+    assert np.all(g(big) == big)                                      # tanh saturates to 1
+    assert np.all(g(-big) == 0.0)
+
+
+def check_gelu_reflection(g):
+    """gelu(x) - gelu(-x) = x: the tanh terms cancel (tanh is odd)."""
+    x = np.random.default_rng(41).normal(0, 3, size=1000)
+    assert np.max(np.abs(g(x) - g(-x) - x)) <= 1e-14 * max(1.0, float(np.max(np.abs(x))))
+
+
+def check_gelu_library(g):
+    torch = pytest.importorskip("torch")
+    x = np.random.default_rng(42).normal(0, 3, size=(64, 64))
+    t = torch.nn.functional.gelu(torch.from_numpy(x), approximate="tanh").numpy()
+    # torch uses sqrt(2/pi) = 0.7978845608...; the pages round it to 0.79788456
+    assert np.max(np.abs(g(x) - t)) <= 1e-8
+
+
+def check_gelu_derivative_at_zero(g):
+    """d/dx gelu at 0 is 1/2 (central difference), and gelu is smooth there."""
+    h = 1e-6
+    d = (g(np.array([h]))[0] - g(np.array([-h]))[0]) / (2 * h)
+    assert abs(d - 0.5) <= 1e-9
+
+
+GELU_CHECKS = [check_gelu_closed_values, check_gelu_reflection, check_gelu_library,
+               check_gelu_derivative_at_zero]
+
+
+@pytest.mark.parametrize("check", GELU_CHECKS, ids=lambda c: c.__name__)
+def test_gelu_pins(check):
+    check(oracle.gelu)
