@@ -21,6 +21,9 @@ The line carries, besides the contract's keys:
                 (cluster / grid / two-phase), the single-pass softmax on the
                 masked-logit rows, the row sum -- each timed on its workload
                 with its roofline fraction and a sampled-row parity check
+  variants      the operations built on the same skeleton -- log-softmax, in
+                place, row max / mean, column softmax, GeLU -- timed and checked
+                the same way
   clocks        SM clock and clock-event reasons sampled during the timed region
 
 ``--impl reference`` times the oracle instead, on the same metric and config.
@@ -61,6 +64,8 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="c2", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--no-suite", action="store_true", help="skip the per-row suite")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the variants (log-softmax, in place, row max/mean, columns, GeLU)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget")
@@ -351,6 +356,8 @@ def run_ours(args):
         out["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     if not args.no_suite:
         out["suite"] = run_suite(args, torch, rrs, dev, rank)
+    if not args.no_variants:
+        out["variants"] = run_variants(args, torch, rrs, dev, rank)
     del xs, ys
     if rank == 0:
         line = json.dumps(out)
@@ -490,6 +497,103 @@ def run_suite(args, torch, rrs, dev, rank):
                                else oracle_parity_row_sum(last, w, rows))
         entries.append(entry)
         del xs, ys
+        torch.cuda.empty_cache()
+    return entries
+
+
+def run_variants(args, torch, rrs, dev, rank):
+    """The variants on the softmax skeleton, each on its workload: log-softmax, in place,
+    row max / mean, column softmax and GeLU -- kernel time, roofline fraction, parity."""
+    import oracle
+    peak, peak_kind = measured_hbm_peak()
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    W = dict(workloads.WORKLOADS)
+    W.update(workloads.VARIANT_WORKLOADS)
+    cases = [("c2", "log_softmax"), ("c3", "log_softmax"), ("c5", "log_softmax"),
+             ("c3", "softmax_in_place"), ("c3", "row_max"), ("c3", "row_mean"),
+             ("cols_c2", "softmax_cols"), ("cols_c4", "softmax_cols"), ("gelu_16k", "gelu")]
+    entries = []
+    for name, op in cases:
+        w = W[name]
+        M, N = w.M, w.N
+        x_host = workloads.matrix(w)
+        reduce = op in ("row_max", "row_mean")
+        alg = 4 * M * N + 4 * M if reduce else 8 * M * N
+        npairs = l2_pairs(torch, alg)
+        xs = [torch.from_numpy(x_host).to(dev) for _ in range(npairs)]
+        ys = [torch.empty(M, dtype=torch.float32, device=dev) if reduce else
+              (xs[r] if op == "softmax_in_place" else torch.empty_like(xs[0]))
+              for r in range(npairs)]
+
+        def call(k, op=op, M=M, N=N):
+            r = k % npairs
+            x, y = xs[r].data_ptr(), ys[r].data_ptr()
+            if op == "log_softmax":
+                rrs.softmax_rows_ex_ptr(x, N, y, N, M, N, rrs.LOG_SOFTMAX, sh)
+            elif op == "softmax_in_place":
+                rrs.softmax_rows_ex_ptr(x, N, x, N, M, N, 0, sh)
+            elif op == "row_max":
+                rrs.row_max_ptr(x, y, M, N, N, sh)
+            elif op == "row_mean":
+                rrs.row_mean_ptr(x, y, M, N, N, sh)
+            elif op == "softmax_cols":
+                rrs.softmax_cols_ptr(x, N, y, N, M, N, 0, sh)
+            else:
+                rrs.gelu_ptr(x, y, M * N, sh)
+
+        for k in range(3):
+            call(k)
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for k in range(args.suite_steps):
+            call(k)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1) / args.suite_steps
+        gbs = alg / (ms / 1e3) / 1e9
+        entry = {"workload": name, "op": op, "M": M, "N": N, "ms_per_call": ms, "hbm_gbs": gbs,
+                 "frac_of_8tbs": gbs / ROOFLINE_GBS, "frac_of_peak": gbs / peak,
+                 "peak_kind": f"of {peak_kind}", "calls_timed": args.suite_steps,
+                 "l2": f"{npairs} rotating pair(s)"}
+        if op == "softmax_cols":
+            entry["path"] = rrs.plan_softmax_cols(M, N)["path_name"]
+        if rank == 0:
+            # one fresh call on the original x, compared with the oracle on a sample
+            xs[0].copy_(torch.from_numpy(x_host))
+            call(0)
+            torch.cuda.synchronize()
+            rows = sampled_rows(M, 6, w.seed)
+            if op in ("log_softmax", "softmax_in_place"):
+                got = ys[0][rows].cpu().numpy().astype(np.float64)
+                want = (oracle.log_softmax_rows if op == "log_softmax" else oracle.softmax_rows)(
+                    x_host[rows].astype(np.float64))
+                fin = np.isfinite(want)
+                entry["parity"] = {"rows_checked": len(rows),
+                                   "max_abs": float(np.max(np.abs(got[fin] - want[fin])))}
+            elif reduce:
+                got = ys[0][rows].cpu().numpy().astype(np.float64)
+                want = (oracle.row_max if op == "row_max" else oracle.row_mean)(
+                    x_host[rows].astype(np.float64))
+                entry["parity"] = {"rows_checked": len(rows),
+                                   "max_abs": float(np.max(np.abs(got - want)))}
+            elif op == "softmax_cols":
+                cols = sampled_rows(N, 6, w.seed + 1)
+                got = ys[0][:, cols].cpu().numpy().astype(np.float64)
+                want = oracle.softmax_cols(x_host[:, cols].astype(np.float64))
+                entry["parity"] = {"cols_checked": len(cols),
+                                   "max_abs": float(np.max(np.abs(got - want)))}
+            else:
+                rng = np.random.default_rng(w.seed)
+                idx = rng.integers(0, M * N, size=100000)
+                got = ys[0].view(-1)[torch.from_numpy(idx).to(dev)].cpu().numpy().astype(np.float64)
+                want = oracle.gelu(x_host.reshape(-1)[idx].astype(np.float64))
+                entry["parity"] = {"elements_checked": int(idx.size),
+                                   "max_rel": float(np.max(np.abs(got - want) /
+                                                           np.maximum(np.abs(want), 1e-30)))}
+        entries.append(entry)
+        del xs, ys, x_host
         torch.cuda.empty_cache()
     return entries
 

@@ -12,13 +12,21 @@
  *   row_sum       same section, paragraph "Row sum, when the row doesn't
  *                 fit": out[i] = sum_j x[i,j].
  *
+ * and variants on the same skeleton (declared further down, each with the
+ * passage it rests on): softmax_rows_ex (separate strides for x and y, in
+ * place, log-softmax), log_softmax_rows, softmax_cols, row_max, row_mean,
+ * and the elementwise gelu of the same pages.
+ *
  * Conventions shared by every entry point
  * ----------------------------------------
  * - Data are fp32.  x, y and out are DEVICE pointers (cudaMalloc, a caching
  *   allocator or managed memory) owned by the caller; the library neither
  *   frees nor keeps them.  Host pointers are rejected (RRS_ERR_INVALID_ARG).
- * - Row i of x occupies x[i*ld .. i*ld + N).  y uses the same ld.  The gap
- *   [N, ld) of every row of y is never written; the gap of x is never read.
+ * - Row i of x occupies x[i*ld .. i*ld + N).  y uses the same ld (except in
+ *   softmax_rows_ex, which takes one stride for each).  The gap [N, ld) of
+ *   every row of y is never written; the gap of x is never read.
+ * - y may be x itself (the same pointer and stride): the softmax is then
+ *   computed in place.  Any other overlap of x and y is RRS_ERR_ALIAS.
  * - stream is a cudaStream_t passed as void* (NULL = the legacy default
  *   stream).  All work is enqueued on it and the call returns without
  *   synchronising; results are ordered before later work on that stream.
@@ -78,6 +86,14 @@ typedef enum rrs_sum_path {
 } rrs_sum_path;
 
 /* A launch plan: what the host side decided for one call (pure host logic). */
+/* Execution paths of softmax_cols. */
+typedef enum rrs_cols_path {
+  RRS_COLS_AUTO = -1,
+  RRS_COLS_TWO_PHASE = 0,  /* any shape/alignment: per-(row chunk, column) partials, then merge + re-read + write */
+  RRS_COLS_CLUSTER = 1,    /* a band of 128 columns over a cluster of CTAs, all rows in registers (M <= 2048) */
+  RRS_COLS_COUNT = 2
+} rrs_cols_path;
+
 typedef struct rrs_plan {
   int32_t path;          /* rrs_path or rrs_sum_path */
   int32_t threads;       /* threads per CTA */
@@ -100,9 +116,46 @@ typedef struct rrs_plan {
  * x, y: device fp32, M rows of N valid entries, row stride ld (elements).
  * M == 0 or N == 0: no work, RRS_OK.  Errors: RRS_ERR_INVALID_ARG (M < 0,
  * N < 0, ld < N, ld < 1, null/host pointer, pointer not 4-byte aligned,
- * extent overflow), RRS_ERR_ALIAS (x and y overlap), RRS_ERR_CUDA,
- * RRS_ERR_NOMEM. */
+ * extent overflow), RRS_ERR_ALIAS (x and y overlap, unless y == x: in
+ * place), RRS_ERR_CUDA, RRS_ERR_NOMEM. */
 RRS_API int softmax_rows(const float* x, float* y, int64_t M, int64_t N, int64_t ld, void* stream);
+
+/* Flag bits of softmax_rows_ex. */
+#define RRS_LOG_SOFTMAX 1 /* write log y[i,j] = (x[i,j] - m_i) - log(s_i) instead of y */
+
+/* softmax_rows with a row stride for each matrix: row i of x at x + i*ldx,
+ * row i of y at y + i*ldy (both >= max(N, 1)).  The pages' softmax kernel
+ * takes the two row strides separately ("CS336 2026 Lecture 6: Kernels,
+ * Triton", section 5.3, the row-wise softmax).  A softmax down the columns
+ * is not a stride of this call (its reduction runs across rows): see
+ * softmax_cols.  x == y with ldx == ldy computes in place; any other
+ * overlap is RRS_ERR_ALIAS.
+ *
+ * flags = RRS_LOG_SOFTMAX writes the log-softmax, log y = (x - m) - log(s),
+ * the logarithm of the softmax definition above (the pages do not show it;
+ * it follows from y = exp(x - m) / s).  -inf entries give -inf; the rows
+ * that give NaN in the softmax give NaN.  RRS_ERR_UNSUPPORTED if a forced
+ * ROW_STAGED path is asked for the log form.  Unknown flag bits are
+ * RRS_ERR_INVALID_ARG.  Other arguments and errors as softmax_rows. */
+RRS_API int softmax_rows_ex(const float* x, int64_t ldx, float* y, int64_t ldy, int64_t M,
+                            int64_t N, int flags, void* stream);
+
+/* softmax_rows_ex(x, ld, y, ld, M, N, RRS_LOG_SOFTMAX, stream). */
+RRS_API int log_softmax_rows(const float* x, float* y, int64_t M, int64_t N, int64_t ld,
+                             void* stream);
+
+/* Softmax down each column: for every j < N and i < M,
+ *   m_j = max_i x[i,j],  s_j = sum_i exp(x[i,j] - m_j),
+ *   y[i,j] = exp(x[i,j] - m_j) / s_j
+ * (flags = RRS_LOG_SOFTMAX: (x[i,j] - m_j) - log(s_j)).  The pages' softmax
+ * with the reduction over rows; the lecture transcript takes it up in the
+ * questions after the softmax kernel, where only the strides change.  Element (i, j) of x is x[i*ldx + j], of y y[i*ldy + j];
+ * columns are read along rows, 512 contiguous bytes per warp access.
+ * Columns that are all -inf or hold +inf or NaN come out NaN.  x == y with
+ * ldx == ldy computes in place.  Arguments, errors and the empty cases as
+ * softmax_rows_ex. */
+RRS_API int softmax_cols(const float* x, int64_t ldx, float* y, int64_t ldy, int64_t M, int64_t N,
+                         int flags, void* stream);
 
 /* out[i] = sum_j x[i*ld + j] for i < M (fp32 accumulation, fixed order:
  * bitwise reproducible run to run).  N == 0 writes zeros (the sum's
@@ -110,8 +163,33 @@ RRS_API int softmax_rows(const float* x, float* y, int64_t M, int64_t N, int64_t
  * softmax_rows. */
 RRS_API int row_sum(const float* x, float* out, int64_t M, int64_t N, int64_t ld, void* stream);
 
-/* softmax_rows for callers that cannot allocate device memory.  The paper
- * has no counterpart: this is a deployment variant of the same operation.
+/* out[i] = max_j x[i*ld + j]: the first of the naive softmax's five steps
+ * ("Kernels, Triton, XLA", section "Reductions and tiling", the softmax
+ * paragraph), on the row-sum skeleton.  Exact (a max does not round).  A row
+ * holding a NaN gives NaN; N == 0 writes -inf (the max's identity).  Other
+ * arguments and errors as row_sum. */
+RRS_API int row_max(const float* x, float* out, int64_t M, int64_t N, int64_t ld, void* stream);
+
+/* out[i] = (sum_j x[i*ld + j]) / N: row_sum's fp32 sum (same order), divided
+ * by N once per row.  N == 0 writes NaN (0 / 0).  Other arguments and errors
+ * as row_sum. */
+RRS_API int row_mean(const float* x, float* out, int64_t M, int64_t N, int64_t ld, void* stream);
+
+/* y[i] = GeLU(x[i]) for i < n, the tanh approximation with the pages'
+ * constants: 0.5 x (1 + tanh(0.79788456 (x + 0.044715 x^3))) ("Kernels,
+ * Triton, XLA", section "GeLU three ways: the case for fusion", and the
+ * Triton GeLU walkthrough; "GPU High-Performance Programming", section
+ * 7.4.1).  The lecture's first kernel: elementwise and HBM-bound like the
+ * softmax.  Computed as x / (1 + exp(-2a)), the same value without the
+ * cancellation of 1 + tanh(a) for negative x.  x, y: device fp32, n
+ * contiguous elements; y == x computes in place, any other overlap is
+ * RRS_ERR_ALIAS.  n == 0: no work.  +inf gives +inf, -inf and NaN give NaN.
+ * Errors: RRS_ERR_INVALID_ARG (n < 0, null/host pointer, not 4-byte
+ * aligned), RRS_ERR_ALIAS, RRS_ERR_CUDA. */
+RRS_API int gelu(const float* x, float* y, int64_t n, void* stream);
+
+/* softmax_rows for callers that cannot allocate device memory.  The pages
+ * have no counterpart: this is a deployment variant of the same operation.
  *
  * Some callers may not call cudaMalloc or anything that allocates: a
  * plugin's execute hook inside an inference engine that owns all device
@@ -156,8 +234,11 @@ RRS_API int rrs_release_workspace(void);
  * RRS_ERR_UNSUPPORTED.  Returns RRS_OK or RRS_ERR_INVALID_ARG. */
 RRS_API int rrs_force_path(int softmax_path, int sum_path);
 
+/* The same for softmax_cols: an rrs_cols_path (AUTO restores the planner). */
+RRS_API int rrs_force_cols_path(int cols_path);
+
 /* Fault injection for failure-detection tests (no counterpart in the
- * paper).  kind 1: in later GRID launches, CTA 0 never publishes the
+ * pages).  kind 1: in later GRID launches, CTA 0 never publishes the
  * partial of its first row segment, so that row's bounded waits run out
  * (about 1 s); the kernel returns early, rrs_device_error() then reports
  * RRS_ERR_TIMEOUT, the output of that call is incomplete, and the CUDA
@@ -174,6 +255,8 @@ RRS_API int rrs_plan_softmax(int64_t M, int64_t N, int64_t ld, int vector_ok, in
                              int smem_optin, rrs_plan* plan);
 RRS_API int rrs_plan_row_sum(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_count,
                              int smem_optin, rrs_plan* plan);
+RRS_API int rrs_plan_softmax_cols(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_count,
+                                  int smem_optin, rrs_plan* plan);
 
 /* Occupancy arithmetic used by the planner ("Kernels, Triton, XLA", section
  * "Where the abstraction leaks", worked example on register pressure):

@@ -6,11 +6,13 @@ PyTorch fallback -- if the library is not built, every call raises.
 
 Two layers, with the C ABI's names:
 
-* ``softmax_rows(x, y=None)`` / ``row_sum(x, out=None)`` take CUDA fp32
-  tensors (2-D, unit column stride; x and y share the row stride ``ld``) and
-  enqueue on the current torch stream.
-* ``softmax_rows_ptr`` / ``row_sum_ptr`` take raw device addresses, sizes and
-  a ``cudaStream_t`` handle, exactly like the C functions.
+* ``softmax_rows(x, y=None)``, ``log_softmax_rows``, ``row_sum(x, out=None)``,
+  ``row_max``, ``row_mean`` take CUDA fp32 tensors (2-D, unit column stride;
+  x and y may have different row strides, and y may be x itself) and enqueue
+  on the current torch stream.
+* ``softmax_rows_ptr``, ``softmax_rows_ex_ptr``, ``row_sum_ptr``, ... take raw
+  device addresses, sizes and a ``cudaStream_t`` handle, exactly like the C
+  functions.
 """
 from __future__ import annotations
 
@@ -21,17 +23,23 @@ import threading
 from ._build import LIB_PATH
 
 __all__ = [
-    "RRSError", "load_library", "softmax_rows", "row_sum", "softmax_rows_ptr", "row_sum_ptr",
+    "RRSError", "load_library", "softmax_rows", "log_softmax_rows", "row_sum", "row_max",
+    "row_mean", "softmax_rows_ptr", "softmax_rows_ex_ptr", "log_softmax_rows_ptr", "row_sum_ptr",
+    "row_max_ptr", "row_mean_ptr", "LOG_SOFTMAX", "softmax_cols", "softmax_cols_ptr",
+    "force_cols_path", "plan_softmax_cols", "COLS_PATHS", "gelu", "gelu_ptr",
     "device_error", "release_workspace", "force_path", "plan_softmax", "plan_row_sum",
     "occupancy", "waves", "PATHS", "SUM_PATHS", "STATUS", "LIB_PATH",
 ]
 
 STATUS = {0: "RRS_OK", 1: "RRS_ERR_INVALID_ARG", 2: "RRS_ERR_ALIAS", 3: "RRS_ERR_CUDA",
           4: "RRS_ERR_TIMEOUT", 5: "RRS_ERR_NOMEM", 6: "RRS_ERR_UNSUPPORTED"}
+LOG_SOFTMAX = 1  # flag bit of softmax_rows_ex
 PATHS = {"auto": -1, "two_phase": 0, "row_regs": 1, "row_staged": 2, "cluster": 3, "grid": 4}
 SUM_PATHS = {"auto": -1, "row": 0, "split": 1}
+COLS_PATHS = {"auto": -1, "two_phase": 0, "cluster": 1}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 SUM_PATH_NAMES = {v: k for k, v in SUM_PATHS.items()}
+COLS_PATH_NAMES = {v: k for k, v in COLS_PATHS.items()}
 
 
 class RRSError(RuntimeError):
@@ -65,6 +73,15 @@ _P = ctypes.c_void_p
 
 _SIGNATURES = {
     "softmax_rows": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P]),
+    "softmax_rows_ex": (ctypes.c_int, [_P, _I64, _P, _I64, _I64, _I64, ctypes.c_int, _P]),
+    "log_softmax_rows": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P]),
+    "row_max": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P]),
+    "gelu": (ctypes.c_int, [_P, _P, _I64, _P]),
+    "softmax_cols": (ctypes.c_int, [_P, _I64, _P, _I64, _I64, _I64, ctypes.c_int, _P]),
+    "rrs_force_cols_path": (ctypes.c_int, [ctypes.c_int]),
+    "rrs_plan_softmax_cols": (ctypes.c_int, [_I64, _I64, _I64, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int, ctypes.POINTER(Plan)]),
+    "row_mean": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P]),
     "softmax_rows_noalloc": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P]),
     "row_sum": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P]),
     "rrs_device_error": (ctypes.c_int, [_P]),
@@ -127,9 +144,41 @@ def softmax_rows_ptr(x: int, y: int, M: int, N: int, ld: int, stream: int = 0) -
     _check(load_library().softmax_rows(x, y, M, N, ld, stream), "softmax_rows")
 
 
+def softmax_rows_ex_ptr(x: int, ldx: int, y: int, ldy: int, M: int, N: int, flags: int = 0,
+                        stream: int = 0) -> None:
+    """C ``softmax_rows_ex``: separate row strides, in place when y == x, LOG_SOFTMAX flag."""
+    _check(load_library().softmax_rows_ex(x, ldx, y, ldy, M, N, flags, stream), "softmax_rows_ex")
+
+
+def softmax_cols_ptr(x: int, ldx: int, y: int, ldy: int, M: int, N: int, flags: int = 0,
+                     stream: int = 0) -> None:
+    """C ``softmax_cols``: softmax down each column (LOG_SOFTMAX flag for the log form)."""
+    _check(load_library().softmax_cols(x, ldx, y, ldy, M, N, flags, stream), "softmax_cols")
+
+
+def gelu_ptr(x: int, y: int, n: int, stream: int = 0) -> None:
+    """C ``gelu`` on raw device addresses (n contiguous floats)."""
+    _check(load_library().gelu(x, y, n, stream), "gelu")
+
+
+def log_softmax_rows_ptr(x: int, y: int, M: int, N: int, ld: int, stream: int = 0) -> None:
+    """C ``log_softmax_rows`` on raw device addresses."""
+    _check(load_library().log_softmax_rows(x, y, M, N, ld, stream), "log_softmax_rows")
+
+
 def row_sum_ptr(x: int, out: int, M: int, N: int, ld: int, stream: int = 0) -> None:
     """C ``row_sum`` on raw device addresses; raises :class:`RRSError` on failure."""
     _check(load_library().row_sum(x, out, M, N, ld, stream), "row_sum")
+
+
+def row_max_ptr(x: int, out: int, M: int, N: int, ld: int, stream: int = 0) -> None:
+    """C ``row_max`` on raw device addresses."""
+    _check(load_library().row_max(x, out, M, N, ld, stream), "row_max")
+
+
+def row_mean_ptr(x: int, out: int, M: int, N: int, ld: int, stream: int = 0) -> None:
+    """C ``row_mean`` on raw device addresses."""
+    _check(load_library().row_mean(x, out, M, N, ld, stream), "row_mean")
 
 
 # ----------------------------------------------------------------- tensors ----
@@ -151,26 +200,66 @@ def _rows_view(t, name: str):
     return M, N, ld
 
 
-def softmax_rows(x, y=None, stream=None):
-    """Row-wise softmax of a CUDA fp32 ``M x N`` tensor into ``y`` (allocated if None).
+def softmax_rows(x, y=None, stream=None, log=False):
+    """Row-wise softmax (``log=True``: log-softmax) of a CUDA fp32 ``M x N`` tensor.
 
-    ``y`` must have x's shape and row stride.  Enqueued on ``stream`` (default:
-    the current torch stream); returns ``y``.
+    ``y`` (allocated with x's row stride if None) must have x's shape; its row
+    stride may differ, and ``y`` may be ``x`` itself (in place).  Enqueued on
+    ``stream`` (default: the current torch stream); returns ``y``.
     """
     import torch
     M, N, ld = _rows_view(x, "x")
     if y is None:
         y = torch.empty_strided((M, N), (ld, 1), dtype=x.dtype, device=x.device)
     My, Ny, ldy = _rows_view(y, "y")
-    if (My, Ny) != (M, N) or (M > 1 and ldy != ld):
-        raise ValueError("y must match x's shape and row stride")
+    if (My, Ny) != (M, N):
+        raise ValueError("y must match x's shape")
     with torch.cuda.device(x.device):
-        softmax_rows_ptr(x.data_ptr(), y.data_ptr(), M, N, ld, _stream_handle(stream))
+        softmax_rows_ex_ptr(x.data_ptr(), ld, y.data_ptr(), ldy, M, N, LOG_SOFTMAX if log else 0,
+                            _stream_handle(stream))
     return y
 
 
-def row_sum(x, out=None, stream=None):
-    """Sum of each row of a CUDA fp32 ``M x N`` tensor into ``out`` (M floats; allocated if None)."""
+def softmax_cols(x, y=None, stream=None, log=False):
+    """Softmax down each column of a CUDA fp32 ``M x N`` tensor (``log=True``: log form).
+
+    Same tensor rules as :func:`softmax_rows`; returns ``y``.
+    """
+    import torch
+    M, N, ld = _rows_view(x, "x")
+    if y is None:
+        y = torch.empty_strided((M, N), (ld, 1), dtype=x.dtype, device=x.device)
+    My, Ny, ldy = _rows_view(y, "y")
+    if (My, Ny) != (M, N):
+        raise ValueError("y must match x's shape")
+    with torch.cuda.device(x.device):
+        softmax_cols_ptr(x.data_ptr(), ld, y.data_ptr(), ldy, M, N, LOG_SOFTMAX if log else 0,
+                         _stream_handle(stream))
+    return y
+
+
+def gelu(x, y=None, stream=None):
+    """Elementwise GeLU (tanh approximation) of a contiguous CUDA fp32 tensor; ``y`` may be ``x``."""
+    import torch
+    if not isinstance(x, torch.Tensor) or not x.is_cuda or x.dtype != torch.float32:
+        raise ValueError("x must be a CUDA float32 tensor")
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    if y is None:
+        y = torch.empty_like(x)
+    if y.shape != x.shape or not y.is_contiguous() or y.dtype != torch.float32 or not y.is_cuda:
+        raise ValueError("y must be a contiguous CUDA float32 tensor of x's shape")
+    with torch.cuda.device(x.device):
+        gelu_ptr(x.data_ptr(), y.data_ptr(), x.numel(), _stream_handle(stream))
+    return y
+
+
+def log_softmax_rows(x, y=None, stream=None):
+    """Row-wise log-softmax, log y = (x - m) - log(s); see :func:`softmax_rows`."""
+    return softmax_rows(x, y, stream, log=True)
+
+
+def _reduce(fn, name, x, out, stream):
     import torch
     M, N, ld = _rows_view(x, "x")
     if out is None:
@@ -178,8 +267,23 @@ def row_sum(x, out=None, stream=None):
     if not out.is_cuda or out.dtype != torch.float32 or out.numel() != M or not out.is_contiguous():
         raise ValueError("out must be a contiguous CUDA float32 tensor of M elements")
     with torch.cuda.device(x.device):
-        row_sum_ptr(x.data_ptr(), out.data_ptr(), M, N, ld, _stream_handle(stream))
+        fn(x.data_ptr(), out.data_ptr(), M, N, ld, _stream_handle(stream))
     return out
+
+
+def row_sum(x, out=None, stream=None):
+    """Sum of each row of a CUDA fp32 ``M x N`` tensor into ``out`` (M floats; allocated if None)."""
+    return _reduce(row_sum_ptr, "row_sum", x, out, stream)
+
+
+def row_max(x, out=None, stream=None):
+    """Max of each row (NaN if the row holds one; -inf for N == 0)."""
+    return _reduce(row_max_ptr, "row_max", x, out, stream)
+
+
+def row_mean(x, out=None, stream=None):
+    """Mean of each row (NaN for N == 0)."""
+    return _reduce(row_mean_ptr, "row_mean", x, out, stream)
 
 
 # ------------------------------------------------------------------- misc ----
@@ -207,6 +311,23 @@ def plan_softmax(M, N, ld=None, vector_ok=True, sm_count=152, smem_optin=232448)
                                            smem_optin, ctypes.byref(p)), "rrs_plan_softmax")
     d = p.as_dict()
     d["path_name"] = PATH_NAMES.get(d["path"], "?")
+    return d
+
+
+def force_cols_path(path: str | int = "auto") -> None:
+    """Force a softmax_cols path for later calls ('auto' restores the planner)."""
+    cp = COLS_PATHS[path] if isinstance(path, str) else int(path)
+    _check(load_library().rrs_force_cols_path(cp), "rrs_force_cols_path")
+
+
+def plan_softmax_cols(M, N, ld=None, vector_ok=True, sm_count=152, smem_optin=232448) -> dict:
+    """The column planner's decision for this shape (pure host logic, no GPU)."""
+    p = Plan()
+    _check(load_library().rrs_plan_softmax_cols(M, N, N if ld is None else ld, int(vector_ok),
+                                                sm_count, smem_optin, ctypes.byref(p)),
+           "rrs_plan_softmax_cols")
+    d = p.as_dict()
+    d["path_name"] = COLS_PATH_NAMES.get(d["path"], "?")
     return d
 
 

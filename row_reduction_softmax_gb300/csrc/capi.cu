@@ -12,6 +12,7 @@
 #include <climits>
 #include <cmath>
 #include <cstring>
+#include <limits>
 #include <map>
 #include <mutex>
 #include <string>
@@ -27,6 +28,7 @@ namespace {
 thread_local std::string g_last_error;
 std::atomic<int> g_force_softmax{RRS_PATH_AUTO};
 std::atomic<int> g_force_sum{RRS_SUM_AUTO};
+std::atomic<int> g_force_cols{RRS_COLS_AUTO};
 std::atomic<int> g_fault{0};
 
 int fail(int status, const std::string& msg) {
@@ -398,6 +400,75 @@ int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_co
   }
 }
 
+// Column softmax.  COLS_CLUSTER: a band of 128 columns per cluster; rows per
+// thread vec (a power of two, at most 16) chosen so that about 8 CTAs share
+// a band, cs = ceil(M / (8 warps x vec)) <= 16 CTAs.  COLS_TWO_PHASE: row
+// chunks sized for about 4 CTAs per SM over all bands.
+enum WorkspaceKindCols { kWsCols = 3 };
+
+bool plan_cols_cluster(int64_t M, int64_t N, rrs_plan* p) {
+  const int64_t warps = cols_threads() / 32;
+  const int64_t vec = std::min<int64_t>(cols_rows_per_thread_max(),
+                                        std::max<int64_t>(1, pow2_ceil(ceil_div(M, warps * 8))));
+  const int64_t cs = ceil_div(M, warps * vec);
+  if (cs > kClusterMax) return false;
+  p->path = RRS_COLS_CLUSTER;
+  p->threads = cols_threads();
+  p->vec = (int32_t)vec;
+  p->cluster = (int32_t)cs;
+  p->grid = ceil_div(N, cols_band()) * cs;
+  p->rows_per_cta = (int32_t)(warps * vec);
+  p->ctas_per_row = cs;
+  p->chunk = ceil_div(M, cs);
+  return true;
+}
+
+void plan_cols_two_phase(int64_t M, int64_t N, int sm_count, rrs_plan* p) {
+  const int64_t bands = ceil_div(N, cols_band());
+  const int64_t want = std::max<int64_t>(1, ceil_div(4 * (int64_t)sm_count, bands));
+  const int64_t chunk = std::max<int64_t>(8, ceil_div(M, want));
+  const int64_t chunks = ceil_div(M, chunk);
+  p->path = RRS_COLS_TWO_PHASE;
+  p->threads = cols_threads();
+  p->grid = bands * chunks;
+  p->ctas_per_row = chunks;
+  p->chunk = chunk;
+  p->rows_per_cta = (int32_t)std::min<int64_t>(chunk, INT_MAX);
+  p->workspace_bytes = chunks * N * 8;
+}
+
+int plan_cols_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_count, int cluster_ok,
+                   int forced, rrs_plan* p) {
+  std::memset(p, 0, sizeof(*p));
+  if (M < 0 || N < 0 || ld < 1 || ld < N || sm_count < 1)
+    return fail(RRS_ERR_INVALID_ARG, "bad shape or device description");
+  p->cluster = 1;
+  p->vector_io = vector_ok ? 1 : 0;
+  if (M == 0 || N == 0) {
+    p->path = (forced == RRS_COLS_AUTO) ? RRS_COLS_TWO_PHASE : forced;
+    return RRS_OK;
+  }
+  const bool cluster_fits = vector_ok && cluster_ok;
+  if (forced == RRS_COLS_AUTO) {
+    if (!(cluster_fits && plan_cols_cluster(M, N, p))) plan_cols_two_phase(M, N, sm_count, p);
+    p->vector_io = vector_ok ? 1 : 0;
+    return RRS_OK;
+  }
+  if (forced == RRS_COLS_CLUSTER) {
+    if (cluster_fits && plan_cols_cluster(M, N, p)) {
+      p->vector_io = 1;
+      return RRS_OK;
+    }
+    return fail(RRS_ERR_UNSUPPORTED, "COLS_CLUSTER needs 16-byte alignment, cluster launch and M <= 2048");
+  }
+  if (forced == RRS_COLS_TWO_PHASE) {
+    plan_cols_two_phase(M, N, sm_count, p);
+    p->vector_io = vector_ok ? 1 : 0;
+    return RRS_OK;
+  }
+  return fail(RRS_ERR_UNSUPPORTED, "column path not available");
+}
+
 int plan_row_sum_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_count,
                       int smem_optin, int forced, rrs_plan* p) {
   std::memset(p, 0, sizeof(*p));
@@ -477,6 +548,12 @@ RRS_API int rrs_force_path(int softmax_path, int sum_path) {
   return RRS_OK;
 }
 
+RRS_API int rrs_force_cols_path(int cols_path) {
+  if (cols_path < RRS_COLS_AUTO || cols_path >= RRS_COLS_COUNT) return RRS_ERR_INVALID_ARG;
+  g_force_cols.store(cols_path);
+  return RRS_OK;
+}
+
 RRS_API int rrs_inject_fault(int kind) {
   if (kind < 0 || kind > 1) return RRS_ERR_INVALID_ARG;
   g_fault.store(kind);
@@ -495,6 +572,13 @@ RRS_API int rrs_plan_row_sum(int64_t M, int64_t N, int64_t ld, int vector_ok_fla
   if (!plan) return RRS_ERR_INVALID_ARG;
   return plan_row_sum_impl(M, N, ld, vector_ok_flag, sm_count, smem_optin, g_force_sum.load(),
                            plan);
+}
+
+RRS_API int rrs_plan_softmax_cols(int64_t M, int64_t N, int64_t ld, int vector_ok_flag,
+                                  int sm_count, int smem_optin, rrs_plan* plan) {
+  if (!plan) return RRS_ERR_INVALID_ARG;
+  (void)smem_optin;
+  return plan_cols_impl(M, N, ld, vector_ok_flag, sm_count, 1, g_force_cols.load(), plan);
 }
 
 RRS_API int rrs_occupancy(int threads, int regs, int sm_regs, int max_warps, int* blocks,
@@ -521,17 +605,21 @@ RRS_API int64_t rrs_waves(int64_t blocks, int64_t slots, int64_t* last_wave, int
   return waves;
 }
 
-RRS_API int softmax_rows(const float* x, float* y, int64_t M, int64_t N, int64_t ld,
-                         void* stream) {
+RRS_API int softmax_rows_ex(const float* x, int64_t ldx, float* y, int64_t ldy, int64_t M,
+                            int64_t N, int flags, void* stream) {
   g_last_error.clear();
-  int64_t extent = 0;
-  int st = check_shape(M, N, ld, &extent);
+  if (flags & ~RRS_LOG_SOFTMAX) return fail(RRS_ERR_INVALID_ARG, "unknown flag bits");
+  int64_t xext = 0, yext = 0;
+  int st = check_shape(M, N, ldx, &xext);
   if (st != RRS_OK) return st;
+  if ((st = check_shape(M, N, ldy, &yext)) != RRS_OK) return st;
   if (M == 0 || N == 0) return RRS_OK;
   if (!x || !y) return fail(RRS_ERR_INVALID_ARG, "null pointer");
   if (reinterpret_cast<uintptr_t>(x) % 4 || reinterpret_cast<uintptr_t>(y) % 4)
     return fail(RRS_ERR_INVALID_ARG, "pointers must be 4-byte aligned");
-  if (overlaps(x, extent * 4, y, extent * 4)) return fail(RRS_ERR_ALIAS, "x and y overlap");
+  // in place (the same matrix, the same stride) is allowed; any other overlap is not
+  const bool in_place = (static_cast<const void*>(x) == static_cast<const void*>(y)) && ldx == ldy;
+  if (!in_place && overlaps(x, xext * 4, y, yext * 4)) return fail(RRS_ERR_ALIAS, "x and y overlap");
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -541,46 +629,114 @@ RRS_API int softmax_rows(const float* x, float* y, int64_t M, int64_t N, int64_t
   DeviceInfo info;
   if ((st = device_info(dev, &info)) != RRS_OK) return st;
 
+  const bool vec = vector_ok(x, y, ldx) && ldy % 4 == 0;
   rrs_plan plan;
-  st = plan_softmax_impl(M, N, ld, vector_ok(x, y, ld) ? 1 : 0, info.sm_count, info.smem_optin,
+  st = plan_softmax_impl(M, N, std::max(ldx, ldy), vec ? 1 : 0, info.sm_count, info.smem_optin,
                          info.cluster_launch, info.coop_launch, g_force_softmax.load(), &plan);
   if (st != RRS_OK) return st;
+  Layout l;
+  l.ldx = ldx;
+  l.ldy = ldy;
+  l.log_out = (flags & RRS_LOG_SOFTMAX) ? 1 : 0;
+  if (l.log_out && plan.path == RRS_PATH_ROW_STAGED)
+    return fail(RRS_ERR_UNSUPPORTED, "ROW_STAGED writes the softmax only");
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   switch (plan.path) {
     case RRS_PATH_ROW_REGS:
-      e = launch_softmax_row_regs(plan, x, y, M, N, ld, s);
+      e = launch_softmax_row_regs(plan, x, y, M, N, l, s);
       break;
     case RRS_PATH_CLUSTER:
-      e = launch_softmax_cluster(plan, x, y, M, N, ld, s);
+      e = launch_softmax_cluster(plan, x, y, M, N, l, s);
       break;
     case RRS_PATH_ROW_STAGED:
-      e = (plan.vec > 0) ? launch_softmax_staged_rows(plan, x, y, M, N, ld, s)
-                         : launch_softmax_staged_long(plan, x, y, M, N, ld, s);
+      e = (plan.vec > 0) ? launch_softmax_staged_rows(plan, x, y, M, N, l, s)
+                         : launch_softmax_staged_long(plan, x, y, M, N, l, s);
       break;
     case RRS_PATH_GRID: {
       void* ws = nullptr;
       uint32_t ticket = 0;
       if ((st = get_workspace(dev, s, kWsGrid, (size_t)plan.workspace_bytes, &ws, &ticket)) != RRS_OK)
         return st;
-      e = launch_softmax_staged_grid(plan, x, y, M, N, ld, ws, ticket, g_fault.load(), s);
+      e = launch_softmax_staged_grid(plan, x, y, M, N, l, ws, ticket, g_fault.load(), s);
       break;
     }
     case RRS_PATH_TWO_PHASE: {
       void* ws = nullptr;
       if ((st = get_workspace(dev, s, kWsTwoPhase, (size_t)plan.workspace_bytes, &ws)) != RRS_OK)
         return st;
-      e = launch_softmax_two_phase(plan, x, y, M, N, ld, ws, s);
+      e = launch_softmax_two_phase(plan, x, y, M, N, l, ws, s);
       break;
     }
     default:
       return fail(RRS_ERR_UNSUPPORTED, "planned path has no launcher");
   }
-  if (e != cudaSuccess) return fail_cuda(e, "softmax_rows launch");
+  if (e != cudaSuccess) return fail_cuda(e, "softmax launch");
   return RRS_OK;
 }
 
-RRS_API int row_sum(const float* x, float* out, int64_t M, int64_t N, int64_t ld, void* stream) {
+RRS_API int softmax_cols(const float* x, int64_t ldx, float* y, int64_t ldy, int64_t M, int64_t N,
+                         int flags, void* stream) {
+  g_last_error.clear();
+  if (flags & ~RRS_LOG_SOFTMAX) return fail(RRS_ERR_INVALID_ARG, "unknown flag bits");
+  int64_t xext = 0, yext = 0;
+  int st = check_shape(M, N, ldx, &xext);
+  if (st != RRS_OK) return st;
+  if ((st = check_shape(M, N, ldy, &yext)) != RRS_OK) return st;
+  if (M == 0 || N == 0) return RRS_OK;
+  if (!x || !y) return fail(RRS_ERR_INVALID_ARG, "null pointer");
+  if (reinterpret_cast<uintptr_t>(x) % 4 || reinterpret_cast<uintptr_t>(y) % 4)
+    return fail(RRS_ERR_INVALID_ARG, "pointers must be 4-byte aligned");
+  const bool in_place = (static_cast<const void*>(x) == static_cast<const void*>(y)) && ldx == ldy;
+  if (!in_place && overlaps(x, xext * 4, y, yext * 4)) return fail(RRS_ERR_ALIAS, "x and y overlap");
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  if ((st = check_device_pointer(x, dev, "x")) != RRS_OK) return st;
+  if ((st = check_device_pointer(y, dev, "y")) != RRS_OK) return st;
+  DeviceInfo info;
+  if ((st = device_info(dev, &info)) != RRS_OK) return st;
+
+  const bool vec = vector_ok(x, y, ldx) && ldy % 4 == 0;
+  rrs_plan plan;
+  st = plan_cols_impl(M, N, std::max(ldx, ldy), vec ? 1 : 0, info.sm_count, info.cluster_launch,
+                      g_force_cols.load(), &plan);
+  if (st != RRS_OK) return st;
+  Layout l;
+  l.ldx = ldx;
+  l.ldy = ldy;
+  l.log_out = (flags & RRS_LOG_SOFTMAX) ? 1 : 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (plan.path == RRS_COLS_CLUSTER) {
+    e = launch_softmax_cols_cluster(plan, x, y, M, N, l, s);
+  } else {
+    void* ws = nullptr;
+    if ((st = get_workspace(dev, s, kWsCols, (size_t)plan.workspace_bytes, &ws)) != RRS_OK) return st;
+    e = launch_softmax_cols_two_phase(plan, x, y, M, N, l, ws, s);
+  }
+  if (e != cudaSuccess) return fail_cuda(e, "softmax_cols launch");
+  return RRS_OK;
+}
+
+RRS_API int softmax_rows(const float* x, float* y, int64_t M, int64_t N, int64_t ld,
+                         void* stream) {
+  return softmax_rows_ex(x, ld, y, ld, M, N, 0, stream);
+}
+
+RRS_API int log_softmax_rows(const float* x, float* y, int64_t M, int64_t N, int64_t ld,
+                             void* stream) {
+  return softmax_rows_ex(x, ld, y, ld, M, N, RRS_LOG_SOFTMAX, stream);
+}
+
+}  // extern "C"
+
+namespace rrs {
+namespace {
+
+// row_sum / row_max / row_mean: one planner and one kernel family (op).
+int row_reduce_impl(int op, const char* name, const float* x, float* out, int64_t M, int64_t N,
+                    int64_t ld, void* stream) {
   g_last_error.clear();
   int64_t extent = 0;
   int st = check_shape(M, N, ld, &extent);
@@ -596,9 +752,12 @@ RRS_API int row_sum(const float* x, float* out, int64_t M, int64_t N, int64_t ld
   if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
   if ((st = check_device_pointer(out, dev, "out")) != RRS_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (N == 0) {
-    e = cudaMemsetAsync(out, 0, (size_t)M * sizeof(float), s);
-    return e == cudaSuccess ? RRS_OK : fail_cuda(e, "cudaMemsetAsync");
+  if (N == 0) {  // the empty row's value: the sum's identity 0, the max's -inf, the mean 0/0
+    const float v = op == kOpSum ? 0.f
+                  : op == kOpMax ? -std::numeric_limits<float>::infinity()
+                                 : std::numeric_limits<float>::quiet_NaN();
+    e = launch_fill(out, M, v, s);
+    return e == cudaSuccess ? RRS_OK : fail_cuda(e, (std::string(name) + " fill").c_str());
   }
   if ((st = check_device_pointer(x, dev, "x")) != RRS_OK) return st;
   DeviceInfo info;
@@ -611,19 +770,59 @@ RRS_API int row_sum(const float* x, float* out, int64_t M, int64_t N, int64_t ld
   if (st != RRS_OK) return st;
   switch (plan.path) {
     case RRS_SUM_ROW:
-      e = launch_row_sum_rows(plan, x, out, M, N, ld, s);
+      e = launch_row_reduce_rows(op, plan, x, out, M, N, ld, s);
       break;
     case RRS_SUM_SPLIT: {
       void* ws = nullptr;
       if ((st = get_workspace(dev, s, kWsRowSum, (size_t)plan.workspace_bytes, &ws)) != RRS_OK)
         return st;
-      e = launch_row_sum_split(plan, x, out, M, N, ld, ws, s);
+      e = launch_row_reduce_split(op, plan, x, out, M, N, ld, ws, s);
       break;
     }
     default:
       return fail(RRS_ERR_UNSUPPORTED, "planned path has no launcher");
   }
-  if (e != cudaSuccess) return fail_cuda(e, "row_sum launch");
+  if (e != cudaSuccess) return fail_cuda(e, (std::string(name) + " launch").c_str());
+  return RRS_OK;
+}
+
+}  // namespace
+}  // namespace rrs
+
+extern "C" {
+
+RRS_API int row_sum(const float* x, float* out, int64_t M, int64_t N, int64_t ld, void* stream) {
+  return row_reduce_impl(kOpSum, "row_sum", x, out, M, N, ld, stream);
+}
+
+RRS_API int row_max(const float* x, float* out, int64_t M, int64_t N, int64_t ld, void* stream) {
+  return row_reduce_impl(kOpMax, "row_max", x, out, M, N, ld, stream);
+}
+
+RRS_API int row_mean(const float* x, float* out, int64_t M, int64_t N, int64_t ld, void* stream) {
+  return row_reduce_impl(kOpMean, "row_mean", x, out, M, N, ld, stream);
+}
+
+RRS_API int gelu(const float* x, float* y, int64_t n, void* stream) {
+  g_last_error.clear();
+  if (n < 0) return fail(RRS_ERR_INVALID_ARG, "n must be >= 0");
+  if (n == 0) return RRS_OK;
+  if (n > INT64_MAX / 8) return fail(RRS_ERR_INVALID_ARG, "extent overflows");
+  if (!x || !y) return fail(RRS_ERR_INVALID_ARG, "null pointer");
+  if (reinterpret_cast<uintptr_t>(x) % 4 || reinterpret_cast<uintptr_t>(y) % 4)
+    return fail(RRS_ERR_INVALID_ARG, "pointers must be 4-byte aligned");
+  if (static_cast<const void*>(x) != static_cast<const void*>(y) && overlaps(x, n * 4, y, n * 4))
+    return fail(RRS_ERR_ALIAS, "x and y overlap");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  int st;
+  if ((st = check_device_pointer(x, dev, "x")) != RRS_OK) return st;
+  if ((st = check_device_pointer(y, dev, "y")) != RRS_OK) return st;
+  DeviceInfo info;
+  if ((st = device_info(dev, &info)) != RRS_OK) return st;
+  e = launch_gelu(x, y, n, info.sm_count, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "gelu launch");
   return RRS_OK;
 }
 

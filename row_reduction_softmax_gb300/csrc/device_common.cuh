@@ -53,6 +53,11 @@ __device__ __forceinline__ float exp_shifted(float v, float m) {
   return exp2_sfu((v - m) * kLog2e);
 }
 
+// One output of log-softmax: log y = (v - m) - log(s), with ls = log(s) of
+// the row (CUDA's logf, once per row).  v = -inf gives -inf (log 0); a NaN
+// row (m or ls NaN) gives NaN, as the softmax does.
+__device__ __forceinline__ float log_softmax_of(float v, float m, float ls) { return (v - m) - ls; }
+
 __device__ __forceinline__ float max4(const float4& v) {
   return max_nan(max_nan(v.x, v.y), max_nan(v.z, v.w));
 }

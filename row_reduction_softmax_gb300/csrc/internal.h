@@ -17,6 +17,14 @@ struct DeviceInfo {
   int coop_launch = 0;      // cooperative launch supported
 };
 
+// Row strides of x and y (elements) and the output form: 0 = softmax,
+// 1 = log-softmax.  x == y with ldx == ldy is an in-place call.
+struct Layout {
+  int64_t ldx = 0;
+  int64_t ldy = 0;
+  int log_out = 0;
+};
+
 // Tuning limits shared by the planner and the launchers.
 constexpr int kRowRegsMaxVec = 16;       // float4 registers per thread (warp-per-row)
 constexpr int kSplitThreads = 256;       // CTA size of the cluster / two-phase kernels
@@ -26,12 +34,14 @@ constexpr int64_t kChunkAlign = 1024;    // two-phase chunk granularity (element
 
 
 // ---- softmax launchers (return the launch's cudaError_t) ----
+// Every softmax launcher takes the strides and output form as a Layout;
+// the staged launchers (ROW_STAGED, GRID) write the softmax only.
 cudaError_t launch_softmax_row_regs(const rrs_plan& p, const float* x, float* y, int64_t M,
-                                    int64_t N, int64_t ld, cudaStream_t s);
+                                    int64_t N, const Layout& l, cudaStream_t s);
 cudaError_t launch_softmax_cluster(const rrs_plan& p, const float* x, float* y, int64_t M,
-                                   int64_t N, int64_t ld, cudaStream_t s);
+                                   int64_t N, const Layout& l, cudaStream_t s);
 cudaError_t launch_softmax_two_phase(const rrs_plan& p, const float* x, float* y, int64_t M,
-                                     int64_t N, int64_t ld, void* workspace, cudaStream_t s);
+                                     int64_t N, const Layout& l, void* workspace, cudaStream_t s);
 
 // Persistent TMA-staged kernels (softmax_staged.cu): ROW_STAGED plans with
 // vec > 0 run staged_rows (rows in registers), vec == 0 run staged_long
@@ -43,23 +53,46 @@ int staged_consumer_warps();
 int grid_threads();
 int grid_partial_threads();
 cudaError_t launch_softmax_staged_rows(const rrs_plan& p, const float* x, float* y, int64_t M,
-                                       int64_t N, int64_t ld, cudaStream_t s);
+                                       int64_t N, const Layout& l, cudaStream_t s);
 cudaError_t launch_softmax_staged_long(const rrs_plan& p, const float* x, float* y, int64_t M,
-                                       int64_t N, int64_t ld, cudaStream_t s);
+                                       int64_t N, const Layout& l, cudaStream_t s);
 // GRID plans: rows split over a cooperative grid of R * C CTAs (one per SM);
 // `workspace` holds 16 bytes per (row, segment) slot, zero-filled when
 // allocated, and `ticket` is unique per launch on that workspace.
 // `fault` != 0 (testing only, rrs_inject_fault): CTA 0 never publishes the
 // partial of its first segment, so its row's waits run out.
 cudaError_t launch_softmax_staged_grid(const rrs_plan& p, const float* x, float* y, int64_t M,
-                                       int64_t N, int64_t ld, void* workspace, uint32_t ticket,
+                                       int64_t N, const Layout& l, void* workspace, uint32_t ticket,
                                        int fault, cudaStream_t s);
 
-// ---- row-sum launchers ----
-cudaError_t launch_row_sum_rows(const rrs_plan& p, const float* x, float* out, int64_t M,
-                                int64_t N, int64_t ld, cudaStream_t s);
-cudaError_t launch_row_sum_split(const rrs_plan& p, const float* x, float* out, int64_t M,
-                                 int64_t N, int64_t ld, void* workspace, cudaStream_t s);
+// ---- column softmax (softmax_cols.cu): COLS_CLUSTER plans carry cluster
+// (CTAs per band) and vec (rows per thread); COLS_TWO_PHASE plans carry
+// ctas_per_row (row chunks) and chunk (rows per chunk), workspace chunks x N
+// (max, sum) pairs.
+int cols_threads();
+int cols_band();
+int cols_rows_per_thread_max();
+cudaError_t launch_softmax_cols_cluster(const rrs_plan& p, const float* x, float* y, int64_t M,
+                                        int64_t N, const Layout& l, cudaStream_t s);
+cudaError_t launch_softmax_cols_two_phase(const rrs_plan& p, const float* x, float* y, int64_t M,
+                                          int64_t N, const Layout& l, void* workspace,
+                                          cudaStream_t s);
+
+// ---- row-reduction launchers (row_sum.cu): op is one of kOp* ----
+constexpr int kOpSum = 0;
+constexpr int kOpMax = 1;
+constexpr int kOpMean = 2;
+cudaError_t launch_row_reduce_rows(int op, const rrs_plan& p, const float* x, float* out,
+                                   int64_t M, int64_t N, int64_t ld, cudaStream_t s);
+cudaError_t launch_row_reduce_split(int op, const rrs_plan& p, const float* x, float* out,
+                                    int64_t M, int64_t N, int64_t ld, void* workspace,
+                                    cudaStream_t s);
+// out[0..M) = v (the result for rows with N == 0).
+cudaError_t launch_fill(float* out, int64_t M, float v, cudaStream_t s);
+
+// ---- elementwise GeLU (gelu.cu) ----
+int gelu_threads();
+cudaError_t launch_gelu(const float* x, float* y, int64_t n, int sm_count, cudaStream_t s);
 
 // ---- device error words (set by kernels whose bounded waits ran out) ----
 cudaError_t read_and_clear_staged_error(cudaStream_t s, unsigned* value);

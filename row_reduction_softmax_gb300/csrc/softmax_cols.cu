@@ -1,0 +1,342 @@
+// Column softmax: y[i, j] = exp(x[i, j] - m_j) / s_j with m_j = max_i x[i, j]
+// and s_j = sum_i exp(x[i, j] - m_j) -- the pages' softmax ("Kernels, Triton,
+// XLA", section "Reductions and tiling") with the reduction taken down each
+// column.  The lecture transcript's question after the softmax kernel asks
+// for it; the answer there is the same kernel with the strides swapped.  A
+// thread per column reading down the rows would touch one float per 128-byte
+// line per warp access -- the uncoalesced pattern of the pages' "memory
+// coalescing" paragraph -- so here a warp reads 128 consecutive columns of a
+// row (one float4 per lane, 512 contiguous bytes) and the reduction runs
+// across warps and CTAs instead of across lanes.
+//
+// COLS_CLUSTER -- a band of 128 columns per CTA group; the M rows are split
+//   over a thread-block cluster of cs CTAs, each CTA's 8 warps hold VEC rows
+//   each in registers.  Per column: max and sum over a thread's rows, then
+//   over the 8 warps (shared memory), then over the cluster's CTAs (DSMEM),
+//   merged with m = max(m_a, m_b), s = s_a e^(m_a - m) + s_b e^(m_b - m).
+//   One read and one write per element.  M <= 16 * 8 * 16 = 2048.
+// COLS_TWO_PHASE -- any M and alignment: kernel 1 writes each (row chunk,
+//   column) online partial to a workspace, kernel 2 merges a column's
+//   partials, re-reads its chunk and writes y (12 bytes per element unless
+//   the re-read hits L2).
+#include <cooperative_groups.h>
+
+#include "device_common.cuh"
+#include "internal.h"
+#include "launch_util.h"
+
+namespace cg = cooperative_groups;
+
+namespace rrs {
+namespace {
+
+constexpr int kCT = 256;           // threads per CTA
+constexpr int kCW = kCT / 32;      // warps per CTA: each owns a set of rows
+constexpr int kBand = 128;         // columns per CTA: 32 lanes x float4
+
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Four consecutive columns j0..j0+3 of one row; lanes past N read `fill`.
+// V4: the row is 16-byte aligned, so the float4 is aligned.
+template <bool V4>
+__device__ __forceinline__ float4 load_cols(const float* row, int64_t j0, int64_t N, float fill) {
+  if (V4 && j0 + 3 < N) return load_stream(reinterpret_cast<const float4*>(row + j0));
+  float4 v;
+  v.x = (j0 + 0 < N) ? load_stream(row + j0 + 0) : fill;
+  v.y = (j0 + 1 < N) ? load_stream(row + j0 + 1) : fill;
+  v.z = (j0 + 2 < N) ? load_stream(row + j0 + 2) : fill;
+  v.w = (j0 + 3 < N) ? load_stream(row + j0 + 3) : fill;
+  return v;
+}
+
+template <bool V4>
+__device__ __forceinline__ void store_cols(float* row, int64_t j0, int64_t N, const float4& v) {
+  if (V4 && j0 + 3 < N) {
+    store_stream(reinterpret_cast<float4*>(row + j0), v);
+    return;
+  }
+  if (j0 + 0 < N) store_stream(row + j0 + 0, v.x);
+  if (j0 + 1 < N) store_stream(row + j0 + 1, v.y);
+  if (j0 + 2 < N) store_stream(row + j0 + 2, v.z);
+  if (j0 + 3 < N) store_stream(row + j0 + 3, v.w);
+}
+
+__device__ __forceinline__ float comp(const float4& v, int c) {
+  return c == 0 ? v.x : (c == 1 ? v.y : (c == 2 ? v.z : v.w));
+}
+
+// ------------------------------------------------------------ COLS_CLUSTER ---
+// Grid: (bands * cs) CTAs in clusters of cs along x; cluster k owns columns
+// [128k, 128k + 128).  Rank r owns rows [r * rseg, min((r + 1) * rseg, M)),
+// rseg = ceil(M / cs) <= kCW * VEC; warp w of the CTA holds rows
+// r * rseg + w + kCW * i, i < VEC.  x, y 16-byte aligned and ldx, ldy
+// multiples of 4 (any N).  log_out != 0 writes (x - m) - log(s).
+template <int VEC>
+__global__ void __launch_bounds__(kCT, 2)
+softmax_cols_cluster_kernel(const float* x, float* y, int64_t M, int64_t N, int64_t ldx,
+                            int64_t ldy, int32_t log_out) {
+  __shared__ float red[kCW][kBand];
+  __shared__ MaxSum part[kBand];   // this CTA's per-column (m_c, s_c), read by its peers
+  __shared__ MaxSum whole[kBand];  // the merged pair of each column
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int cs = (int)cluster.num_blocks();
+  const int rank = (int)cluster.block_rank();
+  const int64_t band = blockIdx.x / cs;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t rseg = (M + cs - 1) / cs;
+  const int64_t r0 = rank * rseg;
+  const int64_t r1 = min(r0 + rseg, M);
+  const int64_t j0 = band * kBand + 4 * lane;
+  const float kNeg = neg_inf();
+  pdl_entry();
+
+  float4 v[VEC];
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) {
+    const int64_t r = r0 + warp + (int64_t)kCW * i;
+    v[i] = (r < r1 && j0 < N) ? load_cols<true>(x + r * ldx, j0, N, kNeg)
+                              : make_float4(kNeg, kNeg, kNeg, kNeg);
+  }
+
+  // per-column max over this thread's rows, then over the CTA's warps
+  float4 m = v[0];
+#pragma unroll
+  for (int i = 1; i < VEC; ++i) {
+    m.x = max_nan(m.x, v[i].x);
+    m.y = max_nan(m.y, v[i].y);
+    m.z = max_nan(m.z, v[i].z);
+    m.w = max_nan(m.w, v[i].w);
+  }
+  reinterpret_cast<float4*>(red[warp])[lane] = m;
+  __syncthreads();
+  if (tid < kBand) {
+    float cm = red[0][tid];
+#pragma unroll
+    for (int w = 1; w < kCW; ++w) cm = max_nan(cm, red[w][tid]);
+    part[tid].m = cm;
+  }
+  __syncthreads();
+  float mc[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) mc[c] = part[4 * lane + c].m;
+
+  // per-column sum of exp(x - m_c); x stays in v for the log form
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) {
+    float4 e;
+    e.x = (mc[0] == kNeg) ? 0.f : exp_shifted(v[i].x, mc[0]);
+    e.y = (mc[1] == kNeg) ? 0.f : exp_shifted(v[i].y, mc[1]);
+    e.z = (mc[2] == kNeg) ? 0.f : exp_shifted(v[i].z, mc[2]);
+    e.w = (mc[3] == kNeg) ? 0.f : exp_shifted(v[i].w, mc[3]);
+    s.x += e.x;
+    s.y += e.y;
+    s.z += e.z;
+    s.w += e.w;
+    if (!log_out) v[i] = e;
+  }
+  __syncthreads();  // every thread has read part[].m
+  reinterpret_cast<float4*>(red[warp])[lane] = s;
+  __syncthreads();
+  if (tid < kBand) {
+    float cs_sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCW; ++w) cs_sum += red[w][tid];
+    part[tid].s = cs_sum;
+  }
+  cluster_arrive_release();  // publish part[] to the cluster
+  cluster_wait_acquire();    // every peer's part[] is visible
+  if (tid < kBand) {
+    MaxSum q{kNeg, 0.f};
+    for (int k = 0; k < cs; ++k) q = merge(q, *cluster.map_shared_rank(&part[tid], k));
+    whole[tid] = q;  // the same ranks in the same order in every CTA
+  }
+  cluster_arrive_relaxed();  // done reading the peers' part[]
+  __syncthreads();
+
+  // per column: the merged max, and either log(s) or e^(m_c - m) / s
+  float wm[4], k4[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const MaxSum w = whole[4 * lane + c];
+    wm[c] = w.m;
+    const bool bad = !(w.s == w.s) || w.m == kNeg;  // NaN / inf / all -inf column
+    k4[c] = log_out ? logf(w.s)
+                    : (bad ? __int_as_float(0x7fc00000)
+                           : (mc[c] == kNeg ? 0.f : exp_shifted(mc[c], w.m) / w.s));
+  }
+#pragma unroll
+  for (int i = 0; i < VEC; ++i) {
+    const int64_t r = r0 + warp + (int64_t)kCW * i;
+    if (r >= r1 || j0 >= N) continue;
+    const float4 o = log_out ? make_float4(log_softmax_of(v[i].x, wm[0], k4[0]),
+                                           log_softmax_of(v[i].y, wm[1], k4[1]),
+                                           log_softmax_of(v[i].z, wm[2], k4[2]),
+                                           log_softmax_of(v[i].w, wm[3], k4[3]))
+                             : make_float4(v[i].x * k4[0], v[i].y * k4[1], v[i].z * k4[2],
+                                           v[i].w * k4[3]);
+    store_cols<true>(y + r * ldy, j0, N, o);
+  }
+  cluster_wait_acquire();  // peers finished reading part[] before this CTA exits
+}
+
+// --------------------------------------------------------- COLS_TWO_PHASE ---
+// Grid: bands x chunks CTAs, CTA (band b, chunk c) = blockIdx.x = c * bands + b.
+// Chunk c holds rows [c * chunk, min((c + 1) * chunk, M)); warp w takes rows
+// w, w + kCW, ... of it.  part[c * N + j] is chunk c's partial of column j.
+template <bool V4>
+__global__ void __launch_bounds__(kCT)
+softmax_cols_partials_kernel(const float* x, MaxSum* __restrict__ part, int64_t M, int64_t N,
+                             int64_t ldx, int64_t chunk, int64_t bands) {
+  __shared__ MaxSum red[kCW][kBand];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t b = blockIdx.x % bands;
+  const int64_t c = blockIdx.x / bands;
+  const int64_t r0 = c * chunk;
+  const int64_t r1 = min(r0 + chunk, M);
+  const int64_t j0 = b * kBand + 4 * lane;
+  const float kNeg = neg_inf();
+  pdl_entry();
+
+  MaxSum p[4] = {{kNeg, 0.f}, {kNeg, 0.f}, {kNeg, 0.f}, {kNeg, 0.f}};
+  if (j0 < N) {
+    for (int64_t r = r0 + warp; r < r1; r += 2 * kCW) {  // two rows in flight
+      const float4 a = load_cols<V4>(x + r * ldx, j0, N, kNeg);
+      const float4 bb = (r + kCW < r1) ? load_cols<V4>(x + (r + kCW) * ldx, j0, N, kNeg)
+                                        : make_float4(kNeg, kNeg, kNeg, kNeg);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float va = comp(a, k), vb = comp(bb, k);
+        rescale_to(p[k], max_nan(va, vb));
+        if (p[k].m != kNeg) p[k].s += exp_shifted(va, p[k].m) + exp_shifted(vb, p[k].m);
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) red[warp][4 * lane + k] = p[k];
+  __syncthreads();
+  if (tid < kBand) {
+    const int64_t j = b * kBand + tid;
+    MaxSum q{kNeg, 0.f};
+#pragma unroll
+    for (int w = 0; w < kCW; ++w) q = merge(q, red[w][tid]);
+    if (j < N) part[c * N + j] = q;
+  }
+}
+
+// Each CTA merges, for its 128 columns, the partials of all chunks in chunk
+// order (so every CTA of a band gets the same pair), then re-reads its rows
+// and writes y.  Every element is read and then written by one thread, so
+// x == y (in place) is safe.
+template <bool V4>
+__global__ void __launch_bounds__(kCT)
+softmax_cols_finalize_kernel(const float* x, float* y, const MaxSum* __restrict__ part, int64_t M,
+                             int64_t N, int64_t ldx, int64_t ldy, int64_t chunk, int64_t chunks,
+                             int64_t bands, int32_t log_out) {
+  __shared__ MaxSum whole[kBand];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t b = blockIdx.x % bands;
+  const int64_t c = blockIdx.x / bands;
+  const int64_t r0 = c * chunk;
+  const int64_t r1 = min(r0 + chunk, M);
+  const int64_t j0 = b * kBand + 4 * lane;
+  const float kNeg = neg_inf();
+  pdl_entry();
+  if (tid < kBand) {
+    const int64_t j = b * kBand + tid;
+    MaxSum q{kNeg, 0.f};
+    if (j < N)
+      for (int64_t k = 0; k < chunks; ++k) q = merge(q, part[k * N + j]);
+    whole[tid] = q;
+  }
+  __syncthreads();
+  if (j0 >= N) return;
+  float m[4], inv[4], ls[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const MaxSum w = whole[4 * lane + k];
+    m[k] = w.m;
+    inv[k] = 1.0f / w.s;
+    ls[k] = logf(w.s);
+  }
+  for (int64_t r = r0 + warp; r < r1; r += kCW) {
+    const float4 a = load_cols<V4>(x + r * ldx, j0, N, 0.f);
+    float4 o;
+    if (log_out) {
+      o = make_float4(log_softmax_of(a.x, m[0], ls[0]), log_softmax_of(a.y, m[1], ls[1]),
+                      log_softmax_of(a.z, m[2], ls[2]), log_softmax_of(a.w, m[3], ls[3]));
+    } else {
+      o = make_float4(exp_shifted(a.x, m[0]) * inv[0], exp_shifted(a.y, m[1]) * inv[1],
+                      exp_shifted(a.z, m[2]) * inv[2], exp_shifted(a.w, m[3]) * inv[3]);
+    }
+    store_cols<V4>(y + r * ldy, j0, N, o);
+  }
+}
+
+template <int VEC>
+cudaError_t launch_cols_cluster_vec(const rrs_plan& p, const float* x, float* y, int64_t M,
+                                    int64_t N, const Layout& l, cudaStream_t s) {
+  auto kern = softmax_cols_cluster_kernel<VEC>;
+  if (p.cluster > 8) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  return launch_pdl(kern, dim3((unsigned)p.grid), dim3(kCT), 0, s, p.cluster, x, y, M, N, l.ldx,
+                    l.ldy, (int32_t)l.log_out);
+}
+
+}  // namespace
+
+int cols_threads() { return kCT; }
+int cols_band() { return kBand; }
+int cols_rows_per_thread_max() { return 16; }
+
+cudaError_t launch_softmax_cols_cluster(const rrs_plan& p, const float* x, float* y, int64_t M,
+                                        int64_t N, const Layout& l, cudaStream_t s) {
+  if (p.threads != kCT) return cudaErrorInvalidConfiguration;
+  switch (p.vec) {
+    case 1: return launch_cols_cluster_vec<1>(p, x, y, M, N, l, s);
+    case 2: return launch_cols_cluster_vec<2>(p, x, y, M, N, l, s);
+    case 4: return launch_cols_cluster_vec<4>(p, x, y, M, N, l, s);
+    case 8: return launch_cols_cluster_vec<8>(p, x, y, M, N, l, s);
+    case 16: return launch_cols_cluster_vec<16>(p, x, y, M, N, l, s);
+    default: return cudaErrorInvalidConfiguration;
+  }
+}
+
+cudaError_t launch_softmax_cols_two_phase(const rrs_plan& p, const float* x, float* y, int64_t M,
+                                          int64_t N, const Layout& l, void* workspace,
+                                          cudaStream_t s) {
+  if (p.threads != kCT) return cudaErrorInvalidConfiguration;
+  MaxSum* part = static_cast<MaxSum*>(workspace);
+  const int64_t bands = (N + kBand - 1) / kBand;
+  const int64_t chunks = p.ctas_per_row;  // row chunks
+  const dim3 grid((unsigned)(bands * chunks)), block(kCT);
+  const int32_t lo = (int32_t)l.log_out;
+  cudaError_t e;
+  if (p.vector_io) {
+    e = launch_pdl(softmax_cols_partials_kernel<true>, grid, block, 0, s, 0, x, part, M, N, l.ldx,
+                   p.chunk, bands);
+    if (e == cudaSuccess)
+      e = launch_pdl(softmax_cols_finalize_kernel<true>, grid, block, 0, s, 0, x, y,
+                     static_cast<const MaxSum*>(part), M, N, l.ldx, l.ldy, p.chunk, chunks, bands, lo);
+  } else {
+    e = launch_pdl(softmax_cols_partials_kernel<false>, grid, block, 0, s, 0, x, part, M, N, l.ldx,
+                   p.chunk, bands);
+    if (e == cudaSuccess)
+      e = launch_pdl(softmax_cols_finalize_kernel<false>, grid, block, 0, s, 0, x, y,
+                     static_cast<const MaxSum*>(part), M, N, l.ldx, l.ldy, p.chunk, chunks, bands, lo);
+  }
+  return e;
+}
+
+}  // namespace rrs

@@ -128,7 +128,10 @@ extern "C" RRS_API int softmax_rows_noalloc(const float* x, float* y, int64_t M,
   // last call's partials.  Nothing in it needs to start at zero: the first
   // kernel writes every slot the second kernel reads.  Two calls whose
   // kernels overlap on the GPU (other streams, other host threads) race on it.
-  e = launch_softmax_two_phase(plan, x, y, M, N, ld, d.scratch, static_cast<cudaStream_t>(stream));
+  Layout l;
+  l.ldx = ld;
+  l.ldy = ld;
+  e = launch_softmax_two_phase(plan, x, y, M, N, l, d.scratch, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return RRS_ERR_CUDA;
   return RRS_OK;
 }

@@ -47,12 +47,14 @@ __device__ __forceinline__ float group_sum(float v, float* red, int gw, int lane
 template <int GW>
 __host__ __device__ constexpr int threads_for() { return (32 * GW < 128) ? 128 : 32 * GW; }
 
-// x, y: 16-byte aligned, ld % 4 == 0.  Row r is owned by group
-// (blockIdx.x * groups + group), striding by gridDim.x * groups.
+// x, y: 16-byte aligned, ldx % 4 == 0, ldy % 4 == 0.  Row r is owned by
+// group (blockIdx.x * groups + group), striding by gridDim.x * groups.
+// log_out != 0 writes log y = (x - m) - log(s) instead of y.  x == y (same
+// stride) is safe: a group reads its whole row before writing it.
 template <int VEC, int GW>
 __global__ void __launch_bounds__(threads_for<GW>())
-softmax_row_regs_kernel(const float* __restrict__ x, float* __restrict__ y, int64_t M, int32_t N,
-                        int64_t ld) {
+softmax_row_regs_kernel(const float* x, float* y, int64_t M, int32_t N, int64_t ldx, int64_t ldy,
+                        int32_t log_out) {
   constexpr int kThreads = threads_for<GW>();
   constexpr int kGroups = kThreads / (32 * GW);
   constexpr int kGT = 32 * GW;  // threads per group
@@ -75,8 +77,8 @@ softmax_row_regs_kernel(const float* __restrict__ x, float* __restrict__ y, int6
 
   for (int64_t row = (int64_t)blockIdx.x * kGroups + group; row < M;
        row += (int64_t)gridDim.x * kGroups) {
-    const float* xr = x + row * ld;
-    float* yr = y + row * ld;
+    const float* xr = x + row * ldx;
+    float* yr = y + row * ldy;
     const float4* xr4 = reinterpret_cast<const float4*>(xr);
     float4* yr4 = reinterpret_cast<float4*>(yr);
 
@@ -93,6 +95,29 @@ softmax_row_regs_kernel(const float* __restrict__ x, float* __restrict__ y, int6
 #pragma unroll
     for (int i = 0; i < VEC; ++i) m = max_nan(m, max4(v[i]));
     m = group_max<GW>(m, gm, gw, lane, bar_id);
+
+    if (log_out) {
+      // row sum of exp(x - m) with x kept, then log y = (x - m) - log(s)
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) {
+        s += (exp_shifted(v[i].x, m) + exp_shifted(v[i].y, m)) +
+             (exp_shifted(v[i].z, m) + exp_shifted(v[i].w, m));
+      }
+      s += exp_shifted(t, m);
+      s = group_sum<GW>(s, gs, gw, lane, bar_id);
+      const float ls = logf(s);
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) {
+        const int c = i * kGT + gt;
+        if (c < n4) {
+          store_stream(yr4 + c, make_float4(log_softmax_of(v[i].x, m, ls), log_softmax_of(v[i].y, m, ls),
+                                            log_softmax_of(v[i].z, m, ls), log_softmax_of(v[i].w, m, ls)));
+        }
+      }
+      if (gt < rem) store_stream(yr + 4 * n4 + gt, log_softmax_of(t, m, ls));
+      continue;
+    }
 
     // (2)+(3) subtract and exponentiate in place, (4) row sum
     float s = 0.f;
@@ -123,21 +148,21 @@ softmax_row_regs_kernel(const float* __restrict__ x, float* __restrict__ y, int6
 
 template <int VEC, int GW>
 cudaError_t launch_rr(const rrs_plan& p, const float* x, float* y, int64_t M, int64_t N,
-                      int64_t ld, cudaStream_t s) {
+                      const Layout& l, cudaStream_t s) {
   constexpr int kThreads = threads_for<GW>();
   if (p.threads != kThreads) return cudaErrorInvalidConfiguration;
   return launch_pdl(softmax_row_regs_kernel<VEC, GW>, dim3((unsigned)p.grid), dim3(kThreads), 0, s,
-                    0, x, y, M, (int32_t)N, ld);
+                    0, x, y, M, (int32_t)N, l.ldx, l.ldy, (int32_t)l.log_out);
 }
 
 }  // namespace
 
 cudaError_t launch_softmax_row_regs(const rrs_plan& p, const float* x, float* y, int64_t M,
-                                    int64_t N, int64_t ld, cudaStream_t s) {
+                                    int64_t N, const Layout& l, cudaStream_t s) {
   const int gw = p.warps_per_row;
   const int vec = p.vec;
 #define RRS_RR(V, G) \
-  if (vec == V && gw == G) return launch_rr<V, G>(p, x, y, M, N, ld, s);
+  if (vec == V && gw == G) return launch_rr<V, G>(p, x, y, M, N, l, s);
   RRS_RR(1, 1)
   RRS_RR(2, 1)
   RRS_RR(4, 1)

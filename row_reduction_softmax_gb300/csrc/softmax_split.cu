@@ -77,11 +77,13 @@ __device__ __forceinline__ void cluster_wait_acquire() {
 // Grid: clusters of `cs` CTAs along x; cluster k owns rows k, k + nclusters, ...
 // Rank r of a cluster owns float4 columns [r*seg4, min((r+1)*seg4, n4)) of the
 // row, seg4 = ceil(n4 / cs) <= VEC * kT; the last rank also owns the N % 4
-// scalar tail.  x, y 16-byte aligned, ld % 4 == 0.
-template <int VEC>
+// scalar tail.  x, y 16-byte aligned, ldx % 4 == 0, ldy % 4 == 0.
+// LOG writes log y = (x - m) - log(s) (a template parameter, so the softmax
+// instantiation keeps the register count that lets 4 CTAs share an SM).  In
+// place (x == y) is safe: a CTA reads its whole segment before writing it.
+template <int VEC, bool LOG>
 __global__ void __launch_bounds__(kT)
-softmax_cluster_kernel(const float* __restrict__ x, float* __restrict__ y, int64_t M, int32_t N,
-                       int64_t ld) {
+softmax_cluster_kernel(const float* x, float* y, int64_t M, int32_t N, int64_t ldx, int64_t ldy) {
   __shared__ float red_m[kW];
   __shared__ float red_s[kW];
   __shared__ MaxSum part;   // this CTA's (m_c, s_c), read by its peers
@@ -105,8 +107,8 @@ softmax_cluster_kernel(const float* __restrict__ x, float* __restrict__ y, int64
   pdl_entry();
 
   for (int64_t row = cluster_id; row < M; row += nclusters) {
-    const float* xr = x + row * ld;
-    float* yr = y + row * ld;
+    const float* xr = x + row * ldx;
+    float* yr = y + row * ldy;
     const float4* xr4 = reinterpret_cast<const float4*>(xr);
     float4* yr4 = reinterpret_cast<float4*>(yr);
 
@@ -125,16 +127,27 @@ softmax_cluster_kernel(const float* __restrict__ x, float* __restrict__ y, int64
     const bool empty = (mc == kNeg);  // segment holds only -inf (or nothing)
 
     float sc = 0.f;
+    if constexpr (LOG) {  // keep x for the log form
+      if (!empty) {
 #pragma unroll
-    for (int i = 0; i < VEC; ++i) {
-      v[i].x = empty ? 0.f : exp_shifted(v[i].x, mc);
-      v[i].y = empty ? 0.f : exp_shifted(v[i].y, mc);
-      v[i].z = empty ? 0.f : exp_shifted(v[i].z, mc);
-      v[i].w = empty ? 0.f : exp_shifted(v[i].w, mc);
-      sc += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+        for (int i = 0; i < VEC; ++i) {
+          sc += (exp_shifted(v[i].x, mc) + exp_shifted(v[i].y, mc)) +
+                (exp_shifted(v[i].z, mc) + exp_shifted(v[i].w, mc));
+        }
+        sc += exp_shifted(t, mc);
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) {
+        v[i].x = empty ? 0.f : exp_shifted(v[i].x, mc);
+        v[i].y = empty ? 0.f : exp_shifted(v[i].y, mc);
+        v[i].z = empty ? 0.f : exp_shifted(v[i].z, mc);
+        v[i].w = empty ? 0.f : exp_shifted(v[i].w, mc);
+        sc += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+      }
+      t = empty ? 0.f : exp_shifted(t, mc);
+      sc += t;
     }
-    t = empty ? 0.f : exp_shifted(t, mc);
-    sc += t;
     sc = cta_sum(sc, red_s);
 
     if (tid == 0) part = MaxSum{mc, sc};
@@ -150,19 +163,31 @@ softmax_cluster_kernel(const float* __restrict__ x, float* __restrict__ y, int64
     cluster_arrive_relaxed();  // done reading the peers' `part`
     __syncthreads();
     const MaxSum w = whole;
-    const bool bad = !(w.s == w.s) || w.m == kNeg;  // NaN / inf / all -inf row
-    const float scale = bad ? __int_as_float(0x7fc00000)
-                            : (empty ? 0.f : exp_shifted(mc, w.m) / w.s);
-
+    if constexpr (LOG) {
+      const float ls = logf(w.s);
 #pragma unroll
-    for (int i = 0; i < VEC; ++i) {
-      const int c = b4 + i * kT + tid;
-      if (c < e4) {
-        store_stream(yr4 + c,
-                     make_float4(v[i].x * scale, v[i].y * scale, v[i].z * scale, v[i].w * scale));
+      for (int i = 0; i < VEC; ++i) {
+        const int c = b4 + i * kT + tid;
+        if (c < e4) {
+          store_stream(yr4 + c, make_float4(log_softmax_of(v[i].x, w.m, ls), log_softmax_of(v[i].y, w.m, ls),
+                                            log_softmax_of(v[i].z, w.m, ls), log_softmax_of(v[i].w, w.m, ls)));
+        }
       }
+      if (has_tail) store_stream(yr + 4 * n4 + tid, log_softmax_of(t, w.m, ls));
+    } else {
+      const bool bad = !(w.s == w.s) || w.m == kNeg;  // NaN / inf / all -inf row
+      const float scale = bad ? __int_as_float(0x7fc00000)
+                              : (empty ? 0.f : exp_shifted(mc, w.m) / w.s);
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) {
+        const int c = b4 + i * kT + tid;
+        if (c < e4) {
+          store_stream(yr4 + c,
+                       make_float4(v[i].x * scale, v[i].y * scale, v[i].z * scale, v[i].w * scale));
+        }
+      }
+      if (has_tail) store_stream(yr + 4 * n4 + tid, t * scale);
     }
-    if (has_tail) store_stream(yr + 4 * n4 + tid, t * scale);
     cluster_wait_acquire();  // peers finished reading `part` before it is reused / freed
   }
 }
@@ -213,8 +238,8 @@ __device__ __forceinline__ MaxSum chunk_partial(const float* __restrict__ xr, in
 
 template <bool V4>
 __global__ void __launch_bounds__(kT)
-softmax_partials_kernel(const float* __restrict__ x, MaxSum* __restrict__ part, int64_t M,
-                        int64_t N, int64_t ld, int64_t chunk, int64_t C) {
+softmax_partials_kernel(const float* x, MaxSum* __restrict__ part, int64_t M, int64_t N,
+                        int64_t ldx, int64_t chunk, int64_t C) {
   __shared__ MaxSum red[kW];
   const int64_t work = M * C;
   pdl_entry();
@@ -223,18 +248,20 @@ softmax_partials_kernel(const float* __restrict__ x, MaxSum* __restrict__ part, 
     const int64_t c = w - row * C;
     const int64_t b = c * chunk;
     const int64_t e = min(b + chunk, N);
-    MaxSum p = chunk_partial<V4>(x + row * ld, b, e, N);
+    MaxSum p = chunk_partial<V4>(x + row * ldx, b, e, N);
     p = cta_merge(p, red);
     if (threadIdx.x == 0) part[w] = p;
     __syncthreads();
   }
 }
 
+// Each thread reads an element and then writes the same element, so x == y
+// (in place) is safe.  log_out != 0 writes log y = (x - m) - log(s).
 template <bool V4>
 __global__ void __launch_bounds__(kT)
-softmax_finalize_kernel(const float* __restrict__ x, float* __restrict__ y,
-                        const MaxSum* __restrict__ part, int64_t M, int64_t N, int64_t ld,
-                        int64_t chunk, int64_t C) {
+softmax_finalize_kernel(const float* x, float* y, const MaxSum* __restrict__ part, int64_t M,
+                        int64_t N, int64_t ldx, int64_t ldy, int64_t chunk, int64_t C,
+                        int32_t log_out) {
   __shared__ MaxSum red[kW];
   const int64_t work = M * C;
   const int tid = threadIdx.x;
@@ -248,11 +275,12 @@ softmax_finalize_kernel(const float* __restrict__ x, float* __restrict__ y,
     q = cta_merge(q, red);
     const float m = q.m;
     const float inv = 1.0f / q.s;
+    const float ls = logf(q.s);
 
     const int64_t b = c * chunk;
     const int64_t e = min(b + chunk, N);
-    const float* xr = x + row * ld;
-    float* yr = y + row * ld;
+    const float* xr = x + row * ldx;
+    float* yr = y + row * ldy;
     int64_t scalar_from = b;
     if constexpr (V4) {
       const int64_t e4 = ((e == N) ? (N & ~int64_t(3)) : e) >> 2;
@@ -269,62 +297,73 @@ softmax_finalize_kernel(const float* __restrict__ x, float* __restrict__ y,
         for (int u = 0; u < kUnroll; ++u) {
           const int64_t idx = k + (int64_t)u * kT;
           if (idx < e4) {
-            store_stream(y4 + idx, make_float4(exp_shifted(a[u].x, m) * inv,
-                                               exp_shifted(a[u].y, m) * inv,
-                                               exp_shifted(a[u].z, m) * inv,
-                                               exp_shifted(a[u].w, m) * inv));
+            store_stream(y4 + idx, log_out ? make_float4(log_softmax_of(a[u].x, m, ls),
+                                                         log_softmax_of(a[u].y, m, ls),
+                                                         log_softmax_of(a[u].z, m, ls),
+                                                         log_softmax_of(a[u].w, m, ls))
+                                           : make_float4(exp_shifted(a[u].x, m) * inv,
+                                                         exp_shifted(a[u].y, m) * inv,
+                                                         exp_shifted(a[u].z, m) * inv,
+                                                         exp_shifted(a[u].w, m) * inv));
           }
         }
       }
       scalar_from = e4 << 2;
     }
-    for (int64_t j = scalar_from + tid; j < e; j += kT) yr[j] = exp_shifted(xr[j], m) * inv;
+    for (int64_t j = scalar_from + tid; j < e; j += kT) {
+      const float v = xr[j];
+      yr[j] = log_out ? log_softmax_of(v, m, ls) : exp_shifted(v, m) * inv;
+    }
     __syncthreads();
   }
 }
 
-template <int VEC>
+template <int VEC, bool LOG>
 cudaError_t launch_cluster_vec(const rrs_plan& p, const float* x, float* y, int64_t M, int64_t N,
-                               int64_t ld, cudaStream_t s) {
-  auto kern = softmax_cluster_kernel<VEC>;
+                               const Layout& l, cudaStream_t s) {
+  auto kern = softmax_cluster_kernel<VEC, LOG>;
   if (p.cluster > 8) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
   }
   return launch_pdl(kern, dim3((unsigned)p.grid), dim3(kT), 0, s, p.cluster, x, y, M, (int32_t)N,
-                    ld);
+                    l.ldx, l.ldy);
 }
 
 }  // namespace
 
 cudaError_t launch_softmax_cluster(const rrs_plan& p, const float* x, float* y, int64_t M,
-                                   int64_t N, int64_t ld, cudaStream_t s) {
+                                   int64_t N, const Layout& l, cudaStream_t s) {
   if (p.threads != kT) return cudaErrorInvalidConfiguration;
+  const bool lg = l.log_out != 0;
   switch (p.vec) {
-    case 4: return launch_cluster_vec<4>(p, x, y, M, N, ld, s);
-    case 8: return launch_cluster_vec<8>(p, x, y, M, N, ld, s);
+    case 4: return lg ? launch_cluster_vec<4, true>(p, x, y, M, N, l, s)
+                      : launch_cluster_vec<4, false>(p, x, y, M, N, l, s);
+    case 8: return lg ? launch_cluster_vec<8, true>(p, x, y, M, N, l, s)
+                      : launch_cluster_vec<8, false>(p, x, y, M, N, l, s);
     default: return cudaErrorInvalidConfiguration;
   }
 }
 
 cudaError_t launch_softmax_two_phase(const rrs_plan& p, const float* x, float* y, int64_t M,
-                                     int64_t N, int64_t ld, void* workspace, cudaStream_t s) {
+                                     int64_t N, const Layout& l, void* workspace, cudaStream_t s) {
   if (p.threads != kT) return cudaErrorInvalidConfiguration;
   MaxSum* part = static_cast<MaxSum*>(workspace);
   const dim3 grid((unsigned)p.grid), block(kT);
+  const int32_t lo = (int32_t)l.log_out;
   cudaError_t e;
   if (p.vector_io) {
-    e = launch_pdl(softmax_partials_kernel<true>, grid, block, 0, s, 0, x, part, M, N, ld, p.chunk,
-                   p.ctas_per_row);
+    e = launch_pdl(softmax_partials_kernel<true>, grid, block, 0, s, 0, x, part, M, N, l.ldx,
+                   p.chunk, p.ctas_per_row);
     if (e == cudaSuccess)
-      e = launch_pdl(softmax_finalize_kernel<true>, grid, block, 0, s, 0, x, y, part, M, N, ld,
-                     p.chunk, p.ctas_per_row);
+      e = launch_pdl(softmax_finalize_kernel<true>, grid, block, 0, s, 0, x, y,
+                     static_cast<const MaxSum*>(part), M, N, l.ldx, l.ldy, p.chunk, p.ctas_per_row, lo);
   } else {
-    e = launch_pdl(softmax_partials_kernel<false>, grid, block, 0, s, 0, x, part, M, N, ld, p.chunk,
-                   p.ctas_per_row);
+    e = launch_pdl(softmax_partials_kernel<false>, grid, block, 0, s, 0, x, part, M, N, l.ldx,
+                   p.chunk, p.ctas_per_row);
     if (e == cudaSuccess)
-      e = launch_pdl(softmax_finalize_kernel<false>, grid, block, 0, s, 0, x, y, part, M, N, ld,
-                     p.chunk, p.ctas_per_row);
+      e = launch_pdl(softmax_finalize_kernel<false>, grid, block, 0, s, 0, x, y,
+                     static_cast<const MaxSum*>(part), M, N, l.ldx, l.ldy, p.chunk, p.ctas_per_row, lo);
   }
   return e;
 }

@@ -146,11 +146,12 @@ __device__ __forceinline__ float group_sum(float v, float* red, int g, int gw, i
 // Rows b, b + G, b + 2G, ... of CTA b (G = gridDim.x); local row j sits in
 // stage j % NS, is issued by producer lane j % kGroups and consumed by warp
 // group j % kGroups (NS % kGroups == 0).  Needs N % 4 == 0, 16-byte aligned
-// x and y, ld % 4 == 0, N <= 32 * GW * VEC * 4.
+// x and y, ldx % 4 == 0, ldy % 4 == 0, N <= 32 * GW * VEC * 4.  x == y (in
+// place) is safe: copies only ever read rows that are not yet written.
 template <int VEC, int GW>
 __global__ void __launch_bounds__(kThreads, 1)
-softmax_staged_rows_kernel(const float* __restrict__ x, float* __restrict__ y, int64_t M,
-                           int32_t N, int64_t ld, int32_t NS, int32_t stage_stride) {
+softmax_staged_rows_kernel(const float* x, float* y, int64_t M, int32_t N, int64_t ldx,
+                           int64_t ldy, int32_t NS, int32_t stage_stride) {
   constexpr int kGroups = kConsumerWarps / GW;
   constexpr int kGT = 32 * GW;
   extern __shared__ __align__(1024) unsigned char smem[];
@@ -188,7 +189,7 @@ softmax_staged_rows_kernel(const float* __restrict__ x, float* __restrict__ y, i
           break;
         }
         mbar_arrive_expect_tx(&full[s], row_bytes);
-        bulk_load(stages + (size_t)s * stage_stride, x + (b + j * G) * ld, row_bytes, &full[s], pol);
+        bulk_load(stages + (size_t)s * stage_stride, x + (b + j * G) * ldx, row_bytes, &full[s], pol);
       }
       if (!ok) drain_copies(full, j, NS);
     }
@@ -234,7 +235,7 @@ softmax_staged_rows_kernel(const float* __restrict__ x, float* __restrict__ y, i
     sum = group_sum<GW>(sum, red_s, g, gw, lane);
     const float inv = 1.0f / sum;
 
-    float4* yr4 = reinterpret_cast<float4*>(y + (b + j * G) * ld);
+    float4* yr4 = reinterpret_cast<float4*>(y + (b + j * G) * ldy);
 #pragma unroll
     for (int i = 0; i < VEC; ++i) {
       const int c = i * kGT + gt;
@@ -271,8 +272,8 @@ constexpr int kLongUnroll = 4;
 // consumer thread goes through every row in order, so each stage's uses are
 // ordered by the same threads.
 __global__ void __launch_bounds__(kThreads, 1)
-softmax_staged_long_kernel(const float* __restrict__ x, float* __restrict__ y, int64_t M,
-                           int64_t N, int64_t ld, int32_t tile_floats, int32_t NS) {
+softmax_staged_long_kernel(const float* x, float* y, int64_t M, int64_t N, int64_t ldx,
+                           int64_t ldy, int32_t tile_floats, int32_t NS) {
   extern __shared__ __align__(1024) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kFullOff);
   uint64_t* empty = reinterpret_cast<uint64_t*>(smem + kEmptyOff);
@@ -302,7 +303,7 @@ softmax_staged_long_kernel(const float* __restrict__ x, float* __restrict__ y, i
       int64_t q = 0;
       bool ok = true;
       for (int64_t k = 0; k < items && ok; ++k) {
-        const float* src = x + (b + k * G) * ld;
+        const float* src = x + (b + k * G) * ldx;
         for (int t = 0; t < n_sub; ++t, ++q) {
           const int s = (int)(q % NS);
           if (q >= NS && !wait_bounded(&empty[s], (uint32_t)(((q / NS) - 1) & 1), abort_flag)) {
@@ -371,7 +372,7 @@ softmax_staged_long_kernel(const float* __restrict__ x, float* __restrict__ y, i
 
     // pass 3: normalise from shared memory, store, release each sub-tile
     const float inv = 1.0f / sum;
-    float* yr = y + row * ld;
+    float* yr = y + row * ldy;
     for (int t = 0; t < n_sub; ++t) {
       const int s = (int)((q + t) % NS);
       const float4* sm = reinterpret_cast<const float4*>(stages + (size_t)s * stage_bytes);
@@ -437,10 +438,10 @@ constexpr int kMaxSlotsPerLane = 5;                 // C <= 160: a row's slots o
 
 template <int VEC, int LEAD>
 __global__ void __launch_bounds__(kGThreads, 1)
-softmax_staged_grid_kernel(const float* __restrict__ x, float* __restrict__ y, int64_t M,
-                           int64_t N, int64_t ld, int64_t seg, int32_t C, int32_t R, int32_t NS,
+softmax_staged_grid_kernel(const float* x, float* y, int64_t M, int64_t N, int64_t ldx,
+                           int64_t ldy, int64_t seg, int32_t C, int32_t R, int32_t NS,
                            int32_t stage_stride, uint64_t* __restrict__ slots, uint32_t ticket,
-                           int32_t fault) {
+                           int32_t fault, int32_t log_out) {
   extern __shared__ __align__(1024) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kFullOff);
   uint64_t* empty = reinterpret_cast<uint64_t*>(smem + kEmptyOff);
@@ -485,7 +486,7 @@ softmax_staged_grid_kernel(const float* __restrict__ x, float* __restrict__ y, i
           break;
         }
         mbar_arrive_expect_tx(&full[st], bytes);
-        bulk_load(stages + (size_t)st * stage_stride, x + (row0 + k * R) * ld + seg_begin, bytes,
+        bulk_load(stages + (size_t)st * stage_stride, x + (row0 + k * R) * ldx + seg_begin, bytes,
                   &full[st], pol);
       }
       if (!ok) drain_copies(full, k, NS);
@@ -521,13 +522,23 @@ softmax_staged_grid_kernel(const float* __restrict__ x, float* __restrict__ y, i
     m = warp_max((lane >= 1 && lane < kGConsumerWarps) ? red_m[lane] : kNeg);
     const bool none = (m == kNeg);  // only -inf (or nothing) in this segment
     float sum = 0.f;
+    if (log_out) {  // keep x for the log form
+      if (!none) {
 #pragma unroll
-    for (int i = 0; i < VEC; ++i) {
-      v[i].x = none ? 0.f : exp_shifted(v[i].x, m);
-      v[i].y = none ? 0.f : exp_shifted(v[i].y, m);
-      v[i].z = none ? 0.f : exp_shifted(v[i].z, m);
-      v[i].w = none ? 0.f : exp_shifted(v[i].w, m);
-      sum += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+        for (int i = 0; i < VEC; ++i) {
+          sum += (exp_shifted(v[i].x, m) + exp_shifted(v[i].y, m)) +
+                 (exp_shifted(v[i].z, m) + exp_shifted(v[i].w, m));
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) {
+        v[i].x = none ? 0.f : exp_shifted(v[i].x, m);
+        v[i].y = none ? 0.f : exp_shifted(v[i].y, m);
+        v[i].z = none ? 0.f : exp_shifted(v[i].z, m);
+        v[i].w = none ? 0.f : exp_shifted(v[i].w, m);
+        sum += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+      }
     }
     sum = warp_sum(sum);
     if (lane == 0) red_s[warp] = sum;
@@ -611,10 +622,24 @@ softmax_staged_grid_kernel(const float* __restrict__ x, float* __restrict__ y, i
     const MaxSum w = *whole;
     named_barrier(kConsumerBar, kGConsumers);
     if (failed) return false;
+    float4* y4 = reinterpret_cast<float4*>(y + (row0 + k * R) * ldy + seg_begin);
+    if (log_out) {
+      const float ls = logf(w.s);
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) {
+        const int idx = ptid + i * kPartialThreads;
+        if (idx < nf4) {
+          store_stream(y4 + idx, make_float4(log_softmax_of(cur[i].x, w.m, ls),
+                                             log_softmax_of(cur[i].y, w.m, ls),
+                                             log_softmax_of(cur[i].z, w.m, ls),
+                                             log_softmax_of(cur[i].w, w.m, ls)));
+        }
+      }
+      return true;
+    }
     const bool bad = !(w.s == w.s) || w.m == kNeg;  // NaN / inf / all -inf row
     const float scale =
         bad ? __int_as_float(0x7fc00000) : (mtc == kNeg ? 0.f : exp_shifted(mtc, w.m) / w.s);
-    float4* y4 = reinterpret_cast<float4*>(y + (row0 + k * R) * ld + seg_begin);
 #pragma unroll
     for (int i = 0; i < VEC; ++i) {
       const int idx = ptid + i * kPartialThreads;
@@ -673,12 +698,12 @@ cudaError_t allow_dynamic_smem(const void* kernel) {
 
 template <int VEC, int GW>
 cudaError_t launch_rows_vg(const rrs_plan& p, const float* x, float* y, int64_t M, int64_t N,
-                           int64_t ld, cudaStream_t s) {
+                           const Layout& l, cudaStream_t s) {
   auto kern = softmax_staged_rows_kernel<VEC, GW>;
   cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(kern));
   if (e != cudaSuccess) return e;
   return launch_pdl(kern, dim3((unsigned)p.grid), dim3(kThreads), (size_t)p.smem_bytes, s, 0, x, y,
-                    M, (int32_t)N, ld, p.stages, p.tile * 4);
+                    M, (int32_t)N, l.ldx, l.ldy, p.stages, p.tile * 4);
 }
 
 }  // namespace
@@ -691,11 +716,11 @@ int grid_threads() { return kGThreads; }
 int grid_partial_threads() { return kPartialThreads; }
 
 cudaError_t launch_softmax_staged_rows(const rrs_plan& p, const float* x, float* y, int64_t M,
-                                       int64_t N, int64_t ld, cudaStream_t s) {
+                                       int64_t N, const Layout& l, cudaStream_t s) {
   if (p.threads != kThreads) return cudaErrorInvalidConfiguration;
   const int gw = p.warps_per_row, vec = p.vec;
 #define RRS_SR(V, G) \
-  if (vec == V && gw == G) return launch_rows_vg<V, G>(p, x, y, M, N, ld, s);
+  if (vec == V && gw == G) return launch_rows_vg<V, G>(p, x, y, M, N, l, s);
   RRS_SR(1, 1)
   RRS_SR(2, 1)
   RRS_SR(4, 1)
@@ -709,16 +734,16 @@ cudaError_t launch_softmax_staged_rows(const rrs_plan& p, const float* x, float*
 }
 
 cudaError_t launch_softmax_staged_long(const rrs_plan& p, const float* x, float* y, int64_t M,
-                                       int64_t N, int64_t ld, cudaStream_t s) {
+                                       int64_t N, const Layout& l, cudaStream_t s) {
   if (p.threads != kThreads) return cudaErrorInvalidConfiguration;
   cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(softmax_staged_long_kernel));
   if (e != cudaSuccess) return e;
   return launch_pdl(softmax_staged_long_kernel, dim3((unsigned)p.grid), dim3(kThreads),
-                    (size_t)p.smem_bytes, s, 0, x, y, M, N, ld, p.tile, p.stages);
+                    (size_t)p.smem_bytes, s, 0, x, y, M, N, l.ldx, l.ldy, p.tile, p.stages);
 }
 
 cudaError_t launch_softmax_staged_grid(const rrs_plan& p, const float* x, float* y, int64_t M,
-                                       int64_t N, int64_t ld, void* workspace, uint32_t ticket,
+                                       int64_t N, const Layout& l, void* workspace, uint32_t ticket,
                                        int fault, cudaStream_t s) {
   if (p.threads != kGThreads) return cudaErrorInvalidConfiguration;
   // segments of up to 4 float4 per thread run partials two items ahead (three
@@ -745,13 +770,13 @@ cudaError_t launch_softmax_staged_grid(const rrs_plan& p, const float* x, float*
   uint64_t* slots = static_cast<uint64_t*>(workspace);
   const int32_t C = (int32_t)p.ctas_per_row;
   if (p.vec == 2)
-    return cudaLaunchKernelEx(&cfg, k2, x, y, M, N, ld, p.chunk, C, p.rows_per_cta, p.stages,
-                              p.tile * 4, slots, ticket, (int32_t)fault);
+    return cudaLaunchKernelEx(&cfg, k2, x, y, M, N, l.ldx, l.ldy, p.chunk, C, p.rows_per_cta, p.stages,
+                              p.tile * 4, slots, ticket, (int32_t)fault, (int32_t)l.log_out);
   if (p.vec == 4)
-    return cudaLaunchKernelEx(&cfg, k4, x, y, M, N, ld, p.chunk, C, p.rows_per_cta, p.stages,
-                              p.tile * 4, slots, ticket, (int32_t)fault);
-  return cudaLaunchKernelEx(&cfg, k8, x, y, M, N, ld, p.chunk, C, p.rows_per_cta, p.stages,
-                            p.tile * 4, slots, ticket, (int32_t)fault);
+    return cudaLaunchKernelEx(&cfg, k4, x, y, M, N, l.ldx, l.ldy, p.chunk, C, p.rows_per_cta, p.stages,
+                              p.tile * 4, slots, ticket, (int32_t)fault, (int32_t)l.log_out);
+  return cudaLaunchKernelEx(&cfg, k8, x, y, M, N, l.ldx, l.ldy, p.chunk, C, p.rows_per_cta, p.stages,
+                            p.tile * 4, slots, ticket, (int32_t)fault, (int32_t)l.log_out);
 }
 
 cudaError_t read_and_clear_staged_error(cudaStream_t s, unsigned* value) {

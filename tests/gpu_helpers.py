@@ -7,7 +7,20 @@ Tolerances (floating point, fp32 kernel against the float64 oracle):
   * y == 0 exactly where x == -inf (rows with a finite entry);
   * rows the oracle makes NaN (all -inf, +inf, NaN inside) are all NaN;
   * row sums: |r - r_oracle| <= 1e-5 * sum_j |x_ij| (an absolute 1e-5 is
-    below one fp32 ulp of sums of magnitude 100+).
+    below one fp32 ulp of sums of magnitude 100+); row means the same over N;
+  * row max: bit-exact (a max of fp32 values is one of them);
+  * log-softmax: |log y - oracle| <= 1e-5 + 2^-21 |oracle| (x - m rounds at
+    2^-24 |x - m|, log(s) carries s's relative error, about 2e-6, as an
+    absolute one, and the final subtraction rounds at 2^-24 |log y|);
+    exactly -inf where x == -inf; NaN rows as for the softmax;
+  * column softmax: the row tolerances applied to each column;
+  * GeLU: |y - oracle| <= 1e-6 (2 + |a|) |oracle| + 2^-50 |x| + 1e-36 with
+    a = 0.79788456 (x + 0.044715 x^3): the kernel forms x / (1 + e^(-2a)),
+    whose relative error is a few ulps of fp32 times |a| (the rounding of a
+    scales e^(-2a) by e^(2 |a| u)); the oracle evaluates the pages' form
+    0.5 x (1 + tanh(a)) in float64, where 1 + tanh(a) keeps nothing below
+    2^-53 (it is exactly 0 once a < -19), hence 2^-50 |x|; 1e-36 absorbs
+    results below the normal range.  +inf -> +inf; -inf, NaN -> NaN.
 """
 from __future__ import annotations
 
@@ -97,3 +110,73 @@ def check_row_sum(got: np.ndarray, x: np.ndarray, where: str = "") -> float:
     err = np.abs(np.asarray(got, dtype=np.float64) - want)
     assert np.all(err <= SUM_TOL * scale + 0.0), f"{where}: row-sum err {float(np.max(err)):.3e}"
     return float(np.max(err / np.maximum(scale, 1e-300))) if err.size else 0.0
+
+
+LOG_ABS_TOL = 1e-5
+LOG_REL_TOL = 2.0 ** -21
+
+
+def check_log_softmax(got: np.ndarray, x: np.ndarray, where: str = "") -> float:
+    got = np.asarray(got, dtype=np.float64)
+    want = oracle.log_softmax_rows(x)
+    assert got.shape == want.shape, where
+    nan_rows = np.isnan(want).any(axis=1)
+    for i in np.nonzero(nan_rows)[0]:
+        assert np.all(np.isnan(got[i])), f"{where}: row {i} should be NaN"
+    ok = ~nan_rows
+    if not ok.any() or want.shape[1] == 0:
+        return 0.0
+    g, w = got[ok], want[ok]
+    neg = np.isneginf(w)
+    assert np.all(np.isneginf(g[neg])), f"{where}: -inf entries must give -inf"
+    fin = ~neg
+    err = np.abs(g[fin] - w[fin])
+    bound = LOG_ABS_TOL + LOG_REL_TOL * np.abs(w[fin])
+    assert np.all(err <= bound), f"{where}: log-softmax err {float(np.max(err)):.3e}"
+    return float(np.max(err)) if err.size else 0.0
+
+
+def check_row_max(got: np.ndarray, x: np.ndarray, where: str = "") -> None:
+    want = oracle.row_max(np.asarray(x, dtype=np.float64))
+    g = np.asarray(got, dtype=np.float64)
+    same = (g == want) | (np.isnan(g) & np.isnan(want))
+    assert np.all(same), f"{where}: row max differs at rows {np.nonzero(~same)[0][:5]}"
+
+
+def check_row_mean(got: np.ndarray, x: np.ndarray, where: str = "") -> float:
+    xv = np.asarray(x, dtype=np.float64)
+    want = oracle.row_mean(xv)
+    g = np.asarray(got, dtype=np.float64)
+    if xv.shape[1] == 0:
+        assert np.all(np.isnan(g)), where
+        return 0.0
+    scale = np.sum(np.abs(xv), axis=1) / xv.shape[1]
+    err = np.abs(g - want)
+    assert np.all(err <= SUM_TOL * scale), f"{where}: row-mean err {float(np.max(err)):.3e}"
+    return float(np.max(err / np.maximum(scale, 1e-300)))
+
+
+def check_softmax_cols(got: np.ndarray, x: np.ndarray, where: str = "", log: bool = False):
+    """Column softmax: the row checks on the transposes."""
+    g = np.ascontiguousarray(np.asarray(got).T)
+    xt = np.ascontiguousarray(np.asarray(x).T)
+    return check_log_softmax(g, xt, where) if log else check_softmax(g, xt, where)
+
+
+def check_gelu(got: np.ndarray, x: np.ndarray, where: str = "") -> float:
+    xv = np.asarray(x, dtype=np.float64).ravel()
+    g = np.asarray(got, dtype=np.float64).ravel()
+    with np.errstate(invalid="ignore", over="ignore"):
+        want = oracle.gelu(xv)
+        a = oracle.GELU_C * (xv + oracle.GELU_K * xv ** 3)
+    nan = np.isnan(want)
+    assert np.all(np.isnan(g[nan])), f"{where}: NaN expected"
+    inf = np.isinf(want) & ~nan
+    assert np.all(g[inf] == want[inf]), f"{where}: inf expected"
+    fin = ~nan & ~inf
+    err = np.abs(g[fin] - want[fin])
+    with np.errstate(over="ignore"):
+        bound = (1e-6 * (2.0 + np.abs(a[fin])) * np.abs(want[fin]) + 2.0 ** -50 * np.abs(xv[fin])
+                 + 1e-36)
+    assert np.all(err <= bound), f"{where}: gelu err {float(np.max(err)):.3e}"
+    return float(np.max(err)) if err.size else 0.0

@@ -218,3 +218,60 @@ def test_occupancy_and_waves_match_the_lecture_problems(lib):
             n, last, idle = rrs.waves(int(a["blocks"]), int(a["sms"]))
             assert (n, last, idle) == (int(want["waves"]), int(want["last"]), int(want["idle"]))
     assert seen == {"occupancy", "waves"}
+
+
+# ------------------------------------------------------------ column softmax ---
+
+@pytest.mark.parametrize("N", [1, 3, 4, 127, 128, 129, 8192, 16384])
+@pytest.mark.parametrize("M", [1, 2, 7, 64, 100, 1024, 2048, 2049, 4096])
+def test_cols_planner(lib, M, N):
+    import row_reduction_softmax_gb300 as rrs
+    p = rrs.plan_softmax_cols(M, N)
+    bands = -(-N // 128)
+    assert p["threads"] == 256
+    if M <= 2048:
+        assert p["path_name"] == "cluster"
+        cs, vec = p["cluster"], p["vec"]
+        assert 1 <= cs <= 16 and vec in (1, 2, 4, 8, 16)
+        assert cs * 8 * vec >= M > (cs - 1) * 8 * vec or cs == 1   # every row held once
+        assert p["grid"] == bands * cs
+    else:
+        assert p["path_name"] == "two_phase"
+        chunks, chunk = p["ctas_per_row"], p["chunk"]
+        assert chunks * chunk >= M > (chunks - 1) * chunk
+        assert p["grid"] == bands * chunks and p["workspace_bytes"] == chunks * N * 8
+    q = rrs.plan_softmax_cols(M, N, vector_ok=False)
+    assert q["path_name"] == "two_phase" and q["vector_io"] == 0
+
+
+def test_cols_forced_paths(lib):
+    import row_reduction_softmax_gb300 as rrs
+    try:
+        rrs.force_cols_path("two_phase")
+        assert rrs.plan_softmax_cols(64, 1024)["path_name"] == "two_phase"
+        rrs.force_cols_path("cluster")
+        with pytest.raises(rrs.RRSError) as e:
+            rrs.plan_softmax_cols(4096, 1024)
+        assert e.value.status == UNSUPPORTED
+    finally:
+        rrs.force_cols_path("auto")
+    assert lib.rrs_force_cols_path(7) == 1
+
+
+def test_new_entry_points_check_arguments(lib):
+    import ctypes
+    # host-side checks run before any device call
+    assert lib.softmax_rows_ex(None, 4, None, 4, 0, 4, 0, None) == 0        # empty: no work
+    assert lib.softmax_rows_ex(None, 4, None, 4, 2, 4, 2, None) == 1        # unknown flag bit
+    assert lib.softmax_rows_ex(None, 3, None, 4, 2, 4, 0, None) == 1        # ldx < N
+    assert lib.softmax_cols(None, 4, None, 2, 2, 4, 0, None) == 1           # ldy < N
+    assert lib.softmax_cols(None, 4, None, 4, 2, 4, 0, None) == 1           # null pointers
+    assert lib.log_softmax_rows(None, None, -1, 4, 4, None) == 1            # M < 0
+    assert lib.row_max(None, None, 0, 4, 4, None) == 0
+    assert lib.row_mean(None, None, 2, 4, 3, None) == 1                     # ld < N
+    buf = (ctypes.c_float * 64)()
+    a = ctypes.addressof(buf)
+    # overlap that is not exact in-place: rejected before the pointers are examined
+    assert lib.softmax_rows_ex(a, 8, a + 16, 8, 2, 8, 0, None) == 2
+    assert lib.softmax_rows_ex(a, 8, a, 4, 2, 4, 0, None) == 2               # same base, other stride
+    assert lib.softmax_cols(a, 8, a + 4, 8, 2, 8, 0, None) == 2

@@ -23,12 +23,13 @@ TIMEOUT = 4
 
 
 def test_grid_wait_runs_out_and_is_reported(lib):
+    path = "grid"
     M, N = 4, 65536
     x_host = workloads.matrix(workloads.WORKLOADS["c5"].with_shape(M, N))
     x = torch.from_numpy(x_host).cuda()
     y = torch.empty_like(x)
     try:
-        rrs.force_path("grid")
+        rrs.force_path(path)
         assert rrs.device_error() == 0
         assert lib.rrs_inject_fault(1) == 0
         rrs.softmax_rows(x, y)                      # the launch itself succeeds
@@ -38,7 +39,7 @@ def test_grid_wait_runs_out_and_is_reported(lib):
         lib.rrs_inject_fault(0)
         rrs.force_path("auto", "auto")
     # the context is still usable and results are right again
-    rrs.force_path("grid")
+    rrs.force_path(path)
     try:
         rrs.softmax_rows(x, y)
         torch.cuda.synchronize()

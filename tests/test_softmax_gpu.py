@@ -221,3 +221,23 @@ def test_full_size_workload(name):
     del x, y
     torch.cuda.empty_cache()
 
+
+
+@pytest.mark.parametrize("path", ["grid", "two_phase"])
+def test_full_size_long_rows_on_each_split_path(path):
+    """32 rows of 2^20 on every path that splits a row over CTAs."""
+    w = workloads.WORKLOADS["c5"]
+    x_host = workloads.matrix(w)
+    x = torch.from_numpy(x_host).cuda()
+    y = torch.empty_like(x)
+    rrs.force_path(path)
+    for _ in range(3):                         # repeated launches reuse the workspace
+        rrs.softmax_rows(x, y)
+    torch.cuda.synchronize()
+    assert rrs.device_error() == 0
+    rows = sampled_rows(w.M, w.seed)
+    check_softmax(y[rows].cpu().numpy(), x_host[rows], f"{path} c5 sampled rows")
+    sums = y.double().sum(dim=1)
+    assert float((sums - 1.0).abs().max()) <= 1e-5
+    del x, y
+    torch.cuda.empty_cache()

@@ -30,7 +30,8 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-__all__ = ["Workload", "WORKLOADS", "row_values", "matrix", "spike_mask_counts"]
+__all__ = ["Workload", "WORKLOADS", "VARIANT_WORKLOADS", "row_values", "matrix",
+           "spike_mask_counts"]
 
 
 @dataclass(frozen=True)
@@ -66,6 +67,19 @@ WORKLOADS = {
     "c4": Workload("c4", 16384, 4096, "logits", seed=3, sigma=3.0, spike=50.0,
                    spike_frac=0.05, mask_frac=0.01),
     "c5": Workload("c5", 32, 1048576, "normal", seed=4, sigma=1.0),
+}
+
+
+# Workloads of the variants built on the same skeleton (the pages give no
+# sizes for them; these reuse the recipes above at shapes of the same size):
+# the column softmax on c2's and c4's values with the long axis down the
+# columns, and the elementwise GeLU on a 16384 x 16384 Normal(0, 1) matrix,
+# the "16,384-dim" input of the pages' GeLU benchmark.
+VARIANT_WORKLOADS = {
+    "cols_c2": Workload("cols_c2", 1024, 8192, "normal", seed=1, sigma=2.0, ops=("softmax_cols",)),
+    "cols_c4": Workload("cols_c4", 4096, 16384, "logits", seed=3, sigma=3.0, spike=50.0,
+                        spike_frac=0.05, mask_frac=0.01, ops=("softmax_cols",)),
+    "gelu_16k": Workload("gelu_16k", 16384, 16384, "normal", seed=6, sigma=1.0, ops=("gelu",)),
 }
 
 
