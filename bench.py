@@ -246,8 +246,8 @@ def kernel_of(plan: dict) -> str:
         return "softmax_staged_rows_kernel" if plan["vec"] > 0 else "softmax_staged_long_kernel"
     return {"row_regs": "softmax_row_regs_kernel", "cluster": "softmax_cluster_kernel",
             "two_phase": "softmax_partials_kernel+softmax_finalize_kernel",
-            "grid": "softmax_staged_grid_kernel", "row": "row_sum_rows_kernel",
-            "split": "row_sum_partials_kernel+row_sum_finalize_kernel"}.get(name, name)
+            "grid": "softmax_staged_grid_kernel", "row": "row_reduce_rows_kernel",
+            "split": "row_reduce_partials_kernel+row_reduce_finalize_kernel"}.get(name, name)
 
 
 def l2_pairs(torch, pair_bytes: int) -> int:

@@ -90,7 +90,7 @@ typedef enum rrs_sum_path {
 typedef enum rrs_cols_path {
   RRS_COLS_AUTO = -1,
   RRS_COLS_TWO_PHASE = 0,  /* any shape/alignment: per-(row chunk, column) partials, then merge + re-read + write */
-  RRS_COLS_CLUSTER = 1,    /* a band of 128 columns over a cluster of CTAs, all rows in registers (M <= 2048) */
+  RRS_COLS_CLUSTER = 1,    /* a band of 32 columns over a cluster of CTAs, all rows in registers (M <= 8192) */
   RRS_COLS_COUNT = 2
 } rrs_cols_path;
 
@@ -150,7 +150,7 @@ RRS_API int log_softmax_rows(const float* x, float* y, int64_t M, int64_t N, int
  * (flags = RRS_LOG_SOFTMAX: (x[i,j] - m_j) - log(s_j)).  The pages' softmax
  * with the reduction over rows; the lecture transcript takes it up in the
  * questions after the softmax kernel, where only the strides change.  Element (i, j) of x is x[i*ldx + j], of y y[i*ldy + j];
- * columns are read along rows, 512 contiguous bytes per warp access.
+ * columns are read along rows, full 128-byte lines.
  * Columns that are all -inf or hold +inf or NaN come out NaN.  x == y with
  * ldx == ldy computes in place.  Arguments, errors and the empty cases as
  * softmax_rows_ex. */

@@ -400,24 +400,29 @@ int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_co
   }
 }
 
-// Column softmax.  COLS_CLUSTER: a band of 128 columns per cluster; rows per
-// thread vec (a power of two, at most 16) chosen so that about 8 CTAs share
-// a band, cs = ceil(M / (8 warps x vec)) <= 16 CTAs.  COLS_TWO_PHASE: row
+// Column softmax.  COLS_CLUSTER: a band of 32 columns per cluster; as many
+// rows per thread as useful (vec a power of two, at most 16), so the fewest
+// CTAs share a band: cs = ceil(M / (32 row groups x vec)) <= 16 (M <= 8192).
+// Measured on GB300 (1024 x 8192, 256 x 32768, 2048 x 4096, 4096 x 16384):
+// fewer, fuller CTAs per band win, and beyond 4 CTAs per band the two-phase
+// path is faster, so the planner takes the cluster only up to cs = 4.  COLS_TWO_PHASE: row
 // chunks sized for about 4 CTAs per SM over all bands.
 enum WorkspaceKindCols { kWsCols = 3 };
 
-bool plan_cols_cluster(int64_t M, int64_t N, rrs_plan* p) {
-  const int64_t warps = cols_threads() / 32;
+constexpr int64_t kColsAutoMaxCluster = 4;
+
+bool plan_cols_cluster(int64_t M, int64_t N, int64_t max_cs, rrs_plan* p) {
+  const int64_t groups = cols_row_groups();
   const int64_t vec = std::min<int64_t>(cols_rows_per_thread_max(),
-                                        std::max<int64_t>(1, pow2_ceil(ceil_div(M, warps * 8))));
-  const int64_t cs = ceil_div(M, warps * vec);
-  if (cs > kClusterMax) return false;
+                                        std::max<int64_t>(1, pow2_ceil(ceil_div(M, groups))));
+  const int64_t cs = ceil_div(M, groups * vec);
+  if (cs > std::min<int64_t>(max_cs, kClusterMax)) return false;
   p->path = RRS_COLS_CLUSTER;
   p->threads = cols_threads();
   p->vec = (int32_t)vec;
   p->cluster = (int32_t)cs;
   p->grid = ceil_div(N, cols_band()) * cs;
-  p->rows_per_cta = (int32_t)(warps * vec);
+  p->rows_per_cta = (int32_t)(groups * vec);
   p->ctas_per_row = cs;
   p->chunk = ceil_div(M, cs);
   return true;
@@ -450,16 +455,17 @@ int plan_cols_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_count
   }
   const bool cluster_fits = vector_ok && cluster_ok;
   if (forced == RRS_COLS_AUTO) {
-    if (!(cluster_fits && plan_cols_cluster(M, N, p))) plan_cols_two_phase(M, N, sm_count, p);
+    if (!(cluster_fits && plan_cols_cluster(M, N, kColsAutoMaxCluster, p)))
+      plan_cols_two_phase(M, N, sm_count, p);
     p->vector_io = vector_ok ? 1 : 0;
     return RRS_OK;
   }
   if (forced == RRS_COLS_CLUSTER) {
-    if (cluster_fits && plan_cols_cluster(M, N, p)) {
+    if (cluster_fits && plan_cols_cluster(M, N, kClusterMax, p)) {
       p->vector_io = 1;
       return RRS_OK;
     }
-    return fail(RRS_ERR_UNSUPPORTED, "COLS_CLUSTER needs 16-byte alignment, cluster launch and M <= 2048");
+    return fail(RRS_ERR_UNSUPPORTED, "COLS_CLUSTER needs 16-byte alignment, cluster launch and M <= 8192");
   }
   if (forced == RRS_COLS_TWO_PHASE) {
     plan_cols_two_phase(M, N, sm_count, p);
@@ -482,8 +488,9 @@ int plan_row_sum_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_co
     path = (M < 2 * (int64_t)sm_count && N >= 65536) ? RRS_SUM_SPLIT : RRS_SUM_ROW;
   }
   if (path == RRS_SUM_ROW) {
-    // about 32 floats per thread before a CTA holds more than 16 warps
-    const int gw = (int)std::min<int64_t>(16, std::max<int64_t>(1, pow2_ceil(ceil_div(N, 32 * 32 * 2))));
+    // about 32 floats per thread before a CTA holds more than 8 warps (a
+    // 256-thread CTA per long row measured faster than 512 on 4096 x 32768)
+    const int gw = (int)std::min<int64_t>(8, std::max<int64_t>(1, pow2_ceil(ceil_div(N, 32 * 32 * 2))));
     p->path = RRS_SUM_ROW;
     p->warps_per_row = gw;
     p->threads = std::max(32 * gw, 128);

@@ -66,11 +66,13 @@ cudaError_t launch_softmax_staged_grid(const rrs_plan& p, const float* x, float*
                                        int fault, cudaStream_t s);
 
 // ---- column softmax (softmax_cols.cu): COLS_CLUSTER plans carry cluster
-// (CTAs per band) and vec (rows per thread); COLS_TWO_PHASE plans carry
+// (CTAs per band of cols_band() columns) and vec (rows per thread; a CTA
+// holds cols_row_groups() x vec rows); COLS_TWO_PHASE plans carry
 // ctas_per_row (row chunks) and chunk (rows per chunk), workspace chunks x N
 // (max, sum) pairs.
 int cols_threads();
 int cols_band();
+int cols_row_groups();
 int cols_rows_per_thread_max();
 cudaError_t launch_softmax_cols_cluster(const rrs_plan& p, const float* x, float* y, int64_t M,
                                         int64_t N, const Layout& l, cudaStream_t s);

@@ -5,16 +5,19 @@
 // for it; the answer there is the same kernel with the strides swapped.  A
 // thread per column reading down the rows would touch one float per 128-byte
 // line per warp access -- the uncoalesced pattern of the pages' "memory
-// coalescing" paragraph -- so here a warp reads 128 consecutive columns of a
-// row (one float4 per lane, 512 contiguous bytes) and the reduction runs
-// across warps and CTAs instead of across lanes.
+// coalescing" paragraph -- so here 8 lanes read 32 consecutive columns of a
+// row (one float4 each: a full 128-byte line) and a warp access covers 4
+// rows; the reduction runs across lanes groups, warps and CTAs.  A narrow
+// band (32 columns) gives many CTAs, so that their load and store phases
+// overlap instead of running in a few lockstep waves.
 //
-// COLS_CLUSTER -- a band of 128 columns per CTA group; the M rows are split
-//   over a thread-block cluster of cs CTAs, each CTA's 8 warps hold VEC rows
-//   each in registers.  Per column: max and sum over a thread's rows, then
-//   over the 8 warps (shared memory), then over the cluster's CTAs (DSMEM),
-//   merged with m = max(m_a, m_b), s = s_a e^(m_a - m) + s_b e^(m_b - m).
-//   One read and one write per element.  M <= 16 * 8 * 16 = 2048.
+// COLS_CLUSTER -- a band of 32 columns per CTA group; the M rows are split
+//   over a thread-block cluster of cs CTAs, each CTA's 32 row groups (8 warps
+//   x 4 rows per access) hold VEC rows each in registers.  Per column: max and
+//   sum over a thread's rows, then over the CTA's row groups (shared memory),
+//   then over the cluster's CTAs (DSMEM), merged with m = max(m_a, m_b),
+//   s = s_a e^(m_a - m) + s_b e^(m_b - m).  One read and one write per
+//   element.  M <= 16 * 32 * 16 = 8192.
 // COLS_TWO_PHASE -- any M and alignment: kernel 1 writes each (row chunk,
 //   column) online partial to a workspace, kernel 2 merges a column's
 //   partials, re-reads its chunk and writes y (12 bytes per element unless
@@ -30,9 +33,12 @@ namespace cg = cooperative_groups;
 namespace rrs {
 namespace {
 
-constexpr int kCT = 256;           // threads per CTA
-constexpr int kCW = kCT / 32;      // warps per CTA: each owns a set of rows
-constexpr int kBand = 128;         // columns per CTA: 32 lanes x float4
+constexpr int kCT = 256;             // threads per CTA
+constexpr int kCW = kCT / 32;        // warps per CTA
+constexpr int kLPR = 8;              // lanes that share a row: 8 x float4 = 128 bytes
+constexpr int kRPW = 32 / kLPR;      // rows per warp access
+constexpr int kGroups = kCW * kRPW;  // row groups per CTA
+constexpr int kBand = 4 * kLPR;      // columns per CTA
 
 __device__ __forceinline__ void cluster_arrive_release() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
@@ -75,15 +81,21 @@ __device__ __forceinline__ float comp(const float4& v, int c) {
 
 // ------------------------------------------------------------ COLS_CLUSTER ---
 // Grid: (bands * cs) CTAs in clusters of cs along x; cluster k owns columns
-// [128k, 128k + 128).  Rank r owns rows [r * rseg, min((r + 1) * rseg, M)),
-// rseg = ceil(M / cs) <= kCW * VEC; warp w of the CTA holds rows
-// r * rseg + w + kCW * i, i < VEC.  x, y 16-byte aligned and ldx, ldy
-// multiples of 4 (any N).  log_out != 0 writes (x - m) - log(s).
+// [32k, 32k + 32).  Rank r owns rows [r * rseg, min((r + 1) * rseg, M)),
+// rseg = ceil(M / cs) <= kGroups * VEC.  Thread (warp w, lane l) is in row
+// group g = 4w + l / 8 and column slot l % 8; it holds rows
+// r * rseg + g + kGroups * i, i < VEC, columns 4 (l % 8) .. + 3 of the band.
+// x, y 16-byte aligned and ldx, ldy multiples of 4 (any N).  LOG writes
+// (x - m) - log(s).
+// Occupancy target per VEC: 4 CTAs per SM up to 4 rows per thread, then 3, 2.
 template <int VEC>
-__global__ void __launch_bounds__(kCT, 2)
+__host__ __device__ constexpr int cols_min_blocks() { return VEC <= 4 ? 4 : (VEC == 8 ? 3 : 2); }
+
+template <int VEC, bool LOG>
+__global__ void __launch_bounds__(kCT, cols_min_blocks<VEC>())
 softmax_cols_cluster_kernel(const float* x, float* y, int64_t M, int64_t N, int64_t ldx,
-                            int64_t ldy, int32_t log_out) {
-  __shared__ float red[kCW][kBand];
+                            int64_t ldy) {
+  __shared__ float red[kGroups][kBand];
   __shared__ MaxSum part[kBand];   // this CTA's per-column (m_c, s_c), read by its peers
   __shared__ MaxSum whole[kBand];  // the merged pair of each column
 
@@ -92,22 +104,24 @@ softmax_cols_cluster_kernel(const float* x, float* y, int64_t M, int64_t N, int6
   const int rank = (int)cluster.block_rank();
   const int64_t band = blockIdx.x / cs;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int slot = lane % kLPR;
+  const int g = warp * kRPW + lane / kLPR;
   const int64_t rseg = (M + cs - 1) / cs;
   const int64_t r0 = rank * rseg;
   const int64_t r1 = min(r0 + rseg, M);
-  const int64_t j0 = band * kBand + 4 * lane;
+  const int64_t j0 = band * kBand + 4 * slot;
   const float kNeg = neg_inf();
   pdl_entry();
 
   float4 v[VEC];
 #pragma unroll
   for (int i = 0; i < VEC; ++i) {
-    const int64_t r = r0 + warp + (int64_t)kCW * i;
+    const int64_t r = r0 + g + (int64_t)kGroups * i;
     v[i] = (r < r1 && j0 < N) ? load_cols<true>(x + r * ldx, j0, N, kNeg)
                               : make_float4(kNeg, kNeg, kNeg, kNeg);
   }
 
-  // per-column max over this thread's rows, then over the CTA's warps
+  // per-column max over this thread's rows, then over the CTA's row groups
   float4 m = v[0];
 #pragma unroll
   for (int i = 1; i < VEC; ++i) {
@@ -116,18 +130,18 @@ softmax_cols_cluster_kernel(const float* x, float* y, int64_t M, int64_t N, int6
     m.z = max_nan(m.z, v[i].z);
     m.w = max_nan(m.w, v[i].w);
   }
-  reinterpret_cast<float4*>(red[warp])[lane] = m;
+  reinterpret_cast<float4*>(red[g])[slot] = m;
   __syncthreads();
   if (tid < kBand) {
     float cm = red[0][tid];
-#pragma unroll
-    for (int w = 1; w < kCW; ++w) cm = max_nan(cm, red[w][tid]);
+#pragma unroll 8
+    for (int k = 1; k < kGroups; ++k) cm = max_nan(cm, red[k][tid]);
     part[tid].m = cm;
   }
   __syncthreads();
   float mc[4];
 #pragma unroll
-  for (int c = 0; c < 4; ++c) mc[c] = part[4 * lane + c].m;
+  for (int c = 0; c < 4; ++c) mc[c] = part[4 * slot + c].m;
 
   // per-column sum of exp(x - m_c); x stays in v for the log form
   float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -142,15 +156,14 @@ softmax_cols_cluster_kernel(const float* x, float* y, int64_t M, int64_t N, int6
     s.y += e.y;
     s.z += e.z;
     s.w += e.w;
-    if (!log_out) v[i] = e;
+    if constexpr (!LOG) v[i] = e;
   }
-  __syncthreads();  // every thread has read part[].m
-  reinterpret_cast<float4*>(red[warp])[lane] = s;
+  reinterpret_cast<float4*>(red[g])[slot] = s;  // red's max values were consumed before the barrier
   __syncthreads();
   if (tid < kBand) {
     float cs_sum = 0.f;
-#pragma unroll
-    for (int w = 0; w < kCW; ++w) cs_sum += red[w][tid];
+#pragma unroll 8
+    for (int k = 0; k < kGroups; ++k) cs_sum += red[k][tid];
     part[tid].s = cs_sum;
   }
   cluster_arrive_release();  // publish part[] to the cluster
@@ -167,23 +180,27 @@ softmax_cols_cluster_kernel(const float* x, float* y, int64_t M, int64_t N, int6
   float wm[4], k4[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    const MaxSum w = whole[4 * lane + c];
+    const MaxSum w = whole[4 * slot + c];
     wm[c] = w.m;
     const bool bad = !(w.s == w.s) || w.m == kNeg;  // NaN / inf / all -inf column
-    k4[c] = log_out ? logf(w.s)
-                    : (bad ? __int_as_float(0x7fc00000)
-                           : (mc[c] == kNeg ? 0.f : exp_shifted(mc[c], w.m) / w.s));
+    if constexpr (LOG) {
+      k4[c] = logf(w.s);
+    } else {
+      k4[c] = bad ? __int_as_float(0x7fc00000)
+                  : (mc[c] == kNeg ? 0.f : exp_shifted(mc[c], w.m) / w.s);
+    }
   }
 #pragma unroll
   for (int i = 0; i < VEC; ++i) {
-    const int64_t r = r0 + warp + (int64_t)kCW * i;
+    const int64_t r = r0 + g + (int64_t)kGroups * i;
     if (r >= r1 || j0 >= N) continue;
-    const float4 o = log_out ? make_float4(log_softmax_of(v[i].x, wm[0], k4[0]),
-                                           log_softmax_of(v[i].y, wm[1], k4[1]),
-                                           log_softmax_of(v[i].z, wm[2], k4[2]),
-                                           log_softmax_of(v[i].w, wm[3], k4[3]))
-                             : make_float4(v[i].x * k4[0], v[i].y * k4[1], v[i].z * k4[2],
-                                           v[i].w * k4[3]);
+    float4 o;
+    if constexpr (LOG) {
+      o = make_float4(log_softmax_of(v[i].x, wm[0], k4[0]), log_softmax_of(v[i].y, wm[1], k4[1]),
+                      log_softmax_of(v[i].z, wm[2], k4[2]), log_softmax_of(v[i].w, wm[3], k4[3]));
+    } else {
+      o = make_float4(v[i].x * k4[0], v[i].y * k4[1], v[i].z * k4[2], v[i].w * k4[3]);
+    }
     store_cols<true>(y + r * ldy, j0, N, o);
   }
   cluster_wait_acquire();  // peers finished reading part[] before this CTA exits
@@ -191,64 +208,79 @@ softmax_cols_cluster_kernel(const float* x, float* y, int64_t M, int64_t N, int6
 
 // --------------------------------------------------------- COLS_TWO_PHASE ---
 // Grid: bands x chunks CTAs, CTA (band b, chunk c) = blockIdx.x = c * bands + b.
-// Chunk c holds rows [c * chunk, min((c + 1) * chunk, M)); warp w takes rows
-// w, w + kCW, ... of it.  part[c * N + j] is chunk c's partial of column j.
+// Chunk c holds rows [c * chunk, min((c + 1) * chunk, M)); row group g takes
+// rows g, g + kGroups, ... of it, kTP rows in flight per thread.
+// part[c * N + j] is chunk c's partial of column j.
+constexpr int kTP = 4;
+
 template <bool V4>
-__global__ void __launch_bounds__(kCT)
+__global__ void __launch_bounds__(kCT, 4)
 softmax_cols_partials_kernel(const float* x, MaxSum* __restrict__ part, int64_t M, int64_t N,
                              int64_t ldx, int64_t chunk, int64_t bands) {
-  __shared__ MaxSum red[kCW][kBand];
+  __shared__ MaxSum red[kGroups][kBand];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int slot = lane % kLPR;
+  const int g = warp * kRPW + lane / kLPR;
   const int64_t b = blockIdx.x % bands;
   const int64_t c = blockIdx.x / bands;
   const int64_t r0 = c * chunk;
   const int64_t r1 = min(r0 + chunk, M);
-  const int64_t j0 = b * kBand + 4 * lane;
+  const int64_t j0 = b * kBand + 4 * slot;
   const float kNeg = neg_inf();
   pdl_entry();
 
   MaxSum p[4] = {{kNeg, 0.f}, {kNeg, 0.f}, {kNeg, 0.f}, {kNeg, 0.f}};
   if (j0 < N) {
-    for (int64_t r = r0 + warp; r < r1; r += 2 * kCW) {  // two rows in flight
-      const float4 a = load_cols<V4>(x + r * ldx, j0, N, kNeg);
-      const float4 bb = (r + kCW < r1) ? load_cols<V4>(x + (r + kCW) * ldx, j0, N, kNeg)
-                                        : make_float4(kNeg, kNeg, kNeg, kNeg);
+    for (int64_t r = r0 + g; r < r1; r += (int64_t)kTP * kGroups) {
+      float4 a[kTP];
+#pragma unroll
+      for (int u = 0; u < kTP; ++u) {
+        const int64_t ru = r + (int64_t)u * kGroups;
+        a[u] = (ru < r1) ? load_cols<V4>(x + ru * ldx, j0, N, kNeg)
+                         : make_float4(kNeg, kNeg, kNeg, kNeg);
+      }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float va = comp(a, k), vb = comp(bb, k);
-        rescale_to(p[k], max_nan(va, vb));
-        if (p[k].m != kNeg) p[k].s += exp_shifted(va, p[k].m) + exp_shifted(vb, p[k].m);
+        float bm = comp(a[0], k);
+#pragma unroll
+        for (int u = 1; u < kTP; ++u) bm = max_nan(bm, comp(a[u], k));
+        rescale_to(p[k], bm);
+        if (p[k].m != kNeg) {
+#pragma unroll
+          for (int u = 0; u < kTP; ++u) p[k].s += exp_shifted(comp(a[u], k), p[k].m);
+        }
       }
     }
   }
 #pragma unroll
-  for (int k = 0; k < 4; ++k) red[warp][4 * lane + k] = p[k];
+  for (int k = 0; k < 4; ++k) red[g][4 * slot + k] = p[k];
   __syncthreads();
   if (tid < kBand) {
     const int64_t j = b * kBand + tid;
     MaxSum q{kNeg, 0.f};
-#pragma unroll
-    for (int w = 0; w < kCW; ++w) q = merge(q, red[w][tid]);
+    for (int k = 0; k < kGroups; ++k) q = merge(q, red[k][tid]);
     if (j < N) part[c * N + j] = q;
   }
 }
 
-// Each CTA merges, for its 128 columns, the partials of all chunks in chunk
+// Each CTA merges, for its 32 columns, the partials of all chunks in chunk
 // order (so every CTA of a band gets the same pair), then re-reads its rows
 // and writes y.  Every element is read and then written by one thread, so
 // x == y (in place) is safe.
 template <bool V4>
-__global__ void __launch_bounds__(kCT)
+__global__ void __launch_bounds__(kCT, 4)
 softmax_cols_finalize_kernel(const float* x, float* y, const MaxSum* __restrict__ part, int64_t M,
                              int64_t N, int64_t ldx, int64_t ldy, int64_t chunk, int64_t chunks,
                              int64_t bands, int32_t log_out) {
   __shared__ MaxSum whole[kBand];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int slot = lane % kLPR;
+  const int g = warp * kRPW + lane / kLPR;
   const int64_t b = blockIdx.x % bands;
   const int64_t c = blockIdx.x / bands;
   const int64_t r0 = c * chunk;
   const int64_t r1 = min(r0 + chunk, M);
-  const int64_t j0 = b * kBand + 4 * lane;
+  const int64_t j0 = b * kBand + 4 * slot;
   const float kNeg = neg_inf();
   pdl_entry();
   if (tid < kBand) {
@@ -263,40 +295,58 @@ softmax_cols_finalize_kernel(const float* x, float* y, const MaxSum* __restrict_
   float m[4], inv[4], ls[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const MaxSum w = whole[4 * lane + k];
+    const MaxSum w = whole[4 * slot + k];
     m[k] = w.m;
     inv[k] = 1.0f / w.s;
     ls[k] = logf(w.s);
   }
-  for (int64_t r = r0 + warp; r < r1; r += kCW) {
-    const float4 a = load_cols<V4>(x + r * ldx, j0, N, 0.f);
-    float4 o;
-    if (log_out) {
-      o = make_float4(log_softmax_of(a.x, m[0], ls[0]), log_softmax_of(a.y, m[1], ls[1]),
-                      log_softmax_of(a.z, m[2], ls[2]), log_softmax_of(a.w, m[3], ls[3]));
-    } else {
-      o = make_float4(exp_shifted(a.x, m[0]) * inv[0], exp_shifted(a.y, m[1]) * inv[1],
-                      exp_shifted(a.z, m[2]) * inv[2], exp_shifted(a.w, m[3]) * inv[3]);
+  for (int64_t r = r0 + g; r < r1; r += (int64_t)kTP * kGroups) {
+    float4 a[kTP];
+#pragma unroll
+    for (int u = 0; u < kTP; ++u) {
+      const int64_t ru = r + (int64_t)u * kGroups;
+      if (ru < r1) a[u] = load_cols<V4>(x + ru * ldx, j0, N, 0.f);
     }
-    store_cols<V4>(y + r * ldy, j0, N, o);
+#pragma unroll
+    for (int u = 0; u < kTP; ++u) {
+      const int64_t ru = r + (int64_t)u * kGroups;
+      if (ru >= r1) continue;
+      float4 o;
+      if (log_out) {
+        o = make_float4(log_softmax_of(a[u].x, m[0], ls[0]), log_softmax_of(a[u].y, m[1], ls[1]),
+                        log_softmax_of(a[u].z, m[2], ls[2]), log_softmax_of(a[u].w, m[3], ls[3]));
+      } else {
+        o = make_float4(exp_shifted(a[u].x, m[0]) * inv[0], exp_shifted(a[u].y, m[1]) * inv[1],
+                        exp_shifted(a[u].z, m[2]) * inv[2], exp_shifted(a[u].w, m[3]) * inv[3]);
+      }
+      store_cols<V4>(y + ru * ldy, j0, N, o);
+    }
   }
 }
 
-template <int VEC>
+template <int VEC, bool LOG>
 cudaError_t launch_cols_cluster_vec(const rrs_plan& p, const float* x, float* y, int64_t M,
                                     int64_t N, const Layout& l, cudaStream_t s) {
-  auto kern = softmax_cols_cluster_kernel<VEC>;
+  auto kern = softmax_cols_cluster_kernel<VEC, LOG>;
   if (p.cluster > 8) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
   }
   return launch_pdl(kern, dim3((unsigned)p.grid), dim3(kCT), 0, s, p.cluster, x, y, M, N, l.ldx,
-                    l.ldy, (int32_t)l.log_out);
+                    l.ldy);
+}
+
+template <int VEC>
+cudaError_t launch_cols_cluster_v(const rrs_plan& p, const float* x, float* y, int64_t M,
+                                  int64_t N, const Layout& l, cudaStream_t s) {
+  return l.log_out ? launch_cols_cluster_vec<VEC, true>(p, x, y, M, N, l, s)
+                   : launch_cols_cluster_vec<VEC, false>(p, x, y, M, N, l, s);
 }
 
 }  // namespace
 
 int cols_threads() { return kCT; }
+int cols_row_groups() { return kGroups; }
 int cols_band() { return kBand; }
 int cols_rows_per_thread_max() { return 16; }
 
@@ -304,11 +354,11 @@ cudaError_t launch_softmax_cols_cluster(const rrs_plan& p, const float* x, float
                                         int64_t N, const Layout& l, cudaStream_t s) {
   if (p.threads != kCT) return cudaErrorInvalidConfiguration;
   switch (p.vec) {
-    case 1: return launch_cols_cluster_vec<1>(p, x, y, M, N, l, s);
-    case 2: return launch_cols_cluster_vec<2>(p, x, y, M, N, l, s);
-    case 4: return launch_cols_cluster_vec<4>(p, x, y, M, N, l, s);
-    case 8: return launch_cols_cluster_vec<8>(p, x, y, M, N, l, s);
-    case 16: return launch_cols_cluster_vec<16>(p, x, y, M, N, l, s);
+    case 1: return launch_cols_cluster_v<1>(p, x, y, M, N, l, s);
+    case 2: return launch_cols_cluster_v<2>(p, x, y, M, N, l, s);
+    case 4: return launch_cols_cluster_v<4>(p, x, y, M, N, l, s);
+    case 8: return launch_cols_cluster_v<8>(p, x, y, M, N, l, s);
+    case 16: return launch_cols_cluster_v<16>(p, x, y, M, N, l, s);
     default: return cudaErrorInvalidConfiguration;
   }
 }

@@ -180,7 +180,7 @@ def test_forced_paths(lib):
 def test_row_sum_planner(lib):
     import row_reduction_softmax_gb300 as rrs
     p = rrs.plan_row_sum(4096, 32768)
-    assert p["path_name"] == "row" and p["threads"] == 512
+    assert p["path_name"] == "row" and p["threads"] == 256 and p["warps_per_row"] == 8
     p = rrs.plan_row_sum(32, 1 << 20)
     assert p["path_name"] == "split" and p["ctas_per_row"] * p["chunk"] >= 1 << 20
     p = rrs.plan_row_sum(10, 10)
@@ -223,17 +223,19 @@ def test_occupancy_and_waves_match_the_lecture_problems(lib):
 # ------------------------------------------------------------ column softmax ---
 
 @pytest.mark.parametrize("N", [1, 3, 4, 127, 128, 129, 8192, 16384])
-@pytest.mark.parametrize("M", [1, 2, 7, 64, 100, 1024, 2048, 2049, 4096])
+@pytest.mark.parametrize("M", [1, 2, 7, 64, 100, 1024, 2048, 2049, 4096, 8192, 8193])
 def test_cols_planner(lib, M, N):
     import row_reduction_softmax_gb300 as rrs
     p = rrs.plan_softmax_cols(M, N)
-    bands = -(-N // 128)
+    bands = -(-N // 32)
     assert p["threads"] == 256
     if M <= 2048:
         assert p["path_name"] == "cluster"
         cs, vec = p["cluster"], p["vec"]
-        assert 1 <= cs <= 16 and vec in (1, 2, 4, 8, 16)
-        assert cs * 8 * vec >= M > (cs - 1) * 8 * vec or cs == 1   # every row held once
+        assert 1 <= cs <= 4 and vec in (1, 2, 4, 8, 16)
+        rows = 32 * vec                                  # rows one CTA holds
+        assert cs * rows >= M > (cs - 1) * rows or cs == 1   # every row held once
+        assert vec == 16 or cs == 1                      # the fewest CTAs per band
         assert p["grid"] == bands * cs
     else:
         assert p["path_name"] == "two_phase"
@@ -250,8 +252,10 @@ def test_cols_forced_paths(lib):
         rrs.force_cols_path("two_phase")
         assert rrs.plan_softmax_cols(64, 1024)["path_name"] == "two_phase"
         rrs.force_cols_path("cluster")
+        p = rrs.plan_softmax_cols(8192, 1024)            # forced: up to 16 CTAs per band
+        assert p["path_name"] == "cluster" and p["cluster"] == 16 and p["vec"] == 16
         with pytest.raises(rrs.RRSError) as e:
-            rrs.plan_softmax_cols(4096, 1024)
+            rrs.plan_softmax_cols(8193, 1024)
         assert e.value.status == UNSUPPORTED
     finally:
         rrs.force_cols_path("auto")

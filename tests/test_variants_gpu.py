@@ -237,13 +237,14 @@ def run_cols(x_host, N, ldx, ldy, path="auto", flags=0, in_place=False, x_off=0,
 
 
 COL_SHAPES = [(1, 1), (2, 5), (7, 3), (8, 128), (9, 129), (64, 250), (100, 33), (129, 512),
-              (1024, 300), (2047, 64), (2048, 131), (2049, 130), (5000, 40)]
+              (1024, 300), (2047, 64), (2048, 131), (2049, 130), (5000, 40), (8192, 37),
+              (8193, 20)]
 
 
 @pytest.mark.parametrize("path", ["cluster", "two_phase"])
 @pytest.mark.parametrize("M,N", COL_SHAPES)
 def test_cols_parity(path, M, N):
-    if path == "cluster" and M > 2048:
+    if path == "cluster" and M > 8192:
         pytest.skip("more rows than a cluster holds")
     x = recipe(["c2", "c4", "c3"][(M + N) % 3], M, N)
     ld = N if path == "two_phase" else -(-N // 4) * 4   # the cluster path wants ld % 4 == 0
