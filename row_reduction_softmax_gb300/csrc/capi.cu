@@ -153,8 +153,10 @@ bool overlaps(const void* a, int64_t a_bytes, const void* b, int64_t b_bytes) {
 }
 
 // ---------------------------------------------------------------- planner ---
-void plan_row_regs(int64_t M, int64_t N, int sm_count, rrs_plan* p) {
-  const int64_t n4 = N >> 2;
+// vector: float4 slots plus an N % 4 tail; scalar (unaligned x or y, or a
+// stride not a multiple of 4): 4 scalars per slot, so the slots cover N.
+void plan_row_regs(int64_t M, int64_t N, int sm_count, rrs_plan* p, bool vector = true) {
+  const int64_t n4 = vector ? (N >> 2) : ceil_div(N, 4);
   int gw, vec;
   if (N <= 32 * 4 * kRowRegsMaxVec) {  // a warp per row
     gw = 1;
@@ -350,7 +352,8 @@ int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_co
     // the two-phase split for what the grid cannot hold or align.
     rrs_plan c;
     if (!vector_ok) {
-      plan_two_phase(M, N, sm_count, p);
+      if (N <= kRowRegsAutoMaxN) plan_row_regs(M, N, sm_count, p, false);
+      else plan_two_phase(M, N, sm_count, p);
     } else if (N % 4 != 0) {
       if (row_regs_fits(N)) plan_row_regs(M, N, sm_count, p);
       else plan_two_phase(M, N, sm_count, p);
@@ -384,9 +387,9 @@ int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_co
       }
       return fail(RRS_ERR_UNSUPPORTED, "GRID needs 16-byte alignment, N % 4 == 0, cooperative launch");
     case RRS_PATH_ROW_REGS:
-      if (!vector_ok || !row_regs_fits(N))
-        return fail(RRS_ERR_UNSUPPORTED, "ROW_REGS needs 16-byte alignment and N <= 32768");
-      plan_row_regs(M, N, sm_count, p);
+      if (!row_regs_fits(N)) return fail(RRS_ERR_UNSUPPORTED, "ROW_REGS needs N <= 32768");
+      plan_row_regs(M, N, sm_count, p, vector_ok != 0);
+      p->vector_io = vector_ok ? 1 : 0;
       return RRS_OK;
     case RRS_PATH_CLUSTER:
       if (!vector_ok || !cluster_ok || !plan_cluster(M, N, p))

@@ -47,11 +47,31 @@ __device__ __forceinline__ float group_sum(float v, float* red, int gw, int lane
 template <int GW>
 __host__ __device__ constexpr int threads_for() { return (32 * GW < 128) ? 128 : 32 * GW; }
 
-// x, y: 16-byte aligned, ldx % 4 == 0, ldy % 4 == 0.  Row r is owned by
-// group (blockIdx.x * groups + group), striding by gridDim.x * groups.
+// Store of a thread's float4 slot i, in the slot layout of the kernel below.
+template <bool V4, int kGT>
+__device__ __forceinline__ void store_slot(float* yr, float4* yr4, int i, int gt, int n4, int N,
+                                           const float4& o) {
+  if constexpr (V4) {
+    const int c = i * kGT + gt;
+    if (c < n4) store_stream(yr4 + c, o);
+  } else {
+    const int j = 4 * i * kGT + gt;
+    if (j < N) store_stream(yr + j, o.x);
+    if (j + kGT < N) store_stream(yr + j + kGT, o.y);
+    if (j + 2 * kGT < N) store_stream(yr + j + 2 * kGT, o.z);
+    if (j + 3 * kGT < N) store_stream(yr + j + 3 * kGT, o.w);
+  }
+}
+
+// V4: x, y 16-byte aligned, ldx % 4 == 0, ldy % 4 == 0; float4 slot i of a
+// thread is columns 4 (i * groupsize + t) .. + 3, the N % 4 tail in `t`.
+// !V4 (any alignment and stride): scalar loads, slot i component k is column
+// (4 i + k) * groupsize + t, so every load instruction of a warp is one
+// contiguous run.  Row r is owned by group (blockIdx.x * groups + group),
+// striding by gridDim.x * groups.
 // log_out != 0 writes log y = (x - m) - log(s) instead of y.  x == y (same
 // stride) is safe: a group reads its whole row before writing it.
-template <int VEC, int GW>
+template <int VEC, int GW, bool V4>
 __global__ void __launch_bounds__(threads_for<GW>())
 softmax_row_regs_kernel(const float* x, float* y, int64_t M, int32_t N, int64_t ldx, int64_t ldy,
                         int32_t log_out) {
@@ -83,12 +103,24 @@ softmax_row_regs_kernel(const float* x, float* y, int64_t M, int32_t N, int64_t 
     float4* yr4 = reinterpret_cast<float4*>(yr);
 
     float4 v[VEC];
+    float t = kNeg;
+    if constexpr (V4) {
 #pragma unroll
-    for (int i = 0; i < VEC; ++i) {
-      const int c = i * kGT + gt;
-      v[i] = (c < n4) ? load_stream(xr4 + c) : make_float4(kNeg, kNeg, kNeg, kNeg);
+      for (int i = 0; i < VEC; ++i) {
+        const int c = i * kGT + gt;
+        v[i] = (c < n4) ? load_stream(xr4 + c) : make_float4(kNeg, kNeg, kNeg, kNeg);
+      }
+      t = (gt < rem) ? load_stream(xr + 4 * n4 + gt) : kNeg;  // ragged tail, N % 4 != 0
+    } else {
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) {
+        const int j = 4 * i * kGT + gt;
+        v[i].x = (j < N) ? load_stream(xr + j) : kNeg;
+        v[i].y = (j + kGT < N) ? load_stream(xr + j + kGT) : kNeg;
+        v[i].z = (j + 2 * kGT < N) ? load_stream(xr + j + 2 * kGT) : kNeg;
+        v[i].w = (j + 3 * kGT < N) ? load_stream(xr + j + 3 * kGT) : kNeg;
+      }
     }
-    float t = (gt < rem) ? load_stream(xr + 4 * n4 + gt) : kNeg;  // ragged tail, N % 4 != 0
 
     // (1) row max
     float m = t;
@@ -109,13 +141,11 @@ softmax_row_regs_kernel(const float* x, float* y, int64_t M, int32_t N, int64_t 
       const float ls = logf(s);
 #pragma unroll
       for (int i = 0; i < VEC; ++i) {
-        const int c = i * kGT + gt;
-        if (c < n4) {
-          store_stream(yr4 + c, make_float4(log_softmax_of(v[i].x, m, ls), log_softmax_of(v[i].y, m, ls),
-                                            log_softmax_of(v[i].z, m, ls), log_softmax_of(v[i].w, m, ls)));
-        }
+        const float4 o = make_float4(log_softmax_of(v[i].x, m, ls), log_softmax_of(v[i].y, m, ls),
+                                     log_softmax_of(v[i].z, m, ls), log_softmax_of(v[i].w, m, ls));
+        store_slot<V4, kGT>(yr, yr4, i, gt, n4, N, o);
       }
-      if (gt < rem) store_stream(yr + 4 * n4 + gt, log_softmax_of(t, m, ls));
+      if (V4 && gt < rem) store_stream(yr + 4 * n4 + gt, log_softmax_of(t, m, ls));
       continue;
     }
 
@@ -136,13 +166,10 @@ softmax_row_regs_kernel(const float* x, float* y, int64_t M, int32_t N, int64_t 
     // (5) divide: one reciprocal per row, then a multiply per element
     const float inv = 1.0f / s;
 #pragma unroll
-    for (int i = 0; i < VEC; ++i) {
-      const int c = i * kGT + gt;
-      if (c < n4) {
-        store_stream(yr4 + c, make_float4(v[i].x * inv, v[i].y * inv, v[i].z * inv, v[i].w * inv));
-      }
-    }
-    if (gt < rem) store_stream(yr + 4 * n4 + gt, t * inv);
+    for (int i = 0; i < VEC; ++i)
+      store_slot<V4, kGT>(yr, yr4, i, gt, n4, N,
+                          make_float4(v[i].x * inv, v[i].y * inv, v[i].z * inv, v[i].w * inv));
+    if (V4 && gt < rem) store_stream(yr + 4 * n4 + gt, t * inv);
   }
 }
 
@@ -151,8 +178,11 @@ cudaError_t launch_rr(const rrs_plan& p, const float* x, float* y, int64_t M, in
                       const Layout& l, cudaStream_t s) {
   constexpr int kThreads = threads_for<GW>();
   if (p.threads != kThreads) return cudaErrorInvalidConfiguration;
-  return launch_pdl(softmax_row_regs_kernel<VEC, GW>, dim3((unsigned)p.grid), dim3(kThreads), 0, s,
-                    0, x, y, M, (int32_t)N, l.ldx, l.ldy, (int32_t)l.log_out);
+  if (p.vector_io)
+    return launch_pdl(softmax_row_regs_kernel<VEC, GW, true>, dim3((unsigned)p.grid), dim3(kThreads),
+                      0, s, 0, x, y, M, (int32_t)N, l.ldx, l.ldy, (int32_t)l.log_out);
+  return launch_pdl(softmax_row_regs_kernel<VEC, GW, false>, dim3((unsigned)p.grid), dim3(kThreads), 0,
+                    s, 0, x, y, M, (int32_t)N, l.ldx, l.ldy, (int32_t)l.log_out);
 }
 
 }  // namespace

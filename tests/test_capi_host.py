@@ -107,8 +107,18 @@ def test_grid_plan_for_the_longest_rows(lib):
 
 
 def test_planner_unaligned_takes_scalar_path(lib):
-    p = plan(100, 1000, ld=1001, vector_ok=False)
+    p = plan(100, 1000, ld=1001, vector_ok=False)         # short rows: scalar warp-per-row
+    assert p["path_name"] == "row_regs" and p["vector_io"] == 0
+    assert p["vec"] * 32 * p["warps_per_row"] * 4 >= 1000
+    p = plan(100, 20000, ld=20001, vector_ok=False)       # long rows: scalar two-phase
     assert p["path_name"] == "two_phase" and p["vector_io"] == 0
+
+
+@pytest.mark.parametrize("N", [1, 3, 5, 127, 129, 1023, 1025, 4097, 16383, 16384])
+def test_scalar_row_plans_cover_the_row(lib, N):
+    p = plan(7, N, ld=N + 1, vector_ok=False)
+    assert p["path_name"] == "row_regs" and p["vector_io"] == 0
+    assert p["vec"] * 32 * p["warps_per_row"] * 4 >= N     # 4 scalars per slot
 
 
 @pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 31, 127, 128, 129, 255, 256, 257, 1000, 1024, 2047,
@@ -171,8 +181,7 @@ def test_forced_paths(lib):
         with pytest.raises(rrs.RRSError) as e:
             plan(4, 65536)
         assert e.value.status == UNSUPPORTED
-        with pytest.raises(rrs.RRSError):
-            plan(4, 1024, vector_ok=False)
+        assert plan(4, 1024, vector_ok=False)["vector_io"] == 0   # the scalar variant
     finally:
         rrs.force_path("auto", "auto")
 

@@ -10,6 +10,7 @@ from __future__ import annotations
 import numpy as np
 import pytest
 
+import oracle
 import row_reduction_softmax_gb300 as rrs
 import workloads
 from gpu_helpers import Guarded, check_softmax
@@ -28,7 +29,7 @@ def supports(path: str, N: int, ld: int) -> bool:
     """Whether a forced path takes this shape (vector paths need ld % 4 == 0)."""
     vector_ok = ld % 4 == 0
     if path == "row_regs":
-        return vector_ok and N <= 32768
+        return N <= 32768                      # scalar loads when not vector_ok
     if path == "cluster":
         return vector_ok and N <= 131072
     if path == "row_staged":
@@ -95,8 +96,12 @@ def test_unaligned_takes_scalar_path(M, N, ld, x_off, y_off):
     y, guards = run(x, N, ld, "auto", x_off, y_off)
     check_softmax(y, x, f"unaligned {M}x{N} ld={ld}")
     assert guards
+    if N <= 32768:
+        y, guards = run(x, N, ld, "row_regs", x_off, y_off)    # the scalar row kernel
+        check_softmax(y, x, f"unaligned row_regs {M}x{N} ld={ld}")
+        assert guards
     with pytest.raises(rrs.RRSError) as e:
-        run(x, N, ld, "row_regs", x_off, y_off)
+        run(x, N, ld, "cluster", x_off, y_off)
     assert e.value.status == 6
 
 
@@ -237,6 +242,51 @@ def test_full_size_long_rows_on_each_split_path(path):
     assert rrs.device_error() == 0
     rows = sampled_rows(w.M, w.seed)
     check_softmax(y[rows].cpu().numpy(), x_host[rows], f"{path} c5 sampled rows")
+    sums = y.double().sum(dim=1)
+    assert float((sums - 1.0).abs().max()) <= 1e-5
+    del x, y
+    torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------- size limits --
+
+def test_one_row_of_two_to_the_28():
+    """A single 1 GiB row: past what a cluster or the grid holds, so the two-phase path."""
+    N = 1 << 28
+    w = workloads.WORKLOADS["c5"].with_shape(1, N)
+    x_host = workloads.matrix(w)
+    x = torch.from_numpy(x_host).cuda()
+    y = torch.empty_like(x)
+    plan = rrs.plan_softmax(1, N)
+    assert plan["path_name"] == "two_phase"
+    rrs.softmax_rows(x, y)
+    torch.cuda.synchronize()
+    want = oracle.softmax_rows(x_host)[0]
+    rng = np.random.default_rng(28)
+    idx = np.concatenate([[0, N - 1, N // 2], rng.integers(0, N, size=200000)])
+    got = y[0, torch.from_numpy(idx).cuda()].cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(got - want[idx])) <= 2e-6
+    big = want[idx] >= 1e-30
+    assert np.max(np.abs(got[big] - want[idx][big]) / want[idx][big]) <= 1e-5
+    assert abs(float(y.double().sum()) - 1.0) <= 1e-5
+    s = torch.empty(1, device="cuda")
+    rrs.row_sum(x, s)
+    rrs_sum = float(s.cpu()[0])
+    assert abs(rrs_sum - float(np.sum(x_host, dtype=np.float64))) <= 1e-5 * float(np.abs(x_host).sum(dtype=np.float64))
+    del x, y
+    torch.cuda.empty_cache()
+
+
+def test_sixteen_million_rows_of_three():
+    """M = 2^24 rows of N = 3 (ld = 3: the scalar two-phase path, one thread per row chunk)."""
+    M, N = 1 << 24, 3
+    rng = np.random.default_rng(24)
+    x_host = rng.normal(0, 2, size=(M, N)).astype(np.float32)
+    x = torch.from_numpy(x_host).cuda()
+    y = rrs.softmax_rows(x)
+    torch.cuda.synchronize()
+    rows = sorted({0, M - 1, *rng.integers(0, M, size=5000).tolist()})
+    check_softmax(y[rows].cpu().numpy(), x_host[rows], "2^24 x 3 sampled rows")
     sums = y.double().sum(dim=1)
     assert float((sums - 1.0).abs().max()) <= 1e-5
     del x, y
