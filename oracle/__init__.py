@@ -47,6 +47,15 @@ Where the pages are silent the oracle takes these readings:
   High-Performance Programming", section 7.4.1), with the constants as
   printed there: 0.5 x (1 + tanh(0.79788456 (x + 0.044715 x^3))).
 
+* Attention is named, not defined, by the pages: the ingredients above
+  (elementwise, row-wise reduction, tiled reduction, tiled matmul) are what a
+  FlashAttention kernel fuses ("Kernels, Triton, XLA", end of "Reductions
+  and tiling"; "CS336 2026 Lecture 6: Kernels, Triton", the assignment
+  paragraph and the summary).  The reading taken is scaled dot-product
+  attention per head, O = softmax(Q K^T * scale) V with the row softmax
+  above over the keys, optionally causal (key j > query i masked with -inf,
+  the softmax's zero), and LSE = m + log(s) per query row.
+
 Pins (see ``tests/test_oracle_pins.py``): every function here is checked
 against values the pages print or the mathematics fixes, never against itself.
 """
@@ -66,6 +75,7 @@ __all__ = [
     "row_mean",
     "softmax_cols",
     "gelu",
+    "attention",
 ]
 
 
@@ -251,3 +261,34 @@ def gelu(x) -> np.ndarray:
     a = np.asarray(x, dtype=np.float64)
     inner = GELU_C * (a + GELU_K * a * a * a)
     return 0.5 * a * (1.0 + np.tanh(inner))
+
+
+def attention(q, k, v, causal: bool = False, scale: float | None = None):
+    """Scaled dot-product attention of one or more heads, in float64.
+
+    q: (..., L, d), k and v: (..., S, d).  Steps: (1) scores = q k^T * scale
+    (a library matmul), (2) causal: scores[i, j] = -inf for j > i + (S - L)
+    (queries aligned to the last keys), (3) P = softmax_rows(scores), the
+    pinned row softmax, (4) O = P v.  Returns (O, LSE) with LSE the log of
+    the row sum of exp(scores) (m + log s), -inf for an all-masked row.
+    scale defaults to 1 / sqrt(d).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    L, d = q.shape[-2], q.shape[-1]
+    S = k.shape[-2]
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    scores = np.matmul(q, np.swapaxes(k, -1, -2)) * scale          # (1)
+    if causal:                                                        # (2)
+        i = np.arange(L)[:, None]
+        j = np.arange(S)[None, :]
+        scores = np.where(j > i + (S - L), -np.inf, scores)
+    flat = scores.reshape(-1, S)
+    p = softmax_rows(flat).reshape(scores.shape)                      # (3)
+    out = np.matmul(p, v)                                             # (4)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        m = np.max(flat, axis=1)
+        lse = m + np.log(np.sum(np.exp(flat - m[:, None]), axis=1))
+    return out, lse.reshape(scores.shape[:-1])

@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 import oracle
-from test_oracle_pins import (GELU_CHECKS, LOG_SOFTMAX_CHECKS, MERGE_CHECKS, ROW_MAX_CHECKS, ROW_MEAN_CHECKS,
+from test_oracle_pins import (ATTENTION_CHECKS, GELU_CHECKS, LOG_SOFTMAX_CHECKS, MERGE_CHECKS, ROW_MAX_CHECKS, ROW_MEAN_CHECKS,
                               ROW_SUM_CHECKS, SOFTMAX_CHECKS, SOFTMAX_COLS_CHECKS)
 
 
@@ -309,3 +309,50 @@ GELU_MUTANTS = [gelu_no_half, gelu_square_term, gelu_minus_tanh, gelu_sigmoid_fo
 @pytest.mark.parametrize("mutant", GELU_MUTANTS, ids=lambda m: m.__name__)
 def test_gelu_mutant_is_caught(mutant):
     assert any(_caught(check, mutant) for check in GELU_CHECKS)
+
+
+
+def _att(q, k, v, causal=False, scale=None, *, flip=False, noscale=False, colsm=False, mask_diag=False):
+    q, k, v = (np.asarray(a, dtype=np.float64) for a in (q, k, v))
+    L, d, S = q.shape[-2], q.shape[-1], k.shape[-2]
+    sc = 1.0 / np.sqrt(d) if scale is None else scale
+    s = np.matmul(q, np.swapaxes(k, -1, -2)) * (1.0 if noscale else sc)
+    if causal:
+        i = np.arange(L)[:, None]
+        j = np.arange(S)[None, :]
+        s = np.where((j >= i + (S - L)) if mask_diag else (j > i + (S - L)), -np.inf, s)
+    with np.errstate(all="ignore"):
+        if colsm:
+            e = np.exp(s - s.max(axis=-2, keepdims=True))
+            p = e / e.sum(axis=-2, keepdims=True)
+        else:
+            e = np.exp(s - s.max(axis=-1, keepdims=True))
+            p = e / e.sum(axis=-1, keepdims=True)
+        m = s.max(axis=-1)
+        lse = m + np.log(np.exp(s - m[..., None]).sum(axis=-1))
+    o = np.matmul(p, v if not flip else v[..., ::-1, :])
+    return o, lse
+
+
+def att_no_scale(q, k, v, causal=False, scale=None):
+    return _att(q, k, v, causal, scale, noscale=True)
+
+
+def att_softmax_over_queries(q, k, v, causal=False, scale=None):
+    return _att(q, k, v, causal, scale, colsm=True)
+
+
+def att_mask_diagonal(q, k, v, causal=False, scale=None):
+    return _att(q, k, v, causal, scale, mask_diag=True)
+
+
+def att_reversed_values(q, k, v, causal=False, scale=None):
+    return _att(q, k, v, causal, scale, flip=True)
+
+
+ATTENTION_MUTANTS = [att_no_scale, att_softmax_over_queries, att_mask_diagonal, att_reversed_values]
+
+
+@pytest.mark.parametrize("mutant", ATTENTION_MUTANTS, ids=lambda m: m.__name__)
+def test_attention_mutant_is_caught(mutant):
+    assert any(_caught(check, mutant) for check in ATTENTION_CHECKS)

@@ -468,3 +468,80 @@ GELU_CHECKS = [check_gelu_closed_values, check_gelu_reflection, check_gelu_libra
 @pytest.mark.parametrize("check", GELU_CHECKS, ids=lambda c: c.__name__)
 def test_gelu_pins(check):
     check(oracle.gelu)
+
+
+
+# -------------------------------------------------------- attention pin checks ----
+
+def check_attn_uniform_scores(att):
+    """q = 0: every score is 0, so every output row is the mean of v's rows."""
+    rng = np.random.default_rng(51)
+    k = rng.normal(size=(2, 7, 16)); v = rng.normal(size=(2, 7, 16))
+    o, lse = att(np.zeros((2, 5, 16)), k, v)
+    assert np.max(np.abs(o - v.mean(axis=1, keepdims=True))) <= 1e-14
+    assert np.max(np.abs(lse - math.log(7))) <= 1e-14
+
+
+def check_attn_one_hot(att):
+    """A query far more aligned with one key than the rest returns that key's value row."""
+    d = 8
+    k = np.eye(d)[:6] * 1.0
+    v = np.arange(6 * d, dtype=np.float64).reshape(6, d)
+    q = np.zeros((3, d))
+    for i, j in enumerate((0, 3, 5)):
+        q[i, j] = 1e4
+    o, _ = att(q, k, v, scale=1.0)
+    for i, j in enumerate((0, 3, 5)):
+        assert np.array_equal(o[i], v[j])
+
+
+def check_attn_causal_first_row(att):
+    """Causal: query 0 sees key 0 only, so O[0] = v[0] and LSE[0] = score[0, 0]."""
+    rng = np.random.default_rng(52)
+    q = rng.normal(size=(4, 8)); k = rng.normal(size=(4, 8)); v = rng.normal(size=(4, 8))
+    o, lse = att(q, k, v, causal=True)
+    assert np.max(np.abs(o[0] - v[0])) <= 1e-15
+    assert abs(lse[0] - float(q[0] @ k[0]) / math.sqrt(8)) <= 1e-14
+    o2, _ = att(q[:1], k[:1], v[:1])                   # prefix = non-causal on the prefix
+    assert np.max(np.abs(o[:1] - o2)) <= 1e-15
+
+
+def check_attn_brute_force(att):
+    """Pure-Python loops with an exactly rounded normaliser."""
+    rng = np.random.default_rng(53)
+    for causal in (False, True):
+        q = rng.normal(size=(5, 3)); k = rng.normal(size=(5, 3)); v = rng.normal(size=(5, 4))
+        o, lse = att(q, k, v, causal=causal, scale=0.7)
+        for i in range(5):
+            js = [j for j in range(5) if not (causal and j > i)]
+            sc = [0.7 * sum(q[i, t] * k[j, t] for t in range(3)) for j in js]
+            den = math.fsum(math.exp(x) for x in sc)
+            assert abs(lse[i] - math.log(den)) <= 1e-13
+            for c in range(4):
+                num = math.fsum(math.exp(x) * v[j, c] for x, j in zip(sc, js))
+                assert abs(o[i, c] - num / den) <= 1e-13 * max(1.0, abs(num / den))
+
+
+def check_attn_library(att):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(54)
+    q = rng.normal(size=(2, 3, 17, 32)); k = rng.normal(size=(2, 3, 23, 32)); v = rng.normal(size=(2, 3, 23, 32))
+    for causal in (False, True):
+        o, _ = att(q, k, v, causal=causal)
+        tq, tk, tv = (torch.from_numpy(a) for a in (q, k, v))
+        if causal:   # torch's is_causal aligns to the top-left; build the bottom-right mask
+            L, S = 17, 23
+            mask = torch.ones(L, S, dtype=torch.bool).tril(diagonal=S - L)
+            t = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask)
+        else:
+            t = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv)
+        assert np.max(np.abs(o - t.numpy())) <= 1e-12
+
+
+ATTENTION_CHECKS = [check_attn_uniform_scores, check_attn_one_hot, check_attn_causal_first_row,
+                    check_attn_brute_force, check_attn_library]
+
+
+@pytest.mark.parametrize("check", ATTENTION_CHECKS, ids=lambda c: c.__name__)
+def test_attention_pins(check):
+    check(oracle.attention)
