@@ -15,7 +15,8 @@
  * and variants on the same skeleton (declared further down, each with the
  * passage it rests on): softmax_rows_ex (separate strides for x and y, in
  * place, log-softmax), log_softmax_rows, softmax_cols, row_max, row_mean,
- * and the elementwise gelu of the same pages.
+ * the elementwise gelu of the same pages, and the fused attention_fwd that
+ * the pages build towards.
  *
  * Conventions shared by every entry point
  * ----------------------------------------
@@ -187,6 +188,30 @@ RRS_API int row_mean(const float* x, float* out, int64_t M, int64_t N, int64_t l
  * Errors: RRS_ERR_INVALID_ARG (n < 0, null/host pointer, not 4-byte
  * aligned), RRS_ERR_ALIAS, RRS_ERR_CUDA. */
 RRS_API int gelu(const float* x, float* y, int64_t n, void* stream);
+
+/* Fused attention forward: for every head h < BH and query i < L,
+ *   O[h,i,:] = sum_j softmax_j(Q[h,i,:] . K[h,j,:] * scale) V[h,j,:],
+ *   LSE[h,i] = log sum_j exp(Q[h,i,:] . K[h,j,:] * scale).
+ * The pages name FlashAttention as the fusion of their elementwise, row-wise
+ * softmax and tiled matmul kernels ("Kernels, Triton, XLA", end of
+ * "Reductions and tiling"; "CS336 2026 Lecture 6: Kernels, Triton", the
+ * assignment paragraph); this is that fusion on the tcgen05 tensor cores,
+ * with the row softmax taken online over key tiles by the merge rule of
+ * softmax_rows' split paths.
+ * q: [BH, L, d], k and v: [BH, S, d], bf16 (IEEE bfloat16 bit patterns),
+ * contiguous, 16-byte aligned, device memory; o: [BH, L, d] fp32; lse: [BH, L]
+ * fp32 or NULL.  d is 64 or 128.  scale = 0 selects 1/sqrt(d).  causal != 0
+ * masks key j for query i when j > i + S - L (queries aligned to the last
+ * keys); a query that sees no key gets NaN and LSE -inf.  The products and
+ * sums accumulate in fp32; the softmax weights enter the second product
+ * rounded to bf16.  BH == 0 or L == 0: no work.  Errors: RRS_ERR_INVALID_ARG
+ * (sizes, d, scale, alignment, null/host pointers), RRS_ERR_ALIAS (an output
+ * overlaps an input or the other output), RRS_ERR_NOMEM (the V^T workspace,
+ * BH x d x S x 2 bytes, kept per stream), RRS_ERR_CUDA; a bounded wait that
+ * ran out shows in rrs_device_error. */
+RRS_API int attention_fwd(const void* q, const void* k, const void* v, float* o, float* lse,
+                          int64_t BH, int64_t L, int64_t S, int64_t d, int causal, float scale,
+                          void* stream);
 
 /* softmax_rows for callers that cannot allocate device memory.  The pages
  * have no counterpart: this is a deployment variant of the same operation.

@@ -26,7 +26,8 @@ __all__ = [
     "RRSError", "load_library", "softmax_rows", "log_softmax_rows", "row_sum", "row_max",
     "row_mean", "softmax_rows_ptr", "softmax_rows_ex_ptr", "log_softmax_rows_ptr", "row_sum_ptr",
     "row_max_ptr", "row_mean_ptr", "LOG_SOFTMAX", "softmax_cols", "softmax_cols_ptr",
-    "force_cols_path", "plan_softmax_cols", "COLS_PATHS", "gelu", "gelu_ptr",
+    "force_cols_path", "plan_softmax_cols", "COLS_PATHS", "gelu", "gelu_ptr", "attention",
+    "attention_ptr",
     "device_error", "release_workspace", "force_path", "plan_softmax", "plan_row_sum",
     "occupancy", "waves", "PATHS", "SUM_PATHS", "STATUS", "LIB_PATH",
 ]
@@ -77,6 +78,8 @@ _SIGNATURES = {
     "log_softmax_rows": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P]),
     "row_max": (ctypes.c_int, [_P, _P, _I64, _I64, _I64, _P]),
     "gelu": (ctypes.c_int, [_P, _P, _I64, _P]),
+    "attention_fwd": (ctypes.c_int, [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, ctypes.c_int,
+                                     ctypes.c_float, _P]),
     "softmax_cols": (ctypes.c_int, [_P, _I64, _P, _I64, _I64, _I64, ctypes.c_int, _P]),
     "rrs_force_cols_path": (ctypes.c_int, [ctypes.c_int]),
     "rrs_plan_softmax_cols": (ctypes.c_int, [_I64, _I64, _I64, ctypes.c_int, ctypes.c_int,
@@ -154,6 +157,13 @@ def softmax_cols_ptr(x: int, ldx: int, y: int, ldy: int, M: int, N: int, flags: 
                      stream: int = 0) -> None:
     """C ``softmax_cols``: softmax down each column (LOG_SOFTMAX flag for the log form)."""
     _check(load_library().softmax_cols(x, ldx, y, ldy, M, N, flags, stream), "softmax_cols")
+
+
+def attention_ptr(q: int, k: int, v: int, o: int, lse: int, BH: int, L: int, S: int, d: int,
+                  causal: bool = False, scale: float = 0.0, stream: int = 0) -> None:
+    """C ``attention_fwd`` on raw device addresses (bf16 q, k, v; fp32 o and lse)."""
+    _check(load_library().attention_fwd(q, k, v, o, lse or None, BH, L, S, d, int(bool(causal)),
+                                        float(scale), stream), "attention_fwd")
 
 
 def gelu_ptr(x: int, y: int, n: int, stream: int = 0) -> None:
@@ -236,6 +246,31 @@ def softmax_cols(x, y=None, stream=None, log=False):
         softmax_cols_ptr(x.data_ptr(), ld, y.data_ptr(), ldy, M, N, LOG_SOFTMAX if log else 0,
                          _stream_handle(stream))
     return y
+
+
+def attention(q, k, v, causal=False, scale=0.0, stream=None, want_lse=True):
+    """Fused attention forward of CUDA bf16 tensors q [..., L, d], k and v [..., S, d].
+
+    Returns (O fp32 [..., L, d], LSE fp32 [..., L] or None).  scale 0 means 1/sqrt(d).
+    """
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be a CUDA bfloat16 tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    L, d = q.shape[-2], q.shape[-1]
+    S = k.shape[-2]
+    if k.shape[-1] != d or v.shape != k.shape or q.shape[:-2] != k.shape[:-2]:
+        raise ValueError("q [..., L, d], k and v [..., S, d] with the same leading dims")
+    BH = int(q.numel() // max(L * d, 1)) if L * d else 0
+    o = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device) if want_lse else None
+    with torch.cuda.device(q.device):
+        attention_ptr(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                      lse.data_ptr() if lse is not None else 0, BH, L, S, d, causal, scale,
+                      _stream_handle(stream))
+    return o, lse
 
 
 def gelu(x, y=None, stream=None):

@@ -410,7 +410,7 @@ int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_co
 // fewer, fuller CTAs per band win, and beyond 4 CTAs per band the two-phase
 // path is faster, so the planner takes the cluster only up to cs = 4.  COLS_TWO_PHASE: row
 // chunks sized for about 4 CTAs per SM over all bands.
-enum WorkspaceKindCols { kWsCols = 3 };
+enum WorkspaceKindCols { kWsCols = 3, kWsAttn = 4 };
 
 constexpr int64_t kColsAutoMaxCluster = 4;
 
@@ -836,10 +836,55 @@ RRS_API int gelu(const float* x, float* y, int64_t n, void* stream) {
   return RRS_OK;
 }
 
+RRS_API int attention_fwd(const void* q, const void* k, const void* v, float* o, float* lse,
+                          int64_t BH, int64_t L, int64_t S, int64_t d, int causal, float scale,
+                          void* stream) {
+  g_last_error.clear();
+  if (BH < 0 || L < 0 || S < 0) return fail(RRS_ERR_INVALID_ARG, "BH, L and S must be >= 0");
+  if (d != 64 && d != 128) return fail(RRS_ERR_INVALID_ARG, "head dimension must be 64 or 128");
+  if (BH == 0 || L == 0) return RRS_OK;
+  if (S == 0) return fail(RRS_ERR_INVALID_ARG, "S must be >= 1 when L >= 1");
+  if (BH > 65535 || L > INT_MAX - 256 || S > INT_MAX - 256)
+    return fail(RRS_ERR_INVALID_ARG, "BH <= 65535, L and S < 2^31 - 256");
+  if (!(scale >= 0.f) || std::isinf(scale)) return fail(RRS_ERR_INVALID_ARG, "scale must be finite and >= 0");
+  if (!q || !k || !v || !o) return fail(RRS_ERR_INVALID_ARG, "null pointer");
+  const void* ptrs[4] = {q, k, v, o};
+  for (const void* p : ptrs)
+    if (reinterpret_cast<uintptr_t>(p) % 16)
+      return fail(RRS_ERR_INVALID_ARG, "q, k, v and o must be 16-byte aligned");
+  if (lse && reinterpret_cast<uintptr_t>(lse) % 4) return fail(RRS_ERR_INVALID_ARG, "lse must be 4-byte aligned");
+  const int64_t qb = BH * L * d * 2, kb = BH * S * d * 2, ob = BH * L * d * 4, lb = BH * L * 4;
+  if (overlaps(o, ob, q, qb) || overlaps(o, ob, k, kb) || overlaps(o, ob, v, kb) ||
+      (lse && (overlaps(lse, lb, q, qb) || overlaps(lse, lb, k, kb) || overlaps(lse, lb, v, kb) ||
+               overlaps(lse, lb, o, ob))))
+    return fail(RRS_ERR_ALIAS, "outputs overlap inputs or each other");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  int st;
+  if ((st = check_device_pointer(q, dev, "q")) != RRS_OK) return st;
+  if ((st = check_device_pointer(k, dev, "k")) != RRS_OK) return st;
+  if ((st = check_device_pointer(v, dev, "v")) != RRS_OK) return st;
+  if ((st = check_device_pointer(o, dev, "o")) != RRS_OK) return st;
+  if (lse && (st = check_device_pointer(lse, dev, "lse")) != RRS_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void* ws = nullptr;
+  const size_t ws_bytes = (size_t)BH * d * attention_vt_stride((int)S) * 2;
+  if ((st = get_workspace(dev, s, kWsAttn, ws_bytes, &ws)) != RRS_OK) return st;
+  const float sc = scale > 0.f ? scale : 1.0f / std::sqrt((float)d);
+  e = launch_attention(static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k),
+                       static_cast<const uint16_t*>(v), static_cast<uint16_t*>(ws), o, lse, (int)BH,
+                       (int)L, (int)S, (int)d, causal ? 1 : 0, sc, s);
+  if (e != cudaSuccess) return fail_cuda(e, "attention_fwd launch");
+  return RRS_OK;
+}
+
 RRS_API int rrs_device_error(void* stream) {
-  unsigned v = 0;
+  unsigned v = 0, w = 0;
   cudaError_t e = read_and_clear_staged_error(static_cast<cudaStream_t>(stream), &v);
+  if (e == cudaSuccess) e = read_and_clear_attn_error(static_cast<cudaStream_t>(stream), &w);
   if (e != cudaSuccess) return fail_cuda(e, "rrs_device_error");
+  v |= w;
   return v ? fail(RRS_ERR_TIMEOUT, "a split-row kernel stopped waiting for its peers") : RRS_OK;
 }
 

@@ -30,8 +30,8 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-__all__ = ["Workload", "WORKLOADS", "VARIANT_WORKLOADS", "row_values", "matrix",
-           "spike_mask_counts"]
+__all__ = ["Workload", "WORKLOADS", "VARIANT_WORKLOADS", "AttentionWorkload", "ATTENTION_WORKLOADS",
+           "row_values", "matrix", "spike_mask_counts", "to_bf16_bits", "attention_inputs"]
 
 
 @dataclass(frozen=True)
@@ -139,3 +139,58 @@ def matrix(w: Workload, ld: int | None = None, rows=None, pad_value=np.nan,
         out[i, :w.N] = row_values(w, r)
     return out
 
+
+
+# ------------------------------------------------------------- attention ----
+
+@dataclass(frozen=True)
+class AttentionWorkload:
+    """Q, K, V of B x H heads: [B*H, L, d] and [B*H, S, d], Normal(0, 1), bf16."""
+    name: str
+    B: int
+    H: int
+    L: int
+    S: int
+    d: int
+    causal: bool
+    seed: int
+
+    @property
+    def BH(self) -> int:
+        return self.B * self.H
+
+    def with_shape(self, BH: int, L: int, S: int, d: int, causal: bool) -> "AttentionWorkload":
+        return AttentionWorkload(self.name, 1, BH, L, S, d, causal, self.seed)
+
+
+# The pages give no attention sizes; this is a common training shape for a
+# 128-wide head (B = 4 sequences of 4096 tokens, 16 heads), both unmasked and
+# causal.
+ATTENTION_WORKLOADS = {
+    "attn": AttentionWorkload("attn", 4, 16, 4096, 4096, 128, False, 7),
+    "attn_causal": AttentionWorkload("attn_causal", 4, 16, 4096, 4096, 128, True, 8),
+}
+
+
+def to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """float32 -> bfloat16 bit patterns (uint16), rounding to nearest, ties to even."""
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    nan = np.isnan(np.asarray(a, dtype=np.float32))
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    r[nan] = 0x7FC0
+    return r
+
+
+def attention_inputs(w: AttentionWorkload, heads=None):
+    """(q, k, v) as bf16 bit patterns (uint16 arrays) for the heads listed
+    (all by default).  Each head is drawn from its own stream keyed by
+    (seed, head, tensor), so one head can be regenerated alone."""
+    hs = range(w.BH) if heads is None else heads
+    out = []
+    for t, n in enumerate((w.L, w.S, w.S)):
+        arr = np.empty((len(hs), n, w.d), dtype=np.uint16)
+        for i, h in enumerate(hs):
+            g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([w.seed, int(h), t])))
+            arr[i] = to_bf16_bits(g.standard_normal((n, w.d), dtype=np.float32))
+        out.append(arr)
+    return tuple(out)
