@@ -11,14 +11,18 @@
 //
 // One CTA owns 128 query rows of one head and walks the key tiles of 128:
 //   warp 4, one thread: TMA loads of Q (once), K and V^T tiles (two-stage
-//     ring), and the tcgen05.mma issue: S = Q K^T into TMEM columns
-//     [0, 128), then O_j = P V into TMEM columns [128, 128 + d);
-//   warps 0..3: thread r owns query row r (TMEM lane r): reads its S row
-//     from TMEM (32 columns per tcgen05.ld), takes the row max and
-//     p = 2^(s log2e scale - m) on the SFU, writes p as bf16 into the
-//     128-byte-swizzled P tile in shared memory (the A operand of the second
-//     MMA), keeps the row sum l in fp32, and accumulates O in registers:
-//     O = alpha O + O_j.
+//     rings with their own barriers, K two tiles ahead), and the tcgen05.mma
+//     issue: S_{j+1} = Q K_{j+1}^T into the second of two TMEM S buffers
+//     while the softmax warps read S_j, then O_j = P_j V_j into TMEM columns
+//     [256, 256 + d) once P_j is written;
+//   warps 0..7: query row r (TMEM lane r) belongs to warps r / 32 and
+//     r / 32 + 4, each taking half of the row's columns: they read S from
+//     TMEM (32 columns per tcgen05.ld), exchange their halves' maxima through
+//     shared memory, take p = 2^(s log2e scale - m) on the SFU, write p as
+//     bf16 into the 128-byte-swizzled P tile in shared memory (the A operand
+//     of the second MMA), keep their halves' row sums in fp32, and, when the
+//     row max rises, rescale their half of O, which accumulates in TMEM
+//     across key tiles (O = alpha O + P_j V_j).
 // Operands are bf16 (K-major, 128-byte swizzle, 1024-byte atoms, written by
 // TMA for Q, K, V^T and by the softmax threads for P); accumulators fp32.
 // V is transposed to V^T (d x S per head) by a small kernel first, so that
@@ -48,8 +52,9 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr unsigned kErrTimeout = 1u;
 constexpr int kBM = 128;               // query rows per CTA
 constexpr int kBN = 128;               // keys per tile
-constexpr int kAttnThreads = 160;      // warps 0..3 softmax, warp 4 loads + MMA issue
-constexpr int kIssuerWarp = 4;
+constexpr int kSoftmaxWarps = 8;       // two warps per group of 32 query rows
+constexpr int kAttnThreads = 32 * (kSoftmaxWarps + 1);   // + the load / MMA-issue warp
+constexpr int kIssuerWarp = kSoftmaxWarps;
 
 template <int D>
 struct Layout2 {
@@ -62,9 +67,10 @@ struct Layout2 {
   static constexpr int kV = kK + 2 * kKBytes;           // 2 stages
   static constexpr int kP = kV + 2 * kVBytes;
   static constexpr int kBar = kP + kPBytes;             // mbarriers and the TMEM address
-  static constexpr int kBytes = kBar + 128;
+  static constexpr int kX = kBar + 128;                 // row-max exchange [2][2][128], row sums [2][128]
+  static constexpr int kBytes = kX + (2 * 2 * kBM + 2 * kBM) * 4;
   static constexpr int kAlloc = kBytes + 1024;          // slack to align the base to 1024
-  static constexpr uint32_t kTmemCols = 256;            // S: 128 columns, O_j: D columns
+  static constexpr uint32_t kTmemCols = 512;            // S: 2 x 128 columns, O_j: D columns
 };
 
 // Bounded parity wait; false (and the error word set) if it ran out or the
@@ -106,7 +112,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-// grid (ceil(L / 128), BH); block 160.  O, LSE: fp32, O row-major [BH, L, D].
+// grid (ceil(L / 128), BH); block 288.  O, LSE: fp32, O row-major [BH, L, D].
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
 attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -118,13 +124,15 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBar);
   uint64_t* bar_q = bars + 0;
-  uint64_t* kv_full = bars + 1;    // [2]
-  uint64_t* kv_empty = bars + 3;   // [2]
-  uint64_t* bar_s = bars + 5;      // S_j in TMEM
-  uint64_t* bar_p = bars + 6;      // S_j read and P_j written (128 arrivals)
-  uint64_t* bar_o = bars + 7;      // O_j in TMEM
-  uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(bars + 8);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 9);
+  uint64_t* k_full = bars + 1;     // [2] K tile landed
+  uint64_t* k_empty = bars + 3;    // [2] S MMA of that K tile done
+  uint64_t* v_full = bars + 5;     // [2] V^T tile landed
+  uint64_t* v_empty = bars + 7;    // [2] P V MMA of that tile done
+  uint64_t* bar_s = bars + 9;      // [2] S_j in TMEM buffer j % 2
+  uint64_t* bar_p = bars + 11;     // S_j read and P_j written (128 arrivals)
+  uint64_t* bar_o = bars + 12;     // O_j in TMEM
+  uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(bars + 13);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 14);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.y;
@@ -139,12 +147,14 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
-    mbar_init(&kv_full[0], 1);
-    mbar_init(&kv_full[1], 1);
-    mbar_init(&kv_empty[0], 1);
-    mbar_init(&kv_empty[1], 1);
-    mbar_init(bar_s, 1);
-    mbar_init(bar_p, kBM);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+      mbar_init(&bar_s[i], 1);
+    }
+    mbar_init(bar_p, 32 * kSoftmaxWarps);
     mbar_init(bar_o, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -157,8 +167,8 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_base_slot;
-  const uint32_t tmem_s = tmem;            // columns [0, 128)
-  const uint32_t tmem_o = tmem + kBN;      // columns [128, 128 + D)
+  const uint32_t tmem_s = tmem;              // two S buffers: columns [0, 128) and [128, 256)
+  const uint32_t tmem_o = tmem + 2 * kBN;    // columns [256, 256 + D)
   const uint32_t sQ = smem_addr(smem + Lay::kQ);
   const uint32_t sK = smem_addr(smem + Lay::kK);
   const uint32_t sV = smem_addr(smem + Lay::kV);
@@ -166,180 +176,217 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
   pdl_entry();
 
   if (warp == kIssuerWarp) {
+    // One thread: loads two tiles ahead, S_{j+1} (into the other S buffer)
+    // while the softmax warps work on S_j, then P_j V_j once P_j is written.
     if (lane == 0 && n_tiles > 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(kBM, kBN);
       constexpr uint32_t kIdO = idesc_bf16_f32(kBM, D);
-      constexpr uint32_t kKVBytes = Lay::kKBytes + Lay::kVBytes;
-      int issued = 0;                       // KV tiles whose loads were issued
-      auto load_kv = [&](int j) {
+      int k_loads = 0, v_loads = 0, pv_done = 0;
+      auto load_k = [&](int j) {
         const int st = j & 1;
-        mbar_arrive_expect_tx(&kv_full[st], kKVBytes);
+        mbar_arrive_expect_tx(&k_full[st], Lay::kKBytes);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d(smem + Lay::kK + st * Lay::kKBytes + c * kBN * 128, &tmk, c * 64, j * kBN, bh,
-                      &kv_full[st]);
+                      &k_full[st]);
+        ++k_loads;
+      };
+      auto load_v = [&](int j) {
+        const int st = j & 1;
+        mbar_arrive_expect_tx(&v_full[st], Lay::kVBytes);
 #pragma unroll
         for (int c = 0; c < kBN / 64; ++c)
           tma_load_3d(smem + Lay::kV + st * Lay::kVBytes + c * D * 128, &tmv, j * kBN + c * 64, 0, bh,
-                      &kv_full[st]);
-        ++issued;
+                      &v_full[st]);
+        ++v_loads;
+      };
+      auto issue_s = [&](int j) -> bool {
+        const int st = j & 1;
+        if (!wait_bar(&k_full[st], (uint32_t)((j >> 1) & 1), abort_flag)) return false;
+        tc_fence_after_sync();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (uint32_t)((kk >> 2) * 128 * 128 + (kk & 3) * 32);
+          mma_bf16(tmem_s + st * kBN, smem_desc_sw128(sQ + off),
+                   smem_desc_sw128(sK + st * Lay::kKBytes + off), kIdS, kk > 0);
+        }
+        mma_commit(&bar_s[st]);
+        mma_commit(&k_empty[st]);
+        return true;
       };
       mbar_arrive_expect_tx(bar_q, Lay::kQBytes);
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) tma_load_3d(smem + Lay::kQ + c * kBM * 128, &tmq, c * 64, q0, bh, bar_q);
-      load_kv(0);
-      if (n_tiles > 1) load_kv(1);
-      bool ok = wait_bar(bar_q, 0, abort_flag);
-      auto issue_s = [&](int j) {
-        const int st = j & 1;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (uint32_t)((kk >> 2) * 128 * 128 + (kk & 3) * 32);
-          mma_bf16(tmem_s, smem_desc_sw128(sQ + off), smem_desc_sw128(sK + st * Lay::kKBytes + off),
-                   kIdS, kk > 0);
-        }
-        mma_commit(bar_s);
-      };
-      int mma_tiles = 0;                    // tiles whose S MMA was issued
-      if (ok && (ok = wait_bar(&kv_full[0], 0, abort_flag))) {
-        issue_s(0);
-        mma_tiles = 1;
+      load_k(0);
+      load_v(0);
+      if (n_tiles > 1) {
+        load_k(1);
+        load_v(1);
       }
+      bool ok = wait_bar(bar_q, 0, abort_flag);
+      ok = ok && issue_s(0);
+      if (n_tiles > 1) ok = ok && issue_s(1);
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int st = j & 1;
-        if (!(ok = wait_bar(bar_p, (uint32_t)(j & 1), abort_flag))) break;   // S_j read, P_j written
-        tc_fence_after_sync();
-        if (j + 1 < n_tiles) {
-          if (!(ok = wait_bar(&kv_full[(j + 1) & 1], (uint32_t)(((j + 1) >> 1) & 1), abort_flag))) break;
-          issue_s(j + 1);
-          mma_tiles = j + 2;
+        const uint32_t use = (uint32_t)((j >> 1) & 1);
+        if (j + 2 < n_tiles) {   // K stage st is free once S_j is done
+          if (!(ok = wait_bar(&k_empty[st], use, abort_flag))) break;
+          load_k(j + 2);
         }
+        if (!(ok = wait_bar(bar_p, (uint32_t)(j & 1), abort_flag))) break;   // S_j read, P_j written
+        if (!(ok = wait_bar(&v_full[st], use, abort_flag))) break;
+        tc_fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           const uint32_t offp = (uint32_t)((kk >> 2) * kBM * 128 + (kk & 3) * 32);
           const uint32_t offv = (uint32_t)((kk >> 2) * D * 128 + (kk & 3) * 32);
           mma_bf16(tmem_o, smem_desc_sw128(sP + offp), smem_desc_sw128(sV + st * Lay::kVBytes + offv),
-                   kIdO, kk > 0);
+                   kIdO, kk > 0 || j > 0);   // O accumulates in TMEM across key tiles
         }
         mma_commit(bar_o);
-        mma_commit(&kv_empty[st]);
-        if (j + 2 < n_tiles) {
-          if (!(ok = wait_bar(&kv_empty[st], (uint32_t)((j >> 1) & 1), abort_flag))) break;
-          load_kv(j + 2);
+        mma_commit(&v_empty[st]);
+        ++pv_done;
+        if (j + 2 < n_tiles) {   // V stage st is free once P_j V_j is done
+          if (!(ok = wait_bar(&v_empty[st], use, abort_flag))) break;
+          load_v(j + 2);
+          ok = issue_s(j + 2);   // S buffer st was read by the softmax warps (bar_p above)
         }
       }
       if (!ok) {
-        // drain: copies issued but not yet waited on, and the last MMAs
-        for (int j = 0; j < issued; ++j) {
-          const uint64_t t0 = global_timer_ns();
-          while (!mbar_try_wait(&kv_full[j & 1], (uint32_t)((j >> 1) & 1)) &&
-                 global_timer_ns() - t0 < kWaitLimitNs) {
-          }
-        }
-        (void)mma_tiles;
-        mma_commit(bar_o);   // one more arrival once everything issued has completed
+        // drain what was issued: the last load of each stage, then every MMA
         const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(bar_o, (uint32_t)(n_tiles & 1)) && global_timer_ns() - t0 < kWaitLimitNs) {
+        for (int st = 0; st < 2; ++st) {
+          const int nk = (k_loads - st + 1) / 2, nv = (v_loads - st + 1) / 2;   // loads into stage st
+          if (nk > 0)
+            while (!mbar_try_wait(&k_full[st], (uint32_t)((nk - 1) & 1)) && global_timer_ns() - t0 < kWaitLimitNs) {
+            }
+          if (nv > 0)
+            while (!mbar_try_wait(&v_full[st], (uint32_t)((nv - 1) & 1)) && global_timer_ns() - t0 < kWaitLimitNs) {
+            }
+        }
+        mma_commit(bar_o);   // one more arrival once everything issued has completed
+        while (!mbar_try_wait(bar_o, (uint32_t)(pv_done & 1)) && global_timer_ns() - t0 < 2 * kWaitLimitNs) {
         }
       }
     }
     __syncwarp();   // lanes 1..31 wait here for the issuing lane
   } else {
-    // ---- softmax warps: thread r owns query row r ----
-    const int r = threadIdx.x;                              // 0..127
+    // ---- softmax warps: warps w and w + 4 share query rows 32 (w % 4) .. + 31
+    // (TMEM lanes); warp w < 4 takes the first half of every key tile's
+    // columns and of O's columns, warp w + 4 the second half ----
+    constexpr int kHalf = kBN / 2;      // key columns per thread and tile
+    constexpr int kDHalf = D / 2;       // O columns per thread
+    const int h = warp >> 2;
+    const int r = ((warp & 3) << 5) + lane;                 // query row within the tile
     const int qrow = q0 + r;
-    const uint32_t lane_off = (uint32_t)((warp * 32) << 16);
+    const uint32_t lane_off = (uint32_t)(((warp & 3) * 32) << 16);
+    const int pair_bar = 1 + (warp & 3);                     // named barrier of the warp pair
+    float* xmax = reinterpret_cast<float*>(smem + Lay::kX);          // [tile parity][half][row]
+    float* xsum = xmax + 2 * 2 * kBM;                                 // [half][row]
     const float kNeg = neg_inf();
-    float o[D];
-#pragma unroll
-    for (int c = 0; c < D; ++c) o[c] = 0.f;
-    float m = kNeg, l = 0.f, alpha_prev = 0.f;
+    const int kmax = causal ? min(S - 1, qrow + (S - L)) : S - 1;   // last visible key
+    float m = kNeg, l = 0.f;
     bool ok = true;
-    // waits are decided warp-uniformly, so the .sync.aligned TMEM loads below
-    // always run on a converged warp
+    // Waits are decided warp-uniformly, so the .sync.aligned TMEM accesses
+    // below always run on a converged warp.  After a failed wait the loop
+    // still runs to the end (the waits then return at once and the values
+    // are discarded), so both warps of a pair meet at every pair barrier.
     for (int j = 0; j < n_tiles; ++j) {
-      if (!(ok = __all_sync(kFullMask, wait_bar(bar_s, (uint32_t)(j & 1), abort_flag)))) break;
+      const uint32_t s_buf = tmem_s + (uint32_t)((j & 1) * kBN + h * kHalf) + lane_off;
+      ok = __all_sync(kFullMask, ok && wait_bar(&bar_s[j & 1], (uint32_t)((j >> 1) & 1), abort_flag));
       tc_fence_after_sync();
-      const int k0 = j * kBN;
-      const int kmax = causal ? min(S - 1, qrow + (S - L)) : S - 1;   // last visible key
-      // pass 1: row max of the scaled, masked scores (log2 units)
+      const int k0 = j * kBN + h * kHalf;
+      // pass 1: max of this half of the row (scaled, masked, log2 units), then of the pair
       float tmax = kNeg;
 #pragma unroll
-      for (int cb = 0; cb < kBN / 32; ++cb) {
+      for (int cb = 0; cb < kHalf / 32; ++cb) {
         float v[32];
-        tmem_ld32(tmem_s + lane_off + cb * 32, v);
+        tmem_ld32(s_buf + cb * 32, v);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int key = k0 + cb * 32 + i;
-          const float sv = (key <= kmax) ? v[i] * scale_log2e : kNeg;
-          tmax = max_nan(tmax, sv);
-        }
+        for (int i = 0; i < 32; ++i)
+          tmax = max_nan(tmax, (k0 + cb * 32 + i <= kmax) ? v[i] * scale_log2e : kNeg);
       }
+      float* xm = xmax + (j & 1) * 2 * kBM;
+      xm[h * kBM + r] = tmax;
+      named_barrier(pair_bar, 64);
+      tmax = max_nan(tmax, xm[(1 - h) * kBM + r]);
       const float m_new = max_nan(m, tmax);
       const float alpha = (m == kNeg) ? 0.f : exp2_sfu(m - m_new);
-      // O_{j-1} is complete: fold it in at the previous tile's scale
+      // O holds the tiles before j at scale m: once P_{j-1} V_{j-1} is in, rescale it to m_new
       if (j > 0) {
-        if (!(ok = __all_sync(kFullMask, wait_bar(bar_o, (uint32_t)((j - 1) & 1), abort_flag)))) break;
+        ok = __all_sync(kFullMask, ok && wait_bar(bar_o, (uint32_t)((j - 1) & 1), abort_flag));
         tc_fence_after_sync();
+        if (ok && __any_sync(kFullMask, alpha != 1.f)) {
 #pragma unroll
-        for (int cb = 0; cb < D / 32; ++cb) {
-          float v[32];
-          tmem_ld32(tmem_o + lane_off + cb * 32, v);
-          tmem_wait_ld();
+          for (int cb = 0; cb < kDHalf / 32; ++cb) {
+            float v[32];
+            const uint32_t ta = tmem_o + lane_off + (uint32_t)(h * kDHalf + cb * 32);
+            tmem_ld32(ta, v);
+            tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[cb * 32 + i] = o[cb * 32 + i] * alpha_prev + v[i];
+            for (int i = 0; i < 32; ++i) v[i] *= alpha;
+            tmem_st32(ta, v);
+          }
+          tmem_wait_st();
         }
       }
-      // pass 2: p = 2^(s - m_new), row sum in fp32, P row as bf16 into the swizzled tile
+      // pass 2: p = 2^(s - m_new), this half's sum in fp32, P as bf16 into the swizzled tile
       float psum = 0.f;
 #pragma unroll
-      for (int cb = 0; cb < kBN / 32; ++cb) {
+      for (int cb = 0; cb < kHalf / 32; ++cb) {
         float v[32];
-        tmem_ld32(tmem_s + lane_off + cb * 32, v);
+        tmem_ld32(s_buf + cb * 32, v);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const int key = k0 + cb * 32 + i;
-          v[i] = (key <= kmax && m_new != kNeg) ? exp2_sfu(v[i] * scale_log2e - m_new) : 0.f;
+          v[i] = (k0 + cb * 32 + i <= kmax && m_new != kNeg) ? exp2_sfu(v[i] * scale_log2e - m_new) : 0.f;
           psum += v[i];
         }
-        // 32 bf16 = four 16-byte chunks, chunk index q = 4 (cb % 2) + t in atom column cb / 2
+        // keys h * 64 + cb * 32 + 8 t .. + 7: atom column h, 16-byte chunk 4 cb + t
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-          st_shared_v4(sw128_chunk(sP, kBM, r, cb >> 1, 4 * (cb & 1) + t),
+          st_shared_v4(sw128_chunk(sP, kBM, r, h, 4 * cb + t),
                        pack_bf16(v[8 * t + 0], v[8 * t + 1]), pack_bf16(v[8 * t + 2], v[8 * t + 3]),
                        pack_bf16(v[8 * t + 4], v[8 * t + 5]), pack_bf16(v[8 * t + 6], v[8 * t + 7]));
         }
       }
       l = l * alpha + psum;
       m = m_new;
-      alpha_prev = alpha;
-      fence_proxy_async_smem();   // P visible to the tensor cores
+      fence_proxy_async_smem();   // P (and the rescaled O) visible to the tensor cores
       tc_fence_before_sync();
       mbar_arrive(bar_p);
     }
-    if (ok && n_tiles > 0) {
-      if (__all_sync(kFullMask, wait_bar(bar_o, (uint32_t)((n_tiles - 1) & 1), abort_flag))) {
-        tc_fence_after_sync();
+    // the row sum is the pair's two halves
+    xsum[h * kBM + r] = l;
+    named_barrier(pair_bar, 64);
+    const float l_row = l + xsum[(1 - h) * kBM + r];
+    const bool have_o =
+        __all_sync(kFullMask, ok && n_tiles > 0 && wait_bar(bar_o, (uint32_t)((n_tiles - 1) & 1), abort_flag));
+    if (have_o) tc_fence_after_sync();
+    if (!*abort_flag && (have_o || n_tiles == 0)) {
+      // O = O / l (a row that sees no key: 0 / 0 = NaN, its LSE -inf)
+      const float inv = 1.0f / l_row;
+      float* orow = O + ((size_t)bh * L + qrow) * D + h * kDHalf;
 #pragma unroll
-        for (int cb = 0; cb < D / 32; ++cb) {
-          float v[32];
-          tmem_ld32(tmem_o + lane_off + cb * 32, v);
+      for (int cb = 0; cb < kDHalf / 32; ++cb) {
+        float v[32];
+        if (have_o) {
+          tmem_ld32(tmem_o + lane_off + (uint32_t)(h * kDHalf + cb * 32), v);
           tmem_wait_ld();
+        } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[cb * 32 + i] = o[cb * 32 + i] * alpha_prev + v[i];
+          for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        }
+        if (qrow < L) {
+          float4* o4 = reinterpret_cast<float4*>(orow + cb * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            o4[i] = make_float4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
         }
       }
-    }
-    // O = O / l (an all-masked row: 0 / 0 = NaN, its LSE -inf)
-    if (qrow < L && !*abort_flag) {
-      const float inv = 1.0f / l;
-      float4* orow = reinterpret_cast<float4*>(O + ((size_t)bh * L + qrow) * D);
-#pragma unroll
-      for (int c = 0; c < D / 4; ++c)
-        orow[c] = make_float4(o[4 * c] * inv, o[4 * c + 1] * inv, o[4 * c + 2] * inv, o[4 * c + 3] * inv);
-      if (LSE) LSE[(size_t)bh * L + qrow] = (m == kNeg) ? kNeg : (m + log2f(l)) * 0.69314718055994531f;
+      if (LSE && h == 0 && qrow < L)
+        LSE[(size_t)bh * L + qrow] = (m == kNeg) ? kNeg : (m + log2f(l_row)) * 0.69314718055994531f;
     }
   }
   tc_fence_before_sync();
