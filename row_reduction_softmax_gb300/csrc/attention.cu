@@ -296,23 +296,32 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
       ok = __all_sync(kFullMask, ok && wait_bar(&bar_s[j & 1], (uint32_t)((j >> 1) & 1), abort_flag));
       tc_fence_after_sync();
       const int k0 = j * kBN + h * kHalf;
-      // pass 1: max of this half of the row (scaled, masked, log2 units), then of the pair
-      float tmax = kNeg;
+      // this half of the row, scaled and masked (log2 units), kept in registers
+      float sv[kHalf];
 #pragma unroll
       for (int cb = 0; cb < kHalf / 32; ++cb) {
         float v[32];
         tmem_ld32(s_buf + cb * 32, v);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          tmax = max_nan(tmax, (k0 + cb * 32 + i <= kmax) ? v[i] * scale_log2e : kNeg);
+        for (int i = 0; i < 32; ++i) sv[cb * 32 + i] = (k0 + cb * 32 + i <= kmax) ? v[i] * scale_log2e : kNeg;
       }
+      float tmax = kNeg;
+#pragma unroll
+      for (int i = 0; i < kHalf; ++i) tmax = max_nan(tmax, sv[i]);
       float* xm = xmax + (j & 1) * 2 * kBM;
       xm[h * kBM + r] = tmax;
       named_barrier(pair_bar, 64);
       tmax = max_nan(tmax, xm[(1 - h) * kBM + r]);
-      const float m_new = max_nan(m, tmax);
-      const float alpha = (m == kNeg) ? 0.f : exp2_sfu(m - m_new);
+      // The reference max moves only when the tile's max exceeds it by more
+      // than 2^8 (or on the first visible key): p = 2^(s - m) then stays
+      // below 256, exact in fp32 and in bf16's range, and O is rescaled far
+      // less often.  The result is the same softmax: O and l share m.
+      float m_new = m, alpha = 1.f;
+      if (m == kNeg || !(tmax <= m + 8.f)) {
+        m_new = max_nan(m, tmax);
+        alpha = (m == kNeg) ? 0.f : exp2_sfu(m - m_new);
+      }
       // O holds the tiles before j at scale m: once P_{j-1} V_{j-1} is in, rescale it to m_new
       if (j > 0) {
         ok = __all_sync(kFullMask, ok && wait_bar(bar_o, (uint32_t)((j - 1) & 1), abort_flag));
@@ -331,16 +340,14 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
           tmem_wait_st();
         }
       }
-      // pass 2: p = 2^(s - m_new), this half's sum in fp32, P as bf16 into the swizzled tile
+      // p = 2^(s - m_new), this half's sum in fp32, P as bf16 into the swizzled tile
       float psum = 0.f;
 #pragma unroll
       for (int cb = 0; cb < kHalf / 32; ++cb) {
         float v[32];
-        tmem_ld32(s_buf + cb * 32, v);
-        tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          v[i] = (k0 + cb * 32 + i <= kmax && m_new != kNeg) ? exp2_sfu(v[i] * scale_log2e - m_new) : 0.f;
+          v[i] = (m_new != kNeg) ? exp2_sfu(sv[cb * 32 + i] - m_new) : 0.f;
           psum += v[i];
         }
         // keys h * 64 + cb * 32 + 8 t .. + 7: atom column h, 16-byte chunk 4 cb + t
