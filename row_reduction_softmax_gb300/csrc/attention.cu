@@ -50,11 +50,18 @@ __device__ unsigned int g_attn_error = 0;
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr unsigned kErrTimeout = 1u;
+constexpr unsigned kErrConfig = 2u;    // the dynamic shared memory was not 1024-byte aligned
 constexpr int kBM = 128;               // query rows per CTA
 constexpr int kBN = 128;               // keys per tile
-constexpr int kSoftmaxWarps = 8;       // two warps per group of 32 query rows
-constexpr int kAttnThreads = 32 * (kSoftmaxWarps + 1);   // + the load / MMA-issue warp
-constexpr int kIssuerWarp = kSoftmaxWarps;
+// Warps sharing a group of 32 query rows (each takes a part of the key
+// columns and of O's columns, at least 32 of the latter).  Two measured
+// faster than four on d = 128 (0.81 against 0.85 ms on 64 heads of
+// 4096^2): the group barrier and exchange grow with the split.  The softmax
+// warps are 4 * split, then one warp issues loads and MMAs.
+template <int D>
+__host__ __device__ constexpr int attn_split() { return 2; }
+template <int D>
+__host__ __device__ constexpr int attn_threads() { return 32 * (4 * attn_split<D>() + 1); }
 
 template <int D>
 struct Layout2 {
@@ -65,11 +72,11 @@ struct Layout2 {
   static constexpr int kQ = 0;
   static constexpr int kK = kQ + kQBytes;               // 2 stages
   static constexpr int kV = kK + 2 * kKBytes;           // 2 stages
-  static constexpr int kP = kV + 2 * kVBytes;
-  static constexpr int kBar = kP + kPBytes;             // mbarriers and the TMEM address
-  static constexpr int kX = kBar + 128;                 // row-max exchange [2][2][128], row sums [2][128]
-  static constexpr int kBytes = kX + (2 * 2 * kBM + 2 * kBM) * 4;
-  static constexpr int kAlloc = kBytes + 1024;          // slack to align the base to 1024
+  static constexpr int kP = kV + 2 * kVBytes;           // 2 buffers
+  static constexpr int kBar = kP + 2 * kPBytes;         // mbarriers and the TMEM address
+  static constexpr int kX = kBar + 256;   // row-max exchange [2][split][128]; the row sums reuse it
+  static constexpr int kBytes = kX + 2 * attn_split<D>() * kBM * 4;
+  static constexpr int kAlloc = kBytes;                 // the dynamic base is 1024-aligned
   static constexpr uint32_t kTmemCols = 512;            // S: 2 x 128 columns, O_j: D columns
 };
 
@@ -112,16 +119,21 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
-// grid (ceil(L / 128), BH); block 288.  O, LSE: fp32, O row-major [BH, L, D].
+// grid (ceil(L / 128), BH); block 32 * (4 kSplit + 1).  O, LSE: fp32, O row-major [BH, L, D].
 template <int D>
-__global__ void __launch_bounds__(kAttnThreads, 1)
+__global__ void __launch_bounds__(attn_threads<D>(), 1)
 attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, float* __restrict__ O,
                      float* __restrict__ LSE, int L, int S, int causal, float scale_log2e) {
   using Lay = Layout2<D>;
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  constexpr int kSplit = attn_split<D>();
+  constexpr int kSoftmaxWarps = 4 * kSplit;
+  constexpr int kIssuerWarp = kSoftmaxWarps;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  if (smem_addr(smem) & 1023u) {   // the swizzled tiles need 1024-byte alignment (uniform)
+    if (threadIdx.x == 0) atomicOr(&g_attn_error, kErrConfig);
+    return;
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBar);
   uint64_t* bar_q = bars + 0;
   uint64_t* k_full = bars + 1;     // [2] K tile landed
@@ -129,10 +141,15 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
   uint64_t* v_full = bars + 5;     // [2] V^T tile landed
   uint64_t* v_empty = bars + 7;    // [2] P V MMA of that tile done
   uint64_t* bar_s = bars + 9;      // [2] S_j in TMEM buffer j % 2
-  uint64_t* bar_p = bars + 11;     // S_j read and P_j written (128 arrivals)
-  uint64_t* bar_o = bars + 12;     // O_j in TMEM
-  uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(bars + 13);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 14);
+  // [2] S_j read and P_j written into P buffer j % 2 (one arrival per softmax
+  // thread).  One barrier per buffer: the softmax warps may finish tile j + 1
+  // before the issuer sees tile j, but tile j + 2 needs P_j V_j, issued only
+  // after that, so no barrier runs two phases ahead of its waiter.
+  uint64_t* bar_p = bars + 11;
+  uint64_t* bar_o = bars + 13;     // [2] P_j V_j accumulated (P buffer j % 2 free again)
+  uint64_t* bar_drain = bars + 15; // everything issued has completed (abort path)
+  uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 17);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.y;
@@ -154,8 +171,11 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
       mbar_init(&v_empty[i], 1);
       mbar_init(&bar_s[i], 1);
     }
-    mbar_init(bar_p, 32 * kSoftmaxWarps);
-    mbar_init(bar_o, 1);
+    mbar_init(&bar_p[0], 32 * kSoftmaxWarps);
+    mbar_init(&bar_p[1], 32 * kSoftmaxWarps);
+    mbar_init(&bar_o[0], 1);
+    mbar_init(&bar_o[1], 1);
+    mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -233,17 +253,18 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
           if (!(ok = wait_bar(&k_empty[st], use, abort_flag))) break;
           load_k(j + 2);
         }
-        if (!(ok = wait_bar(bar_p, (uint32_t)(j & 1), abort_flag))) break;   // S_j read, P_j written
+        if (!(ok = wait_bar(&bar_p[st], use, abort_flag))) break;   // S_j read, P_j written
         if (!(ok = wait_bar(&v_full[st], use, abort_flag))) break;
         tc_fence_after_sync();
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           const uint32_t offp = (uint32_t)((kk >> 2) * kBM * 128 + (kk & 3) * 32);
           const uint32_t offv = (uint32_t)((kk >> 2) * D * 128 + (kk & 3) * 32);
-          mma_bf16(tmem_o, smem_desc_sw128(sP + offp), smem_desc_sw128(sV + st * Lay::kVBytes + offv),
-                   kIdO, kk > 0 || j > 0);   // O accumulates in TMEM across key tiles
+          mma_bf16(tmem_o, smem_desc_sw128(sP + st * Lay::kPBytes + offp),
+                   smem_desc_sw128(sV + st * Lay::kVBytes + offv), kIdO,
+                   kk > 0 || j > 0);   // O accumulates in TMEM across key tiles
         }
-        mma_commit(bar_o);
+        mma_commit(&bar_o[st]);
         mma_commit(&v_empty[st]);
         ++pv_done;
         if (j + 2 < n_tiles) {   // V stage st is free once P_j V_j is done
@@ -264,25 +285,25 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
             while (!mbar_try_wait(&v_full[st], (uint32_t)((nv - 1) & 1)) && global_timer_ns() - t0 < kWaitLimitNs) {
             }
         }
-        mma_commit(bar_o);   // one more arrival once everything issued has completed
-        while (!mbar_try_wait(bar_o, (uint32_t)(pv_done & 1)) && global_timer_ns() - t0 < 2 * kWaitLimitNs) {
+        mma_commit(bar_drain);   // arrives once everything issued has completed
+        (void)pv_done;
+        while (!mbar_try_wait(bar_drain, 0u) && global_timer_ns() - t0 < 2 * kWaitLimitNs) {
         }
       }
     }
     __syncwarp();   // lanes 1..31 wait here for the issuing lane
   } else {
-    // ---- softmax warps: warps w and w + 4 share query rows 32 (w % 4) .. + 31
-    // (TMEM lanes); warp w < 4 takes the first half of every key tile's
-    // columns and of O's columns, warp w + 4 the second half ----
-    constexpr int kHalf = kBN / 2;      // key columns per thread and tile
-    constexpr int kDHalf = D / 2;       // O columns per thread
+    // ---- softmax warps: warps w, w + 4, ... (kSplit of them) share query
+    // rows 32 (w % 4) .. + 31 (TMEM lanes); warp w takes part w / 4 of every
+    // key tile's columns and of O's columns ----
+    constexpr int kHalf = kBN / kSplit;    // key columns per thread and tile
+    constexpr int kDHalf = D / kSplit;     // O columns per thread
     const int h = warp >> 2;
     const int r = ((warp & 3) << 5) + lane;                 // query row within the tile
     const int qrow = q0 + r;
     const uint32_t lane_off = (uint32_t)(((warp & 3) * 32) << 16);
-    const int pair_bar = 1 + (warp & 3);                     // named barrier of the warp pair
-    float* xmax = reinterpret_cast<float*>(smem + Lay::kX);          // [tile parity][half][row]
-    float* xsum = xmax + 2 * 2 * kBM;                                 // [half][row]
+    const int pair_bar = 1 + (warp & 3);                     // named barrier of the row group's warps
+    float* xmax = reinterpret_cast<float*>(smem + Lay::kX);          // [tile parity][part][row]
     const float kNeg = neg_inf();
     const int kmax = causal ? min(S - 1, qrow + (S - L)) : S - 1;   // last visible key
     float m = kNeg, l = 0.f;
@@ -290,13 +311,13 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
     // Waits are decided warp-uniformly, so the .sync.aligned TMEM accesses
     // below always run on a converged warp.  After a failed wait the loop
     // still runs to the end (the waits then return at once and the values
-    // are discarded), so both warps of a pair meet at every pair barrier.
+    // are discarded), so a row group's warps meet at every group barrier.
     for (int j = 0; j < n_tiles; ++j) {
       const uint32_t s_buf = tmem_s + (uint32_t)((j & 1) * kBN + h * kHalf) + lane_off;
       ok = __all_sync(kFullMask, ok && wait_bar(&bar_s[j & 1], (uint32_t)((j >> 1) & 1), abort_flag));
       tc_fence_after_sync();
       const int k0 = j * kBN + h * kHalf;
-      // this half of the row, scaled and masked (log2 units), kept in registers
+    // this half of the row, scaled and masked (log2 units), kept in registers
       float sv[kHalf];
 #pragma unroll
       for (int cb = 0; cb < kHalf / 32; ++cb) {
@@ -309,10 +330,11 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
       float tmax = kNeg;
 #pragma unroll
       for (int i = 0; i < kHalf; ++i) tmax = max_nan(tmax, sv[i]);
-      float* xm = xmax + (j & 1) * 2 * kBM;
+      float* xm = xmax + (j & 1) * kSplit * kBM;
       xm[h * kBM + r] = tmax;
-      named_barrier(pair_bar, 64);
-      tmax = max_nan(tmax, xm[(1 - h) * kBM + r]);
+      named_barrier(pair_bar, 32 * kSplit);
+#pragma unroll
+      for (int k = 0; k < kSplit; ++k) tmax = max_nan(tmax, xm[k * kBM + r]);
       // The reference max moves only when the tile's max exceeds it by more
       // than 2^8 (or on the first visible key): p = 2^(s - m) then stays
       // below 256, exact in fp32 and in bf16's range, and O is rescaled far
@@ -322,11 +344,14 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
         m_new = max_nan(m, tmax);
         alpha = (m == kNeg) ? 0.f : exp2_sfu(m - m_new);
       }
-      // O holds the tiles before j at scale m: once P_{j-1} V_{j-1} is in, rescale it to m_new
-      if (j > 0) {
-        ok = __all_sync(kFullMask, ok && wait_bar(bar_o, (uint32_t)((j - 1) & 1), abort_flag));
+      // O holds the tiles before j at scale m: if m moves, wait for P_{j-1} V_{j-1}
+      // and rescale O to m_new
+      bool waited_prev = false;
+      if (j > 0 && __any_sync(kFullMask, alpha != 1.f)) {
+        ok = __all_sync(kFullMask, ok && wait_bar(&bar_o[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), abort_flag));
+        waited_prev = true;
         tc_fence_after_sync();
-        if (ok && __any_sync(kFullMask, alpha != 1.f)) {
+        if (ok) {
 #pragma unroll
           for (int cb = 0; cb < kDHalf / 32; ++cb) {
             float v[32];
@@ -340,7 +365,13 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
           tmem_wait_st();
         }
       }
-      // p = 2^(s - m_new), this half's sum in fp32, P as bf16 into the swizzled tile
+      // P buffer j % 2 was last read by P_{j-2} V_{j-2} (done if P_{j-1} V_{j-1} is)
+      if (j >= 2 && !waited_prev) {
+        ok = __all_sync(kFullMask, ok && wait_bar(&bar_o[j & 1], (uint32_t)(((j - 2) >> 1) & 1), abort_flag));
+        tc_fence_after_sync();
+      }
+      const uint32_t sPj = sP + (uint32_t)((j & 1) * Lay::kPBytes);
+      // p = 2^(s - m_new), this part's sum in fp32, P as bf16 into the swizzled tile
       float psum = 0.f;
 #pragma unroll
       for (int cb = 0; cb < kHalf / 32; ++cb) {
@@ -350,10 +381,11 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
           v[i] = (m_new != kNeg) ? exp2_sfu(sv[cb * 32 + i] - m_new) : 0.f;
           psum += v[i];
         }
-        // keys h * 64 + cb * 32 + 8 t .. + 7: atom column h, 16-byte chunk 4 cb + t
+        // keys kc = h * kHalf + cb * 32 + 8 t .. + 7: atom column kc / 64, 16-byte chunk (kc % 64) / 8
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-          st_shared_v4(sw128_chunk(sP, kBM, r, h, 4 * cb + t),
+          const int kc = h * kHalf + cb * 32 + 8 * t;
+          st_shared_v4(sw128_chunk(sPj, kBM, r, kc >> 6, (kc & 63) >> 3),
                        pack_bf16(v[8 * t + 0], v[8 * t + 1]), pack_bf16(v[8 * t + 2], v[8 * t + 3]),
                        pack_bf16(v[8 * t + 4], v[8 * t + 5]), pack_bf16(v[8 * t + 6], v[8 * t + 7]));
         }
@@ -362,14 +394,19 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
       m = m_new;
       fence_proxy_async_smem();   // P (and the rescaled O) visible to the tensor cores
       tc_fence_before_sync();
-      mbar_arrive(bar_p);
+      mbar_arrive(&bar_p[j & 1]);
     }
-    // the row sum is the pair's two halves
+    // the row sum is the sum of the row group's parts (xsum: the exchange
+    // buffer of the parity the last tile did not use, free since its barrier)
+    float* xsum = xmax + ((n_tiles & 1) * kSplit * kBM);
     xsum[h * kBM + r] = l;
-    named_barrier(pair_bar, 64);
-    const float l_row = l + xsum[(1 - h) * kBM + r];
-    const bool have_o =
-        __all_sync(kFullMask, ok && n_tiles > 0 && wait_bar(bar_o, (uint32_t)((n_tiles - 1) & 1), abort_flag));
+    named_barrier(pair_bar, 32 * kSplit);
+    float l_row = 0.f;
+#pragma unroll
+    for (int k = 0; k < kSplit; ++k) l_row += xsum[k * kBM + r];
+    const bool have_o = __all_sync(kFullMask, ok && n_tiles > 0 &&
+                                                  wait_bar(&bar_o[(n_tiles - 1) & 1],
+                                                           (uint32_t)(((n_tiles - 1) >> 1) & 1), abort_flag));
     if (have_o) tc_fence_after_sync();
     if (!*abort_flag && (have_o || n_tiles == 0)) {
       // O = O / l (a row that sees no key: 0 / 0 = NaN, its LSE -inf)
@@ -481,7 +518,7 @@ cudaError_t launch_attn_d(const uint16_t* q, const uint16_t* k, const uint16_t* 
   cudaError_t e = allow_smem(reinterpret_cast<const void*>(kern), Layout2<D>::kAlloc);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)((L + kBM - 1) / kBM), (unsigned)BH);
-  return launch_pdl(kern, grid, dim3(kAttnThreads), (size_t)Layout2<D>::kAlloc, s, 0, mq, mk, mv, o, lse,
+  return launch_pdl(kern, grid, dim3(attn_threads<D>()), (size_t)Layout2<D>::kAlloc, s, 0, mq, mk, mv, o, lse,
                     L, S, causal, scale * kLog2e);
 }
 
