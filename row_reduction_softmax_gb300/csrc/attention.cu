@@ -317,19 +317,21 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
       ok = __all_sync(kFullMask, ok && wait_bar(&bar_s[j & 1], (uint32_t)((j >> 1) & 1), abort_flag));
       tc_fence_after_sync();
       const int k0 = j * kBN + h * kHalf;
-    // this half of the row, scaled and masked (log2 units), kept in registers
+      // this part of the row's raw scores, masked, kept in registers (one
+      // TMEM load of the 64 columns, one wait)
+      static_assert(kHalf == 64, "one 64-column TMEM load per thread and tile");
       float sv[kHalf];
+      tmem_ld64(s_buf, sv);
+      tmem_wait_ld();
+      if (k0 + kHalf - 1 > kmax) {   // the causal diagonal or the ragged end crosses this part
 #pragma unroll
-      for (int cb = 0; cb < kHalf / 32; ++cb) {
-        float v[32];
-        tmem_ld32(s_buf + cb * 32, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sv[cb * 32 + i] = (k0 + cb * 32 + i <= kmax) ? v[i] * scale_log2e : kNeg;
+        for (int i = 0; i < kHalf; ++i) sv[i] = (k0 + i <= kmax) ? sv[i] : kNeg;
       }
+      // max of the raw scores, then scaled (scale_log2e > 0 keeps the order)
       float tmax = kNeg;
 #pragma unroll
       for (int i = 0; i < kHalf; ++i) tmax = max_nan(tmax, sv[i]);
+      tmax *= scale_log2e;
       float* xm = xmax + (j & 1) * kSplit * kBM;
       xm[h * kBM + r] = tmax;
       named_barrier(pair_bar, 32 * kSplit);
@@ -352,15 +354,29 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
         waited_prev = true;
         tc_fence_after_sync();
         if (ok) {
-#pragma unroll
-          for (int cb = 0; cb < kDHalf / 32; ++cb) {
-            float v[32];
-            const uint32_t ta = tmem_o + lane_off + (uint32_t)(h * kDHalf + cb * 32);
-            tmem_ld32(ta, v);
+          const uint32_t ta = tmem_o + lane_off + (uint32_t)(h * kDHalf);
+          if constexpr (kDHalf == 64) {   // one load, one wait
+            float v[64];
+            tmem_ld64(ta, v);
             tmem_wait_ld();
+            float lo[32], hi[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] *= alpha;
-            tmem_st32(ta, v);
+            for (int i = 0; i < 32; ++i) {
+              lo[i] = v[i] * alpha;
+              hi[i] = v[32 + i] * alpha;
+            }
+            tmem_st32(ta, lo);
+            tmem_st32(ta + 32, hi);
+          } else {
+#pragma unroll
+            for (int cb = 0; cb < kDHalf / 32; ++cb) {
+              float v[32];
+              tmem_ld32(ta + cb * 32, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] *= alpha;
+              tmem_st32(ta + cb * 32, v);
+            }
           }
           tmem_wait_st();
         }
@@ -376,10 +392,15 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
 #pragma unroll
       for (int cb = 0; cb < kHalf / 32; ++cb) {
         float v[32];
+        if (m_new != kNeg) {   // p = 2^(s scale log2e - m): one FMA and one SFU op per key
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          v[i] = (m_new != kNeg) ? exp2_sfu(sv[cb * 32 + i] - m_new) : 0.f;
-          psum += v[i];
+          for (int i = 0; i < 32; ++i) {
+            v[i] = exp2_sfu(fmaf(sv[cb * 32 + i], scale_log2e, -m_new));
+            psum += v[i];
+          }
+        } else {   // no visible key yet
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.f;
         }
         // keys kc = h * kHalf + cb * 32 + 8 t .. + 7: atom column kc / 64, 16-byte chunk (kc % 64) / 8
 #pragma unroll
