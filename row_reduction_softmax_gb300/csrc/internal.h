@@ -56,7 +56,8 @@ cudaError_t launch_softmax_staged_rows(const rrs_plan& p, const float* x, float*
                                        int64_t N, const Layout& l, cudaStream_t s);
 cudaError_t launch_softmax_staged_long(const rrs_plan& p, const float* x, float* y, int64_t M,
                                        int64_t N, const Layout& l, cudaStream_t s);
-// GRID plans: rows split over a cooperative grid of R * C CTAs (one per SM);
+// GRID plans: rows split over a grid of R * C <= SMs CTAs (one per SM, all
+// resident together; launched with programmatic dependent launch);
 // `workspace` holds 16 bytes per (row, segment) slot, zero-filled when
 // allocated, and `ticket` is unique per launch on that workspace.
 // `fault` != 0 (testing only, rrs_inject_fault): CTA 0 never publishes the
