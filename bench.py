@@ -23,7 +23,8 @@ The line carries, besides the contract's keys:
                 with its roofline fraction and a sampled-row parity check
   variants      the operations built on the same skeleton -- log-softmax, in
                 place, row max / mean, column softmax, GeLU -- timed and checked
-                the same way
+                the same way, and the fused attention forward (TFLOP/s against
+                the measured bf16 tensor peak)
   clocks        SM clock and clock-event reasons sampled during the timed region
 
 ``--impl reference`` times the oracle instead, on the same metric and config.
@@ -107,6 +108,17 @@ def measured_hbm_peak():
         return v, "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_bf16_peak():
+    """Dense bf16 tensor peak (TFLOP/s) for a kernel timed on its own: the burst figure."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            v = float(json.load(f)["bf16_tflops"])
+        return v, "measured"
+    except Exception:
+        return 1900.0, "fallback"
 
 
 def source_hash() -> str:
@@ -594,6 +606,71 @@ def run_variants(args, torch, rrs, dev, rank):
                                                            np.maximum(np.abs(want), 1e-30)))}
         entries.append(entry)
         del xs, ys, x_host
+        torch.cuda.empty_cache()
+    entries.extend(run_attention(args, torch, rrs, dev, rank))
+    return entries
+
+
+def attention_flops(L: int, S: int, d: int, causal: bool) -> int:
+    """FLOPs of one head: 2 d per (query, visible key) pair for Q K^T and as many for P V."""
+    if not causal:
+        pairs = L * S
+    else:  # key j visible to query i when j <= i + S - L
+        pairs = sum(max(0, min(S, i + S - L + 1)) for i in range(L))
+    return 4 * d * pairs
+
+
+def run_attention(args, torch, rrs, dev, rank):
+    """Fused attention forward (softmax inside the two products) on its workloads:
+    kernel time, tensor-core roofline fraction against the measured bf16 peak, and
+    parity of sampled heads and rows against the oracle."""
+    import oracle
+    peak, peak_kind = measured_bf16_peak()
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    entries = []
+    for name, w in workloads.ATTENTION_WORKLOADS.items():
+        q, k, v = workloads.attention_inputs(w)
+        dq, dk, dv = (torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16) for a in (q, k, v))
+        o = torch.empty(w.BH, w.L, w.d, dtype=torch.float32, device=dev)
+        lse = torch.empty(w.BH, w.L, dtype=torch.float32, device=dev)
+
+        def call():
+            rrs.attention_ptr(dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                              w.BH, w.L, w.S, w.d, w.causal, 0.0, sh)
+
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        steps = max(3, min(args.suite_steps, 20))
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(steps):
+            call()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1) / steps
+        flops = w.BH * attention_flops(w.L, w.S, w.d, w.causal)
+        tflops = flops / (ms / 1e3) / 1e12
+        entry = {"workload": name, "op": "attention_fwd", "B": w.B, "H": w.H, "L": w.L, "S": w.S,
+                 "d": w.d, "causal": w.causal, "dtype": "bf16 in, fp32 accumulate and out",
+                 "ms_per_call": ms, "tflops": tflops,
+                 "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s",
+                              "frac": tflops / peak, "peak_kind": f"of {peak_kind}",
+                              "flops_per_launch": flops},
+                 "calls_timed": steps, "inputs": "resident (K/V of one head: 2 MiB, L2-resident)"}
+        if rank == 0:
+            h = w.BH // 2
+            rows = sampled_rows(w.L, 6, w.seed)
+            f64 = lambda a: (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            want_o, want_l = oracle.attention(f64(q[h]), f64(k[h]), f64(v[h]), causal=w.causal)
+            got_o = o[h][rows].cpu().numpy().astype(np.float64)
+            got_l = lse[h][rows].cpu().numpy().astype(np.float64)
+            entry["parity"] = {"head": h, "rows_checked": len(rows),
+                               "max_abs_o": float(np.max(np.abs(got_o - want_o[rows]))),
+                               "max_abs_lse": float(np.max(np.abs(got_l - want_l[rows])))}
+        entries.append(entry)
+        del dq, dk, dv, o, lse
         torch.cuda.empty_cache()
     return entries
 

@@ -273,6 +273,7 @@ softmax_cols_finalize_kernel(const float* x, float* y, const MaxSum* __restrict_
                              int64_t N, int64_t ldx, int64_t ldy, int64_t chunk, int64_t chunks,
                              int64_t bands, int32_t log_out) {
   __shared__ MaxSum whole[kBand];
+  __shared__ MaxSum red[kCW][kBand];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int slot = lane % kLPR;
   const int g = warp * kRPW + lane / kLPR;
@@ -283,12 +284,34 @@ softmax_cols_finalize_kernel(const float* x, float* y, const MaxSum* __restrict_
   const int64_t j0 = b * kBand + 4 * slot;
   const float kNeg = neg_inf();
   pdl_entry();
-  if (tid < kBand) {
-    const int64_t j = b * kBand + tid;
+  {
+    // Merge the column's chunk partials: warp w takes chunks w, w + 8, ...
+    // for column `lane` of the band, loading 4 partials before merging them;
+    // then thread `lane` of warp 0 merges the 8 warps' results.  The order is
+    // fixed, so every CTA of the band gets the same pair.
+    static_assert(kBand == 32, "one lane per column of the band");
+    const int64_t j = b * kBand + lane;
     MaxSum q{kNeg, 0.f};
-    if (j < N)
-      for (int64_t k = 0; k < chunks; ++k) q = merge(q, part[k * N + j]);
-    whole[tid] = q;
+    if (j < N) {
+      for (int64_t k0 = warp; k0 < chunks; k0 += 4 * kCW) {
+        MaxSum t[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int64_t k = k0 + (int64_t)u * kCW;
+          t[u] = (k < chunks) ? part[k * N + j] : MaxSum{kNeg, 0.f};
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) q = merge(q, t[u]);
+      }
+    }
+    red[warp][lane] = q;
+    __syncthreads();
+    if (warp == 0) {
+      MaxSum w = red[0][lane];
+#pragma unroll
+      for (int k = 1; k < kCW; ++k) w = merge(w, red[k][lane]);
+      whole[lane] = w;
+    }
   }
   __syncthreads();
   if (j0 >= N) return;
