@@ -71,9 +71,33 @@ __device__ __forceinline__ void store_stream(float* p, float v) { __stcs(p, v); 
 
 // Start of every kernel launched with launch_pdl(): allow the next kernel on
 // the stream to be scheduled, then wait for the previous one to complete.
-__device__ __forceinline__ void pdl_entry() {
+__device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_entry() {
+  pdl_launch_dependents();
+  pdl_wait();
+}
+
+// L2 prefetch of the 128-byte line holding p (PTX prefetch.global.L2: a
+// hint that returns no data).  Issued before pdl_wait() on a row the kernel
+// is about to read, it overlaps the row's DRAM latency with the previous
+// kernel's last stores.  That is safe even when the previous kernel writes
+// the row: the L2 is the point of coherence for global memory, so the loads
+// issued after pdl_wait() see that kernel's stores whatever the prefetch
+// brought in; only the timing changes.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// Threads t = 0 .. nt-1 prefetch the lines of bytes [0, n) from p (every
+// address stays inside the range).
+__device__ __forceinline__ void prefetch_l2_range(const void* p, int64_t n, int t, int nt) {
+  const char* c = static_cast<const char*>(p);
+  const int64_t first = -(int64_t)(reinterpret_cast<uintptr_t>(p) & 127);  // line start, relative
+  for (int64_t o = first + 128 * (int64_t)t; o < n; o += 128 * (int64_t)nt)
+    prefetch_l2(c + (o < 0 ? 0 : o));
 }
 
 // Named barrier over `threads` threads (a multiple of 32) of this CTA.

@@ -466,7 +466,10 @@ softmax_staged_grid_kernel(const float* x, float* y, int64_t M, int64_t N, int64
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) init_barriers(smem, NS, kPartialWarps);
   __syncthreads();
-  pdl_entry();
+  pdl_launch_dependents();
+  // the first segment: into the L2 while the previous kernel drains
+  if (items > 0) prefetch_l2_range(x + row0 * ldx + seg_begin, seg_n * 4, threadIdx.x, kGThreads);
+  pdl_wait();
 
   if (warp == kGProducerWarp) {
     if (lane == 0) {
