@@ -51,33 +51,31 @@ __device__ unsigned int g_attn_error = 0;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr unsigned kErrTimeout = 1u;
 constexpr unsigned kErrConfig = 2u;    // the dynamic shared memory was not 1024-byte aligned
-constexpr int kBM = 128;               // query rows per CTA
-constexpr int kBN = 128;               // keys per tile
-// Warps sharing a group of 32 query rows (each takes a part of the key
-// columns and of O's columns, at least 32 of the latter).  Two measured
-// faster than four on d = 128 (0.81 against 0.85 ms on 64 heads of
-// 4096^2): the group barrier and exchange grow with the split.  The softmax
-// warps are 4 * split, then one warp issues loads and MMAs.
-template <int D>
-__host__ __device__ constexpr int attn_split() { return 2; }
-template <int D>
-__host__ __device__ constexpr int attn_threads() { return 32 * (4 * attn_split<D>() + 1); }
+constexpr int kBM = 128;                          // query rows per query tile (TMEM lanes)
+constexpr int kBN = 128;                          // keys per key tile
+constexpr int kQT = 2;                            // query tiles per CTA
+constexpr int kSoftmaxWarps = 4 * kQT;            // a warpgroup per query tile, a thread per row
+constexpr int kIssuerWarp = kSoftmaxWarps;        // one thread issues the MMAs
+constexpr int kLoaderWarp = kSoftmaxWarps + 1;    // one thread issues the TMA loads
+constexpr int kAttnThreads = 32 * (kSoftmaxWarps + 2);
+constexpr int kStages = 2;                        // K and V^T ring depth
 
 template <int D>
-struct Layout2 {
+struct AttnLayout {
   static constexpr int kQBytes = kBM * D * 2;   // D / 64 atom columns of 128 rows x 128 B
   static constexpr int kKBytes = kBN * D * 2;
   static constexpr int kVBytes = D * kBN * 2;   // V^T tile: 2 atom columns of D rows x 128 B
-  static constexpr int kPBytes = kBM * kBN * 2;
-  static constexpr int kQ = 0;
-  static constexpr int kK = kQ + kQBytes;               // 2 stages
-  static constexpr int kV = kK + 2 * kKBytes;           // 2 stages
-  static constexpr int kP = kV + 2 * kVBytes;           // 2 buffers
-  static constexpr int kBar = kP + 2 * kPBytes;         // mbarriers and the TMEM address
-  static constexpr int kX = kBar + 256;   // row-max exchange [2][split][128]; the row sums reuse it
-  static constexpr int kBytes = kX + 2 * attn_split<D>() * kBM * 4;
-  static constexpr int kAlloc = kBytes;                 // the dynamic base is 1024-aligned
-  static constexpr uint32_t kTmemCols = 512;            // S: 2 x 128 columns, O_j: D columns
+  static constexpr int kQ = 0;                          // kQT query tiles
+  static constexpr int kK = kQ + kQT * kQBytes;         // kStages stages
+  static constexpr int kV = kK + kStages * kKBytes;     // kStages stages
+  static constexpr int kBar = kV + kStages * kVBytes;   // mbarriers, TMEM address, abort flag
+  static constexpr int kBytes = kBar + 256;
+  // The dynamic base is 1024-aligned.  At least 116 KB, so that one CTA
+  // fits an SM: each CTA allocates all 512 TMEM columns.
+  static constexpr int kAlloc = kBytes > 116 * 1024 ? kBytes : 116 * 1024;
+  // TMEM: query tile t holds S (fp32, 128 columns, P as bf16 pairs over its
+  // first 64 columns) at column 256 t and O (D columns) at 256 t + 128.
+  static constexpr uint32_t kTmemCols = 512;
 };
 
 // Bounded parity wait; false (and the error word set) if it ran out or the
@@ -99,82 +97,69 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   return true;
 }
 
-// Address of the 16-byte chunk q (0..7) of row r in a K-major tile whose
-// atom column holds `rows` rows (128-byte swizzle: chunk q of row r sits at
-// chunk position q ^ (r % 8) of its 128-byte row).
-__device__ __forceinline__ uint32_t sw128_chunk(uint32_t base, int rows, int r, int col_atom, int q) {
-  return base + (uint32_t)(col_atom * rows * 128 + (r >> 3) * 1024 + (r & 7) * 128 + ((q ^ (r & 7)) << 4));
-}
-
-// Two floats rounded to bf16 (nearest even) and packed: a in the low half,
-// b in the high half (PTX cvt.rn.bf16x2.f32 puts its first source high).
+// Two floats rounded to bf16 (nearest even) and packed: a in the low half
+// (the even key), b in the high half (PTX cvt.rn.bf16x2.f32 puts its first
+// source high).
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
   return r;
 }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-               : "memory");
-}
-
-// grid (ceil(L / 128), BH); block 32 * (4 kSplit + 1).  O, LSE: fp32, O row-major [BH, L, D].
+// grid (ceil(L / 256), BH); block kAttnThreads.  O, LSE: fp32, O row-major [BH, L, D].
 template <int D>
-__global__ void __launch_bounds__(attn_threads<D>(), 1)
+__global__ void __launch_bounds__(kAttnThreads, 1)
 attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tmv, float* __restrict__ O,
                      float* __restrict__ LSE, int L, int S, int causal, float scale_log2e) {
-  using Lay = Layout2<D>;
-  constexpr int kSplit = attn_split<D>();
-  constexpr int kSoftmaxWarps = 4 * kSplit;
-  constexpr int kIssuerWarp = kSoftmaxWarps;
+  using Lay = AttnLayout<D>;
   extern __shared__ __align__(1024) unsigned char smem[];
   if (smem_addr(smem) & 1023u) {   // the swizzled tiles need 1024-byte alignment (uniform)
     if (threadIdx.x == 0) atomicOr(&g_attn_error, kErrConfig);
     return;
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBar);
-  uint64_t* bar_q = bars + 0;
-  uint64_t* k_full = bars + 1;     // [2] K tile landed
-  uint64_t* k_empty = bars + 3;    // [2] S MMA of that K tile done
-  uint64_t* v_full = bars + 5;     // [2] V^T tile landed
-  uint64_t* v_empty = bars + 7;    // [2] P V MMA of that tile done
-  uint64_t* bar_s = bars + 9;      // [2] S_j in TMEM buffer j % 2
-  // [2] S_j read and P_j written into P buffer j % 2 (one arrival per softmax
-  // thread).  One barrier per buffer: the softmax warps may finish tile j + 1
-  // before the issuer sees tile j, but tile j + 2 needs P_j V_j, issued only
-  // after that, so no barrier runs two phases ahead of its waiter.
-  uint64_t* bar_p = bars + 11;
-  uint64_t* bar_o = bars + 13;     // [2] P_j V_j accumulated (P buffer j % 2 free again)
-  uint64_t* bar_drain = bars + 15; // everything issued has completed (abort path)
+  uint64_t* bar_q = bars + 0;      // both query tiles landed
+  uint64_t* k_full = bars + 1;     // [kStages] K tile landed
+  uint64_t* k_empty = bars + 3;    // [kStages] both S MMAs of that K tile done
+  uint64_t* v_full = bars + 5;     // [kStages] V^T tile landed
+  uint64_t* v_empty = bars + 7;    // [kStages] both P V MMAs of that tile done
+  uint64_t* bar_s = bars + 9;      // [kQT] S_t(j) in TMEM (and everything issued before it done)
+  uint64_t* bar_p = bars + 11;     // [kQT] P_t(j) written over S_t(j) (one arrival per row)
+  uint64_t* bar_o = bars + 13;     // [kQT] the last P_t V MMA done
+  uint64_t* bar_drain = bars + 15; // everything the issuer issued has completed (abort path)
   uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 17);
+  static_assert(kStages == 2 && kQT == 2, "barrier slots above");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.y;
-  const int q0 = blockIdx.x * kBM;
-  // key tiles this query tile needs: all of them, or up to the causal bound
-  // (query i sees keys j <= i + S - L)
-  int n_tiles = (S + kBN - 1) / kBN;
-  if (causal) {
-    const int last_key = q0 + kBM - 1 + (S - L);
-    n_tiles = min(n_tiles, last_key < 0 ? 0 : last_key / kBN + 1);
-  }
+  // causal: the CTAs with the most key tiles (the last query rows) go first
+  const int qp = causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+  const int q0 = qp * kQT * kBM;
+  // key tiles each query tile needs: all of them, or up to the causal bound
+  // (query i sees keys j <= i + S - L); the later tile never needs fewer
+  const int n_all = (S + kBN - 1) / kBN;
+  auto tiles_for = [&](int t) {
+    if (!causal) return n_all;
+    const int last_key = q0 + t * kBM + kBM - 1 + (S - L);
+    return min(n_all, last_key < 0 ? 0 : last_key / kBN + 1);
+  };
+  const int n0 = tiles_for(0), n_max = tiles_for(1);
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
-      mbar_init(&bar_s[i], 1);
     }
-    mbar_init(&bar_p[0], 32 * kSoftmaxWarps);
-    mbar_init(&bar_p[1], 32 * kSoftmaxWarps);
-    mbar_init(&bar_o[0], 1);
-    mbar_init(&bar_o[1], 1);
+    for (int t = 0; t < kQT; ++t) {
+      mbar_init(&bar_s[t], 1);
+      mbar_init(&bar_p[t], kBM);
+      mbar_init(&bar_o[t], 1);
+    }
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -187,96 +172,41 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_base_slot;
-  const uint32_t tmem_s = tmem;              // two S buffers: columns [0, 128) and [128, 256)
-  const uint32_t tmem_o = tmem + 2 * kBN;    // columns [256, 256 + D)
   const uint32_t sQ = smem_addr(smem + Lay::kQ);
   const uint32_t sK = smem_addr(smem + Lay::kK);
   const uint32_t sV = smem_addr(smem + Lay::kV);
-  const uint32_t sP = smem_addr(smem + Lay::kP);
   pdl_entry();
 
-  if (warp == kIssuerWarp) {
-    // One thread: loads two tiles ahead, S_{j+1} (into the other S buffer)
-    // while the softmax warps work on S_j, then P_j V_j once P_j is written.
-    if (lane == 0 && n_tiles > 0) {
-      constexpr uint32_t kIdS = idesc_bf16_f32(kBM, kBN);
-      constexpr uint32_t kIdO = idesc_bf16_f32(kBM, D);
-      int k_loads = 0, v_loads = 0, pv_done = 0;
-      auto load_k = [&](int j) {
+  if (warp == kLoaderWarp) {
+    // ---- one thread: Q tiles once, then K_j and V^T_j into a two-stage ring ----
+    if (lane == 0 && n_max > 0) {
+      int k_loads = 0, v_loads = 0;
+      bool ok = true;
+      mbar_arrive_expect_tx(bar_q, kQT * Lay::kQBytes);
+#pragma unroll
+      for (int t = 0; t < kQT; ++t)
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem + Lay::kQ + t * Lay::kQBytes + c * kBM * 128, &tmq, c * 64, q0 + t * kBM, bh, bar_q);
+      for (int j = 0; ok && j < n_max; ++j) {
         const int st = j & 1;
+        const uint32_t prev = (uint32_t)(((j >> 1) - 1) & 1);   // phase of the stage's previous use
+        if (j >= kStages && !(ok = wait_bar(&k_empty[st], prev, abort_flag))) break;
         mbar_arrive_expect_tx(&k_full[st], Lay::kKBytes);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(smem + Lay::kK + st * Lay::kKBytes + c * kBN * 128, &tmk, c * 64, j * kBN, bh,
-                      &k_full[st]);
+          tma_load_3d(smem + Lay::kK + st * Lay::kKBytes + c * kBN * 128, &tmk, c * 64, j * kBN, bh, &k_full[st]);
         ++k_loads;
-      };
-      auto load_v = [&](int j) {
-        const int st = j & 1;
+        if (j >= kStages && !(ok = wait_bar(&v_empty[st], prev, abort_flag))) break;
         mbar_arrive_expect_tx(&v_full[st], Lay::kVBytes);
 #pragma unroll
         for (int c = 0; c < kBN / 64; ++c)
-          tma_load_3d(smem + Lay::kV + st * Lay::kVBytes + c * D * 128, &tmv, j * kBN + c * 64, 0, bh,
-                      &v_full[st]);
+          tma_load_3d(smem + Lay::kV + st * Lay::kVBytes + c * D * 128, &tmv, j * kBN + c * 64, 0, bh, &v_full[st]);
         ++v_loads;
-      };
-      auto issue_s = [&](int j) -> bool {
-        const int st = j & 1;
-        if (!wait_bar(&k_full[st], (uint32_t)((j >> 1) & 1), abort_flag)) return false;
-        tc_fence_after_sync();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (uint32_t)((kk >> 2) * 128 * 128 + (kk & 3) * 32);
-          mma_bf16(tmem_s + st * kBN, smem_desc_sw128(sQ + off),
-                   smem_desc_sw128(sK + st * Lay::kKBytes + off), kIdS, kk > 0);
-        }
-        mma_commit(&bar_s[st]);
-        mma_commit(&k_empty[st]);
-        return true;
-      };
-      mbar_arrive_expect_tx(bar_q, Lay::kQBytes);
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) tma_load_3d(smem + Lay::kQ + c * kBM * 128, &tmq, c * 64, q0, bh, bar_q);
-      load_k(0);
-      load_v(0);
-      if (n_tiles > 1) {
-        load_k(1);
-        load_v(1);
       }
-      bool ok = wait_bar(bar_q, 0, abort_flag);
-      ok = ok && issue_s(0);
-      if (n_tiles > 1) ok = ok && issue_s(1);
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int st = j & 1;
-        const uint32_t use = (uint32_t)((j >> 1) & 1);
-        if (j + 2 < n_tiles) {   // K stage st is free once S_j is done
-          if (!(ok = wait_bar(&k_empty[st], use, abort_flag))) break;
-          load_k(j + 2);
-        }
-        if (!(ok = wait_bar(&bar_p[st], use, abort_flag))) break;   // S_j read, P_j written
-        if (!(ok = wait_bar(&v_full[st], use, abort_flag))) break;
-        tc_fence_after_sync();
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint32_t offp = (uint32_t)((kk >> 2) * kBM * 128 + (kk & 3) * 32);
-          const uint32_t offv = (uint32_t)((kk >> 2) * D * 128 + (kk & 3) * 32);
-          mma_bf16(tmem_o, smem_desc_sw128(sP + st * Lay::kPBytes + offp),
-                   smem_desc_sw128(sV + st * Lay::kVBytes + offv), kIdO,
-                   kk > 0 || j > 0);   // O accumulates in TMEM across key tiles
-        }
-        mma_commit(&bar_o[st]);
-        mma_commit(&v_empty[st]);
-        ++pv_done;
-        if (j + 2 < n_tiles) {   // V stage st is free once P_j V_j is done
-          if (!(ok = wait_bar(&v_empty[st], use, abort_flag))) break;
-          load_v(j + 2);
-          ok = issue_s(j + 2);   // S buffer st was read by the softmax warps (bar_p above)
-        }
-      }
-      if (!ok) {
-        // drain what was issued: the last load of each stage, then every MMA
+      if (!ok) {   // let the last load of each stage land before the CTA can exit
         const uint64_t t0 = global_timer_ns();
-        for (int st = 0; st < 2; ++st) {
+        for (int st = 0; st < kStages; ++st) {
           const int nk = (k_loads - st + 1) / 2, nv = (v_loads - st + 1) / 2;   // loads into stage st
           if (nk > 0)
             while (!mbar_try_wait(&k_full[st], (uint32_t)((nk - 1) & 1)) && global_timer_ns() - t0 < kWaitLimitNs) {
@@ -285,58 +215,126 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
             while (!mbar_try_wait(&v_full[st], (uint32_t)((nv - 1) & 1)) && global_timer_ns() - t0 < kWaitLimitNs) {
             }
         }
-        mma_commit(bar_drain);   // arrives once everything issued has completed
-        (void)pv_done;
+      }
+    }
+    __syncwarp();
+  } else if (warp == kIssuerWarp) {
+    // ---- one thread: the MMAs, in this order per key tile j:
+    //   P_0(j) V_j, S_0(j+1), P_1(j) V_j, S_1(j+1)
+    // so the tensor cores work on one query tile while the other tile's
+    // softmax runs.  S_t(j+1) overwrites the TMEM that P_t(j) V_j reads:
+    // tcgen05 MMAs issued by one thread run in issue order. ----
+    if (lane == 0 && n_max > 0) {
+      constexpr uint32_t kIdS = idesc_bf16_f32(kBM, kBN);
+      constexpr uint32_t kIdO = idesc_bf16_f32(kBM, D);
+      auto issue_s = [&](int t, int j) {
+        const uint32_t sq = sQ + (uint32_t)(t * Lay::kQBytes);
+        const uint32_t sk = sK + (uint32_t)((j & 1) * Lay::kKBytes);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (uint32_t)((kk >> 2) * 128 * 128 + (kk & 3) * 32);
+          mma_bf16(tmem + (uint32_t)(t * 256), smem_desc_sw128(sq + off), smem_desc_sw128(sk + off), kIdS,
+                   kk > 0);
+        }
+        mma_commit(&bar_s[t]);
+      };
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t sv = sV + (uint32_t)((j & 1) * Lay::kVBytes);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {   // P: 8 TMEM columns (16 bf16 keys) per step
+          const uint32_t offv = (uint32_t)((kk >> 2) * D * 128 + (kk & 3) * 32);
+          mma_bf16_tmem_a(tmem + (uint32_t)(t * 256 + 128), tmem + (uint32_t)(t * 256 + 8 * kk),
+                          smem_desc_sw128(sv + offv), kIdO, kk > 0 || j > 0);
+        }
+      };
+      bool ok = wait_bar(bar_q, 0, abort_flag) && wait_bar(&k_full[0], 0, abort_flag);
+      if (ok) {
+        tc_fence_after_sync();
+        if (n0 > 0) issue_s(0, 0);
+        issue_s(1, 0);
+        mma_commit(&k_empty[0]);
+      }
+      for (int j = 0; ok && j < n_max; ++j) {
+        const int st = j & 1;
+        const uint32_t use = (uint32_t)((j >> 1) & 1);
+        const int jn = j + 1;
+        if (!(ok = wait_bar(&v_full[st], use, abort_flag))) break;
+        if (j < n0) {
+          if (!(ok = wait_bar(&bar_p[0], (uint32_t)(j & 1), abort_flag))) break;
+          tc_fence_after_sync();
+          issue_pv(0, j);
+          if (jn < n0) {
+            if (!(ok = wait_bar(&k_full[jn & 1], (uint32_t)((jn >> 1) & 1), abort_flag))) break;
+            tc_fence_after_sync();
+            issue_s(0, jn);
+          } else {
+            mma_commit(&bar_o[0]);
+          }
+        }
+        if (!(ok = wait_bar(&bar_p[1], (uint32_t)(j & 1), abort_flag))) break;
+        tc_fence_after_sync();
+        issue_pv(1, j);
+        mma_commit(&v_empty[st]);
+        if (jn < n_max) {
+          if (!(ok = wait_bar(&k_full[jn & 1], (uint32_t)((jn >> 1) & 1), abort_flag))) break;
+          tc_fence_after_sync();
+          issue_s(1, jn);
+          mma_commit(&k_empty[jn & 1]);
+        } else {
+          mma_commit(&bar_o[1]);
+        }
+      }
+      if (!ok) {   // every MMA issued so far completes before TMEM is freed
+        const uint64_t t0 = global_timer_ns();
+        mma_commit(bar_drain);
         while (!mbar_try_wait(bar_drain, 0u) && global_timer_ns() - t0 < 2 * kWaitLimitNs) {
         }
       }
     }
-    __syncwarp();   // lanes 1..31 wait here for the issuing lane
+    __syncwarp();
   } else {
-    // ---- softmax warps: warps w, w + 4, ... (kSplit of them) share query
-    // rows 32 (w % 4) .. + 31 (TMEM lanes); warp w takes part w / 4 of every
-    // key tile's columns and of O's columns ----
-    constexpr int kHalf = kBN / kSplit;    // key columns per thread and tile
-    constexpr int kDHalf = D / kSplit;     // O columns per thread
-    const int h = warp >> 2;
-    const int r = ((warp & 3) << 5) + lane;                 // query row within the tile
-    const int qrow = q0 + r;
+    // ---- softmax warpgroup t: thread r owns query row r of tile t (TMEM
+    // lane r): per key tile it reads its 128 scores, updates the row max,
+    // writes p = 2^(s scale log2e - m) as bf16 over the scores, and rescales
+    // its row of O when the reference max moves ----
+    const int t = warp >> 2;
+    const int r = ((warp & 3) << 5) + lane;
+    const int qrow = q0 + t * kBM + r;
     const uint32_t lane_off = (uint32_t)(((warp & 3) * 32) << 16);
-    const int pair_bar = 1 + (warp & 3);                     // named barrier of the row group's warps
-    float* xmax = reinterpret_cast<float*>(smem + Lay::kX);          // [tile parity][part][row]
+    const uint32_t ts = tmem + (uint32_t)(t * 256) + lane_off;        // S_t, then P_t
+    const uint32_t to = tmem + (uint32_t)(t * 256 + 128) + lane_off;  // O_t
+    const int nt = (t == 0) ? n0 : n_max;
     const float kNeg = neg_inf();
     const int kmax = causal ? min(S - 1, qrow + (S - L)) : S - 1;   // last visible key
     float m = kNeg, l = 0.f;
     bool ok = true;
     // Waits are decided warp-uniformly, so the .sync.aligned TMEM accesses
-    // below always run on a converged warp.  After a failed wait the loop
-    // still runs to the end (the waits then return at once and the values
-    // are discarded), so a row group's warps meet at every group barrier.
-    for (int j = 0; j < n_tiles; ++j) {
-      const uint32_t s_buf = tmem_s + (uint32_t)((j & 1) * kBN + h * kHalf) + lane_off;
-      ok = __all_sync(kFullMask, ok && wait_bar(&bar_s[j & 1], (uint32_t)((j >> 1) & 1), abort_flag));
+    // always run on a converged warp.
+    for (int j = 0; j < nt; ++j) {
+      ok = __all_sync(kFullMask, ok && wait_bar(&bar_s[t], (uint32_t)(j & 1), abort_flag));
+      if (!ok) break;
       tc_fence_after_sync();
-      const int k0 = j * kBN + h * kHalf;
-      // this part of the row's raw scores, masked, kept in registers (one
-      // TMEM load of the 64 columns, one wait)
-      static_assert(kHalf == 64, "one 64-column TMEM load per thread and tile");
-      float sv[kHalf];
-      tmem_ld64(s_buf, sv);
+      float sa[64], sb[64];
+      tmem_ld64(ts, sa);
+      tmem_ld64(ts + 64, sb);
       tmem_wait_ld();
-      if (k0 + kHalf - 1 > kmax) {   // the causal diagonal or the ragged end crosses this part
+      const int k0 = j * kBN;
+      if (k0 + kBN - 1 > kmax) {   // the causal diagonal or the ragged end crosses this tile
 #pragma unroll
-        for (int i = 0; i < kHalf; ++i) sv[i] = (k0 + i <= kmax) ? sv[i] : kNeg;
+        for (int i = 0; i < 64; ++i) {
+          sa[i] = (k0 + i <= kmax) ? sa[i] : kNeg;
+          sb[i] = (k0 + 64 + i <= kmax) ? sb[i] : kNeg;
+        }
       }
-      // max of the raw scores, then scaled (scale_log2e > 0 keeps the order)
-      float tmax = kNeg;
+      // row max of the raw scores (eight chains), then scaled (scale_log2e > 0 keeps the order)
+      float mx[8];
 #pragma unroll
-      for (int i = 0; i < kHalf; ++i) tmax = max_nan(tmax, sv[i]);
+      for (int c = 0; c < 8; ++c) mx[c] = max_nan(sa[c], sb[c]);
+#pragma unroll
+      for (int i = 8; i < 64; ++i) mx[i & 7] = max_nan(mx[i & 7], max_nan(sa[i], sb[i]));
+      float tmax = max_nan(max_nan(max_nan(mx[0], mx[1]), max_nan(mx[2], mx[3])),
+                           max_nan(max_nan(mx[4], mx[5]), max_nan(mx[6], mx[7])));
       tmax *= scale_log2e;
-      float* xm = xmax + (j & 1) * kSplit * kBM;
-      xm[h * kBM + r] = tmax;
-      named_barrier(pair_bar, 32 * kSplit);
-#pragma unroll
-      for (int k = 0; k < kSplit; ++k) tmax = max_nan(tmax, xm[k * kBM + r]);
       // The reference max moves only when the tile's max exceeds it by more
       // than 2^8 (or on the first visible key): p = 2^(s - m) then stays
       // below 256, exact in fp32 and in bf16's range, and O is rescaled far
@@ -346,98 +344,60 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
         m_new = max_nan(m, tmax);
         alpha = (m == kNeg) ? 0.f : exp2_sfu(m - m_new);
       }
-      // O holds the tiles before j at scale m: if m moves, wait for P_{j-1} V_{j-1}
-      // and rescale O to m_new
-      bool waited_prev = false;
+      // O_t holds the tiles before j at scale m.  P_t(j-1) V_{j-1} is
+      // complete: S_t(j) was issued after it and bar_s covers both.
       if (j > 0 && __any_sync(kFullMask, alpha != 1.f)) {
-        ok = __all_sync(kFullMask, ok && wait_bar(&bar_o[(j - 1) & 1], (uint32_t)(((j - 1) >> 1) & 1), abort_flag));
-        waited_prev = true;
-        tc_fence_after_sync();
-        if (ok) {
-          const uint32_t ta = tmem_o + lane_off + (uint32_t)(h * kDHalf);
-          if constexpr (kDHalf == 64) {   // one load, one wait
-            float v[64];
-            tmem_ld64(ta, v);
-            tmem_wait_ld();
-            float lo[32], hi[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              lo[i] = v[i] * alpha;
-              hi[i] = v[32 + i] * alpha;
-            }
-            tmem_st32(ta, lo);
-            tmem_st32(ta + 32, hi);
-          } else {
+        for (int cb = 0; cb < D / 32; ++cb) {
+          float v[32];
+          tmem_ld32(to + cb * 32, v);
+          tmem_wait_ld();
 #pragma unroll
-            for (int cb = 0; cb < kDHalf / 32; ++cb) {
-              float v[32];
-              tmem_ld32(ta + cb * 32, v);
-              tmem_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] *= alpha;
-              tmem_st32(ta + cb * 32, v);
-            }
-          }
-          tmem_wait_st();
+          for (int i = 0; i < 32; ++i) v[i] *= alpha;
+          tmem_st32(to + cb * 32, v);
         }
       }
-      // P buffer j % 2 was last read by P_{j-2} V_{j-2} (done if P_{j-1} V_{j-1} is)
-      if (j >= 2 && !waited_prev) {
-        ok = __all_sync(kFullMask, ok && wait_bar(&bar_o[j & 1], (uint32_t)(((j - 2) >> 1) & 1), abort_flag));
-        tc_fence_after_sync();
+      // p = 2^(s scale log2e - m_new): one FMA and one SFU op per key; the
+      // row's part of l in fp32 (eight chains); P as bf16 pairs over S
+      float ps[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) ps[c] = 0.f;
+      const bool live = (m_new != kNeg);
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float a = live ? exp2_sfu(fmaf(sa[2 * i], scale_log2e, -m_new)) : 0.f;
+        const float b = live ? exp2_sfu(fmaf(sa[2 * i + 1], scale_log2e, -m_new)) : 0.f;
+        ps[i & 7] += a + b;
+        pk[i] = pack_bf16(a, b);
       }
-      const uint32_t sPj = sP + (uint32_t)((j & 1) * Lay::kPBytes);
-      // p = 2^(s - m_new), this part's sum in fp32, P as bf16 into the swizzled tile
-      float psum = 0.f;
+      tmem_st32u(ts, pk);
 #pragma unroll
-      for (int cb = 0; cb < kHalf / 32; ++cb) {
-        float v[32];
-        if (m_new != kNeg) {   // p = 2^(s scale log2e - m): one FMA and one SFU op per key
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            v[i] = exp2_sfu(fmaf(sv[cb * 32 + i], scale_log2e, -m_new));
-            psum += v[i];
-          }
-        } else {   // no visible key yet
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0.f;
-        }
-        // keys kc = h * kHalf + cb * 32 + 8 t .. + 7: atom column kc / 64, 16-byte chunk (kc % 64) / 8
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const int kc = h * kHalf + cb * 32 + 8 * t;
-          st_shared_v4(sw128_chunk(sPj, kBM, r, kc >> 6, (kc & 63) >> 3),
-                       pack_bf16(v[8 * t + 0], v[8 * t + 1]), pack_bf16(v[8 * t + 2], v[8 * t + 3]),
-                       pack_bf16(v[8 * t + 4], v[8 * t + 5]), pack_bf16(v[8 * t + 6], v[8 * t + 7]));
-        }
+      for (int i = 0; i < 32; ++i) {
+        const float a = live ? exp2_sfu(fmaf(sb[2 * i], scale_log2e, -m_new)) : 0.f;
+        const float b = live ? exp2_sfu(fmaf(sb[2 * i + 1], scale_log2e, -m_new)) : 0.f;
+        ps[i & 7] += a + b;
+        pk[i] = pack_bf16(a, b);
       }
+      tmem_st32u(ts + 32, pk);
+      tmem_wait_st();
+      const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       l = l * alpha + psum;
       m = m_new;
-      fence_proxy_async_smem();   // P (and the rescaled O) visible to the tensor cores
       tc_fence_before_sync();
-      mbar_arrive(&bar_p[j & 1]);
+      mbar_arrive(&bar_p[t]);
     }
-    // the row sum is the sum of the row group's parts (xsum: the exchange
-    // buffer of the parity the last tile did not use, free since its barrier)
-    float* xsum = xmax + ((n_tiles & 1) * kSplit * kBM);
-    xsum[h * kBM + r] = l;
-    named_barrier(pair_bar, 32 * kSplit);
-    float l_row = 0.f;
-#pragma unroll
-    for (int k = 0; k < kSplit; ++k) l_row += xsum[k * kBM + r];
-    const bool have_o = __all_sync(kFullMask, ok && n_tiles > 0 &&
-                                                  wait_bar(&bar_o[(n_tiles - 1) & 1],
-                                                           (uint32_t)(((n_tiles - 1) >> 1) & 1), abort_flag));
+    const bool have_o = __all_sync(kFullMask, ok && nt > 0 && wait_bar(&bar_o[t], 0u, abort_flag));
     if (have_o) tc_fence_after_sync();
-    if (!*abort_flag && (have_o || n_tiles == 0)) {
+    if (!*abort_flag && (have_o || nt == 0)) {
       // O = O / l (a row that sees no key: 0 / 0 = NaN, its LSE -inf)
-      const float inv = 1.0f / l_row;
-      float* orow = O + ((size_t)bh * L + qrow) * D + h * kDHalf;
+      const float inv = 1.0f / l;
+      float* orow = O + ((size_t)bh * L + qrow) * D;
 #pragma unroll
-      for (int cb = 0; cb < kDHalf / 32; ++cb) {
+      for (int cb = 0; cb < D / 32; ++cb) {
         float v[32];
         if (have_o) {
-          tmem_ld32(tmem_o + lane_off + (uint32_t)(h * kDHalf + cb * 32), v);
+          tmem_ld32(to + cb * 32, v);
           tmem_wait_ld();
         } else {
 #pragma unroll
@@ -450,13 +410,14 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
             o4[i] = make_float4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
         }
       }
-      if (LSE && h == 0 && qrow < L)
-        LSE[(size_t)bh * L + qrow] = (m == kNeg) ? kNeg : (m + log2f(l_row)) * 0.69314718055994531f;
+      if (LSE && qrow < L)
+        LSE[(size_t)bh * L + qrow] = (m == kNeg) ? kNeg : (m + log2f(l)) * 0.69314718055994531f;
     }
   }
   tc_fence_before_sync();
   __syncthreads();
   if (warp == kIssuerWarp) {
+
     tc_fence_after_sync();
     tmem_dealloc(tmem, Lay::kTmemCols);
   }
@@ -536,10 +497,10 @@ cudaError_t launch_attn_d(const uint16_t* q, const uint16_t* k, const uint16_t* 
       !make_map(&mv, vt, S, D, BH, ldt, (uint64_t)D * ldt, D))
     return cudaErrorInvalidValue;
   auto kern = attention_fwd_kernel<D>;
-  cudaError_t e = allow_smem(reinterpret_cast<const void*>(kern), Layout2<D>::kAlloc);
+  cudaError_t e = allow_smem(reinterpret_cast<const void*>(kern), AttnLayout<D>::kAlloc);
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)((L + kBM - 1) / kBM), (unsigned)BH);
-  return launch_pdl(kern, grid, dim3(attn_threads<D>()), (size_t)Layout2<D>::kAlloc, s, 0, mq, mk, mv, o, lse,
+  const dim3 grid((unsigned)((L + kQT * kBM - 1) / (kQT * kBM)), (unsigned)BH);
+  return launch_pdl(kern, grid, dim3(kAttnThreads), (size_t)AttnLayout<D>::kAlloc, s, 0, mq, mk, mv, o, lse,
                     L, S, causal, scale * kLog2e);
 }
 
