@@ -219,74 +219,93 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
     }
     __syncwarp();
   } else if (warp == kIssuerWarp) {
-    // ---- one thread: the MMAs, in this order per key tile j:
+    // ---- the MMAs, in this order per key tile j:
     //   P_0(j) V_j, S_0(j+1), P_1(j) V_j, S_1(j+1)
     // so the tensor cores work on one query tile while the other tile's
     // softmax runs.  S_t(j+1) overwrites the TMEM that P_t(j) V_j reads:
-    // tcgen05 MMAs issued by one thread run in issue order. ----
-    if (lane == 0 && n_max > 0) {
+    // tcgen05 MMAs issued by one thread run in issue order.  The whole warp
+    // runs the loop (so the descriptors stay warp-uniform) and one elected
+    // lane issues each MMA and commit. ----
+    if (n_max > 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(kBM, kBN);
       constexpr uint32_t kIdO = idesc_bf16_f32(kBM, D);
+      const bool leader = elect_one();
+      // descriptor bases; a K step adds its byte offset >> 4 to the start
+      // address field (every address stays below 2^18, inside the field)
+      const uint64_t dq0 = smem_desc_sw128(sQ), dk0 = smem_desc_sw128(sK), dv0 = smem_desc_sw128(sV);
       auto issue_s = [&](int t, int j) {
-        const uint32_t sq = sQ + (uint32_t)(t * Lay::kQBytes);
-        const uint32_t sk = sK + (uint32_t)((j & 1) * Lay::kKBytes);
+        const uint64_t dq = dq0 + (uint64_t)((t * Lay::kQBytes) >> 4);
+        const uint64_t dk = dk0 + (uint64_t)(((j & 1) * Lay::kKBytes) >> 4);
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (uint32_t)((kk >> 2) * 128 * 128 + (kk & 3) * 32);
-          mma_bf16(tmem + (uint32_t)(t * 256), smem_desc_sw128(sq + off), smem_desc_sw128(sk + off), kIdS,
-                   kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t off = (uint64_t)(((kk >> 2) * 128 * 128 + (kk & 3) * 32) >> 4);
+            mma_bf16(tmem + (uint32_t)(t * 256), dq + off, dk + off, kIdS, kk > 0);
+          }
+          mma_commit(&bar_s[t]);
         }
-        mma_commit(&bar_s[t]);
+        __syncwarp();
       };
       auto issue_pv = [&](int t, int j) {
-        const uint32_t sv = sV + (uint32_t)((j & 1) * Lay::kVBytes);
+        const uint64_t dv = dv0 + (uint64_t)(((j & 1) * Lay::kVBytes) >> 4);
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {   // P: 8 TMEM columns (16 bf16 keys) per step
-          const uint32_t offv = (uint32_t)((kk >> 2) * D * 128 + (kk & 3) * 32);
-          mma_bf16_tmem_a(tmem + (uint32_t)(t * 256 + 128), tmem + (uint32_t)(t * 256 + 8 * kk),
-                          smem_desc_sw128(sv + offv), kIdO, kk > 0 || j > 0);
+          for (int kk = 0; kk < kBN / 16; ++kk) {   // P: 8 TMEM columns (16 bf16 keys) per step
+            const uint64_t offv = (uint64_t)(((kk >> 2) * D * 128 + (kk & 3) * 32) >> 4);
+            mma_bf16_tmem_a(tmem + (uint32_t)(t * 256 + 128), tmem + (uint32_t)(t * 256 + 8 * kk), dv + offv,
+                            kIdO, kk > 0 || j > 0);
+          }
         }
+        __syncwarp();
       };
-      bool ok = wait_bar(bar_q, 0, abort_flag) && wait_bar(&k_full[0], 0, abort_flag);
+      auto commit = [&](uint64_t* bar) {
+        if (leader) mma_commit(bar);
+        __syncwarp();
+      };
+      // every lane waits; the warp proceeds only if all of them saw the phase
+      auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+        return __all_sync(kFullMask, wait_bar(bar, parity, abort_flag));
+      };
+      bool ok = wait_all(bar_q, 0) && wait_all(&k_full[0], 0);
       if (ok) {
         tc_fence_after_sync();
         if (n0 > 0) issue_s(0, 0);
         issue_s(1, 0);
-        mma_commit(&k_empty[0]);
+        commit(&k_empty[0]);
       }
       for (int j = 0; ok && j < n_max; ++j) {
         const int st = j & 1;
         const uint32_t use = (uint32_t)((j >> 1) & 1);
         const int jn = j + 1;
-        if (!(ok = wait_bar(&v_full[st], use, abort_flag))) break;
+        if (!(ok = wait_all(&v_full[st], use))) break;
         if (j < n0) {
-          if (!(ok = wait_bar(&bar_p[0], (uint32_t)(j & 1), abort_flag))) break;
+          if (!(ok = wait_all(&bar_p[0], (uint32_t)(j & 1)))) break;
           tc_fence_after_sync();
           issue_pv(0, j);
           if (jn < n0) {
-            if (!(ok = wait_bar(&k_full[jn & 1], (uint32_t)((jn >> 1) & 1), abort_flag))) break;
+            if (!(ok = wait_all(&k_full[jn & 1], (uint32_t)((jn >> 1) & 1)))) break;
             tc_fence_after_sync();
             issue_s(0, jn);
           } else {
-            mma_commit(&bar_o[0]);
+            commit(&bar_o[0]);
           }
         }
-        if (!(ok = wait_bar(&bar_p[1], (uint32_t)(j & 1), abort_flag))) break;
+        if (!(ok = wait_all(&bar_p[1], (uint32_t)(j & 1)))) break;
         tc_fence_after_sync();
         issue_pv(1, j);
-        mma_commit(&v_empty[st]);
+        commit(&v_empty[st]);
         if (jn < n_max) {
-          if (!(ok = wait_bar(&k_full[jn & 1], (uint32_t)((jn >> 1) & 1), abort_flag))) break;
+          if (!(ok = wait_all(&k_full[jn & 1], (uint32_t)((jn >> 1) & 1)))) break;
           tc_fence_after_sync();
           issue_s(1, jn);
-          mma_commit(&k_empty[jn & 1]);
+          commit(&k_empty[jn & 1]);
         } else {
-          mma_commit(&bar_o[1]);
+          commit(&bar_o[1]);
         }
       }
       if (!ok) {   // every MMA issued so far completes before TMEM is freed
         const uint64_t t0 = global_timer_ns();
-        mma_commit(bar_drain);
+        commit(bar_drain);
         while (!mbar_try_wait(bar_drain, 0u) && global_timer_ns() - t0 < 2 * kWaitLimitNs) {
         }
       }
@@ -363,23 +382,20 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
 #pragma unroll
       for (int c = 0; c < 8; ++c) ps[c] = 0.f;
       const bool live = (m_new != kNeg);
-      uint32_t pk[32];
+      // four chunks of 32 keys, each written as 16 columns of bf16 pairs
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float a = live ? exp2_sfu(fmaf(sa[2 * i], scale_log2e, -m_new)) : 0.f;
-        const float b = live ? exp2_sfu(fmaf(sa[2 * i + 1], scale_log2e, -m_new)) : 0.f;
-        ps[i & 7] += a + b;
-        pk[i] = pack_bf16(a, b);
-      }
-      tmem_st32u(ts, pk);
+      for (int cb = 0; cb < 4; ++cb) {
+        const float* sv = (cb < 2) ? sa + 32 * cb : sb + 32 * (cb - 2);
+        uint32_t pk[16];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float a = live ? exp2_sfu(fmaf(sb[2 * i], scale_log2e, -m_new)) : 0.f;
-        const float b = live ? exp2_sfu(fmaf(sb[2 * i + 1], scale_log2e, -m_new)) : 0.f;
-        ps[i & 7] += a + b;
-        pk[i] = pack_bf16(a, b);
+        for (int i = 0; i < 16; ++i) {
+          const float a = live ? exp2_sfu(fmaf(sv[2 * i], scale_log2e, -m_new)) : 0.f;
+          const float b = live ? exp2_sfu(fmaf(sv[2 * i + 1], scale_log2e, -m_new)) : 0.f;
+          ps[i & 7] += a + b;
+          pk[i] = pack_bf16(a, b);
+        }
+        tmem_st16u(ts + 16 * cb, pk);
       }
-      tmem_st32u(ts + 32, pk);
       tmem_wait_st();
       const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       l = l * alpha + psum;
