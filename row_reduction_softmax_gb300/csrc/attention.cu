@@ -106,6 +106,32 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return r;
 }
 
+// Packed pairs of fp32 (PTX .f32x2 arithmetic: two lanes per instruction).
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// max of three that propagates NaN (PTX three-input max.NaN.f32)
+__device__ __forceinline__ float max3_nan(float a, float b, float c) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // grid (ceil(L / 256), BH); block kAttnThreads.  O, LSE: fp32, O row-major [BH, L, D].
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
@@ -350,9 +376,9 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
 #pragma unroll
       for (int c = 0; c < 8; ++c) mx[c] = max_nan(sa[c], sb[c]);
 #pragma unroll
-      for (int i = 8; i < 64; ++i) mx[i & 7] = max_nan(mx[i & 7], max_nan(sa[i], sb[i]));
-      float tmax = max_nan(max_nan(max_nan(mx[0], mx[1]), max_nan(mx[2], mx[3])),
-                           max_nan(max_nan(mx[4], mx[5]), max_nan(mx[6], mx[7])));
+      for (int i = 8; i < 64; ++i) mx[i & 7] = max3_nan(mx[i & 7], sa[i], sb[i]);
+      float tmax = max3_nan(max3_nan(mx[0], mx[1], mx[2]), max3_nan(mx[3], mx[4], mx[5]),
+                            max_nan(mx[6], mx[7]));
       tmax *= scale_log2e;
       // The reference max moves only when the tile's max exceeds it by more
       // than 2^8 (or on the first visible key): p = 2^(s - m) then stays
@@ -376,26 +402,32 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
           tmem_st32(to + cb * 32, v);
         }
       }
-      // p = 2^(s scale log2e - m_new): one FMA and one SFU op per key; the
-      // row's part of l in fp32 (eight chains); P as bf16 pairs over S
-      float ps[8];
+      // p = 2^(s scale log2e - m_new): one FMA (in pairs) and one SFU op per
+      // key; the row's part of l in fp32 (four chains of pairs); P as bf16
+      // pairs over S, in four chunks of 32 keys (16 columns each)
+      uint64_t ps2[4];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) ps[c] = 0.f;
+      for (int c = 0; c < 4; ++c) ps2[c] = 0ull;   // +0.0f in both halves
       const bool live = (m_new != kNeg);
-      // four chunks of 32 keys, each written as 16 columns of bf16 pairs
+      const uint64_t c2 = f2_pack(scale_log2e, scale_log2e), nm2 = f2_pack(-m_new, -m_new);
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) {
         const float* sv = (cb < 2) ? sa + 32 * cb : sb + 32 * (cb - 2);
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float a = live ? exp2_sfu(fmaf(sv[2 * i], scale_log2e, -m_new)) : 0.f;
-          const float b = live ? exp2_sfu(fmaf(sv[2 * i + 1], scale_log2e, -m_new)) : 0.f;
-          ps[i & 7] += a + b;
+          float xa, xb;
+          f2_unpack(f2_fma(f2_pack(sv[2 * i], sv[2 * i + 1]), c2, nm2), xa, xb);
+          const float a = live ? exp2_sfu(xa) : 0.f;
+          const float b = live ? exp2_sfu(xb) : 0.f;
+          ps2[i & 3] = f2_add(ps2[i & 3], f2_pack(a, b));
           pk[i] = pack_bf16(a, b);
         }
         tmem_st16u(ts + 16 * cb, pk);
       }
+      float ps[8];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) f2_unpack(ps2[c], ps[2 * c], ps[2 * c + 1]);
       tmem_wait_st();
       const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       l = l * alpha + psum;
