@@ -206,9 +206,8 @@ RRS_API int gelu(const float* x, float* y, int64_t n, void* stream);
  * sums accumulate in fp32; the softmax weights enter the second product
  * rounded to bf16.  BH == 0 or L == 0: no work.  Errors: RRS_ERR_INVALID_ARG
  * (sizes, d, scale, alignment, null/host pointers), RRS_ERR_ALIAS (an output
- * overlaps an input or the other output), RRS_ERR_NOMEM (the V^T workspace,
- * BH x d x S x 2 bytes, kept per stream), RRS_ERR_CUDA; a bounded wait that
- * ran out shows in rrs_device_error. */
+ * overlaps an input or the other output), RRS_ERR_CUDA; a bounded wait that
+ * ran out shows in rrs_device_error.  No workspace is allocated. */
 RRS_API int attention_fwd(const void* q, const void* k, const void* v, float* o, float* lse,
                           int64_t BH, int64_t L, int64_t S, int64_t d, int causal, float scale,
                           void* stream);

@@ -9,26 +9,26 @@
 // rest of this library: with m the running row max and l the running sum,
 // a new tile with max m' rescales by e^(m - max(m, m')).
 //
-// One CTA owns 128 query rows of one head and walks the key tiles of 128:
-//   warp 4, one thread: TMA loads of Q (once), K and V^T tiles (two-stage
-//     rings with their own barriers, K two tiles ahead), and the tcgen05.mma
-//     issue: S_{j+1} = Q K_{j+1}^T into the second of two TMEM S buffers
-//     while the softmax warps read S_j, then O_j = P_j V_j into TMEM columns
-//     [256, 256 + d) once P_j is written;
-//   warps 0..7: query row r (TMEM lane r) belongs to warps r / 32 and
-//     r / 32 + 4, each taking half of the row's columns: they read S from
-//     TMEM (32 columns per tcgen05.ld), exchange their halves' maxima through
-//     shared memory, take p = 2^(s log2e scale - m) on the SFU, write p as
-//     bf16 into the 128-byte-swizzled P tile in shared memory (the A operand
-//     of the second MMA), keep their halves' row sums in fp32, and, when the
-//     row max rises, rescale their half of O, which accumulates in TMEM
-//     across key tiles (O = alpha O + P_j V_j).
-// Operands are bf16 (K-major, 128-byte swizzle, 1024-byte atoms, written by
-// TMA for Q, K, V^T and by the softmax threads for P); accumulators fp32.
-// V is transposed to V^T (d x S per head) by a small kernel first, so that
-// both MMAs take K-major operands.  Every mbarrier wait is bounded (1 s): on
-// timeout the CTA records an error, stops issuing, drains what it issued
-// and frees its TMEM.
+// One CTA owns 256 query rows of one head, as two tiles of 128 (TMEM lanes),
+// and walks the key tiles of 128 keys:
+//   warp 9, one thread: TMA loads of both query tiles (once), then K_j and
+//     V_j into two-stage rings;
+//   warp 8: the tcgen05.mma issue (one elected lane), per key tile in the
+//     order P_0(j) V_j, S_0(j+1) = Q_0 K_{j+1}^T, P_1(j) V_j, S_1(j+1), so
+//     the tensor cores work on one query tile while the other's softmax runs;
+//   warps 0..3 and 4..7: the softmax warpgroup of query tile 0 and 1, one
+//     thread per query row: it reads its 128 scores from TMEM, updates the
+//     row max, writes p = 2^(s log2e scale - m) as bf16 pairs over the first
+//     half of the scores' TMEM columns (the A operand of P V, read from TMEM),
+//     keeps the row sum in fp32, and rescales its row of O, which
+//     accumulates in TMEM across key tiles (O = alpha O + P_j V_j), when the
+//     row max rises.
+// TMEM per query tile: S (128 fp32 columns, P over the first 64) and O (D
+// columns): 512 columns for the two tiles.  Q and K are K-major operands,
+// V [keys][d] is the MN-major B operand of P V (no transposed copy); all
+// are bf16 in 128-byte-swizzled tiles written by TMA; accumulators fp32.
+// Every mbarrier wait is bounded (1 s): on timeout the CTA records an
+// error, stops issuing, drains what it issued and frees its TMEM.
 #include <algorithm>
 #include <mutex>
 #include <set>
@@ -58,13 +58,13 @@ constexpr int kSoftmaxWarps = 4 * kQT;            // a warpgroup per query tile,
 constexpr int kIssuerWarp = kSoftmaxWarps;        // one thread issues the MMAs
 constexpr int kLoaderWarp = kSoftmaxWarps + 1;    // one thread issues the TMA loads
 constexpr int kAttnThreads = 32 * (kSoftmaxWarps + 2);
-constexpr int kStages = 2;                        // K and V^T ring depth
+constexpr int kStages = 2;                        // K and V ring depth
 
 template <int D>
 struct AttnLayout {
   static constexpr int kQBytes = kBM * D * 2;   // D / 64 atom columns of 128 rows x 128 B
   static constexpr int kKBytes = kBN * D * 2;
-  static constexpr int kVBytes = D * kBN * 2;   // V^T tile: 2 atom columns of D rows x 128 B
+  static constexpr int kVBytes = kBN * D * 2;   // V tile: D / 64 blocks of 128 keys x 128 B
   static constexpr int kQ = 0;                          // kQT query tiles
   static constexpr int kK = kQ + kQT * kQBytes;         // kStages stages
   static constexpr int kV = kK + kStages * kKBytes;     // kStages stages
@@ -148,7 +148,7 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
   uint64_t* bar_q = bars + 0;      // both query tiles landed
   uint64_t* k_full = bars + 1;     // [kStages] K tile landed
   uint64_t* k_empty = bars + 3;    // [kStages] both S MMAs of that K tile done
-  uint64_t* v_full = bars + 5;     // [kStages] V^T tile landed
+  uint64_t* v_full = bars + 5;     // [kStages] V tile landed
   uint64_t* v_empty = bars + 7;    // [kStages] both P V MMAs of that tile done
   uint64_t* bar_s = bars + 9;      // [kQT] S_t(j) in TMEM (and everything issued before it done)
   uint64_t* bar_p = bars + 11;     // [kQT] P_t(j) written over S_t(j) (one arrival per row)
@@ -204,7 +204,7 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
   pdl_entry();
 
   if (warp == kLoaderWarp) {
-    // ---- one thread: Q tiles once, then K_j and V^T_j into a two-stage ring ----
+    // ---- one thread: Q tiles once, then K_j and V_j into a two-stage ring ----
     if (lane == 0 && n_max > 0) {
       int k_loads = 0, v_loads = 0;
       bool ok = true;
@@ -226,8 +226,8 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
         if (j >= kStages && !(ok = wait_bar(&v_empty[st], prev, abort_flag))) break;
         mbar_arrive_expect_tx(&v_full[st], Lay::kVBytes);
 #pragma unroll
-        for (int c = 0; c < kBN / 64; ++c)
-          tma_load_3d(smem + Lay::kV + st * Lay::kVBytes + c * D * 128, &tmv, j * kBN + c * 64, 0, bh, &v_full[st]);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(smem + Lay::kV + st * Lay::kVBytes + c * kBN * 128, &tmv, c * 64, j * kBN, bh, &v_full[st]);
         ++v_loads;
       }
       if (!ok) {   // let the last load of each stage land before the CTA can exit
@@ -254,11 +254,12 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
     // lane issues each MMA and commit. ----
     if (n_max > 0) {
       constexpr uint32_t kIdS = idesc_bf16_f32(kBM, kBN);
-      constexpr uint32_t kIdO = idesc_bf16_f32(kBM, D);
+      constexpr uint32_t kIdO = idesc_bf16_f32_bmn(kBM, D);   // B = V [keys][d]: MN-major
       const bool leader = elect_one();
       // descriptor bases; a K step adds its byte offset >> 4 to the start
       // address field (every address stays below 2^18, inside the field)
-      const uint64_t dq0 = smem_desc_sw128(sQ), dk0 = smem_desc_sw128(sK), dv0 = smem_desc_sw128(sV);
+      const uint64_t dq0 = smem_desc_sw128(sQ), dk0 = smem_desc_sw128(sK);
+      const uint64_t dv0 = smem_desc_sw128_mn(sV, kBN * 128);   // d blocks of 64 are 128 keys x 128 B apart
       auto issue_s = [&](int t, int j) {
         const uint64_t dq = dq0 + (uint64_t)((t * Lay::kQBytes) >> 4);
         const uint64_t dk = dk0 + (uint64_t)(((j & 1) * Lay::kKBytes) >> 4);
@@ -277,7 +278,7 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
         if (leader) {
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk) {   // P: 8 TMEM columns (16 bf16 keys) per step
-            const uint64_t offv = (uint64_t)(((kk >> 2) * D * 128 + (kk & 3) * 32) >> 4);
+            const uint64_t offv = (uint64_t)((kk * 16 * 128) >> 4);   // V: 16 keys = two 1024-byte atoms
             mma_bf16_tmem_a(tmem + (uint32_t)(t * 256 + 128), tmem + (uint32_t)(t * 256 + 8 * kk), dv + offv,
                             kIdO, kk > 0 || j > 0);
           }
@@ -465,30 +466,8 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
   tc_fence_before_sync();
   __syncthreads();
   if (warp == kIssuerWarp) {
-
     tc_fence_after_sync();
     tmem_dealloc(tmem, Lay::kTmemCols);
-  }
-}
-
-// V [BH, S, D] -> V^T [BH, D, ldt] (bf16), 32 x 32 tiles through shared memory.
-__global__ void __launch_bounds__(256) transpose_v_kernel(const uint16_t* __restrict__ v,
-                                                          uint16_t* __restrict__ vt, int S, int D,
-                                                          int ldt) {
-  __shared__ uint16_t tile[32][33];
-  pdl_entry();
-  const int bh = blockIdx.z;
-  const int s0 = blockIdx.x * 32, d0 = blockIdx.y * 32;
-  const uint16_t* src = v + (size_t)bh * S * D;
-  uint16_t* dst = vt + (size_t)bh * D * ldt;
-  for (int i = threadIdx.y; i < 32; i += 8) {
-    const int s = s0 + i, d = d0 + threadIdx.x;
-    if (s < S && d < D) tile[i][threadIdx.x] = src[(size_t)s * D + d];
-  }
-  __syncthreads();
-  for (int i = threadIdx.y; i < 32; i += 8) {
-    const int d = d0 + i, s = s0 + threadIdx.x;
-    if (s < S && d < D) dst[(size_t)d * ldt + s] = tile[threadIdx.x][i];
   }
 }
 
@@ -537,12 +516,12 @@ cudaError_t allow_smem(const void* kernel, int bytes) {
 }
 
 template <int D>
-cudaError_t launch_attn_d(const uint16_t* q, const uint16_t* k, const uint16_t* vt, int ldt, float* o,
+cudaError_t launch_attn_d(const uint16_t* q, const uint16_t* k, const uint16_t* v, float* o,
                           float* lse, int BH, int L, int S, int causal, float scale, cudaStream_t s) {
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, q, D, L, BH, D, (uint64_t)L * D, kBM) ||
       !make_map(&mk, k, D, S, BH, D, (uint64_t)S * D, kBN) ||
-      !make_map(&mv, vt, S, D, BH, ldt, (uint64_t)D * ldt, D))
+      !make_map(&mv, v, D, S, BH, D, (uint64_t)S * D, kBN))
     return cudaErrorInvalidValue;
   auto kern = attention_fwd_kernel<D>;
   cudaError_t e = allow_smem(reinterpret_cast<const void*>(kern), AttnLayout<D>::kAlloc);
@@ -554,17 +533,10 @@ cudaError_t launch_attn_d(const uint16_t* q, const uint16_t* k, const uint16_t* 
 
 }  // namespace
 
-int attention_vt_stride(int S) { return (S + 7) / 8 * 8; }
-
-cudaError_t launch_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* vt_ws,
-                             float* o, float* lse, int BH, int L, int S, int D, int causal, float scale,
-                             cudaStream_t s) {
-  const int ldt = attention_vt_stride(S);
-  const dim3 tgrid((unsigned)((S + 31) / 32), (unsigned)((D + 31) / 32), (unsigned)BH);
-  cudaError_t e = launch_pdl(transpose_v_kernel, tgrid, dim3(32, 8), 0, s, 0, v, vt_ws, S, D, ldt);
-  if (e != cudaSuccess) return e;
-  if (D == 64) return launch_attn_d<64>(q, k, vt_ws, ldt, o, lse, BH, L, S, causal, scale, s);
-  if (D == 128) return launch_attn_d<128>(q, k, vt_ws, ldt, o, lse, BH, L, S, causal, scale, s);
+cudaError_t launch_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, float* o, float* lse,
+                             int BH, int L, int S, int D, int causal, float scale, cudaStream_t s) {
+  if (D == 64) return launch_attn_d<64>(q, k, v, o, lse, BH, L, S, causal, scale, s);
+  if (D == 128) return launch_attn_d<128>(q, k, v, o, lse, BH, L, S, causal, scale, s);
   return cudaErrorInvalidValue;
 }
 

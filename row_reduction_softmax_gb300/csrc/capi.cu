@@ -410,7 +410,7 @@ int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_co
 // fewer, fuller CTAs per band win, and beyond 4 CTAs per band the two-phase
 // path is faster, so the planner takes the cluster only up to cs = 4.  COLS_TWO_PHASE: row
 // chunks sized for about 4 CTAs per SM over all bands.
-enum WorkspaceKindCols { kWsCols = 3, kWsAttn = 4 };
+enum WorkspaceKindCols { kWsCols = 3 };
 
 constexpr int64_t kColsAutoMaxCluster = 4;
 
@@ -868,13 +868,10 @@ RRS_API int attention_fwd(const void* q, const void* k, const void* v, float* o,
   if ((st = check_device_pointer(o, dev, "o")) != RRS_OK) return st;
   if (lse && (st = check_device_pointer(lse, dev, "lse")) != RRS_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  void* ws = nullptr;
-  const size_t ws_bytes = (size_t)BH * d * attention_vt_stride((int)S) * 2;
-  if ((st = get_workspace(dev, s, kWsAttn, ws_bytes, &ws)) != RRS_OK) return st;
   const float sc = scale > 0.f ? scale : 1.0f / std::sqrt((float)d);
   e = launch_attention(static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(k),
-                       static_cast<const uint16_t*>(v), static_cast<uint16_t*>(ws), o, lse, (int)BH,
-                       (int)L, (int)S, (int)d, causal ? 1 : 0, sc, s);
+                       static_cast<const uint16_t*>(v), o, lse, (int)BH, (int)L, (int)S, (int)d,
+                       causal ? 1 : 0, sc, s);
   if (e != cudaSuccess) return fail_cuda(e, "attention_fwd launch");
   return RRS_OK;
 }

@@ -99,12 +99,9 @@ cudaError_t launch_gelu(const float* x, float* y, int64_t n, int sm_count, cudaS
 
 // ---- fused attention forward (attention.cu) ----
 // q, k, v: bf16 bit patterns, [BH, L | S, D] contiguous, 16-byte aligned;
-// vt_ws: workspace of BH x D x attention_vt_stride(S) bf16 for V^T; o: fp32
-// [BH, L, D]; lse: fp32 [BH, L] or null.  D is 64 or 128.
-int attention_vt_stride(int S);
-cudaError_t launch_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* vt_ws,
-                             float* o, float* lse, int BH, int L, int S, int D, int causal, float scale,
-                             cudaStream_t s);
+// o: fp32 [BH, L, D]; lse: fp32 [BH, L] or null.  D is 64 or 128.
+cudaError_t launch_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, float* o, float* lse,
+                             int BH, int L, int S, int D, int causal, float scale, cudaStream_t s);
 
 // ---- device error words (set by kernels whose bounded waits ran out) ----
 cudaError_t read_and_clear_staged_error(cudaStream_t s, unsigned* value);

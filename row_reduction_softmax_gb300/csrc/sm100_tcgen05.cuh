@@ -56,12 +56,27 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
          ((uint64_t)(1024u >> 4) << 32) | ((uint64_t)1u << 46) | ((uint64_t)2u << 61);
 }
 
+// The same layout with the tile's contiguous 128-byte rows running along M
+// or N instead of K (an MN-major operand: for example V [keys][d] as the
+// B operand of P V, whose N is d): 8 rows of 128 bytes (8 K indices x 64
+// M/N elements) form a 1024-byte swizzle atom, the stride byte offset (bits
+// [32, 46)) steps 8 K indices (1024 bytes) and the leading byte offset
+// (bits [16, 30)) steps from one 64-element block of M/N to the next.
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t saddr, uint32_t lbo_bytes) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)(1024u >> 4) << 32) | ((uint64_t)1u << 46) | ((uint64_t)2u << 61);
+}
+
 // Instruction descriptor of tcgen05.mma kind::f16 with bf16 A and B, fp32
 // D, both operands K-major: D format in bits [4, 6) (1 = f32), A and B
 // formats in [7, 10) and [10, 13) (1 = bf16), N >> 3 in [17, 23), M >> 4 in
 // [24, 29).
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// The same with an MN-major B operand (the B major bit, bit 16).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(int M, int N) {
+  return idesc_bf16_f32(M, N) | (1u << 16);
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
