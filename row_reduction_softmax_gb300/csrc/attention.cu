@@ -409,8 +409,10 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
       uint64_t ps2[4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) ps2[c] = 0ull;   // +0.0f in both halves
-      const bool live = (m_new != kNeg);
-      const uint64_t c2 = f2_pack(scale_log2e, scale_log2e), nm2 = f2_pack(-m_new, -m_new);
+      // a row with no visible key so far has only -inf scores: shifting by 0
+      // instead of -inf gives 2^-inf = 0 for all of them (never -inf - -inf)
+      const float m_eff = (m_new == kNeg) ? 0.f : m_new;
+      const uint64_t c2 = f2_pack(scale_log2e, scale_log2e), nm2 = f2_pack(-m_eff, -m_eff);
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) {
         const float* sv = (cb < 2) ? sa + 32 * cb : sb + 32 * (cb - 2);
@@ -419,8 +421,8 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
         for (int i = 0; i < 16; ++i) {
           float xa, xb;
           f2_unpack(f2_fma(f2_pack(sv[2 * i], sv[2 * i + 1]), c2, nm2), xa, xb);
-          const float a = live ? exp2_sfu(xa) : 0.f;
-          const float b = live ? exp2_sfu(xb) : 0.f;
+          const float a = exp2_sfu(xa);
+          const float b = exp2_sfu(xb);
           ps2[i & 3] = f2_add(ps2[i & 3], f2_pack(a, b));
           pk[i] = pack_bf16(a, b);
         }
