@@ -92,7 +92,8 @@ typedef enum rrs_cols_path {
   RRS_COLS_AUTO = -1,
   RRS_COLS_TWO_PHASE = 0,  /* any shape/alignment: per-(row chunk, column) partials, then merge + re-read + write */
   RRS_COLS_CLUSTER = 1,    /* a band of 32 columns over a cluster of CTAs, all rows in registers (M <= 8192) */
-  RRS_COLS_COUNT = 2
+  RRS_COLS_BAND = 2,       /* a band of 32 columns over a cluster of CTAs, rows streamed twice (second read from L2) */
+  RRS_COLS_COUNT = 3
 } rrs_cols_path;
 
 typedef struct rrs_plan {

@@ -403,16 +403,12 @@ int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_co
   }
 }
 
-// Column softmax.  COLS_CLUSTER: a band of 32 columns per cluster; as many
-// rows per thread as useful (vec a power of two, at most 16), so the fewest
-// CTAs share a band: cs = ceil(M / (32 row groups x vec)) <= 16 (M <= 8192).
-// Measured on GB300 (1024 x 8192, 256 x 32768, 2048 x 4096, 4096 x 16384):
-// fewer, fuller CTAs per band win, and beyond 4 CTAs per band the two-phase
-// path is faster, so the planner takes the cluster only up to cs = 4.  COLS_TWO_PHASE: row
-// chunks sized for about 4 CTAs per SM over all bands.
+// Column softmax.  COLS_CLUSTER (forced only): a band of 32 columns per
+// cluster; as many rows per thread as useful (vec a power of two, at most
+// 16), so the fewest CTAs share a band: cs = ceil(M / (32 row groups x vec))
+// <= 16 (M <= 8192).  COLS_TWO_PHASE: row chunks sized for about 4 CTAs per
+// SM over all bands (unaligned inputs).  COLS_BAND: below.
 enum WorkspaceKindCols { kWsCols = 3 };
-
-constexpr int64_t kColsAutoMaxCluster = 4;
 
 bool plan_cols_cluster(int64_t M, int64_t N, int64_t max_cs, rrs_plan* p) {
   const int64_t groups = cols_row_groups();
@@ -445,6 +441,28 @@ void plan_cols_two_phase(int64_t M, int64_t N, int sm_count, rrs_plan* p) {
   p->workspace_bytes = chunks * N * 8;
 }
 
+// COLS_BAND: the fewest CTAs per band (a power of two, at most 8) that keep
+// a CTA's rows at most 512 (M < 2048) or 1024: measured on GB300,
+// 1024 x 8192 ran fastest with 512 rows per CTA (18.3 us; 256 rows: 22.6,
+// 1024: 25.5) and 4096 x 16384 with 1024 (119.8 us; 512: 128, 2048: 124.9).
+// At most 1024 rows (128 KB of x) per CTA and four CTAs per SM keep the x
+// that pass 2 re-reads within the L2.
+bool bands_fit_grid(int64_t N) { return ceil_div(N, cols_band()) * 8 <= (int64_t)INT_MAX; }
+
+void plan_cols_band(int64_t M, int64_t N, rrs_plan* p) {
+  const int64_t bands = ceil_div(N, cols_band());
+  const int64_t max_rows = (M < 2048) ? 512 : 1024;
+  int64_t cs = 1;
+  while (cs < 8 && ceil_div(M, cs) > max_rows) cs *= 2;
+  p->path = RRS_COLS_BAND;
+  p->threads = cols_threads();
+  p->cluster = (int32_t)cs;
+  p->grid = bands * cs;
+  p->ctas_per_row = cs;
+  p->chunk = ceil_div(M, cs);
+  p->rows_per_cta = (int32_t)std::min<int64_t>(p->chunk, INT_MAX);
+}
+
 int plan_cols_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_count, int cluster_ok,
                    int forced, rrs_plan* p) {
   std::memset(p, 0, sizeof(*p));
@@ -458,9 +476,16 @@ int plan_cols_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_count
   }
   const bool cluster_fits = vector_ok && cluster_ok;
   if (forced == RRS_COLS_AUTO) {
-    if (!(cluster_fits && plan_cols_cluster(M, N, kColsAutoMaxCluster, p)))
+    // measured on GB300: the band path is the fastest wherever it applies
+    // (1024 x 8192: 18.3 us against 19.5 cluster and 28.6 two-phase;
+    // 4096 x 16384: 119.8 against 172.8 and 140.9)
+    if (cluster_fits && bands_fit_grid(N)) {
+      plan_cols_band(M, N, p);
+      p->vector_io = 1;
+    } else {
       plan_cols_two_phase(M, N, sm_count, p);
-    p->vector_io = vector_ok ? 1 : 0;
+      p->vector_io = vector_ok ? 1 : 0;
+    }
     return RRS_OK;
   }
   if (forced == RRS_COLS_CLUSTER) {
@@ -474,6 +499,14 @@ int plan_cols_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_count
     plan_cols_two_phase(M, N, sm_count, p);
     p->vector_io = vector_ok ? 1 : 0;
     return RRS_OK;
+  }
+  if (forced == RRS_COLS_BAND) {
+    if (cluster_fits && bands_fit_grid(N)) {
+      plan_cols_band(M, N, p);
+      p->vector_io = 1;
+      return RRS_OK;
+    }
+    return fail(RRS_ERR_UNSUPPORTED, "COLS_BAND needs 16-byte alignment and cluster launch");
   }
   return fail(RRS_ERR_UNSUPPORTED, "column path not available");
 }
@@ -720,6 +753,8 @@ RRS_API int softmax_cols(const float* x, int64_t ldx, float* y, int64_t ldy, int
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (plan.path == RRS_COLS_CLUSTER) {
     e = launch_softmax_cols_cluster(plan, x, y, M, N, l, s);
+  } else if (plan.path == RRS_COLS_BAND) {
+    e = launch_softmax_cols_band(plan, x, y, M, N, l, s);
   } else {
     void* ws = nullptr;
     if ((st = get_workspace(dev, s, kWsCols, (size_t)plan.workspace_bytes, &ws)) != RRS_OK) return st;

@@ -77,6 +77,9 @@ int cols_row_groups();
 int cols_rows_per_thread_max();
 cudaError_t launch_softmax_cols_cluster(const rrs_plan& p, const float* x, float* y, int64_t M,
                                         int64_t N, const Layout& l, cudaStream_t s);
+// COLS_BAND plans carry cluster (CTAs per band, <= 8) and rows_per_cta.
+cudaError_t launch_softmax_cols_band(const rrs_plan& p, const float* x, float* y, int64_t M, int64_t N,
+                                     const Layout& l, cudaStream_t s);
 cudaError_t launch_softmax_cols_two_phase(const rrs_plan& p, const float* x, float* y, int64_t M,
                                           int64_t N, const Layout& l, void* workspace,
                                           cudaStream_t s);

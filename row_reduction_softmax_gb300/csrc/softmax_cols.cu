@@ -18,6 +18,15 @@
 //   then over the cluster's CTAs (DSMEM), merged with m = max(m_a, m_b),
 //   s = s_a e^(m_a - m) + s_b e^(m_b - m).  One read and one write per
 //   element.  M <= 16 * 32 * 16 = 8192.
+// COLS_BAND -- a band of 32 columns per cluster of cs <= 8 CTAs, each CTA
+//   streaming its rows twice: pass 1 loads them at L2 evict-last priority
+//   and forms per-column online (max, sum) partials, the cluster merges
+//   them over DSMEM, pass 2 re-reads the rows -- from the L2, where pass 1
+//   left them moments before -- and writes y.  HBM sees one read and one
+//   write per element, with nothing but a few registers of state per
+//   thread, so any M fits.  The planner sizes a CTA's rows (at most 1024 =
+//   128 KB of x) so that the x of all resident CTAs (four per SM) fits the
+//   L2 together.
 // COLS_TWO_PHASE -- any M and alignment: kernel 1 writes each (row chunk,
 //   column) online partial to a workspace, kernel 2 merges a column's
 //   partials, re-reads its chunk and writes y (12 bytes per element unless
@@ -206,6 +215,148 @@ softmax_cols_cluster_kernel(const float* x, float* y, int64_t M, int64_t N, int6
   cluster_wait_acquire();  // peers finished reading part[] before this CTA exits
 }
 
+// --------------------------------------------------------------- COLS_BAND ---
+// Grid: (bands * cs) CTAs in clusters of cs along x; cluster k owns columns
+// [32k, 32k + 32).  Rank r owns rows [r * rseg, min((r + 1) * rseg, M)),
+// rseg = ceil(M / cs).  Thread (warp w, lane l) is in row group
+// g = 4w + l / 8 and column slot l % 8 (columns 4 (l % 8) .. + 3 of the
+// band); it walks rows r0 + g, r0 + g + 32, ... with kBU rows in flight.
+// x, y 16-byte aligned and ldx, ldy multiples of 4 (any M, N).  LOG writes
+// (x - m) - log(s).  In place (x == y) is safe: every element is read by the
+// thread that writes it, and pass 2 reads an element before writing it.
+constexpr int kBU = 8;   // rows in flight per thread and batch
+
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ float4 load_evict_last(const float4* p, uint64_t pol) {
+  float4 v;
+  asm volatile("ld.global.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
+
+template <bool LOG>
+__global__ void __launch_bounds__(kCT, 4)
+softmax_cols_band_kernel(const float* x, float* y, int64_t M, int64_t N, int64_t ldx, int64_t ldy) {
+  __shared__ MaxSum red[kGroups][kBand];
+  __shared__ MaxSum part[kBand];   // this CTA's per-column (m_c, s_c), read by its peers
+  __shared__ MaxSum whole[kBand];  // the merged pair of each column
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int cs = (int)cluster.num_blocks();
+  const int rank = (int)cluster.block_rank();
+  const int64_t band = blockIdx.x / cs;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int slot = lane % kLPR;
+  const int g = warp * kRPW + lane / kLPR;
+  const int64_t rseg = (M + cs - 1) / cs;
+  const int64_t r0 = rank * rseg;
+  const int64_t r1 = min(r0 + rseg, M);
+  const int64_t j0 = band * kBand + 4 * slot;
+  const bool live_col = j0 < N;   // N % 4 == 0 is not required: see the tail below
+  const bool full4 = j0 + 3 < N;
+  const float kNeg = neg_inf();
+  pdl_entry();
+  const uint64_t pol = l2_evict_last_policy();
+
+  auto load_row = [&](int64_t r, bool keep) -> float4 {
+    const float* row = x + r * ldx;
+    if (full4) return keep ? load_evict_last(reinterpret_cast<const float4*>(row + j0), pol)
+                           : load_stream(reinterpret_cast<const float4*>(row + j0));
+    float4 v;
+    v.x = (j0 + 0 < N) ? row[j0 + 0] : kNeg;
+    v.y = (j0 + 1 < N) ? row[j0 + 1] : kNeg;
+    v.z = (j0 + 2 < N) ? row[j0 + 2] : kNeg;
+    v.w = kNeg;
+    return v;
+  };
+
+  // ---- pass 1: online (max, sum) per column over this thread's rows ----
+  MaxSum p[4] = {{kNeg, 0.f}, {kNeg, 0.f}, {kNeg, 0.f}, {kNeg, 0.f}};
+  if (live_col) {
+    for (int64_t r = r0 + g; r < r1; r += (int64_t)kBU * kGroups) {
+      float4 a[kBU];
+#pragma unroll
+      for (int u = 0; u < kBU; ++u) {
+        const int64_t ru = r + (int64_t)u * kGroups;
+        a[u] = (ru < r1) ? load_row(ru, true) : make_float4(kNeg, kNeg, kNeg, kNeg);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float bm = comp(a[0], k);
+#pragma unroll
+        for (int u = 1; u < kBU; ++u) bm = max_nan(bm, comp(a[u], k));
+        rescale_to(p[k], bm);
+        if (p[k].m != kNeg) {
+#pragma unroll
+          for (int u = 0; u < kBU; ++u) p[k].s += exp_shifted(comp(a[u], k), p[k].m);
+        }
+      }
+    }
+  }
+  // ---- merge: the CTA's 32 row groups (fixed order), then the cluster's ranks ----
+#pragma unroll
+  for (int k = 0; k < 4; ++k) red[g][4 * slot + k] = p[k];
+  __syncthreads();
+  if (tid < kBand) {
+    MaxSum q{kNeg, 0.f};
+    for (int k = 0; k < kGroups; ++k) q = merge(q, red[k][tid]);
+    part[tid] = q;
+  }
+  cluster_arrive_release();  // publish part[] to the cluster
+  cluster_wait_acquire();    // every peer's part[] is visible
+  if (tid < kBand) {
+    MaxSum q{kNeg, 0.f};
+    for (int k = 0; k < cs; ++k) q = merge(q, *cluster.map_shared_rank(&part[tid], k));
+    whole[tid] = q;  // the same ranks in the same order in every CTA
+  }
+  cluster_arrive_relaxed();  // done reading the peers' part[]
+  __syncthreads();
+
+  // ---- pass 2: re-read (from the L2), normalise, write ----
+  float wm[4], k4[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const MaxSum w = whole[(4 * slot + c) & (kBand - 1)];
+    wm[c] = w.m;
+    const bool bad = !(w.s == w.s) || w.m == kNeg;  // NaN / inf / all -inf column
+    if constexpr (LOG) {
+      k4[c] = logf(w.s);
+    } else {
+      k4[c] = bad ? __int_as_float(0x7fc00000) : 1.0f / w.s;
+    }
+  }
+  if (live_col) {
+    for (int64_t r = r0 + g; r < r1; r += (int64_t)kBU * kGroups) {
+      float4 a[kBU];
+#pragma unroll
+      for (int u = 0; u < kBU; ++u) {
+        const int64_t ru = r + (int64_t)u * kGroups;
+        if (ru < r1) a[u] = load_row(ru, false);
+      }
+#pragma unroll
+      for (int u = 0; u < kBU; ++u) {
+        const int64_t ru = r + (int64_t)u * kGroups;
+        if (ru >= r1) continue;
+        float4 o;
+        if constexpr (LOG) {
+          o = make_float4(log_softmax_of(a[u].x, wm[0], k4[0]), log_softmax_of(a[u].y, wm[1], k4[1]),
+                          log_softmax_of(a[u].z, wm[2], k4[2]), log_softmax_of(a[u].w, wm[3], k4[3]));
+        } else {
+          o = make_float4(exp_shifted(a[u].x, wm[0]) * k4[0], exp_shifted(a[u].y, wm[1]) * k4[1],
+                          exp_shifted(a[u].z, wm[2]) * k4[2], exp_shifted(a[u].w, wm[3]) * k4[3]);
+        }
+        store_cols<true>(y + ru * ldy, j0, N, o);
+      }
+    }
+  }
+  cluster_wait_acquire();  // peers finished reading part[] before this CTA exits
+}
+
 // --------------------------------------------------------- COLS_TWO_PHASE ---
 // Grid: bands x chunks CTAs, CTA (band b, chunk c) = blockIdx.x = c * bands + b.
 // Chunk c holds rows [c * chunk, min((c + 1) * chunk, M)); row group g takes
@@ -384,6 +535,16 @@ cudaError_t launch_softmax_cols_cluster(const rrs_plan& p, const float* x, float
     case 16: return launch_cols_cluster_v<16>(p, x, y, M, N, l, s);
     default: return cudaErrorInvalidConfiguration;
   }
+}
+
+cudaError_t launch_softmax_cols_band(const rrs_plan& p, const float* x, float* y, int64_t M, int64_t N,
+                                     const Layout& l, cudaStream_t s) {
+  if (p.threads != kCT || p.cluster < 1 || p.cluster > 8) return cudaErrorInvalidConfiguration;
+  if (l.log_out)
+    return launch_pdl(softmax_cols_band_kernel<true>, dim3((unsigned)p.grid), dim3(kCT), 0, s, p.cluster, x, y,
+                      M, N, l.ldx, l.ldy);
+  return launch_pdl(softmax_cols_band_kernel<false>, dim3((unsigned)p.grid), dim3(kCT), 0, s, p.cluster, x, y,
+                    M, N, l.ldx, l.ldy);
 }
 
 cudaError_t launch_softmax_cols_two_phase(const rrs_plan& p, const float* x, float* y, int64_t M,

@@ -238,19 +238,15 @@ def test_cols_planner(lib, M, N):
     p = rrs.plan_softmax_cols(M, N)
     bands = -(-N // 32)
     assert p["threads"] == 256
-    if M <= 2048:
-        assert p["path_name"] == "cluster"
-        cs, vec = p["cluster"], p["vec"]
-        assert 1 <= cs <= 4 and vec in (1, 2, 4, 8, 16)
-        rows = 32 * vec                                  # rows one CTA holds
-        assert cs * rows >= M > (cs - 1) * rows or cs == 1   # every row held once
-        assert vec == 16 or cs == 1                      # the fewest CTAs per band
-        assert p["grid"] == bands * cs
-    else:
-        assert p["path_name"] == "two_phase"
-        chunks, chunk = p["ctas_per_row"], p["chunk"]
-        assert chunks * chunk >= M > (chunks - 1) * chunk
-        assert p["grid"] == bands * chunks and p["workspace_bytes"] == chunks * N * 8
+    # aligned input: the band path, the fewest CTAs per band (a power of two,
+    # at most 8) that keep a CTA at most 512 rows (M < 2048) or 1024 rows
+    assert p["path_name"] == "band" and p["workspace_bytes"] == 0
+    cs, rows = p["cluster"], p["rows_per_cta"]
+    cap = 512 if M < 2048 else 1024
+    assert cs in (1, 2, 4, 8) and rows == -(-M // cs)
+    assert rows <= cap or cs == 8
+    assert cs == 1 or -(-M // (cs // 2)) > cap                # no smaller cluster would do
+    assert p["grid"] == bands * cs
     q = rrs.plan_softmax_cols(M, N, vector_ok=False)
     assert q["path_name"] == "two_phase" and q["vector_io"] == 0
 
@@ -260,6 +256,15 @@ def test_cols_forced_paths(lib):
     try:
         rrs.force_cols_path("two_phase")
         assert rrs.plan_softmax_cols(64, 1024)["path_name"] == "two_phase"
+        p = rrs.plan_softmax_cols(4096, 1024)
+        chunks, chunk = p["ctas_per_row"], p["chunk"]
+        assert chunks * chunk >= 4096 > (chunks - 1) * chunk
+        assert p["grid"] == 32 * chunks and p["workspace_bytes"] == chunks * 1024 * 8
+        rrs.force_cols_path("band")
+        assert rrs.plan_softmax_cols(64, 1024)["path_name"] == "band"
+        with pytest.raises(rrs.RRSError) as e:
+            rrs.plan_softmax_cols(64, 1024, vector_ok=False)
+        assert e.value.status == UNSUPPORTED
         rrs.force_cols_path("cluster")
         p = rrs.plan_softmax_cols(8192, 1024)            # forced: up to 16 CTAs per band
         assert p["path_name"] == "cluster" and p["cluster"] == 16 and p["vec"] == 16

@@ -238,16 +238,16 @@ def run_cols(x_host, N, ldx, ldy, path="auto", flags=0, in_place=False, x_off=0,
 
 COL_SHAPES = [(1, 1), (2, 5), (7, 3), (8, 128), (9, 129), (64, 250), (100, 33), (129, 512),
               (1024, 300), (2047, 64), (2048, 131), (2049, 130), (5000, 40), (8192, 37),
-              (8193, 20)]
+              (8193, 20), (20000, 36)]
 
 
-@pytest.mark.parametrize("path", ["cluster", "two_phase"])
+@pytest.mark.parametrize("path", ["cluster", "band", "two_phase"])
 @pytest.mark.parametrize("M,N", COL_SHAPES)
 def test_cols_parity(path, M, N):
     if path == "cluster" and M > 8192:
         pytest.skip("more rows than a cluster holds")
     x = recipe(["c2", "c4", "c3"][(M + N) % 3], M, N)
-    ld = N if path == "two_phase" else -(-N // 4) * 4   # the cluster path wants ld % 4 == 0
+    ld = N if path == "two_phase" else -(-N // 4) * 4   # the cluster and band paths want ld % 4 == 0
     y, guards = run_cols(x, N, ld, ld, path)
     check_softmax_cols(y, x, f"cols {path} {M}x{N}")
     assert guards
@@ -256,7 +256,7 @@ def test_cols_parity(path, M, N):
     assert guards
 
 
-@pytest.mark.parametrize("path", ["cluster", "two_phase"])
+@pytest.mark.parametrize("path", ["cluster", "band", "two_phase"])
 def test_cols_strides_in_place_and_specials(path):
     M, N = 300, 260
     rng = np.random.default_rng(32)
@@ -280,9 +280,10 @@ def test_cols_unaligned_takes_two_phase():
     y, guards = run_cols(x, 301, 303, 305, "auto", x_off=1, y_off=3)
     check_softmax_cols(y, x, "cols unaligned")
     assert guards
-    with pytest.raises(rrs.RRSError) as e:
-        run_cols(x, 301, 303, 305, "cluster", x_off=1, y_off=3)
-    assert e.value.status == 6
+    for path in ("cluster", "band"):
+        with pytest.raises(rrs.RRSError) as e:
+            run_cols(x, 301, 303, 305, path, x_off=1, y_off=3)
+        assert e.value.status == 6
 
 
 # ------------------------------------------------------- full-size variants ----
