@@ -157,6 +157,7 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
   uint32_t* tmem_base_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 17);
   static_assert(kStages == 2 && kQT == 2, "barrier slots above");
+  static_assert(Lay::kQBytes >= 4 * 32 * 32 * 4, "a query tile's buffer stages its O blocks");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.y;
@@ -440,10 +441,20 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
     }
     const bool have_o = __all_sync(kFullMask, ok && nt > 0 && wait_bar(&bar_o[t], 0u, abort_flag));
     if (have_o) tc_fence_after_sync();
-    if (!*abort_flag && (have_o || nt == 0)) {
-      // O = O / l (a row that sees no key: 0 / 0 = NaN, its LSE -inf)
+    // A tile with no visible key still stages its NaN rows through its Q
+    // buffer: wait until the Q load (issued whenever the other tile has work)
+    // has landed there.
+    const bool q_ready = nt > 0 || n_max == 0 || __all_sync(kFullMask, wait_bar(bar_q, 0u, abort_flag));
+    if (!*abort_flag && q_ready && (have_o || nt == 0)) {
+      // O = O / l (a row that sees no key: 0 / 0 = NaN, its LSE -inf).  Each
+      // warp passes its 32 rows x 32 columns blocks through shared memory
+      // (XOR-swizzled, conflict-free both ways) so that every global store
+      // writes 128 contiguous bytes of one row.  The staging space is this
+      // tile's Q buffer: the tile's last S MMA completed before bar_o.
       const float inv = 1.0f / l;
-      float* orow = O + ((size_t)bh * L + qrow) * D;
+      float* stg = reinterpret_cast<float*>(smem + Lay::kQ + t * Lay::kQBytes) + (warp & 3) * 32 * 32;
+      const int row0 = q0 + t * kBM + (warp & 3) * 32;   // the warp's first row
+      float* obase = O + ((size_t)bh * L + row0) * D + lane;
 #pragma unroll
       for (int cb = 0; cb < D / 32; ++cb) {
         float v[32];
@@ -454,12 +465,13 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0.f;
         }
-        if (qrow < L) {
-          float4* o4 = reinterpret_cast<float4*>(orow + cb * 32);
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            o4[i] = make_float4(v[4 * i] * inv, v[4 * i + 1] * inv, v[4 * i + 2] * inv, v[4 * i + 3] * inv);
-        }
+        for (int i = 0; i < 32; ++i) stg[lane * 32 + (i ^ lane)] = v[i] * inv;
+        __syncwarp();
+#pragma unroll 8
+        for (int k = 0; k < 32; ++k)
+          if (row0 + k < L) obase[(size_t)k * D + cb * 32] = stg[k * 32 + (lane ^ k)];
+        __syncwarp();
       }
       if (LSE && qrow < L)
         LSE[(size_t)bh * L + qrow] = (m == kNeg) ? kNeg : (m + log2f(l)) * 0.69314718055994531f;
