@@ -69,6 +69,24 @@ __device__ __forceinline__ void store_stream(float4* p, const float4& v) { __stc
 __device__ __forceinline__ float load_stream(const float* p) { return __ldcs(p); }
 __device__ __forceinline__ void store_stream(float* p, float v) { __stcs(p, v); }
 
+// Loads marked last use (PTX ld.global.lu: on global memory a streaming
+// load, like ld.cs).  Measured on GB300, the row-register softmax on
+// 8192 x 1024 runs in 11.2 us with them against 11.7 us with ld.cs (and no
+// other kernel here changed), so only that kernel uses them.
+__device__ __forceinline__ float4 load_last_use(const float4* p) {
+  float4 v;
+  asm volatile("ld.global.lu.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ float load_last_use(const float* p) {
+  float v;
+  asm volatile("ld.global.lu.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // Start of every kernel launched with launch_pdl(): allow the next kernel on
 // the stream to be scheduled, then wait for the previous one to complete.
 __device__ __forceinline__ void pdl_launch_dependents() {

@@ -108,17 +108,17 @@ softmax_row_regs_kernel(const float* x, float* y, int64_t M, int32_t N, int64_t 
 #pragma unroll
       for (int i = 0; i < VEC; ++i) {
         const int c = i * kGT + gt;
-        v[i] = (c < n4) ? load_stream(xr4 + c) : make_float4(kNeg, kNeg, kNeg, kNeg);
+        v[i] = (c < n4) ? load_last_use(xr4 + c) : make_float4(kNeg, kNeg, kNeg, kNeg);
       }
-      t = (gt < rem) ? load_stream(xr + 4 * n4 + gt) : kNeg;  // ragged tail, N % 4 != 0
+      t = (gt < rem) ? load_last_use(xr + 4 * n4 + gt) : kNeg;  // ragged tail, N % 4 != 0
     } else {
 #pragma unroll
       for (int i = 0; i < VEC; ++i) {
         const int j = 4 * i * kGT + gt;
-        v[i].x = (j < N) ? load_stream(xr + j) : kNeg;
-        v[i].y = (j + kGT < N) ? load_stream(xr + j + kGT) : kNeg;
-        v[i].z = (j + 2 * kGT < N) ? load_stream(xr + j + 2 * kGT) : kNeg;
-        v[i].w = (j + 3 * kGT < N) ? load_stream(xr + j + 3 * kGT) : kNeg;
+        v[i].x = (j < N) ? load_last_use(xr + j) : kNeg;
+        v[i].y = (j + kGT < N) ? load_last_use(xr + j + kGT) : kNeg;
+        v[i].z = (j + 2 * kGT < N) ? load_last_use(xr + j + 2 * kGT) : kNeg;
+        v[i].w = (j + 3 * kGT < N) ? load_last_use(xr + j + 3 * kGT) : kNeg;
       }
     }
 

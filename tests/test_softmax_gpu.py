@@ -175,6 +175,33 @@ def test_rejects_host_memory():
     assert e.value.status == 2
 
 
+@pytest.mark.parametrize("name", ["c2", "c4"])
+@pytest.mark.parametrize("path", ["auto", "cluster", "two_phase"])
+def test_input_written_just_before_reads_back_intact(name, path):
+    """x written by kernels right before the call -- its lines still dirty in
+    the L2 -- is read back unchanged by a later kernel, and the softmax of it
+    is right: the library's streaming loads never drop or alter x."""
+    rrs.force_path(path, "auto")
+    try:
+        w = workloads.WORKLOADS[name]
+        x_host = workloads.matrix(w)
+        src = torch.from_numpy(x_host).cuda()
+        x = torch.zeros_like(src)
+        y = torch.empty_like(src)
+        rows = [0, 7, w.M // 2, w.M - 1]
+        for _ in range(3):
+            x.zero_()
+            x.copy_(src)             # device writes of x: dirty in the L2
+            x.mul_(1.0)              # and once more
+            rrs.softmax_rows(x, y)
+            back = x.clone()         # a later kernel reads x
+            torch.cuda.synchronize()
+            assert torch.equal(back, src)
+            check_softmax(y[rows].cpu().numpy(), x_host[rows], f"{name} {path} after device writes")
+    finally:
+        rrs.force_path("auto", "auto")
+
+
 def test_two_streams_use_separate_workspaces():
     rrs.force_path("two_phase")
     xs = [recipe("c5", 4, 300000 + 17 * i) for i in range(2)]
