@@ -373,69 +373,90 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
           sb[i] = (k0 + 64 + i <= kmax) ? sb[i] : kNeg;
         }
       }
-      // row max of the raw scores (eight chains), then scaled (scale_log2e > 0 keeps the order)
-      float mx[8];
+      // p = 2^(s scale log2e - m_ref) for the tile's 128 keys: one FMA (in
+      // pairs) and one SFU op per key; P as bf16 pairs over S, in four chunks
+      // of 32 keys (16 columns each); returns the tile's part of l in fp32
+      // (four chains of pairs).  A row with no visible key so far has only
+      // -inf scores: shifting by 0 instead of -inf gives 2^-inf = 0 for all
+      // of them (never -inf - -inf).
+      const uint64_t c2 = f2_pack(scale_log2e, scale_log2e);
+      auto write_p = [&](float m_ref) -> float {
+        const float m_eff = (m_ref == kNeg) ? 0.f : m_ref;
+        const uint64_t nm2 = f2_pack(-m_eff, -m_eff);
+        uint64_t ps2[4];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) mx[c] = max_nan(sa[c], sb[c]);
+        for (int c = 0; c < 4; ++c) ps2[c] = 0ull;   // +0.0f in both halves
 #pragma unroll
-      for (int i = 8; i < 64; ++i) mx[i & 7] = max3_nan(mx[i & 7], sa[i], sb[i]);
-      float tmax = max3_nan(max3_nan(mx[0], mx[1], mx[2]), max3_nan(mx[3], mx[4], mx[5]),
-                            max_nan(mx[6], mx[7]));
-      tmax *= scale_log2e;
-      // The reference max moves only when the tile's max exceeds it by more
-      // than 2^8 (or on the first visible key): p = 2^(s - m) then stays
-      // below 256, exact in fp32 and in bf16's range, and O is rescaled far
-      // less often.  The result is the same softmax: O and l share m.
-      float m_new = m, alpha = 1.f;
-      if (m == kNeg || !(tmax <= m + 8.f)) {
-        m_new = max_nan(m, tmax);
-        alpha = (m == kNeg) ? 0.f : exp2_sfu(m - m_new);
-      }
-      // O_t holds the tiles before j at scale m.  P_t(j-1) V_{j-1} is
-      // complete: S_t(j) was issued after it and bar_s covers both.
-      if (j > 0 && __any_sync(kFullMask, alpha != 1.f)) {
+        for (int cb = 0; cb < 4; ++cb) {
+          const float* sv = (cb < 2) ? sa + 32 * cb : sb + 32 * (cb - 2);
+          uint32_t pk[16];
 #pragma unroll
-        for (int cb = 0; cb < D / 32; ++cb) {
-          float v[32];
-          tmem_ld32(to + cb * 32, v);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= alpha;
-          tmem_st32(to + cb * 32, v);
+          for (int i = 0; i < 16; ++i) {
+            float xa, xb;
+            f2_unpack(f2_fma(f2_pack(sv[2 * i], sv[2 * i + 1]), c2, nm2), xa, xb);
+            const float a = exp2_sfu(xa);
+            const float b = exp2_sfu(xb);
+            ps2[i & 3] = f2_add(ps2[i & 3], f2_pack(a, b));
+            pk[i] = pack_bf16(a, b);
+          }
+          tmem_st16u(ts + 16 * cb, pk);
         }
+        float ps[8];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) f2_unpack(ps2[c], ps[2 * c], ps[2 * c + 1]);
+        return ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+      };
+      // m is a reference value, not the running max: O and l share it, so
+      // any m gives the same softmax as long as no p overflows.  Once m is
+      // set, a tile takes p against it directly; its sum bounds every p, so
+      // a sum below 2^64 shows that nothing overflowed (and P, l and O stay
+      // far inside the fp32 / bf16 range).  Only the first visible tile, or
+      // a tile whose sum is at or above 2^64 (or NaN: a NaN or +inf score),
+      // takes the tile max -- and then the whole warp, whose TMEM accesses
+      // are warp-wide.
+      float psum = 0.f;
+      bool done = false;
+      if (__all_sync(kFullMask, m != kNeg)) {
+        psum = write_p(m);
+        done = !__any_sync(kFullMask, !(psum < 0x1p64f));
+        if (done) l += psum;
+        else tmem_wait_st();   // P is written again below
       }
-      // p = 2^(s scale log2e - m_new): one FMA (in pairs) and one SFU op per
-      // key; the row's part of l in fp32 (four chains of pairs); P as bf16
-      // pairs over S, in four chunks of 32 keys (16 columns each)
-      uint64_t ps2[4];
+      if (!done) {
+        // row max of the raw scores (eight chains), then scaled (scale_log2e > 0 keeps the order)
+        float mx[8];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) ps2[c] = 0ull;   // +0.0f in both halves
-      // a row with no visible key so far has only -inf scores: shifting by 0
-      // instead of -inf gives 2^-inf = 0 for all of them (never -inf - -inf)
-      const float m_eff = (m_new == kNeg) ? 0.f : m_new;
-      const uint64_t c2 = f2_pack(scale_log2e, scale_log2e), nm2 = f2_pack(-m_eff, -m_eff);
+        for (int c = 0; c < 8; ++c) mx[c] = max_nan(sa[c], sb[c]);
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb) {
-        const float* sv = (cb < 2) ? sa + 32 * cb : sb + 32 * (cb - 2);
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float xa, xb;
-          f2_unpack(f2_fma(f2_pack(sv[2 * i], sv[2 * i + 1]), c2, nm2), xa, xb);
-          const float a = exp2_sfu(xa);
-          const float b = exp2_sfu(xb);
-          ps2[i & 3] = f2_add(ps2[i & 3], f2_pack(a, b));
-          pk[i] = pack_bf16(a, b);
+        for (int i = 8; i < 64; ++i) mx[i & 7] = max3_nan(mx[i & 7], sa[i], sb[i]);
+        float tmax = max3_nan(max3_nan(mx[0], mx[1], mx[2]), max3_nan(mx[3], mx[4], mx[5]),
+                              max_nan(mx[6], mx[7]));
+        tmax *= scale_log2e;
+        // the reference moves to the tile max when that exceeds it by more
+        // than 2^8 (or on the first visible key), so that p <= 256 here
+        float m_new = m, alpha = 1.f;
+        if (m == kNeg || !(tmax <= m + 8.f)) {
+          m_new = max_nan(m, tmax);
+          alpha = (m == kNeg) ? 0.f : exp2_sfu(m - m_new);
         }
-        tmem_st16u(ts + 16 * cb, pk);
-      }
-      float ps[8];
+        // O_t holds the tiles before j at scale m.  P_t(j-1) V_{j-1} is
+        // complete: S_t(j) was issued after it and bar_s covers both.
+        if (j > 0 && __any_sync(kFullMask, alpha != 1.f)) {
 #pragma unroll
-      for (int c = 0; c < 4; ++c) f2_unpack(ps2[c], ps[2 * c], ps[2 * c + 1]);
+          for (int cb = 0; cb < D / 32; ++cb) {
+            float v[32];
+            tmem_ld32(to + cb * 32, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= alpha;
+            tmem_st32(to + cb * 32, v);
+          }
+        }
+        psum = write_p(m_new);
+        l = l * alpha + psum;
+        m = m_new;
+      }
       tmem_wait_st();
-      const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-      l = l * alpha + psum;
-      m = m_new;
       tc_fence_before_sync();
       mbar_arrive(&bar_p[t]);
     }

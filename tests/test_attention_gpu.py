@@ -90,6 +90,25 @@ def test_attention_scale_and_repeat(lib):
     assert float(np.max(np.abs(l1.cpu().numpy() - want_lse))) <= 1e-4
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_attention_scores_rising_across_key_tiles(lib, causal):
+    """Scores that grow by hundreds (log2 units) from one key tile to the
+    next: p against the first tile's reference would overflow, so every later
+    tile must move the reference and rescale O -- the same softmax."""
+    BH, L, S, d = 2, 256, 640, 64
+    rng = np.random.default_rng(41)
+    q = np.ones((BH, L, d), dtype=np.float32) * rng.uniform(0.5, 1.0, size=(BH, L, 1)).astype(np.float32)
+    ramp = (np.arange(S, dtype=np.float32) / S * 40.0)[None, :, None]   # up to 40 per component:
+    # the max score rises by about 90 log2 units per key tile
+    k = np.broadcast_to(ramp, (BH, S, d)) + rng.normal(0, 0.05, size=(BH, S, d)).astype(np.float32)
+    v = rng.normal(0, 1, size=(BH, S, d)).astype(np.float32)
+    qb, kb, vb = (workloads.to_bf16_bits(a) for a in (q, k, v))
+    o, lse = rrs.attention(to_dev(qb), to_dev(kb), to_dev(vb), causal=causal)
+    torch.cuda.synchronize()
+    assert rrs.device_error() == 0
+    check(o.cpu().numpy(), lse.cpu().numpy(), qb, kb, vb, causal, f"rising scores causal={causal}")
+
+
 def test_attention_rejects_bad_arguments(lib):
     q = torch.zeros(1, 128, 96, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(rrs.RRSError) as e:
