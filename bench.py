@@ -73,6 +73,9 @@ def parse_args(argv=None):
     ap.add_argument("--suite-steps", type=int, default=30)
     ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--path", default="auto", help="force a softmax path (auto, row_regs, cluster, ...)")
+    ap.add_argument("--only", default=None,
+                    help="run only the suite / variant entries named here, as workload:op, comma-separated "
+                         "(for example c3:softmax,cols_c4:softmax_cols,attn:attention_fwd)")
     ap.add_argument("--json-out", default=None, help="also write the JSON line to this file")
     return ap.parse_args(argv)
 
@@ -460,6 +463,8 @@ def run_suite(args, torch, rrs, dev, rank):
     entries = []
     for name, op in [("c1", "softmax"), ("c2", "softmax"), ("c3", "softmax"), ("c3", "row_sum"),
                      ("c4", "softmax"), ("c5", "softmax")]:
+        if not selected(args, name, op):
+            continue
         w = workloads.WORKLOADS[name]
         M, N = w.M, w.N
         x_host = workloads.matrix(w)
@@ -527,6 +532,8 @@ def run_variants(args, torch, rrs, dev, rank):
              ("cols_c2", "softmax_cols"), ("cols_c4", "softmax_cols"), ("gelu_16k", "gelu")]
     entries = []
     for name, op in cases:
+        if not selected(args, name, op):
+            continue
         w = W[name]
         M, N = w.M, w.N
         x_host = workloads.matrix(w)
@@ -611,6 +618,13 @@ def run_variants(args, torch, rrs, dev, rank):
     return entries
 
 
+def selected(args, name: str, op: str) -> bool:
+    """Whether --only lets the suite / variant entry workload:op run."""
+    if not args.only:
+        return True
+    return f"{name}:{op}" in {t.strip() for t in args.only.split(",")}
+
+
 def attention_flops(L: int, S: int, d: int, causal: bool) -> int:
     """FLOPs of one head: 2 d per (query, visible key) pair for Q K^T and as many for P V."""
     if not causal:
@@ -630,6 +644,8 @@ def run_attention(args, torch, rrs, dev, rank):
     sh = stream.cuda_stream
     entries = []
     for name, w in workloads.ATTENTION_WORKLOADS.items():
+        if not selected(args, name, "attention_fwd"):
+            continue
         q, k, v = workloads.attention_inputs(w)
         dq, dk, dv = (torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16) for a in (q, k, v))
         o = torch.empty(w.BH, w.L, w.d, dtype=torch.float32, device=dev)
