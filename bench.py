@@ -328,6 +328,18 @@ def run_ours(args):
     if rrs.device_error() != 0:
         raise SystemExit("device error word set during the timed region")
 
+    # The same call timed one at a time (an event pair around each of 50
+    # calls, after the timed region): the distribution behind the average.
+    trial_us = []
+    if rank == 0:
+        pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(50)]
+        for k, (a, b) in enumerate(pairs):
+            a.record(stream)
+            step(k)
+            b.record(stream)
+        torch.cuda.synchronize()
+        trial_us = sorted(a.elapsed_time(b) * 1e3 for a, b in pairs)
+
     ms_per_step = ms / args.steps
     rows_per_s = job_rows_per_s(M, args.steps, world, ms)
     alg_bytes = 8 * M * N
@@ -364,6 +376,10 @@ def run_ours(args):
         "clocks": sampler.summary(),
         "parity": parity,
     }
+    if trial_us:
+        out["trials"] = {"n": len(trial_us), "median_us": statistics.median(trial_us),
+                         "p95_us": trial_us[int(0.95 * (len(trial_us) - 1))],
+                         "how": "one call between a CUDA event pair, 50 calls, after the timed loop"}
 
     if not args.no_e2e:
         out["e2e"] = run_e2e(args, torch, rrs, dev, x_host, w)
