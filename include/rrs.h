@@ -101,7 +101,8 @@ typedef struct rrs_plan {
   int32_t threads;       /* threads per CTA */
   int64_t grid;          /* CTAs launched (first kernel for two-kernel paths) */
   int32_t cluster;       /* CTAs per cluster (1 = no cluster) */
-  int32_t vec;           /* float4 registers per thread per row segment (0 for streaming paths) */
+  int32_t vec;           /* float4 registers per thread per row segment (0 for streaming paths; the
+                            column band path: CTAs per SM its registers are budgeted for, 3 or 4) */
   int32_t warps_per_row; /* warps that share one row (ROW_REGS) */
   int32_t rows_per_cta;  /* rows one CTA holds at a time */
   int64_t ctas_per_row;  /* CTAs one row is split over (split paths) */

@@ -239,8 +239,18 @@ __device__ __forceinline__ float4 load_evict_last(const float4* p, uint64_t pol)
   return v;
 }
 
-template <bool LOG>
-__global__ void __launch_bounds__(kCT, 4)
+// 2^((v - m) log2 e) for a pair: v - m as v + (-m), exact like the scalar
+// subtraction, then the scalar's rounding of the product.
+__device__ __forceinline__ uint64_t exp_shifted2(float va, float vb, uint64_t neg_m2, uint64_t log2e2) {
+  float ta, tb;
+  f2_unpack(f2_mul(f2_add(f2_pack(va, vb), neg_m2), log2e2), ta, tb);
+  return f2_pack(exp2_sfu(ta), exp2_sfu(tb));
+}
+
+// MINB: CTAs per SM the registers are budgeted for (4: 64 registers; 3: 80,
+// which keeps more of the batch in flight on slices of 1024 rows).
+template <bool LOG, int MINB>
+__global__ void __launch_bounds__(kCT, MINB)
 softmax_cols_band_kernel(const float* x, float* y, int64_t M, int64_t N, int64_t ldx, int64_t ldy) {
   __shared__ MaxSum red[kGroups][kBand];
   __shared__ MaxSum part[kBand];   // this CTA's per-column (m_c, s_c), read by its peers
@@ -260,6 +270,8 @@ softmax_cols_band_kernel(const float* x, float* y, int64_t M, int64_t N, int64_t
   const bool live_col = j0 < N;   // N % 4 == 0 is not required: see the tail below
   const bool full4 = j0 + 3 < N;
   const float kNeg = neg_inf();
+  const int64_t xstep = (int64_t)kGroups * ldx, ystep = (int64_t)kGroups * ldy;   // a thread's next row
+  const uint64_t log2e2 = f2_pack(kLog2e, kLog2e);
   pdl_entry();
   const uint64_t pol = l2_evict_last_policy();
 
@@ -274,16 +286,26 @@ softmax_cols_band_kernel(const float* x, float* y, int64_t M, int64_t N, int64_t
     v.w = kNeg;
     return v;
   };
+  // a batch is whole when its last row is inside the slice and the four
+  // columns are: then it needs no per-row check
+  auto whole_batch = [&](int64_t r) { return full4 && r + (int64_t)(kBU - 1) * kGroups < r1; };
 
   // ---- pass 1: online (max, sum) per column over this thread's rows ----
   MaxSum p[4] = {{kNeg, 0.f}, {kNeg, 0.f}, {kNeg, 0.f}, {kNeg, 0.f}};
   if (live_col) {
-    for (int64_t r = r0 + g; r < r1; r += (int64_t)kBU * kGroups) {
+    const float* xr = x + (r0 + g) * ldx + j0;
+    for (int64_t r = r0 + g; r < r1; r += (int64_t)kBU * kGroups, xr += kBU * xstep) {
       float4 a[kBU];
+      if (whole_batch(r)) {
+        const float* q = xr;
 #pragma unroll
-      for (int u = 0; u < kBU; ++u) {
-        const int64_t ru = r + (int64_t)u * kGroups;
-        a[u] = (ru < r1) ? load_row(ru, true) : make_float4(kNeg, kNeg, kNeg, kNeg);
+        for (int u = 0; u < kBU; ++u, q += xstep) a[u] = load_evict_last(reinterpret_cast<const float4*>(q), pol);
+      } else {
+#pragma unroll
+        for (int u = 0; u < kBU; ++u) {
+          const int64_t ru = r + (int64_t)u * kGroups;
+          a[u] = (ru < r1) ? load_row(ru, true) : make_float4(kNeg, kNeg, kNeg, kNeg);
+        }
       }
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -291,11 +313,24 @@ softmax_cols_band_kernel(const float* x, float* y, int64_t M, int64_t N, int64_t
 #pragma unroll
         for (int u = 1; u < kBU; ++u) bm = max_nan(bm, comp(a[u], k));
         rescale_to(p[k], bm);
-        if (p[k].m != kNeg) {
-#pragma unroll
-          for (int u = 0; u < kBU; ++u) p[k].s += exp_shifted(comp(a[u], k), p[k].m);
-        }
       }
+      // a column whose max is still -inf has seen only -inf: shifting by 0
+      // gives 2^-inf = 0 for all of them, which adds nothing
+      uint64_t nm[2], s2[2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float ma = (p[2 * h].m == kNeg) ? 0.f : p[2 * h].m;
+        const float mb = (p[2 * h + 1].m == kNeg) ? 0.f : p[2 * h + 1].m;
+        nm[h] = f2_pack(-ma, -mb);
+        s2[h] = f2_pack(p[2 * h].s, p[2 * h + 1].s);
+      }
+#pragma unroll
+      for (int u = 0; u < kBU; ++u) {
+        s2[0] = f2_add(s2[0], exp_shifted2(a[u].x, a[u].y, nm[0], log2e2));
+        s2[1] = f2_add(s2[1], exp_shifted2(a[u].z, a[u].w, nm[1], log2e2));
+      }
+      f2_unpack(s2[0], p[0].s, p[1].s);
+      f2_unpack(s2[1], p[2].s, p[3].s);
     }
   }
   // ---- merge: the CTA's 32 row groups (fixed order), then the cluster's ranks ----
@@ -330,27 +365,43 @@ softmax_cols_band_kernel(const float* x, float* y, int64_t M, int64_t N, int64_t
       k4[c] = bad ? __int_as_float(0x7fc00000) : 1.0f / w.s;
     }
   }
+  const uint64_t nwm[2] = {f2_pack(-wm[0], -wm[1]), f2_pack(-wm[2], -wm[3])};
+  const uint64_t kk2[2] = {f2_pack(k4[0], k4[1]), f2_pack(k4[2], k4[3])};
+  auto normalise = [&](const float4& v) -> float4 {
+    float4 o;
+    if constexpr (LOG) {
+      o = make_float4(log_softmax_of(v.x, wm[0], k4[0]), log_softmax_of(v.y, wm[1], k4[1]),
+                      log_softmax_of(v.z, wm[2], k4[2]), log_softmax_of(v.w, wm[3], k4[3]));
+    } else {
+      f2_unpack(f2_mul(exp_shifted2(v.x, v.y, nwm[0], log2e2), kk2[0]), o.x, o.y);
+      f2_unpack(f2_mul(exp_shifted2(v.z, v.w, nwm[1], log2e2), kk2[1]), o.z, o.w);
+    }
+    return o;
+  };
   if (live_col) {
-    for (int64_t r = r0 + g; r < r1; r += (int64_t)kBU * kGroups) {
+    const float* xr = x + (r0 + g) * ldx + j0;
+    float* yr = y + (r0 + g) * ldy + j0;
+    for (int64_t r = r0 + g; r < r1; r += (int64_t)kBU * kGroups, xr += kBU * xstep, yr += kBU * ystep) {
       float4 a[kBU];
+      if (whole_batch(r)) {
+        const float* q = xr;
 #pragma unroll
-      for (int u = 0; u < kBU; ++u) {
-        const int64_t ru = r + (int64_t)u * kGroups;
-        if (ru < r1) a[u] = load_row(ru, false);
-      }
+        for (int u = 0; u < kBU; ++u, q += xstep) a[u] = load_stream(reinterpret_cast<const float4*>(q));
+        float* o = yr;
 #pragma unroll
-      for (int u = 0; u < kBU; ++u) {
-        const int64_t ru = r + (int64_t)u * kGroups;
-        if (ru >= r1) continue;
-        float4 o;
-        if constexpr (LOG) {
-          o = make_float4(log_softmax_of(a[u].x, wm[0], k4[0]), log_softmax_of(a[u].y, wm[1], k4[1]),
-                          log_softmax_of(a[u].z, wm[2], k4[2]), log_softmax_of(a[u].w, wm[3], k4[3]));
-        } else {
-          o = make_float4(exp_shifted(a[u].x, wm[0]) * k4[0], exp_shifted(a[u].y, wm[1]) * k4[1],
-                          exp_shifted(a[u].z, wm[2]) * k4[2], exp_shifted(a[u].w, wm[3]) * k4[3]);
+        for (int u = 0; u < kBU; ++u, o += ystep) store_stream(reinterpret_cast<float4*>(o), normalise(a[u]));
+      } else {
+#pragma unroll
+        for (int u = 0; u < kBU; ++u) {
+          const int64_t ru = r + (int64_t)u * kGroups;
+          if (ru < r1) a[u] = load_row(ru, false);
         }
-        store_cols<true>(y + ru * ldy, j0, N, o);
+#pragma unroll
+        for (int u = 0; u < kBU; ++u) {
+          const int64_t ru = r + (int64_t)u * kGroups;
+          if (ru >= r1) continue;
+          store_cols<true>(y + ru * ldy, j0, N, normalise(a[u]));
+        }
       }
     }
   }
@@ -539,12 +590,18 @@ cudaError_t launch_softmax_cols_cluster(const rrs_plan& p, const float* x, float
 
 cudaError_t launch_softmax_cols_band(const rrs_plan& p, const float* x, float* y, int64_t M, int64_t N,
                                      const Layout& l, cudaStream_t s) {
-  if (p.threads != kCT || p.cluster < 1 || p.cluster > 8) return cudaErrorInvalidConfiguration;
-  if (l.log_out)
-    return launch_pdl(softmax_cols_band_kernel<true>, dim3((unsigned)p.grid), dim3(kCT), 0, s, p.cluster, x, y,
-                      M, N, l.ldx, l.ldy);
-  return launch_pdl(softmax_cols_band_kernel<false>, dim3((unsigned)p.grid), dim3(kCT), 0, s, p.cluster, x, y,
-                    M, N, l.ldx, l.ldy);
+  if (p.threads != kCT || p.cluster < 1 || p.cluster > 8 || (p.vec != 3 && p.vec != 4))
+    return cudaErrorInvalidConfiguration;
+  const dim3 grid((unsigned)p.grid), block(kCT);
+  if (p.vec == 3)
+    return l.log_out ? launch_pdl(softmax_cols_band_kernel<true, 3>, grid, block, 0, s, p.cluster, x, y, M, N,
+                                  l.ldx, l.ldy)
+                     : launch_pdl(softmax_cols_band_kernel<false, 3>, grid, block, 0, s, p.cluster, x, y, M, N,
+                                  l.ldx, l.ldy);
+  return l.log_out ? launch_pdl(softmax_cols_band_kernel<true, 4>, grid, block, 0, s, p.cluster, x, y, M, N,
+                                l.ldx, l.ldy)
+                   : launch_pdl(softmax_cols_band_kernel<false, 4>, grid, block, 0, s, p.cluster, x, y, M, N,
+                                l.ldx, l.ldy);
 }
 
 cudaError_t launch_softmax_cols_two_phase(const rrs_plan& p, const float* x, float* y, int64_t M,

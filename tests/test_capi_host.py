@@ -247,6 +247,8 @@ def test_cols_planner(lib, M, N):
     assert rows <= cap or cs == 8
     assert cs == 1 or -(-M // (cs // 2)) > cap                # no smaller cluster would do
     assert p["grid"] == bands * cs
+    # registers budgeted for 3 CTAs per SM only when the grid fills three such waves
+    assert p["vec"] == (3 if p["grid"] >= 9 * 152 else 4)
     q = rrs.plan_softmax_cols(M, N, vector_ok=False)
     assert q["path_name"] == "two_phase" and q["vector_io"] == 0
 
