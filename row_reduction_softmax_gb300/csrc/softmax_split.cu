@@ -151,7 +151,12 @@ softmax_cluster_kernel(const float* x, float* y, int64_t M, int32_t N, int64_t l
     sc = cta_sum(sc, red_s);
 
     if (tid == 0) part = MaxSum{mc, sc};
-    cluster_arrive_release();  // publish `part` to the cluster
+    // publish `part` to the cluster: its writer's warp arrives with release
+    // semantics; the other warps wrote nothing the peers read, and a relaxed
+    // arrival spares them the release's memory barrier (measured on
+    // 4096 x 32768: 168.0 -> 163.2 us)
+    if (warp == 0) cluster_arrive_release();
+    else cluster_arrive_relaxed();
     cluster_wait_acquire();    // every peer's `part` is visible
 
     if (warp == 0) {
