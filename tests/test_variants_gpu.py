@@ -266,6 +266,21 @@ def test_cols_strides_in_place_and_specials(path):
     assert guards
 
 
+# Grids of at least nine CTAs per SM run the band kernel built for three CTAs
+# per SM (80 registers); check every column of such shapes, with a partial
+# last batch of rows and a ragged last band.
+@pytest.mark.parametrize("M,N", [(100, 44002), (1500, 11000)])
+def test_cols_band_three_ctas_per_sm(M, N):
+    ld = -(-N // 4) * 4
+    p = rrs.plan_softmax_cols(M, N, ld, sm_count=torch.cuda.get_device_properties(0).multi_processor_count)
+    assert p["path_name"] == "band" and p["vec"] == 3
+    x = recipe("c4", M, N)
+    for flags, log in ((0, False), (LOG, True)):
+        y, guards = run_cols(x, N, ld, ld, "auto", flags)
+        check_softmax_cols(y, x, f"cols band 3/SM {M}x{N} log={log}", log=log)
+        assert guards
+
+
 def test_cols_unaligned_takes_two_phase():
     x = recipe("c2", 77, 301)
     y, guards = run_cols(x, 301, 303, 305, "auto", x_off=1, y_off=3)
