@@ -16,7 +16,8 @@ The line carries, besides the contract's keys:
   e2e           the same metric through the public API with pinned host
                 buffers: H2D of x, the call, D2H of y, all in the timed region
   cpu_baseline  the float64 oracle timed on this host (test infrastructure,
-                timed here only as a baseline)
+                timed here only as a baseline): one process, and in
+                `all_cores` one process per host core over blocks of rows
   suite         every other row of the hot path -- the split-row softmax
                 (cluster / grid / two-phase), the single-pass softmax on the
                 masked-logit rows, the row sum -- each timed on its workload
@@ -385,6 +386,7 @@ def run_ours(args):
         out["e2e"] = run_e2e(args, torch, rrs, dev, x_host, w)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        out["cpu_baseline"]["all_cores"] = cpu_baseline_all_cores(w, args.cpu_seconds / 2)
     if not args.no_suite:
         out["suite"] = run_suite(args, torch, rrs, dev, rank)
     if not args.no_variants:
@@ -448,6 +450,45 @@ def run_e2e(args, torch, rrs, dev, x_host, w):
             "d2h_bytes_per_step": M * N * 4, "steps": steps,
             "ms_per_step": dt / steps * 1e3, "max_abs_err_readback": float(np.max(np.abs(got - want))),
             "how": "pinned host x -> device, softmax_rows, device -> pinned host y; 2 slots, 3 streams"}
+
+
+def _oracle_block_worker(task):
+    """One host process of the all-cores CPU baseline: the oracle, as it
+    stands, over its block of the workload's rows from a common start
+    instant until the budget is spent."""
+    name, r0, r1, start_at, budget_s = task
+    import oracle
+    w = workloads.WORKLOADS[name]
+    x = workloads.matrix(w, rows=range(r0, r1))
+    while time.time() < start_at:
+        time.sleep(0.001)
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.softmax_rows(x)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    return (r1 - r0) * reps, time.perf_counter() - t0
+
+
+def cpu_baseline_all_cores(w, budget_s: float, start_delay_s: float = 5.0):
+    """The oracle on every host core: the rows split into one block per
+    core, one spawned process each (no CUDA in them), timed together."""
+    import multiprocessing as mp
+    n = max(1, min(os.cpu_count() or 1, w.M))
+    bounds = [(w.M * i // n, w.M * (i + 1) // n) for i in range(n)]
+    start_at = time.time() + start_delay_s   # after every process has imported and built its block
+    tasks = [(w.name, a, b, start_at, budget_s) for a, b in bounds if b > a]
+    with mp.get_context("spawn").Pool(len(tasks)) as pool:
+        res = pool.map(_oracle_block_worker, tasks)
+    rows = sum(r for r, _ in res)
+    dt = max(t for _, t in res)
+    return {"value": rows / dt, "unit": "rows/s", "cores": len(tasks), "kind": "oracle",
+            "sample": f"{len(tasks)} processes, each the float64 numpy oracle over a block of "
+                      f"{w.M // len(tasks)}-{-(-w.M // len(tasks))} rows of the {w.M}x{w.N} matrix, "
+                      f"{dt:.1f} s together",
+            "gbs": 8 * w.N * rows / dt / 1e9}
 
 
 def cpu_baseline(w, budget_s: float):

@@ -57,3 +57,15 @@ def test_single_rank_is_unchanged():
     import bench
     assert bench.max_over_ranks(3.25, 1) == 3.25
     assert bench.job_rows_per_s(128, 10, 1, 2.0) == 128 * 10 / 0.002
+
+
+def test_cpu_baseline_all_cores_splits_the_rows():
+    """The all-cores oracle baseline: every row in exactly one block, one
+    spawned process per block, throughput over the common timed window."""
+    import bench
+    import workloads
+    w = workloads.WORKLOADS["c1"]
+    r = bench.cpu_baseline_all_cores(w, 0.2, start_delay_s=2.0)
+    assert r["kind"] == "oracle" and r["unit"] == "rows/s"
+    assert 1 <= r["cores"] <= max(1, min(os.cpu_count() or 1, w.M))
+    assert r["value"] > 0 and r["gbs"] > 0
