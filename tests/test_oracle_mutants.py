@@ -4,7 +4,7 @@ Each mutant below is the oracle with one slip a reader could make when
 restating the pages: a dropped max subtraction, the wrong axis, a missing
 exp, a flipped sign, masked lanes loaded as 0 instead of -inf, a dropped
 tail tile, a merge that forgets to rescale.  A pin suite that lets one of
-these through would not be trusted to judge the CUDA path.
+these through would not be trusted to check the CUDA path.
 """
 from __future__ import annotations
 
