@@ -59,6 +59,7 @@ constexpr int kIssuerWarp = kSoftmaxWarps;        // one thread issues the MMAs
 constexpr int kLoaderWarp = kSoftmaxWarps + 1;    // one thread issues the TMA loads
 constexpr int kAttnThreads = 32 * (kSoftmaxWarps + 2);
 constexpr int kStages = 2;                        // K and V ring depth
+constexpr int kGroupHeads = 8;                    // causal launch order: heads per group
 
 template <int D>
 struct AttnLayout {
@@ -141,9 +142,26 @@ attention_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_const
   static_assert(Lay::kQBytes >= 4 * 32 * 32 * 4, "a query tile's buffer stages its O blocks");
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.y;
-  // causal: the CTAs with the most key tiles (the last query rows) go first
-  const int qp = causal ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+  // Which (head, query pair) this CTA takes.  Blocks start roughly in order
+  // of their linear index.  Causal CTAs differ in work (query pair p sees
+  // 2p + 2 key tiles), so heads go in groups of kGroupHeads and within a
+  // group every head's heaviest pair starts first, then the next: the light
+  // pairs fill the end of the grid, and a group's K and V (a few MB) stay in
+  // the L2 while its CTAs run.  Unmasked CTAs are all alike: head-major.
+  int bh, qp;
+  if (causal) {
+    const int npairs = (int)gridDim.x;
+    const int i = (int)blockIdx.x + npairs * (int)blockIdx.y;
+    const int per_group = kGroupHeads * npairs;
+    const int g = i / per_group;
+    const int r = i - g * per_group;
+    const int gh = min(kGroupHeads, (int)gridDim.y - g * kGroupHeads);   // heads in this group
+    qp = npairs - 1 - r / gh;
+    bh = g * kGroupHeads + r % gh;
+  } else {
+    bh = (int)blockIdx.y;
+    qp = (int)blockIdx.x;
+  }
   const int q0 = qp * kQT * kBM;
   // key tiles each query tile needs: all of them, or up to the causal bound
   // (query i sees keys j <= i + S - L); the later tile never needs fewer
