@@ -125,9 +125,30 @@ def measured_bf16_peak():
         return 1900.0, "fallback"
 
 
-def source_hash() -> str:
+# The sources each timed kernel is built from, beyond the files every kernel
+# shares (the common device headers and the planner, which sets its launch).
+KERNEL_SOURCES = {
+    "softmax_row_regs_kernel": ["softmax_row.cu"],
+    "softmax_cluster_kernel": ["softmax_split.cu"],
+    "softmax_staged_grid_kernel": ["softmax_staged.cu", "sm100_async.cuh"],
+    "row_reduce_rows_kernel": ["row_sum.cu"],
+    "softmax_cols_band_kernel": ["softmax_cols.cu"],
+    "attention_fwd_kernel": ["attention.cu", "sm100_async.cuh", "sm100_tcgen05.cuh"],
+    "gelu_kernel": ["gelu.cu"],
+}
+COMMON_SOURCES = ["capi.cu", "device_common.cuh", "internal.h", "launch_util.h", "../../include/rrs.h"]
+
+
+def source_hash(kernel: str | None = None) -> str:
+    """Hash of the sources a kernel is built from (all of csrc/ for an unknown
+    or no kernel): a committed ncu figure stands only while it matches."""
+    csrc = os.path.join(ROOT, "row_reduction_softmax_gb300", "csrc")
+    if kernel in KERNEL_SOURCES:
+        paths = [os.path.join(csrc, n) for n in sorted(COMMON_SOURCES + KERNEL_SOURCES[kernel])]
+    else:
+        paths = sorted(glob.glob(os.path.join(csrc, "*")))
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "row_reduction_softmax_gb300", "csrc", "*"))):
+    for p in paths:
         with open(p, "rb") as f:
             h.update(os.path.basename(p).encode())
             h.update(f.read())
@@ -135,8 +156,8 @@ def source_hash() -> str:
 
 
 def ncu_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if it matches the current sources."""
-    want = source_hash()
+    """DRAM bytes per launch from a committed ncu summary, if it matches the kernel's current sources."""
+    want = source_hash(kernel)
     pat = re.compile(r"traffic:\s+kernel=(\S+)\s+workload=(\S+)\s+bytes_per_launch=(\d+)\s+source=(\w+)")
     for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
         with open(path) as f:
@@ -372,7 +393,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"of {peak_kind}",
                      "kernel": kernel_name, "algorithmic_bytes_per_launch": alg_bytes,
-                     "traffic": ncu_traffic(kernel_name, w.name), "source": source_hash()},
+                     "traffic": ncu_traffic(kernel_name, w.name), "source": source_hash(kernel_name)},
         "gpu_launches": args.steps * launches_per_call,
         "clocks": sampler.summary(),
         "parity": parity,
