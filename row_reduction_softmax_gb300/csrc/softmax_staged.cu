@@ -467,8 +467,10 @@ softmax_staged_grid_kernel(const float* x, float* y, int64_t M, int64_t N, int64
   if (threadIdx.x == 0) init_barriers(smem, NS, kPartialWarps);
   __syncthreads();
   pdl_launch_dependents();
-  // the first segment: into the L2 while the previous kernel drains
-  if (items > 0) prefetch_l2_range(x + row0 * ldx + seg_begin, seg_n * 4, threadIdx.x, kGThreads);
+  // the first two items' segments: into the L2 while the previous kernel
+  // drains (on 32 x 2^20: one 46.1 -> 44.5 us, two 44.4, three 44.5, four 45.0)
+  for (int64_t q = 0; q < 2 && q < items; ++q)
+    prefetch_l2_range(x + (row0 + q * R) * ldx + seg_begin, seg_n * 4, threadIdx.x, kGThreads);
   pdl_wait();
 
   if (warp == kGProducerWarp) {
