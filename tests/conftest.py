@@ -13,8 +13,16 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+def pytest_addoption(parser):
+    parser.addoption("--cuda-blocking", action="store_true",
+                     help="debug mode: every launch synchronous (CUDA_LAUNCH_BLOCKING=1), so a "
+                          "failing kernel is reported at its own launch")
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (runs the kernels through the C ABI)")
+    if config.getoption("--cuda-blocking"):
+        os.environ["CUDA_LAUNCH_BLOCKING"] = "1"   # before the first CUDA call of the session
 
 
 def _cuda_available() -> bool:
