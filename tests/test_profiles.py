@@ -41,3 +41,24 @@ def test_each_element_of_x_is_read_once(name, x_bytes, slack):
     assert x_bytes * (1 - 0.01) <= got <= x_bytes * (1 + slack), \
         f"{name}: {got / 1e6:.2f} MB read from DRAM for {x_bytes / 1e6:.2f} MB of x"
 
+
+
+def test_every_profiled_kernel_has_its_sources_listed():
+    """Each kernel with a committed traffic figure is keyed to its own
+    sources (the bench falls back to hashing all of csrc/ otherwise, which
+    would drop every figure on any change), and those files exist."""
+    import bench
+    csrc = os.path.join(ROOT, "row_reduction_softmax_gb300", "csrc")
+    for names in bench.KERNEL_SOURCES.values():
+        for n in names + bench.COMMON_SOURCES:
+            assert os.path.exists(os.path.join(csrc, n)), n
+    pat = re.compile(r"traffic:\s+kernel=(\S+)\s+workload=(\S+)\s+bytes_per_launch=(\d+)\s+source=(\w+)")
+    seen = 0
+    for name in sorted(os.listdir(os.path.join(ROOT, "profiles"))):
+        with open(os.path.join(ROOT, "profiles", name)) as f:
+            for line in f:
+                m = pat.search(line)
+                if m:
+                    seen += 1
+                    assert m.group(1) in bench.KERNEL_SOURCES, f"{name}: {m.group(1)} has no source list"
+    assert seen >= 6
