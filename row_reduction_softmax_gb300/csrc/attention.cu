@@ -17,12 +17,12 @@
 //     order P_0(j) V_j, S_0(j+1) = Q_0 K_{j+1}^T, P_1(j) V_j, S_1(j+1), so
 //     the tensor cores work on one query tile while the other's softmax runs;
 //   warps 0..3 and 4..7: the softmax warpgroup of query tile 0 and 1, one
-//     thread per query row: it reads its 128 scores from TMEM, updates the
-//     row max, writes p = 2^(s log2e scale - m) as bf16 pairs over the first
-//     half of the scores' TMEM columns (the A operand of P V, read from TMEM),
-//     keeps the row sum in fp32, and rescales its row of O, which
-//     accumulates in TMEM across key tiles (O = alpha O + P_j V_j), when the
-//     row max rises.
+//     thread per query row: it reads its 128 scores from TMEM, writes
+//     p = 2^(s log2e scale - m) against the row's reference m as bf16 pairs
+//     over the first half of the scores' TMEM columns (the A operand of P V,
+//     read from TMEM), keeps the row sum in fp32, and rescales its row of O,
+//     which accumulates in TMEM across key tiles (O = alpha O + P_j V_j),
+//     when m moves (only when the tile sum shows that m can no longer hold).
 // TMEM per query tile: S (128 fp32 columns, P over the first 64) and O (D
 // columns): 512 columns for the two tiles.  Q and K are K-major operands,
 // V [keys][d] is the MN-major B operand of P V (no transposed copy); all
