@@ -226,8 +226,10 @@ RRS_API int attention_fwd(const void* q, const void* k, const void* v, float* o,
  * device memory inside the library (131072 pairs), which every GPU that
  * loads the library holds until the process exits.
  *
- * Same arguments, layout, results and error codes as softmax_rows, plus
- * RRS_ERR_INVALID_ARG when M > 131072 (each row needs a slot).  Rows are cut
+ * Same arguments, layout, results and error codes as softmax_rows (y == x
+ * computes in place, any other overlap is RRS_ERR_ALIAS; rrs_last_error()
+ * holds the message of a refused call), plus RRS_ERR_INVALID_ARG when
+ * M > 131072 (each row needs a slot).  Rows are cut
  * into at most 131072 / M chunks, so few-row calls keep their parallelism.
  * The first call on a device looks up the array's device address with that
  * device current; make that first call before any stream capture.  All calls

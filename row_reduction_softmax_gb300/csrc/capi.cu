@@ -23,13 +23,15 @@
 #include "rrs.h"
 
 namespace rrs {
-namespace {
 
+// ------------------------------------------- checks shared by entry points ---
+// (declared in internal.h: every entry point reports through the same
+// per-thread message and applies the same shape, alias and pointer rules)
+namespace {
 thread_local std::string g_last_error;
-std::atomic<int> g_force_softmax{RRS_PATH_AUTO};
-std::atomic<int> g_force_sum{RRS_SUM_AUTO};
-std::atomic<int> g_force_cols{RRS_COLS_AUTO};
-std::atomic<int> g_fault{0};
+}  // namespace
+
+void clear_last_error() { g_last_error.clear(); }
 
 int fail(int status, const std::string& msg) {
   g_last_error = msg;
@@ -40,6 +42,45 @@ int fail_cuda(cudaError_t e, const char* what) {
   g_last_error = std::string(what) + ": " + cudaGetErrorString(e);
   return RRS_ERR_CUDA;
 }
+
+// A pointer the current device can use as global memory.
+int check_device_pointer(const void* p, int dev, const char* name) {
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(RRS_ERR_INVALID_ARG, std::string(name) + " is not a CUDA pointer");
+  }
+  if (a.type == cudaMemoryTypeManaged) return RRS_OK;
+  if (a.type == cudaMemoryTypeDevice && a.device == dev) return RRS_OK;
+  if (a.type == cudaMemoryTypeDevice)
+    return fail(RRS_ERR_INVALID_ARG, std::string(name) + " lives on another device");
+  return fail(RRS_ERR_INVALID_ARG, std::string(name) + " is not device memory");
+}
+
+// Shape checks shared by the row operations; sets *extent (elements spanned
+// by x) when M > 0.
+int check_shape(int64_t M, int64_t N, int64_t ld, int64_t* extent) {
+  if (M < 0 || N < 0) return fail(RRS_ERR_INVALID_ARG, "M and N must be >= 0");
+  if (ld < 1 || ld < N) return fail(RRS_ERR_INVALID_ARG, "ld must be >= max(N, 1)");
+  *extent = 0;
+  if (M == 0 || N == 0) return RRS_OK;
+  if (M - 1 > (INT64_MAX / 8 - N) / ld) return fail(RRS_ERR_INVALID_ARG, "extent overflows");
+  *extent = (M - 1) * ld + N;
+  return RRS_OK;
+}
+
+bool overlaps(const void* a, int64_t a_bytes, const void* b, int64_t b_bytes) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + (uintptr_t)b_bytes && b0 < a0 + (uintptr_t)a_bytes;
+}
+
+namespace {
+
+std::atomic<int> g_force_softmax{RRS_PATH_AUTO};
+std::atomic<int> g_force_sum{RRS_SUM_AUTO};
+std::atomic<int> g_force_cols{RRS_COLS_AUTO};
+std::atomic<int> g_fault{0};
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
@@ -117,39 +158,6 @@ int get_workspace(int dev, cudaStream_t s, int kind, size_t bytes, void** ptr,
   }
   *ptr = w.ptr;
   return RRS_OK;
-}
-
-// ----------------------------------------------------------------- checks ---
-// A pointer the current device can use as global memory.
-int check_device_pointer(const void* p, int dev, const char* name) {
-  cudaPointerAttributes a;
-  cudaError_t e = cudaPointerGetAttributes(&a, p);
-  if (e != cudaSuccess) {
-    (void)cudaGetLastError();
-    return fail(RRS_ERR_INVALID_ARG, std::string(name) + " is not a CUDA pointer");
-  }
-  if (a.type == cudaMemoryTypeManaged) return RRS_OK;
-  if (a.type == cudaMemoryTypeDevice && a.device == dev) return RRS_OK;
-  if (a.type == cudaMemoryTypeDevice)
-    return fail(RRS_ERR_INVALID_ARG, std::string(name) + " lives on another device");
-  return fail(RRS_ERR_INVALID_ARG, std::string(name) + " is not device memory");
-}
-
-// Shape checks shared by both operations; sets *extent (elements spanned by
-// x) when M > 0.
-int check_shape(int64_t M, int64_t N, int64_t ld, int64_t* extent) {
-  if (M < 0 || N < 0) return fail(RRS_ERR_INVALID_ARG, "M and N must be >= 0");
-  if (ld < 1 || ld < N) return fail(RRS_ERR_INVALID_ARG, "ld must be >= max(N, 1)");
-  *extent = 0;
-  if (M == 0 || N == 0) return RRS_OK;
-  if (M - 1 > (INT64_MAX / 8 - N) / ld) return fail(RRS_ERR_INVALID_ARG, "extent overflows");
-  *extent = (M - 1) * ld + N;
-  return RRS_OK;
-}
-
-bool overlaps(const void* a, int64_t a_bytes, const void* b, int64_t b_bytes) {
-  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
-  return a0 < b0 + (uintptr_t)b_bytes && b0 < a0 + (uintptr_t)a_bytes;
 }
 
 // ---------------------------------------------------------------- planner ---
@@ -587,7 +595,7 @@ RRS_API const char* rrs_status_string(int status) {
   }
 }
 
-RRS_API const char* rrs_last_error(void) { return g_last_error.c_str(); }
+RRS_API const char* rrs_last_error(void) { return rrs::g_last_error.c_str(); }
 
 RRS_API int rrs_force_path(int softmax_path, int sum_path) {
   if (softmax_path < RRS_PATH_AUTO || softmax_path >= RRS_PATH_COUNT) return RRS_ERR_INVALID_ARG;
@@ -656,7 +664,7 @@ RRS_API int64_t rrs_waves(int64_t blocks, int64_t slots, int64_t* last_wave, int
 
 RRS_API int softmax_rows_ex(const float* x, int64_t ldx, float* y, int64_t ldy, int64_t M,
                             int64_t N, int flags, void* stream) {
-  g_last_error.clear();
+  clear_last_error();
   if (flags & ~RRS_LOG_SOFTMAX) return fail(RRS_ERR_INVALID_ARG, "unknown flag bits");
   int64_t xext = 0, yext = 0;
   int st = check_shape(M, N, ldx, &xext);
@@ -726,7 +734,7 @@ RRS_API int softmax_rows_ex(const float* x, int64_t ldx, float* y, int64_t ldy, 
 
 RRS_API int softmax_cols(const float* x, int64_t ldx, float* y, int64_t ldy, int64_t M, int64_t N,
                          int flags, void* stream) {
-  g_last_error.clear();
+  clear_last_error();
   if (flags & ~RRS_LOG_SOFTMAX) return fail(RRS_ERR_INVALID_ARG, "unknown flag bits");
   int64_t xext = 0, yext = 0;
   int st = check_shape(M, N, ldx, &xext);
@@ -788,7 +796,7 @@ namespace {
 // row_sum / row_max / row_mean: one planner and one kernel family (op).
 int row_reduce_impl(int op, const char* name, const float* x, float* out, int64_t M, int64_t N,
                     int64_t ld, void* stream) {
-  g_last_error.clear();
+  clear_last_error();
   int64_t extent = 0;
   int st = check_shape(M, N, ld, &extent);
   if (st != RRS_OK) return st;
@@ -855,7 +863,7 @@ RRS_API int row_mean(const float* x, float* out, int64_t M, int64_t N, int64_t l
 }
 
 RRS_API int gelu(const float* x, float* y, int64_t n, void* stream) {
-  g_last_error.clear();
+  clear_last_error();
   if (n < 0) return fail(RRS_ERR_INVALID_ARG, "n must be >= 0");
   if (n == 0) return RRS_OK;
   if (n > INT64_MAX / 8) return fail(RRS_ERR_INVALID_ARG, "extent overflows");
@@ -880,7 +888,7 @@ RRS_API int gelu(const float* x, float* y, int64_t n, void* stream) {
 RRS_API int attention_fwd(const void* q, const void* k, const void* v, float* o, float* lse,
                           int64_t BH, int64_t L, int64_t S, int64_t d, int causal, float scale,
                           void* stream) {
-  g_last_error.clear();
+  clear_last_error();
   if (BH < 0 || L < 0 || S < 0) return fail(RRS_ERR_INVALID_ARG, "BH, L and S must be >= 0");
   if (d != 64 && d != 128) return fail(RRS_ERR_INVALID_ARG, "head dimension must be 64 or 128");
   if (BH == 0 || L == 0) return RRS_OK;

@@ -5,9 +5,24 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <string>
+
 #include "rrs.h"
 
 namespace rrs {
+
+// ---- argument checks and error reporting shared by every entry point
+// (capi.cu).  fail* record the calling thread's message for rrs_last_error
+// and return the status; every entry point starts with clear_last_error().
+void clear_last_error();
+int fail(int status, const std::string& msg);
+int fail_cuda(cudaError_t e, const char* what);
+// RRS_OK if p is device memory of device `dev` or managed memory.
+int check_device_pointer(const void* p, int dev, const char* name);
+// M, N >= 0, ld >= max(N, 1), no overflow; *extent = elements spanned by a
+// matrix of M rows of N entries at stride ld (0 when M or N is 0).
+int check_shape(int64_t M, int64_t N, int64_t ld, int64_t* extent);
+bool overlaps(const void* a, int64_t a_bytes, const void* b, int64_t b_bytes);
 
 // Per-device facts the planner needs, queried once per device.
 struct DeviceInfo {

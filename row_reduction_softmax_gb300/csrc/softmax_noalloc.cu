@@ -35,6 +35,8 @@ namespace {
 // Capacity: (max, sum) pairs, one per (row, chunk) of a call.  8 bytes each,
 // so 1 MiB of device memory per GPU.
 constexpr int64_t kNoAllocPairs = 131072;
+// Smallest chunk a row is cut into before the SM count asks for more.
+constexpr int64_t kNoAllocMinChunk = 4096;
 
 static __device__ __align__(256) MaxSum g_noalloc_partials[kNoAllocPairs];
 
@@ -57,9 +59,10 @@ int noalloc_device(int dev, NoAllocDevice* out) {
   }
   NoAllocDevice d;
   cudaError_t e = cudaGetSymbolAddress(&d.scratch, g_noalloc_partials);
-  if (e != cudaSuccess || d.scratch == nullptr) return RRS_ERR_CUDA;
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(noalloc scratch)");
+  if (d.scratch == nullptr) return fail(RRS_ERR_CUDA, "noalloc scratch has no device address");
   e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return RRS_ERR_CUDA;
+  if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
   g_noalloc_devices[dev] = d;
   *out = d;
   return RRS_OK;
@@ -74,39 +77,37 @@ using namespace rrs;
 
 extern "C" RRS_API int softmax_rows_noalloc(const float* x, float* y, int64_t M, int64_t N,
                                             int64_t ld, void* stream) {
-  if (M < 0 || N < 0) return RRS_ERR_INVALID_ARG;
-  if (ld < 1 || ld < N) return RRS_ERR_INVALID_ARG;
+  // The same checks and messages as softmax_rows (shared with capi.cu).
+  clear_last_error();
+  int64_t extent = 0;
+  int st = check_shape(M, N, ld, &extent);
+  if (st != RRS_OK) return st;
   if (M == 0 || N == 0) return RRS_OK;
-  if (!x || !y) return RRS_ERR_INVALID_ARG;
+  if (!x || !y) return fail(RRS_ERR_INVALID_ARG, "null pointer");
   if (reinterpret_cast<uintptr_t>(x) % 4 || reinterpret_cast<uintptr_t>(y) % 4)
-    return RRS_ERR_INVALID_ARG;
-  if (M - 1 > (INT64_MAX / 8 - N) / ld) return RRS_ERR_INVALID_ARG;
+    return fail(RRS_ERR_INVALID_ARG, "pointers must be 4-byte aligned");
   // Every row needs at least one (max, sum) slot of the fixed scratch.
-  if (M > kNoAllocPairs) return RRS_ERR_INVALID_ARG;
-  const int64_t bytes = ((M - 1) * ld + N) * 4;
+  if (M > kNoAllocPairs)
+    return fail(RRS_ERR_INVALID_ARG, "softmax_rows_noalloc takes at most 131072 rows");
+  // In place (y == x, one shared stride) is allowed, as in softmax_rows: the
+  // finalize kernel reads each element before the same thread writes it.
+  // Any other overlap is refused.
+  const bool in_place = static_cast<const void*>(x) == static_cast<const void*>(y);
+  if (!in_place && overlaps(x, extent * 4, y, extent * 4)) return fail(RRS_ERR_ALIAS, "x and y overlap");
   const uintptr_t xa = reinterpret_cast<uintptr_t>(x), ya = reinterpret_cast<uintptr_t>(y);
-  if (xa < ya + (uintptr_t)bytes && ya < xa + (uintptr_t)bytes)
-    return RRS_ERR_ALIAS;
 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return RRS_ERR_CUDA;
-  for (const void* p : {static_cast<const void*>(x), static_cast<const void*>(y)}) {
-    cudaPointerAttributes a;
-    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return RRS_ERR_INVALID_ARG;
-    }
-    const bool ok = a.type == cudaMemoryTypeManaged || (a.type == cudaMemoryTypeDevice && a.device == dev);
-    if (!ok) return RRS_ERR_INVALID_ARG;
-  }
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  if ((st = check_device_pointer(x, dev, "x")) != RRS_OK) return st;
+  if ((st = check_device_pointer(y, dev, "y")) != RRS_OK) return st;
   NoAllocDevice d;
-  int st = noalloc_device(dev, &d);
-  if (st != RRS_OK) return st;
+  if ((st = noalloc_device(dev, &d)) != RRS_OK) return st;
 
-  // Chunks per row: enough CTAs to fill the GPU, chunks of at least 1024
-  // columns, and never more (row, chunk) pairs than the scratch holds.
-  int64_t C = std::max<int64_t>(1, std::min(cdiv(4 * (int64_t)d.sm_count, M), cdiv(N, 4096)));
+  // Chunks per row: enough CTAs to fill the GPU (about 4 per SM), chunks of
+  // about kNoAllocMinChunk columns or more (rounded up to kChunkAlign), and
+  // never more (row, chunk) pairs than the scratch holds.
+  int64_t C = std::max<int64_t>(1, std::min(cdiv(4 * (int64_t)d.sm_count, M), cdiv(N, kNoAllocMinChunk)));
   C = std::min<int64_t>(C, kNoAllocPairs / M);
   const int64_t chunk = cdiv(cdiv(N, C), kChunkAlign) * kChunkAlign;
   C = cdiv(N, chunk);
@@ -132,6 +133,6 @@ extern "C" RRS_API int softmax_rows_noalloc(const float* x, float* y, int64_t M,
   l.ldx = ld;
   l.ldy = ld;
   e = launch_softmax_two_phase(plan, x, y, M, N, l, d.scratch, static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return RRS_ERR_CUDA;
+  if (e != cudaSuccess) return fail_cuda(e, "softmax_rows_noalloc launch");
   return RRS_OK;
 }

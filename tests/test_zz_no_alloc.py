@@ -11,49 +11,116 @@ last on purpose.
 """
 from __future__ import annotations
 
+import ctypes
+
 import numpy as np
 import pytest
 
 import row_reduction_softmax_gb300 as rrs
 import workloads
-from gpu_helpers import ABS_TOL, ROW_SUM_TOL, check_softmax
+from gpu_helpers import ABS_TOL, ROW_SUM_TOL, Guarded, check_softmax
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-INVALID = 1
+OK, INVALID, ALIAS = 0, 1, 2
 
 
-def _call_noalloc(lib, x, y, M, N, ld):
-    return lib.softmax_rows_noalloc(x.data_ptr(), y.data_ptr(), M, N, ld,
-                                    torch.cuda.current_stream().cuda_stream)
+def _stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _call_noalloc(lib, xp, yp, M, N, ld):
+    return lib.softmax_rows_noalloc(xp, yp, M, N, ld, _stream())
+
+
+def _twice_against_softmax_rows(lib, x_host, ld, offset=0):
+    """Two calls in a row (the second on a different input), each compared with
+    softmax_rows on the same input and with the oracle on a few rows; the gap
+    [N, ld) and the guard floats around y stay untouched."""
+    M, N = x_host.shape
+    inputs = [x_host, np.flip(x_host, axis=0).copy() * np.float32(0.5)]
+    for k, xh in enumerate(inputs):
+        xg, yg, rg = Guarded(M, ld, offset), Guarded(M, ld, offset), Guarded(M, ld, offset)
+        xg.mat[:, :N].copy_(torch.from_numpy(xh))
+        assert lib.softmax_rows(xg.ptr, rg.ptr, M, N, ld, _stream()) == OK
+        assert _call_noalloc(lib, xg.ptr, yg.ptr, M, N, ld) == OK
+        torch.cuda.synchronize()
+        y, ref = yg.mat[:, :N].double(), rg.mat[:, :N].double()
+        diff = (y - ref).abs().max().item()
+        assert diff <= ABS_TOL, (k, diff)
+        assert (y.sum(dim=1) - 1.0).abs().max().item() <= ROW_SUM_TOL
+        assert yg.untouched_outside(N)
+        rows = sorted({0, M // 2, M - 1})
+        check_softmax(yg.mat[rows, :N].cpu().numpy(), xh[rows], f"noalloc {M}x{N} ld {ld} call {k}")
 
 
 @pytest.mark.parametrize("name,M,N", [("c5", 32, 1 << 20), ("c4", 300, 4096), ("c3", 7, 40003)])
 def test_noalloc_matches_softmax_rows_twice(lib, name, M, N):
     rrs.force_path("auto", "auto")
-    w = workloads.WORKLOADS[name].with_shape(M, N)
-    inputs = [workloads.matrix(w)]
-    inputs.append(np.flip(inputs[0], axis=0).copy() * np.float32(0.5))   # a different second input
-    for x_host in inputs:                                                  # two calls in a row
-        x = torch.from_numpy(x_host).cuda()
-        y_ref = torch.empty_like(x)
+    _twice_against_softmax_rows(lib, workloads.matrix(workloads.WORKLOADS[name].with_shape(M, N)), N)
+
+
+def test_noalloc_strided_scalar_path(lib):
+    """ld = N + 3: rows not 16-byte aligned, so the scalar loads; the gap is never written."""
+    rrs.force_path("auto", "auto")
+    M, N = 37, 9000
+    _twice_against_softmax_rows(lib, workloads.matrix(workloads.WORKLOADS["c2"].with_shape(M, N)), N + 3)
+
+
+def test_noalloc_at_the_row_limit(lib):
+    """M = 131072 rows, the most the scratch holds (one (max, sum) pair per row)."""
+    rrs.force_path("auto", "auto")
+    M, N = 131072, 2048
+    w = workloads.WORKLOADS["c2"].with_shape(M, N)
+    rows = [0, 1, 4097, M // 2, M - 2, M - 1]
+    x_rows = workloads.matrix(w, rows=rows)
+    x = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    x.normal_(0.0, 2.0, generator=torch.Generator(device="cuda").manual_seed(131072))
+    x[rows] = torch.from_numpy(x_rows).cuda()
+    ref = torch.empty_like(x)
+    for k in range(2):
         y = torch.full_like(x, float("nan"))
-        lib_status = lib.softmax_rows(x.data_ptr(), y_ref.data_ptr(), M, N, N,
-                                      torch.cuda.current_stream().cuda_stream)
-        assert lib_status == 0
-        assert _call_noalloc(lib, x, y, M, N, N) == 0
+        assert lib.softmax_rows(x.data_ptr(), ref.data_ptr(), M, N, N, _stream()) == OK
+        assert _call_noalloc(lib, x.data_ptr(), y.data_ptr(), M, N, N) == OK
         torch.cuda.synchronize()
-        diff = (y.double() - y_ref.double()).abs().max().item()
-        assert diff <= ABS_TOL, diff
+        assert (y.double() - ref.double()).abs().max().item() <= ABS_TOL
         assert (y.double().sum(dim=1) - 1.0).abs().max().item() <= ROW_SUM_TOL
+        check_softmax(y[rows].cpu().numpy(), x_rows, f"noalloc {M} x {N} call {k}")
+        x.mul_(0.5)                        # the second call sees another input
+        x_rows = x_rows * np.float32(0.5)
+        del y
+    del x, ref
+    torch.cuda.empty_cache()
+
+
+def test_noalloc_in_place(lib):
+    """y == x with one stride computes in place, the same result as softmax_rows out of place."""
+    rrs.force_path("auto", "auto")
+    for M, N in [(32, 1 << 20), (300, 4096)]:
+        x_host = workloads.matrix(workloads.WORKLOADS["c4"].with_shape(M, N))
+        x = torch.from_numpy(x_host).cuda()
+        ref = torch.empty_like(x)
+        assert lib.softmax_rows(x.data_ptr(), ref.data_ptr(), M, N, N, _stream()) == OK
+        assert _call_noalloc(lib, x.data_ptr(), x.data_ptr(), M, N, N) == OK
+        torch.cuda.synchronize()
+        assert (x.double() - ref.double()).abs().max().item() <= ABS_TOL
         rows = [0, M // 2, M - 1]
-        check_softmax(y[rows].cpu().numpy(), x_host[rows], f"noalloc {name}")
+        check_softmax(x[rows].cpu().numpy(), x_host[rows], f"noalloc in place {M}x{N}")
 
 
-def test_noalloc_rejects_too_many_rows_without_launching(lib):
+def test_noalloc_refusals_leave_y_untouched(lib):
+    """Too many rows and partial overlaps are refused before anything is enqueued:
+    y keeps its sentinel and rrs_last_error says why."""
+    lib.rrs_last_error.restype = ctypes.c_char_p
     x = torch.zeros(131073, 4, device="cuda")
-    y = torch.empty_like(x)
-    assert _call_noalloc(lib, x, y, 131073, 4, 4) == INVALID
-    assert _call_noalloc(lib, x, y, 0, 4, 4) == 0                       # nothing to do
-    assert _call_noalloc(lib, x, x, 4, 4, 4) == 2                       # x and y overlap
+    y = Guarded(131073, 4)
+    assert _call_noalloc(lib, x.data_ptr(), y.ptr, 131073, 4, 4) == INVALID
+    assert b"131072" in lib.rrs_last_error()
+    assert _call_noalloc(lib, x.data_ptr(), y.ptr, 0, 4, 4) == OK            # nothing to do
+    assert lib.rrs_last_error() == b""
+    assert _call_noalloc(lib, x.data_ptr(), x.data_ptr() + 16, 4, 4, 4) == ALIAS   # y = x + 1 row
+    assert b"overlap" in lib.rrs_last_error()
+    assert _call_noalloc(lib, x.data_ptr(), x.data_ptr(), 4, 4, 3) == INVALID     # ld < N
+    torch.cuda.synchronize()
+    assert y.untouched_outside(0)
