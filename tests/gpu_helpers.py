@@ -180,3 +180,55 @@ def check_gelu(got: np.ndarray, x: np.ndarray, where: str = "") -> float:
                  + 1e-36)
     assert np.all(err <= bound), f"{where}: gelu err {float(np.max(err)):.3e}"
     return float(np.max(err)) if err.size else 0.0
+
+
+def attention_reference(qf, kf, vf, causal: bool, scale=None):
+    """The oracle's (O, LSE) and, per element, the bound |O - O_oracle| may reach.
+
+    O = P V / l with l = sum_j p_j.  Per output element (i, c), with
+    A_ic = sum_j P_ij |v_jc| (the oracle's attention with |V| for V, taken in
+    the same call as O by stacking V and |V| side by side):
+      * p_j enters the second product rounded to bf16, relative error <= 2^-9
+        each, while l sums p in fp32: at most 2^-9 A_ic;
+      * a score is an fp32 sum of d exact bf16 products: absolute error <=
+        d 2^-24 scale sum_k |q_ik k_jk| =: e_i (bounded by the componentwise
+        max of |k| over keys), a relative error of about e_i in p_j, which
+        moves O by at most e_i (A_ic + |O_ic|);
+      * the fp32 sums over S keys of p v and of p: at most S 2^-24 (A_ic + |O_ic|);
+      * 1e-6 for results near zero.
+    A wrong V tile or a misplaced key block moves O by the weight of whole
+    tiles, far above this bound."""
+    d = qf.shape[-1]
+    S = kf.shape[-2]
+    sc = (1.0 / np.sqrt(d)) if not scale else scale
+    both, lse = oracle.attention(qf, kf, np.concatenate([vf, np.abs(vf)], axis=-1), causal=causal,
+                                 scale=scale or None)
+    o, a = both[..., :d], both[..., d:]
+    kmax = np.max(np.abs(kf), axis=-2)                               # (..., d)
+    e = d * 2.0 ** -24 * sc * np.einsum("...ik,...k->...i", np.abs(qf), kmax)[..., None]
+    with np.errstate(invalid="ignore"):
+        bound = 2.0 ** -9 * a + (e + S * 2.0 ** -24) * (a + np.abs(o)) + 1e-6
+    return o, lse, bound
+
+
+def row_blocks(M: int, N: int, elements: int = 1 << 24):
+    """Consecutive row ranges [r0, r1) of about ``elements`` entries each."""
+    step = max(1, elements // max(N, 1))
+    for r0 in range(0, M, step):
+        yield r0, min(M, r0 + step)
+
+
+def check_every_row(check, y_dev, x_host: np.ndarray, where: str = "") -> dict:
+    """Apply a row check (check_softmax, check_log_softmax, ...) to every row of
+    a device result against the oracle, one block of rows at a time; returns
+    the largest of each error the check reports."""
+    M, N = x_host.shape[0], x_host.shape[1]
+    worst: dict = {}
+    for r0, r1 in row_blocks(M, N):
+        res = check(y_dev[r0:r1].cpu().numpy(), x_host[r0:r1], f"{where} rows {r0}-{r1}")
+        if isinstance(res, dict):
+            for k, v in res.items():
+                worst[k] = max(worst.get(k, 0.0), v)
+        elif res is not None:
+            worst["max"] = max(worst.get("max", 0.0), float(res))
+    return worst
