@@ -94,15 +94,12 @@ def test_tensor_api():
 
 
 def test_full_size_workload():
+    """Every row of the 4096 x 32768 row sum against the oracle's float64 sum."""
     w = workloads.WORKLOADS["c3"]
     x_host = workloads.matrix(w)
     x = torch.from_numpy(x_host).cuda()
     out = rrs.row_sum(x)
     torch.cuda.synchronize()
-    rng = np.random.default_rng(7)
-    rows = sorted({0, w.M - 1, *rng.choice(w.M, size=64, replace=False).tolist()})
-    check_row_sum(out.cpu().numpy()[rows], x_host[rows], "c3 sampled rows")
-    # every row: against a float64 sum on the device, same normwise bound
-    ref = x.double().sum(dim=1)
-    scale = x.double().abs().sum(dim=1)
-    assert bool(((out.double() - ref).abs() <= 1e-5 * scale).all())
+    check_row_sum(out.cpu().numpy(), x_host, "c3 every row")
+    del x
+    torch.cuda.empty_cache()

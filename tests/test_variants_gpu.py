@@ -19,7 +19,7 @@ import pytest
 
 import row_reduction_softmax_gb300 as rrs
 import workloads
-from gpu_helpers import (Guarded, check_gelu, check_log_softmax, check_row_max, check_row_mean,
+from gpu_helpers import (Guarded, check_every_row, check_gelu, check_log_softmax, check_row_max, check_row_mean,
                          check_softmax, check_softmax_cols)
 from test_softmax_gpu import PATHS, supports
 
@@ -309,10 +309,7 @@ def test_full_size_log_softmax(name):
     y = rrs.log_softmax_rows(x)
     torch.cuda.synchronize()
     assert rrs.device_error() == 0
-    rows = sampled(w.M, w.seed)
-    check_log_softmax(y[rows].cpu().numpy(), x_host[rows], f"{name} log sampled rows")
-    lse = torch.logsumexp(y.double(), dim=1)          # every row: log sum exp(log y) == 0
-    assert float(lse.abs().max()) <= 1e-5
+    check_every_row(check_log_softmax, y, x_host, f"{name} log")
     del x, y
     torch.cuda.empty_cache()
 
@@ -323,12 +320,10 @@ def test_full_size_columns(M, N, name):
     x = torch.from_numpy(x_host).cuda()
     y = rrs.softmax_cols(x)
     torch.cuda.synchronize()
-    cols = sampled(N, M)
-    got = y[:, cols].cpu().numpy()
-    want_in = x_host[:, cols]
-    check_softmax_cols(got, want_in, f"columns {M}x{N} sampled")
-    sums = y.double().sum(dim=0)
-    assert float((sums - 1.0).abs().max()) <= 1e-5
+    step = max(1, (1 << 23) // M)             # every column, a block of columns at a time
+    for c0 in range(0, N, step):
+        c1 = min(N, c0 + step)
+        check_softmax_cols(y[:, c0:c1].cpu().numpy(), x_host[:, c0:c1], f"columns {M}x{N}, {c0}-{c1}")
     if name == "c4":
         assert bool((y[torch.isneginf(x)] == 0).all())
     del x, y
@@ -341,10 +336,8 @@ def test_full_size_row_max_and_mean():
     x = torch.from_numpy(x_host).cuda()
     mx = rrs.row_max(x).cpu().numpy()
     mean = rrs.row_mean(x).cpu().numpy()
-    rows = sampled(w.M, w.seed)
-    check_row_max(mx[rows], x_host[rows], "c3 max sampled")
-    check_row_mean(mean[rows], x_host[rows], "c3 mean sampled")
-    assert np.array_equal(mx, x.max(dim=1).values.cpu().numpy())   # exact on every row
+    check_row_max(mx, x_host, "c3 max, every row")                    # bit-exact
+    check_row_mean(mean, x_host, "c3 mean, every row")
     del x
     torch.cuda.empty_cache()
 
