@@ -188,8 +188,9 @@ def attention_reference(qf, kf, vf, causal: bool, scale=None):
     O = P V / l with l = sum_j p_j.  Per output element (i, c), with
     A_ic = sum_j P_ij |v_jc| (the oracle's attention with |V| for V, taken in
     the same call as O by stacking V and |V| side by side):
-      * p_j enters the second product rounded to bf16, relative error <= 2^-9
-        each, while l sums p in fp32: at most 2^-9 A_ic;
+      * p_j enters the second product rounded to bf16 (8 significant bits,
+        so a relative error <= 2^-8 each), while l sums p in fp32: at most
+        2^-8 A_ic;
       * a score is an fp32 sum of d exact bf16 products: absolute error <=
         d 2^-24 scale sum_k |q_ik k_jk| =: e_i (bounded by the componentwise
         max of |k| over keys), a relative error of about e_i in p_j, which
@@ -207,7 +208,7 @@ def attention_reference(qf, kf, vf, causal: bool, scale=None):
     kmax = np.max(np.abs(kf), axis=-2)                               # (..., d)
     e = d * 2.0 ** -24 * sc * np.einsum("...ik,...k->...i", np.abs(qf), kmax)[..., None]
     with np.errstate(invalid="ignore"):
-        bound = 2.0 ** -9 * a + (e + S * 2.0 ** -24) * (a + np.abs(o)) + 1e-6
+        bound = 2.0 ** -8 * a + (e + S * 2.0 ** -24) * (a + np.abs(o)) + 1e-6
     return o, lse, bound
 
 

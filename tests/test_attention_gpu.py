@@ -3,8 +3,8 @@
 Inputs are bf16 (the generator rounds Normal(0, 1) draws to bf16, and the
 oracle takes the same bf16 values in float64).  Tolerances, derived from the
 kernel's arithmetic (``gpu_helpers.attention_reference``): per element,
-|O - O_ref| <= 2^-9 sum_j p_j |v_jc| (p rounded to bf16 for the second
-product, l summed in fp32) plus the fp32 error of the scores and of the two
+|O - O_ref| <= 2^-8 sum_j p_j |v_jc| (p rounded to bf16, 8 significant
+bits, for the second product; l summed in fp32) plus the fp32 error of the scores and of the two
 sums over keys, plus 1e-6.  LSE is m + log l in fp32: |LSE - LSE_ref| <=
 1e-5 * max(1, |LSE_ref|) + 1e-5.
 """
