@@ -243,7 +243,22 @@ RRS_API int softmax_rows_noalloc(const float* x, float* y, int64_t M, int64_t N,
 /* Synchronises `stream`, then returns and clears the device-side error word
  * of the current device: RRS_ERR_TIMEOUT if a split-row kernel stopped
  * waiting for its peers since the last call (its output is then incomplete),
- * RRS_OK otherwise, RRS_ERR_CUDA if the synchronisation failed. */
+ * RRS_OK otherwise, RRS_ERR_CUDA if the synchronisation failed.
+ *
+ * A timeout is also visible without this call.  The CTAs of a GRID-path
+ * row (RRS_PATH_GRID) wait for one another.  Each CTA takes its row and
+ * segment in the order the CTAs start, so the CTAs a CTA waits on are the
+ * ones that started around it: a complete row group always runs to the end
+ * and frees its SMs, and no CTA waits on one that could only start after it
+ * finished.  Every wait is also bounded (about a second), for a group whose
+ * later CTAs find no free SM for that long (other work holding the SMs).
+ * A GRID kernel whose wait runs out
+ * also sets a word of pinned host memory, so that once that kernel has
+ * finished, every later call of this library on the same device (any entry
+ * point that enqueues work) returns RRS_ERR_TIMEOUT without enqueuing
+ * anything, until rrs_device_error() reports and clears the timeout -- a
+ * sticky error, in the manner of CUDA's own.  The word is allocated with
+ * the first GRID-path call on a device. */
 RRS_API int rrs_device_error(void* stream);
 
 /* Static string naming a status code. */
@@ -273,6 +288,14 @@ RRS_API int rrs_force_cols_path(int cols_path);
  * context stays usable.  kind 0 turns injection off.  Nothing here faults
  * or hangs the GPU.  Returns RRS_OK or RRS_ERR_INVALID_ARG. */
 RRS_API int rrs_inject_fault(int kind);
+
+/* Testing only (no counterpart in the pages): enqueue on `stream` `ctas`
+ * CTAs that each hold `smem_bytes` of shared memory (at most the opt-in
+ * limit) for `nanoseconds` (at most 2e8) of the GPU's global timer and then
+ * return on their own, so that a test can run a call while other work holds
+ * SMs.  Nothing is read or written.  Returns RRS_OK, RRS_ERR_INVALID_ARG or
+ * RRS_ERR_CUDA. */
+RRS_API int rrs_test_occupy(int ctas, int smem_bytes, int64_t nanoseconds, void* stream);
 
 /* The planner, as pure host logic: the plan softmax_rows / row_sum would use
  * for this shape on a device with `sm_count` SMs and `smem_optin` bytes of

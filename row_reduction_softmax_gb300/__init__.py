@@ -93,6 +93,7 @@ _SIGNATURES = {
     "rrs_release_workspace": (ctypes.c_int, []),
     "rrs_force_path": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
     "rrs_inject_fault": (ctypes.c_int, [ctypes.c_int]),
+    "rrs_test_occupy": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _I64, _P]),
     "rrs_plan_softmax": (ctypes.c_int, [_I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                         ctypes.POINTER(Plan)]),
     "rrs_plan_row_sum": (ctypes.c_int, [_I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int,

@@ -114,6 +114,57 @@ int device_info(int dev, DeviceInfo* out) {
   return RRS_OK;
 }
 
+// ------------------------------------------------------ host error words ---
+// One word of pinned, mapped host memory per device.  A GRID kernel whose
+// bounded wait runs out writes RRS_ERR_TIMEOUT into it; every later call on
+// that device reads it (a plain host load, no synchronisation) and refuses
+// to enqueue with RRS_ERR_TIMEOUT until rrs_device_error() clears it.
+struct HostErrWord {
+  unsigned* host = nullptr;  // host address
+  unsigned* dev = nullptr;   // device address of the same word
+};
+std::map<int, HostErrWord> g_host_err;
+
+// The device address of `dev`'s word, allocated on first use (under g_mu).
+int host_err_word(int dev, unsigned** dptr) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  HostErrWord& w = g_host_err[dev];
+  if (!w.host) {
+    void* h = nullptr;
+    cudaError_t e = cudaHostAlloc(&h, 64, cudaHostAllocMapped | cudaHostAllocPortable);
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      return fail(RRS_ERR_NOMEM, std::string("cudaHostAlloc(error word): ") + cudaGetErrorString(e));
+    }
+    std::memset(h, 0, 64);
+    void* d = nullptr;
+    e = cudaHostGetDevicePointer(&d, h, 0);
+    if (e != cudaSuccess) {
+      (void)cudaFreeHost(h);
+      return fail_cuda(e, "cudaHostGetDevicePointer(error word)");
+    }
+    w.host = static_cast<unsigned*>(h);
+    w.dev = static_cast<unsigned*>(d);
+  }
+  *dptr = w.dev;
+  return RRS_OK;
+}
+
+// The word's value for `dev` (0 if it was never allocated); allocates nothing.
+unsigned host_err_value(int dev) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  auto it = g_host_err.find(dev);
+  if (it == g_host_err.end() || !it->second.host) return 0;
+  return *reinterpret_cast<volatile unsigned*>(it->second.host);
+}
+
+void host_err_clear(int dev) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  auto it = g_host_err.find(dev);
+  if (it != g_host_err.end() && it->second.host)
+    *reinterpret_cast<volatile unsigned*>(it->second.host) = 0;
+}
+
 // --------------------------------------------------------------- workspace ---
 // One buffer per (device, stream, kind): calls on one stream are ordered, so
 // they can share it; calls on different streams never do.  Grown with the
@@ -339,7 +390,7 @@ bool plan_grid(int64_t M, int64_t N, int sm_count, int smem_optin, int coop_ok, 
   p->stages = (int32_t)b_ns;
   p->tile = (int32_t)(b_stride / 4);
   p->smem_bytes = (int32_t)(staged_header_bytes() + b_ns * b_stride);
-  p->workspace_bytes = M * b_c * 16;
+  p->workspace_bytes = kGridArrivalBytes + M * b_c * 16;
   return true;
 }
 
@@ -574,6 +625,15 @@ bool vector_ok(const void* x, const void* y, int64_t ld) {
 }
 
 }  // namespace
+
+int check_no_pending_timeout(int dev) {
+  if (host_err_value(dev) != 0)
+    return fail(RRS_ERR_TIMEOUT,
+                "an earlier split-row kernel on this device stopped waiting for its peers (its output "
+                "is incomplete); rrs_device_error() reports and clears this");
+  return RRS_OK;
+}
+
 }  // namespace rrs
 
 using namespace rrs;
@@ -681,6 +741,7 @@ RRS_API int softmax_rows_ex(const float* x, int64_t ldx, float* y, int64_t ldy, 
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  if ((st = check_no_pending_timeout(dev)) != RRS_OK) return st;
   if ((st = check_device_pointer(x, dev, "x")) != RRS_OK) return st;
   if ((st = check_device_pointer(y, dev, "y")) != RRS_OK) return st;
   DeviceInfo info;
@@ -713,9 +774,11 @@ RRS_API int softmax_rows_ex(const float* x, int64_t ldx, float* y, int64_t ldy, 
     case RRS_PATH_GRID: {
       void* ws = nullptr;
       uint32_t ticket = 0;
+      unsigned* herr = nullptr;
+      if ((st = host_err_word(dev, &herr)) != RRS_OK) return st;
       if ((st = get_workspace(dev, s, kWsGrid, (size_t)plan.workspace_bytes, &ws, &ticket)) != RRS_OK)
         return st;
-      e = launch_softmax_staged_grid(plan, x, y, M, N, l, ws, ticket, g_fault.load(), s);
+      e = launch_softmax_staged_grid(plan, x, y, M, N, l, ws, ticket, g_fault.load(), herr, s);
       break;
     }
     case RRS_PATH_TWO_PHASE: {
@@ -750,6 +813,7 @@ RRS_API int softmax_cols(const float* x, int64_t ldx, float* y, int64_t ldy, int
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  if ((st = check_no_pending_timeout(dev)) != RRS_OK) return st;
   if ((st = check_device_pointer(x, dev, "x")) != RRS_OK) return st;
   if ((st = check_device_pointer(y, dev, "y")) != RRS_OK) return st;
   DeviceInfo info;
@@ -809,6 +873,7 @@ int row_reduce_impl(int op, const char* name, const float* x, float* out, int64_
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  if ((st = check_no_pending_timeout(dev)) != RRS_OK) return st;
   if ((st = check_device_pointer(out, dev, "out")) != RRS_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (N == 0) {  // the empty row's value: the sum's identity 0, the max's -inf, the mean 0/0
@@ -876,6 +941,7 @@ RRS_API int gelu(const float* x, float* y, int64_t n, void* stream) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
   int st;
+  if ((st = check_no_pending_timeout(dev)) != RRS_OK) return st;
   if ((st = check_device_pointer(x, dev, "x")) != RRS_OK) return st;
   if ((st = check_device_pointer(y, dev, "y")) != RRS_OK) return st;
   DeviceInfo info;
@@ -911,6 +977,7 @@ RRS_API int attention_fwd(const void* q, const void* k, const void* v, float* o,
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
   int st;
+  if ((st = check_no_pending_timeout(dev)) != RRS_OK) return st;
   if ((st = check_device_pointer(q, dev, "q")) != RRS_OK) return st;
   if ((st = check_device_pointer(k, dev, "k")) != RRS_OK) return st;
   if ((st = check_device_pointer(v, dev, "v")) != RRS_OK) return st;
@@ -926,12 +993,34 @@ RRS_API int attention_fwd(const void* q, const void* k, const void* v, float* o,
 }
 
 RRS_API int rrs_device_error(void* stream) {
+  clear_last_error();
   unsigned v = 0, w = 0;
   cudaError_t e = read_and_clear_staged_error(static_cast<cudaStream_t>(stream), &v);
   if (e == cudaSuccess) e = read_and_clear_attn_error(static_cast<cudaStream_t>(stream), &w);
   if (e != cudaSuccess) return fail_cuda(e, "rrs_device_error");
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) {
+    if (host_err_value(dev) != 0) v |= 1u;
+    host_err_clear(dev);
+  }
   v |= w;
   return v ? fail(RRS_ERR_TIMEOUT, "a split-row kernel stopped waiting for its peers") : RRS_OK;
+}
+
+RRS_API int rrs_test_occupy(int ctas, int smem_bytes, int64_t nanoseconds, void* stream) {
+  clear_last_error();
+  if (ctas < 1 || ctas > 65535 || smem_bytes < 0 || nanoseconds < 0 || nanoseconds > 200000000)
+    return fail(RRS_ERR_INVALID_ARG, "1 <= ctas <= 65535, smem_bytes >= 0, 0 <= ns <= 2e8");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  DeviceInfo info;
+  int st;
+  if ((st = device_info(dev, &info)) != RRS_OK) return st;
+  if (smem_bytes > info.smem_optin) return fail(RRS_ERR_INVALID_ARG, "smem_bytes above the opt-in limit");
+  e = launch_occupy(ctas, smem_bytes, nanoseconds, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "rrs_test_occupy launch");
+  return RRS_OK;
 }
 
 RRS_API int rrs_release_workspace(void) {

@@ -23,6 +23,10 @@ int check_device_pointer(const void* p, int dev, const char* name);
 // matrix of M rows of N entries at stride ld (0 when M or N is 0).
 int check_shape(int64_t M, int64_t N, int64_t ld, int64_t* extent);
 bool overlaps(const void* a, int64_t a_bytes, const void* b, int64_t b_bytes);
+// RRS_ERR_TIMEOUT (with its message) while a GRID kernel's timeout on `dev`
+// has not been collected by rrs_device_error(); reads one host word and
+// allocates nothing.
+int check_no_pending_timeout(int dev);
 
 // Per-device facts the planner needs, queried once per device.
 struct DeviceInfo {
@@ -46,6 +50,7 @@ constexpr int kSplitThreads = 256;       // CTA size of the cluster / two-phase 
 constexpr int kClusterVec = 8;           // float4 per thread in a cluster CTA segment
 constexpr int kClusterMax = 16;          // largest cluster (non-portable beyond 8)
 constexpr int64_t kChunkAlign = 1024;    // two-phase chunk granularity (elements)
+constexpr int64_t kGridArrivalBytes = 128;  // GRID workspace: the arrival counter, before the slots
 
 
 // ---- softmax launchers (return the launch's cudaError_t) ----
@@ -71,15 +76,24 @@ cudaError_t launch_softmax_staged_rows(const rrs_plan& p, const float* x, float*
                                        int64_t N, const Layout& l, cudaStream_t s);
 cudaError_t launch_softmax_staged_long(const rrs_plan& p, const float* x, float* y, int64_t M,
                                        int64_t N, const Layout& l, cudaStream_t s);
-// GRID plans: rows split over a grid of R * C <= SMs CTAs (one per SM, all
-// resident together; launched with programmatic dependent launch);
-// `workspace` holds 16 bytes per (row, segment) slot, zero-filled when
-// allocated, and `ticket` is unique per launch on that workspace.
+// GRID plans: rows split over a grid of R * C <= SMs CTAs (one per SM; a
+// CTA takes its row group and segment in arrival order, so a row's CTAs
+// are resident together; programmatic dependent launch).  `workspace`
+// (zero-filled when allocated) holds the arrival counter in its first
+// kGridArrivalBytes, then 16 bytes per (row, segment) slot; `ticket` is
+// unique per launch on that workspace.
 // `fault` != 0 (testing only, rrs_inject_fault): CTA 0 never publishes the
-// partial of its first segment, so its row's waits run out.
+// partial of its first segment, so its row's waits run out.  `host_err`
+// (device address of a mapped, pinned host word, or null) is set to
+// RRS_ERR_TIMEOUT when a wait runs out.
 cudaError_t launch_softmax_staged_grid(const rrs_plan& p, const float* x, float* y, int64_t M,
                                        int64_t N, const Layout& l, void* workspace, uint32_t ticket,
-                                       int fault, cudaStream_t s);
+                                       int fault, unsigned* host_err, cudaStream_t s);
+
+// Testing only: `ctas` CTAs of one thread and `smem_bytes` of dynamic shared
+// memory each, which hold their SMs for `ns` nanoseconds (global timer) and
+// return on their own.
+cudaError_t launch_occupy(int ctas, int smem_bytes, int64_t ns, cudaStream_t s);
 
 // ---- column softmax (softmax_cols.cu): COLS_CLUSTER plans carry cluster
 // (CTAs per band of cols_band() columns) and vec (rows per thread; a CTA

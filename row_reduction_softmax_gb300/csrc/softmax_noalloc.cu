@@ -99,6 +99,7 @@ extern "C" RRS_API int softmax_rows_noalloc(const float* x, float* y, int64_t M,
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
+  if ((st = check_no_pending_timeout(dev)) != RRS_OK) return st;
   if ((st = check_device_pointer(x, dev, "x")) != RRS_OK) return st;
   if ((st = check_device_pointer(y, dev, "y")) != RRS_OK) return st;
   NoAllocDevice d;

@@ -70,12 +70,25 @@ constexpr int kFailOff = kAbortOff + 16;               // int
 constexpr int kRedMOff = kFailOff + 16;                // float[32]
 constexpr int kRedSOff = kRedMOff + 128;               // float[32]
 constexpr int kWholeOff = kRedSOff + 128;              // MaxSum
+constexpr int kArrivalOff = kWholeOff + 16;            // int (GRID: this CTA's arrival index)
 constexpr int kHeaderBytes = 2048;
-static_assert(kWholeOff + 16 <= kHeaderBytes, "header overflow");
+static_assert(kArrivalOff + 16 <= kHeaderBytes, "header overflow");
 
-// Bounded wait on an mbarrier phase.  False on timeout (error word and the
+// A wait ran out: set the device error word and, when the launch was given
+// one, the host-visible word (pinned, mapped host memory the library checks
+// at the start of later calls without synchronising).
+__device__ void report_timeout(unsigned* host_err) {
+  atomicOr(&g_device_error, kErrTimeout);
+  if (host_err) {
+    *reinterpret_cast<volatile unsigned*>(host_err) = kErrTimeout;
+    __threadfence_system();
+  }
+}
+
+// Bounded wait on an mbarrier phase.  False on timeout (error words and the
 // CTA's abort flag set) or if another thread of the CTA already aborted.
-__device__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+__device__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                             unsigned* host_err = nullptr) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   uint32_t n = 0;
@@ -83,7 +96,7 @@ __device__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort
     if ((++n & 63u) == 0) {
       if (*abort_flag) return false;
       if (global_timer_ns() - t0 > kWaitLimitNs) {
-        atomicOr(&g_device_error, kErrTimeout);
+        report_timeout(host_err);
         *abort_flag = 1;
         return false;
       }
@@ -420,8 +433,20 @@ softmax_staged_long_kernel(const float* x, float* y, int64_t M, int64_t N, int64
 // spare register set) while warp 0 runs E(k); then the 15 consumer warps
 // meet and warps 1..14 write y = e * exp(m_c - m) / s of item k.  E(k) needs
 // P(k) of its row's CTAs, each published before that CTA's own E(k - LEAD);
-// all of a row's CTAs are resident (one CTA per SM, R * C <= SMs), so the
-// waits end.
+// the CTAs of a row all start (see below), so the waits end.
+//
+// Which (row group, segment) a CTA takes is decided by its ARRIVAL order,
+// not by blockIdx: the first CTA to start takes arrival index 0, and CTA a
+// takes segment a % C of rows a / C + k R.  So the C CTAs a CTA waits on are
+// the ones that arrived just before or just after it: at any time at most
+// one row group is partly resident, every complete group runs to the end
+// and frees its SMs, and the rest start.  No CTA waits on a CTA that can
+// only start once it has finished, whatever else holds SMs (another
+// stream's kernels, another process); only a group whose later members find
+// no free SM for the whole bounded wait gives up, and that is reported.  The
+// counter lives in the workspace and starts each launch at 0: the CTA that
+// draws the last index resets it, before it lets the next kernel on the
+// stream launch (and so before any CTA of that kernel draws).
 __device__ __forceinline__ uint64_t pack_tagged(uint32_t ticket, float v) {
   return ((uint64_t)ticket << 32) | (uint64_t)__float_as_uint(v);
 }
@@ -441,18 +466,31 @@ template <int VEC, int LEAD>
 __global__ void __launch_bounds__(kGThreads, 1)
 softmax_staged_grid_kernel(const float* x, float* y, int64_t M, int64_t N, int64_t ldx,
                            int64_t ldy, int64_t seg, int32_t C, int32_t R, int32_t NS,
-                           int32_t stage_stride, uint64_t* __restrict__ slots, uint32_t ticket,
-                           int32_t fault, int32_t log_out) {
+                           int32_t stage_stride, unsigned* __restrict__ arrivals,
+                           uint64_t* __restrict__ slots, uint32_t ticket, int32_t fault,
+                           int32_t log_out, unsigned* host_err) {
   extern __shared__ __align__(1024) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kFullOff);
   uint64_t* empty = reinterpret_cast<uint64_t*>(smem + kEmptyOff);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAbortOff);
   volatile int* fail_flag = reinterpret_cast<volatile int*>(smem + kFailOff);
   MaxSum* whole = reinterpret_cast<MaxSum*>(smem + kWholeOff);
+  volatile int* arrival = reinterpret_cast<volatile int*>(smem + kArrivalOff);
   unsigned char* stages = smem + kHeaderBytes;
 
-  const int c = (int)(blockIdx.x % C);
-  const int64_t row0 = blockIdx.x / C;
+  // arrival index (every CTA draws one, before anything can return)
+  if (threadIdx.x == 0) {
+    const unsigned a = atomicAdd(arrivals, 1u);
+    if (a == gridDim.x - 1) {   // the last: ready for the next launch, before it may start
+      atomicExch(arrivals, 0u);
+      __threadfence();
+    }
+    *arrival = (int)a;
+  }
+  __syncthreads();
+  const int me = *arrival;
+  const int c = me % C;
+  const int64_t row0 = me / C;
   const int64_t seg_begin = (int64_t)c * seg;
   const int64_t seg_n = min(seg, N - seg_begin);
   const int64_t items = (M > row0) ? (M - row0 + R - 1) / R : 0;
@@ -481,13 +519,13 @@ softmax_staged_grid_kernel(const float* x, float* y, int64_t M, int64_t N, int64
       bool ok = true;
       for (; k < items; ++k) {
         const int st = (int)(k % NS);
-        if (k >= NS && !wait_bounded(&empty[st], (uint32_t)(((k / NS) - 1) & 1), abort_flag)) {
+        if (k >= NS && !wait_bounded(&empty[st], (uint32_t)(((k / NS) - 1) & 1), abort_flag, host_err)) {
           ok = false;
           break;
         }
         // every CTA's first segment gates the first exchange of its row: let
         // it land before the rest of the ring is queued behind it in HBM
-        if (k == 2 && NS > 2 && !wait_bounded(&full[0], 0, abort_flag)) {
+        if (k == 2 && NS > 2 && !wait_bounded(&full[0], 0, abort_flag, host_err)) {
           ok = false;
           break;
         }
@@ -510,7 +548,7 @@ softmax_staged_grid_kernel(const float* x, float* y, int64_t M, int64_t N, int64
   // reduction trees).  False if a wait ran out (the same answer in all of them).
   auto partial = [&](int64_t k, float4 (&v)[VEC], float& mc_out) -> bool {
     const int st = (int)(k % NS);
-    const bool got = wait_bounded(&full[st], (uint32_t)((k / NS) & 1), abort_flag);
+    const bool got = wait_bounded(&full[st], (uint32_t)((k / NS) & 1), abort_flag, host_err);
     const float4* sm = reinterpret_cast<const float4*>(stages + (size_t)st * stage_stride);
 #pragma unroll
     for (int i = 0; i < VEC; ++i) {
@@ -551,7 +589,7 @@ softmax_staged_grid_kernel(const float* x, float* y, int64_t M, int64_t N, int64
     named_barrier(kPartialBar, kPartialThreads);
     sum = warp_sum((lane >= 1 && lane < kGConsumerWarps) ? red_s[lane] : 0.f);
     mc_out = m;
-    if (ptid == 0 && !(fault != 0 && blockIdx.x == 0 && k == 0)) {
+    if (ptid == 0 && !(fault != 0 && me == 0 && k == 0)) {
       uint64_t* sl = slots + 2 * ((row0 + k * R) * C + c);
       publish_gpu_u64(sl, pack_tagged(ticket, m));
       publish_gpu_u64(sl + 1, pack_tagged(ticket, sum));
@@ -594,7 +632,7 @@ softmax_staged_grid_kernel(const float* x, float* y, int64_t M, int64_t N, int64
     if (lane == 0) {
       *whole = acc;
       if (!seen) {
-        atomicOr(&g_device_error, kErrTimeout);
+        report_timeout(host_err);
         *abort_flag = 1;
         *fail_flag = 1;
       }
@@ -750,7 +788,7 @@ cudaError_t launch_softmax_staged_long(const rrs_plan& p, const float* x, float*
 
 cudaError_t launch_softmax_staged_grid(const rrs_plan& p, const float* x, float* y, int64_t M,
                                        int64_t N, const Layout& l, void* workspace, uint32_t ticket,
-                                       int fault, cudaStream_t s) {
+                                       int fault, unsigned* host_err, cudaStream_t s) {
   if (p.threads != kGThreads) return cudaErrorInvalidConfiguration;
   // segments of up to 4 float4 per thread run partials two items ahead (three
   // register sets); longer ones, up to 8 float4, one item ahead
@@ -764,24 +802,42 @@ cudaError_t launch_softmax_staged_grid(const rrs_plan& p, const float* x, float*
   cudaError_t e = allow_dynamic_smem(kern);
   if (e != cudaSuccess) return e;
   // A plain launch with programmatic dependent launch, not a cooperative
-  // one: a cooperative launch cannot overlap the previous kernel's drain
-  // (measured: 3.4 to 4.5 us between back-to-back calls, against an
-  // overlap with the plain launch).  Co-residency of the R * C <= SMs CTAs
-  // rests on one CTA fitting each SM; if other work holds SMs for longer
-  // than the bounded wait, the call reports RRS_ERR_TIMEOUT instead of
-  // hanging.
-  uint64_t* slots = static_cast<uint64_t*>(workspace);
+  // one: a cooperative launch waits for every SM to be free, so it cannot
+  // overlap the previous kernel's drain (measured on 32 x 2^20: 48.3 us
+  // against 44.9 us).  The CTAs of a row are made co-resident by drawing
+  // their work in arrival order instead (see the kernel).  Every wait is
+  // still bounded: if one runs out, the kernel sets the device error word
+  // and `host_err`, and later calls report RRS_ERR_TIMEOUT.
+  unsigned* arrivals = static_cast<unsigned*>(workspace);
+  uint64_t* slots = reinterpret_cast<uint64_t*>(static_cast<unsigned char*>(workspace) + kGridArrivalBytes);
   const int32_t C = (int32_t)p.ctas_per_row;
   const dim3 grid((unsigned)p.grid), block(kGThreads);
   const size_t smem = (size_t)p.smem_bytes;
   if (p.vec == 2)
-    return launch_pdl(k2, grid, block, smem, s, 0, x, y, M, N, l.ldx, l.ldy, p.chunk, C, p.rows_per_cta,
-                      p.stages, p.tile * 4, slots, ticket, (int32_t)fault, (int32_t)l.log_out);
+    return launch_pdl(k2, grid, block, smem, s, 0, x, y, M, N, l.ldx, l.ldy, p.chunk, C,
+                      p.rows_per_cta, p.stages, p.tile * 4, arrivals, slots, ticket, (int32_t)fault,
+                      (int32_t)l.log_out, host_err);
   if (p.vec == 4)
-    return launch_pdl(k4, grid, block, smem, s, 0, x, y, M, N, l.ldx, l.ldy, p.chunk, C, p.rows_per_cta,
-                      p.stages, p.tile * 4, slots, ticket, (int32_t)fault, (int32_t)l.log_out);
-  return launch_pdl(k8, grid, block, smem, s, 0, x, y, M, N, l.ldx, l.ldy, p.chunk, C, p.rows_per_cta,
-                    p.stages, p.tile * 4, slots, ticket, (int32_t)fault, (int32_t)l.log_out);
+    return launch_pdl(k4, grid, block, smem, s, 0, x, y, M, N, l.ldx, l.ldy, p.chunk, C,
+                      p.rows_per_cta, p.stages, p.tile * 4, arrivals, slots, ticket, (int32_t)fault,
+                      (int32_t)l.log_out, host_err);
+  return launch_pdl(k8, grid, block, smem, s, 0, x, y, M, N, l.ldx, l.ldy, p.chunk, C,
+                    p.rows_per_cta, p.stages, p.tile * 4, arrivals, slots, ticket, (int32_t)fault,
+                    (int32_t)l.log_out, host_err);
+}
+
+// Testing only (rrs_test_occupy): holds an SM's shared memory for `ns`
+// nanoseconds of the global timer, then returns; no memory is touched.
+__global__ void occupy_kernel(int64_t ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (global_timer_ns() - t0 < (uint64_t)ns) __nanosleep(2000);
+}
+
+cudaError_t launch_occupy(int ctas, int smem_bytes, int64_t ns, cudaStream_t s) {
+  cudaError_t e = allow_dynamic_smem(reinterpret_cast<const void*>(occupy_kernel));
+  if (e != cudaSuccess) return e;
+  occupy_kernel<<<ctas, 32, (size_t)smem_bytes, s>>>(ns);
+  return cudaGetLastError();
 }
 
 cudaError_t read_and_clear_staged_error(cudaStream_t s, unsigned* value) {

@@ -160,7 +160,7 @@ def test_planner_covers_every_column(lib, M, N):
         assert p["tile"] >= seg and p["tile"] % 32 == 0 and 2 <= p["stages"] <= 64
         assert -(-seg // 4) <= p["vec"] * 448 and p["vec"] in (2, 4, 8)
         assert p["smem_bytes"] == 2048 + p["stages"] * p["tile"] * 4 <= 232448
-        assert p["rounds"] == -(-M // R) and p["workspace_bytes"] == M * C * 16
+        assert p["rounds"] == -(-M // R) and p["workspace_bytes"] == 128 + M * C * 16
 
 
 def test_forced_paths(lib):

@@ -14,7 +14,7 @@ import pytest
 
 import row_reduction_softmax_gb300 as rrs
 import workloads
-from gpu_helpers import check_softmax
+from gpu_helpers import check_every_row, check_softmax
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -45,5 +45,69 @@ def test_grid_wait_runs_out_and_is_reported(lib):
         torch.cuda.synchronize()
         assert rrs.device_error() == 0
         check_softmax(y.cpu().numpy(), x_host, "after an injected timeout")
+    finally:
+        rrs.force_path("auto", "auto")
+
+
+def test_grid_timeout_is_refused_until_collected(lib):
+    """After a GRID kernel's wait ran out (and the kernel finished), later
+    calls on the device return RRS_ERR_TIMEOUT without a synchronising poll,
+    until rrs_device_error collects it."""
+    M, N = 4, 65536
+    x_host = workloads.matrix(workloads.WORKLOADS["c5"].with_shape(M, N))
+    x = torch.from_numpy(x_host).cuda()
+    y = torch.empty_like(x)
+    s = torch.empty(M, device="cuda")
+    try:
+        rrs.force_path("grid")
+        assert rrs.device_error() == 0
+        assert lib.rrs_inject_fault(1) == 0
+        rrs.softmax_rows(x, y)                       # enqueued: RRS_OK
+        lib.rrs_inject_fault(0)
+        torch.cuda.synchronize()                     # the kernel gave up and finished
+        for call in (lambda: rrs.softmax_rows(x, y), lambda: rrs.row_sum(x, s),
+                     lambda: rrs.softmax_cols(x)):
+            with pytest.raises(rrs.RRSError) as e:
+                call()
+            assert e.value.status == TIMEOUT
+        assert lib.softmax_rows_noalloc(x.data_ptr(), y.data_ptr(), M, N, N,
+                                        torch.cuda.current_stream().cuda_stream) == TIMEOUT
+        assert rrs.device_error() == TIMEOUT         # collected ...
+        assert rrs.device_error() == 0               # ... and cleared
+        rrs.softmax_rows(x, y)
+        torch.cuda.synchronize()
+        assert rrs.device_error() == 0
+        check_softmax(y.cpu().numpy(), x_host, "after a collected timeout")
+    finally:
+        lib.rrs_inject_fault(0)
+        rrs.force_path("auto", "auto")
+
+
+def test_grid_runs_while_other_work_holds_sms(lib):
+    """Half the SMs held for 50 ms by CTAs of another stream whose shared
+    memory leaves no room for a GRID CTA: the GRID CTAs draw their rows in
+    arrival order, so the first complete row group runs on the free SMs and
+    the rest follow, and the result is right (a timeout would have to be
+    reported, never an incomplete y behind RRS_OK)."""
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    w = workloads.WORKLOADS["c5"]
+    x_host = workloads.matrix(w)
+    x = torch.from_numpy(x_host).cuda()
+    other = torch.cuda.Stream()
+    try:
+        rrs.force_path("auto", "auto")
+        assert rrs.plan_softmax(w.M, w.N)["path_name"] == "grid"
+        for trial in range(2):
+            y = torch.full_like(x, float("nan"))
+            torch.cuda.synchronize()
+            assert lib.rrs_test_occupy(props.multi_processor_count // 2,
+                                       props.shared_memory_per_block_optin, 50_000_000,
+                                       other.cuda_stream) == 0
+            rrs.softmax_rows(x, y)
+            torch.cuda.synchronize()
+            st = rrs.device_error()
+            assert st in (0, TIMEOUT), st
+            if st == 0:
+                check_every_row(check_softmax, y, x_host, f"c5 beside held SMs, trial {trial}")
     finally:
         rrs.force_path("auto", "auto")
