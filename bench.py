@@ -131,23 +131,27 @@ def measured_bf16_peak():
         return 1900.0, "fallback"
 
 
-# The sources each timed kernel is built from, beyond the files every kernel
-# shares (the common device headers and the planner, which sets its launch).
+# The sources each timed kernel is built from, beyond the device headers
+# every kernel shares.  A committed ncu figure is keyed to a hash of these
+# files and of the launch plan the planner makes for the workload, so it
+# stands while neither the kernel nor its launch changes.
 KERNEL_SOURCES = {
     "softmax_row_regs_kernel": ["softmax_row.cu"],
     "softmax_cluster_kernel": ["softmax_split.cu"],
     "softmax_staged_grid_kernel": ["softmax_staged.cu", "sm100_async.cuh"],
     "row_reduce_rows_kernel": ["row_sum.cu"],
     "softmax_cols_band_kernel": ["softmax_cols.cu"],
+    "softmax_cols_staged_kernel": ["softmax_cols_staged.cu", "sm100_async.cuh"],
     "attention_fwd_kernel": ["attention.cu", "sm100_async.cuh", "sm100_tcgen05.cuh"],
     "gelu_kernel": ["gelu.cu"],
 }
-COMMON_SOURCES = ["capi.cu", "device_common.cuh", "internal.h", "launch_util.h", "../../include/rrs.h"]
+COMMON_SOURCES = ["device_common.cuh", "launch_util.h"]
 
 
-def source_hash(kernel: str | None = None) -> str:
+def source_hash(kernel: str | None = None, plan: dict | None = None) -> str:
     """Hash of the sources a kernel is built from (all of csrc/ for an unknown
-    or no kernel): a committed ncu figure stands only while it matches."""
+    or no kernel) and of its launch plan: a committed ncu figure stands only
+    while it matches."""
     csrc = os.path.join(ROOT, "row_reduction_softmax_gb300", "csrc")
     if kernel in KERNEL_SOURCES:
         paths = [os.path.join(csrc, n) for n in sorted(COMMON_SOURCES + KERNEL_SOURCES[kernel])]
@@ -158,12 +162,15 @@ def source_hash(kernel: str | None = None) -> str:
         with open(p, "rb") as f:
             h.update(os.path.basename(p).encode())
             h.update(f.read())
+    if plan is not None:
+        h.update(json.dumps({k: plan[k] for k in sorted(plan) if k != "path_name"}, sort_keys=True).encode())
     return h.hexdigest()[:12]
 
 
-def ncu_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if it matches the kernel's current sources."""
-    want = source_hash(kernel)
+def ncu_traffic(kernel: str, workload: str, plan: dict | None = None):
+    """DRAM bytes per launch from a committed ncu summary, if it matches the
+    kernel's current sources and launch plan."""
+    want = source_hash(kernel, plan)
     pat = re.compile(r"traffic:\s+kernel=(\S+)\s+workload=(\S+)\s+bytes_per_launch=(\d+)\s+source=(\w+)")
     for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
         with open(path) as f:
@@ -407,7 +414,8 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": f"of {peak_kind}",
                      "kernel": kernel_name, "algorithmic_bytes_per_launch": alg_bytes,
-                     "traffic": ncu_traffic(kernel_name, w.name), "source": source_hash(kernel_name)},
+                     "traffic": ncu_traffic(kernel_name, w.name, plan),
+                     "source": source_hash(kernel_name, plan)},
         "gpu_launches": args.steps * launches_per_call,
         "clocks": sampler.summary(),
         "parity": parity,
