@@ -141,7 +141,6 @@ KERNEL_SOURCES = {
     "softmax_staged_grid_kernel": ["softmax_staged.cu", "sm100_async.cuh"],
     "row_reduce_rows_kernel": ["row_sum.cu"],
     "softmax_cols_band_kernel": ["softmax_cols.cu"],
-    "softmax_cols_staged_kernel": ["softmax_cols_staged.cu", "sm100_async.cuh"],
     "attention_fwd_kernel": ["attention.cu", "sm100_async.cuh", "sm100_tcgen05.cuh"],
     "gelu_kernel": ["gelu.cu"],
 }
