@@ -77,7 +77,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget")
-    ap.add_argument("--suite-steps", type=int, default=30)
+    ap.add_argument("--suite-steps", type=int, default=200)
     ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--path", default="auto", help="force a softmax path (auto, row_regs, cluster, ...)")
     ap.add_argument("--only", default=None,

@@ -257,8 +257,10 @@ RRS_API int softmax_rows_noalloc(const float* x, float* y, int64_t M, int64_t N,
  * finished, every later call of this library on the same device (any entry
  * point that enqueues work) returns RRS_ERR_TIMEOUT without enqueuing
  * anything, until rrs_device_error() reports and clears the timeout -- a
- * sticky error, in the manner of CUDA's own.  The word is allocated with
- * the first GRID-path call on a device. */
+ * sticky error, in the manner of CUDA's own.  The word (pinned host
+ * memory, cudaHostAlloc) is allocated with the first GRID-path call on a
+ * device and kept until the process exits: make that first call before any
+ * stream capture. */
 RRS_API int rrs_device_error(void* stream);
 
 /* Static string naming a status code. */

@@ -117,52 +117,52 @@ int device_info(int dev, DeviceInfo* out) {
 // ------------------------------------------------------ host error words ---
 // One word of pinned, mapped host memory per device.  A GRID kernel whose
 // bounded wait runs out writes RRS_ERR_TIMEOUT into it; every later call on
-// that device reads it (a plain host load, no synchronisation) and refuses
-// to enqueue with RRS_ERR_TIMEOUT until rrs_device_error() clears it.
-struct HostErrWord {
-  unsigned* host = nullptr;  // host address
-  unsigned* dev = nullptr;   // device address of the same word
-};
-std::map<int, HostErrWord> g_host_err;
+// that device reads it (a plain host load, no lock, no synchronisation) and
+// refuses to enqueue with RRS_ERR_TIMEOUT until rrs_device_error() clears it.
+constexpr int kMaxDevices = 64;
+std::atomic<unsigned*> g_host_err[kMaxDevices];      // host address of each device's word
+std::atomic<unsigned*> g_host_err_dev[kMaxDevices];  // the same word's device address
 
 // The device address of `dev`'s word, allocated on first use (under g_mu).
 int host_err_word(int dev, unsigned** dptr) {
+  if (dev < 0 || dev >= kMaxDevices) return fail(RRS_ERR_INVALID_ARG, "device ordinal out of range");
+  if (unsigned* d = g_host_err_dev[dev].load(std::memory_order_acquire)) {
+    *dptr = d;
+    return RRS_OK;
+  }
   std::lock_guard<std::mutex> lock(g_mu);
-  HostErrWord& w = g_host_err[dev];
-  if (!w.host) {
-    void* h = nullptr;
-    cudaError_t e = cudaHostAlloc(&h, 64, cudaHostAllocMapped | cudaHostAllocPortable);
+  if (!g_host_err_dev[dev].load()) {
+    void* p = nullptr;
+    cudaError_t e = cudaHostAlloc(&p, 64, cudaHostAllocMapped | cudaHostAllocPortable);
     if (e != cudaSuccess) {
       (void)cudaGetLastError();
       return fail(RRS_ERR_NOMEM, std::string("cudaHostAlloc(error word): ") + cudaGetErrorString(e));
     }
-    std::memset(h, 0, 64);
+    std::memset(p, 0, 64);
     void* d = nullptr;
-    e = cudaHostGetDevicePointer(&d, h, 0);
+    e = cudaHostGetDevicePointer(&d, p, 0);
     if (e != cudaSuccess) {
-      (void)cudaFreeHost(h);
+      (void)cudaFreeHost(p);
       return fail_cuda(e, "cudaHostGetDevicePointer(error word)");
     }
-    w.host = static_cast<unsigned*>(h);
-    w.dev = static_cast<unsigned*>(d);
+    g_host_err[dev].store(static_cast<unsigned*>(p), std::memory_order_release);
+    g_host_err_dev[dev].store(static_cast<unsigned*>(d), std::memory_order_release);
   }
-  *dptr = w.dev;
+  *dptr = g_host_err_dev[dev].load();
   return RRS_OK;
 }
 
 // The word's value for `dev` (0 if it was never allocated); allocates nothing.
 unsigned host_err_value(int dev) {
-  std::lock_guard<std::mutex> lock(g_mu);
-  auto it = g_host_err.find(dev);
-  if (it == g_host_err.end() || !it->second.host) return 0;
-  return *reinterpret_cast<volatile unsigned*>(it->second.host);
+  if (dev < 0 || dev >= kMaxDevices) return 0;
+  const unsigned* h = g_host_err[dev].load(std::memory_order_acquire);
+  return h ? *reinterpret_cast<const volatile unsigned*>(h) : 0;
 }
 
 void host_err_clear(int dev) {
-  std::lock_guard<std::mutex> lock(g_mu);
-  auto it = g_host_err.find(dev);
-  if (it != g_host_err.end() && it->second.host)
-    *reinterpret_cast<volatile unsigned*>(it->second.host) = 0;
+  if (dev < 0 || dev >= kMaxDevices) return;
+  unsigned* h = g_host_err[dev].load(std::memory_order_acquire);
+  if (h) *reinterpret_cast<volatile unsigned*>(h) = 0;
 }
 
 // --------------------------------------------------------------- workspace ---
