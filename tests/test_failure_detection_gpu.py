@@ -111,3 +111,29 @@ def test_grid_runs_while_other_work_holds_sms(lib):
                 check_every_row(check_softmax, y, x_host, f"c5 beside held SMs, trial {trial}")
     finally:
         rrs.force_path("auto", "auto")
+
+
+def test_two_grid_calls_at_once_on_two_streams(lib):
+    """Two c5 calls on two streams at the same time: 304 grid CTAs for 152 SMs,
+    so each launch gets only part of the GPU while the other runs.  Each CTA
+    draws its row in arrival order from its own stream's workspace, so a
+    complete row group of either launch always runs; both results are right."""
+    w = workloads.WORKLOADS["c5"]
+    xs = [workloads.matrix(w), np.flip(workloads.matrix(w), axis=1).copy()]
+    dx = [torch.from_numpy(a).cuda() for a in xs]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    try:
+        rrs.force_path("auto", "auto")
+        assert rrs.plan_softmax(w.M, w.N)["path_name"] == "grid"
+        ys = [torch.full_like(dx[0], float("nan")) for _ in range(2)]
+        torch.cuda.synchronize()
+        for _ in range(3):
+            for s, x, y in zip(streams, dx, ys):
+                with torch.cuda.stream(s):
+                    rrs.softmax_rows(x, y)
+        torch.cuda.synchronize()
+        assert rrs.device_error() == 0
+        for k in range(2):
+            check_every_row(check_softmax, ys[k], xs[k], f"c5 concurrent stream {k}")
+    finally:
+        rrs.force_path("auto", "auto")
