@@ -169,20 +169,17 @@ void host_err_clear(int dev) {
 // One buffer per (device, stream, kind): calls on one stream are ordered, so
 // they can share it; calls on different streams never do.  Grown with the
 // stream-ordered allocator (ordered after earlier work on the stream that
-// still reads the old buffer) and zero-filled when (re)allocated.  The GRID
-// kind also carries the ticket its partials are published under: one per
-// launch, never 0, so slots left by earlier launches never look current.
+// still reads the old buffer) and zero-filled when (re)allocated (the GRID
+// kind's kernels keep their own launch counter and tickets in it).
 enum WorkspaceKind { kWsTwoPhase = 0, kWsGrid = 1, kWsRowSum = 2 };
 
 struct Workspace {
   void* ptr = nullptr;
   size_t bytes = 0;
-  uint32_t ticket = 0;
 };
 std::map<std::tuple<int, uintptr_t, int>, Workspace> g_workspaces;
 
-int get_workspace(int dev, cudaStream_t s, int kind, size_t bytes, void** ptr,
-                  uint32_t* ticket = nullptr) {
+int get_workspace(int dev, cudaStream_t s, int kind, size_t bytes, void** ptr) {
   std::lock_guard<std::mutex> lock(g_mu);
   Workspace& w = g_workspaces[{dev, reinterpret_cast<uintptr_t>(s), kind}];
   if (w.bytes < bytes) {
@@ -202,10 +199,6 @@ int get_workspace(int dev, cudaStream_t s, int kind, size_t bytes, void** ptr,
     e = cudaMemsetAsync(w.ptr, 0, want, s);
     if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(workspace)");
     w.bytes = want;
-  }
-  if (ticket) {
-    if (++w.ticket == 0) w.ticket = 1;
-    *ticket = w.ticket;
   }
   *ptr = w.ptr;
   return RRS_OK;
@@ -773,12 +766,10 @@ RRS_API int softmax_rows_ex(const float* x, int64_t ldx, float* y, int64_t ldy, 
       break;
     case RRS_PATH_GRID: {
       void* ws = nullptr;
-      uint32_t ticket = 0;
       unsigned* herr = nullptr;
       if ((st = host_err_word(dev, &herr)) != RRS_OK) return st;
-      if ((st = get_workspace(dev, s, kWsGrid, (size_t)plan.workspace_bytes, &ws, &ticket)) != RRS_OK)
-        return st;
-      e = launch_softmax_staged_grid(plan, x, y, M, N, l, ws, ticket, g_fault.load(), herr, s);
+      if ((st = get_workspace(dev, s, kWsGrid, (size_t)plan.workspace_bytes, &ws)) != RRS_OK) return st;
+      e = launch_softmax_staged_grid(plan, x, y, M, N, l, ws, g_fault.load(), herr, s);
       break;
     }
     case RRS_PATH_TWO_PHASE: {

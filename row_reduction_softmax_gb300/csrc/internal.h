@@ -79,16 +79,16 @@ cudaError_t launch_softmax_staged_long(const rrs_plan& p, const float* x, float*
 // GRID plans: rows split over a grid of R * C <= SMs CTAs (one per SM; a
 // CTA takes its row group and segment in arrival order, so a row's CTAs
 // are resident together; programmatic dependent launch).  `workspace`
-// (zero-filled when allocated) holds the arrival counter in its first
-// kGridArrivalBytes, then 16 bytes per (row, segment) slot; `ticket` is
-// unique per launch on that workspace.
+// (zero-filled when allocated) holds the arrival counter, which also hands
+// each launch its ticket, in its first kGridArrivalBytes, then 16 bytes per
+// (row, segment) slot.
 // `fault` != 0 (testing only, rrs_inject_fault): CTA 0 never publishes the
 // partial of its first segment, so its row's waits run out.  `host_err`
 // (device address of a mapped, pinned host word, or null) is set to
 // RRS_ERR_TIMEOUT when a wait runs out.
 cudaError_t launch_softmax_staged_grid(const rrs_plan& p, const float* x, float* y, int64_t M,
-                                       int64_t N, const Layout& l, void* workspace, uint32_t ticket,
-                                       int fault, unsigned* host_err, cudaStream_t s);
+                                       int64_t N, const Layout& l, void* workspace, int fault,
+                                       unsigned* host_err, cudaStream_t s);
 
 // Testing only: `ctas` CTAs of one thread and `smem_bytes` of dynamic shared
 // memory each, which hold their SMs for `ns` nanoseconds (global timer) and

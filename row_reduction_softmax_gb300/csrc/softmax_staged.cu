@@ -70,7 +70,7 @@ constexpr int kFailOff = kAbortOff + 16;               // int
 constexpr int kRedMOff = kFailOff + 16;                // float[32]
 constexpr int kRedSOff = kRedMOff + 128;               // float[32]
 constexpr int kWholeOff = kRedSOff + 128;              // MaxSum
-constexpr int kArrivalOff = kWholeOff + 16;            // int (GRID: this CTA's arrival index)
+constexpr int kArrivalOff = kWholeOff + 16;            // int[2] (GRID: arrival index, ticket)
 constexpr int kHeaderBytes = 2048;
 static_assert(kArrivalOff + 16 <= kHeaderBytes, "header overflow");
 
@@ -444,9 +444,14 @@ softmax_staged_long_kernel(const float* x, float* y, int64_t M, int64_t N, int64
 // only start once it has finished, whatever else holds SMs (another
 // stream's kernels, another process); only a group whose later members find
 // no free SM for the whole bounded wait gives up, and that is reported.  The
-// counter lives in the workspace and starts each launch at 0: the CTA that
-// draws the last index resets it, before it lets the next kernel on the
-// stream launch (and so before any CTA of that kernel draws).
+// counter is one 64-bit word in the workspace, (epoch << 32 | count): a CTA's
+// atomic add returns its arrival index (count) and its launch's ticket
+// (epoch + 1) at once, and the CTA that draws the last index sets the word to
+// (epoch + 1) << 32 before it lets the next kernel on the stream launch (and
+// so before any CTA of that kernel draws).  Every launch thus gets a fresh
+// ticket on the device -- also each replay of a captured CUDA graph, whose
+// kernel arguments never change -- so a slot left by an earlier launch never
+// looks current.
 __device__ __forceinline__ uint64_t pack_tagged(uint32_t ticket, float v) {
   return ((uint64_t)ticket << 32) | (uint64_t)__float_as_uint(v);
 }
@@ -466,9 +471,9 @@ template <int VEC, int LEAD>
 __global__ void __launch_bounds__(kGThreads, 1)
 softmax_staged_grid_kernel(const float* x, float* y, int64_t M, int64_t N, int64_t ldx,
                            int64_t ldy, int64_t seg, int32_t C, int32_t R, int32_t NS,
-                           int32_t stage_stride, unsigned* __restrict__ arrivals,
-                           uint64_t* __restrict__ slots, uint32_t ticket, int32_t fault,
-                           int32_t log_out, unsigned* host_err) {
+                           int32_t stage_stride, unsigned long long* __restrict__ arrivals,
+                           uint64_t* __restrict__ slots, int32_t fault, int32_t log_out,
+                           unsigned* host_err) {
   extern __shared__ __align__(1024) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kFullOff);
   uint64_t* empty = reinterpret_cast<uint64_t*>(smem + kEmptyOff);
@@ -478,17 +483,21 @@ softmax_staged_grid_kernel(const float* x, float* y, int64_t M, int64_t N, int64
   volatile int* arrival = reinterpret_cast<volatile int*>(smem + kArrivalOff);
   unsigned char* stages = smem + kHeaderBytes;
 
-  // arrival index (every CTA draws one, before anything can return)
+  // arrival index and ticket (every CTA draws, before anything can return)
   if (threadIdx.x == 0) {
-    const unsigned a = atomicAdd(arrivals, 1u);
-    if (a == gridDim.x - 1) {   // the last: ready for the next launch, before it may start
-      atomicExch(arrivals, 0u);
+    const unsigned long long old = atomicAdd(arrivals, 1ull);
+    const unsigned a = (unsigned)(old & 0xffffffffull);
+    const unsigned epoch = (unsigned)(old >> 32);
+    if (a == gridDim.x - 1) {   // the last: the next launch's epoch and count 0, before it may start
+      atomicExch(arrivals, (unsigned long long)(epoch == 0xfffffffeu ? 0u : epoch + 1u) << 32);
       __threadfence();
     }
-    *arrival = (int)a;
+    arrival[0] = (int)a;
+    arrival[1] = (int)(epoch + 1u);   // never 0, the tag of a zero-filled slot
   }
   __syncthreads();
-  const int me = *arrival;
+  const int me = arrival[0];
+  const uint32_t ticket = (uint32_t)arrival[1];
   const int c = me % C;
   const int64_t row0 = me / C;
   const int64_t seg_begin = (int64_t)c * seg;
@@ -496,7 +505,7 @@ softmax_staged_grid_kernel(const float* x, float* y, int64_t M, int64_t N, int64
   const int64_t items = (M > row0) ? (M - row0 + R - 1) / R : 0;
   const int nf4 = (int)(seg_n >> 2);
   if (NS < 2 || NS > kMaxStages || seg_n <= 0 || seg_n * 4 > stage_stride ||
-      C > 32 * kMaxSlotsPerLane || nf4 > VEC * kPartialThreads) {  // uniform
+      C > 32 * kMaxSlotsPerLane || nf4 > VEC * kPartialThreads || me >= (int)gridDim.x) {
     if (threadIdx.x == 0) atomicOr(&g_device_error, kErrConfig);
     return;
   }
@@ -787,8 +796,8 @@ cudaError_t launch_softmax_staged_long(const rrs_plan& p, const float* x, float*
 }
 
 cudaError_t launch_softmax_staged_grid(const rrs_plan& p, const float* x, float* y, int64_t M,
-                                       int64_t N, const Layout& l, void* workspace, uint32_t ticket,
-                                       int fault, unsigned* host_err, cudaStream_t s) {
+                                       int64_t N, const Layout& l, void* workspace, int fault,
+                                       unsigned* host_err, cudaStream_t s) {
   if (p.threads != kGThreads) return cudaErrorInvalidConfiguration;
   // segments of up to 4 float4 per thread run partials two items ahead (three
   // register sets); longer ones, up to 8 float4, one item ahead
@@ -808,21 +817,21 @@ cudaError_t launch_softmax_staged_grid(const rrs_plan& p, const float* x, float*
   // their work in arrival order instead (see the kernel).  Every wait is
   // still bounded: if one runs out, the kernel sets the device error word
   // and `host_err`, and later calls report RRS_ERR_TIMEOUT.
-  unsigned* arrivals = static_cast<unsigned*>(workspace);
+  auto* arrivals = static_cast<unsigned long long*>(workspace);
   uint64_t* slots = reinterpret_cast<uint64_t*>(static_cast<unsigned char*>(workspace) + kGridArrivalBytes);
   const int32_t C = (int32_t)p.ctas_per_row;
   const dim3 grid((unsigned)p.grid), block(kGThreads);
   const size_t smem = (size_t)p.smem_bytes;
   if (p.vec == 2)
     return launch_pdl(k2, grid, block, smem, s, 0, x, y, M, N, l.ldx, l.ldy, p.chunk, C,
-                      p.rows_per_cta, p.stages, p.tile * 4, arrivals, slots, ticket, (int32_t)fault,
+                      p.rows_per_cta, p.stages, p.tile * 4, arrivals, slots, (int32_t)fault,
                       (int32_t)l.log_out, host_err);
   if (p.vec == 4)
     return launch_pdl(k4, grid, block, smem, s, 0, x, y, M, N, l.ldx, l.ldy, p.chunk, C,
-                      p.rows_per_cta, p.stages, p.tile * 4, arrivals, slots, ticket, (int32_t)fault,
+                      p.rows_per_cta, p.stages, p.tile * 4, arrivals, slots, (int32_t)fault,
                       (int32_t)l.log_out, host_err);
   return launch_pdl(k8, grid, block, smem, s, 0, x, y, M, N, l.ldx, l.ldy, p.chunk, C,
-                    p.rows_per_cta, p.stages, p.tile * 4, arrivals, slots, ticket, (int32_t)fault,
+                    p.rows_per_cta, p.stages, p.tile * 4, arrivals, slots, (int32_t)fault,
                     (int32_t)l.log_out, host_err);
 }
 

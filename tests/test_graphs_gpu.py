@@ -1,0 +1,84 @@
+"""CUDA graphs: the hot-path calls captured once and replayed.
+
+A caller that captures softmax_rows or row_sum in a CUDA graph replays the
+same kernel arguments every time.  The split-row grid path draws a fresh
+ticket for every launch on the device, so a replay never takes a (max, sum)
+partial left by the previous replay for one of its own; to show it, x changes
+between replays (a stale partial would then give a wrong row).  Each path's
+first call runs before the capture: it allocates the path's workspace (and
+the grid path's host error word), which a capture may not do.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+
+import row_reduction_softmax_gb300 as rrs
+import workloads
+from gpu_helpers import check_every_row, check_row_sum, check_softmax
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _auto_path(lib):
+    rrs.force_path("auto", "auto")
+    yield
+    rrs.force_path("auto", "auto")
+
+
+def _plan_path(M, N):
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    return rrs.plan_softmax(M, N, N, True, props.multi_processor_count,
+                            props.shared_memory_per_block_optin)["path_name"]
+
+
+@pytest.mark.parametrize("name,M,N,path", [("c1", 128, 256, "row_regs"), ("c3", 8, 32768, "cluster"),
+                                           ("c5", 32, 1 << 20, "grid"), ("c5", 6, 300001, "two_phase")])
+def test_softmax_replayed_from_a_graph(name, M, N, path):
+    x1 = workloads.matrix(workloads.WORKLOADS[name].with_shape(M, N))
+    x2 = np.flip(x1, axis=1).copy() * np.float32(-0.5)          # other values, other row maxima
+    if path == "two_phase":
+        rrs.force_path("two_phase")
+    else:
+        assert _plan_path(M, N) == path
+    x = torch.from_numpy(x1).cuda()
+    y = torch.empty_like(x)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        rrs.softmax_rows(x, y)                                   # allocations happen here, eagerly
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        rrs.softmax_rows(x, y)
+    for k, xh in enumerate([x1, x2, x1, x2, x2]):
+        x.copy_(torch.from_numpy(xh))
+        y.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert rrs.device_error() == 0
+        check_every_row(check_softmax, y, xh, f"{path} {M}x{N} replay {k}")
+    del g
+
+
+def test_row_sum_replayed_from_a_graph():
+    M, N = 4096, 32768
+    x1 = workloads.matrix(workloads.WORKLOADS["c3"])
+    x = torch.from_numpy(x1).cuda()
+    out = torch.empty(M, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        rrs.row_sum(x, out)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        rrs.row_sum(x, out)
+    for k, scale in enumerate([1.0, -0.5]):
+        xh = x1 * np.float32(scale)
+        x.copy_(torch.from_numpy(xh))
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        check_row_sum(out.cpu().numpy(), xh, f"row sum replay {k}")
+    del g
