@@ -41,6 +41,11 @@
  *   entries of other rows come out as exactly 0.
  * - Calls are thread-safe.  The split-row paths use a small per-(device,
  *   stream) workspace the library allocates on first use and keeps.
+ * - Calls can be captured in a CUDA graph once each path has run eagerly on
+ *   the capturing stream (the first call may allocate its workspace, which a
+ *   capture may not).  A captured call keeps using that stream's workspace:
+ *   do not replay the graph concurrently with other calls on the capturing
+ *   stream, or with another replay of it.
  */
 #ifndef RRS_H
 #define RRS_H
