@@ -42,10 +42,14 @@
  * - Calls are thread-safe.  The split-row paths use a small per-(device,
  *   stream) workspace the library allocates on first use and keeps.
  * - Calls can be captured in a CUDA graph once each path has run eagerly on
- *   the capturing stream (the first call may allocate its workspace, which a
- *   capture may not).  A captured call keeps using that stream's workspace:
- *   do not replay the graph concurrently with other calls on the capturing
- *   stream, or with another replay of it.
+ *   the capturing stream with at least the captured shape (the first call
+ *   may allocate its workspace, which a capture may not): a captured call
+ *   that would need to allocate returns RRS_ERR_UNSUPPORTED and enqueues
+ *   nothing.  A captured call keeps using that stream's workspace, which
+ *   the library then never frees before rrs_release_workspace(), even when
+ *   a later eager call grows it: do not replay the graph concurrently with
+ *   other calls on the capturing stream, with another replay of it, or
+ *   after rrs_release_workspace().
  */
 #ifndef RRS_H
 #define RRS_H
@@ -274,8 +278,10 @@ RRS_API const char* rrs_status_string(int status);
 /* The calling thread's last error message ("" if none). */
 RRS_API const char* rrs_last_error(void);
 
-/* Frees every cached workspace (after a device synchronisation).  Later
- * calls allocate again on demand.  Returns RRS_OK or RRS_ERR_CUDA. */
+/* Frees every cached workspace (after a device synchronisation), including
+ * those kept for CUDA graphs that captured calls (such graphs must not be
+ * replayed afterwards).  Later calls allocate again on demand.  Returns
+ * RRS_OK or RRS_ERR_CUDA. */
 RRS_API int rrs_release_workspace(void);
 
 /* Force a path for later calls from any thread (testing / measurement):

@@ -18,6 +18,7 @@
 #include <string>
 #include <tuple>
 #include <utility>
+#include <vector>
 
 #include "internal.h"
 #include "rrs.h"
@@ -123,13 +124,19 @@ constexpr int kMaxDevices = 64;
 std::atomic<unsigned*> g_host_err[kMaxDevices];      // host address of each device's word
 std::atomic<unsigned*> g_host_err_dev[kMaxDevices];  // the same word's device address
 
-// The device address of `dev`'s word, allocated on first use (under g_mu).
-int host_err_word(int dev, unsigned** dptr) {
+// The device address of `dev`'s word, allocated on first use (under g_mu;
+// refused during a stream capture on `s`, which may not allocate).
+bool capturing(cudaStream_t s);
+int host_err_word(int dev, cudaStream_t s, unsigned** dptr) {
   if (dev < 0 || dev >= kMaxDevices) return fail(RRS_ERR_INVALID_ARG, "device ordinal out of range");
   if (unsigned* d = g_host_err_dev[dev].load(std::memory_order_acquire)) {
     *dptr = d;
     return RRS_OK;
   }
+  if (capturing(s))
+    return fail(RRS_ERR_UNSUPPORTED,
+                "the first grid-path call on a device allocates pinned host memory, which a stream "
+                "capture cannot: make an eager call first");
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_host_err_dev[dev].load()) {
     void* p = nullptr;
@@ -173,21 +180,52 @@ void host_err_clear(int dev) {
 // kind's kernels keep their own launch counter and tickets in it).
 enum WorkspaceKind { kWsTwoPhase = 0, kWsGrid = 1, kWsRowSum = 2 };
 
+//
+// Under stream capture: a call that needs more workspace than the stream has
+// is refused (a capture may not allocate; make an eager call of the shape on
+// that stream first), and a workspace handed to a captured call is never
+// freed when it later grows -- a graph may still replay into it -- but kept
+// until rrs_release_workspace().
 struct Workspace {
   void* ptr = nullptr;
   size_t bytes = 0;
+  bool captured = false;   // handed to a call during a stream capture
 };
 std::map<std::tuple<int, uintptr_t, int>, Workspace> g_workspaces;
+std::vector<std::pair<int, void*>> g_retired;   // (device, buffer) a captured graph may still use
+
+bool capturing(cudaStream_t s) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  return cs != cudaStreamCaptureStatusNone;
+}
 
 int get_workspace(int dev, cudaStream_t s, int kind, size_t bytes, void** ptr) {
+  const bool cap = capturing(s);
   std::lock_guard<std::mutex> lock(g_mu);
   Workspace& w = g_workspaces[{dev, reinterpret_cast<uintptr_t>(s), kind}];
   if (w.bytes < bytes) {
+    if (cap)
+      return fail(RRS_ERR_UNSUPPORTED,
+                  "this call needs a larger workspace, which a stream capture cannot allocate: make an "
+                  "eager call of this shape on the capturing stream first");
     if (w.ptr) {
-      cudaError_t e = cudaFreeAsync(w.ptr, s);
+      if (w.captured) {
+        g_retired.emplace_back(dev, w.ptr);
+      } else {
+        cudaError_t e = cudaFreeAsync(w.ptr, s);
+        if (e != cudaSuccess) {
+          w.ptr = nullptr;
+          w.bytes = 0;
+          return fail_cuda(e, "cudaFreeAsync(workspace)");
+        }
+      }
       w.ptr = nullptr;
       w.bytes = 0;
-      if (e != cudaSuccess) return fail_cuda(e, "cudaFreeAsync(workspace)");
+      w.captured = false;
     }
     const size_t want = std::max<size_t>(round_up((int64_t)bytes, 1 << 16), 1 << 16);
     cudaError_t e = cudaMallocAsync(&w.ptr, want, s);
@@ -200,6 +238,7 @@ int get_workspace(int dev, cudaStream_t s, int kind, size_t bytes, void** ptr) {
     if (e != cudaSuccess) return fail_cuda(e, "cudaMemsetAsync(workspace)");
     w.bytes = want;
   }
+  if (cap) w.captured = true;
   *ptr = w.ptr;
   return RRS_OK;
 }
@@ -767,7 +806,7 @@ RRS_API int softmax_rows_ex(const float* x, int64_t ldx, float* y, int64_t ldy, 
     case RRS_PATH_GRID: {
       void* ws = nullptr;
       unsigned* herr = nullptr;
-      if ((st = host_err_word(dev, &herr)) != RRS_OK) return st;
+      if ((st = host_err_word(dev, s, &herr)) != RRS_OK) return st;
       if ((st = get_workspace(dev, s, kWsGrid, (size_t)plan.workspace_bytes, &ws)) != RRS_OK) return st;
       e = launch_softmax_staged_grid(plan, x, y, M, N, l, ws, g_fault.load(), herr, s);
       break;
@@ -1028,6 +1067,14 @@ RRS_API int rrs_release_workspace(void) {
     }
   }
   g_workspaces.clear();
+  for (auto& r : g_retired) {
+    if (cudaSetDevice(r.first) == cudaSuccess) {
+      cudaError_t e = cudaDeviceSynchronize();
+      if (e == cudaSuccess) e = cudaFree(r.second);
+      if (e != cudaSuccess) status = fail_cuda(e, "rrs_release_workspace");
+    }
+  }
+  g_retired.clear();
   (void)cudaSetDevice(cur);
   return status;
 }

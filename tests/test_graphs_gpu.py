@@ -82,3 +82,46 @@ def test_row_sum_replayed_from_a_graph():
         torch.cuda.synchronize()
         check_row_sum(out.cpu().numpy(), xh, f"row sum replay {k}")
     del g
+
+
+@pytest.mark.filterwarnings("ignore:The CUDA Graph is empty")   # the refused call captured nothing
+def test_capture_refuses_to_allocate_and_keeps_captured_workspaces():
+    """A captured call that would need a larger workspace is refused (nothing
+    is enqueued); a workspace a graph captured stays valid when a later eager
+    call on the same stream grows it."""
+    small = workloads.matrix(workloads.WORKLOADS["c5"].with_shape(2, 1 << 18))
+    big = workloads.matrix(workloads.WORKLOADS["c5"].with_shape(64, 1 << 20))   # slots past 64 KiB
+    assert _plan_path(2, 1 << 18) == "grid" and _plan_path(64, 1 << 20) == "grid"
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    ws = [rrs.plan_softmax(M, N, N, True, props.multi_processor_count,
+                           props.shared_memory_per_block_optin)["workspace_bytes"]
+          for M, N in ((2, 1 << 18), (64, 1 << 20))]
+    assert ws[0] <= 65536 < ws[1]                       # the smallest workspace is 64 KiB
+    xs, xb = torch.from_numpy(small).cuda(), torch.from_numpy(big).cuda()
+    ys, yb = torch.empty_like(xs), torch.empty_like(xb)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        rrs.softmax_rows(xs, ys)                        # this stream's grid workspace: small
+    torch.cuda.synchronize()
+    g_bad = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_bad, stream=s):
+        with pytest.raises(rrs.RRSError) as e:
+            rrs.softmax_rows(xb, yb)                    # would grow the workspace inside the capture
+    assert e.value.status == 6
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        rrs.softmax_rows(xs, ys)                        # captured: uses the small workspace
+    with torch.cuda.stream(s):
+        rrs.softmax_rows(xb, yb)                        # eager: grows the workspace (the old one is kept)
+    torch.cuda.synchronize()
+    assert rrs.device_error() == 0
+    check_every_row(check_softmax, yb, big, "eager call after growth")
+    for k, xh in enumerate([small, np.flip(small, axis=1).copy()]):
+        xs.copy_(torch.from_numpy(xh))
+        ys.fill_(float("nan"))
+        g.replay()                                      # still replays into the kept workspace
+        torch.cuda.synchronize()
+        assert rrs.device_error() == 0
+        check_every_row(check_softmax, ys, xh, f"replay {k} after growth")
+    del g, g_bad
