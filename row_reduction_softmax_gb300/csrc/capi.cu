@@ -107,8 +107,6 @@ int device_info(int dev, DeviceInfo* out) {
   if (e == cudaSuccess)
     e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.cluster_launch, cudaDevAttrClusterLaunch, dev);
-  if (e == cudaSuccess)
-    e = cudaDeviceGetAttribute(&d.coop_launch, cudaDevAttrCooperativeLaunch, dev);
   if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
   g_devices[dev] = d;
   *out = d;
@@ -382,8 +380,8 @@ bool plan_staged_long(int64_t M, int64_t N, int sm_count, int smem_optin, rrs_pl
 // holds at least 2 stages.  C minimises rounds x (per-SM segment time + a
 // fixed per-segment cost).
 
-bool plan_grid(int64_t M, int64_t N, int sm_count, int smem_optin, int coop_ok, rrs_plan* p) {
-  if (N % 4 != 0 || !coop_ok) return false;
+bool plan_grid(int64_t M, int64_t N, int sm_count, int smem_optin, rrs_plan* p) {
+  if (N % 4 != 0) return false;
   const int64_t budget = staged_budget(smem_optin);
   const int64_t kGridMaxSegFloats = 8 * 4 * (int64_t)grid_partial_threads();
   double best = 1e300;
@@ -427,7 +425,7 @@ bool plan_grid(int64_t M, int64_t N, int sm_count, int smem_optin, int coop_ok, 
 }
 
 int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_count,
-                      int smem_optin, int cluster_ok, int coop_ok, int forced, rrs_plan* p) {
+                      int smem_optin, int cluster_ok, int forced, rrs_plan* p) {
   std::memset(p, 0, sizeof(*p));
   if (M < 0 || N < 0 || ld < 1 || ld < N || sm_count < 1)
     return fail(RRS_ERR_INVALID_ARG, "bad shape or device description");
@@ -452,7 +450,7 @@ int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_co
       plan_row_regs(M, N, sm_count, p);
     } else if (cluster_ok && plan_cluster(M, N, &c)) {
       *p = c;
-    } else if (plan_grid(M, N, sm_count, smem_optin, coop_ok, p)) {
+    } else if (plan_grid(M, N, sm_count, smem_optin, p)) {
     } else {
       plan_two_phase(M, N, sm_count, p);
     }
@@ -471,12 +469,12 @@ int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_co
       }
       return fail(RRS_ERR_UNSUPPORTED, "ROW_STAGED needs 16-byte alignment, N % 4 == 0, N <= 32912");
     case RRS_PATH_GRID:
-      if (vector_ok && plan_grid(M, N, sm_count, smem_optin, coop_ok, p)) {
+      if (vector_ok && plan_grid(M, N, sm_count, smem_optin, p)) {
         p->cluster = 1;
         p->vector_io = 1;
         return RRS_OK;
       }
-      return fail(RRS_ERR_UNSUPPORTED, "GRID needs 16-byte alignment, N % 4 == 0, cooperative launch");
+      return fail(RRS_ERR_UNSUPPORTED, "GRID needs 16-byte alignment and N % 4 == 0");
     case RRS_PATH_ROW_REGS:
       if (!row_regs_fits(N)) return fail(RRS_ERR_UNSUPPORTED, "ROW_REGS needs N <= 32768");
       plan_row_regs(M, N, sm_count, p, vector_ok != 0);
@@ -712,8 +710,8 @@ RRS_API int rrs_inject_fault(int kind) {
 RRS_API int rrs_plan_softmax(int64_t M, int64_t N, int64_t ld, int vector_ok_flag, int sm_count,
                              int smem_optin, rrs_plan* plan) {
   if (!plan) return RRS_ERR_INVALID_ARG;
-  return plan_softmax_impl(M, N, ld, vector_ok_flag, sm_count, smem_optin, 1, 1,
-                           g_force_softmax.load(), plan);
+  return plan_softmax_impl(M, N, ld, vector_ok_flag, sm_count, smem_optin, 1, g_force_softmax.load(),
+                           plan);
 }
 
 RRS_API int rrs_plan_row_sum(int64_t M, int64_t N, int64_t ld, int vector_ok_flag, int sm_count,
@@ -782,7 +780,7 @@ RRS_API int softmax_rows_ex(const float* x, int64_t ldx, float* y, int64_t ldy, 
   const bool vec = vector_ok(x, y, ldx) && ldy % 4 == 0;
   rrs_plan plan;
   st = plan_softmax_impl(M, N, std::max(ldx, ldy), vec ? 1 : 0, info.sm_count, info.smem_optin,
-                         info.cluster_launch, info.coop_launch, g_force_softmax.load(), &plan);
+                         info.cluster_launch, g_force_softmax.load(), &plan);
   if (st != RRS_OK) return st;
   Layout l;
   l.ldx = ldx;

@@ -33,7 +33,6 @@ struct DeviceInfo {
   int sm_count = 0;
   int smem_optin = 0;       // max dynamic shared memory per CTA (opt-in), bytes
   int cluster_launch = 0;   // thread-block clusters supported
-  int coop_launch = 0;      // cooperative launch supported
 };
 
 // Row strides of x and y (elements) and the output form: 0 = softmax,
