@@ -30,9 +30,10 @@ The line carries, besides the contract's keys:
                 the same way, and the fused attention forward (TFLOP/s against
                 the measured bf16 tensor peak)
   clocks        SM clock and clock-event reasons sampled during the timed region
-  summary       last, one short entry per suite / variant row (time per call
-                and fraction of the peak), so that a reader of only the end of
-                the line still sees every row
+  summary       last, one short entry per suite / variant row (time per call,
+                fraction of the peak and, for the softmax rows, the time of a
+                plain device copy of the same bytes), so that a reader of only
+                the end of the line still sees every row
 
 ``--impl reference`` times the oracle instead, on the same metric and config.
 """
@@ -601,6 +602,19 @@ def run_suite(args, torch, rrs, dev, rank):
         torch.cuda.synchronize()
         ms = ev0.elapsed_time(ev1) / args.suite_steps
         gbs = alg / (ms / 1e3) / 1e9
+        copy_ms = None
+        if op == "softmax":
+            # context: torch's device copy of the same bytes (y <- x) over the same
+            # rotating buffers, outside the timed region above
+            for k in range(3):
+                ys[k % npairs].copy_(xs[k % npairs])
+            torch.cuda.synchronize()
+            ev0.record(stream)
+            for k in range(args.suite_steps):
+                ys[k % npairs].copy_(xs[k % npairs])
+            ev1.record(stream)
+            torch.cuda.synchronize()
+            copy_ms = ev0.elapsed_time(ev1) / args.suite_steps
         entry = {"workload": name, "op": op, "M": M, "N": N, "path": plan["path_name"],
                  "kernel": kernel_of(plan),
                  "grid": plan["grid"], "threads": plan["threads"], "cluster": plan["cluster"],
@@ -608,9 +622,16 @@ def run_suite(args, torch, rrs, dev, rank):
                  "frac_of_8tbs": gbs / ROOFLINE_GBS, "frac_of_peak": gbs / peak,
                  "peak_kind": f"of {peak_kind}", "calls_timed": args.suite_steps,
                  "l2": f"{npairs} rotating pair(s)"}
+        if copy_ms is not None:
+            entry["copy_us"] = copy_ms * 1e3
+            entry["vs_copy"] = copy_ms / ms
         if rank == 0:
+            # parity of the softmax's own output: one more call on pair 0
+            if copy_ms is not None:
+                fn(xs[0].data_ptr(), ys[0].data_ptr(), M, N, N, sh)
+                torch.cuda.synchronize()
             rows = sampled_rows(M, 6, w.seed)
-            last = ys[(args.suite_steps - 1) % npairs]
+            last = ys[0] if copy_ms is not None else ys[(args.suite_steps - 1) % npairs]
             entry["parity"] = (oracle_parity_softmax(last, w, rows) if op == "softmax"
                                else oracle_parity_row_sum(last, w, rows))
         entries.append(entry)
@@ -729,6 +750,8 @@ def summary(out: dict) -> dict:
     for e in out.get("suite", []) + out.get("variants", []):
         frac = e["roofline"]["frac"] if "roofline" in e else e["frac_of_peak"]
         rows[f"{e['workload']}:{e['op']}"] = [round(e["ms_per_call"] * 1e3, 2), round(frac, 3)]
+        if "copy_us" in e:
+            rows[f"{e['workload']}:{e['op']}"].append(round(e["copy_us"], 2))
     return rows
 
 
