@@ -67,6 +67,14 @@ def test_inject_fault_rejects_unknown(lib):
     assert lib.rrs_inject_fault(0) == OK
 
 
+def test_occupy_rejects_bad_arguments_before_any_gpu_call(lib):
+    """The SM-holding test kernel is bounded: at most 0.2 s, at least one CTA,
+    no negative sizes -- refused before the library touches a device."""
+    for ctas, smem, ns in [(0, 0, 1000), (-1, 0, 1000), (70000, 0, 1000), (1, -1, 1000),
+                           (1, 0, -1), (1, 0, 200_000_001)]:
+        assert lib.rrs_test_occupy(ctas, smem, ns, None) == INVALID, (ctas, smem, ns)
+
+
 def test_force_path_rejects_unknown(lib):
     assert lib.rrs_force_path(99, -1) == INVALID
     assert lib.rrs_force_path(-1, 99) == INVALID
