@@ -120,6 +120,32 @@ def test_special_values(path, N):
     assert y[2, 0] == 1.0 and np.all(y[2, 1:] == 0.0)
 
 
+@pytest.mark.parametrize("path,N", [(p, N) for N in [6, 1003, 5000, 40000, 300000] for p in PATHS
+                                    if supports(p, N, N)])
+def test_extreme_magnitudes_and_tail_maxima(path, N):
+    """Values near fp32's limits and maxima in awkward places, on every path:
+    x - m overflowing to -inf (its exp is 0, as the true value is), a row at
+    3.4e38, subnormal rows, a maximum only in the ragged tail or only in the
+    first column, a row of huge negative values."""
+    rng = np.random.default_rng(N + 7)
+    x = rng.normal(0, 3, size=(8, N)).astype(np.float32)
+    x[0, ::2] = 3.0e38                          # x - m = -6e38 overflows to -inf: exactly 0
+    x[0, 1::2] = -3.0e38
+    x[1, :] = np.float32(3.4e38)                # the largest magnitudes, all equal: uniform
+    x[2, :] = (np.arange(N) % 7 + 1).astype(np.float32) * np.float32(1e-40)   # subnormals
+    x[3, N - 1] = 20.0                          # the maximum only in the last column
+    x[4, 0] = 20.0                              # ... only in the first
+    x[5, :] = np.float32(-1e30) + x[5]          # huge negative: the noise rounds away, uniform
+    x[6, :] = -np.inf
+    x[6, N // 3] = np.float32(-1e30)            # one finite entry among -inf
+    x[7, :] = np.float32(2.0) ** -126           # the smallest normal, all equal
+    y, guards = run(x, N, N, path)
+    check_softmax(y, x, f"{path} extremes N={N}")
+    assert guards
+    assert np.all(y[1] == y[1][0]) and np.all(y[5] == y[5][0]) and np.all(y[7] == y[7][0])
+    assert y[6, N // 3] == 1.0 and np.count_nonzero(y[6]) == 1
+
+
 @pytest.mark.parametrize("path", PATHS)
 def test_shift_invariance_on_gpu(path):
     N = 40000 if path in ("cluster", "grid") else 4096
