@@ -252,7 +252,7 @@ __device__ __forceinline__ uint64_t exp_shifted2(float va, float vb, uint64_t ne
 template <bool LOG, int MINB>
 __global__ void __launch_bounds__(kCT, MINB)
 softmax_cols_band_kernel(const float* x, float* y, int64_t M, int64_t N, int64_t ldx, int64_t ldy) {
-  __shared__ MaxSum red[kGroups][kBand];
+  __shared__ MaxSum red[kCW][kBand];   // per warp, after the shuffle merge
   __shared__ MaxSum part[kBand];   // this CTA's per-column (m_c, s_c), read by its peers
   __shared__ MaxSum whole[kBand];  // the merged pair of each column
 
@@ -333,13 +333,29 @@ softmax_cols_band_kernel(const float* x, float* y, int64_t M, int64_t N, int64_t
       f2_unpack(s2[1], p[2].s, p[3].s);
     }
   }
-  // ---- merge: the CTA's 32 row groups (fixed order), then the cluster's ranks ----
+  // ---- merge: a warp's 4 row groups (lanes l, l ^ 8, l ^ 16, l ^ 24 hold
+  // the same columns) by shuffles, the CTA's 8 warps in order, then the
+  // cluster's ranks: a fixed order, and merge is commutative, so the lanes
+  // of a column agree bit for bit ----
 #pragma unroll
-  for (int k = 0; k < 4; ++k) red[g][4 * slot + k] = p[k];
+  for (int k = 0; k < 4; ++k) {
+#pragma unroll
+    for (int o = kLPR; o < 32; o <<= 1) {
+      MaxSum q;
+      q.m = __shfl_xor_sync(kFullMask, p[k].m, o);
+      q.s = __shfl_xor_sync(kFullMask, p[k].s, o);
+      p[k] = merge(p[k], q);
+    }
+  }
+  if (lane < kLPR) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) red[warp][4 * slot + k] = p[k];
+  }
   __syncthreads();
   if (tid < kBand) {
     MaxSum q{kNeg, 0.f};
-    for (int k = 0; k < kGroups; ++k) q = merge(q, red[k][tid]);
+#pragma unroll
+    for (int k = 0; k < kCW; ++k) q = merge(q, red[k][tid]);
     part[tid] = q;
   }
   cluster_arrive_release();  // publish part[] to the cluster
