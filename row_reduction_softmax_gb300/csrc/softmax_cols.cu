@@ -359,6 +359,25 @@ softmax_cols_band_kernel(const float* x, float* y, int64_t M, int64_t N, int64_t
     part[tid] = q;
   }
   cluster_arrive_release();  // publish part[] to the cluster
+  // pass 2's first batch does not depend on the exchange: its loads are in
+  // flight while the cluster barrier completes
+  auto load_batch2 = [&](float4 (&a)[kBU], int64_t r, const float* xr) {
+    if (whole_batch(r)) {
+      const float* q = xr;
+#pragma unroll
+      for (int u = 0; u < kBU; ++u, q += xstep) a[u] = load_stream(reinterpret_cast<const float4*>(q));
+    } else {
+#pragma unroll
+      for (int u = 0; u < kBU; ++u) {
+        const int64_t ru = r + (int64_t)u * kGroups;
+        if (ru < r1) a[u] = load_row(ru, false);
+      }
+    }
+  };
+  const int64_t rfirst = r0 + g;
+  const bool any2 = live_col && rfirst < r1;
+  float4 a2[kBU];
+  if (any2) load_batch2(a2, rfirst, x + rfirst * ldx + j0);
   cluster_wait_acquire();    // every peer's part[] is visible
   if (tid < kBand) {
     MaxSum q{kNeg, 0.f};
@@ -394,31 +413,28 @@ softmax_cols_band_kernel(const float* x, float* y, int64_t M, int64_t N, int64_t
     }
     return o;
   };
-  if (live_col) {
-    const float* xr = x + (r0 + g) * ldx + j0;
-    float* yr = y + (r0 + g) * ldy + j0;
-    for (int64_t r = r0 + g; r < r1; r += (int64_t)kBU * kGroups, xr += kBU * xstep, yr += kBU * ystep) {
-      float4 a[kBU];
+  if (any2) {
+    int64_t r = rfirst;
+    const float* xr = x + rfirst * ldx + j0;
+    float* yr = y + rfirst * ldy + j0;
+    for (;;) {   // a2 holds the batch of rows r
       if (whole_batch(r)) {
-        const float* q = xr;
-#pragma unroll
-        for (int u = 0; u < kBU; ++u, q += xstep) a[u] = load_stream(reinterpret_cast<const float4*>(q));
         float* o = yr;
 #pragma unroll
-        for (int u = 0; u < kBU; ++u, o += ystep) store_stream(reinterpret_cast<float4*>(o), normalise(a[u]));
+        for (int u = 0; u < kBU; ++u, o += ystep) store_stream(reinterpret_cast<float4*>(o), normalise(a2[u]));
       } else {
 #pragma unroll
         for (int u = 0; u < kBU; ++u) {
           const int64_t ru = r + (int64_t)u * kGroups;
-          if (ru < r1) a[u] = load_row(ru, false);
-        }
-#pragma unroll
-        for (int u = 0; u < kBU; ++u) {
-          const int64_t ru = r + (int64_t)u * kGroups;
           if (ru >= r1) continue;
-          store_cols<true>(y + ru * ldy, j0, N, normalise(a[u]));
+          store_cols<true>(y + ru * ldy, j0, N, normalise(a2[u]));
         }
       }
+      r += (int64_t)kBU * kGroups;
+      if (r >= r1) break;
+      xr += kBU * xstep;
+      yr += kBU * ystep;
+      load_batch2(a2, r, xr);
     }
   }
   cluster_wait_acquire();  // peers finished reading part[] before this CTA exits
