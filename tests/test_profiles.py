@@ -63,20 +63,23 @@ def steady(name: str) -> dict:
 
 # summary file, bytes of x, bytes of y written (the softmax writes M N floats,
 # the row sum M), the DRAM writes expected at least (fraction of y: c2's 32 MiB
-# of y partly stay dirty in the L2 between the bench's launches)
+# of y partly stay dirty in the L2 between the bench's launches), the reads
+# allowed above the bytes of x (fraction: the column band kernel re-reads x,
+# the second time mostly from the L2)
 STEADY = [
-    ("softmax_cluster_c3.md", 4 * 4096 * 32768, 4 * 4096 * 32768, 0.99),
-    ("softmax_row_regs_c2.md", 4 * 8192 * 1024, 4 * 8192 * 1024, 0.9),
-    ("softmax_row_regs_c4.md", 4 * 16384 * 4096, 4 * 16384 * 4096, 0.97),
-    ("softmax_staged_grid_c5.md", 4 * 32 * 1048576, 4 * 32 * 1048576, 0.95),
-    ("row_reduce_rows_c3.md", 4 * 4096 * 32768, 4 * 4096, 0.0),
+    ("softmax_cluster_c3.md", 4 * 4096 * 32768, 4 * 4096 * 32768, 0.99, 0.01),
+    ("softmax_row_regs_c2.md", 4 * 8192 * 1024, 4 * 8192 * 1024, 0.9, 0.01),
+    ("softmax_row_regs_c4.md", 4 * 16384 * 4096, 4 * 16384 * 4096, 0.97, 0.01),
+    ("softmax_staged_grid_c5.md", 4 * 32 * 1048576, 4 * 32 * 1048576, 0.95, 0.01),
+    ("row_reduce_rows_c3.md", 4 * 4096 * 32768, 4 * 4096, 0.0, 0.01),
+    ("softmax_cols_band_cols_c4.md", 4 * 4096 * 16384, 4 * 4096 * 16384, 0.97, 0.10),
 ]
 
 
-@pytest.mark.parametrize("name,x_bytes,y_bytes,min_write", STEADY)
-def test_steady_state_reads_x_once_and_writes_y_once(name, x_bytes, y_bytes, min_write):
+@pytest.mark.parametrize("name,x_bytes,y_bytes,min_write,read_slack", STEADY)
+def test_steady_state_reads_x_once_and_writes_y_once(name, x_bytes, y_bytes, min_write, read_slack):
     st = steady(name)
-    assert 0.98 * x_bytes <= st["read"] <= 1.01 * x_bytes, f"{name}: {st['read'] / 1e6:.2f} MB read"
+    assert 0.98 * x_bytes <= st["read"] <= (1 + read_slack) * x_bytes, f"{name}: {st['read'] / 1e6:.2f} MB read"
     # every store lands in the L2 once: the sectors written are the bytes of y
     assert abs(st["l2_write"] - y_bytes) <= max(0.001 * y_bytes, 0.2e6), f"{name}: {st['l2_write'] / 1e6:.2f} MB"
     assert min_write * y_bytes <= st["write"] <= 1.01 * y_bytes + 2e6, f"{name}: {st['write'] / 1e6:.2f} MB"
