@@ -178,7 +178,6 @@ void host_err_clear(int dev) {
 // kind's kernels keep their own launch counter and tickets in it).
 enum WorkspaceKind { kWsTwoPhase = 0, kWsGrid = 1, kWsRowSum = 2 };
 
-//
 // Under stream capture: a call that needs more workspace than the stream has
 // is refused (a capture may not allocate; make an eager call of the shape on
 // that stream first), and a workspace handed to a captured call is never
