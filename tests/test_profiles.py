@@ -73,6 +73,7 @@ STEADY = [
     ("softmax_staged_grid_c5.md", 4 * 32 * 1048576, 4 * 32 * 1048576, 0.95, 0.01),
     ("row_reduce_rows_c3.md", 4 * 4096 * 32768, 4 * 4096, 0.0, 0.01),
     ("softmax_cols_band_cols_c4.md", 4 * 4096 * 16384, 4 * 4096 * 16384, 0.97, 0.10),
+    ("gelu_kernel_gelu_16k.md", 4 * 16384 * 16384, 4 * 16384 * 16384, 0.99, 0.01),
 ]
 
 
@@ -115,3 +116,30 @@ def test_every_profiled_kernel_has_its_sources_listed():
                     seen += 1
                     assert m.group(1) in bench.KERNEL_SOURCES, f"{name}: {m.group(1)} has no source list"
     assert seen >= 6
+
+
+def test_every_traffic_figure_is_for_the_current_sources(lib):
+    """Each committed traffic line is keyed to its kernel's sources, the
+    shared device headers and the launch plan of its workload on a GB300
+    (152 SMs, 227 KB of shared memory per CTA): a kernel changed since its
+    counters were taken fails here until they are taken again."""
+    import bench
+    import row_reduction_softmax_gb300 as rrs
+    import workloads
+    pat = re.compile(r"traffic:\s+kernel=(\S+)\s+workload=(\S+)\s+bytes_per_launch=(\d+)\s+source=(\w+)")
+    for name in sorted(os.listdir(os.path.join(ROOT, "profiles"))):
+        with open(os.path.join(ROOT, "profiles", name)) as f:
+            for line in f:
+                m = pat.search(line)
+                if not m:
+                    continue
+                kernel, wl, _, source = m.groups()
+                plan = None
+                if wl in workloads.WORKLOADS:
+                    w = workloads.WORKLOADS[wl]
+                    planner = rrs.plan_row_sum if kernel == "row_reduce_rows_kernel" else rrs.plan_softmax
+                    plan = planner(w.M, w.N, w.N, True, 152, 232448)
+                elif kernel == "softmax_cols_band_kernel":
+                    w = workloads.VARIANT_WORKLOADS[wl]
+                    plan = rrs.plan_softmax_cols(w.M, w.N, w.N, True, 152, 232448)
+                assert bench.source_hash(kernel, plan) == source, f"{name}: {kernel} changed since its capture"
