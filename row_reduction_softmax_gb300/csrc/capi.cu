@@ -267,8 +267,10 @@ void plan_row_regs(int64_t M, int64_t N, int sm_count, rrs_plan* p, bool vector 
 
 bool row_regs_fits(int64_t N) { return N <= (int64_t)32 * 32 * 4 * 8; }
 
-bool plan_cluster(int64_t M, int64_t N, rrs_plan* p) {
-  const int64_t n4 = N >> 2;
+// vector: float4 slots plus an N % 4 tail in the last CTA; scalar: 4 scalars
+// per slot, so the slots cover N.
+bool plan_cluster(int64_t M, int64_t N, rrs_plan* p, bool vector = true) {
+  const int64_t n4 = vector ? (N >> 2) : ceil_div(N, 4);
   int vec = kClusterVec;
   int cs = pow2_ceil(std::max<int64_t>(1, ceil_div(n4, (int64_t)kSplitThreads * vec)));
   if (cs > kClusterMax) return false;
@@ -438,12 +440,17 @@ int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_co
     // Measured on GB300: registers win for rows that fit one CTA, the cluster
     // split for rows up to 16 CTAs' registers, the staged grid split beyond,
     // the two-phase split for what the grid cannot hold or align.
+    // Rows whose start or stride is not 16-byte aligned take the scalar
+    // forms of the register and cluster kernels; N % 4 != 0 the vector forms
+    // with a ragged tail (the grid split needs whole float4 segments).
     rrs_plan c;
     if (!vector_ok) {
       if (N <= kRowRegsAutoMaxN) plan_row_regs(M, N, sm_count, p, false);
+      else if (cluster_ok && plan_cluster(M, N, &c, false)) *p = c;
       else plan_two_phase(M, N, sm_count, p);
     } else if (N % 4 != 0) {
-      if (row_regs_fits(N)) plan_row_regs(M, N, sm_count, p);
+      if (N <= kRowRegsAutoMaxN) plan_row_regs(M, N, sm_count, p);
+      else if (cluster_ok && plan_cluster(M, N, &c)) *p = c;
       else plan_two_phase(M, N, sm_count, p);
     } else if (N <= kRowRegsAutoMaxN) {
       plan_row_regs(M, N, sm_count, p);
@@ -480,8 +487,9 @@ int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_co
       p->vector_io = vector_ok ? 1 : 0;
       return RRS_OK;
     case RRS_PATH_CLUSTER:
-      if (!vector_ok || !cluster_ok || !plan_cluster(M, N, p))
-        return fail(RRS_ERR_UNSUPPORTED, "CLUSTER needs 16-byte alignment, cluster launch and N <= 131072");
+      if (!cluster_ok || !plan_cluster(M, N, p, vector_ok != 0))
+        return fail(RRS_ERR_UNSUPPORTED, "CLUSTER needs cluster launch and N <= 131072");
+      p->vector_io = vector_ok ? 1 : 0;
       return RRS_OK;
     case RRS_PATH_TWO_PHASE:
       plan_two_phase(M, N, sm_count, p);

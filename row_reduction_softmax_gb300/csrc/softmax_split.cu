@@ -75,13 +75,33 @@ __device__ __forceinline__ void cluster_wait_acquire() {
 
 // ----------------------------------------------------------------- CLUSTER ---
 // Grid: clusters of `cs` CTAs along x; cluster k owns rows k, k + nclusters, ...
-// Rank r of a cluster owns float4 columns [r*seg4, min((r+1)*seg4, n4)) of the
-// row, seg4 = ceil(n4 / cs) <= VEC * kT; the last rank also owns the N % 4
-// scalar tail.  x, y 16-byte aligned, ldx % 4 == 0, ldy % 4 == 0.
+// V4: rank r of a cluster owns float4 columns [r*seg4, min((r+1)*seg4, n4))
+// of the row, seg4 = ceil(n4 / cs) <= VEC * kT; the last rank also owns the
+// N % 4 scalar tail; x, y 16-byte aligned, ldx % 4 == 0, ldy % 4 == 0.
+// Scalar (any alignment and stride): rank r owns columns [r*segs,
+// min((r+1)*segs, N)), segs = ceil(N / cs) <= 4 * VEC * kT, each thread four
+// scalars per register slot, so that every warp load is one contiguous run.
 // LOG writes log y = (x - m) - log(s) (a template parameter, so the softmax
 // instantiation keeps the register count that lets 4 CTAs share an SM).  In
 // place (x == y) is safe: a CTA reads its whole segment before writing it.
-template <int VEC, bool LOG>
+// Slot i of thread tid into the CTA's segment of the row: one float4 (V4),
+// or four scalars kT apart (the scalar layout above).
+template <bool V4>
+__device__ __forceinline__ void store_segment(float* yr, float4* yr4, int i, int tid, int b4, int e4, int bs,
+                                              int es, const float4& o) {
+  if constexpr (V4) {
+    const int c = b4 + i * kT + tid;
+    if (c < e4) store_stream(yr4 + c, o);
+  } else {
+    const int j = bs + 4 * i * kT + tid;
+    if (j < es) store_stream(yr + j, o.x);
+    if (j + kT < es) store_stream(yr + j + kT, o.y);
+    if (j + 2 * kT < es) store_stream(yr + j + 2 * kT, o.z);
+    if (j + 3 * kT < es) store_stream(yr + j + 3 * kT, o.w);
+  }
+}
+
+template <int VEC, bool LOG, bool V4>
 __global__ void __launch_bounds__(kT)
 softmax_cluster_kernel(const float* x, float* y, int64_t M, int32_t N, int64_t ldx, int64_t ldy) {
   __shared__ float red_m[kW];
@@ -102,7 +122,10 @@ softmax_cluster_kernel(const float* x, float* y, int64_t M, int32_t N, int64_t l
   const int seg4 = (n4 + cs - 1) / cs;
   const int b4 = rank * seg4;
   const int e4 = min(b4 + seg4, n4);
-  const bool has_tail = (rank == cs - 1) && (tid < rem);
+  const bool has_tail = V4 && (rank == cs - 1) && (tid < rem);
+  const int segs = (N + cs - 1) / cs;   // scalar layout
+  const int bs = rank * segs;
+  const int es = min(bs + segs, N);
   const float kNeg = neg_inf();
   pdl_entry();
 
@@ -113,12 +136,24 @@ softmax_cluster_kernel(const float* x, float* y, int64_t M, int32_t N, int64_t l
     float4* yr4 = reinterpret_cast<float4*>(yr);
 
     float4 v[VEC];
+    float t = kNeg;
+    if constexpr (V4) {
 #pragma unroll
-    for (int i = 0; i < VEC; ++i) {
-      const int c = b4 + i * kT + tid;
-      v[i] = (c < e4) ? load_stream(xr4 + c) : make_float4(kNeg, kNeg, kNeg, kNeg);
+      for (int i = 0; i < VEC; ++i) {
+        const int c = b4 + i * kT + tid;
+        v[i] = (c < e4) ? load_stream(xr4 + c) : make_float4(kNeg, kNeg, kNeg, kNeg);
+      }
+      t = has_tail ? load_stream(xr + 4 * n4 + tid) : kNeg;
+    } else {
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) {
+        const int j = bs + 4 * i * kT + tid;
+        v[i].x = (j < es) ? load_stream(xr + j) : kNeg;
+        v[i].y = (j + kT < es) ? load_stream(xr + j + kT) : kNeg;
+        v[i].z = (j + 2 * kT < es) ? load_stream(xr + j + 2 * kT) : kNeg;
+        v[i].w = (j + 3 * kT < es) ? load_stream(xr + j + 3 * kT) : kNeg;
+      }
     }
-    float t = has_tail ? load_stream(xr + 4 * n4 + tid) : kNeg;
 
     float mc = t;
 #pragma unroll
@@ -172,11 +207,9 @@ softmax_cluster_kernel(const float* x, float* y, int64_t M, int32_t N, int64_t l
       const float ls = logf(w.s);
 #pragma unroll
       for (int i = 0; i < VEC; ++i) {
-        const int c = b4 + i * kT + tid;
-        if (c < e4) {
-          store_stream(yr4 + c, make_float4(log_softmax_of(v[i].x, w.m, ls), log_softmax_of(v[i].y, w.m, ls),
-                                            log_softmax_of(v[i].z, w.m, ls), log_softmax_of(v[i].w, w.m, ls)));
-        }
+        const float4 o = make_float4(log_softmax_of(v[i].x, w.m, ls), log_softmax_of(v[i].y, w.m, ls),
+                                     log_softmax_of(v[i].z, w.m, ls), log_softmax_of(v[i].w, w.m, ls));
+        store_segment<V4>(yr, yr4, i, tid, b4, e4, bs, es, o);
       }
       if (has_tail) store_stream(yr + 4 * n4 + tid, log_softmax_of(t, w.m, ls));
     } else {
@@ -184,13 +217,9 @@ softmax_cluster_kernel(const float* x, float* y, int64_t M, int32_t N, int64_t l
       const float scale = bad ? __int_as_float(0x7fc00000)
                               : (empty ? 0.f : exp_shifted(mc, w.m) / w.s);
 #pragma unroll
-      for (int i = 0; i < VEC; ++i) {
-        const int c = b4 + i * kT + tid;
-        if (c < e4) {
-          store_stream(yr4 + c,
-                       make_float4(v[i].x * scale, v[i].y * scale, v[i].z * scale, v[i].w * scale));
-        }
-      }
+      for (int i = 0; i < VEC; ++i)
+        store_segment<V4>(yr, yr4, i, tid, b4, e4, bs, es,
+                          make_float4(v[i].x * scale, v[i].y * scale, v[i].z * scale, v[i].w * scale));
       if (has_tail) store_stream(yr + 4 * n4 + tid, t * scale);
     }
     cluster_wait_acquire();  // peers finished reading `part` before it is reused / freed
@@ -323,10 +352,10 @@ softmax_finalize_kernel(const float* x, float* y, const MaxSum* __restrict__ par
   }
 }
 
-template <int VEC, bool LOG>
+template <int VEC, bool LOG, bool V4>
 cudaError_t launch_cluster_vec(const rrs_plan& p, const float* x, float* y, int64_t M, int64_t N,
                                const Layout& l, cudaStream_t s) {
-  auto kern = softmax_cluster_kernel<VEC, LOG>;
+  auto kern = softmax_cluster_kernel<VEC, LOG, V4>;
   if (p.cluster > 8) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
@@ -341,11 +370,20 @@ cudaError_t launch_softmax_cluster(const rrs_plan& p, const float* x, float* y, 
                                    int64_t N, const Layout& l, cudaStream_t s) {
   if (p.threads != kT) return cudaErrorInvalidConfiguration;
   const bool lg = l.log_out != 0;
+  if (!p.vector_io) {
+    switch (p.vec) {
+      case 4: return lg ? launch_cluster_vec<4, true, false>(p, x, y, M, N, l, s)
+                        : launch_cluster_vec<4, false, false>(p, x, y, M, N, l, s);
+      case 8: return lg ? launch_cluster_vec<8, true, false>(p, x, y, M, N, l, s)
+                        : launch_cluster_vec<8, false, false>(p, x, y, M, N, l, s);
+      default: return cudaErrorInvalidConfiguration;
+    }
+  }
   switch (p.vec) {
-    case 4: return lg ? launch_cluster_vec<4, true>(p, x, y, M, N, l, s)
-                      : launch_cluster_vec<4, false>(p, x, y, M, N, l, s);
-    case 8: return lg ? launch_cluster_vec<8, true>(p, x, y, M, N, l, s)
-                      : launch_cluster_vec<8, false>(p, x, y, M, N, l, s);
+    case 4: return lg ? launch_cluster_vec<4, true, true>(p, x, y, M, N, l, s)
+                      : launch_cluster_vec<4, false, true>(p, x, y, M, N, l, s);
+    case 8: return lg ? launch_cluster_vec<8, true, true>(p, x, y, M, N, l, s)
+                      : launch_cluster_vec<8, false, true>(p, x, y, M, N, l, s);
     default: return cudaErrorInvalidConfiguration;
   }
 }

@@ -118,8 +118,21 @@ def test_planner_unaligned_takes_scalar_path(lib):
     p = plan(100, 1000, ld=1001, vector_ok=False)         # short rows: scalar warp-per-row
     assert p["path_name"] == "row_regs" and p["vector_io"] == 0
     assert p["vec"] * 32 * p["warps_per_row"] * 4 >= 1000
-    p = plan(100, 20000, ld=20001, vector_ok=False)       # long rows: scalar two-phase
+    p = plan(100, 20000, ld=20001, vector_ok=False)       # long rows: scalar cluster split
+    assert p["path_name"] == "cluster" and p["vector_io"] == 0
+    p = plan(100, 131075, ld=131075, vector_ok=False)     # beyond 16 CTAs' registers: scalar two-phase
     assert p["path_name"] == "two_phase" and p["vector_io"] == 0
+    p = plan(100, 50257, ld=50260)                          # aligned rows, N % 4 != 0: cluster with a tail
+    assert p["path_name"] == "cluster" and p["vector_io"] == 1
+
+
+@pytest.mark.parametrize("N", [16385, 20001, 32767, 50257, 65537, 100001, 131072])
+def test_scalar_cluster_plans_cover_the_row(lib, N):
+    p = plan(5, N, ld=N + 1, vector_ok=False)
+    assert p["path_name"] == "cluster" and p["vector_io"] == 0
+    cs = p["cluster"]
+    assert 1 <= cs <= 16 and p["grid"] == 5 * cs
+    assert -(-N // cs) <= 4 * p["vec"] * p["threads"]     # each CTA's scalar segment fits its slots
 
 
 @pytest.mark.parametrize("N", [1, 3, 5, 127, 129, 1023, 1025, 4097, 16383, 16384])

@@ -31,7 +31,7 @@ def supports(path: str, N: int, ld: int) -> bool:
     if path == "row_regs":
         return N <= 32768                      # scalar loads when not vector_ok
     if path == "cluster":
-        return vector_ok and N <= 131072
+        return N <= 131072                     # scalar loads when not vector_ok
     if path == "row_staged":
         return vector_ok and N % 4 == 0 and N <= 32912
     if path == "grid":
@@ -86,19 +86,44 @@ def test_leading_dimension_gap(path, M, N, gap):
 
 @pytest.mark.parametrize("M,N,ld,x_off,y_off", [(4, 1000, 1001, 0, 0), (3, 4096, 4096, 1, 0),
                                                 (3, 4096, 4096, 0, 3), (5, 33, 35, 2, 1),
-                                                (2, 40000, 40003, 1, 1)])
+                                                (2, 40000, 40003, 1, 1), (3, 50257, 50257, 0, 0),
+                                                (2, 16385, 16387, 0, 1), (2, 131072, 131073, 1, 2),
+                                                (2, 131075, 131075, 0, 0)])
 def test_unaligned_takes_scalar_path(M, N, ld, x_off, y_off):
+    """Rows whose start or stride is not 16-byte aligned: the scalar register
+    kernel up to 16384, the scalar cluster split up to 131072 (each CTA's
+    segment in four-scalar slots), the scalar two-phase split beyond."""
     x = recipe("c2", M, N)
     y, guards = run(x, N, ld, "auto", x_off, y_off)
     check_softmax(y, x, f"unaligned {M}x{N} ld={ld}")
     assert guards
+    want = "row_regs" if N <= 16384 else ("cluster" if N <= 131072 else "two_phase")
+    assert rrs.plan_softmax(M, N, ld, False, torch.cuda.get_device_properties(0).multi_processor_count)[
+        "path_name"] == want
     if N <= 32768:
         y, guards = run(x, N, ld, "row_regs", x_off, y_off)    # the scalar row kernel
         check_softmax(y, x, f"unaligned row_regs {M}x{N} ld={ld}")
         assert guards
-    with pytest.raises(rrs.RRSError) as e:
-        run(x, N, ld, "cluster", x_off, y_off)
-    assert e.value.status == 6
+    if N <= 131072:
+        y, guards = run(x, N, ld, "cluster", x_off, y_off)     # the scalar cluster kernel
+        check_softmax(y, x, f"unaligned cluster {M}x{N} ld={ld}")
+        assert guards
+    else:
+        with pytest.raises(rrs.RRSError) as e:
+            run(x, N, ld, "cluster", x_off, y_off)
+        assert e.value.status == 6
+
+
+@pytest.mark.parametrize("M,N,ld", [(3, 50257, 50260), (2, 16385, 16388), (2, 131073, 131076)])
+def test_ragged_long_rows_take_the_cluster_split(M, N, ld):
+    """Aligned rows with N % 4 != 0 past 16384 floats: the vector cluster
+    kernel with the ragged tail in its last CTA."""
+    x = recipe("c4", M, N)
+    assert rrs.plan_softmax(M, N, ld, True, torch.cuda.get_device_properties(0).multi_processor_count)[
+        "path_name"] == "cluster"
+    y, guards = run(x, N, ld, "auto")
+    check_softmax(y, x, f"ragged {M}x{N} ld={ld}")
+    assert guards
 
 
 @pytest.mark.parametrize("path,N", [(p, N) for N in [2, 8, 1024, 5000, 40000] for p in PATHS if supports(p, N, N)])

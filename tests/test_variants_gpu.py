@@ -389,3 +389,30 @@ def test_full_size_gelu():
     assert bool((resid <= 3e-5 * x.double().abs() + 1e-30).all())
     del x, y, y2, idx, resid
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------- the scalar cluster split ----
+
+@pytest.mark.parametrize("N,ldx,ldy,x_off,y_off", [(20000, 20001, 20003, 1, 2), (50257, 50257, 50260, 0, 0),
+                                                   (131071, 131073, 131071, 3, 0)])
+def test_scalar_cluster_specials_log_and_in_place(N, ldx, ldy, x_off, y_off):
+    """Long rows with unaligned starts or strides on the cluster split's
+    scalar form: special values, the log form, separate strides and in
+    place (same stride), every row against the oracle."""
+    rng = np.random.default_rng(N)
+    x = rng.normal(0, 3, size=(8, N)).astype(np.float32)
+    x[0] = -np.inf
+    x[1, :] = 7.25
+    x[2, 1:] = -np.inf
+    x[3, N // 2] = np.inf
+    x[4, N - 1] = np.nan
+    x[5, ::2] = -np.inf
+    x[6] += 1000.0
+    x[7, N - 1] = 88.0                         # the row's maximum in the last CTA's last column
+    for flags, check in ((0, check_softmax), (LOG, check_log_softmax)):
+        y, guards = run_ex(x, N, ldx, ldy, "cluster", flags, x_off=x_off, y_off=y_off)
+        check(y, x, f"scalar cluster N={N} flags={flags}")
+        assert guards
+    y, guards = run_ex(x, N, ldx, ldx, "cluster", 0, in_place=True, x_off=x_off)
+    check_softmax(y, x, f"scalar cluster in place N={N}")
+    assert guards
