@@ -33,7 +33,8 @@
  *   synchronising; results are ordered before later work on that stream.
  * - Any ld >= N and any 4-byte-aligned pointer is accepted.  The 128-bit
  *   vector paths run when x and y are 16-byte aligned and ld % 4 == 0;
- *   otherwise a scalar path gives the same results.
+ *   otherwise the scalar forms of the same single-pass kernels (rows up to
+ *   131072 floats) or of the two-phase split give the same results.
  * - Arguments are checked before anything is enqueued.  A failed launch
  *   returns RRS_ERR_CUDA and rrs_last_error() holds the runtime's message.
  * - Rows that contain +inf or NaN, or are entirely -inf, come out as NaN
