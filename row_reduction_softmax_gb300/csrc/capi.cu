@@ -267,16 +267,18 @@ void plan_row_regs(int64_t M, int64_t N, int sm_count, rrs_plan* p, bool vector 
 
 bool row_regs_fits(int64_t N) { return N <= (int64_t)32 * 32 * 4 * 8; }
 
-// vector: float4 slots plus an N % 4 tail in the last CTA; scalar: 4 scalars
-// per slot, so the slots cover N.
-bool plan_cluster(int64_t M, int64_t N, rrs_plan* p, bool vector = true) {
-  const int64_t n4 = vector ? (N >> 2) : ceil_div(N, 4);
+// mode 1 (vector): float4 slots plus an N % 4 tail in the last CTA; 0
+// (scalar): 4 scalars per slot, so the slots cover N; 2 (shifted window):
+// float4 slots over a window of up to N + 3 floats.
+bool plan_cluster(int64_t M, int64_t N, rrs_plan* p, int mode = 1) {
+  const int64_t n4 = mode == 1 ? (N >> 2) : (mode == 0 ? ceil_div(N, 4) : ceil_div(N + 3, 4));
   int vec = kClusterVec;
   int cs = pow2_ceil(std::max<int64_t>(1, ceil_div(n4, (int64_t)kSplitThreads * vec)));
   if (cs > kClusterMax) return false;
   // a cluster of one CTA per 4 KiB-aligned segment; shrink registers when the segment is short
   if (ceil_div(n4, cs) <= (int64_t)kSplitThreads * 4) vec = 4;
   p->path = RRS_PATH_CLUSTER;
+  p->vector_io = mode;
   p->vec = vec;
   p->warps_per_row = kSplitThreads / 32;
   p->threads = kSplitThreads;
@@ -425,13 +427,19 @@ bool plan_grid(int64_t M, int64_t N, int sm_count, int smem_optin, rrs_plan* p) 
   return true;
 }
 
-int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_count,
+// vector_ok: 1 = x and y 16-byte aligned with strides multiples of 4; 2 =
+// not, but misaligned alike (the same address mod 16 bytes, strides equal
+// mod 4), so every row of both can be read and written through one shifted
+// float4 window; 0 = neither.
+int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok_in, int sm_count,
                       int smem_optin, int cluster_ok, int forced, rrs_plan* p) {
   std::memset(p, 0, sizeof(*p));
-  if (M < 0 || N < 0 || ld < 1 || ld < N || sm_count < 1)
+  if (M < 0 || N < 0 || ld < 1 || ld < N || sm_count < 1 || vector_ok_in < 0 || vector_ok_in > 2)
     return fail(RRS_ERR_INVALID_ARG, "bad shape or device description");
+  const int vector_ok = vector_ok_in == 1 ? 1 : 0;
+  const int shift_mode = vector_ok_in == 2 ? 2 : 0;   // the cluster kernel's mode for unaligned rows
   p->cluster = 1;
-  p->vector_io = vector_ok ? 1 : 0;
+  p->vector_io = vector_ok;
   if (M == 0 || N == 0) {
     p->path = (forced == RRS_PATH_AUTO) ? RRS_PATH_ROW_REGS : forced;
     return RRS_OK;
@@ -446,7 +454,8 @@ int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_co
     rrs_plan c;
     if (!vector_ok) {
       if (N <= kRowRegsAutoMaxN) plan_row_regs(M, N, sm_count, p, false);
-      else if (cluster_ok && plan_cluster(M, N, &c, false)) *p = c;
+      else if (cluster_ok && shift_mode && plan_cluster(M, N, &c, shift_mode)) *p = c;
+      else if (cluster_ok && plan_cluster(M, N, &c, 0)) *p = c;   // a window of N + 3 may not fit: scalar
       else plan_two_phase(M, N, sm_count, p);
     } else if (N % 4 != 0) {
       if (N <= kRowRegsAutoMaxN) plan_row_regs(M, N, sm_count, p);
@@ -461,7 +470,7 @@ int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_co
       plan_two_phase(M, N, sm_count, p);
     }
     p->cluster = std::max(p->cluster, 1);
-    p->vector_io = vector_ok ? 1 : 0;
+    if (p->path != RRS_PATH_CLUSTER) p->vector_io = vector_ok;
     return RRS_OK;
   }
   const int path = forced;
@@ -487,9 +496,9 @@ int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_co
       p->vector_io = vector_ok ? 1 : 0;
       return RRS_OK;
     case RRS_PATH_CLUSTER:
-      if (!cluster_ok || !plan_cluster(M, N, p, vector_ok != 0))
+      if (!cluster_ok || !(plan_cluster(M, N, p, vector_ok ? 1 : shift_mode) ||
+                           (!vector_ok && plan_cluster(M, N, p, 0))))
         return fail(RRS_ERR_UNSUPPORTED, "CLUSTER needs cluster launch and N <= 131072");
-      p->vector_io = vector_ok ? 1 : 0;
       return RRS_OK;
     case RRS_PATH_TWO_PHASE:
       plan_two_phase(M, N, sm_count, p);
@@ -785,8 +794,10 @@ RRS_API int softmax_rows_ex(const float* x, int64_t ldx, float* y, int64_t ldy, 
   if ((st = device_info(dev, &info)) != RRS_OK) return st;
 
   const bool vec = vector_ok(x, y, ldx) && ldy % 4 == 0;
+  const bool alike = (reinterpret_cast<uintptr_t>(x) - reinterpret_cast<uintptr_t>(y)) % 16 == 0 &&
+                     (ldx - ldy) % 4 == 0;   // every row of x and of y misaligned the same way
   rrs_plan plan;
-  st = plan_softmax_impl(M, N, std::max(ldx, ldy), vec ? 1 : 0, info.sm_count, info.smem_optin,
+  st = plan_softmax_impl(M, N, std::max(ldx, ldy), vec ? 1 : (alike ? 2 : 0), info.sm_count, info.smem_optin,
                          info.cluster_launch, g_force_softmax.load(), &plan);
   if (st != RRS_OK) return st;
   Layout l;

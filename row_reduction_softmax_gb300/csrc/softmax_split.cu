@@ -81,9 +81,18 @@ __device__ __forceinline__ void cluster_wait_acquire() {
 // Scalar (any alignment and stride): rank r owns columns [r*segs,
 // min((r+1)*segs, N)), segs = ceil(N / cs) <= 4 * VEC * kT, each thread four
 // scalars per register slot, so that every warp load is one contiguous run.
+// Shifted (rows not 16-byte aligned, but x and y misaligned alike): each row
+// is read through a window that starts o = (address of the row / 4) mod 4
+// floats before it, so that float4 c of the window (columns 4c - o ..
+// 4c - o + 3) is 16-byte aligned; rank r owns window float4s [r*seg4w,
+// (r+1)*seg4w), seg4w = ceil(ceil((N + 3) / 4) / cs).  Lanes outside [0, N)
+// read neighbouring bytes of the same 16-byte chunks (mapped memory) and are
+// masked; stores of the two edge float4s go lane by lane.
 // LOG writes log y = (x - m) - log(s) (a template parameter, so the softmax
 // instantiation keeps the register count that lets 4 CTAs share an SM).  In
 // place (x == y) is safe: a CTA reads its whole segment before writing it.
+constexpr int kModeScalar = 0, kModeVec = 1, kModeShift = 2;
+
 // Slot i of thread tid into the CTA's segment of the row: one float4 (V4),
 // or four scalars kT apart (the scalar layout above).
 template <bool V4>
@@ -101,9 +110,24 @@ __device__ __forceinline__ void store_segment(float* yr, float4* yr4, int i, int
   }
 }
 
-template <int VEC, bool LOG, bool V4>
-__global__ void __launch_bounds__(kT)
+// Slot i into a shifted window (float4 c holds columns 4c - o .. 4c - o + 3).
+__device__ __forceinline__ void store_window(float* yr, float4* yw, int c, int e4w, int o, int N, const float4& v) {
+  if (c >= e4w) return;
+  const int lo = 4 * c - o;
+  if (lo >= 0 && lo + 3 < N) {
+    store_stream(yw + c, v);
+    return;
+  }
+  if (lo >= 0 && lo < N) store_stream(yr + lo, v.x);
+  if (lo + 1 >= 0 && lo + 1 < N) store_stream(yr + lo + 1, v.y);
+  if (lo + 2 >= 0 && lo + 2 < N) store_stream(yr + lo + 2, v.z);
+  if (lo + 3 >= 0 && lo + 3 < N) store_stream(yr + lo + 3, v.w);
+}
+
+template <int VEC, bool LOG, int MODE>
+__global__ void __launch_bounds__(kT, MODE == kModeShift ? 4 : 0)
 softmax_cluster_kernel(const float* x, float* y, int64_t M, int32_t N, int64_t ldx, int64_t ldy) {
+  constexpr bool V4 = MODE == kModeVec;
   __shared__ float red_m[kW];
   __shared__ float red_s[kW];
   __shared__ MaxSum part;   // this CTA's (m_c, s_c), read by its peers
@@ -126,6 +150,8 @@ softmax_cluster_kernel(const float* x, float* y, int64_t M, int32_t N, int64_t l
   const int segs = (N + cs - 1) / cs;   // scalar layout
   const int bs = rank * segs;
   const int es = min(bs + segs, N);
+  const int seg4w = (((N + 6) >> 2) + cs - 1) / cs;   // shifted layout
+  const int b4w = rank * seg4w;
   const float kNeg = neg_inf();
   pdl_entry();
 
@@ -137,7 +163,31 @@ softmax_cluster_kernel(const float* x, float* y, int64_t M, int32_t N, int64_t l
 
     float4 v[VEC];
     float t = kNeg;
-    if constexpr (V4) {
+    int o = 0, e4w = 0;
+    const float4* xw = nullptr;
+    float4* yw = nullptr;
+    if constexpr (MODE == kModeShift) {
+      o = (int)((reinterpret_cast<uintptr_t>(xr) >> 2) & 3);
+      xw = reinterpret_cast<const float4*>(xr - o);
+      yw = reinterpret_cast<float4*>(yr - o);
+      e4w = min(b4w + seg4w, (N + o + 3) >> 2);
+      // every load first (all in flight), then the edge masks
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) {
+        const int c = b4w + i * kT + tid;
+        v[i] = (c < e4w) ? load_stream(xw + c) : make_float4(kNeg, kNeg, kNeg, kNeg);
+      }
+#pragma unroll
+      for (int i = 0; i < VEC; ++i) {
+        const int lo = 4 * (b4w + i * kT + tid) - o;
+        if (lo < 0 || lo + 3 >= N) {   // an edge of the row (or past it: already -inf)
+          v[i].x = (lo >= 0 && lo < N) ? v[i].x : kNeg;
+          v[i].y = (lo + 1 >= 0 && lo + 1 < N) ? v[i].y : kNeg;
+          v[i].z = (lo + 2 >= 0 && lo + 2 < N) ? v[i].z : kNeg;
+          v[i].w = (lo + 3 < N) ? v[i].w : kNeg;
+        }
+      }
+    } else if constexpr (V4) {
 #pragma unroll
       for (int i = 0; i < VEC; ++i) {
         const int c = b4 + i * kT + tid;
@@ -207,9 +257,10 @@ softmax_cluster_kernel(const float* x, float* y, int64_t M, int32_t N, int64_t l
       const float ls = logf(w.s);
 #pragma unroll
       for (int i = 0; i < VEC; ++i) {
-        const float4 o = make_float4(log_softmax_of(v[i].x, w.m, ls), log_softmax_of(v[i].y, w.m, ls),
+        const float4 r = make_float4(log_softmax_of(v[i].x, w.m, ls), log_softmax_of(v[i].y, w.m, ls),
                                      log_softmax_of(v[i].z, w.m, ls), log_softmax_of(v[i].w, w.m, ls));
-        store_segment<V4>(yr, yr4, i, tid, b4, e4, bs, es, o);
+        if constexpr (MODE == kModeShift) store_window(yr, yw, b4w + i * kT + tid, e4w, o, N, r);
+        else store_segment<V4>(yr, yr4, i, tid, b4, e4, bs, es, r);
       }
       if (has_tail) store_stream(yr + 4 * n4 + tid, log_softmax_of(t, w.m, ls));
     } else {
@@ -217,9 +268,11 @@ softmax_cluster_kernel(const float* x, float* y, int64_t M, int32_t N, int64_t l
       const float scale = bad ? __int_as_float(0x7fc00000)
                               : (empty ? 0.f : exp_shifted(mc, w.m) / w.s);
 #pragma unroll
-      for (int i = 0; i < VEC; ++i)
-        store_segment<V4>(yr, yr4, i, tid, b4, e4, bs, es,
-                          make_float4(v[i].x * scale, v[i].y * scale, v[i].z * scale, v[i].w * scale));
+      for (int i = 0; i < VEC; ++i) {
+        const float4 r = make_float4(v[i].x * scale, v[i].y * scale, v[i].z * scale, v[i].w * scale);
+        if constexpr (MODE == kModeShift) store_window(yr, yw, b4w + i * kT + tid, e4w, o, N, r);
+        else store_segment<V4>(yr, yr4, i, tid, b4, e4, bs, es, r);
+      }
       if (has_tail) store_stream(yr + 4 * n4 + tid, t * scale);
     }
     cluster_wait_acquire();  // peers finished reading `part` before it is reused / freed
@@ -352,10 +405,10 @@ softmax_finalize_kernel(const float* x, float* y, const MaxSum* __restrict__ par
   }
 }
 
-template <int VEC, bool LOG, bool V4>
+template <int VEC, bool LOG, int MODE>
 cudaError_t launch_cluster_vec(const rrs_plan& p, const float* x, float* y, int64_t M, int64_t N,
                                const Layout& l, cudaStream_t s) {
-  auto kern = softmax_cluster_kernel<VEC, LOG, V4>;
+  auto kern = softmax_cluster_kernel<VEC, LOG, MODE>;
   if (p.cluster > 8) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
@@ -370,20 +423,19 @@ cudaError_t launch_softmax_cluster(const rrs_plan& p, const float* x, float* y, 
                                    int64_t N, const Layout& l, cudaStream_t s) {
   if (p.threads != kT) return cudaErrorInvalidConfiguration;
   const bool lg = l.log_out != 0;
-  if (!p.vector_io) {
-    switch (p.vec) {
-      case 4: return lg ? launch_cluster_vec<4, true, false>(p, x, y, M, N, l, s)
-                        : launch_cluster_vec<4, false, false>(p, x, y, M, N, l, s);
-      case 8: return lg ? launch_cluster_vec<8, true, false>(p, x, y, M, N, l, s)
-                        : launch_cluster_vec<8, false, false>(p, x, y, M, N, l, s);
-      default: return cudaErrorInvalidConfiguration;
-    }
-  }
-  switch (p.vec) {
-    case 4: return lg ? launch_cluster_vec<4, true, true>(p, x, y, M, N, l, s)
-                      : launch_cluster_vec<4, false, true>(p, x, y, M, N, l, s);
-    case 8: return lg ? launch_cluster_vec<8, true, true>(p, x, y, M, N, l, s)
-                      : launch_cluster_vec<8, false, true>(p, x, y, M, N, l, s);
+  switch (p.vector_io * 16 + p.vec) {   // (mode, VEC)
+    case kModeScalar * 16 + 4: return lg ? launch_cluster_vec<4, true, kModeScalar>(p, x, y, M, N, l, s)
+                                         : launch_cluster_vec<4, false, kModeScalar>(p, x, y, M, N, l, s);
+    case kModeScalar * 16 + 8: return lg ? launch_cluster_vec<8, true, kModeScalar>(p, x, y, M, N, l, s)
+                                         : launch_cluster_vec<8, false, kModeScalar>(p, x, y, M, N, l, s);
+    case kModeVec * 16 + 4: return lg ? launch_cluster_vec<4, true, kModeVec>(p, x, y, M, N, l, s)
+                                      : launch_cluster_vec<4, false, kModeVec>(p, x, y, M, N, l, s);
+    case kModeVec * 16 + 8: return lg ? launch_cluster_vec<8, true, kModeVec>(p, x, y, M, N, l, s)
+                                      : launch_cluster_vec<8, false, kModeVec>(p, x, y, M, N, l, s);
+    case kModeShift * 16 + 4: return lg ? launch_cluster_vec<4, true, kModeShift>(p, x, y, M, N, l, s)
+                                        : launch_cluster_vec<4, false, kModeShift>(p, x, y, M, N, l, s);
+    case kModeShift * 16 + 8: return lg ? launch_cluster_vec<8, true, kModeShift>(p, x, y, M, N, l, s)
+                                        : launch_cluster_vec<8, false, kModeShift>(p, x, y, M, N, l, s);
     default: return cudaErrorInvalidConfiguration;
   }
 }

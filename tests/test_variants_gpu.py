@@ -416,3 +416,37 @@ def test_scalar_cluster_specials_log_and_in_place(N, ldx, ldy, x_off, y_off):
     y, guards = run_ex(x, N, ldx, ldx, "cluster", 0, in_place=True, x_off=x_off)
     check_softmax(y, x, f"scalar cluster in place N={N}")
     assert guards
+
+
+@pytest.mark.parametrize("N,pad,off", [(16385, 1, 0), (50257, 0, 1), (50257, 2, 3), (100003, 1, 2),
+                                       (131069, 0, 0)])
+def test_shifted_window_cluster(N, pad, off):
+    """Rows that are not 16-byte aligned but whose x and y are misaligned
+    alike (the same offset, the same stride): the cluster split reads and
+    writes each row through a float4 window shifted back to the 16-byte
+    boundary (the shift cycles through 0..3 when the stride is not a
+    multiple of 4, and is the base offset when it is), masking the lanes
+    outside the row.  Special values at both ends
+    of rows, the log form and in place."""
+    ld = N + pad
+    assert ld % 4 != 0 or off % 4 != 0          # not a 16-byte-aligned layout
+    props = torch.cuda.get_device_properties(0)
+    p = rrs.plan_softmax(8, N, ld, 2, props.multi_processor_count, props.shared_memory_per_block_optin)
+    assert p["path_name"] == "cluster" and p["vector_io"] == 2
+    rng = np.random.default_rng(N + pad + off)
+    x = rng.normal(0, 3, size=(8, N)).astype(np.float32)
+    x[0, 0] = 60.0                             # the maximum in the first column
+    x[1, N - 1] = 60.0                         # ... in the last column
+    x[2, :3] = np.inf                          # +inf in the masked-edge float4: a NaN row
+    x[3, N - 3:] = -np.inf
+    x[4] = -np.inf
+    x[5, 1:] = -np.inf                         # only the first column visible
+    x[6, :-1] = -np.inf                        # only the last column visible
+    x[7, ::3] = np.nan if N % 2 else -np.inf
+    for flags, check in ((0, check_softmax), (LOG, check_log_softmax)):
+        y, guards = run_ex(x, N, ld, ld, "auto", flags, x_off=off, y_off=off)
+        check(y, x, f"shifted N={N} ld={ld} off={off} flags={flags}")
+        assert guards
+    y, guards = run_ex(x, N, ld, ld, "auto", 0, in_place=True, x_off=off)
+    check_softmax(y, x, f"shifted in place N={N} ld={ld}")
+    assert guards
