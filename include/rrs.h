@@ -119,7 +119,8 @@ typedef struct rrs_plan {
   int64_t chunk;         /* columns per CTA segment in split paths (last one shorter) */
   int64_t rounds;        /* persistent rounds (GRID / STAGED) */
   int32_t smem_bytes;    /* dynamic shared memory per CTA */
-  int32_t vector_io;     /* 1 if 128-bit loads/stores are used */
+  int32_t vector_io;     /* 1: 128-bit loads/stores; 2: 128-bit through a window shifted per row to the
+                            16-byte boundary (CLUSTER, rows not 16-byte aligned); 0: scalar */
   int64_t workspace_bytes;
   int32_t stages;        /* shared-memory ring depth (staged paths) */
   int32_t tile;          /* floats per shared-memory stage (staged paths) */
@@ -313,9 +314,11 @@ RRS_API int rrs_test_occupy(int ctas, int smem_bytes, int64_t nanoseconds, void*
 
 /* The planner, as pure host logic: the plan softmax_rows / row_sum would use
  * for this shape on a device with `sm_count` SMs and `smem_optin` bytes of
- * opt-in shared memory per CTA.  `vector_ok` says whether x and y are
- * 16-byte aligned with ld % 4 == 0.  Honors rrs_force_path.  Returns RRS_OK,
- * RRS_ERR_INVALID_ARG or RRS_ERR_UNSUPPORTED; touches no GPU. */
+ * opt-in shared memory per CTA.  `vector_ok`: 1 if x and y are 16-byte
+ * aligned with ld % 4 == 0; for rrs_plan_softmax also 2 if they are not but
+ * are misaligned alike (the same address mod 16 bytes, strides equal mod 4);
+ * 0 otherwise.  Honors rrs_force_path.  Returns RRS_OK, RRS_ERR_INVALID_ARG
+ * or RRS_ERR_UNSUPPORTED; touches no GPU. */
 RRS_API int rrs_plan_softmax(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_count,
                              int smem_optin, rrs_plan* plan);
 RRS_API int rrs_plan_row_sum(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_count,
