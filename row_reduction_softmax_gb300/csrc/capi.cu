@@ -314,7 +314,10 @@ int64_t staged_budget(int smem_optin) { return (int64_t)smem_optin - staged_head
 int64_t staged_tile_max(int smem_optin) { return (staged_budget(smem_optin) / 7) / 16 * 4; }
 
 constexpr int64_t kStagedRowsMaxN = 8192;
-constexpr int64_t kRowRegsAutoMaxN = 16384;
+constexpr int64_t kRowRegsFirstMaxN = 4096;   // the register kernel always, up to here
+constexpr int64_t kRowRegsAutoMaxN = 16384;   // the register kernel or the cluster split, up to here
+constexpr int64_t kClusterShortRowMaxN = 8192;      // rows this short ...
+constexpr int64_t kClusterShortRowMinElems = 1 << 23;   // ... split only in matrices this large
 constexpr double kPerSmBytesPerSec = 6.7e12 / 152.0;  // planning model only
 constexpr double kItemSec = 0.4e-6;                    // per-segment fixed cost (planning model)
 constexpr int64_t kGridMaxSegments = 160;              // slots one exchange warp polls
@@ -445,27 +448,44 @@ int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok_in, int sm
     return RRS_OK;
   }
   if (forced == RRS_PATH_AUTO) {
-    // Measured on GB300: registers win for rows that fit one CTA, the cluster
-    // split for rows up to 16 CTAs' registers, the staged grid split beyond,
-    // the two-phase split for what the grid cannot hold or align.
-    // Rows whose start or stride is not 16-byte aligned take the scalar
-    // forms of the register and cluster kernels; N % 4 != 0 the vector forms
-    // with a ragged tail (the grid split needs whole float4 segments).
-    rrs_plan c;
-    if (!vector_ok) {
-      if (N <= kRowRegsAutoMaxN) plan_row_regs(M, N, sm_count, p, false);
-      else if (cluster_ok && shift_mode && plan_cluster(M, N, &c, shift_mode)) *p = c;
-      else if (cluster_ok && plan_cluster(M, N, &c, 0)) *p = c;   // a window of N + 3 may not fit: scalar
-      else plan_two_phase(M, N, sm_count, p);
-    } else if (N % 4 != 0) {
-      if (N <= kRowRegsAutoMaxN) plan_row_regs(M, N, sm_count, p);
-      else if (cluster_ok && plan_cluster(M, N, &c)) *p = c;
-      else plan_two_phase(M, N, sm_count, p);
+    // Measured on GB300 (N from 3584 to 16384; cluster split against register
+    // kernel): the register kernel wins up
+    // to 4096 floats (8192 rows of 4096: 39.6 against 47.9 us).  Past that
+    // the cluster split wins where it fills its register slots at least as
+    // well and the rows are more than one wave of CTAs (2^25 floats:
+    // 16384-float rows 43.4 against 54.0 us, 12288 47.4 against 60.9, 10240
+    // 51.8 against 67.1; 456 x 16384 13.2 against 14.4); with at most one
+    // row per SM the register kernel's single pass has the shorter latency
+    // (152 x 12288: 5.7 against 4.9 us), and rows of up to 8192 floats gain
+    // only in matrices of 2^23 floats and more (8192: 1216 rows 15.4
+    // against 15.9, 608 rows 9.2 both; 6144: 456 rows 7.1 against 7.0).  A
+    // row that the register kernel fills and the cluster does not (an
+    // unaligned 8191, whose shifted window spills into a second, half-empty
+    // CTA: 63.0 against 50.2 us) stays on the register kernel.  Past 16384
+    // the cluster split runs up to 16 CTAs' registers, then the staged grid
+    // split, then the two-phase split for what the grid cannot hold or
+    // align.  Rows whose start or stride is not 16-byte aligned take the
+    // shifted-window or scalar forms; N % 4 != 0 the vector forms with a
+    // ragged tail (the grid split needs whole float4 segments).
+    rrs_plan c{}, r{};   // every field the planners leave alone stays 0
+    r.cluster = c.cluster = 1;
+    const int mode = vector_ok ? 1 : shift_mode;   // the cluster kernel's form for these rows
+    auto cluster_plan = [&](rrs_plan* out) {
+      return cluster_ok && (plan_cluster(M, N, out, mode) || (mode == 2 && plan_cluster(M, N, out, 0)));
+    };
+    auto slots = [](const rrs_plan& q, bool cluster) -> double {   // floats one row's register slots hold
+      return cluster ? 4.0 * q.vec * q.threads * q.cluster : 4.0 * q.vec * 32 * q.warps_per_row;
+    };
+    if (N <= kRowRegsFirstMaxN) {
+      plan_row_regs(M, N, sm_count, p, vector_ok != 0);
     } else if (N <= kRowRegsAutoMaxN) {
-      plan_row_regs(M, N, sm_count, p);
-    } else if (cluster_ok && plan_cluster(M, N, &c)) {
+      plan_row_regs(M, N, sm_count, &r, vector_ok != 0);
+      const bool many_rows = M > sm_count && (N > kClusterShortRowMaxN || M * N >= kClusterShortRowMinElems);
+      if (many_rows && cluster_plan(&c) && slots(c, true) <= slots(r, false)) *p = c;
+      else *p = r;
+    } else if (cluster_plan(&c)) {
       *p = c;
-    } else if (plan_grid(M, N, sm_count, smem_optin, p)) {
+    } else if (vector_ok && N % 4 == 0 && plan_grid(M, N, sm_count, smem_optin, p)) {
     } else {
       plan_two_phase(M, N, sm_count, p);
     }

@@ -135,11 +135,51 @@ def test_scalar_cluster_plans_cover_the_row(lib, N):
     assert -(-N // cs) <= 4 * p["vec"] * p["threads"]     # each CTA's scalar segment fits its slots
 
 
-@pytest.mark.parametrize("N", [1, 3, 5, 127, 129, 1023, 1025, 4097, 16383, 16384])
-def test_scalar_row_plans_cover_the_row(lib, N):
-    p = plan(7, N, ld=N + 1, vector_ok=False)
-    assert p["path_name"] == "row_regs" and p["vector_io"] == 0
-    assert p["vec"] * 32 * p["warps_per_row"] * 4 >= N     # 4 scalars per slot
+def row_slots(q):
+    """Floats one row's register slots hold under a plan."""
+    if q["path_name"] == "cluster":
+        return 4 * q["vec"] * q["threads"] * q["cluster"]
+    return 4 * q["vec"] * 32 * q["warps_per_row"]
+
+
+def forced_plan(path, M, N, ld, vector_ok):
+    import row_reduction_softmax_gb300 as rrs
+    rrs.force_path(path)
+    try:
+        return plan(M, N, ld=ld, vector_ok=vector_ok)
+    finally:
+        rrs.force_path("auto", "auto")
+
+
+@pytest.mark.parametrize("vector_ok", [False, True])
+@pytest.mark.parametrize("N", [1, 3, 5, 127, 129, 1023, 1025, 4095, 4096, 4097, 6144, 8191, 8192,
+                               12287, 12288, 16383, 16384])
+@pytest.mark.parametrize("M", [7, 152, 153, 1024, 4096])
+def test_row_plans_cover_the_row(lib, M, N, vector_ok):
+    """Up to 4096 floats the register kernel; up to 16384 the register
+    kernel or the cluster split, whichever holds the row in no more register
+    slots (the cluster split when they tie), the cluster split only for more
+    rows than SMs and, for rows of up to 8192 floats, 2^23 floats or more."""
+    ld = N if vector_ok else N + 1
+    p = plan(M, N, ld=ld, vector_ok=vector_ok)
+    if not vector_ok:
+        assert p["vector_io"] == 0
+    if N <= 4096:
+        assert p["path_name"] == "row_regs"
+    assert p["path_name"] in ("row_regs", "cluster")
+    # a slot holds 4 scalars, or one float4 with the N % 4 tail beside the slots
+    need = N // 4 if p["vector_io"] == 1 else -(-N // 4)
+    if p["path_name"] == "row_regs":
+        assert p["vec"] * 32 * p["warps_per_row"] >= need
+    else:
+        assert -(-need // p["cluster"]) <= p["vec"] * p["threads"]
+    if 4096 < N:
+        r = forced_plan("row_regs", M, N, ld, vector_ok)
+        c = forced_plan("cluster", M, N, ld, vector_ok)
+        assert r["path_name"] == "row_regs" and c["path_name"] == "cluster"
+        many_rows = M > 152 and (N > 8192 or M * N >= 1 << 23)
+        want = "cluster" if many_rows and row_slots(c) <= row_slots(r) else "row_regs"
+        assert p["path_name"] == want, (row_slots(c), row_slots(r))
 
 
 @pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 31, 127, 128, 129, 255, 256, 257, 1000, 1024, 2047,

@@ -88,18 +88,21 @@ def test_leading_dimension_gap(path, M, N, gap):
                                                 (3, 4096, 4096, 0, 3), (5, 33, 35, 2, 1),
                                                 (2, 40000, 40003, 1, 1), (3, 50257, 50257, 0, 0),
                                                 (2, 16385, 16387, 0, 1), (2, 131072, 131073, 1, 2),
-                                                (2, 131075, 131075, 0, 0)])
+                                                (2, 131075, 131075, 0, 0), (3, 8191, 8193, 1, 3),
+                                                (3, 12287, 12289, 2, 1), (2, 16384, 16385, 0, 0)])
 def test_unaligned_takes_scalar_path(M, N, ld, x_off, y_off):
     """Rows whose start or stride is not 16-byte aligned: the scalar register
-    kernel up to 16384, the scalar cluster split up to 131072 (each CTA's
-    segment in four-scalar slots), the scalar two-phase split beyond."""
+    kernel up to 4096, the scalar register kernel or the scalar cluster split
+    up to 16384, the scalar cluster split up to 131072 (each CTA's segment in
+    four-scalar slots), the scalar two-phase split beyond."""
     x = recipe("c2", M, N)
     y, guards = run(x, N, ld, "auto", x_off, y_off)
     check_softmax(y, x, f"unaligned {M}x{N} ld={ld}")
     assert guards
-    want = "row_regs" if N <= 16384 else ("cluster" if N <= 131072 else "two_phase")
+    want = {"row_regs"} if N <= 4096 else ({"row_regs", "cluster"} if N <= 16384 else
+                                           {"cluster"} if N <= 131072 else {"two_phase"})
     assert rrs.plan_softmax(M, N, ld, False, torch.cuda.get_device_properties(0).multi_processor_count)[
-        "path_name"] == want
+        "path_name"] in want
     if N <= 32768:
         y, guards = run(x, N, ld, "row_regs", x_off, y_off)    # the scalar row kernel
         check_softmax(y, x, f"unaligned row_regs {M}x{N} ld={ld}")
