@@ -141,7 +141,8 @@ KERNEL_SOURCES = {
     "softmax_cluster_kernel": ["softmax_split.cu"],
     "softmax_staged_grid_kernel": ["softmax_staged.cu", "sm100_async.cuh"],
     "row_reduce_rows_kernel": ["row_sum.cu"],
-    "softmax_cols_band_kernel": ["softmax_cols.cu"],
+    "softmax_cols_band_kernel": ["softmax_cols.cu", "sm100_async.cuh"],
+    "softmax_cols_two_pass_kernel": ["softmax_cols.cu", "sm100_async.cuh"],
     "attention_fwd_kernel": ["attention.cu", "sm100_async.cuh", "sm100_tcgen05.cuh"],
     "gelu_kernel": ["gelu.cu"],
 }

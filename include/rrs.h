@@ -103,7 +103,8 @@ typedef enum rrs_cols_path {
   RRS_COLS_TWO_PHASE = 0,  /* any shape/alignment: per-(row chunk, column) partials, then merge + re-read + write */
   RRS_COLS_CLUSTER = 1,    /* a band of 32 columns over a cluster of CTAs, all rows in registers (M <= 8192) */
   RRS_COLS_BAND = 2,       /* a band of 32 columns over a cluster of CTAs, rows streamed twice (second read from L2) */
-  RRS_COLS_COUNT = 3
+  RRS_COLS_TWO_PASS = 3,   /* the band path's two passes as work items of one launch, dealt out in arrival order */
+  RRS_COLS_COUNT = 4
 } rrs_cols_path;
 
 typedef struct rrs_plan {
@@ -167,7 +168,13 @@ RRS_API int log_softmax_rows(const float* x, float* y, int64_t M, int64_t N, int
  * columns are read along rows, full 128-byte lines.
  * Columns that are all -inf or hold +inf or NaN come out NaN.  x == y with
  * ldx == ldy computes in place.  Arguments, errors and the empty cases as
- * softmax_rows_ex. */
+ * softmax_rows_ex.  On the two-pass path (large aligned inputs) CTAs wait
+ * for other CTAs' column partials; every such wait is bounded (1 s), and one
+ * that runs out leaves its slice of y unwritten and is reported like a grid
+ * path timeout: rrs_device_error returns RRS_ERR_TIMEOUT, and later calls
+ * on the device return it until then.  Its first call on a device, like the
+ * grid path's, allocates (a workspace and the host error word), so make it
+ * before capturing the call in a CUDA graph. */
 RRS_API int softmax_cols(const float* x, int64_t ldx, float* y, int64_t ldy, int64_t M, int64_t N,
                          int flags, void* stream);
 
@@ -300,9 +307,18 @@ RRS_API int rrs_force_cols_path(int cols_path);
  * partial of its first row segment, so that row's bounded waits run out
  * (about 1 s); the kernel returns early, rrs_device_error() then reports
  * RRS_ERR_TIMEOUT, the output of that call is incomplete, and the CUDA
- * context stays usable.  kind 0 turns injection off.  Nothing here faults
+ * context stays usable.  kind 2: the same for COLS_TWO_PASS launches, whose
+ * first pass-1 item never publishes its column partials, so the second
+ * passes of band 0 time out.  kind 0 turns injection off.  Nothing here faults
  * or hangs the GPU.  Returns RRS_OK or RRS_ERR_INVALID_ARG. */
 RRS_API int rrs_inject_fault(int kind);
+
+/* Testing only: the work item that arrival index t draws in a COLS_TWO_PASS
+ * launch with Q items per pass and lag D (1 <= D <= Q): *pass = 1 (partials
+ * of item *k) or 2 (normalise item *k), items k = band x S + slice.  Pure
+ * host logic, the same function the kernel runs.  Returns RRS_OK or
+ * RRS_ERR_INVALID_ARG (t outside [0, 2Q), D outside [1, Q], null outputs). */
+RRS_API int rrs_cols_two_pass_item(int64_t t, int64_t Q, int64_t D, int* pass, int64_t* k);
 
 /* Testing only (no counterpart in the pages): enqueue on `stream` `ctas`
  * CTAs that each hold `smem_bytes` of shared memory (at most the opt-in

@@ -37,7 +37,7 @@ STATUS = {0: "RRS_OK", 1: "RRS_ERR_INVALID_ARG", 2: "RRS_ERR_ALIAS", 3: "RRS_ERR
 LOG_SOFTMAX = 1  # flag bit of softmax_rows_ex
 PATHS = {"auto": -1, "two_phase": 0, "row_regs": 1, "row_staged": 2, "cluster": 3, "grid": 4}
 SUM_PATHS = {"auto": -1, "row": 0, "split": 1}
-COLS_PATHS = {"auto": -1, "two_phase": 0, "cluster": 1, "band": 2}
+COLS_PATHS = {"auto": -1, "two_phase": 0, "cluster": 1, "band": 2, "two_pass": 3}
 PATH_NAMES = {v: k for k, v in PATHS.items()}
 SUM_PATH_NAMES = {v: k for k, v in SUM_PATHS.items()}
 COLS_PATH_NAMES = {v: k for k, v in COLS_PATHS.items()}
@@ -93,6 +93,8 @@ _SIGNATURES = {
     "rrs_release_workspace": (ctypes.c_int, []),
     "rrs_force_path": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
     "rrs_inject_fault": (ctypes.c_int, [ctypes.c_int]),
+    "rrs_cols_two_pass_item": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                               ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int64)]),
     "rrs_test_occupy": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _I64, _P]),
     "rrs_plan_softmax": (ctypes.c_int, [_I64, _I64, _I64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                         ctypes.POINTER(Plan)]),

@@ -533,7 +533,7 @@ int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok_in, int sm
 // 16), so the fewest CTAs share a band: cs = ceil(M / (32 row groups x vec))
 // <= 16 (M <= 8192).  COLS_TWO_PHASE: row chunks sized for about 4 CTAs per
 // SM over all bands (unaligned inputs).  COLS_BAND: below.
-enum WorkspaceKindCols { kWsCols = 3 };
+enum WorkspaceKindCols { kWsCols = 3, kWsColsTwoPass = 4 };
 
 bool plan_cols_cluster(int64_t M, int64_t N, int64_t max_cs, rrs_plan* p) {
   const int64_t groups = cols_row_groups();
@@ -594,6 +594,32 @@ void plan_cols_band(int64_t M, int64_t N, int sm_count, rrs_plan* p) {
   p->vec = (p->grid >= 9 * (int64_t)sm_count) ? 3 : 4;
 }
 
+// COLS_TWO_PASS: slices of kColsTwoPassRows rows, one CTA per (pass,
+// item), and a lag of kColsTwoPassLagPerSm x SMs items between an item's
+// first and second pass (at least the band's slice count, so every first
+// pass of a band comes before its second passes; at most the item count).
+constexpr int64_t kColsTwoPassRows = 512;
+constexpr int64_t kColsTwoPassLagPerSm = 3;
+
+bool plan_cols_two_pass(int64_t M, int64_t N, int sm_count, rrs_plan* p) {
+  const int64_t bands = ceil_div(N, cols_band());
+  const int64_t R = kColsTwoPassRows;
+  const int64_t S = ceil_div(M, R);
+  const int64_t Q = bands * S;
+  if (2 * Q > (int64_t)INT_MAX) return false;
+  const int64_t D = std::min(Q, std::max(S, kColsTwoPassLagPerSm * (int64_t)sm_count));
+  p->path = RRS_COLS_TWO_PASS;
+  p->threads = cols_threads();
+  p->grid = 2 * Q;
+  p->chunk = R;
+  p->ctas_per_row = S;
+  p->stages = (int32_t)D;
+  p->rows_per_cta = (int32_t)R;
+  p->workspace_bytes = kColsArrivalBytes + Q * cols_band() * 16;
+  p->vector_io = 1;
+  return true;
+}
+
 int plan_cols_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_count, int cluster_ok,
                    int forced, rrs_plan* p) {
   std::memset(p, 0, sizeof(*p));
@@ -607,10 +633,22 @@ int plan_cols_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_count
   }
   const bool cluster_fits = vector_ok && cluster_ok;
   if (forced == RRS_COLS_AUTO) {
-    // measured on GB300: the band path is the fastest wherever it applies
-    // (1024 x 8192: 18.3 us against 19.5 cluster and 28.6 two-phase;
-    // 4096 x 16384: 119.8 against 172.8 and 140.9)
-    if (cluster_fits && bands_fit_grid(N)) {
+    // Measured on GB300: the band path is the fastest of the cluster, band
+    // and two-phase paths wherever it applies (1024 x 8192: 18.3 us against
+    // 19.5 cluster and 28.6 two-phase; 4096 x 16384: 119.8 against 172.8 and
+    // 140.9); the two-pass path beats it once there are items enough for
+    // its passes to interleave, at least twice its lag, and at most 8
+    // slices per band, so its merge takes one round of loads (4096 x 16384:
+    // 102.1-102.6 against 106.8-108.5 us; 2048 x 65536: 192.9-196.5 against
+    // 202.3-202.8; 4096 x 8192: 54.0 against 57.1); it loses where its
+    // passes run one after the other (1024 x 8192: 16.2-16.5 against 16.0)
+    // and ties or loses with 16-32 slices (8192 x 4096: 57.8 against 57.2,
+    // 16384 x 2048: 63.3-65.8 against 63.0-63.7).
+    rrs_plan t{};
+    if (vector_ok && plan_cols_two_pass(M, N, sm_count, &t) && t.ctas_per_row <= 8 &&
+        (int64_t)t.ctas_per_row * ceil_div(N, cols_band()) >= 2 * kColsTwoPassLagPerSm * (int64_t)sm_count) {
+      *p = t;
+    } else if (cluster_fits && bands_fit_grid(N)) {
       plan_cols_band(M, N, sm_count, p);
       p->vector_io = 1;
     } else {
@@ -638,6 +676,10 @@ int plan_cols_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_count
       return RRS_OK;
     }
     return fail(RRS_ERR_UNSUPPORTED, "COLS_BAND needs 16-byte alignment and cluster launch");
+  }
+  if (forced == RRS_COLS_TWO_PASS) {
+    if (vector_ok && plan_cols_two_pass(M, N, sm_count, p)) return RRS_OK;
+    return fail(RRS_ERR_UNSUPPORTED, "COLS_TWO_PASS needs 16-byte alignment and 2 x items <= INT_MAX");
   }
   return fail(RRS_ERR_UNSUPPORTED, "column path not available");
 }
@@ -738,8 +780,14 @@ RRS_API int rrs_force_cols_path(int cols_path) {
 }
 
 RRS_API int rrs_inject_fault(int kind) {
-  if (kind < 0 || kind > 1) return RRS_ERR_INVALID_ARG;
+  if (kind < 0 || kind > 2) return RRS_ERR_INVALID_ARG;
   g_fault.store(kind);
+  return RRS_OK;
+}
+
+RRS_API int rrs_cols_two_pass_item(int64_t t, int64_t Q, int64_t D, int* pass, int64_t* k) {
+  if (!pass || !k || Q < 1 || D < 1 || D > Q || t < 0 || t >= 2 * Q) return RRS_ERR_INVALID_ARG;
+  cols_two_pass_item(t, Q, D, pass, k);
   return RRS_OK;
 }
 
@@ -844,7 +892,7 @@ RRS_API int softmax_rows_ex(const float* x, int64_t ldx, float* y, int64_t ldy, 
       unsigned* herr = nullptr;
       if ((st = host_err_word(dev, s, &herr)) != RRS_OK) return st;
       if ((st = get_workspace(dev, s, kWsGrid, (size_t)plan.workspace_bytes, &ws)) != RRS_OK) return st;
-      e = launch_softmax_staged_grid(plan, x, y, M, N, l, ws, g_fault.load(), herr, s);
+      e = launch_softmax_staged_grid(plan, x, y, M, N, l, ws, g_fault.load() == 1 ? 1 : 0, herr, s);
       break;
     }
     case RRS_PATH_TWO_PHASE: {
@@ -899,6 +947,12 @@ RRS_API int softmax_cols(const float* x, int64_t ldx, float* y, int64_t ldy, int
     e = launch_softmax_cols_cluster(plan, x, y, M, N, l, s);
   } else if (plan.path == RRS_COLS_BAND) {
     e = launch_softmax_cols_band(plan, x, y, M, N, l, s);
+  } else if (plan.path == RRS_COLS_TWO_PASS) {
+    void* ws = nullptr;
+    unsigned* herr = nullptr;
+    if ((st = host_err_word(dev, s, &herr)) != RRS_OK) return st;
+    if ((st = get_workspace(dev, s, kWsColsTwoPass, (size_t)plan.workspace_bytes, &ws)) != RRS_OK) return st;
+    e = launch_softmax_cols_two_pass(plan, x, y, M, N, l, ws, g_fault.load() == 2 ? 1 : 0, herr, s);
   } else {
     void* ws = nullptr;
     if ((st = get_workspace(dev, s, kWsCols, (size_t)plan.workspace_bytes, &ws)) != RRS_OK) return st;
@@ -1063,13 +1117,15 @@ RRS_API int rrs_device_error(void* stream) {
   unsigned v = 0, w = 0;
   cudaError_t e = read_and_clear_staged_error(static_cast<cudaStream_t>(stream), &v);
   if (e == cudaSuccess) e = read_and_clear_attn_error(static_cast<cudaStream_t>(stream), &w);
+  unsigned c = 0;
+  if (e == cudaSuccess) e = read_and_clear_cols_error(static_cast<cudaStream_t>(stream), &c);
   if (e != cudaSuccess) return fail_cuda(e, "rrs_device_error");
   int dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) {
     if (host_err_value(dev) != 0) v |= 1u;
     host_err_clear(dev);
   }
-  v |= w;
+  v |= w | c;
   return v ? fail(RRS_ERR_TIMEOUT, "a split-row kernel stopped waiting for its peers") : RRS_OK;
 }
 

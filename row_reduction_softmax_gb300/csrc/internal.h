@@ -111,6 +111,19 @@ cudaError_t launch_softmax_cols_band(const rrs_plan& p, const float* x, float* y
 cudaError_t launch_softmax_cols_two_phase(const rrs_plan& p, const float* x, float* y, int64_t M,
                                           int64_t N, const Layout& l, void* workspace,
                                           cudaStream_t s);
+// COLS_TWO_PASS plans carry chunk (rows per slice, R), ctas_per_row (slices
+// per band, S = ceil(M / R)), stages (the lag D, S <= D <= bands x S) and
+// grid = 2 x bands x S; the workspace holds the arrival counter in its first
+// kColsArrivalBytes, then 16 bytes per (band, slice, column).  fault != 0:
+// item 0's partials are never published (fault injection).  host_err: the
+// mapped host error word (may be null).
+constexpr int64_t kColsArrivalBytes = 128;
+cudaError_t launch_softmax_cols_two_pass(const rrs_plan& p, const float* x, float* y, int64_t M,
+                                         int64_t N, const Layout& l, void* workspace, int fault,
+                                         unsigned* host_err, cudaStream_t s);
+// The (pass, item) of arrival index t of a COLS_TWO_PASS launch with Q items
+// per pass and lag D (host copy of the kernel's sequence, for tests).
+void cols_two_pass_item(int64_t t, int64_t Q, int64_t D, int* pass, int64_t* k);
 
 // ---- row-reduction launchers (row_sum.cu): op is one of kOp* ----
 constexpr int kOpSum = 0;
@@ -137,5 +150,6 @@ cudaError_t launch_attention(const uint16_t* q, const uint16_t* k, const uint16_
 // ---- device error words (set by kernels whose bounded waits ran out) ----
 cudaError_t read_and_clear_staged_error(cudaStream_t s, unsigned* value);
 cudaError_t read_and_clear_attn_error(cudaStream_t s, unsigned* value);
+cudaError_t read_and_clear_cols_error(cudaStream_t s, unsigned* value);
 
 }  // namespace rrs

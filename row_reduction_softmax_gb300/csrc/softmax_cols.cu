@@ -31,15 +31,26 @@
 //   column) online partial to a workspace, kernel 2 merges a column's
 //   partials, re-reads its chunk and writes y (12 bytes per element unless
 //   the re-read hits L2).
+// COLS_TWO_PASS -- the band path's two passes as separate work items of one
+//   launch, dealt out in arrival order so that every SM runs first passes
+//   (HBM reads) beside second passes (L2 re-reads, HBM writes) and no CTA
+//   waits at a cluster barrier; see the kernel.
+#include <climits>
+
 #include <cooperative_groups.h>
 
 #include "device_common.cuh"
 #include "internal.h"
 #include "launch_util.h"
+#include "sm100_async.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace rrs {
+
+// Set by COLS_TWO_PASS CTAs that gave up a bounded wait; read by rrs_device_error().
+__device__ unsigned int g_cols_error = 0;
+
 namespace {
 
 constexpr int kCT = 256;             // threads per CTA
@@ -440,6 +451,323 @@ softmax_cols_band_kernel(const float* x, float* y, int64_t M, int64_t N, int64_t
   cluster_wait_acquire();  // peers finished reading part[] before this CTA exits
 }
 
+// ----------------------------------------------------------- COLS_TWO_PASS ---
+// Item k = (band b, slice r), k = b S + r, covers columns [32b, 32b + 32) of
+// rows [r R, min((r + 1) R, M)), S = ceil(M / R) slices per band.
+//   Pass 1 of item k: online (max, sum) per column over the slice, with the
+//   loads at L2 evict-last priority, merged over the CTA (the band kernel's
+//   shuffle and shared-memory steps) and published to item k's 32 column
+//   slots as two tagged 64-bit words, (ticket << 32 | bits(m)) and
+//   (ticket << 32 | bits(s)): each word is single-copy atomic, so a reader
+//   that sees this launch's ticket in a word has its value.
+//   Pass 2 of item k: one warp merges the band's S slice pairs of each
+//   column in slice order (the same order in every CTA of the band, so they
+//   agree bit for bit) while the other warps' first loads are in flight;
+//   then the slice is re-read -- from the L2, where pass 1 left it -- and y
+//   written.
+// One CTA per (pass, item).  A CTA's (pass, item) follows from its arrival
+// index t (an atomic counter in the workspace, as on the staged grid path:
+// (epoch << 32 | count), the last CTA to draw opens the next epoch, and
+// epoch + 1 is this launch's ticket) through a fixed sequence: pass 1 of items 0 .. D - 1, then pass 1
+// of item D + i and pass 2 of item i alternately, then pass 2 of the last D
+// items.  Pass 2 of an item thus trails its pass 1 by 2 D + 1 arrivals, and
+// D >= S keeps pass 1 of every slice of a band ahead of the band's pass 2s.
+// A pass-2 CTA waits only for pass-1 items drawn before it, by CTAs that are
+// running or done, so the wait ends whatever else holds the GPU; it is still
+// bounded (1 s), and on timeout the CTA sets the error words and leaves its
+// slice of y unwritten.  Every element is read by pass 1 of its slice before
+// pass 2 writes it, so x == y (in place) is safe.
+constexpr uint64_t kColsWaitNs = 1000000000ull;
+constexpr unsigned kColsErrTimeout = 1u;
+
+__host__ __device__ inline void two_pass_item(int64_t t, int64_t Q, int64_t D, int* pass, int64_t* k) {
+  if (t < D) {
+    *pass = 1;
+    *k = t;
+    return;
+  }
+  const int64_t u = t - D;
+  if (u < 2 * (Q - D)) {
+    *pass = (u & 1) ? 2 : 1;
+    *k = (u & 1) ? (u >> 1) : D + (u >> 1);
+    return;
+  }
+  *pass = 2;
+  *k = (Q - D) + (u - 2 * (Q - D));
+}
+
+__device__ __forceinline__ uint64_t cols_tagged(uint32_t ticket, float v) {
+  return ((uint64_t)ticket << 32) | (uint64_t)__float_as_uint(v);
+}
+
+// The arrival index of this CTA among the `draws` of its launch, and the
+// launch's ticket; the last of the draws opens the next epoch.
+__device__ __forceinline__ unsigned draw_arrival(unsigned long long* arrivals, unsigned draws, unsigned* ticket) {
+  const unsigned long long old = atomicAdd(arrivals, 1ull);
+  const unsigned a = (unsigned)(old & 0xffffffffull);
+  const unsigned epoch = (unsigned)(old >> 32);
+  if (a == draws - 1) {
+    atomicExch(arrivals, (unsigned long long)(epoch == 0xfffffffeu ? 0u : epoch + 1u) << 32);
+    __threadfence();
+  }
+  *ticket = epoch + 1u;   // never 0, the tag of a zero-filled slot
+  return a;
+}
+
+// The item of a COLS_TWO_PASS CTA (t: its arrival index), by the whole
+// CTA.  gave_up: set when the CTA's wait ran out; its slice of y is then
+// left unwritten.
+template <bool LOG>
+__device__ __forceinline__ void two_pass_run(const float* x, float* y, int64_t M, int64_t N, int64_t ldx,
+                                             int64_t ldy, int64_t R, int64_t S, int64_t bands, int64_t D,
+                                             uint64_t* __restrict__ slots, int32_t fault, unsigned* host_err,
+                                             int64_t t, uint32_t ticket, MaxSum (*red)[kBand], MaxSum* whole,
+                                             volatile int* gave_up) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int slot = lane % kLPR;
+  const int g = warp * kRPW + lane / kLPR;
+  int pass;
+  int64_t k;
+  two_pass_item(t, bands * S, D, &pass, &k);
+  const int64_t band = (int64_t)((uint32_t)k / (uint32_t)S);   // both below 2^31 (checked at launch)
+  const int64_t r0 = (k - band * S) * R;
+  const int nrows = (int)(min(r0 + R, M) - r0);   // rows of the slice, at most R
+  const int64_t j0 = band * kBand + 4 * slot;
+  const int ncol = (int)max((int64_t)0, min((int64_t)4, N - j0));   // this thread's columns inside the row
+  const float kNeg = neg_inf();
+  const int64_t xstep = (int64_t)kGroups * ldx;   // a thread's next row in pass 1
+  const float* xs = x + r0 * ldx + j0;   // the slice's first row, this thread's columns
+  const uint64_t log2e2 = f2_pack(kLog2e, kLog2e);
+
+  auto load4 = [&](const float* q, bool keep, uint64_t pol) -> float4 {
+    if (ncol == 4) return keep ? load_evict_last(reinterpret_cast<const float4*>(q), pol)
+                               : load_stream(reinterpret_cast<const float4*>(q));
+    float4 v;
+    v.x = (ncol > 0) ? q[0] : kNeg;
+    v.y = (ncol > 1) ? q[1] : kNeg;
+    v.z = (ncol > 2) ? q[2] : kNeg;
+    v.w = kNeg;
+    return v;
+  };
+  // a batch is whole when its last row is inside the slice and the four
+  // columns are: then it needs no per-row check (pass 1's row groups)
+  auto whole_batch = [&](int i) { return ncol == 4 && i + (kBU - 1) * kGroups < nrows; };
+
+  if (pass == 1) {
+    const uint64_t pol = l2_evict_last_policy();
+    MaxSum p[4] = {{kNeg, 0.f}, {kNeg, 0.f}, {kNeg, 0.f}, {kNeg, 0.f}};
+    if (ncol > 0) {
+      const float* xr = xs + g * ldx;
+      for (int i = g; i < nrows; i += kBU * kGroups, xr += kBU * xstep) {
+        float4 a[kBU];
+        if (whole_batch(i)) {
+          const float* q = xr;
+#pragma unroll
+          for (int u = 0; u < kBU; ++u, q += xstep) a[u] = load_evict_last(reinterpret_cast<const float4*>(q), pol);
+        } else {
+          const float* q = xr;
+#pragma unroll
+          for (int u = 0; u < kBU; ++u, q += xstep)
+            a[u] = (i + u * kGroups < nrows) ? load4(q, true, pol) : make_float4(kNeg, kNeg, kNeg, kNeg);
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float bm = comp(a[0], c);
+#pragma unroll
+          for (int u = 1; u < kBU; ++u) bm = max_nan(bm, comp(a[u], c));
+          rescale_to(p[c], bm);
+        }
+        uint64_t nm[2], s2[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float ma = (p[2 * h].m == kNeg) ? 0.f : p[2 * h].m;
+          const float mb = (p[2 * h + 1].m == kNeg) ? 0.f : p[2 * h + 1].m;
+          nm[h] = f2_pack(-ma, -mb);
+          s2[h] = f2_pack(p[2 * h].s, p[2 * h + 1].s);
+        }
+#pragma unroll
+        for (int u = 0; u < kBU; ++u) {
+          s2[0] = f2_add(s2[0], exp_shifted2(a[u].x, a[u].y, nm[0], log2e2));
+          s2[1] = f2_add(s2[1], exp_shifted2(a[u].z, a[u].w, nm[1], log2e2));
+        }
+        f2_unpack(s2[0], p[0].s, p[1].s);
+        f2_unpack(s2[1], p[2].s, p[3].s);
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+      for (int o = kLPR; o < 32; o <<= 1) {
+        MaxSum q;
+        q.m = __shfl_xor_sync(kFullMask, p[c].m, o);
+        q.s = __shfl_xor_sync(kFullMask, p[c].s, o);
+        p[c] = merge(p[c], q);
+      }
+    }
+    if (lane < kLPR) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) red[warp][4 * slot + c] = p[c];
+    }
+    __syncthreads();
+    if (tid < kBand && !(fault != 0 && k == 0)) {   // fault: item 0's partials never appear
+      MaxSum q{kNeg, 0.f};
+#pragma unroll
+      for (int w = 0; w < kCW; ++w) q = merge(q, red[w][tid]);
+      uint64_t* sl = slots + 2 * (k * kBand + tid);
+      publish_gpu_u64(sl, cols_tagged(ticket, q.m));
+      publish_gpu_u64(sl + 1, cols_tagged(ticket, q.s));
+    }
+    return;
+  }
+
+  // ---- pass 2: warps 1..7 issue their first batch of loads while warp 0
+  // merges (in separate branches: the poll words and a batch do not fit the
+  // register budget together); warp 0 loads its batch after the merge.  (A
+  // dedicated merge warp, with seven warps holding the rows, was slower:
+  // 105.2 against 102.2 us on 4096 x 16384.) ----
+  const int64_t ystep = (int64_t)kGroups * ldy;
+  auto load_batch2 = [&](float4 (&a)[kBU], int i, const float* xr) {
+    const float* q = xr;
+    if (whole_batch(i)) {
+#pragma unroll
+      for (int u = 0; u < kBU; ++u, q += xstep) a[u] = load_stream(reinterpret_cast<const float4*>(q));
+    } else {
+#pragma unroll
+      for (int u = 0; u < kBU; ++u, q += xstep)
+        if (i + u * kGroups < nrows) a[u] = load4(q, false, 0);
+    }
+  };
+  const bool any2 = ncol > 0 && g < nrows;
+  float4 a2[kBU];
+  if (warp != 0) {
+    if (any2) load_batch2(a2, g, xs + g * ldx);
+  } else {
+    // lane c merges column c over the band's slices, 8 slices' words in flight
+    const uint64_t* col = slots + 2 * (band * S * kBand + lane);
+    MaxSum acc{kNeg, 0.f};
+    bool ok = true;
+    const uint64_t t0 = global_timer_ns();
+    for (int64_t i0 = 0; i0 < S && ok; i0 += 8) {
+      const int n = (S - i0 < 8) ? (int)(S - i0) : 8;
+      uint64_t wm[8], ws[8];
+      uint32_t polls = 0;
+      for (;;) {
+        bool mine = true;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (u < n) {
+            const uint64_t* w = col + 2 * (i0 + u) * kBand;
+            wm[u] = ld_relaxed_gpu_u64(w);
+            ws[u] = ld_relaxed_gpu_u64(w + 1);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (u < n) mine &= ((uint32_t)(wm[u] >> 32) == ticket) && ((uint32_t)(ws[u] >> 32) == ticket);
+        }
+        if (__all_sync(kFullMask, mine)) break;
+        // one vote, so the warp leaves together
+        if ((++polls & 15u) == 0 && __any_sync(kFullMask, global_timer_ns() - t0 > kColsWaitNs)) {
+          ok = false;
+          break;
+        }
+      }
+      if (!ok) break;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (u < n) acc = merge(acc, MaxSum{__uint_as_float((uint32_t)wm[u]), __uint_as_float((uint32_t)ws[u])});
+      }
+    }
+    whole[lane] = acc;
+    if (!ok && lane == 0) {
+      atomicOr(&g_cols_error, kColsErrTimeout);
+      if (host_err) {
+        *reinterpret_cast<volatile unsigned*>(host_err) = kColsErrTimeout;
+        __threadfence_system();
+      }
+      *gave_up = 1;
+    }
+  }
+  __syncthreads();
+  if (*gave_up || !any2) return;
+  if (warp == 0) load_batch2(a2, g, xs + g * ldx);
+
+  float wm[4], k4[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const MaxSum w = whole[4 * slot + c];
+    wm[c] = w.m;
+    const bool bad = !(w.s == w.s) || w.m == kNeg;  // NaN / inf / all -inf column
+    if constexpr (LOG) {
+      k4[c] = logf(w.s);
+    } else {
+      k4[c] = bad ? __int_as_float(0x7fc00000) : 1.0f / w.s;
+    }
+  }
+  const uint64_t nwm[2] = {f2_pack(-wm[0], -wm[1]), f2_pack(-wm[2], -wm[3])};
+  const uint64_t kk2[2] = {f2_pack(k4[0], k4[1]), f2_pack(k4[2], k4[3])};
+  auto normalise = [&](const float4& v) -> float4 {
+    float4 o;
+    if constexpr (LOG) {
+      o = make_float4(log_softmax_of(v.x, wm[0], k4[0]), log_softmax_of(v.y, wm[1], k4[1]),
+                      log_softmax_of(v.z, wm[2], k4[2]), log_softmax_of(v.w, wm[3], k4[3]));
+    } else {
+      f2_unpack(f2_mul(exp_shifted2(v.x, v.y, nwm[0], log2e2), kk2[0]), o.x, o.y);
+      f2_unpack(f2_mul(exp_shifted2(v.z, v.w, nwm[1], log2e2), kk2[1]), o.z, o.w);
+    }
+    return o;
+  };
+  const float* xr = xs + g * ldx;
+  float* yr = y + r0 * ldy + j0 + g * ldy;
+  for (int i = g;;) {   // a2 holds the batch of rows i
+    if (whole_batch(i)) {
+      float* o = yr;
+#pragma unroll
+      for (int u = 0; u < kBU; ++u, o += ystep) store_stream(reinterpret_cast<float4*>(o), normalise(a2[u]));
+    } else {
+      float* o = yr;
+#pragma unroll
+      for (int u = 0; u < kBU; ++u, o += ystep) {
+        if (i + u * kGroups >= nrows) continue;
+        const float4 v = normalise(a2[u]);
+        if (ncol == 4) {
+          store_stream(reinterpret_cast<float4*>(o), v);
+        } else {
+          if (ncol > 0) store_stream(o + 0, v.x);
+          if (ncol > 1) store_stream(o + 1, v.y);
+          if (ncol > 2) store_stream(o + 2, v.z);
+        }
+      }
+    }
+    i += kBU * kGroups;
+    if (i >= nrows) break;
+    xr += kBU * xstep;
+    yr += kBU * ystep;
+    load_batch2(a2, i, xr);
+  }
+}
+
+template <bool LOG>
+__global__ void __launch_bounds__(kCT, 4)
+softmax_cols_two_pass_kernel(const float* x, float* y, int64_t M, int64_t N, int64_t ldx, int64_t ldy,
+                             int64_t R, int64_t S, int64_t bands, int64_t D,
+                             unsigned long long* __restrict__ arrivals, uint64_t* __restrict__ slots,
+                             int32_t fault, unsigned* host_err) {
+  __shared__ MaxSum red[kCW][kBand];   // per warp, after the shuffle merge
+  __shared__ MaxSum whole[kBand];      // the merged pair of each column
+  __shared__ unsigned drawn[2];        // arrival index, ticket
+  __shared__ int gave_up;
+  // every CTA draws before it lets the next kernel on the stream launch
+  if (threadIdx.x == 0) {
+    drawn[0] = draw_arrival(arrivals, gridDim.x, &drawn[1]);
+    gave_up = 0;
+  }
+  __syncthreads();
+  pdl_entry();
+  two_pass_run<LOG>(x, y, M, N, ldx, ldy, R, S, bands, D, slots, fault, host_err, (int64_t)drawn[0], drawn[1], red,
+                    whole, &gave_up);
+}
+
 // --------------------------------------------------------- COLS_TWO_PHASE ---
 // Grid: bands x chunks CTAs, CTA (band b, chunk c) = blockIdx.x = c * bands + b.
 // Chunk c holds rows [c * chunk, min((c + 1) * chunk, M)); row group g takes
@@ -634,6 +962,38 @@ cudaError_t launch_softmax_cols_band(const rrs_plan& p, const float* x, float* y
                                 l.ldx, l.ldy)
                    : launch_pdl(softmax_cols_band_kernel<false, 4>, grid, block, 0, s, p.cluster, x, y, M, N,
                                 l.ldx, l.ldy);
+}
+
+cudaError_t launch_softmax_cols_two_pass(const rrs_plan& p, const float* x, float* y, int64_t M,
+                                         int64_t N, const Layout& l, void* workspace, int fault,
+                                         unsigned* host_err, cudaStream_t s) {
+  const int64_t bands = (N + kBand - 1) / kBand;
+  const int64_t R = p.chunk, S = p.ctas_per_row, D = p.stages;
+  if (p.threads != kCT || !p.vector_io || R < 1 || S != (M + R - 1) / R || D < S || D > bands * S ||
+      p.grid != 2 * bands * S || p.grid > (int64_t)INT_MAX)
+    return cudaErrorInvalidConfiguration;
+  auto* arrivals = static_cast<unsigned long long*>(workspace);
+  uint64_t* slots = reinterpret_cast<uint64_t*>(static_cast<unsigned char*>(workspace) + kColsArrivalBytes);
+  const dim3 grid((unsigned)p.grid), block(kCT);
+  return l.log_out ? launch_pdl(softmax_cols_two_pass_kernel<true>, grid, block, 0, s, 0, x, y, M, N, l.ldx,
+                                l.ldy, R, S, bands, D, arrivals, slots, (int32_t)fault, host_err)
+                   : launch_pdl(softmax_cols_two_pass_kernel<false>, grid, block, 0, s, 0, x, y, M, N, l.ldx,
+                                l.ldy, R, S, bands, D, arrivals, slots, (int32_t)fault, host_err);
+}
+
+void cols_two_pass_item(int64_t t, int64_t Q, int64_t D, int* pass, int64_t* k) { two_pass_item(t, Q, D, pass, k); }
+
+cudaError_t read_and_clear_cols_error(cudaStream_t s, unsigned* value) {
+  unsigned host = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&host, g_cols_error, sizeof(host), 0, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && host != 0) {
+    const unsigned zero = 0;
+    e = cudaMemcpyToSymbolAsync(g_cols_error, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  }
+  *value = host;
+  return e;
 }
 
 cudaError_t launch_softmax_cols_two_phase(const rrs_plan& p, const float* x, float* y, int64_t M,

@@ -299,8 +299,16 @@ def test_cols_planner(lib, M, N):
     p = rrs.plan_softmax_cols(M, N)
     bands = -(-N // 32)
     assert p["threads"] == 256
-    # aligned input: the band path, the fewest CTAs per band (a power of two,
-    # at most 8) that keep a CTA at most 512 rows (M < 2048) or 1024 rows
+    q = rrs.plan_softmax_cols(M, N, vector_ok=False)
+    assert q["path_name"] == "two_phase" and q["vector_io"] == 0
+    # aligned input with items enough to interleave (slices of 512 rows x
+    # bands at least twice the lag of 3 x 152 items) and at most 8 slices
+    # per band: the two-pass path
+    if -(-M // 512) * bands >= 2 * 3 * 152 and -(-M // 512) <= 8:
+        assert p["path_name"] == "two_pass" and p["stages"] == 3 * 152
+        return
+    # otherwise the band path, the fewest CTAs per band (a power of two, at
+    # most 8) that keep a CTA at most 512 rows (M < 2048) or 1024 rows
     assert p["path_name"] == "band" and p["workspace_bytes"] == 0
     cs, rows = p["cluster"], p["rows_per_cta"]
     cap = 512 if M < 2048 else 1024
@@ -310,8 +318,6 @@ def test_cols_planner(lib, M, N):
     assert p["grid"] == bands * cs
     # registers budgeted for 3 CTAs per SM only when the grid fills three such waves
     assert p["vec"] == (3 if p["grid"] >= 9 * 152 else 4)
-    q = rrs.plan_softmax_cols(M, N, vector_ok=False)
-    assert q["path_name"] == "two_phase" and q["vector_io"] == 0
 
 
 def test_cols_forced_paths(lib):
@@ -356,3 +362,55 @@ def test_new_entry_points_check_arguments(lib):
     assert lib.softmax_rows_ex(a, 8, a + 16, 8, 2, 8, 0, None) == 2
     assert lib.softmax_rows_ex(a, 8, a, 4, 2, 4, 0, None) == 2               # same base, other stride
     assert lib.softmax_cols(a, 8, a + 4, 8, 2, 8, 0, None) == 2
+
+
+def two_pass_item(lib, t, Q, D):
+    pass_, k = ctypes.c_int(), ctypes.c_int64()
+    assert lib.rrs_cols_two_pass_item(t, Q, D, ctypes.byref(pass_), ctypes.byref(k)) == OK
+    return pass_.value, k.value
+
+
+@pytest.mark.parametrize("bands,S,D", [(1, 1, 1), (3, 1, 1), (3, 1, 3), (5, 4, 4), (5, 4, 7), (5, 4, 20),
+                                       (512, 8, 304), (256, 2, 304), (7, 3, 3)])
+def test_cols_two_pass_sequence(lib, bands, S, D):
+    """COLS_TWO_PASS deals every item once to each pass, and the first pass of
+    every slice of a band comes before any second pass of that band (so a
+    second pass waits only on CTAs that drew earlier, hence are running)."""
+    Q = bands * S
+    seen = {1: {}, 2: {}}
+    for t in range(2 * Q):
+        p, k = two_pass_item(lib, t, Q, D)
+        assert p in (1, 2) and 0 <= k < Q and k not in seen[p]
+        seen[p][k] = t
+    assert len(seen[1]) == Q and len(seen[2]) == Q
+    for k, t2 in seen[2].items():
+        b = k // S
+        assert max(seen[1][b * S + r] for r in range(S)) < t2
+    if D < Q:   # the second pass of an item trails its first by 2 D + 1 arrivals in the interleaved stretch
+        k = D
+        if k < Q - D:
+            assert seen[2][k] - seen[1][k] == 2 * D + 1
+
+
+def test_cols_two_pass_item_rejects_bad_arguments(lib):
+    p, k = ctypes.c_int(), ctypes.c_int64()
+    assert lib.rrs_cols_two_pass_item(0, 4, 0, ctypes.byref(p), ctypes.byref(k)) == INVALID
+    assert lib.rrs_cols_two_pass_item(0, 4, 5, ctypes.byref(p), ctypes.byref(k)) == INVALID
+    assert lib.rrs_cols_two_pass_item(8, 4, 2, ctypes.byref(p), ctypes.byref(k)) == INVALID
+    assert lib.rrs_cols_two_pass_item(-1, 4, 2, ctypes.byref(p), ctypes.byref(k)) == INVALID
+    assert lib.rrs_cols_two_pass_item(0, 4, 2, None, ctypes.byref(k)) == INVALID
+
+
+@pytest.mark.parametrize("M,N", [(1, 1), (5, 33), (512, 64), (513, 64), (4096, 16384), (1024, 8192), (70000, 40)])
+def test_cols_two_pass_plan(lib, M, N):
+    import row_reduction_softmax_gb300 as rrs
+    rrs.force_cols_path("two_pass")
+    try:
+        p = rrs.plan_softmax_cols(M, N, N, True, 152)
+    finally:
+        rrs.force_cols_path("auto")
+    assert p["path_name"] == "two_pass"
+    bands = -(-N // 32)
+    R, S, D = p["chunk"], p["ctas_per_row"], p["stages"]
+    assert S == -(-M // R) and S <= D <= bands * S and p["grid"] == 2 * bands * S
+    assert p["workspace_bytes"] == 128 + bands * S * 32 * 16

@@ -49,6 +49,39 @@ def test_grid_wait_runs_out_and_is_reported(lib):
         rrs.force_path("auto", "auto")
 
 
+def test_cols_two_pass_wait_runs_out_and_is_reported(lib):
+    """COLS_TWO_PASS: the second passes wait for the first passes' column
+    partials.  With item 0's partials withheld, band 0's second passes give
+    up after their bounded wait and leave their rows unwritten; the status
+    is reported, later calls are refused until it is collected, and the
+    path is right again afterwards."""
+    M, N = 1024, 256
+    x_host = workloads.matrix(workloads.WORKLOADS["c4"].with_shape(M, N))
+    x = torch.from_numpy(x_host).cuda()
+    y = torch.full_like(x, float("nan"))
+    try:
+        rrs.force_cols_path("two_pass")
+        assert rrs.device_error() == 0
+        assert lib.rrs_inject_fault(2) == 0
+        rrs.softmax_cols(x, y)                      # enqueued: RRS_OK
+        lib.rrs_inject_fault(0)
+        torch.cuda.synchronize()
+        with pytest.raises(rrs.RRSError) as e:
+            rrs.softmax_cols(x, y)
+        assert e.value.status == TIMEOUT
+        assert rrs.device_error() == TIMEOUT
+        assert rrs.device_error() == 0
+        assert bool(torch.isnan(y[:, :32]).all())   # band 0 was never written
+        rrs.softmax_cols(x, y)
+        torch.cuda.synchronize()
+        assert rrs.device_error() == 0
+        from gpu_helpers import check_softmax_cols
+        check_softmax_cols(y.cpu().numpy(), x_host, "cols two-pass after an injected timeout")
+    finally:
+        lib.rrs_inject_fault(0)
+        rrs.force_cols_path("auto")
+
+
 def test_grid_timeout_is_refused_until_collected(lib):
     """After a GRID kernel's wait ran out (and the kernel finished), later
     calls on the device return RRS_ERR_TIMEOUT without a synchronising poll,

@@ -96,7 +96,7 @@ def test_fuzz_softmax_cols(case):
     ld = (-(-N // 4) * 4 if aligned else N) + (4 * int(rng.integers(0, 3)) if aligned else int(rng.integers(0, 3)))
     path = "auto"
     if aligned and rng.random() < 0.6:
-        path = str(rng.choice(["band", "two_phase"] + (["cluster"] if M <= 8192 else [])))
+        path = str(rng.choice(["band", "two_phase", "two_pass"] + (["cluster"] if M <= 8192 else [])))
     log = rng.random() < 0.25
     x = values(rng, M, N)
     if rng.random() < 0.1:

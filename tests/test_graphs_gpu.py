@@ -125,3 +125,32 @@ def test_capture_refuses_to_allocate_and_keeps_captured_workspaces():
         assert rrs.device_error() == 0
         check_every_row(check_softmax, ys, xh, f"replay {k} after growth")
     del g, g_bad
+
+
+def test_softmax_cols_two_pass_replayed_from_a_graph():
+    """The two-pass column path draws its ticket on the device too: a replay
+    never takes a column partial of the previous replay (x changes between
+    replays, and every column is checked)."""
+    from gpu_helpers import check_softmax_cols
+    M, N = 4096, 8192
+    x1 = workloads.matrix(workloads.WORKLOADS["c4"].with_shape(M, N))
+    x2 = np.flip(x1, axis=0).copy() * np.float32(-0.5)
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    assert rrs.plan_softmax_cols(M, N, N, True, sms)["path_name"] == "two_pass"
+    x = torch.from_numpy(x1).cuda()
+    y = torch.empty_like(x)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        rrs.softmax_cols(x, y)                                   # allocations happen here, eagerly
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        rrs.softmax_cols(x, y)
+    for k, xh in enumerate([x2, x1, x2]):
+        x.copy_(torch.from_numpy(xh))
+        y.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert rrs.device_error() == 0
+        check_softmax_cols(y.cpu().numpy(), xh, f"cols two-pass replay {k}")
+    del g

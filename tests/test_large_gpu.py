@@ -101,9 +101,11 @@ def test_row_sum_past_2_31_elements(lib, path):
         assert bool((err <= SUM_TOL * blk.abs().sum(dim=1)).all()), f"row sum {path}: rows {r0}+"
 
 
-def test_softmax_cols_past_2_31_elements(lib):
-    """4096 x 524320: the last row holds elements past 2^31.  Sampled columns
-    are the workload generator's rows of the transposed shape."""
+@pytest.mark.parametrize("path", ["auto", "band"])
+def test_softmax_cols_past_2_31_elements(lib, path):
+    """4096 x 524320: the last row holds elements past 2^31, on the planner's
+    path (two-pass) and on the band path.  Sampled columns are the workload
+    generator's rows of the transposed shape."""
     M = 4096
     N = LIMIT // M + 32
     assert M * N > LIMIT
@@ -116,10 +118,12 @@ def test_softmax_cols_past_2_31_elements(lib):
     xt_cols = workloads.matrix(wt, rows=cols)                  # (len(cols), M)
     x[:, torch.tensor(cols, device="cuda")] = torch.from_numpy(np.ascontiguousarray(xt_cols.T)).cuda()
     y = torch.empty_like(x)
+    rrs.force_cols_path(path)
     p = rrs.plan_softmax_cols(M, N, N, True, torch.cuda.get_device_properties(0).multi_processor_count)
-    assert p["path_name"] == "band"
+    assert p["path_name"] == ("two_pass" if path == "auto" else path)
     rrs.softmax_cols_ptr(x.data_ptr(), N, y.data_ptr(), N, M, N, 0, torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
+    assert rrs.device_error() == 0
     got = y[:, torch.tensor(cols, device="cuda")].cpu().numpy().T   # columns as rows
     check_softmax(got, xt_cols, f"cols {M}x{N} columns {cols}")
     acc = torch.zeros(N, dtype=torch.float64, device="cuda")

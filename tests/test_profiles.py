@@ -27,8 +27,9 @@ CASES = [
     ("softmax_staged_grid_c5.md", 4 * 32 * 1048576, 0.01),
     ("row_reduce_rows_c3.md", 4 * 4096 * 32768, 0.01),
     ("gelu_kernel_gelu_16k.md", 4 * 16384 * 16384, 0.01),
-    # the column band kernel reads x twice, the second time mostly from the L2
-    ("softmax_cols_band_cols_c4.md", 4 * 4096 * 16384, 0.15),
+    # the column kernels read x twice, the second time mostly from the L2
+    ("softmax_cols_two_pass_cols_c4.md", 4 * 4096 * 16384, 0.15),
+    ("softmax_cols_band_cols_c2.md", 4 * 1024 * 8192, 0.15),
 ]
 
 
@@ -58,31 +59,43 @@ def steady(name: str) -> dict:
         m = re.search(pat, text)
         assert m, f"{name}: no steady {key} line"
         out[key] = float(m.group(1)) * 1e6
+    # optional: the global-store sectors leaving the SMs (no local-memory spill stores)
+    m = re.search(r"\| steady global store sectors x 32 B[^|]*\| ([0-9.]+) MB \|", text)
+    if m:
+        out["global_st"] = float(m.group(1)) * 1e6
     return out
 
 
 # summary file, bytes of x, bytes of y written (the softmax writes M N floats,
-# the row sum M), the DRAM writes expected at least (fraction of y: c2's 32 MiB
-# of y partly stay dirty in the L2 between the bench's launches), the reads
-# allowed above the bytes of x (fraction: the column band kernel re-reads x,
-# the second time mostly from the L2)
+# the row sum M), the DRAM writes expected at least (fraction of y: 32 MiB of
+# y partly stay dirty in the L2 between the bench's launches), the reads
+# allowed above the bytes of x (fraction: the column kernels re-read x, the
+# second time mostly from the L2), and the L2 write sectors allowed above the
+# bytes of y (fraction: the band kernel's 64-register build on cols_c2 spills
+# a few registers, and local-memory stores reach the L2 too; its
+# global-store sectors are then checked to be exactly y)
 STEADY = [
-    ("softmax_cluster_c3.md", 4 * 4096 * 32768, 4 * 4096 * 32768, 0.99, 0.01),
-    ("softmax_row_regs_c2.md", 4 * 8192 * 1024, 4 * 8192 * 1024, 0.9, 0.01),
-    ("softmax_row_regs_c4.md", 4 * 16384 * 4096, 4 * 16384 * 4096, 0.97, 0.01),
-    ("softmax_staged_grid_c5.md", 4 * 32 * 1048576, 4 * 32 * 1048576, 0.95, 0.01),
-    ("row_reduce_rows_c3.md", 4 * 4096 * 32768, 4 * 4096, 0.0, 0.01),
-    ("softmax_cols_band_cols_c4.md", 4 * 4096 * 16384, 4 * 4096 * 16384, 0.97, 0.10),
-    ("gelu_kernel_gelu_16k.md", 4 * 16384 * 16384, 4 * 16384 * 16384, 0.99, 0.01),
+    ("softmax_cluster_c3.md", 4 * 4096 * 32768, 4 * 4096 * 32768, 0.99, 0.01, 0.001),
+    ("softmax_row_regs_c2.md", 4 * 8192 * 1024, 4 * 8192 * 1024, 0.9, 0.01, 0.001),
+    ("softmax_row_regs_c4.md", 4 * 16384 * 4096, 4 * 16384 * 4096, 0.97, 0.01, 0.001),
+    ("softmax_staged_grid_c5.md", 4 * 32 * 1048576, 4 * 32 * 1048576, 0.95, 0.01, 0.001),
+    ("row_reduce_rows_c3.md", 4 * 4096 * 32768, 4 * 4096, 0.0, 0.01, 0.001),
+    ("softmax_cols_two_pass_cols_c4.md", 4 * 4096 * 16384, 4 * 4096 * 16384, 0.97, 0.10, 0.01),
+    ("softmax_cols_band_cols_c2.md", 4 * 1024 * 8192, 4 * 1024 * 8192, 0.85, 0.10, 0.25),
+    ("gelu_kernel_gelu_16k.md", 4 * 16384 * 16384, 4 * 16384 * 16384, 0.99, 0.01, 0.001),
 ]
 
 
-@pytest.mark.parametrize("name,x_bytes,y_bytes,min_write,read_slack", STEADY)
-def test_steady_state_reads_x_once_and_writes_y_once(name, x_bytes, y_bytes, min_write, read_slack):
+@pytest.mark.parametrize("name,x_bytes,y_bytes,min_write,read_slack,l2_extra", STEADY)
+def test_steady_state_reads_x_once_and_writes_y_once(name, x_bytes, y_bytes, min_write, read_slack, l2_extra):
     st = steady(name)
     assert 0.98 * x_bytes <= st["read"] <= (1 + read_slack) * x_bytes, f"{name}: {st['read'] / 1e6:.2f} MB read"
     # every store lands in the L2 once: the sectors written are the bytes of y
-    assert abs(st["l2_write"] - y_bytes) <= max(0.001 * y_bytes, 0.2e6), f"{name}: {st['l2_write'] / 1e6:.2f} MB"
+    # (plus, where allowed, register spill stores)
+    assert y_bytes - max(0.001 * y_bytes, 0.2e6) <= st["l2_write"] <= y_bytes + max(l2_extra * y_bytes, 0.2e6), \
+        f"{name}: {st['l2_write'] / 1e6:.2f} MB"
+    if "global_st" in st:
+        assert abs(st["global_st"] - y_bytes) <= max(0.001 * y_bytes, 0.2e6), f"{name}: {st['global_st'] / 1e6:.2f} MB"
     assert min_write * y_bytes <= st["write"] <= 1.01 * y_bytes + 2e6, f"{name}: {st['write'] / 1e6:.2f} MB"
 
 
@@ -139,7 +152,7 @@ def test_every_traffic_figure_is_for_the_current_sources(lib):
                     w = workloads.WORKLOADS[wl]
                     planner = rrs.plan_row_sum if kernel == "row_reduce_rows_kernel" else rrs.plan_softmax
                     plan = planner(w.M, w.N, w.N, True, 152, 232448)
-                elif kernel == "softmax_cols_band_kernel":
+                elif kernel.startswith("softmax_cols_"):
                     w = workloads.VARIANT_WORKLOADS[wl]
                     plan = rrs.plan_softmax_cols(w.M, w.N, w.N, True, 152, 232448)
                 assert bench.source_hash(kernel, plan) == source, f"{name}: {kernel} changed since its capture"

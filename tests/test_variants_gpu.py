@@ -234,11 +234,12 @@ COL_SHAPES = [(1, 1), (2, 5), (7, 3), (8, 128), (9, 129), (64, 250), (100, 33), 
 
 
 # the cluster path holds at most 8192 rows of a column
-@pytest.mark.parametrize("path,M,N", [(p, M, N) for M, N in COL_SHAPES for p in ["cluster", "band", "two_phase"]
+@pytest.mark.parametrize("path,M,N", [(p, M, N) for M, N in COL_SHAPES
+                                      for p in ["cluster", "band", "two_phase", "two_pass"]
                                       if not (p == "cluster" and M > 8192)])
 def test_cols_parity(path, M, N):
     x = recipe(["c2", "c4", "c3"][(M + N) % 3], M, N)
-    ld = N if path == "two_phase" else -(-N // 4) * 4   # the cluster and band paths want ld % 4 == 0
+    ld = N if path == "two_phase" else -(-N // 4) * 4   # the other paths want ld % 4 == 0
     y, guards = run_cols(x, N, ld, ld, path)
     check_softmax_cols(y, x, f"cols {path} {M}x{N}")
     assert guards
@@ -247,7 +248,7 @@ def test_cols_parity(path, M, N):
     assert guards
 
 
-@pytest.mark.parametrize("path", ["cluster", "band", "two_phase"])
+@pytest.mark.parametrize("path", ["cluster", "band", "two_phase", "two_pass"])
 def test_cols_strides_in_place_and_specials(path):
     M, N = 300, 260
     rng = np.random.default_rng(32)
@@ -272,11 +273,15 @@ def test_cols_strides_in_place_and_specials(path):
 @pytest.mark.parametrize("M,N", [(100, 44002), (1500, 11000)])
 def test_cols_band_three_ctas_per_sm(M, N):
     ld = -(-N // 4) * 4
-    p = rrs.plan_softmax_cols(M, N, ld, sm_count=torch.cuda.get_device_properties(0).multi_processor_count)
+    rrs.force_cols_path("band")
+    try:
+        p = rrs.plan_softmax_cols(M, N, ld, sm_count=torch.cuda.get_device_properties(0).multi_processor_count)
+    finally:
+        rrs.force_cols_path("auto")
     assert p["path_name"] == "band" and p["vec"] == 3
     x = recipe("c4", M, N)
     for flags, log in ((0, False), (LOG, True)):
-        y, guards = run_cols(x, N, ld, ld, "auto", flags)
+        y, guards = run_cols(x, N, ld, ld, "band", flags)
         check_softmax_cols(y, x, f"cols band 3/SM {M}x{N} log={log}", log=log)
         assert guards
 
@@ -286,10 +291,36 @@ def test_cols_unaligned_takes_two_phase():
     y, guards = run_cols(x, 301, 303, 305, "auto", x_off=1, y_off=3)
     check_softmax_cols(y, x, "cols unaligned")
     assert guards
-    for path in ("cluster", "band"):
+    for path in ("cluster", "band", "two_pass"):
         with pytest.raises(rrs.RRSError) as e:
             run_cols(x, 301, 303, 305, path, x_off=1, y_off=3)
         assert e.value.status == 6
+
+
+# Shapes with more items per pass than the lag, so that first and second
+# passes interleave in one launch (and, with 20000 rows, 40 slices per band
+# take five rounds of the merge's eight-slice polls); every column is
+# compared with the oracle, in place too.
+@pytest.mark.parametrize("M,N", [(2048, 5100), (20000, 1000), (600, 40000)])
+def test_cols_two_pass_interleaved(M, N):
+    ld = -(-N // 4) * 4
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rrs.force_cols_path("two_pass")
+    try:
+        p = rrs.plan_softmax_cols(M, N, ld, sm_count=sms)
+    finally:
+        rrs.force_cols_path("auto")
+    bands = -(-N // 32)
+    assert p["path_name"] == "two_pass" and p["stages"] < bands * p["ctas_per_row"]
+    x = recipe("c4", M, N)
+    for flags, log in ((0, False), (LOG, True)):
+        y, guards = run_cols(x, N, ld, ld, "two_pass", flags)
+        check_softmax_cols(y, x, f"cols two-pass {M}x{N} log={log}", log=log)
+        assert guards
+    y, guards = run_cols(x, N, ld, ld, "two_pass", in_place=True)
+    check_softmax_cols(y, x, f"cols two-pass in place {M}x{N}")
+    assert guards
+    assert rrs.device_error() == 0
 
 
 # ------------------------------------------------------- full-size variants ----
