@@ -258,6 +258,89 @@ __device__ __forceinline__ uint64_t exp_shifted2(float va, float vb, uint64_t ne
   return f2_pack(exp2_sfu(ta), exp2_sfu(tb));
 }
 
+// A batch of kBU rows of a thread's four columns folded into its online
+// (max, sum) pairs: the batch's column max rescales each pair once, then the
+// exponentials against the pair's max are added in f32x2 pairs.  A column
+// whose max is still -inf has seen only -inf: shifting by 0 gives 2^-inf = 0
+// for all of them, which adds nothing.
+__device__ __forceinline__ void fold_batch(MaxSum (&p)[4], const float4 (&a)[kBU], uint64_t log2e2) {
+  const float kNeg = neg_inf();
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float bm = comp(a[0], k);
+#pragma unroll
+    for (int u = 1; u < kBU; ++u) bm = max_nan(bm, comp(a[u], k));
+    rescale_to(p[k], bm);
+  }
+  uint64_t nm[2], s2[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float ma = (p[2 * h].m == kNeg) ? 0.f : p[2 * h].m;
+    const float mb = (p[2 * h + 1].m == kNeg) ? 0.f : p[2 * h + 1].m;
+    nm[h] = f2_pack(-ma, -mb);
+    s2[h] = f2_pack(p[2 * h].s, p[2 * h + 1].s);
+  }
+#pragma unroll
+  for (int u = 0; u < kBU; ++u) {
+    s2[0] = f2_add(s2[0], exp_shifted2(a[u].x, a[u].y, nm[0], log2e2));
+    s2[1] = f2_add(s2[1], exp_shifted2(a[u].z, a[u].w, nm[1], log2e2));
+  }
+  f2_unpack(s2[0], p[0].s, p[1].s);
+  f2_unpack(s2[1], p[2].s, p[3].s);
+}
+
+// Lanes l, l ^ 8, l ^ 16 and l ^ 24 of a warp hold the same four columns:
+// their pairs merged by shuffles (merge is commutative, so each lane gets
+// the same result).
+__device__ __forceinline__ void merge_column_lanes(MaxSum (&p)[4]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+#pragma unroll
+    for (int o = kLPR; o < 32; o <<= 1) {
+      MaxSum q;
+      q.m = __shfl_xor_sync(kFullMask, p[k].m, o);
+      q.s = __shfl_xor_sync(kFullMask, p[k].s, o);
+      p[k] = merge(p[k], q);
+    }
+  }
+}
+
+// The second pass's arithmetic for a thread's four columns, from their
+// merged pairs w[0..3]: y = 2^((x - m) log2 e) / s, or (x - m) - log s in
+// the log form; a column that is all -inf or holds +inf or NaN gives NaN.
+template <bool LOG>
+struct ColumnScale {
+  float wm[4], k4[4];
+  uint64_t nwm[2], kk2[2];
+  __device__ __forceinline__ explicit ColumnScale(const MaxSum* w) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      wm[c] = w[c].m;
+      const bool bad = !(w[c].s == w[c].s) || w[c].m == neg_inf();
+      if constexpr (LOG) {
+        k4[c] = logf(w[c].s);
+      } else {
+        k4[c] = bad ? __int_as_float(0x7fc00000) : 1.0f / w[c].s;
+      }
+    }
+    nwm[0] = f2_pack(-wm[0], -wm[1]);
+    nwm[1] = f2_pack(-wm[2], -wm[3]);
+    kk2[0] = f2_pack(k4[0], k4[1]);
+    kk2[1] = f2_pack(k4[2], k4[3]);
+  }
+  __device__ __forceinline__ float4 operator()(const float4& v, uint64_t log2e2) const {
+    float4 o;
+    if constexpr (LOG) {
+      o = make_float4(log_softmax_of(v.x, wm[0], k4[0]), log_softmax_of(v.y, wm[1], k4[1]),
+                      log_softmax_of(v.z, wm[2], k4[2]), log_softmax_of(v.w, wm[3], k4[3]));
+    } else {
+      f2_unpack(f2_mul(exp_shifted2(v.x, v.y, nwm[0], log2e2), kk2[0]), o.x, o.y);
+      f2_unpack(f2_mul(exp_shifted2(v.z, v.w, nwm[1], log2e2), kk2[1]), o.z, o.w);
+    }
+    return o;
+  }
+};
+
 // MINB: CTAs per SM the registers are budgeted for (4: 64 registers; 3: 80,
 // which keeps more of the batch in flight on slices of 1024 rows).
 template <bool LOG, int MINB>
@@ -318,46 +401,13 @@ softmax_cols_band_kernel(const float* x, float* y, int64_t M, int64_t N, int64_t
           a[u] = (ru < r1) ? load_row(ru, true) : make_float4(kNeg, kNeg, kNeg, kNeg);
         }
       }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        float bm = comp(a[0], k);
-#pragma unroll
-        for (int u = 1; u < kBU; ++u) bm = max_nan(bm, comp(a[u], k));
-        rescale_to(p[k], bm);
-      }
-      // a column whose max is still -inf has seen only -inf: shifting by 0
-      // gives 2^-inf = 0 for all of them, which adds nothing
-      uint64_t nm[2], s2[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const float ma = (p[2 * h].m == kNeg) ? 0.f : p[2 * h].m;
-        const float mb = (p[2 * h + 1].m == kNeg) ? 0.f : p[2 * h + 1].m;
-        nm[h] = f2_pack(-ma, -mb);
-        s2[h] = f2_pack(p[2 * h].s, p[2 * h + 1].s);
-      }
-#pragma unroll
-      for (int u = 0; u < kBU; ++u) {
-        s2[0] = f2_add(s2[0], exp_shifted2(a[u].x, a[u].y, nm[0], log2e2));
-        s2[1] = f2_add(s2[1], exp_shifted2(a[u].z, a[u].w, nm[1], log2e2));
-      }
-      f2_unpack(s2[0], p[0].s, p[1].s);
-      f2_unpack(s2[1], p[2].s, p[3].s);
+      fold_batch(p, a, log2e2);
     }
   }
-  // ---- merge: a warp's 4 row groups (lanes l, l ^ 8, l ^ 16, l ^ 24 hold
-  // the same columns) by shuffles, the CTA's 8 warps in order, then the
-  // cluster's ranks: a fixed order, and merge is commutative, so the lanes
-  // of a column agree bit for bit ----
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-#pragma unroll
-    for (int o = kLPR; o < 32; o <<= 1) {
-      MaxSum q;
-      q.m = __shfl_xor_sync(kFullMask, p[k].m, o);
-      q.s = __shfl_xor_sync(kFullMask, p[k].s, o);
-      p[k] = merge(p[k], q);
-    }
-  }
+  // ---- merge: a warp's 4 row groups by shuffles, the CTA's 8 warps in
+  // order, then the cluster's ranks: a fixed order, and merge is
+  // commutative, so the lanes of a column agree bit for bit ----
+  merge_column_lanes(p);
   if (lane < kLPR) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) red[warp][4 * slot + k] = p[k];
@@ -399,31 +449,8 @@ softmax_cols_band_kernel(const float* x, float* y, int64_t M, int64_t N, int64_t
   __syncthreads();
 
   // ---- pass 2: re-read (from the L2), normalise, write ----
-  float wm[4], k4[4];
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const MaxSum w = whole[(4 * slot + c) & (kBand - 1)];
-    wm[c] = w.m;
-    const bool bad = !(w.s == w.s) || w.m == kNeg;  // NaN / inf / all -inf column
-    if constexpr (LOG) {
-      k4[c] = logf(w.s);
-    } else {
-      k4[c] = bad ? __int_as_float(0x7fc00000) : 1.0f / w.s;
-    }
-  }
-  const uint64_t nwm[2] = {f2_pack(-wm[0], -wm[1]), f2_pack(-wm[2], -wm[3])};
-  const uint64_t kk2[2] = {f2_pack(k4[0], k4[1]), f2_pack(k4[2], k4[3])};
-  auto normalise = [&](const float4& v) -> float4 {
-    float4 o;
-    if constexpr (LOG) {
-      o = make_float4(log_softmax_of(v.x, wm[0], k4[0]), log_softmax_of(v.y, wm[1], k4[1]),
-                      log_softmax_of(v.z, wm[2], k4[2]), log_softmax_of(v.w, wm[3], k4[3]));
-    } else {
-      f2_unpack(f2_mul(exp_shifted2(v.x, v.y, nwm[0], log2e2), kk2[0]), o.x, o.y);
-      f2_unpack(f2_mul(exp_shifted2(v.z, v.w, nwm[1], log2e2), kk2[1]), o.z, o.w);
-    }
-    return o;
-  };
+  const ColumnScale<LOG> scale(&whole[4 * slot]);
+  auto normalise = [&](const float4& v) -> float4 { return scale(v, log2e2); };
   if (any2) {
     int64_t r = rfirst;
     const float* xr = x + rfirst * ldx + j0;
@@ -570,40 +597,10 @@ __device__ __forceinline__ void two_pass_run(const float* x, float* y, int64_t M
           for (int u = 0; u < kBU; ++u, q += xstep)
             a[u] = (i + u * kGroups < nrows) ? load4(q, true, pol) : make_float4(kNeg, kNeg, kNeg, kNeg);
         }
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float bm = comp(a[0], c);
-#pragma unroll
-          for (int u = 1; u < kBU; ++u) bm = max_nan(bm, comp(a[u], c));
-          rescale_to(p[c], bm);
-        }
-        uint64_t nm[2], s2[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const float ma = (p[2 * h].m == kNeg) ? 0.f : p[2 * h].m;
-          const float mb = (p[2 * h + 1].m == kNeg) ? 0.f : p[2 * h + 1].m;
-          nm[h] = f2_pack(-ma, -mb);
-          s2[h] = f2_pack(p[2 * h].s, p[2 * h + 1].s);
-        }
-#pragma unroll
-        for (int u = 0; u < kBU; ++u) {
-          s2[0] = f2_add(s2[0], exp_shifted2(a[u].x, a[u].y, nm[0], log2e2));
-          s2[1] = f2_add(s2[1], exp_shifted2(a[u].z, a[u].w, nm[1], log2e2));
-        }
-        f2_unpack(s2[0], p[0].s, p[1].s);
-        f2_unpack(s2[1], p[2].s, p[3].s);
+        fold_batch(p, a, log2e2);
       }
     }
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-#pragma unroll
-      for (int o = kLPR; o < 32; o <<= 1) {
-        MaxSum q;
-        q.m = __shfl_xor_sync(kFullMask, p[c].m, o);
-        q.s = __shfl_xor_sync(kFullMask, p[c].s, o);
-        p[c] = merge(p[c], q);
-      }
-    }
+    merge_column_lanes(p);
     if (lane < kLPR) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) red[warp][4 * slot + c] = p[c];
@@ -692,31 +689,8 @@ __device__ __forceinline__ void two_pass_run(const float* x, float* y, int64_t M
   if (*gave_up || !any2) return;
   if (warp == 0) load_batch2(a2, g, xs + g * ldx);
 
-  float wm[4], k4[4];
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    const MaxSum w = whole[4 * slot + c];
-    wm[c] = w.m;
-    const bool bad = !(w.s == w.s) || w.m == kNeg;  // NaN / inf / all -inf column
-    if constexpr (LOG) {
-      k4[c] = logf(w.s);
-    } else {
-      k4[c] = bad ? __int_as_float(0x7fc00000) : 1.0f / w.s;
-    }
-  }
-  const uint64_t nwm[2] = {f2_pack(-wm[0], -wm[1]), f2_pack(-wm[2], -wm[3])};
-  const uint64_t kk2[2] = {f2_pack(k4[0], k4[1]), f2_pack(k4[2], k4[3])};
-  auto normalise = [&](const float4& v) -> float4 {
-    float4 o;
-    if constexpr (LOG) {
-      o = make_float4(log_softmax_of(v.x, wm[0], k4[0]), log_softmax_of(v.y, wm[1], k4[1]),
-                      log_softmax_of(v.z, wm[2], k4[2]), log_softmax_of(v.w, wm[3], k4[3]));
-    } else {
-      f2_unpack(f2_mul(exp_shifted2(v.x, v.y, nwm[0], log2e2), kk2[0]), o.x, o.y);
-      f2_unpack(f2_mul(exp_shifted2(v.z, v.w, nwm[1], log2e2), kk2[1]), o.z, o.w);
-    }
-    return o;
-  };
+  const ColumnScale<LOG> scale(&whole[4 * slot]);
+  auto normalise = [&](const float4& v) -> float4 { return scale(v, log2e2); };
   const float* xr = xs + g * ldx;
   float* yr = y + r0 * ldy + j0 + g * ldy;
   for (int i = g;;) {   // a2 holds the batch of rows i
