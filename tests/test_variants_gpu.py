@@ -297,6 +297,25 @@ def test_cols_unaligned_takes_two_phase():
         assert e.value.status == 6
 
 
+# The planner's boundary between the band and the two-pass paths: at least
+# 912 items (slices of 512 rows x bands of 32 columns, twice the lag of
+# 3 x 152) and at most 8 slices per band take the two-pass path.  Each side
+# of both limits runs on the planner's choice, every column checked.
+@pytest.mark.parametrize("M,N,path", [(4096, 3648, "two_pass"), (4096, 3616, "band"),
+                                      (4097, 16384, "band"), (4096, 16388, "two_pass")])
+def test_cols_auto_path_at_the_planner_boundary(M, N, path):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if sms != 152:
+        pytest.skip("the boundary shapes are laid out for 152 SMs")
+    ld = -(-N // 4) * 4
+    assert rrs.plan_softmax_cols(M, N, ld, sm_count=sms)["path_name"] == path
+    x = recipe("c3", M, N)
+    y, guards = run_cols(x, N, ld, ld, "auto")
+    check_softmax_cols(y, x, f"cols auto {path} {M}x{N}")
+    assert guards
+    assert rrs.device_error() == 0
+
+
 # Shapes with more items per pass than the lag, so that first and second
 # passes interleave in one launch (and, with 20000 rows, 40 slices per band
 # take five rounds of the merge's eight-slice polls); every column is
