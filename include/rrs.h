@@ -239,22 +239,27 @@ RRS_API int attention_fwd(const void* q, const void* k, const void* v, float* o,
  * plugin's execute hook inside an inference engine that owns all device
  * memory, or a latency-critical loop where an allocation could synchronise
  * the device or fail mid-step.  softmax_rows may allocate a small workspace
- * the first time it meets a stream; this call never allocates.  It runs the
- * two-phase kernels with their (max, sum) partials in a fixed 1 MiB array of
- * device memory inside the library (131072 pairs), which every GPU that
- * loads the library holds until the process exits.
+ * the first time it meets a stream; this call never allocates.  Where
+ * softmax_rows would run a kernel that needs no workspace (the register
+ * kernel or the cluster split: aligned rows of up to 131072 floats, and
+ * unaligned ones as the planner takes them), it runs that same kernel, with
+ * the same result.  Otherwise it runs the two-phase kernels with their
+ * (max, sum) partials in a fixed 1 MiB array of device memory inside the
+ * library (131072 pairs), which every GPU that loads the library holds
+ * until the process exits.
  *
  * Same arguments, layout, results and error codes as softmax_rows (y == x
  * computes in place, any other overlap is RRS_ERR_ALIAS; rrs_last_error()
- * holds the message of a refused call), plus RRS_ERR_INVALID_ARG when
- * M > 131072 (each row needs a slot).  Rows are cut
- * into at most 131072 / M chunks, so few-row calls keep their parallelism.
- * The first call on a device looks up the array's device address with that
- * device current; make that first call before any stream capture.  All calls
- * on a device share the array and it keeps the last call's contents (nothing
- * needs clearing: each call writes every slot it reads).  Calls whose kernels
- * overlap on the GPU -- on different streams or host threads -- race on it,
- * so order them on one stream. */
+ * holds the message of a refused call), plus RRS_ERR_INVALID_ARG when the
+ * two-phase kernels would run on M > 131072 rows (each row needs a slot).
+ * Those kernels cut rows into at most 131072 / M chunks, so few-row calls
+ * keep their parallelism.
+ * The first two-phase call on a device looks up the array's device address
+ * with that device current; make that first call before any stream capture.
+ * All two-phase calls on a device share the array and it keeps the last
+ * call's contents (nothing needs clearing: each call writes every slot it
+ * reads).  Two-phase calls whose kernels overlap on the GPU -- on different
+ * streams or host threads -- race on it, so order them on one stream. */
 RRS_API int softmax_rows_noalloc(const float* x, float* y, int64_t M, int64_t N, int64_t ld,
                                  void* stream);
 

@@ -746,6 +746,30 @@ int check_no_pending_timeout(int dev) {
 
 using namespace rrs;
 
+namespace rrs {
+
+// For softmax_rows_noalloc: the plan softmax_rows would launch for these
+// arguments on `dev` when that plan needs no workspace (the register kernel
+// or the cluster split): true, with *p set.  False for every other plan, and
+// when the planner refuses the shape (a forced path that cannot run it);
+// rrs_last_error is left clear either way.
+bool plan_without_workspace(const float* x, const float* y, int64_t M, int64_t N, int64_t ld, int dev,
+                            rrs_plan* p) {
+  DeviceInfo info;
+  if (device_info(dev, &info) != RRS_OK) {
+    clear_last_error();
+    return false;
+  }
+  const bool vec = vector_ok(x, y, ld);
+  const bool alike = (reinterpret_cast<uintptr_t>(x) - reinterpret_cast<uintptr_t>(y)) % 16 == 0;
+  const int st = plan_softmax_impl(M, N, ld, vec ? 1 : (alike ? 2 : 0), info.sm_count, info.smem_optin,
+                                   info.cluster_launch, g_force_softmax.load(), p);
+  clear_last_error();
+  return st == RRS_OK && (p->path == RRS_PATH_ROW_REGS || p->path == RRS_PATH_CLUSTER);
+}
+
+}  // namespace rrs
+
 extern "C" {
 
 RRS_API int rrs_version(void) { return 100; }

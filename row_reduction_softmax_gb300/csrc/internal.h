@@ -27,6 +27,11 @@ bool overlaps(const void* a, int64_t a_bytes, const void* b, int64_t b_bytes);
 // has not been collected by rrs_device_error(); reads one host word and
 // allocates nothing.
 int check_no_pending_timeout(int dev);
+// The plan softmax_rows would launch for these arguments (one stride for x
+// and y) on device `dev`, if it needs no workspace (ROW_REGS or CLUSTER):
+// true and *p set; false otherwise.  Leaves rrs_last_error clear.
+bool plan_without_workspace(const float* x, const float* y, int64_t M, int64_t N, int64_t ld, int dev,
+                            rrs_plan* p);
 
 // Per-device facts the planner needs, queried once per device.
 struct DeviceInfo {

@@ -7,10 +7,12 @@
 // memory and allocation there is forbidden; or a latency-critical loop where
 // an allocation could synchronise the device or fail under memory pressure
 // halfway through a step.  softmax_rows may allocate a small workspace on
-// first use of a stream; this entry point never does.  It runs the same
-// two-phase kernels (per-chunk (max, sum) partials, then merge, re-read and
-// write) with the partials in a fixed array of device memory that is part of
-// the library image itself.
+// first use of a stream; this entry point never does.  Where softmax_rows
+// would run a kernel that needs no workspace (the register kernel or the
+// cluster split), it runs that same kernel; otherwise it runs the two-phase
+// kernels (per-chunk (max, sum) partials, then merge, re-read and write)
+// with the partials in a fixed array of device memory that is part of the
+// library image itself.
 //
 // The array is a file-scope __device__ variable, so every GPU that loads the
 // library holds it until the process exits.  In host code its name is only a
@@ -86,12 +88,9 @@ extern "C" RRS_API int softmax_rows_noalloc(const float* x, float* y, int64_t M,
   if (!x || !y) return fail(RRS_ERR_INVALID_ARG, "null pointer");
   if (reinterpret_cast<uintptr_t>(x) % 4 || reinterpret_cast<uintptr_t>(y) % 4)
     return fail(RRS_ERR_INVALID_ARG, "pointers must be 4-byte aligned");
-  // Every row needs at least one (max, sum) slot of the fixed scratch.
-  if (M > kNoAllocPairs)
-    return fail(RRS_ERR_INVALID_ARG, "softmax_rows_noalloc takes at most 131072 rows");
-  // In place (y == x, one shared stride) is allowed, as in softmax_rows: the
-  // finalize kernel reads each element before the same thread writes it.
-  // Any other overlap is refused.
+  // In place (y == x, one shared stride) is allowed, as in softmax_rows:
+  // every kernel reads each element before the same thread writes it.  Any
+  // other overlap is refused.
   const bool in_place = static_cast<const void*>(x) == static_cast<const void*>(y);
   if (!in_place && overlaps(x, extent * 4, y, extent * 4)) return fail(RRS_ERR_ALIAS, "x and y overlap");
   const uintptr_t xa = reinterpret_cast<uintptr_t>(x), ya = reinterpret_cast<uintptr_t>(y);
@@ -102,6 +101,21 @@ extern "C" RRS_API int softmax_rows_noalloc(const float* x, float* y, int64_t M,
   if ((st = check_no_pending_timeout(dev)) != RRS_OK) return st;
   if ((st = check_device_pointer(x, dev, "x")) != RRS_OK) return st;
   if ((st = check_device_pointer(y, dev, "y")) != RRS_OK) return st;
+  Layout l;
+  l.ldx = ld;
+  l.ldy = ld;
+  rrs_plan plan;
+  if (plan_without_workspace(x, y, M, N, ld, dev, &plan)) {
+    e = plan.path == RRS_PATH_ROW_REGS
+            ? launch_softmax_row_regs(plan, x, y, M, N, l, static_cast<cudaStream_t>(stream))
+            : launch_softmax_cluster(plan, x, y, M, N, l, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e, "softmax_rows_noalloc launch");
+    return RRS_OK;
+  }
+  // Every row needs at least one (max, sum) slot of the fixed scratch.
+  if (M > kNoAllocPairs)
+    return fail(RRS_ERR_INVALID_ARG,
+                "softmax_rows_noalloc takes at most 131072 rows where its two-phase kernels run");
   NoAllocDevice d;
   if ((st = noalloc_device(dev, &d)) != RRS_OK) return st;
 
@@ -113,7 +127,6 @@ extern "C" RRS_API int softmax_rows_noalloc(const float* x, float* y, int64_t M,
   const int64_t chunk = cdiv(cdiv(N, C), kChunkAlign) * kChunkAlign;
   C = cdiv(N, chunk);
 
-  rrs_plan plan;
   std::memset(&plan, 0, sizeof(plan));
   plan.path = RRS_PATH_TWO_PHASE;
   plan.threads = kSplitThreads;
@@ -130,9 +143,6 @@ extern "C" RRS_API int softmax_rows_noalloc(const float* x, float* y, int64_t M,
   // last call's partials.  Nothing in it needs to start at zero: the first
   // kernel writes every slot the second kernel reads.  Two calls whose
   // kernels overlap on the GPU (other streams, other host threads) race on it.
-  Layout l;
-  l.ldx = ld;
-  l.ldy = ld;
   e = launch_softmax_two_phase(plan, x, y, M, N, l, d.scratch, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail_cuda(e, "softmax_rows_noalloc launch");
   return RRS_OK;

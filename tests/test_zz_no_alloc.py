@@ -68,9 +68,30 @@ def test_noalloc_strided_scalar_path(lib):
     _twice_against_softmax_rows(lib, workloads.matrix(workloads.WORKLOADS["c2"].with_shape(M, N)), N + 3)
 
 
-def test_noalloc_at_the_row_limit(lib):
-    """M = 131072 rows, the most the scratch holds (one (max, sum) pair per row)."""
+def test_noalloc_takes_the_workspace_free_kernels(lib):
+    """Where softmax_rows runs the register kernel or the cluster split (no
+    workspace), the no-allocation call runs the same kernel: the results are
+    bitwise equal, also past the two-phase kernels' row limit."""
     rrs.force_path("auto", "auto")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for name, M, N, path in [("c2", 8192, 1024, "row_regs"), ("c3", 64, 32768, "cluster"),
+                             ("c4", 200000, 36, "row_regs")]:
+        assert rrs.plan_softmax(M, N, N, True, sms)["path_name"] == path
+        x_host = workloads.matrix(workloads.WORKLOADS[name].with_shape(M, N))
+        x = torch.from_numpy(x_host).cuda()
+        ref, y = torch.empty_like(x), torch.full_like(x, float("nan"))
+        assert lib.softmax_rows(x.data_ptr(), ref.data_ptr(), M, N, N, _stream()) == OK
+        assert _call_noalloc(lib, x.data_ptr(), y.data_ptr(), M, N, N) == OK
+        torch.cuda.synchronize()
+        assert torch.equal(y, ref), (name, M, N)
+        rows = sorted({0, M // 2, M - 1})
+        check_softmax(y[rows].cpu().numpy(), x_host[rows], f"noalloc {path} {M}x{N}")
+
+
+def test_noalloc_at_the_row_limit(lib):
+    """M = 131072 rows on the two-phase kernels (forced), the most the scratch
+    holds (one (max, sum) pair per row)."""
+    rrs.force_path("two_phase", "auto")
     M, N = 131072, 2048
     w = workloads.WORKLOADS["c2"].with_shape(M, N)
     rows = [0, 1, 4097, M // 2, M - 2, M - 1]
@@ -90,6 +111,7 @@ def test_noalloc_at_the_row_limit(lib):
         x.mul_(0.5)                        # the second call sees another input
         x_rows = x_rows * np.float32(0.5)
         del y
+    rrs.force_path("auto", "auto")
     del x, ref
     torch.cuda.empty_cache()
 
@@ -110,13 +132,19 @@ def test_noalloc_in_place(lib):
 
 
 def test_noalloc_refusals_leave_y_untouched(lib):
-    """Too many rows and partial overlaps are refused before anything is enqueued:
-    y keeps its sentinel and rrs_last_error says why."""
+    """Too many rows for the two-phase kernels (forced here; a shape that
+    needs them past 131072 rows would take 68 GB) and partial overlaps are
+    refused before anything is enqueued: y keeps its sentinel and
+    rrs_last_error says why."""
     lib.rrs_last_error.restype = ctypes.c_char_p
     x = torch.zeros(131073, 4, device="cuda")
     y = Guarded(131073, 4)
-    assert _call_noalloc(lib, x.data_ptr(), y.ptr, 131073, 4, 4) == INVALID
-    assert b"131072" in lib.rrs_last_error()
+    rrs.force_path("two_phase", "auto")
+    try:
+        assert _call_noalloc(lib, x.data_ptr(), y.ptr, 131073, 4, 4) == INVALID
+        assert b"131072" in lib.rrs_last_error()
+    finally:
+        rrs.force_path("auto", "auto")
     assert _call_noalloc(lib, x.data_ptr(), y.ptr, 0, 4, 4) == OK            # nothing to do
     assert lib.rrs_last_error() == b""
     assert _call_noalloc(lib, x.data_ptr(), x.data_ptr() + 16, 4, 4, 4) == ALIAS   # y = x + 1 row
