@@ -243,10 +243,14 @@ RRS_API int attention_fwd(const void* q, const void* k, const void* v, float* o,
  * softmax_rows would run a kernel that needs no workspace (the register
  * kernel or the cluster split: aligned rows of up to 131072 floats, and
  * unaligned ones as the planner takes them), it runs that same kernel, with
- * the same result.  Otherwise it runs the two-phase kernels with their
- * (max, sum) partials in a fixed 1 MiB array of device memory inside the
- * library (131072 pairs), which every GPU that loads the library holds
- * until the process exits.
+ * the same result.  Where softmax_rows would run the grid split, it runs
+ * that kernel too, with its workspace in a fixed 1 MiB array inside the
+ * library (when the shape's (row, segment) slots fit it); a wait of that
+ * kernel that runs out is reported by rrs_device_error, and makes later
+ * calls refuse only if an earlier softmax_rows grid call made the host
+ * error word.  Otherwise it runs the two-phase kernels with their
+ * (max, sum) partials in another fixed 1 MiB array (131072 pairs).  Every
+ * GPU that loads the library holds both arrays until the process exits.
  *
  * Same arguments, layout, results and error codes as softmax_rows (y == x
  * computes in place, any other overlap is RRS_ERR_ALIAS; rrs_last_error()
@@ -254,12 +258,14 @@ RRS_API int attention_fwd(const void* q, const void* k, const void* v, float* o,
  * two-phase kernels would run on M > 131072 rows (each row needs a slot).
  * Those kernels cut rows into at most 131072 / M chunks, so few-row calls
  * keep their parallelism.
- * The first two-phase call on a device looks up the array's device address
- * with that device current; make that first call before any stream capture.
- * All two-phase calls on a device share the array and it keeps the last
- * call's contents (nothing needs clearing: each call writes every slot it
- * reads).  Two-phase calls whose kernels overlap on the GPU -- on different
- * streams or host threads -- race on it, so order them on one stream. */
+ * The first grid or two-phase call on a device looks up the arrays' device
+ * addresses with that device current; make that first call before any
+ * stream capture.  All such calls on a device share the arrays, which keep
+ * the last call's contents (nothing needs clearing: the two-phase kernels
+ * write every slot they read, and the grid kernel's slots carry the ticket
+ * of the launch that wrote them).  Grid or two-phase calls whose kernels
+ * overlap on the GPU -- on different streams or host threads -- race on
+ * them, so order them on one stream. */
 RRS_API int softmax_rows_noalloc(const float* x, float* y, int64_t M, int64_t N, int64_t ld,
                                  void* stream);
 

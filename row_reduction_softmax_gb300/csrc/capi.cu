@@ -749,11 +749,10 @@ using namespace rrs;
 namespace rrs {
 
 // For softmax_rows_noalloc: the plan softmax_rows would launch for these
-// arguments on `dev` when that plan needs no workspace (the register kernel
-// or the cluster split): true, with *p set.  False for every other plan, and
-// when the planner refuses the shape (a forced path that cannot run it);
-// rrs_last_error is left clear either way.
-bool plan_without_workspace(const float* x, const float* y, int64_t M, int64_t N, int64_t ld, int dev,
+// arguments on `dev` (true, *p set), or false when the planner refuses the
+// shape (a forced path that cannot run it); rrs_last_error is left clear
+// either way.
+bool plan_like_softmax_rows(const float* x, const float* y, int64_t M, int64_t N, int64_t ld, int dev,
                             rrs_plan* p) {
   DeviceInfo info;
   if (device_info(dev, &info) != RRS_OK) {
@@ -765,7 +764,14 @@ bool plan_without_workspace(const float* x, const float* y, int64_t M, int64_t N
   const int st = plan_softmax_impl(M, N, ld, vec ? 1 : (alike ? 2 : 0), info.sm_count, info.smem_optin,
                                    info.cluster_launch, g_force_softmax.load(), p);
   clear_last_error();
-  return st == RRS_OK && (p->path == RRS_PATH_ROW_REGS || p->path == RRS_PATH_CLUSTER);
+  return st == RRS_OK;
+}
+
+// The device address of `dev`'s host error word if an earlier call made it,
+// else null (allocates nothing).
+unsigned* host_err_word_if_made(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  return g_host_err_dev[dev].load(std::memory_order_acquire);
 }
 
 }  // namespace rrs

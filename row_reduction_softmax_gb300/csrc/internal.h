@@ -28,10 +28,13 @@ bool overlaps(const void* a, int64_t a_bytes, const void* b, int64_t b_bytes);
 // allocates nothing.
 int check_no_pending_timeout(int dev);
 // The plan softmax_rows would launch for these arguments (one stride for x
-// and y) on device `dev`, if it needs no workspace (ROW_REGS or CLUSTER):
-// true and *p set; false otherwise.  Leaves rrs_last_error clear.
-bool plan_without_workspace(const float* x, const float* y, int64_t M, int64_t N, int64_t ld, int dev,
+// and y) on device `dev`: true and *p set; false if the planner refuses the
+// shape.  Leaves rrs_last_error clear.
+bool plan_like_softmax_rows(const float* x, const float* y, int64_t M, int64_t N, int64_t ld, int dev,
                             rrs_plan* p);
+// The device address of `dev`'s host error word if an earlier call made it,
+// else null; allocates nothing.
+unsigned* host_err_word_if_made(int dev);
 
 // Per-device facts the planner needs, queried once per device.
 struct DeviceInfo {

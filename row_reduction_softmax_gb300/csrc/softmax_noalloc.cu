@@ -9,10 +9,11 @@
 // halfway through a step.  softmax_rows may allocate a small workspace on
 // first use of a stream; this entry point never does.  Where softmax_rows
 // would run a kernel that needs no workspace (the register kernel or the
-// cluster split), it runs that same kernel; otherwise it runs the two-phase
-// kernels (per-chunk (max, sum) partials, then merge, re-read and write)
-// with the partials in a fixed array of device memory that is part of the
-// library image itself.
+// cluster split), it runs that same kernel; where it would run the grid
+// split, it runs that kernel with its workspace in a fixed array of device
+// memory that is part of the library image (when the shape's slots fit);
+// otherwise it runs the two-phase kernels (per-chunk (max, sum) partials,
+// then merge, re-read and write) with the partials in another such array.
 //
 // The array is a file-scope __device__ variable, so every GPU that loads the
 // library holds it until the process exits.  In host code its name is only a
@@ -42,8 +43,16 @@ constexpr int64_t kNoAllocMinChunk = 4096;
 
 static __device__ __align__(256) MaxSum g_noalloc_partials[kNoAllocPairs];
 
+// The grid split's workspace (its arrival counter, then 16 bytes per (row,
+// segment) slot).  Zero at load, and each launch leaves it ready for the
+// next: the last CTA to draw opens the next epoch, and a slot only counts
+// when it carries the current launch's ticket.
+constexpr int64_t kNoAllocGridBytes = 1 << 20;
+static __device__ __align__(256) unsigned char g_noalloc_grid_ws[kNoAllocGridBytes];
+
 struct NoAllocDevice {
-  void* scratch = nullptr;  // device address of g_noalloc_partials on this device
+  void* scratch = nullptr;   // device address of g_noalloc_partials on this device
+  void* grid_ws = nullptr;   // device address of g_noalloc_grid_ws on this device
   int sm_count = 0;
 };
 
@@ -62,7 +71,9 @@ int noalloc_device(int dev, NoAllocDevice* out) {
   NoAllocDevice d;
   cudaError_t e = cudaGetSymbolAddress(&d.scratch, g_noalloc_partials);
   if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(noalloc scratch)");
-  if (d.scratch == nullptr) return fail(RRS_ERR_CUDA, "noalloc scratch has no device address");
+  e = cudaGetSymbolAddress(&d.grid_ws, g_noalloc_grid_ws);
+  if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(noalloc grid workspace)");
+  if (d.scratch == nullptr || d.grid_ws == nullptr) return fail(RRS_ERR_CUDA, "noalloc scratch has no device address");
   e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
   g_noalloc_devices[dev] = d;
@@ -104,11 +115,22 @@ extern "C" RRS_API int softmax_rows_noalloc(const float* x, float* y, int64_t M,
   Layout l;
   l.ldx = ld;
   l.ldy = ld;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
   rrs_plan plan;
-  if (plan_without_workspace(x, y, M, N, ld, dev, &plan)) {
-    e = plan.path == RRS_PATH_ROW_REGS
-            ? launch_softmax_row_regs(plan, x, y, M, N, l, static_cast<cudaStream_t>(stream))
-            : launch_softmax_cluster(plan, x, y, M, N, l, static_cast<cudaStream_t>(stream));
+  const bool planned = plan_like_softmax_rows(x, y, M, N, ld, dev, &plan);
+  if (planned && (plan.path == RRS_PATH_ROW_REGS || plan.path == RRS_PATH_CLUSTER)) {
+    e = plan.path == RRS_PATH_ROW_REGS ? launch_softmax_row_regs(plan, x, y, M, N, l, s)
+                                       : launch_softmax_cluster(plan, x, y, M, N, l, s);
+    if (e != cudaSuccess) return fail_cuda(e, "softmax_rows_noalloc launch");
+    return RRS_OK;
+  }
+  NoAllocDevice d;
+  if ((st = noalloc_device(dev, &d)) != RRS_OK) return st;
+  if (planned && plan.path == RRS_PATH_GRID && plan.workspace_bytes <= kNoAllocGridBytes) {
+    // A wait that runs out sets the device error word (rrs_device_error);
+    // the host word that makes later calls refuse is used only if an
+    // earlier call made it, since making it allocates.
+    e = launch_softmax_staged_grid(plan, x, y, M, N, l, d.grid_ws, 0, host_err_word_if_made(dev), s);
     if (e != cudaSuccess) return fail_cuda(e, "softmax_rows_noalloc launch");
     return RRS_OK;
   }
@@ -116,8 +138,6 @@ extern "C" RRS_API int softmax_rows_noalloc(const float* x, float* y, int64_t M,
   if (M > kNoAllocPairs)
     return fail(RRS_ERR_INVALID_ARG,
                 "softmax_rows_noalloc takes at most 131072 rows where its two-phase kernels run");
-  NoAllocDevice d;
-  if ((st = noalloc_device(dev, &d)) != RRS_OK) return st;
 
   // Chunks per row: enough CTAs to fill the GPU (about 4 per SM), chunks of
   // about kNoAllocMinChunk columns or more (rounded up to kChunkAlign), and
@@ -143,7 +163,7 @@ extern "C" RRS_API int softmax_rows_noalloc(const float* x, float* y, int64_t M,
   // last call's partials.  Nothing in it needs to start at zero: the first
   // kernel writes every slot the second kernel reads.  Two calls whose
   // kernels overlap on the GPU (other streams, other host threads) race on it.
-  e = launch_softmax_two_phase(plan, x, y, M, N, l, d.scratch, static_cast<cudaStream_t>(stream));
+  e = launch_softmax_two_phase(plan, x, y, M, N, l, d.scratch, s);
   if (e != cudaSuccess) return fail_cuda(e, "softmax_rows_noalloc launch");
   return RRS_OK;
 }

@@ -68,15 +68,19 @@ def test_noalloc_strided_scalar_path(lib):
     _twice_against_softmax_rows(lib, workloads.matrix(workloads.WORKLOADS["c2"].with_shape(M, N)), N + 3)
 
 
-def test_noalloc_takes_the_workspace_free_kernels(lib):
+def test_noalloc_takes_the_planned_kernels(lib):
     """Where softmax_rows runs the register kernel or the cluster split (no
-    workspace), the no-allocation call runs the same kernel: the results are
-    bitwise equal, also past the two-phase kernels' row limit."""
+    workspace) or the grid split (its workspace in a fixed array here), the
+    no-allocation call runs the same kernel: the results are bitwise equal,
+    also past the two-phase kernels' row limit, and on a second grid call
+    (the fixed workspace left ready by the first)."""
     rrs.force_path("auto", "auto")
     sms = torch.cuda.get_device_properties(0).multi_processor_count
+    smem = torch.cuda.get_device_properties(0).shared_memory_per_block_optin
     for name, M, N, path in [("c2", 8192, 1024, "row_regs"), ("c3", 64, 32768, "cluster"),
-                             ("c4", 200000, 36, "row_regs")]:
-        assert rrs.plan_softmax(M, N, N, True, sms)["path_name"] == path
+                             ("c4", 200000, 36, "row_regs"), ("c5", 32, 1 << 20, "grid"),
+                             ("c5", 16, 1 << 20, "grid")]:
+        assert rrs.plan_softmax(M, N, N, True, sms, smem)["path_name"] == path
         x_host = workloads.matrix(workloads.WORKLOADS[name].with_shape(M, N))
         x = torch.from_numpy(x_host).cuda()
         ref, y = torch.empty_like(x), torch.full_like(x, float("nan"))
