@@ -172,3 +172,51 @@ def test_two_grid_calls_at_once_on_two_streams(lib):
             check_every_row(check_softmax, ys[k], xs[k], f"c5 concurrent stream {k}")
     finally:
         rrs.force_path("auto", "auto")
+
+
+@pytest.mark.parametrize("held", [0.5, 0.9])
+def test_cols_two_pass_runs_while_other_work_holds_sms(lib, held):
+    """The column two-pass path waits only for items drawn before the waiting
+    CTA (so by CTAs that run), never for co-residency: with most SMs held for
+    50 ms by another stream's CTAs, it runs on the rest, never times out, and
+    every column is right."""
+    from gpu_helpers import check_softmax_cols
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    M, N = 4096, 8192
+    x_host = workloads.matrix(workloads.WORKLOADS["c4"].with_shape(M, N))
+    x = torch.from_numpy(x_host).cuda()
+    other = torch.cuda.Stream()
+    rrs.force_cols_path("auto")
+    assert rrs.plan_softmax_cols(M, N, sm_count=props.multi_processor_count)["path_name"] == "two_pass"
+    for trial in range(2):
+        y = torch.full_like(x, float("nan"))
+        torch.cuda.synchronize()
+        assert lib.rrs_test_occupy(int(props.multi_processor_count * held),
+                                   props.shared_memory_per_block_optin, 50_000_000, other.cuda_stream) == 0
+        rrs.softmax_cols(x, y)
+        torch.cuda.synchronize()
+        assert rrs.device_error() == 0
+        check_softmax_cols(y.cpu().numpy(), x_host, f"cols two-pass beside {held:.0%} held SMs, trial {trial}")
+
+
+def test_two_cols_two_pass_calls_at_once_on_two_streams(lib):
+    """Two two-pass column calls on two streams at the same time, each with its
+    own stream's workspace (arrival counter and ticketed slots): both right."""
+    from gpu_helpers import check_softmax_cols
+    M, N = 4096, 8192
+    w = workloads.WORKLOADS["c4"].with_shape(M, N)
+    xs = [workloads.matrix(w), np.flip(workloads.matrix(w), axis=0).copy() * np.float32(0.5)]
+    dx = [torch.from_numpy(a).cuda() for a in xs]
+    dy = [torch.full_like(d, float("nan")) for d in dx]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    rrs.force_cols_path("auto")
+    for k in range(2):   # eager first calls make each stream's workspace
+        rrs.softmax_cols(dx[k], dy[k], stream=streams[k])
+    torch.cuda.synchronize()
+    for _ in range(3):
+        for k in range(2):
+            rrs.softmax_cols(dx[k], dy[k], stream=streams[k])
+    torch.cuda.synchronize()
+    assert rrs.device_error() == 0
+    for k in range(2):
+        check_softmax_cols(dy[k].cpu().numpy(), xs[k], f"cols two-pass on stream {k}")
