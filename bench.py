@@ -141,8 +141,9 @@ KERNEL_SOURCES = {
     "softmax_cluster_kernel": ["softmax_split.cu"],
     "softmax_staged_grid_kernel": ["softmax_staged.cu", "sm100_async.cuh"],
     "row_reduce_rows_kernel": ["row_sum.cu"],
-    "softmax_cols_band_kernel": ["softmax_cols.cu", "sm100_async.cuh"],
-    "softmax_cols_two_pass_kernel": ["softmax_cols.cu", "sm100_async.cuh"],
+    "softmax_cols_band_kernel": ["softmax_cols.cu", "sm100_async.cuh", "two_pass_common.cuh"],
+    "softmax_cols_two_pass_kernel": ["softmax_cols.cu", "sm100_async.cuh", "two_pass_common.cuh"],
+    "softmax_rows_two_pass_kernel": ["softmax_rows_two_pass.cu", "sm100_async.cuh", "two_pass_common.cuh"],
     "attention_fwd_kernel": ["attention.cu", "sm100_async.cuh", "sm100_tcgen05.cuh"],
     "gelu_kernel": ["gelu.cu"],
 }
@@ -297,7 +298,8 @@ def kernel_of(plan: dict) -> str:
         return "softmax_staged_rows_kernel" if plan["vec"] > 0 else "softmax_staged_long_kernel"
     return {"row_regs": "softmax_row_regs_kernel", "cluster": "softmax_cluster_kernel",
             "two_phase": "softmax_partials_kernel+softmax_finalize_kernel",
-            "grid": "softmax_staged_grid_kernel", "row": "row_reduce_rows_kernel",
+            "grid": "softmax_staged_grid_kernel", "two_pass": "softmax_rows_two_pass_kernel",
+            "row": "row_reduce_rows_kernel",
             "split": "row_reduce_partials_kernel+row_reduce_finalize_kernel"}.get(name, name)
 
 

@@ -85,7 +85,9 @@ typedef enum rrs_path {
   RRS_PATH_ROW_STAGED = 2,  /* persistent CTAs stage rows in shared memory with bulk async copies (TMA) */
   RRS_PATH_CLUSTER = 3,     /* row split over a thread-block cluster; (max,sum) merged through DSMEM */
   RRS_PATH_GRID = 4,        /* row split over co-resident CTAs; (max,sum) merged through global memory */
-  RRS_PATH_COUNT = 5
+  RRS_PATH_TWO_PASS = 5,    /* any shape/alignment: the two passes as work items of one launch, dealt in arrival
+                               order; the second pass re-reads its chunk from the L2 */
+  RRS_PATH_COUNT = 6
 } rrs_path;
 
 /* Execution paths of row_sum. */
@@ -318,9 +320,10 @@ RRS_API int rrs_force_cols_path(int cols_path);
  * partial of its first row segment, so that row's bounded waits run out
  * (about 1 s); the kernel returns early, rrs_device_error() then reports
  * RRS_ERR_TIMEOUT, the output of that call is incomplete, and the CUDA
- * context stays usable.  kind 2: the same for COLS_TWO_PASS launches, whose
- * first pass-1 item never publishes its column partials, so the second
- * passes of band 0 time out.  kind 0 turns injection off.  Nothing here faults
+ * context stays usable.  kind 2: the same for COLS_TWO_PASS and the rows'
+ * TWO_PASS launches, whose first pass-1 item never publishes its partials,
+ * so the second passes of band 0 / row 0 time out.  kind 0 turns injection
+ * off.  Nothing here faults
  * or hangs the GPU.  Returns RRS_OK or RRS_ERR_INVALID_ARG. */
 RRS_API int rrs_inject_fault(int kind);
 

@@ -35,7 +35,7 @@ __all__ = [
 STATUS = {0: "RRS_OK", 1: "RRS_ERR_INVALID_ARG", 2: "RRS_ERR_ALIAS", 3: "RRS_ERR_CUDA",
           4: "RRS_ERR_TIMEOUT", 5: "RRS_ERR_NOMEM", 6: "RRS_ERR_UNSUPPORTED"}
 LOG_SOFTMAX = 1  # flag bit of softmax_rows_ex
-PATHS = {"auto": -1, "two_phase": 0, "row_regs": 1, "row_staged": 2, "cluster": 3, "grid": 4}
+PATHS = {"auto": -1, "two_phase": 0, "row_regs": 1, "row_staged": 2, "cluster": 3, "grid": 4, "two_pass": 5}
 SUM_PATHS = {"auto": -1, "row": 0, "split": 1}
 COLS_PATHS = {"auto": -1, "two_phase": 0, "cluster": 1, "band": 2, "two_pass": 3}
 PATH_NAMES = {v: k for k, v in PATHS.items()}

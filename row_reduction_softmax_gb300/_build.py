@@ -22,7 +22,7 @@ LIB_DIR = os.path.join(PKG_DIR, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "librrs.so")
 
 SOURCES = ["capi.cu", "softmax_row.cu", "softmax_split.cu", "softmax_staged.cu", "row_sum.cu",
-           "softmax_noalloc.cu", "softmax_cols.cu",
+           "softmax_noalloc.cu", "softmax_cols.cu", "softmax_rows_two_pass.cu",
            "gelu.cu", "attention.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -176,7 +176,7 @@ void host_err_clear(int dev) {
 // stream-ordered allocator (ordered after earlier work on the stream that
 // still reads the old buffer) and zero-filled when (re)allocated (the GRID
 // kind's kernels keep their own launch counter and tickets in it).
-enum WorkspaceKind { kWsTwoPhase = 0, kWsGrid = 1, kWsRowSum = 2 };
+enum WorkspaceKind { kWsTwoPhase = 0, kWsGrid = 1, kWsRowSum = 2, kWsRowsTwoPass = 6 };
 
 // Under stream capture: a call that needs more workspace than the stream has
 // is refused (a capture may not allocate; make an eager call of the shape on
@@ -430,6 +430,30 @@ bool plan_grid(int64_t M, int64_t N, int sm_count, int smem_optin, rrs_plan* p) 
   return true;
 }
 
+// ROW_TWO_PASS: items of rows_two_pass_chunk() floats, one CTA per (pass,
+// item), and a lag of kRowTwoPassLagPerSm x SMs items (at least S, at most
+// the item count); float4 access when x, y, the stride and N allow.
+constexpr int64_t kRowTwoPassLagPerSm = 3;
+constexpr int64_t kRowTwoPassMaxChunks = 256;   // a row's pairs in one round of the merging warp's loads
+
+bool plan_row_two_pass(int64_t M, int64_t N, int sm_count, bool vector_ok, rrs_plan* p) {
+  const int64_t S = ceil_div(N, rows_two_pass_chunk());
+  const int64_t Q = M * S;
+  if (2 * Q > (int64_t)INT_MAX) return false;
+  const int64_t D = std::min(Q, std::max(S, kRowTwoPassLagPerSm * (int64_t)sm_count));
+  p->path = RRS_PATH_TWO_PASS;
+  p->threads = rows_two_pass_threads();
+  p->grid = 2 * Q;
+  p->chunk = rows_two_pass_chunk();
+  p->ctas_per_row = S;
+  p->stages = (int32_t)D;
+  p->rows_per_cta = 1;
+  p->cluster = 1;
+  p->vector_io = (vector_ok && N % 4 == 0) ? 1 : 0;
+  p->workspace_bytes = kRowsTwoPassArrivalBytes + Q * 16;
+  return true;
+}
+
 // vector_ok: 1 = x and y 16-byte aligned with strides multiples of 4; 2 =
 // not, but misaligned alike (the same address mod 16 bytes, strides equal
 // mod 4), so every row of both can be read and written through one shifted
@@ -463,12 +487,17 @@ int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok_in, int sm
     // unaligned 8191, whose shifted window spills into a second, half-empty
     // CTA: 63.0 against 50.2 us) stays on the register kernel.  Past 16384
     // the cluster split runs up to 16 CTAs' registers, then the staged grid
-    // split, then the two-phase split for what the grid cannot hold or
-    // align.  Rows whose start or stride is not 16-byte aligned take the
-    // shifted-window or scalar forms; N % 4 != 0 the vector forms with a
-    // ragged tail (the grid split needs whole float4 segments).
-    rrs_plan c{}, r{};   // every field the planners leave alone stays 0
-    r.cluster = c.cluster = 1;
+    // split, then the two-pass split for what the grid cannot hold or align
+    // (one launch, its second pass re-reading from the L2: 32 x 1048577
+    // unaligned 61.7 against 228 us on the two-phase pair, 1024 x 200001
+    // unaligned 324 against 849, 32 x 1048575 58.3 against 69.8) up to 256
+    // chunks a row, and the two-phase pair past that (4 x 2^24: 141 against
+    // 157 us, where the two-pass merge takes eight rounds of loads).  Rows
+    // whose start or stride is not 16-byte aligned take the shifted-window
+    // or scalar forms; N % 4 != 0 the vector forms with a ragged tail (the
+    // grid split needs whole float4 segments, the two-pass split scalars).
+    rrs_plan c{}, r{}, t{};   // every field the planners leave alone stays 0
+    r.cluster = c.cluster = t.cluster = 1;
     const int mode = vector_ok ? 1 : shift_mode;   // the cluster kernel's form for these rows
     auto cluster_plan = [&](rrs_plan* out) {
       return cluster_ok && (plan_cluster(M, N, out, mode) || (mode == 2 && plan_cluster(M, N, out, 0)));
@@ -486,11 +515,13 @@ int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok_in, int sm
     } else if (cluster_plan(&c)) {
       *p = c;
     } else if (vector_ok && N % 4 == 0 && plan_grid(M, N, sm_count, smem_optin, p)) {
+    } else if (plan_row_two_pass(M, N, sm_count, vector_ok != 0, &t) && t.ctas_per_row <= kRowTwoPassMaxChunks) {
+      *p = t;
     } else {
       plan_two_phase(M, N, sm_count, p);
     }
     p->cluster = std::max(p->cluster, 1);
-    if (p->path != RRS_PATH_CLUSTER) p->vector_io = vector_ok;
+    if (p->path != RRS_PATH_CLUSTER && p->path != RRS_PATH_TWO_PASS) p->vector_io = vector_ok;
     return RRS_OK;
   }
   const int path = forced;
@@ -523,6 +554,9 @@ int plan_softmax_impl(int64_t M, int64_t N, int64_t ld, int vector_ok_in, int sm
     case RRS_PATH_TWO_PHASE:
       plan_two_phase(M, N, sm_count, p);
       return RRS_OK;
+    case RRS_PATH_TWO_PASS:
+      if (plan_row_two_pass(M, N, sm_count, vector_ok != 0, p)) return RRS_OK;
+      return fail(RRS_ERR_UNSUPPORTED, "TWO_PASS needs 2 x rows x chunks <= INT_MAX");
     default:
       return fail(RRS_ERR_UNSUPPORTED, "path not available");
   }
@@ -932,6 +966,14 @@ RRS_API int softmax_rows_ex(const float* x, int64_t ldx, float* y, int64_t ldy, 
       e = launch_softmax_two_phase(plan, x, y, M, N, l, ws, s);
       break;
     }
+    case RRS_PATH_TWO_PASS: {
+      void* ws = nullptr;
+      unsigned* herr = nullptr;
+      if ((st = host_err_word(dev, s, &herr)) != RRS_OK) return st;
+      if ((st = get_workspace(dev, s, kWsRowsTwoPass, (size_t)plan.workspace_bytes, &ws)) != RRS_OK) return st;
+      e = launch_softmax_rows_two_pass(plan, x, y, M, N, l, ws, g_fault.load() == 2 ? 1 : 0, herr, s);
+      break;
+    }
     default:
       return fail(RRS_ERR_UNSUPPORTED, "planned path has no launcher");
   }
@@ -1147,15 +1189,16 @@ RRS_API int rrs_device_error(void* stream) {
   unsigned v = 0, w = 0;
   cudaError_t e = read_and_clear_staged_error(static_cast<cudaStream_t>(stream), &v);
   if (e == cudaSuccess) e = read_and_clear_attn_error(static_cast<cudaStream_t>(stream), &w);
-  unsigned c = 0;
+  unsigned c = 0, r2 = 0;
   if (e == cudaSuccess) e = read_and_clear_cols_error(static_cast<cudaStream_t>(stream), &c);
+  if (e == cudaSuccess) e = read_and_clear_rows_two_pass_error(static_cast<cudaStream_t>(stream), &r2);
   if (e != cudaSuccess) return fail_cuda(e, "rrs_device_error");
   int dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) {
     if (host_err_value(dev) != 0) v |= 1u;
     host_err_clear(dev);
   }
-  v |= w | c;
+  v |= w | c | r2;
   return v ? fail(RRS_ERR_TIMEOUT, "a split-row kernel stopped waiting for its peers") : RRS_OK;
 }
 

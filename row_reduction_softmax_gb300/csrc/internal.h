@@ -102,6 +102,20 @@ cudaError_t launch_softmax_staged_grid(const rrs_plan& p, const float* x, float*
 // return on their own.
 cudaError_t launch_occupy(int ctas, int smem_bytes, int64_t ns, cudaStream_t s);
 
+// ---- ROW_TWO_PASS (softmax_rows_two_pass.cu): plans carry chunk (floats
+// per item, rows_two_pass_chunk()), ctas_per_row (S, chunks per row),
+// stages (the lag D, S <= D <= M S), grid = 2 M S and vector_io (float4
+// when x, y, the strides and N allow); the workspace holds the arrival
+// counter in its first kRowsTwoPassArrivalBytes, then 16 bytes per (row,
+// chunk).  fault != 0: item 0's pair is never published (fault injection).
+constexpr int64_t kRowsTwoPassArrivalBytes = 128;
+int rows_two_pass_threads();
+int rows_two_pass_chunk();
+cudaError_t launch_softmax_rows_two_pass(const rrs_plan& p, const float* x, float* y, int64_t M, int64_t N,
+                                         const Layout& l, void* workspace, int fault, unsigned* host_err,
+                                         cudaStream_t s);
+cudaError_t read_and_clear_rows_two_pass_error(cudaStream_t s, unsigned* value);
+
 // ---- column softmax (softmax_cols.cu): COLS_CLUSTER plans carry cluster
 // (CTAs per band of cols_band() columns) and vec (rows per thread; a CTA
 // holds cols_row_groups() x vec rows); COLS_TWO_PHASE plans carry

@@ -43,6 +43,7 @@
 #include "internal.h"
 #include "launch_util.h"
 #include "sm100_async.cuh"
+#include "two_pass_common.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -250,13 +251,6 @@ __device__ __forceinline__ float4 load_evict_last(const float4* p, uint64_t pol)
   return v;
 }
 
-// 2^((v - m) log2 e) for a pair: v - m as v + (-m), exact like the scalar
-// subtraction, then the scalar's rounding of the product.
-__device__ __forceinline__ uint64_t exp_shifted2(float va, float vb, uint64_t neg_m2, uint64_t log2e2) {
-  float ta, tb;
-  f2_unpack(f2_mul(f2_add(f2_pack(va, vb), neg_m2), log2e2), ta, tb);
-  return f2_pack(exp2_sfu(ta), exp2_sfu(tb));
-}
 
 // A batch of kBU rows of a thread's four columns folded into its online
 // (max, sum) pairs: the batch's column max rescales each pair once, then the
@@ -504,42 +498,8 @@ softmax_cols_band_kernel(const float* x, float* y, int64_t M, int64_t N, int64_t
 // bounded (1 s), and on timeout the CTA sets the error words and leaves its
 // slice of y unwritten.  Every element is read by pass 1 of its slice before
 // pass 2 writes it, so x == y (in place) is safe.
-constexpr uint64_t kColsWaitNs = 1000000000ull;
+constexpr uint64_t kColsWaitNs = kTwoPassWaitNs;
 constexpr unsigned kColsErrTimeout = 1u;
-
-__host__ __device__ inline void two_pass_item(int64_t t, int64_t Q, int64_t D, int* pass, int64_t* k) {
-  if (t < D) {
-    *pass = 1;
-    *k = t;
-    return;
-  }
-  const int64_t u = t - D;
-  if (u < 2 * (Q - D)) {
-    *pass = (u & 1) ? 2 : 1;
-    *k = (u & 1) ? (u >> 1) : D + (u >> 1);
-    return;
-  }
-  *pass = 2;
-  *k = (Q - D) + (u - 2 * (Q - D));
-}
-
-__device__ __forceinline__ uint64_t cols_tagged(uint32_t ticket, float v) {
-  return ((uint64_t)ticket << 32) | (uint64_t)__float_as_uint(v);
-}
-
-// The arrival index of this CTA among the `draws` of its launch, and the
-// launch's ticket; the last of the draws opens the next epoch.
-__device__ __forceinline__ unsigned draw_arrival(unsigned long long* arrivals, unsigned draws, unsigned* ticket) {
-  const unsigned long long old = atomicAdd(arrivals, 1ull);
-  const unsigned a = (unsigned)(old & 0xffffffffull);
-  const unsigned epoch = (unsigned)(old >> 32);
-  if (a == draws - 1) {
-    atomicExch(arrivals, (unsigned long long)(epoch == 0xfffffffeu ? 0u : epoch + 1u) << 32);
-    __threadfence();
-  }
-  *ticket = epoch + 1u;   // never 0, the tag of a zero-filled slot
-  return a;
-}
 
 // The item of a COLS_TWO_PASS CTA (t: its arrival index), by the whole
 // CTA.  gave_up: set when the CTA's wait ran out; its slice of y is then
@@ -611,8 +571,8 @@ __device__ __forceinline__ void two_pass_run(const float* x, float* y, int64_t M
 #pragma unroll
       for (int w = 0; w < kCW; ++w) q = merge(q, red[w][tid]);
       uint64_t* sl = slots + 2 * (k * kBand + tid);
-      publish_gpu_u64(sl, cols_tagged(ticket, q.m));
-      publish_gpu_u64(sl + 1, cols_tagged(ticket, q.s));
+      publish_gpu_u64(sl, tagged_word(ticket, q.m));
+      publish_gpu_u64(sl + 1, tagged_word(ticket, q.s));
     }
     return;
   }

@@ -10,8 +10,9 @@
 // first use of a stream; this entry point never does.  Where softmax_rows
 // would run a kernel that needs no workspace (the register kernel or the
 // cluster split), it runs that same kernel; where it would run the grid
-// split, it runs that kernel with its workspace in a fixed array of device
-// memory that is part of the library image (when the shape's slots fit);
+// split or the two-pass split, it runs that kernel with its workspace in a
+// fixed array of device memory that is part of the library image (when the
+// shape's slots fit);
 // otherwise it runs the two-phase kernels (per-chunk (max, sum) partials,
 // then merge, re-read and write) with the partials in another such array.
 //
@@ -43,10 +44,10 @@ constexpr int64_t kNoAllocMinChunk = 4096;
 
 static __device__ __align__(256) MaxSum g_noalloc_partials[kNoAllocPairs];
 
-// The grid split's workspace (its arrival counter, then 16 bytes per (row,
-// segment) slot).  Zero at load, and each launch leaves it ready for the
-// next: the last CTA to draw opens the next epoch, and a slot only counts
-// when it carries the current launch's ticket.
+// The grid and two-pass splits' workspace (an arrival counter, then 16
+// bytes per (row, segment) or (row, chunk) slot).  Zero at load, and each
+// launch leaves it ready for the next: the last CTA to draw opens the next
+// epoch, and a slot only counts when it carries the current launch's ticket.
 constexpr int64_t kNoAllocGridBytes = 1 << 20;
 static __device__ __align__(256) unsigned char g_noalloc_grid_ws[kNoAllocGridBytes];
 
@@ -126,11 +127,17 @@ extern "C" RRS_API int softmax_rows_noalloc(const float* x, float* y, int64_t M,
   }
   NoAllocDevice d;
   if ((st = noalloc_device(dev, &d)) != RRS_OK) return st;
-  if (planned && plan.path == RRS_PATH_GRID && plan.workspace_bytes <= kNoAllocGridBytes) {
-    // A wait that runs out sets the device error word (rrs_device_error);
-    // the host word that makes later calls refuse is used only if an
-    // earlier call made it, since making it allocates.
-    e = launch_softmax_staged_grid(plan, x, y, M, N, l, d.grid_ws, 0, host_err_word_if_made(dev), s);
+  if (planned && (plan.path == RRS_PATH_GRID || plan.path == RRS_PATH_TWO_PASS) &&
+      plan.workspace_bytes <= kNoAllocGridBytes) {
+    // Both kernels keep an arrival counter (epoch << 32 | count) and
+    // ticket-tagged slots in the same layout, so they share the array: each
+    // launch opens the next epoch for whichever comes next.  A wait that
+    // runs out sets the device error word (rrs_device_error); the host word
+    // that makes later calls refuse is used only if an earlier call made it,
+    // since making it allocates.
+    unsigned* herr = host_err_word_if_made(dev);
+    e = plan.path == RRS_PATH_GRID ? launch_softmax_staged_grid(plan, x, y, M, N, l, d.grid_ws, 0, herr, s)
+                                   : launch_softmax_rows_two_pass(plan, x, y, M, N, l, d.grid_ws, 0, herr, s);
     if (e != cudaSuccess) return fail_cuda(e, "softmax_rows_noalloc launch");
     return RRS_OK;
   }

@@ -120,8 +120,12 @@ def test_planner_unaligned_takes_scalar_path(lib):
     assert p["vec"] * 32 * p["warps_per_row"] * 4 >= 1000
     p = plan(100, 20000, ld=20001, vector_ok=False)       # long rows: scalar cluster split
     assert p["path_name"] == "cluster" and p["vector_io"] == 0
-    p = plan(100, 131075, ld=131075, vector_ok=False)     # beyond 16 CTAs' registers: scalar two-phase
-    assert p["path_name"] == "two_phase" and p["vector_io"] == 0
+    p = plan(100, 131075, ld=131075, vector_ok=False)     # beyond 16 CTAs' registers: scalar two-pass
+    assert p["path_name"] == "two_pass" and p["vector_io"] == 0
+    p = plan(4, 1 << 24)                                    # past the grid, 2048 chunks a row: two-phase
+    assert p["path_name"] == "two_phase"
+    p = plan(32, 1048575, ld=1048576)                       # ragged past the cluster: scalar two-pass
+    assert p["path_name"] == "two_pass" and p["vector_io"] == 0
     p = plan(100, 50257, ld=50260)                          # aligned rows, N % 4 != 0: cluster with a tail
     assert p["path_name"] == "cluster" and p["vector_io"] == 1
 
@@ -414,3 +418,20 @@ def test_cols_two_pass_plan(lib, M, N):
     R, S, D = p["chunk"], p["ctas_per_row"], p["stages"]
     assert S == -(-M // R) and S <= D <= bands * S and p["grid"] == 2 * bands * S
     assert p["workspace_bytes"] == 128 + bands * S * 32 * 16
+
+
+@pytest.mark.parametrize("M,N,ld,vec", [(1, 1, 1, False), (3, 8192, 8192, True), (3, 8193, 8196, True),
+                                        (32, 1 << 20, 1 << 20, True), (4, 300001, 300003, False),
+                                        (2, 5_000_000, 5_000_000, True)])
+def test_row_two_pass_plan(lib, M, N, ld, vec):
+    import row_reduction_softmax_gb300 as rrs
+    rrs.force_path("two_pass")
+    try:
+        p = plan(M, N, ld=ld, vector_ok=vec)
+    finally:
+        rrs.force_path("auto", "auto")
+    assert p["path_name"] == "two_pass" and p["threads"] == 256 and p["chunk"] == 8192
+    S = -(-N // 8192)
+    assert p["ctas_per_row"] == S and S <= p["stages"] <= M * S and p["grid"] == 2 * M * S
+    assert p["workspace_bytes"] == 128 + M * S * 16
+    assert p["vector_io"] == (1 if vec and N % 4 == 0 else 0)   # float4 only for whole float4 rows

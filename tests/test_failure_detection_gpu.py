@@ -220,3 +220,58 @@ def test_two_cols_two_pass_calls_at_once_on_two_streams(lib):
     assert rrs.device_error() == 0
     for k in range(2):
         check_softmax_cols(dy[k].cpu().numpy(), xs[k], f"cols two-pass on stream {k}")
+
+
+def test_rows_two_pass_wait_runs_out_and_is_reported(lib):
+    """The rows' two-pass path: with item 0's pair withheld, row 0's second
+    passes give up after their bounded wait and leave their chunks unwritten;
+    the status is reported, later calls are refused until it is collected,
+    and the path is right again afterwards."""
+    M, N = 4, 100003
+    x_host = workloads.matrix(workloads.WORKLOADS["c5"].with_shape(M, N))
+    x = torch.from_numpy(x_host).cuda()
+    y = torch.full_like(x, float("nan"))
+    try:
+        rrs.force_path("two_pass")
+        assert rrs.device_error() == 0
+        assert lib.rrs_inject_fault(2) == 0
+        rrs.softmax_rows(x, y)                      # enqueued: RRS_OK
+        lib.rrs_inject_fault(0)
+        torch.cuda.synchronize()
+        with pytest.raises(rrs.RRSError) as e:
+            rrs.softmax_rows(x, y)
+        assert e.value.status == TIMEOUT
+        assert rrs.device_error() == TIMEOUT
+        assert rrs.device_error() == 0
+        assert bool(torch.isnan(y[0]).all())        # row 0 was never written
+        rrs.softmax_rows(x, y)
+        torch.cuda.synchronize()
+        assert rrs.device_error() == 0
+        check_softmax(y.cpu().numpy(), x_host, "rows two-pass after an injected timeout")
+    finally:
+        lib.rrs_inject_fault(0)
+        rrs.force_path("auto", "auto")
+
+
+@pytest.mark.parametrize("held", [0.5, 0.9])
+def test_rows_two_pass_runs_while_other_work_holds_sms(lib, held):
+    """Unaligned long rows (the two-pass path) beside another stream's CTAs
+    holding most SMs for 50 ms: no timeout, every row right."""
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    M, N, ld = 16, 1048577, 1048579
+    x_host = workloads.matrix(workloads.WORKLOADS["c5"].with_shape(M, N))
+    xb = torch.zeros(M * ld + 4, device="cuda")
+    xv = xb[1:1 + M * ld].view(M, ld)
+    xv[:, :N].copy_(torch.from_numpy(x_host))
+    yb = torch.full((M * ld + 4,), float("nan"), device="cuda")
+    yv = yb[1:1 + M * ld].view(M, ld)
+    assert rrs.plan_softmax(M, N, ld, False, props.multi_processor_count)["path_name"] == "two_pass"
+    other = torch.cuda.Stream()
+    for trial in range(2):
+        torch.cuda.synchronize()
+        assert lib.rrs_test_occupy(int(props.multi_processor_count * held),
+                                   props.shared_memory_per_block_optin, 50_000_000, other.cuda_stream) == 0
+        rrs.softmax_rows_ptr(xv.data_ptr(), yv.data_ptr(), M, N, ld, torch.cuda.current_stream().cuda_stream)
+        torch.cuda.synchronize()
+        assert rrs.device_error() == 0
+        check_every_row(check_softmax, yv[:, :N], x_host, f"rows two-pass beside {held:.0%} held SMs, trial {trial}")

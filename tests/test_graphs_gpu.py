@@ -35,7 +35,8 @@ def _plan_path(M, N):
 
 
 @pytest.mark.parametrize("name,M,N,path", [("c1", 128, 256, "row_regs"), ("c3", 8, 32768, "cluster"),
-                                           ("c5", 32, 1 << 20, "grid"), ("c5", 6, 300001, "two_phase")])
+                                           ("c5", 32, 1 << 20, "grid"), ("c5", 6, 300001, "two_phase"),
+                                           ("c5", 6, 300001, "two_pass")])
 def test_softmax_replayed_from_a_graph(name, M, N, path):
     x1 = workloads.matrix(workloads.WORKLOADS[name].with_shape(M, N))
     x2 = np.flip(x1, axis=1).copy() * np.float32(-0.5)          # other values, other row maxima

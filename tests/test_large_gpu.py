@@ -64,7 +64,7 @@ def check_all_rows_sum_to_one(y, where: str):
 
 
 @pytest.mark.parametrize("path,N", [("row_regs", 4096), ("cluster", 32768), ("grid", 1 << 20),
-                                    ("two_phase", 1 << 20), ("two_phase", 4096)])
+                                    ("two_phase", 1 << 20), ("two_phase", 4096), ("two_pass", 1 << 20)])
 def test_softmax_rows_past_2_31_elements(lib, path, N):
     M = LIMIT // N + 3
     assert M * N > LIMIT

@@ -18,7 +18,7 @@ from gpu_helpers import Guarded, check_every_row, check_softmax
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-PATHS = ["row_regs", "cluster", "two_phase", "row_staged", "grid"]
+PATHS = ["row_regs", "cluster", "two_phase", "row_staged", "grid", "two_pass"]
 
 SHAPES = [(1, 1), (3, 2), (5, 3), (7, 5), (4, 31), (9, 33), (16, 128), (17, 129), (128, 256),
           (33, 1000), (8, 1024), (5, 2047), (3, 2049), (6, 4097), (4, 8191), (2, 16385),
@@ -94,19 +94,23 @@ def test_unaligned_takes_scalar_path(M, N, ld, x_off, y_off):
     """Rows whose start or stride is not 16-byte aligned: the scalar register
     kernel up to 4096, the scalar register kernel or the scalar cluster split
     up to 16384, the scalar cluster split up to 131072 (each CTA's segment in
-    four-scalar slots), the scalar two-phase split beyond."""
+    four-scalar slots), the scalar two-pass split beyond; the two-pass split
+    forced on every shape too."""
     x = recipe("c2", M, N)
     y, guards = run(x, N, ld, "auto", x_off, y_off)
     check_softmax(y, x, f"unaligned {M}x{N} ld={ld}")
     assert guards
     want = {"row_regs"} if N <= 4096 else ({"row_regs", "cluster"} if N <= 16384 else
-                                           {"cluster"} if N <= 131072 else {"two_phase"})
+                                           {"cluster"} if N <= 131072 else {"two_pass"})
     assert rrs.plan_softmax(M, N, ld, False, torch.cuda.get_device_properties(0).multi_processor_count)[
         "path_name"] in want
     if N <= 32768:
         y, guards = run(x, N, ld, "row_regs", x_off, y_off)    # the scalar row kernel
         check_softmax(y, x, f"unaligned row_regs {M}x{N} ld={ld}")
         assert guards
+    y, guards = run(x, N, ld, "two_pass", x_off, y_off)        # the scalar two-pass kernel
+    check_softmax(y, x, f"unaligned two_pass {M}x{N} ld={ld}")
+    assert guards
     if N <= 131072:
         y, guards = run(x, N, ld, "cluster", x_off, y_off)     # the scalar cluster kernel
         check_softmax(y, x, f"unaligned cluster {M}x{N} ld={ld}")
@@ -223,7 +227,7 @@ def test_rejects_host_memory():
 
 
 @pytest.mark.parametrize("name", ["c2", "c4"])
-@pytest.mark.parametrize("path", ["auto", "cluster", "two_phase"])
+@pytest.mark.parametrize("path", ["auto", "cluster", "two_phase", "two_pass"])
 def test_input_written_just_before_reads_back_intact(name, path):
     """x written by kernels right before the call -- its lines still dirty in
     the L2 -- is read back unchanged by a later kernel, and the softmax of it
@@ -287,7 +291,7 @@ def test_full_size_workload(name):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("path", ["grid", "two_phase"])
+@pytest.mark.parametrize("path", ["grid", "two_phase", "two_pass"])
 def test_full_size_long_rows_on_each_split_path(path):
     """32 rows of 2^20 on every path that splits a row over CTAs, every row checked."""
     w = workloads.WORKLOADS["c5"]

@@ -4,7 +4,7 @@ ctypes releases the GIL during a foreign call, so these calls run inside the
 library concurrently: the per-(device, stream) workspace cache, the device
 table and the error words are shared state behind a mutex or atomics, and
 each thread's messages are its own.  Each thread runs a different path (row
-registers, cluster split in both forms, two-phase split with its
+registers, cluster split in both forms, two-pass split with its
 workspace, split row sum with its workspace) many times on its own buffers;
 every result is then compared with the float64 oracle.
 """
@@ -25,7 +25,7 @@ pytestmark = pytest.mark.gpu
 # (op, workload recipe, M, N, ld, the path the planner picks)
 JOBS = [("softmax", "c2", 256, 1024, 1024, "row_regs"),
         ("softmax", "c3", 8, 32768, 32768, "cluster"),
-        ("softmax", "c4", 4, 140000, 140001, "two_phase"),  # unaligned past 131072: the scalar two-phase path
+        ("softmax", "c4", 4, 140000, 140001, "two_pass"),   # unaligned past 131072: the scalar two-pass path
         ("softmax", "c2", 6, 40000, 40001, "cluster"),      # unaligned: the scalar cluster split
         ("row_sum", "c3", 8, 200000, 200000, "split"),
         ("softmax", "c4", 64, 4096, 4096, "row_regs"),

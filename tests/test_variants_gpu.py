@@ -123,7 +123,7 @@ def test_log_softmax_small(path, M, N):
 
 
 @pytest.mark.parametrize("path,N", [(p, N) for N in [2, 8, 1024, 5000, 40000]
-                                    for p in ["row_regs", "cluster", "two_phase", "grid"] if supports(p, N, N)])
+                                    for p in ["row_regs", "cluster", "two_phase", "grid", "two_pass"] if supports(p, N, N)])
 def test_log_softmax_special_values(path, N):
     rng = np.random.default_rng(N + 7)
     x = rng.normal(0, 3, size=(8, N)).astype(np.float32)
