@@ -82,6 +82,7 @@ STEADY = [
     ("row_reduce_rows_c3.md", 4 * 4096 * 32768, 4 * 4096, 0.0, 0.01, 0.001),
     ("softmax_cols_two_pass_cols_c4.md", 4 * 4096 * 16384, 4 * 4096 * 16384, 0.97, 0.10, 0.01),
     ("softmax_cols_band_cols_c2.md", 4 * 1024 * 8192, 4 * 1024 * 8192, 0.85, 0.10, 0.25),
+    ("softmax_rows_two_pass_c5.md", 4 * 32 * 1048576, 4 * 32 * 1048576, 0.97, 0.10, 0.001),
     ("gelu_kernel_gelu_16k.md", 4 * 16384 * 16384, 4 * 16384 * 16384, 0.99, 0.01, 0.001),
 ]
 
