@@ -635,7 +635,7 @@ void plan_cols_band(int64_t M, int64_t N, int sm_count, rrs_plan* p) {
 constexpr int64_t kColsTwoPassRows = 512;
 constexpr int64_t kColsTwoPassLagPerSm = 3;
 
-bool plan_cols_two_pass(int64_t M, int64_t N, int sm_count, rrs_plan* p) {
+bool plan_cols_two_pass(int64_t M, int64_t N, int sm_count, bool vector_ok, rrs_plan* p) {
   const int64_t bands = ceil_div(N, cols_band());
   const int64_t R = kColsTwoPassRows;
   const int64_t S = ceil_div(M, R);
@@ -650,7 +650,7 @@ bool plan_cols_two_pass(int64_t M, int64_t N, int sm_count, rrs_plan* p) {
   p->stages = (int32_t)D;
   p->rows_per_cta = (int32_t)R;
   p->workspace_bytes = kColsArrivalBytes + Q * cols_band() * 16;
-  p->vector_io = 1;
+  p->vector_io = vector_ok ? 1 : 0;
   return true;
 }
 
@@ -679,12 +679,18 @@ int plan_cols_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_count
     // and ties or loses with 16-32 slices (8192 x 4096: 57.8 against 57.2,
     // 16384 x 2048: 63.3-65.8 against 63.0-63.7).
     rrs_plan t{};
-    if (vector_ok && plan_cols_two_pass(M, N, sm_count, &t) && t.ctas_per_row <= 8 &&
+    if (vector_ok && plan_cols_two_pass(M, N, sm_count, true, &t) && t.ctas_per_row <= 8 &&
         (int64_t)t.ctas_per_row * ceil_div(N, cols_band()) >= 2 * kColsTwoPassLagPerSm * (int64_t)sm_count) {
       *p = t;
     } else if (cluster_fits && bands_fit_grid(N)) {
       plan_cols_band(M, N, sm_count, p);
       p->vector_io = 1;
+    } else if (!vector_ok && plan_cols_two_pass(M, N, sm_count, false, &t) && t.ctas_per_row <= 8) {
+      // unaligned: the two-pass path's scalar form beats the two-phase pair
+      // at every size measured (4096 x 16384, ld 16385: 166.8 against 207.9
+      // us; 1024 x 8192, ld 8193: 28.3 against 34.1; 2048 x 65536, ld 65537,
+      // offset 3 floats: 317.9 against 402.3)
+      *p = t;
     } else {
       plan_cols_two_phase(M, N, sm_count, p);
       p->vector_io = vector_ok ? 1 : 0;
@@ -712,8 +718,8 @@ int plan_cols_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_count
     return fail(RRS_ERR_UNSUPPORTED, "COLS_BAND needs 16-byte alignment and cluster launch");
   }
   if (forced == RRS_COLS_TWO_PASS) {
-    if (vector_ok && plan_cols_two_pass(M, N, sm_count, p)) return RRS_OK;
-    return fail(RRS_ERR_UNSUPPORTED, "COLS_TWO_PASS needs 16-byte alignment and 2 x items <= INT_MAX");
+    if (plan_cols_two_pass(M, N, sm_count, vector_ok != 0, p)) return RRS_OK;
+    return fail(RRS_ERR_UNSUPPORTED, "COLS_TWO_PASS needs 2 x items <= INT_MAX");
   }
   return fail(RRS_ERR_UNSUPPORTED, "column path not available");
 }

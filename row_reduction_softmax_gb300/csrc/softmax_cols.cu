@@ -504,7 +504,7 @@ constexpr unsigned kColsErrTimeout = 1u;
 // The item of a COLS_TWO_PASS CTA (t: its arrival index), by the whole
 // CTA.  gave_up: set when the CTA's wait ran out; its slice of y is then
 // left unwritten.
-template <bool LOG>
+template <bool LOG, bool V4>
 __device__ __forceinline__ void two_pass_run(const float* x, float* y, int64_t M, int64_t N, int64_t ldx,
                                              int64_t ldy, int64_t R, int64_t S, int64_t bands, int64_t D,
                                              uint64_t* __restrict__ slots, int32_t fault, unsigned* host_err,
@@ -526,19 +526,22 @@ __device__ __forceinline__ void two_pass_run(const float* x, float* y, int64_t M
   const float* xs = x + r0 * ldx + j0;   // the slice's first row, this thread's columns
   const uint64_t log2e2 = f2_pack(kLog2e, kLog2e);
 
+  // V4: a thread's four columns as one float4 (x, y 16-byte aligned, strides
+  // multiples of 4); otherwise four scalars
   auto load4 = [&](const float* q, bool keep, uint64_t pol) -> float4 {
-    if (ncol == 4) return keep ? load_evict_last(reinterpret_cast<const float4*>(q), pol)
-                               : load_stream(reinterpret_cast<const float4*>(q));
+    if (V4 && ncol == 4) return keep ? load_evict_last(reinterpret_cast<const float4*>(q), pol)
+                                     : load_stream(reinterpret_cast<const float4*>(q));
     float4 v;
     v.x = (ncol > 0) ? q[0] : kNeg;
     v.y = (ncol > 1) ? q[1] : kNeg;
     v.z = (ncol > 2) ? q[2] : kNeg;
-    v.w = kNeg;
+    v.w = (ncol > 3) ? q[3] : kNeg;
     return v;
   };
   // a batch is whole when its last row is inside the slice and the four
-  // columns are: then it needs no per-row check (pass 1's row groups)
-  auto whole_batch = [&](int i) { return ncol == 4 && i + (kBU - 1) * kGroups < nrows; };
+  // columns are (float4 access): then it needs no per-row check (pass 1's
+  // row groups)
+  auto whole_batch = [&](int i) { return V4 && ncol == 4 && i + (kBU - 1) * kGroups < nrows; };
 
   if (pass == 1) {
     const uint64_t pol = l2_evict_last_policy();
@@ -664,12 +667,13 @@ __device__ __forceinline__ void two_pass_run(const float* x, float* y, int64_t M
       for (int u = 0; u < kBU; ++u, o += ystep) {
         if (i + u * kGroups >= nrows) continue;
         const float4 v = normalise(a2[u]);
-        if (ncol == 4) {
+        if (V4 && ncol == 4) {
           store_stream(reinterpret_cast<float4*>(o), v);
         } else {
           if (ncol > 0) store_stream(o + 0, v.x);
           if (ncol > 1) store_stream(o + 1, v.y);
           if (ncol > 2) store_stream(o + 2, v.z);
+          if (ncol > 3) store_stream(o + 3, v.w);
         }
       }
     }
@@ -681,7 +685,7 @@ __device__ __forceinline__ void two_pass_run(const float* x, float* y, int64_t M
   }
 }
 
-template <bool LOG>
+template <bool LOG, bool V4>
 __global__ void __launch_bounds__(kCT, 4)
 softmax_cols_two_pass_kernel(const float* x, float* y, int64_t M, int64_t N, int64_t ldx, int64_t ldy,
                              int64_t R, int64_t S, int64_t bands, int64_t D,
@@ -698,7 +702,7 @@ softmax_cols_two_pass_kernel(const float* x, float* y, int64_t M, int64_t N, int
   }
   __syncthreads();
   pdl_entry();
-  two_pass_run<LOG>(x, y, M, N, ldx, ldy, R, S, bands, D, slots, fault, host_err, (int64_t)drawn[0], drawn[1], red,
+  two_pass_run<LOG, V4>(x, y, M, N, ldx, ldy, R, S, bands, D, slots, fault, host_err, (int64_t)drawn[0], drawn[1], red,
                     whole, &gave_up);
 }
 
@@ -903,16 +907,16 @@ cudaError_t launch_softmax_cols_two_pass(const rrs_plan& p, const float* x, floa
                                          unsigned* host_err, cudaStream_t s) {
   const int64_t bands = (N + kBand - 1) / kBand;
   const int64_t R = p.chunk, S = p.ctas_per_row, D = p.stages;
-  if (p.threads != kCT || !p.vector_io || R < 1 || S != (M + R - 1) / R || D < S || D > bands * S ||
+  if (p.threads != kCT || R < 1 || S != (M + R - 1) / R || D < S || D > bands * S ||
       p.grid != 2 * bands * S || p.grid > (int64_t)INT_MAX)
     return cudaErrorInvalidConfiguration;
   auto* arrivals = static_cast<unsigned long long*>(workspace);
   uint64_t* slots = reinterpret_cast<uint64_t*>(static_cast<unsigned char*>(workspace) + kColsArrivalBytes);
   const dim3 grid((unsigned)p.grid), block(kCT);
-  return l.log_out ? launch_pdl(softmax_cols_two_pass_kernel<true>, grid, block, 0, s, 0, x, y, M, N, l.ldx,
-                                l.ldy, R, S, bands, D, arrivals, slots, (int32_t)fault, host_err)
-                   : launch_pdl(softmax_cols_two_pass_kernel<false>, grid, block, 0, s, 0, x, y, M, N, l.ldx,
-                                l.ldy, R, S, bands, D, arrivals, slots, (int32_t)fault, host_err);
+  auto k = p.vector_io ? (l.log_out ? softmax_cols_two_pass_kernel<true, true> : softmax_cols_two_pass_kernel<false, true>)
+                       : (l.log_out ? softmax_cols_two_pass_kernel<true, false> : softmax_cols_two_pass_kernel<false, false>);
+  return launch_pdl(k, grid, block, 0, s, 0, x, y, M, N, l.ldx, l.ldy, R, S, bands, D, arrivals, slots,
+                    (int32_t)fault, host_err);
 }
 
 void cols_two_pass_item(int64_t t, int64_t Q, int64_t D, int* pass, int64_t* k) { two_pass_item(t, Q, D, pass, k); }

@@ -286,15 +286,38 @@ def test_cols_band_three_ctas_per_sm(M, N):
         assert guards
 
 
-def test_cols_unaligned_takes_two_phase():
+def test_cols_unaligned_takes_the_scalar_paths():
+    """x and y not 16-byte aligned, strides not multiples of 4: the planner's
+    choice (the two-pass path's scalar form) and both scalar paths forced are
+    right, in the log form too; the float4-only paths refuse."""
     x = recipe("c2", 77, 301)
-    y, guards = run_cols(x, 301, 303, 305, "auto", x_off=1, y_off=3)
-    check_softmax_cols(y, x, "cols unaligned")
-    assert guards
-    for path in ("cluster", "band", "two_pass"):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert rrs.plan_softmax_cols(77, 301, 305, vector_ok=False, sm_count=sms)["path_name"] == "two_pass"
+    for path in ("auto", "two_pass", "two_phase"):
+        for flags, log in ((0, False), (LOG, True)):
+            y, guards = run_cols(x, 301, 303, 305, path, flags, x_off=1, y_off=3)
+            check_softmax_cols(y, x, f"cols unaligned {path} log={log}", log=log)
+            assert guards
+    for path in ("cluster", "band"):
         with pytest.raises(rrs.RRSError) as e:
             run_cols(x, 301, 303, 305, path, x_off=1, y_off=3)
         assert e.value.status == 6
+
+
+# Unaligned shapes on the scalar two-pass path with items enough to
+# interleave, every column against the oracle, and in place.
+@pytest.mark.parametrize("M,N,ld,off", [(4096, 4100, 4101, 1), (2048, 9001, 9003, 3)])
+def test_cols_two_pass_scalar_form(M, N, ld, off):
+    x = recipe("c4", M, N)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert rrs.plan_softmax_cols(M, N, ld, vector_ok=False, sm_count=sms)["path_name"] == "two_pass"
+    y, guards = run_cols(x, N, ld, ld, "auto", x_off=off, y_off=off)
+    check_softmax_cols(y, x, f"cols scalar two-pass {M}x{N} ld={ld}")
+    assert guards
+    y, guards = run_cols(x, N, ld, ld, "auto", in_place=True, x_off=off)
+    check_softmax_cols(y, x, f"cols scalar two-pass in place {M}x{N}")
+    assert guards
+    assert rrs.device_error() == 0
 
 
 # The planner's boundary between the band and the two-pass paths: at least
