@@ -436,3 +436,13 @@ def test_row_two_pass_plan(lib, M, N, ld, vec):
     assert p["ctas_per_row"] == S and S <= p["stages"] <= M * S and p["grid"] == 2 * M * S
     assert p["workspace_bytes"] == 128 + M * S * 16
     assert p["vector_io"] == (1 if vec and N % 4 == 0 else 0)   # float4 only for whole float4 rows
+
+
+@pytest.mark.parametrize("N,path", [(2_097_152, "two_pass"), (2_097_153, "two_phase")])
+def test_unaligned_long_rows_between_two_pass_and_two_phase(lib, N, path):
+    """Rows the grid split cannot align take the two-pass split up to 256
+    chunks of 8192 floats a row, the two-phase pair past that."""
+    p = plan(8, N, ld=N + 1, vector_ok=False)
+    assert p["path_name"] == path and p["vector_io"] == 0
+    if path == "two_pass":
+        assert p["ctas_per_row"] == 256
