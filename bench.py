@@ -653,7 +653,7 @@ def run_variants(args, torch, rrs, dev, rank):
     W = dict(workloads.WORKLOADS)
     W.update(workloads.VARIANT_WORKLOADS)
     cases = [("c2", "log_softmax"), ("c3", "log_softmax"), ("c5", "log_softmax"),
-             ("c3", "softmax_in_place"), ("c3", "row_max"), ("c3", "row_mean"),
+             ("c3", "softmax_in_place"), ("c5", "softmax_unaligned"), ("c3", "row_max"), ("c3", "row_mean"),
              ("cols_c2", "softmax_cols"), ("cols_c4", "softmax_cols"), ("gelu_16k", "gelu")]
     entries = []
     for name, op in cases:
@@ -665,11 +665,25 @@ def run_variants(args, torch, rrs, dev, rank):
         reduce = op in ("row_max", "row_mean")
         alg = 4 * M * N + 4 * M if reduce else 8 * M * N
         npairs = l2_pairs(torch, alg)
-        xs = [torch.from_numpy(x_host).to(dev) for _ in range(npairs)]
-        ys = [torch.empty(M, dtype=torch.float32, device=dev) if reduce else
-              (xs[r] if op == "softmax_in_place" else torch.empty_like(xs[0]))
-              for r in range(npairs)]
-        if op != "softmax_in_place":
+        if op == "softmax_unaligned":
+            # rows one float past a 16-byte boundary, stride N + 1: no float4
+            # access, and x and y misaligned differently, so the planner's
+            # scalar paths (the two-pass split for rows this long)
+            ld_u = N + 1
+            xs, ys = [], []
+            for _ in range(npairs):
+                xb = torch.zeros(M * ld_u + 4, dtype=torch.float32, device=dev)
+                xv = xb[1:1 + M * ld_u].view(M, ld_u)
+                xv[:, :N].copy_(torch.from_numpy(x_host))
+                xs.append(xv)
+                yb = torch.zeros(M * ld_u + 4, dtype=torch.float32, device=dev)
+                ys.append(yb[2:2 + M * ld_u].view(M, ld_u))
+        else:
+            xs = [torch.from_numpy(x_host).to(dev) for _ in range(npairs)]
+            ys = [torch.empty(M, dtype=torch.float32, device=dev) if reduce else
+                  (xs[r] if op == "softmax_in_place" else torch.empty_like(xs[0]))
+                  for r in range(npairs)]
+        if op not in ("softmax_in_place", "softmax_unaligned"):
             touch(ys)
 
         def call(k, op=op, M=M, N=N):
@@ -679,6 +693,8 @@ def run_variants(args, torch, rrs, dev, rank):
                 rrs.softmax_rows_ex_ptr(x, N, y, N, M, N, rrs.LOG_SOFTMAX, sh)
             elif op == "softmax_in_place":
                 rrs.softmax_rows_ex_ptr(x, N, x, N, M, N, 0, sh)
+            elif op == "softmax_unaligned":
+                rrs.softmax_rows_ex_ptr(x, N + 1, y, N + 1, M, N, 0, sh)
             elif op == "row_max":
                 rrs.row_max_ptr(x, y, M, N, N, sh)
             elif op == "row_mean":
@@ -705,13 +721,23 @@ def run_variants(args, torch, rrs, dev, rank):
                  "l2": f"{npairs} rotating pair(s)"}
         if op == "softmax_cols":
             entry["path"] = rrs.plan_softmax_cols(M, N)["path_name"]
+        if op == "softmax_unaligned":
+            entry["path"] = rrs.plan_softmax(M, N, N + 1, False)["path_name"]
+            entry["ld"] = N + 1
         if rank == 0:
             # one fresh call on the original x, compared with the oracle on a sample
-            xs[0].copy_(torch.from_numpy(x_host))
+            if op == "softmax_unaligned":
+                xs[0][:, :N].copy_(torch.from_numpy(x_host))
+            else:
+                xs[0].copy_(torch.from_numpy(x_host))
             call(0)
             torch.cuda.synchronize()
             rows = sampled_rows(M, 6, w.seed)
-            if op in ("log_softmax", "softmax_in_place"):
+            if op == "softmax_unaligned":
+                got = ys[0][rows, :N].cpu().numpy().astype(np.float64)
+                want = oracle.softmax_rows(x_host[rows].astype(np.float64))
+                entry["parity"] = {"rows_checked": len(rows), "max_abs": float(np.max(np.abs(got - want)))}
+            elif op in ("log_softmax", "softmax_in_place"):
                 got = ys[0][rows].cpu().numpy().astype(np.float64)
                 want = (oracle.log_softmax_rows if op == "log_softmax" else oracle.softmax_rows)(
                     x_host[rows].astype(np.float64))
