@@ -433,8 +433,10 @@ bool plan_grid(int64_t M, int64_t N, int sm_count, int smem_optin, rrs_plan* p) 
 // ROW_TWO_PASS: items of rows_two_pass_chunk() floats, one CTA per (pass,
 // item), and a lag of kRowTwoPassLagPerSm x SMs items (at least S, at most
 // the item count); float4 access when x, y, the stride and N allow.
-constexpr int64_t kRowTwoPassLagPerSm = 3;
-constexpr int64_t kRowTwoPassMaxChunks = 256;   // a row's pairs in one round of the merging warp's loads
+// A lag of 4 x SMs against 3: 46.1 against 46.7 us on 32 x 2^20, 51.3
+// against 52.0 with those rows unaligned, 287 against 286 on 1024 x 200001.
+constexpr int64_t kRowTwoPassLagPerSm = 4;
+constexpr int64_t kRowTwoPassMaxChunks = 256;   // a row's pairs in two rounds of the merging warp's loads
 
 bool plan_row_two_pass(int64_t M, int64_t N, int sm_count, bool vector_ok, rrs_plan* p) {
   const int64_t S = ceil_div(N, rows_two_pass_chunk());

@@ -434,6 +434,7 @@ def test_row_two_pass_plan(lib, M, N, ld, vec):
     assert p["path_name"] == "two_pass" and p["threads"] == 256 and p["chunk"] == 8192
     S = -(-N // 8192)
     assert p["ctas_per_row"] == S and S <= p["stages"] <= M * S and p["grid"] == 2 * M * S
+    assert p["stages"] == min(M * S, max(S, 4 * 152))             # the lag: 4 x SMs, clamped
     assert p["workspace_bytes"] == 128 + M * S * 16
     assert p["vector_io"] == (1 if vec and N % 4 == 0 else 0)   # float4 only for whole float4 rows
 

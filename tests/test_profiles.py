@@ -69,8 +69,8 @@ def steady(name: str) -> dict:
 # summary file, bytes of x, bytes of y written (the softmax writes M N floats,
 # the row sum M), the DRAM writes expected at least (fraction of y: 32 MiB of
 # y partly stay dirty in the L2 between the bench's launches), the reads
-# allowed above the bytes of x (fraction: the column kernels re-read x, the
-# second time mostly from the L2), and the L2 write sectors allowed above the
+# allowed above the bytes of x (fraction: the column and row two-pass kernels
+# re-read x, the second time mostly from the L2), and the L2 write sectors allowed above the
 # bytes of y (fraction: the band kernel's 64-register build on cols_c2 spills
 # a few registers, and local-memory stores reach the L2 too; its
 # global-store sectors are then checked to be exactly y)
@@ -82,7 +82,7 @@ STEADY = [
     ("row_reduce_rows_c3.md", 4 * 4096 * 32768, 4 * 4096, 0.0, 0.01, 0.001),
     ("softmax_cols_two_pass_cols_c4.md", 4 * 4096 * 16384, 4 * 4096 * 16384, 0.97, 0.10, 0.01),
     ("softmax_cols_band_cols_c2.md", 4 * 1024 * 8192, 4 * 1024 * 8192, 0.85, 0.10, 0.25),
-    ("softmax_rows_two_pass_c5.md", 4 * 32 * 1048576, 4 * 32 * 1048576, 0.97, 0.10, 0.001),
+    ("softmax_rows_two_pass_c5.md", 4 * 32 * 1048576, 4 * 32 * 1048576, 0.97, 0.15, 0.001),
     ("gelu_kernel_gelu_16k.md", 4 * 16384 * 16384, 4 * 16384 * 16384, 0.99, 0.01, 0.001),
 ]
 
