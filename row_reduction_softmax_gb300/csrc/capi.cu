@@ -610,7 +610,7 @@ void plan_cols_two_phase(int64_t M, int64_t N, int sm_count, rrs_plan* p) {
 // that pass 2 re-reads within the L2.
 bool bands_fit_grid(int64_t N) { return ceil_div(N, cols_band()) * 8 <= (int64_t)INT_MAX; }
 
-void plan_cols_band(int64_t M, int64_t N, int sm_count, rrs_plan* p) {
+void plan_cols_band(int64_t M, int64_t N, rrs_plan* p) {
   const int64_t bands = ceil_div(N, cols_band());
   const int64_t max_rows = (M < 2048) ? 512 : 1024;
   int64_t cs = 1;
@@ -622,12 +622,10 @@ void plan_cols_band(int64_t M, int64_t N, int sm_count, rrs_plan* p) {
   p->ctas_per_row = cs;
   p->chunk = ceil_div(M, cs);
   p->rows_per_cta = (int32_t)std::min<int64_t>(p->chunk, INT_MAX);
-  // vec: the CTAs per SM the kernel's registers are budgeted for.  Measured
-  // on GB300: 3 (80 registers) takes 4096 x 16384 from 119.6 to 111.0 us,
-  // but a grid of one wave at 4 per SM (1024 x 8192: 512 CTAs) spills into
-  // a second wave at 3 (17.7 -> 20.3 us); so 3 only when the grid fills at
-  // least three waves of it.
-  p->vec = (p->grid >= 9 * (int64_t)sm_count) ? 3 : 4;
+  // vec: the CTAs per SM the kernel's registers are budgeted for, four (a
+  // budget of three, once faster on grids of three or more such waves, lost
+  // everywhere once the four-CTA build stopped spilling)
+  p->vec = 4;
 }
 
 // COLS_TWO_PASS: slices of kColsTwoPassRows rows, one CTA per (pass,
@@ -685,7 +683,7 @@ int plan_cols_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_count
         (int64_t)t.ctas_per_row * ceil_div(N, cols_band()) >= 2 * kColsTwoPassLagPerSm * (int64_t)sm_count) {
       *p = t;
     } else if (cluster_fits && bands_fit_grid(N)) {
-      plan_cols_band(M, N, sm_count, p);
+      plan_cols_band(M, N, p);
       p->vector_io = 1;
     } else if (!vector_ok && plan_cols_two_pass(M, N, sm_count, false, &t) && t.ctas_per_row <= 8) {
       // unaligned: the two-pass path's scalar form beats the two-phase pair
@@ -713,7 +711,7 @@ int plan_cols_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_count
   }
   if (forced == RRS_COLS_BAND) {
     if (cluster_fits && bands_fit_grid(N)) {
-      plan_cols_band(M, N, sm_count, p);
+      plan_cols_band(M, N, p);
       p->vector_io = 1;
       return RRS_OK;
     }

@@ -321,8 +321,8 @@ def test_cols_planner(lib, M, N):
     assert rows <= cap or cs == 8
     assert cs == 1 or -(-M // (cs // 2)) > cap                # no smaller cluster would do
     assert p["grid"] == bands * cs
-    # registers budgeted for 3 CTAs per SM only when the grid fills three such waves
-    assert p["vec"] == (3 if p["grid"] >= 9 * 152 else 4)
+    # registers budgeted for four CTAs per SM
+    assert p["vec"] == 4
 
 
 def test_cols_forced_paths(lib):

@@ -71,9 +71,9 @@ def steady(name: str) -> dict:
 # y partly stay dirty in the L2 between the bench's launches), the reads
 # allowed above the bytes of x (fraction: the column and row two-pass kernels
 # re-read x, the second time mostly from the L2), and the L2 write sectors allowed above the
-# bytes of y (fraction: the band kernel's 64-register build on cols_c2 spills
-# a few registers, and local-memory stores reach the L2 too; its
-# global-store sectors are then checked to be exactly y)
+# bytes of y (fraction: a kernel that spills registers sends its
+# local-memory stores to the L2 too; where a summary gives the global-store
+# sectors, those are checked to be exactly y)
 STEADY = [
     ("softmax_cluster_c3.md", 4 * 4096 * 32768, 4 * 4096 * 32768, 0.99, 0.01, 0.001),
     ("softmax_row_regs_c2.md", 4 * 8192 * 1024, 4 * 8192 * 1024, 0.9, 0.01, 0.001),
@@ -81,7 +81,7 @@ STEADY = [
     ("softmax_staged_grid_c5.md", 4 * 32 * 1048576, 4 * 32 * 1048576, 0.95, 0.01, 0.001),
     ("row_reduce_rows_c3.md", 4 * 4096 * 32768, 4 * 4096, 0.0, 0.01, 0.001),
     ("softmax_cols_two_pass_cols_c4.md", 4 * 4096 * 16384, 4 * 4096 * 16384, 0.97, 0.10, 0.01),
-    ("softmax_cols_band_cols_c2.md", 4 * 1024 * 8192, 4 * 1024 * 8192, 0.85, 0.10, 0.25),
+    ("softmax_cols_band_cols_c2.md", 4 * 1024 * 8192, 4 * 1024 * 8192, 0.85, 0.10, 0.001),
     ("softmax_rows_two_pass_c5.md", 4 * 32 * 1048576, 4 * 32 * 1048576, 0.97, 0.15, 0.001),
     ("gelu_kernel_gelu_16k.md", 4 * 16384 * 16384, 4 * 16384 * 16384, 0.99, 0.01, 0.001),
 ]
