@@ -226,6 +226,26 @@ def test_rejects_host_memory():
     assert e.value.status == 2
 
 
+# Rows of more than 128 chunks of 8192 floats: the two-pass kernel's merging
+# warp loads a row's (max, sum) pairs 128 at a time, so these rows take two
+# or three rounds of its loads (up to the planner's 256-chunk limit, and past
+# it when the path is forced).
+@pytest.mark.parametrize("M,N,ld,x_off,y_off,path", [
+    (2, 2_097_152, 2_097_153, 1, 2, "auto"),       # 256 chunks, unaligned: the planner's two-pass limit
+    (3, 1_500_001, 1_500_001, 0, 0, "two_pass"),   # 184 chunks, a ragged last chunk, scalar form
+    (2, 2_105_344, 2_105_344, 0, 0, "two_pass"),   # 257 chunks, float4 form: three rounds
+])
+def test_two_pass_rows_of_many_chunks(M, N, ld, x_off, y_off, path):
+    x = recipe("c5", M, N)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if path == "auto":
+        assert rrs.plan_softmax(M, N, ld, False, sms)["path_name"] == "two_pass"
+    y, guards = run(x, N, ld, path, x_off, y_off)
+    assert rrs.device_error() == 0
+    check_softmax(y, x, f"two_pass {M}x{N} ld={ld}")
+    assert guards
+
+
 @pytest.mark.parametrize("name", ["c2", "c4"])
 @pytest.mark.parametrize("path", ["auto", "cluster", "two_phase", "two_pass"])
 def test_input_written_just_before_reads_back_intact(name, path):
