@@ -674,9 +674,10 @@ int plan_cols_impl(int64_t M, int64_t N, int64_t ld, int vector_ok, int sm_count
     // its passes to interleave, at least twice its lag, and at most 8
     // slices per band, so its merge takes one round of loads (4096 x 16384:
     // 102.1-102.6 against 106.8-108.5 us; 2048 x 65536: 192.9-196.5 against
-    // 202.3-202.8; 4096 x 8192: 54.0 against 57.1); it loses where its
-    // passes run one after the other (1024 x 8192: 16.2-16.5 against 16.0)
-    // and ties or loses with 16-32 slices (8192 x 4096: 57.8 against 57.2,
+    // 202.3-202.8; 4096 x 8192: 54.0 against 57.1, 55.1 on the band path
+    // since its second pass stopped spilling); it loses where its passes
+    // run one after the other (1024 x 8192: 16.2-16.5 against 15.3) and
+    // ties or loses with 16-32 slices (8192 x 4096: 57.8 against 57.2,
     // 16384 x 2048: 63.3-65.8 against 63.0-63.7).
     rrs_plan t{};
     if (vector_ok && plan_cols_two_pass(M, N, sm_count, true, &t) && t.ctas_per_row <= 8 &&
